@@ -1,0 +1,358 @@
+"""Benchmark of the NVFP4 fused-MoE forward on GB300 (one JSON line on stdout).
+
+Workload (one step = one fused forward pass over one batch): the decode
+w4a16 case -- M=8 tokens, H=7168, I=2048, E=256, top_k=8, BF16 activations,
+NVFP4 weights, softmax top-8 routing, seed 0.  Weights are generated once and
+stay resident; each step re-runs routing, GEMM1+SwiGLU, GEMM2 and finalize.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload decode_w4a16|...]
+
+`--impl reference` times the CPU oracle (test infrastructure, never tuned)
+on the host cores over the same workload.  Under torchrun every rank runs its
+own replica (independent batches, no collective on the data path: weak
+scaling); times are the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused-MoE tokens/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_w4a16")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(cfg, T):
+    return {"workload": cfg.name, "M": cfg.M, "H": cfg.H, "I": cfg.I, "E": cfg.E,
+            "top_k": cfg.top_k, "mode": cfg.mode, "routing": cfg.routing, "route_tile": T,
+            "seed": cfg.seed}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def time_oracle(inp, T, steps, warmup, tokens=None):
+    import numpy as np
+    import oracle
+    oracle.build()
+    cfg = inp.cfg
+    orc = oracle.OracleMoE.from_inputs(inp, T=T)
+    toks = np.arange(cfg.M) if tokens is None else np.asarray(tokens)
+    cores = min(os.cpu_count() or 1, len(toks))
+    for _ in range(warmup):
+        orc.forward(toks, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        orc.forward(toks, nthreads=cores)
+    dt = (time.perf_counter() - t0) / max(steps, 1)
+    return len(toks) / dt, dt, cores, len(toks)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import block_scaled_fp4_sort_gb300 as fm
+    import synth
+    from block_scaled_fp4_sort_gb300 import build as fbuild
+    from block_scaled_fp4_sort_gb300.buffers import MoEBuffers, problem_for
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        fbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    fbuild.build()
+    cfg = synth.CONFIGS[args.workload]
+    T = synth.route_tile_for(cfg)
+    inp = synth.generate(cfg, device=dev)
+    p = problem_for(cfg, T)
+    B = MoEBuffers(p, dev).prepare(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+    ids = inp.token_selected_experts.to(dev)
+    wts = inp.token_final_scales.to(dev)
+    x = inp.x if inp.x is not None else inp.x_q
+    out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.forward(x, inp.x_sf, ids, wts, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale,
+                  stream=stream)
+
+    # ---------------- device-resident timed region
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    err = fm.read_error(B.fused_ws)
+    if err:
+        raise RuntimeError("device error word %d" % err)
+
+    # ---------------- per-kernel breakdown through the staged entry points
+    # (same kernels as the fused call, events around each launch)
+    kernels = {}
+    names = ["route_sort", "gemm1_swiglu", "gemm2", "finalize"]
+    ev = {n: [] for n in names}
+
+    if cfg.mode == "w4a16":
+        h = torch.zeros(B.S, cfg.I, dtype=torch.bfloat16, device=dev)
+        hsf = None
+    else:
+        h = torch.zeros(B.S, cfg.I // 2, dtype=torch.uint8, device=dev)
+        hsf = torch.zeros(B.S, cfg.I // 16, dtype=torch.uint8, device=dev)
+    y = torch.zeros(B.S, cfg.H, dtype=torch.float32, device=dev)
+
+    def launch(name):
+        if name == "route_sort":
+            fm.moe_route_sort(p, ids, B.e2p, B.p2e, B.tile_expert, B.tile_mn, B.num_tiles, None,
+                              B.route_ws, stream)
+        elif name == "gemm1_swiglu":
+            fm.moe_gemm1_swiglu(p, x, inp.x_sf, B.p2e, B.w1p, inp.w1_alpha, inp.fc2_input_scale,
+                                B.tile_expert, B.tile_mn, B.num_tiles, h, hsf, B.gemm1_ws, stream)
+        elif name == "gemm2":
+            fm.moe_gemm2(p, h, hsf, B.w2p, inp.w2_alpha, B.tile_expert, B.tile_mn, B.num_tiles, y,
+                         B.gemm2_ws, stream)
+        elif name == "finalize":
+            fm.moe_finalize(p, y, B.e2p, wts, 1.0, False, out, stream)
+
+    for it in range(max(args.warmup, 3) + args.steps):
+        for n in names:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch(n)
+            b.record(stream)
+            if it >= max(args.warmup, 3):
+                ev[n].append((a, b))
+    torch.cuda.synchronize()
+    for n in names:
+        kernels[n] = statistics.mean(a.elapsed_time(b) for a, b in ev[n])
+
+    # ---------------- end to end through host buffers
+    pin = lambda t: t.detach().cpu().pin_memory()
+    hx = pin(x)
+    hxsf = pin(inp.x_sf) if inp.x_sf is not None else None
+    hids = pin(inp.token_selected_experts)
+    hw = pin(inp.token_final_scales)
+    hout = torch.empty(cfg.M, cfg.H, dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty_like(x)
+    dxsf = torch.empty_like(inp.x_sf) if inp.x_sf is not None else None
+    dids = torch.empty_like(ids)
+    dw = torch.empty_like(wts)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        if dxsf is not None:
+            dxsf.copy_(hxsf, non_blocking=True)
+        dids.copy_(hids, non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        B.forward(dx, dxsf, dids, dw, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale,
+                  stream=stream)
+        hout.copy_(out, non_blocking=True)
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hw) + ((hxsf,) if hxsf is not None else ()))
+    d2h = hout.numel() * hout.element_size()
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---------------- roofline of the dominant kernel (GEMM1)
+    peaks, peak_src = load_peaks()
+    ids_np = inp.token_selected_experts.numpy()
+    touched = len(np.unique(ids_np))
+    H, I, M, R = cfg.H, cfg.I, cfg.M, cfg.routes
+    w1_bytes_per_expert = 2 * I * H // 2 + 2 * I * H // 16
+    w2_bytes_per_expert = H * I // 2 + H * I // 16
+    act1 = M * H * 2 if cfg.mode == "w4a16" else M * H // 2 + M * H // 16
+    g1_bytes = touched * w1_bytes_per_expert + act1 + R * I * 2
+    g1_ms = kernels["gemm1_swiglu"]
+    achieved = g1_bytes / (g1_ms * 1e-3) / 1e9
+    step_bytes = touched * (w1_bytes_per_expert + w2_bytes_per_expert) + act1 + M * H * 2
+    traffic_path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
+    traffic = None
+    if os.path.exists(traffic_path):
+        with open(traffic_path) as f:
+            tj = json.load(f)
+        if tj.get("workload") == cfg.name:
+            traffic = tj.get("dram_bytes_per_launch")
+    tokens_s = world * cfg.M / (ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": tokens_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.mode == "w4a16" else "nvfp4->bf16",
+        "data": "synthetic (seeded generator; random NVFP4 weights)",
+        "config": dict(workload_config(cfg, T), l2="inputs larger than L2: %.2f GB of weights "
+                       "per step vs 126 MB L2" % (step_bytes / 1e9), parallelism="replicas" if world > 1 else "1 GPU"),
+        "tflops": world * cfg.flops() / (ms * 1e-3) / 1e12,
+        "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
+        "roofline": {"kernel": "moe_gemm_kernel (GEMM1 + SwiGLU)", "bound": "hbm",
+                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes": g1_bytes, "peak_source": peak_src,
+                     "touched_experts": touched},
+        "kernels_ms": kernels,
+        "e2e": {"value": world * cfg.M / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clk.summary(),
+        "gpu_launches": args.steps * (4 if cfg.mode == "w4a16" else 6),
+    }
+    return line, inp, T
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        torch.distributed.init_process_group(backend)
+    import synth
+    cfg = synth.CONFIGS[args.workload]
+    T = synth.route_tile_for(cfg)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        inp = synth.generate(cfg, device="cpu")
+        v, dt, cores, n = time_oracle(inp, T, args.steps, args.warmup)
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload_config(cfg, T),
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                 "sample": "all %d tokens of one %s batch per step" % (n, cfg.name)},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    line, inp, T = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            inp_cpu = inp.to("cpu")
+            v, dt, cores, n = time_oracle(inp_cpu, T, 3, 1)
+            line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": "all %d tokens of one %s batch, 3 timed runs" % (n, cfg.name)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

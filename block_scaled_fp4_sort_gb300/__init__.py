@@ -1,0 +1,234 @@
+"""Python binding of libfp4moe (the GB300 NVFP4 fused-MoE forward).
+
+Argument marshalling only: every function here forwards torch tensors'
+device pointers and sizes to the C ABI of include/fp4moe.h and raises
+Fp4MoeError on a non-OK status.  There is no fallback: if the CUDA library is
+not built, importing the functions raises.  Build it with
+`python -m block_scaled_fp4_sort_gb300.build` (or __graft_entry__.build()).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp4moe.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_DEVICE, ERR_DEVICE_TIMEOUT = range(7)
+W4A16, W4A4 = 0, 1
+FINALIZE_DETERMINISTIC, FINALIZE_ATOMIC = 0, 1
+
+ABI_FUNCTIONS = (
+    "fp4moe_status_string", "fp4moe_route_tile", "fp4moe_max_permuted_slots",
+    "fp4moe_route_workspace_size", "fp4moe_gemm_workspace_size", "fp4moe_workspace_size",
+    "fp4moe_prepared_weight_size", "fp4moe_read_error", "fp4moe_clear_error",
+    "fp4moe_prepare_weights", "moe_route_sort", "moe_permute", "moe_gemm1_swiglu", "moe_gemm2",
+    "moe_finalize", "fused_moe_forward", "fp4moe_debug_quantize_nvfp4",
+    "fp4moe_debug_decode_prepared",
+)
+
+
+class Fp4MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, status_string(status), status))
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("inter", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("num_local_experts", ctypes.c_int32),
+                ("local_expert_offset", ctypes.c_int32), ("route_tile", ctypes.c_int32),
+                ("mode", ctypes.c_int32)]
+
+
+def problem(num_tokens, hidden, inter, num_experts, top_k, num_local_experts=0,
+            local_expert_offset=0, route_tile=0, mode=W4A16) -> Problem:
+    return Problem(num_tokens, hidden, inter, num_experts, top_k, num_local_experts,
+                   local_expert_offset, route_tile, mode)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfp4moe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libfp4moe.so is not built (%s); run "
+                               "`python -m block_scaled_fp4_sort_gb300.build`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+        P = ctypes.POINTER(Problem)
+        sig = {
+            "fp4moe_status_string": (ctypes.c_char_p, [i32]),
+            "fp4moe_route_tile": (i32, [P]),
+            "fp4moe_max_permuted_slots": (i64, [P]),
+            "fp4moe_route_workspace_size": (sz, [P]),
+            "fp4moe_gemm_workspace_size": (sz, [P, i32]),
+            "fp4moe_workspace_size": (sz, [P]),
+            "fp4moe_prepared_weight_size": (sz, [P, i32]),
+            "fp4moe_read_error": (i32, [vp, ctypes.POINTER(i32), vp]),
+            "fp4moe_clear_error": (i32, [vp, vp]),
+            "fp4moe_prepare_weights": (i32, [P, i32, vp, vp, vp, vp]),
+            "moe_route_sort": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "moe_permute": (i32, [P, vp, vp, vp, vp, vp, vp, vp]),
+            "moe_gemm1_swiglu": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "moe_gemm2": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "moe_finalize": (i32, [P, vp, vp, vp, f32, i32, vp, vp]),
+            "fused_moe_forward": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp, vp,
+                                        sz, vp]),
+            "fp4moe_debug_quantize_nvfp4": (i32, [vp, i64, vp, vp, vp, vp]),
+            "fp4moe_debug_decode_prepared": (i32, [P, i32, vp, vp, vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fp4moe_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise Fp4MoeError(status, where)
+
+
+def _p(t) -> Optional[int]:
+    """Device pointer of a tensor (None -> NULL)."""
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------- queries
+
+def route_tile(p: Problem) -> int:
+    v = lib().fp4moe_route_tile(ctypes.byref(p))
+    if v < 0:
+        raise Fp4MoeError(-v, "fp4moe_route_tile")
+    return v
+
+
+def max_permuted_slots(p: Problem) -> int:
+    v = lib().fp4moe_max_permuted_slots(ctypes.byref(p))
+    if v < 0:
+        raise Fp4MoeError(-v, "fp4moe_max_permuted_slots")
+    return v
+
+
+def route_workspace_size(p: Problem) -> int:
+    return lib().fp4moe_route_workspace_size(ctypes.byref(p))
+
+
+def gemm_workspace_size(p: Problem, which: int) -> int:
+    return lib().fp4moe_gemm_workspace_size(ctypes.byref(p), which)
+
+
+def workspace_size(p: Problem) -> int:
+    return lib().fp4moe_workspace_size(ctypes.byref(p))
+
+
+def prepared_weight_size(p: Problem, which: int) -> int:
+    return lib().fp4moe_prepared_weight_size(ctypes.byref(p), which)
+
+
+def read_error(workspace, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(lib().fp4moe_read_error(_p(workspace), ctypes.byref(code), _stream(stream)),
+           "fp4moe_read_error")
+    return code.value
+
+
+def clear_error(workspace, stream=None):
+    _check(lib().fp4moe_clear_error(_p(workspace), _stream(stream)), "fp4moe_clear_error")
+
+
+# ---------------------------------------------------------------- entry points
+
+def prepare_weights(p: Problem, which: int, w, w_sf, prepared, stream=None):
+    _check(lib().fp4moe_prepare_weights(ctypes.byref(p), which, _p(w), _p(w_sf), _p(prepared),
+                                        _stream(stream)), "fp4moe_prepare_weights")
+
+
+def moe_route_sort(p: Problem, token_selected_experts, expanded_idx_to_permuted_idx,
+                   permuted_idx_to_expanded_idx, tile_idx_to_expert, tile_idx_to_mn_limit,
+                   num_non_exiting_tiles, expert_counts, workspace, stream=None):
+    _check(lib().moe_route_sort(ctypes.byref(p), _p(token_selected_experts),
+                                _p(expanded_idx_to_permuted_idx), _p(permuted_idx_to_expanded_idx),
+                                _p(tile_idx_to_expert), _p(tile_idx_to_mn_limit),
+                                _p(num_non_exiting_tiles), _p(expert_counts), _p(workspace),
+                                _nbytes(workspace), _stream(stream)), "moe_route_sort")
+
+
+def moe_permute(p: Problem, x, x_sf, permuted_idx_to_expanded_idx, num_non_exiting_tiles,
+                permuted_x, permuted_x_sf=None, stream=None):
+    _check(lib().moe_permute(ctypes.byref(p), _p(x), _p(x_sf), _p(permuted_idx_to_expanded_idx),
+                             _p(num_non_exiting_tiles), _p(permuted_x), _p(permuted_x_sf),
+                             _stream(stream)), "moe_permute")
+
+
+def moe_gemm1_swiglu(p: Problem, a, a_sf, gather_rows, w1_prepared, w1_alpha, fc2_input_scale,
+                     tile_idx_to_expert, tile_idx_to_mn_limit, num_non_exiting_tiles, h, h_sf,
+                     workspace, stream=None):
+    _check(lib().moe_gemm1_swiglu(ctypes.byref(p), _p(a), _p(a_sf), _p(gather_rows),
+                                  _p(w1_prepared), _p(w1_alpha), _p(fc2_input_scale),
+                                  _p(tile_idx_to_expert), _p(tile_idx_to_mn_limit),
+                                  _p(num_non_exiting_tiles), _p(h), _p(h_sf), _p(workspace),
+                                  _nbytes(workspace), _stream(stream)), "moe_gemm1_swiglu")
+
+
+def moe_gemm2(p: Problem, h, h_sf, w2_prepared, w2_alpha, tile_idx_to_expert,
+              tile_idx_to_mn_limit, num_non_exiting_tiles, y, workspace, stream=None):
+    _check(lib().moe_gemm2(ctypes.byref(p), _p(h), _p(h_sf), _p(w2_prepared), _p(w2_alpha),
+                           _p(tile_idx_to_expert), _p(tile_idx_to_mn_limit),
+                           _p(num_non_exiting_tiles), _p(y), _p(workspace), _nbytes(workspace),
+                           _stream(stream)), "moe_gemm2")
+
+
+def moe_finalize(p: Problem, y, expanded_idx_to_permuted_idx, token_final_scales,
+                 routed_scaling_factor, accumulate, out, stream=None):
+    _check(lib().moe_finalize(ctypes.byref(p), _p(y), _p(expanded_idx_to_permuted_idx),
+                              _p(token_final_scales), float(routed_scaling_factor),
+                              int(bool(accumulate)), _p(out), _stream(stream)), "moe_finalize")
+
+
+def fused_moe_forward(p: Problem, x, x_sf, token_selected_experts, token_final_scales,
+                      w1_prepared, w1_alpha, fc2_input_scale, w2_prepared, w2_alpha,
+                      routed_scaling_factor, accumulate, finalize_mode, out, workspace,
+                      stream=None):
+    _check(lib().fused_moe_forward(ctypes.byref(p), _p(x), _p(x_sf), _p(token_selected_experts),
+                                   _p(token_final_scales), _p(w1_prepared), _p(w1_alpha),
+                                   _p(fc2_input_scale), _p(w2_prepared), _p(w2_alpha),
+                                   float(routed_scaling_factor), int(bool(accumulate)),
+                                   int(finalize_mode), _p(out), _p(workspace), _nbytes(workspace),
+                                   _stream(stream)), "fused_moe_forward")
+
+
+def debug_quantize_nvfp4(x, scale, q, sf, stream=None):
+    _check(lib().fp4moe_debug_quantize_nvfp4(_p(x), x.numel(), _p(scale), _p(q), _p(sf),
+                                             _stream(stream)), "fp4moe_debug_quantize_nvfp4")
+
+
+def debug_decode_prepared(p: Problem, which: int, prepared, out, stream=None):
+    _check(lib().fp4moe_debug_decode_prepared(ctypes.byref(p), which, _p(prepared), _p(out),
+                                              _stream(stream)), "fp4moe_debug_decode_prepared")

@@ -1,0 +1,120 @@
+"""Device buffers for one fused-MoE problem (torch is used for memory only).
+
+`MoEBuffers` owns the routing-plan arrays, the prepared weights and the
+workspaces, sized by the library's own size queries, and calls the C ABI
+through the binding.  No arithmetic of the forward pass happens here.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (W4A4, W4A16, FINALIZE_DETERMINISTIC, fused_moe_forward, gemm_workspace_size,
+               max_permuted_slots, moe_finalize, moe_gemm1_swiglu, moe_gemm2, moe_permute,
+               moe_route_sort, prepare_weights, prepared_weight_size, problem, route_tile,
+               route_workspace_size, workspace_size)
+
+
+def _empty(n, dtype, device):
+    return torch.empty(max(int(n), 1), dtype=dtype, device=device)
+
+
+def _zeros(n, dtype, device):
+    # workspaces start zeroed: their first word is the sticky device error word
+    return torch.zeros(max(int(n), 1), dtype=dtype, device=device)
+
+
+class MoEBuffers:
+    """Plan, prepared weights and workspaces for `p` on `device`."""
+
+    def __init__(self, p, device="cuda"):
+        self.p = p
+        self.device = torch.device(device)
+        self.T = route_tile(p)
+        self.S = max_permuted_slots(p)
+        self.tiles = self.S // self.T
+        M, k = p.num_tokens, p.top_k
+        E_local = p.num_local_experts or p.num_experts
+        d = self.device
+        i32 = torch.int32
+        self.e2p = _empty(M * k, i32, d)
+        self.p2e = _empty(self.S, i32, d)
+        self.tile_expert = _empty(self.tiles, i32, d)
+        self.tile_mn = _empty(self.tiles, i32, d)
+        self.num_tiles = _empty(4, i32, d)
+        self.counts = _empty(E_local, i32, d)
+        self.route_ws = _zeros(route_workspace_size(p), torch.uint8, d)
+        self.gemm1_ws = _zeros(gemm_workspace_size(p, 1), torch.uint8, d)
+        self.gemm2_ws = _zeros(gemm_workspace_size(p, 2), torch.uint8, d)
+        self.fused_ws = None
+        self.w1p = None
+        self.w2p = None
+
+    # -- weights
+    def prepare(self, w1, w1_sf, w2, w2_sf, stream=None):
+        p, d = self.p, self.device
+        self.w1p = _empty(prepared_weight_size(p, 1), torch.uint8, d)
+        self.w2p = _empty(prepared_weight_size(p, 2), torch.uint8, d)
+        prepare_weights(p, 1, w1, w1_sf, self.w1p, stream)
+        prepare_weights(p, 2, w2, w2_sf, self.w2p, stream)
+        return self
+
+    def ensure_fused_ws(self):
+        if self.fused_ws is None:
+            self.fused_ws = _zeros(workspace_size(self.p), torch.uint8, self.device)
+        return self.fused_ws
+
+    # -- staged path
+    def route(self, ids, stream=None):
+        moe_route_sort(self.p, ids, self.e2p, self.p2e, self.tile_expert, self.tile_mn,
+                       self.num_tiles, self.counts, self.route_ws, stream)
+
+    def permute(self, x, x_sf=None, stream=None):
+        p = self.p
+        if p.mode == W4A16:
+            px = torch.zeros(self.S, p.hidden, dtype=torch.bfloat16, device=self.device)
+            psf = None
+        else:
+            px = torch.zeros(self.S, p.hidden // 2, dtype=torch.uint8, device=self.device)
+            psf = torch.zeros(self.S, p.hidden // 16, dtype=torch.uint8, device=self.device)
+        moe_permute(p, x, x_sf, self.p2e, self.num_tiles, px, psf, stream)
+        return px, psf
+
+    def gemm1(self, a, a_sf, w1_alpha, fc2_input_scale=None, gather=True, stream=None):
+        p = self.p
+        if p.mode == W4A16:
+            h = torch.zeros(self.S, p.inter, dtype=torch.bfloat16, device=self.device)
+            hsf = None
+        else:
+            h = torch.zeros(self.S, p.inter // 2, dtype=torch.uint8, device=self.device)
+            hsf = torch.zeros(self.S, p.inter // 16, dtype=torch.uint8, device=self.device)
+        moe_gemm1_swiglu(p, a, a_sf, self.p2e if gather else None, self.w1p, w1_alpha,
+                         fc2_input_scale, self.tile_expert, self.tile_mn, self.num_tiles, h, hsf,
+                         self.gemm1_ws, stream)
+        return h, hsf
+
+    def gemm2(self, h, hsf, w2_alpha, stream=None):
+        p = self.p
+        y = torch.zeros(self.S, p.hidden, dtype=torch.float32, device=self.device)
+        moe_gemm2(p, h, hsf, self.w2p, w2_alpha, self.tile_expert, self.tile_mn, self.num_tiles, y,
+                  self.gemm2_ws, stream)
+        return y
+
+    def finalize(self, y, token_final_scales, out, rsf=1.0, accumulate=False, stream=None):
+        moe_finalize(self.p, y, self.e2p, token_final_scales, rsf, accumulate, out, stream)
+        return out
+
+    # -- fused path
+    def forward(self, x, x_sf, ids, token_final_scales, w1_alpha, w2_alpha, out,
+                fc2_input_scale=None, rsf=1.0, accumulate=False,
+                finalize_mode=FINALIZE_DETERMINISTIC, stream=None):
+        ws = self.ensure_fused_ws()
+        fused_moe_forward(self.p, x, x_sf, ids, token_final_scales, self.w1p, w1_alpha,
+                          fc2_input_scale, self.w2p, w2_alpha, rsf, accumulate, finalize_mode, out,
+                          ws, stream)
+        return out
+
+
+def problem_for(cfg, route_tile_=0, num_local_experts=0, local_expert_offset=0):
+    """fp4moe_problem for a synth.MoEConfig."""
+    return problem(cfg.M, cfg.H, cfg.I, cfg.E, cfg.top_k, num_local_experts, local_expert_offset,
+                   route_tile_, W4A4 if cfg.mode == "w4a4" else W4A16)

@@ -1,0 +1,422 @@
+// fp4moe_api.cu -- the extern "C" boundary declared in include/fp4moe.h:
+// host-side validation (modelled on the pages' can_implement checks and
+// ValueError rejections), workspace carving, and the launch sequence of the
+// fused forward (vllm.models.flint.ops.moe_cute, grouped_moe: moe_sort ->
+// moe_permute -> GEMM1 + SwiGLU -> GEMM2, then the weighted top-k reduction;
+// here GEMM1 gathers its activation rows by TMA, so no permuted copy exists).
+// Nothing here allocates, synchronises or reads device memory, except
+// fp4moe_read_error, which is documented as a synchronising diagnostic.
+#include <algorithm>
+#include <cstring>
+
+#include "../../include/fp4moe.h"
+#include "internal.h"
+
+using namespace fp4moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+int32_t auto_tile(int64_t R, int64_t EL) {
+  const int64_t avg = std::max<int64_t>(1, (R + EL - 1) / EL);
+  int32_t t = 16;
+  while (t < avg && t < 128) t *= 2;
+  return t;
+}
+
+fp4moe_status validate(const fp4moe_problem* p, Shape* s) {
+  if (!p) return FP4MOE_ERR_INVALID_ARG;
+  if (p->num_tokens < 0 || p->hidden <= 0 || p->inter <= 0 || p->num_experts < 1 || p->top_k < 1)
+    return FP4MOE_ERR_INVALID_ARG;
+  if (p->hidden % 128 != 0 || p->inter % 128 != 0) return FP4MOE_ERR_INVALID_ARG;
+  const int64_t EL = p->num_local_experts == 0 ? p->num_experts : p->num_local_experts;
+  if (EL < 1 || EL > p->num_experts || p->local_expert_offset < 0 ||
+      p->local_expert_offset + EL > p->num_experts)
+    return FP4MOE_ERR_INVALID_ARG;
+  if (p->top_k > p->num_experts) return FP4MOE_ERR_INVALID_ARG;
+  if (p->mode != FP4MOE_W4A16 && p->mode != FP4MOE_W4A4) return FP4MOE_ERR_INVALID_ARG;
+  if (EL > kMaxLocalExperts) return FP4MOE_ERR_UNSUPPORTED;
+  const int64_t R = (int64_t)p->num_tokens * p->top_k;
+  int32_t T = p->route_tile;
+  if (T == 0) {
+    T = auto_tile(R, EL);
+  } else if (T < 8 || T % 8 != 0) {
+    return FP4MOE_ERR_INVALID_ARG;
+  } else if (T != 16 && T != 32 && T != 64 && T != 128) {
+    return FP4MOE_ERR_UNSUPPORTED;
+  }
+  const int64_t ne = std::min<int64_t>(R, EL);
+  int64_t S = (R + ne * (T - 1) + T - 1) / T * T;
+  if (S < T) S = T;
+  if (R > INT32_MAX || S > INT32_MAX) return FP4MOE_ERR_UNSUPPORTED;
+  s->M = p->num_tokens;
+  s->H = p->hidden;
+  s->I = p->inter;
+  s->E = p->num_experts;
+  s->K = p->top_k;
+  s->EL = EL;
+  s->off = p->local_expert_offset;
+  s->T = T;
+  s->mode = p->mode;
+  s->R = R;
+  s->S = S;
+  s->tiles = S / T;
+  return FP4MOE_OK;
+}
+
+inline fp4moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? FP4MOE_OK : FP4MOE_ERR_CUDA; }
+
+// ---- workspace layouts ----
+struct RouteWs {
+  size_t scratch, total;
+};
+RouteWs route_ws(const Shape& s) {
+  RouteWs w;
+  w.scratch = kWsHeader;
+  w.total = up(w.scratch + route_scratch_bytes(s));
+  return w;
+}
+
+size_t gemm_ws_bytes(const Shape& s, int which) {
+  size_t b = kWsHeader;
+  if (s.mode == FP4MOE_W4A4) {
+    const int64_t rows = which == 1 ? std::max(s.M, s.S) : s.S;
+    const int64_t K = which == 1 ? s.H : s.I;
+    b += up((size_t)rows * K * 2);
+  }
+  return up(b);
+}
+
+struct FusedWs {
+  size_t e2p, p2e, tile_expert, tile_mn, num_tiles, route_scratch, h, h_sf, y, deq1, deq2, total;
+};
+FusedWs fused_ws(const Shape& s) {
+  FusedWs w = {};
+  size_t o = kWsHeader;
+  w.e2p = o; o = up(o + (size_t)s.R * 4);
+  w.p2e = o; o = up(o + (size_t)s.S * 4);
+  w.tile_expert = o; o = up(o + (size_t)s.tiles * 4);
+  w.tile_mn = o; o = up(o + (size_t)s.tiles * 4);
+  w.num_tiles = o; o = up(o + 16);
+  w.route_scratch = o; o = up(o + route_scratch_bytes(s));
+  if (s.mode == FP4MOE_W4A16) {
+    w.h = o; o = up(o + (size_t)s.S * s.I * 2);
+  } else {
+    w.h = o; o = up(o + (size_t)s.S * s.I / 2);
+    w.h_sf = o; o = up(o + (size_t)s.S * s.I / 16);
+    w.deq1 = o; o = up(o + (size_t)s.M * s.H * 2);     // x in BF16 (exact)
+    w.deq2 = o; o = up(o + (size_t)s.S * s.I * 2);     // h in BF16 (exact)
+  }
+  w.y = o; o = up(o + (size_t)s.S * s.H * 4);  // fp32 route storage
+  w.total = o;
+  return w;
+}
+
+inline int* err_word(void* ws) { return static_cast<int*>(ws); }
+
+}  // namespace
+
+extern "C" {
+
+const char* fp4moe_status_string(int32_t st) {
+  switch (st) {
+    case FP4MOE_OK: return "ok";
+    case FP4MOE_ERR_INVALID_ARG: return "invalid argument";
+    case FP4MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FP4MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FP4MOE_ERR_CUDA: return "CUDA runtime error";
+    case FP4MOE_ERR_DEVICE: return "device error: invalid expert id";
+    case FP4MOE_ERR_DEVICE_TIMEOUT: return "device error: bounded wait expired";
+    default: return "unknown status";
+  }
+}
+
+int32_t fp4moe_route_tile(const fp4moe_problem* p) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  return st == FP4MOE_OK ? (int32_t)s.T : -(int32_t)st;
+}
+
+int64_t fp4moe_max_permuted_slots(const fp4moe_problem* p) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  return st == FP4MOE_OK ? s.S : -(int64_t)st;
+}
+
+size_t fp4moe_route_workspace_size(const fp4moe_problem* p) {
+  Shape s;
+  if (validate(p, &s) != FP4MOE_OK) return 0;
+  return route_ws(s).total;
+}
+
+size_t fp4moe_gemm_workspace_size(const fp4moe_problem* p, int32_t which) {
+  Shape s;
+  if (validate(p, &s) != FP4MOE_OK || (which != 1 && which != 2)) return 0;
+  return gemm_ws_bytes(s, which);
+}
+
+size_t fp4moe_workspace_size(const fp4moe_problem* p) {
+  Shape s;
+  if (validate(p, &s) != FP4MOE_OK) return 0;
+  return fused_ws(s).total;
+}
+
+size_t fp4moe_prepared_weight_size(const fp4moe_problem* p, int32_t which) {
+  Shape s;
+  if (validate(p, &s) != FP4MOE_OK || (which != 1 && which != 2)) return 0;
+  return prepared_bytes(s, which);
+}
+
+fp4moe_status fp4moe_read_error(const void* workspace, int32_t* code, void* stream) {
+  if (!workspace || !code) return FP4MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
+  *code = v;
+  return FP4MOE_OK;
+}
+
+fp4moe_status fp4moe_clear_error(void* workspace, void* stream) {
+  if (!ok_ptr(workspace)) return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(workspace, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status fp4moe_prepare_weights(const fp4moe_problem* p, int32_t which, const uint8_t* w,
+                                     const uint8_t* w_sf, void* prepared, void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  if ((which != 1 && which != 2) || !ok_ptr(w) || !ok_ptr(w_sf) || !ok_ptr(prepared))
+    return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_prepare(s, which, w, w_sf, static_cast<uint8_t*>(prepared),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status moe_route_sort(const fp4moe_problem* p, const int32_t* ids, int32_t* e2p,
+                             int32_t* p2e, int32_t* tile_expert, int32_t* tile_mn,
+                             int32_t* num_tiles, int32_t* counts, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  if ((s.R > 0 && (!ok_ptr(ids) || !ok_ptr(e2p))) || !ok_ptr(p2e) || !ok_ptr(tile_expert) ||
+      !ok_ptr(tile_mn) || !ok_ptr(num_tiles) || (counts && !aligned16(counts)) || !ok_ptr(workspace))
+    return FP4MOE_ERR_INVALID_ARG;
+  RouteWs w = route_ws(s);
+  if (workspace_bytes < w.total) return FP4MOE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return cuda_status(launch_route_sort(s, ids, e2p, p2e, tile_expert, tile_mn, num_tiles, counts,
+                                       err_word(ws), ws + w.scratch,
+                                       static_cast<cudaStream_t>(stream), false));
+}
+
+fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
+                          const int32_t* p2e, const int32_t* num_tiles, void* px, uint8_t* px_sf,
+                          void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  if ((s.M > 0 && !ok_ptr(x)) || !ok_ptr(p2e) || !ok_ptr(num_tiles) || !ok_ptr(px))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (s.mode == FP4MOE_W4A4 && ((s.M > 0 && !ok_ptr(x_sf)) || !ok_ptr(px_sf)))
+    return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_permute(s, x, x_sf, p2e, num_tiles, px, px_sf,
+                                    static_cast<cudaStream_t>(stream), false));
+}
+
+fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uint8_t* a_sf,
+                               const int32_t* gather_rows, const void* w1_prepared,
+                               const float* w1_alpha, const float* fc2_input_scale,
+                               const int32_t* tile_expert, const int32_t* tile_mn,
+                               const int32_t* num_tiles, void* h, uint8_t* h_sf, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  const bool w4 = s.mode == FP4MOE_W4A4;
+  if (!ok_ptr(w1_prepared) || !ok_ptr(w1_alpha) || !ok_ptr(tile_expert) || !ok_ptr(tile_mn) ||
+      !ok_ptr(num_tiles) || !ok_ptr(h) || !ok_ptr(workspace) || (gather_rows && !ok_ptr(gather_rows)))
+    return FP4MOE_ERR_INVALID_ARG;
+  const int64_t act_rows = gather_rows ? s.M : s.S;
+  if (act_rows > 0 && !ok_ptr(a)) return FP4MOE_ERR_INVALID_ARG;
+  if (w4 && ((act_rows > 0 && !ok_ptr(a_sf)) || !ok_ptr(h_sf) || !ok_ptr(fc2_input_scale)))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < gemm_ws_bytes(s, 1)) return FP4MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const void* act = a;
+  if (w4) {
+    act = ws + kWsHeader;
+    cudaError_t e = launch_dequant_rows(static_cast<const uint8_t*>(a), a_sf, act_rows, s.H,
+                                        gather_rows ? nullptr : num_tiles, s.T, ws + kWsHeader, cs,
+                                        false);
+    if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
+  }
+  GemmLaunch g = {};
+  g.which = 1;
+  g.epi = w4 ? kEpiSwigluNvfp4 : kEpiSwigluBf16;
+  g.wprep = static_cast<const uint8_t*>(w1_prepared);
+  g.alpha = w1_alpha;
+  g.tile_expert = tile_expert;
+  g.tile_mn = tile_mn;
+  g.num_tiles = num_tiles;
+  g.gather_rows = gather_rows;
+  g.act = act;
+  g.act_rows = act_rows;
+  g.out = h;
+  g.out_sf = h_sf;
+  g.fc2_scale = fc2_input_scale;
+  g.err = err_word(ws);
+  return cuda_status(launch_gemm(s, g, cs, w4));
+}
+
+fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h_sf,
+                        const void* w2_prepared, const float* w2_alpha, const int32_t* tile_expert,
+                        const int32_t* tile_mn, const int32_t* num_tiles, void* y, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  const bool w4 = s.mode == FP4MOE_W4A4;
+  if (!ok_ptr(h) || !ok_ptr(w2_prepared) || !ok_ptr(w2_alpha) || !ok_ptr(tile_expert) ||
+      !ok_ptr(tile_mn) || !ok_ptr(num_tiles) || !ok_ptr(y) || !ok_ptr(workspace) ||
+      (w4 && !ok_ptr(h_sf)))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < gemm_ws_bytes(s, 2)) return FP4MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const void* act = h;
+  if (w4) {
+    act = ws + kWsHeader;
+    cudaError_t e = launch_dequant_rows(static_cast<const uint8_t*>(h), h_sf, s.S, s.I, num_tiles,
+                                        s.T, ws + kWsHeader, cs, false);
+    if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
+  }
+  GemmLaunch g = {};
+  g.which = 2;
+  g.epi = kEpiPlainBf16;
+  g.wprep = static_cast<const uint8_t*>(w2_prepared);
+  g.alpha = w2_alpha;
+  g.tile_expert = tile_expert;
+  g.tile_mn = tile_mn;
+  g.num_tiles = num_tiles;
+  g.act = act;
+  g.act_rows = s.S;
+  g.out = y;
+  g.err = err_word(ws);
+  return cuda_status(launch_gemm(s, g, cs, w4));
+}
+
+fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y, const int32_t* e2p,
+                           const float* w, float rsf, int32_t accumulate, void* out, void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  if (s.M > 0 && (!ok_ptr(y) || !ok_ptr(e2p) || !ok_ptr(w) || !ok_ptr(out)))
+    return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_finalize(s, y, e2p, w, rsf, accumulate ? 1 : 0, out,
+                                     static_cast<cudaStream_t>(stream), false));
+}
+
+fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
+                                const int32_t* ids, const float* wts, const void* w1_prepared,
+                                const float* w1_alpha, const float* fc2_input_scale,
+                                const void* w2_prepared, const float* w2_alpha, float rsf,
+                                int32_t accumulate, int32_t finalize_mode, void* out,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  const bool w4 = s.mode == FP4MOE_W4A4;
+  if (finalize_mode != FP4MOE_FINALIZE_DETERMINISTIC && finalize_mode != FP4MOE_FINALIZE_ATOMIC)
+    return FP4MOE_ERR_INVALID_ARG;
+  if (finalize_mode == FP4MOE_FINALIZE_ATOMIC) return FP4MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(w1_prepared) || !ok_ptr(w1_alpha) || !ok_ptr(w2_prepared) || !ok_ptr(w2_alpha) ||
+      !ok_ptr(workspace))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (s.M > 0 && (!ok_ptr(x) || !ok_ptr(ids) || !ok_ptr(wts) || !ok_ptr(out)))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (w4 && ((s.M > 0 && !ok_ptr(x_sf)) || !ok_ptr(fc2_input_scale))) return FP4MOE_ERR_INVALID_ARG;
+  const FusedWs L = fused_ws(s);
+  if (workspace_bytes < L.total) return FP4MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (s.M == 0) return FP4MOE_OK;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* err = err_word(ws);
+  int32_t* e2p = reinterpret_cast<int32_t*>(ws + L.e2p);
+  int32_t* p2e = reinterpret_cast<int32_t*>(ws + L.p2e);
+  int32_t* te = reinterpret_cast<int32_t*>(ws + L.tile_expert);
+  int32_t* tm = reinterpret_cast<int32_t*>(ws + L.tile_mn);
+  int32_t* nt = reinterpret_cast<int32_t*>(ws + L.num_tiles);
+  cudaError_t e = launch_route_sort(s, ids, e2p, p2e, te, tm, nt, nullptr, err, ws + L.route_scratch,
+                                    cs, true);
+  const void* xb = x;
+  if (e == cudaSuccess && w4) {
+    e = launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.M, s.H, nullptr, s.T,
+                            ws + L.deq1, cs, true);
+    xb = ws + L.deq1;
+  }
+  GemmLaunch g1 = {};
+  g1.which = 1;
+  g1.epi = w4 ? kEpiSwigluNvfp4 : kEpiSwigluBf16;
+  g1.wprep = static_cast<const uint8_t*>(w1_prepared);
+  g1.alpha = w1_alpha;
+  g1.tile_expert = te;
+  g1.tile_mn = tm;
+  g1.num_tiles = nt;
+  g1.gather_rows = p2e;      // rows gathered by TMA straight from x
+  g1.act = xb;
+  g1.act_rows = s.M;
+  g1.out = ws + L.h;
+  g1.out_sf = w4 ? ws + L.h_sf : nullptr;
+  g1.fc2_scale = fc2_input_scale;
+  g1.err = err;
+  if (e == cudaSuccess) e = launch_gemm(s, g1, cs, true);
+  const void* hin = ws + L.h;
+  if (e == cudaSuccess && w4) {
+    e = launch_dequant_rows(ws + L.h, ws + L.h_sf, s.S, s.I, nt, s.T, ws + L.deq2, cs, true);
+    hin = ws + L.deq2;
+  }
+  GemmLaunch g2 = {};
+  g2.which = 2;
+  g2.epi = kEpiPlainBf16;
+  g2.wprep = static_cast<const uint8_t*>(w2_prepared);
+  g2.alpha = w2_alpha;
+  g2.tile_expert = te;
+  g2.tile_mn = tm;
+  g2.num_tiles = nt;
+  g2.act = hin;
+  g2.act_rows = s.S;
+  g2.out = ws + L.y;
+  g2.err = err;
+  if (e == cudaSuccess) e = launch_gemm(s, g2, cs, true);
+  if (e == cudaSuccess)
+    e = launch_finalize(s, ws + L.y, e2p, wts, rsf, accumulate ? 1 : 0, out, cs, true);
+  return cuda_status(e);
+}
+
+fp4moe_status fp4moe_debug_quantize_nvfp4(const float* in, int64_t n, const float* scale,
+                                          uint8_t* q, uint8_t* sf, void* stream) {
+  if (n < 0 || n % 16 != 0 || (n > 0 && (!ok_ptr(in) || !ok_ptr(q) || !ok_ptr(sf))) || !scale)
+    return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_debug_quantize(in, n, scale, q, sf, static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status fp4moe_debug_decode_prepared(const fp4moe_problem* p, int32_t which,
+                                           const void* prepared, void* out, void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  if ((which != 1 && which != 2) || !ok_ptr(prepared) || !ok_ptr(out)) return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_debug_decode(s, which, static_cast<const uint8_t*>(prepared), out,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// internal.h -- host-side launchers shared between the C ABI and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fp4moe {
+
+// ---- prepared weight layout (see prepare.cu) ----
+// A work item covers 256 weight rows (two 128-row MMA tiles) and the whole K
+// range in chunks of kBK elements.  One (expert, row block, K chunk) block is
+// kWBlockBytes contiguous bytes: 256 rows x 64 bytes of bit-permuted E2M1
+// codes, then 256 rows x 8 E4M3 scale bytes.
+constexpr int kBK = 128;
+constexpr int kRowsPerItem = 256;
+constexpr int kWDataBytes = kRowsPerItem * kBK / 2;     // 16384
+constexpr int kWScaleBytes = kRowsPerItem * kBK / 16;   // 2048
+constexpr int kWBlockBytes = kWDataBytes + kWScaleBytes;
+
+// error word lives at offset 0 of every workspace; the header is 256 bytes
+constexpr size_t kWsHeader = 256;
+
+struct Shape {
+  int64_t M, H, I, E, K, EL, off, T, mode;
+  int64_t R, S, tiles;  // routes, permuted slots, S / T
+};
+
+inline int64_t row_blocks(const Shape& s, int which) {
+  return which == 1 ? s.I / 128 : (s.H + 255) / 256;
+}
+inline int64_t k_chunks(const Shape& s, int which) { return which == 1 ? s.H / kBK : s.I / kBK; }
+inline size_t prepared_bytes(const Shape& s, int which) {
+  return (size_t)s.EL * row_blocks(s, which) * k_chunks(s, which) * kWBlockBytes;
+}
+
+// ---- routing (route_sort.cu) ----
+constexpr int kRouteChunk = 4096;  // routes per CTA in the multi-CTA path
+constexpr int kMaxLocalExperts = 2048;
+size_t route_scratch_bytes(const Shape& s);
+cudaError_t launch_route_sort(const Shape& s, const int32_t* ids, int32_t* e2p, int32_t* p2e,
+                              int32_t* tile_expert, int32_t* tile_mn, int32_t* num_tiles,
+                              int32_t* counts, int* err, void* scratch, cudaStream_t st, bool pdl);
+
+// ---- elementwise steps (permute.cu) ----
+cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, const int32_t* p2e,
+                           const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
+                           bool pdl);
+cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, const float* w,
+                            float rsf, int accumulate, void* out, cudaStream_t st, bool pdl);
+cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
+                                const int32_t* row_limit_tiles, int64_t T, void* out,
+                                cudaStream_t st, bool pdl);
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl);
+cudaError_t launch_debug_quantize(const float* in, int64_t n, const float* scale, uint8_t* q,
+                                  uint8_t* sf, cudaStream_t st);
+
+// ---- weight preparation (prepare.cu) ----
+cudaError_t launch_prepare(const Shape& s, int which, const uint8_t* w, const uint8_t* w_sf,
+                           uint8_t* prepared, cudaStream_t st);
+cudaError_t launch_debug_decode(const Shape& s, int which, const uint8_t* prepared, void* out,
+                                cudaStream_t st);
+
+// ---- grouped GEMM (moe_gemm.cu) ----
+enum Epilogue { kEpiSwigluBf16 = 0, kEpiSwigluNvfp4 = 1, kEpiPlainBf16 = 2, kEpiAtomicFinal = 3 };
+
+struct GemmLaunch {
+  int which;                   // 1 = GEMM1 (+SwiGLU), 2 = GEMM2
+  Epilogue epi;
+  const uint8_t* wprep;
+  const float* alpha;
+  const int32_t* tile_expert;
+  const int32_t* tile_mn;
+  const int32_t* num_tiles;
+  const int32_t* gather_rows;  // GEMM1 row gather (permuted_idx_to_expanded_idx) or null
+  const void* act;             // bf16 activations: x [M, K] (gather) or permuted [S, K]
+  int64_t act_rows;            // rows of `act`
+  void* out;                   // h bf16 [S, I] | hq [S, I/2] | y bf16 [S, H] | out bf16 [M, H]
+  uint8_t* out_sf;             // hsf [S, I/16]
+  const float* fc2_scale;      // [1]
+  // atomic finalize epilogue
+  const int32_t* p2e;
+  const float* route_w;
+  float rsf;
+  int* err;
+};
+cudaError_t launch_gemm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl);
+
+}  // namespace fp4moe

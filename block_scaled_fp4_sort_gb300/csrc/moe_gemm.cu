@@ -1,0 +1,450 @@
+// moe_gemm.cu -- grouped NVFP4-weight GEMMs on tcgen05 (sm_103a).
+//
+// What is computed (vllm.models.flint.ops.moe_cute, module docstring; the
+// grouped GEMM calls of grouped_moe): E2M1*E4M3 weight tiles decoded to
+// BF16, BF16 MMAs with fp32 accumulation, the per-expert fp32 alpha applied
+// to the accumulator, and for GEMM1 a SwiGLU epilogue that keeps gate and up
+// in fp32 and rounds silu(g)*u once.
+//
+// Orientation ("weights on M"): MMA M = 128 weight rows, N = the route tile
+// (BN route slots), K = the reduction.  One work item = (route tile tau,
+// 256-row weight block f): GEMM1 blocks are 128 gate rows + the matching 128
+// up rows, so SwiGLU pairs meet in one CTA; GEMM2 blocks are 256 rows of w2.
+//
+// Per CTA (persistent, one per SM, 320 threads):
+//   warp 8     TMA producer: 1D bulk copy of the prepared weight block
+//              (codes + scales, 18 KB per 128-K chunk) and a 2D tiled (or
+//              four-row gather) tensor copy of the BF16 activation tile into
+//              a 128-byte-swizzled K-major shared-memory ring.
+//   warps 0-7  decode: thread r reads weight row r's 64 code bytes and 8
+//              scales, turns them into 64 BF16x2 words and stores them with
+//              tcgen05.st straight into tensor memory -- the A operand of the
+//              MMA lives in TMEM, so the decoded weights never touch shared
+//              memory.  After the last chunk the same warps run the epilogue
+//              (tcgen05.ld of the fp32 accumulators).
+//   warp 9     MMA issuer: tcgen05.mma.cta_group::1.kind::f16, A from TMEM,
+//              B from shared memory, D in TMEM; tcgen05.commit releases the
+//              shared-memory stage and the TMEM A stage.
+// Every wait is bounded (common.cuh); on timeout the error word is set, the
+// producer waits for its copies in flight, the MMA warp drains, TMEM is freed.
+#include <algorithm>
+
+#include "common.cuh"
+#include "decode.cuh"
+#include "internal.h"
+#include "nvfp4.cuh"
+
+namespace fp4moe {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kDecodeWarps = 8;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+
+struct GemmArgs {
+  const uint8_t* wprep;
+  const float* alpha;
+  const int32_t* tile_expert;
+  const int32_t* tile_mn;
+  const int32_t* num_tiles;
+  const int32_t* gather_rows;  // non-null: B rows are gathered (row = gather_rows[s] / top_k)
+  int32_t top_k;
+  int32_t F;                   // 256-row weight blocks per expert
+  int32_t C;                   // 128-element K chunks
+  int64_t out_ld;              // output row length (elements)
+  int32_t valid_rows;          // weight rows that exist (GEMM2: H)
+  void* out;
+  uint8_t* out_sf;
+  const float* fc2_scale;
+  int* err;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int kBBytes = 2 * BN * 128;                 // two 64-element K atoms
+  static constexpr int kStage = kWBlockBytes + kBBytes;        // multiple of 1024
+  static constexpr int kStagesRaw = (200 * 1024) / kStage;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kABase = 2 * BN <= 128 ? 128 : 256;     // TMEM column of A stage 0
+  static constexpr int kAStages = (512 - kABase) / 128;        // 128 columns per A stage
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes + 4 * 128;
+  static_assert(kStage % 1024 == 0, "stage alignment");
+  static_assert(kStages >= 2, "pipeline depth");
+};
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* afull = empty + C::kStages;
+  uint64_t* aempty = afull + C::kAStages;
+  uint64_t* accfull = aempty + C::kAStages;
+  uint64_t* drain = accfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int32_t* gidx = reinterpret_cast<int32_t*>(smem + C::kStages * C::kStage + C::kBarBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < C::kAStages; ++i) {
+      mbar_init(&afull[i], kDecodeWarps);
+      mbar_init(&aempty[i], 1);
+    }
+    mbar_init(accfull, 1);
+    mbar_init(drain, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) prefetch_tensormap(&bmap);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  grid_dependency_wait();
+  const int64_t n_items = (int64_t)a.num_tiles[0] * a.F;
+  const bool gather = a.gather_rows != nullptr;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
+    bool ok = true;
+    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
+      const int32_t e = a.tile_expert[tau];
+      if (gather) {
+        __syncwarp();
+        for (int i = lane; i < BN; i += 32) {
+          const int32_t r = a.gather_rows[(int64_t)tau * BN + i];
+          gidx[i] = r >= 0 ? r / a.top_k : 0;
+        }
+        __syncwarp();
+      }
+      const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kWBlockBytes;
+      for (int c = 0; c < a.C; ++c) {
+        if (lane == 0) {
+          ok = mbar_wait(&empty[stage], phase ^ 1u, a.err);
+          if (ok) {
+            uint8_t* sw = stages + stage * C::kStage;
+            uint8_t* sb = sw + kWBlockBytes;
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWBlockBytes + C::kBBytes));
+            tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &full[stage]);
+#pragma unroll
+            for (int at = 0; at < 2; ++at) {
+              const int32_t kc = c * kBK + at * 64;
+              uint8_t* dst = sb + at * BN * 128;
+              if (gather) {
+#pragma unroll
+                for (int g = 0; g < BN / 4; ++g)
+                  tma_gather4(dst + g * 512, &bmap, kc, gidx[4 * g], gidx[4 * g + 1],
+                              gidx[4 * g + 2], gidx[4 * g + 3], &full[stage]);
+              } else {
+                tma_load_2d(dst, &bmap, kc, tau * BN, &full[stage]);
+              }
+            }
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // copies still in flight must land before the CTA exits
+    if (lane == 0)
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_parity >> s) & 1u, a.err);
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
+      int stage = 0, astage = 0;
+      uint32_t phase = 0, aphase = 0;
+      bool ok = true;
+      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        for (int c = 0; c < a.C; ++c) {
+          if (!mbar_wait(&afull[astage], aphase, a.err) || !mbar_wait(&full[stage], phase, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sb = smem_u32(stages + stage * C::kStage + kWBlockBytes);
+#pragma unroll
+          for (int tile = 0; tile < 2; ++tile) {
+            const uint32_t d = tmem + (uint32_t)(tile * BN);
+            const uint32_t abase = tmem + (uint32_t)(C::kABase + astage * 128 + tile * 64);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bd = smem_desc_sw128(sb + (kk >> 2) * BN * 128 + (kk & 3) * 32);
+              mma_bf16_ts(d, abase + kk * 8, bd, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          tc_commit(&aempty[astage]);
+          tc_commit(&empty[stage]);
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++astage == C::kAStages) {
+            astage = 0;
+            aphase ^= 1u;
+          }
+        }
+        if (ok) tc_commit(accfull);
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, a.err);
+    }
+  } else {
+    // ------------------------------------------------------------ decode + epilogue
+    const int t = threadIdx.x;  // 0..255
+    const int tile = t >> 7, row = t & 127;
+    const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
+    int stage = 0, astage = 0;
+    uint32_t phase = 0, aphase = 0, accphase = 0;
+    bool ok = true;
+    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
+      for (int c = 0; c < a.C; ++c) {
+        bool good = mbar_wait(&full[stage], phase, a.err);
+        good = good && mbar_wait(&aempty[astage], aphase ^ 1u, a.err);
+        if (!__all_sync(0xffffffffu, good)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* blk = stages + stage * C::kStage;
+        const uint32_t r = (uint32_t)(tile * 128 + row);
+        uint4 dv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dv[q] = *reinterpret_cast<const uint4*>(blk + prep_chunk_offset(r, q));
+        const uint2 sv = *reinterpret_cast<const uint2*>(blk + kWDataBytes + r * 8);
+        uint32_t o[64];
+#pragma unroll
+        for (int sblk = 0; sblk < 8; ++sblk) {
+          const uint32_t sbyte = ((sblk < 4 ? sv.x : sv.y) >> (8 * (sblk & 3))) & 0xFFu;
+          const uint32_t sc2 = scale_bf16x2(sbyte);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int word = 2 * sblk + h;
+            const uint4& d4 = dv[word >> 2];
+            const uint32_t w = (word & 3) == 0 ? d4.x : (word & 3) == 1 ? d4.y : (word & 3) == 2 ? d4.z : d4.w;
+            decode_word(w, sc2, &o[4 * word]);
+          }
+        }
+        const uint32_t acol = tmem + lane_base + (uint32_t)(C::kABase + astage * 128 + tile * 64);
+        tmem_st16(acol + 0, o);
+        tmem_st16(acol + 16, o + 16);
+        tmem_st16(acol + 32, o + 32);
+        tmem_st16(acol + 48, o + 48);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afull[astage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++astage == C::kAStages) {
+          astage = 0;
+          aphase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      // ---------------- epilogue
+      if (!__all_sync(0xffffffffu, mbar_wait(accfull, accphase, a.err))) {
+        ok = false;
+        break;
+      }
+      accphase ^= 1u;
+      tc_fence_after();
+      const int32_t e = a.tile_expert[tau];
+      const int32_t mn = a.tile_mn[tau];
+      const float scale = a.alpha[e] * 256.0f;  // undo the decode's 2^-8
+      const int64_t s0 = (int64_t)tau * BN;
+      if (EPI == kEpiPlainBf16) {
+        const int64_t n = (int64_t)f * 256 + tile * 128 + row;
+        float* y = static_cast<float*>(a.out);   // fp32 route storage
+#pragma unroll 1
+        for (int cc = 0; cc < BN; cc += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc), v);
+          tmem_wait_ld();
+          if (n < a.valid_rows) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int64_t s = s0 + cc + i;
+              if (s < mn) y[s * a.out_ld + n] = __uint_as_float(v[i]) * scale;
+            }
+          }
+        }
+      } else {
+        constexpr int kCols = BN >= 32 ? BN / 2 : BN;
+        if (BN >= 32 || warp < 4) {
+          const int cbase = (BN >= 32 && warp >= 4) ? kCols : 0;
+          const int64_t n = (int64_t)f * 128 + row;
+          const float fs = EPI == kEpiSwigluNvfp4 ? a.fc2_scale[0] : 0.0f;
+#pragma unroll 1
+          for (int cc = 0; cc < kCols; cc += 16) {
+            uint32_t g[16], u[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)(cbase + cc), g);
+            tmem_ld16(tmem + lane_base + (uint32_t)(BN + cbase + cc), u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int64_t s = s0 + cbase + cc + i;
+              const float hv = s < mn ? swiglu(__uint_as_float(g[i]) * scale,
+                                               __uint_as_float(u[i]) * scale)
+                                      : 0.0f;
+              if (EPI == kEpiSwigluBf16) {
+                static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] = __float2bfloat16_rn(hv);
+              } else {
+                uint32_t sf;
+                const uint32_t code = nvfp4_quant_lane16(hv, fs, &sf);
+                const uint32_t other = __shfl_down_sync(0xffffffffu, code, 1);
+                if ((lane & 1) == 0)
+                  static_cast<uint8_t*>(a.out)[s * (a.out_ld / 2) + n / 2] = (uint8_t)(code | (other << 4));
+                if ((lane & 15) == 0) a.out_sf[s * (a.out_ld / 16) + n / 16] = (uint8_t)sf;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  __syncthreads();
+  launch_dependents();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// BF16 activation matrix [rows, K] -> tensor map, box {64, box_rows}, 128B swizzle
+bool make_act_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)std::max<int64_t>(rows, 1)};
+  const cuuint64_t strides[1] = {(cuuint64_t)(K * 2)};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  using Cf = Cfg<BN>;
+  GemmArgs a = {};
+  a.wprep = g.wprep;
+  a.alpha = g.alpha;
+  a.tile_expert = g.tile_expert;
+  a.tile_mn = g.tile_mn;
+  a.num_tiles = g.num_tiles;
+  a.gather_rows = g.gather_rows;
+  a.top_k = (int32_t)s.K;
+  a.F = (int32_t)row_blocks(s, g.which);
+  a.C = (int32_t)k_chunks(s, g.which);
+  a.out_ld = g.which == 1 ? s.I : s.H;
+  a.valid_rows = (int32_t)(g.which == 1 ? 2 * s.I : s.H);
+  a.out = g.out;
+  a.out_sf = g.out_sf;
+  a.fc2_scale = g.fc2_scale;
+  a.err = g.err;
+  const int64_t Kdim = g.which == 1 ? s.H : s.I;
+  CUtensorMap map;
+  if (!make_act_map(&map, g.act, g.act_rows, Kdim, g.gather_rows ? 1 : BN))
+    return cudaErrorInvalidValue;
+  auto kern = moe_gemm_kernel<BN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(sm_count(), max_items));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cf::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, map);
+}
+
+template <int BN>
+cudaError_t launch_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  switch (g.epi) {
+    case kEpiSwigluBf16: return launch_t<BN, kEpiSwigluBf16>(s, g, st, pdl);
+    case kEpiSwigluNvfp4: return launch_t<BN, kEpiSwigluNvfp4>(s, g, st, pdl);
+    case kEpiPlainBf16: return launch_t<BN, kEpiPlainBf16>(s, g, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  switch (s.T) {
+    case 16: return launch_bn<16>(s, g, st, pdl);
+    case 32: return launch_bn<32>(s, g, st, pdl);
+    case 64: return launch_bn<64>(s, g, st, pdl);
+    case 128: return launch_bn<128>(s, g, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fp4moe

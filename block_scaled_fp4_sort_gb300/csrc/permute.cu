@@ -1,0 +1,221 @@
+// permute.cu -- the bandwidth-bound steps around the GEMMs:
+//   * moe_permute: gather activation rows into permuted order
+//     (vllm.models.flint.ops.moe_cute, grouped_moe -> moe_permute);
+//   * the deterministic finalize: route-order weighted top-k sum
+//     (alphamoe_nvfp4_routed_moe: "finalize contributions in route order",
+//     routed_scaling_factor, accumulate; cute_dsl_fused_moe
+//     use_fused_finalize=False: the two-stage finalize);
+//   * NVFP4 row dequantisation to BF16 (exact) for the w4a4 GEMM inputs;
+//   * the standalone NVFP4 quantiser used by tests.
+// One warp or thread block per row, 16-byte vector accesses throughout.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "nvfp4.cuh"
+
+namespace fp4moe {
+namespace {
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern k, dim3 grid, dim3 block, cudaStream_t st, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// One warp per permuted row; rows past num_tiles*T are not touched.
+__global__ void permute_rows(const uint8_t* __restrict__ x, const uint8_t* __restrict__ x_sf,
+                             const int32_t* __restrict__ p2e, const int32_t* __restrict__ num_tiles,
+                             int64_t T, int64_t top_k, int64_t row_bytes, int64_t sf_bytes,
+                             uint8_t* __restrict__ px, uint8_t* __restrict__ px_sf) {
+  grid_dependency_wait();
+  const int64_t rows = (int64_t)num_tiles[0] * T;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t s = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); s < rows;
+       s += warps) {
+    const int32_t r = p2e[s];
+    const int64_t src = r >= 0 ? r / top_k : -1;
+    uint4* dst = reinterpret_cast<uint4*>(px + s * row_bytes);
+    const uint4* sp = reinterpret_cast<const uint4*>(x + src * row_bytes);
+    for (int64_t i = lane; i < row_bytes / 16; i += 32) dst[i] = src >= 0 ? sp[i] : make_uint4(0, 0, 0, 0);
+    if (x_sf != nullptr) {
+      uint2* dsf = reinterpret_cast<uint2*>(px_sf + s * sf_bytes);
+      const uint2* ssf = reinterpret_cast<const uint2*>(x_sf + src * sf_bytes);
+      for (int64_t i = lane; i < sf_bytes / 8; i += 32) dsf[i] = src >= 0 ? ssf[i] : make_uint2(0, 0);
+    }
+  }
+  launch_dependents();
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&p);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// out[t] = bf16(seed + sum_j (rsf * w[t,j]) * y[e2p[t,j]]), fp32, route order;
+// y is the fp32 route storage GEMM2 writes.
+__global__ void finalize_rows(const float4* __restrict__ y, const int32_t* __restrict__ e2p,
+                              const float* __restrict__ w, float rsf, int accumulate,
+                              uint4* __restrict__ out, int64_t M, int64_t H8, int top_k) {
+  grid_dependency_wait();
+  for (int64_t t = blockIdx.x; t < M; t += gridDim.x) {
+    for (int64_t c = threadIdx.x; c < H8; c += blockDim.x) {
+      float acc[8];
+      if (accumulate) {
+        bf16x8_to_f32(out[t * H8 + c], acc);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      }
+      for (int j = 0; j < top_k; ++j) {
+        const int32_t s = e2p[t * top_k + j];
+        if (s < 0) continue;
+        const float wk = rsf * w[t * top_k + j];
+        const float4 y0 = y[((int64_t)s * H8 + c) * 2], y1 = y[((int64_t)s * H8 + c) * 2 + 1];
+        const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk, yv[i], acc[i]);
+      }
+      out[t * H8 + c] = f32_to_bf16x8(acc);
+    }
+  }
+  launch_dependents();
+}
+
+__constant__ float kE2M1[16] = {0.0f,  0.5f,  1.0f,  1.5f,  2.0f,  3.0f,  4.0f,  6.0f,
+                                -0.0f, -0.5f, -1.0f, -1.5f, -2.0f, -3.0f, -4.0f, -6.0f};
+
+// NVFP4 rows -> BF16 rows (exact: every E2M1*E4M3 product is a BF16 value).
+// One thread per 8 elements.
+__global__ void dequant_rows(const uint32_t* __restrict__ q, const uint8_t* __restrict__ sf,
+                             int64_t rows, int64_t K, const int32_t* __restrict__ num_tiles,
+                             int64_t T, uint4* __restrict__ out) {
+  grid_dependency_wait();
+  const int64_t nrows = num_tiles ? min(rows, (int64_t)num_tiles[0] * T) : rows;
+  const int64_t per_row = K / 8;
+  const int64_t n = nrows * per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / per_row, c = i % per_row;
+    const uint32_t codes = q[r * (K / 8) + c];
+    const float s = e4m3_to_float(sf[r * (K / 16) + c / 2]);
+    float f[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) f[k] = kE2M1[(codes >> (4 * k)) & 15u] * s;
+    out[r * per_row + c] = f32_to_bf16x8(f);
+  }
+  launch_dependents();
+}
+
+__global__ void zero_bytes(uint4* p, int64_t n16) {
+  grid_dependency_wait();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = make_uint4(0, 0, 0, 0);
+  launch_dependents();
+}
+
+// 16 lanes per 16-element block; even lanes write the packed byte.
+__global__ void debug_quantize(const float* __restrict__ in, int64_t n, const float* scale,
+                               uint8_t* __restrict__ q, uint8_t* __restrict__ sf) {
+  const float s = scale[0];
+  const int lane = threadIdx.x & 31;
+  for (int64_t base = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) & ~31ll; base < n;
+       base += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = base + lane;
+    const float h = i < n ? in[i] : 0.0f;
+    uint32_t sc;
+    const uint32_t code = nvfp4_quant_lane16(h, s, &sc);
+    const uint32_t other = __shfl_down_sync(0xffffffffu, code, 1);
+    if (i < n && (lane & 1) == 0) q[i / 2] = (uint8_t)(code | (other << 4));
+    if (i < n && (lane & 15) == 0) sf[i / 16] = (uint8_t)sc;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, const int32_t* p2e,
+                           const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
+                           bool pdl) {
+  const int64_t row_bytes = s.mode == 0 ? s.H * 2 : s.H / 2;
+  const int64_t sf_bytes = s.mode == 0 ? 0 : s.H / 16;
+  const int64_t blocks = std::min<int64_t>((s.S + 7) / 8, (int64_t)num_sms() * 8);
+  return launch_pdl(permute_rows, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), st, pdl,
+                    static_cast<const uint8_t*>(x), s.mode == 0 ? nullptr : x_sf, p2e, num_tiles,
+                    s.T, s.K, row_bytes, sf_bytes, static_cast<uint8_t*>(px),
+                    s.mode == 0 ? nullptr : px_sf);
+}
+
+cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, const float* w,
+                            float rsf, int accumulate, void* out, cudaStream_t st, bool pdl) {
+  if (s.M == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>(s.M, (int64_t)num_sms() * 16);
+  const int threads = (int)std::min<int64_t>(256, ((s.H / 8) + 31) / 32 * 32);
+  return launch_pdl(finalize_rows, dim3((unsigned)blocks), dim3(threads), st, pdl,
+                    static_cast<const float4*>(y), e2p, w, rsf, accumulate,
+                    static_cast<uint4*>(out), s.M, s.H / 8, (int)s.K);
+}
+
+cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
+                                const int32_t* row_limit_tiles, int64_t T, void* out,
+                                cudaStream_t st, bool pdl) {
+  const int64_t n = rows * (K / 8);
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 16);
+  return launch_pdl(dequant_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
+                    reinterpret_cast<const uint32_t*>(q), sf, rows, K, row_limit_tiles, T,
+                    static_cast<uint4*>(out));
+}
+
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl) {
+  const int64_t n16 = (int64_t)(bytes / 16);
+  if (n16 == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n16 + 255) / 256, (int64_t)num_sms() * 16);
+  return launch_pdl(zero_bytes, dim3((unsigned)blocks), dim3(256), st, pdl,
+                    static_cast<uint4*>(p), n16);
+}
+
+cudaError_t launch_debug_quantize(const float* in, int64_t n, const float* scale, uint8_t* q,
+                                  uint8_t* sf, cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4096);
+  debug_quantize<<<(unsigned)blocks, 256, 0, st>>>(in, n, scale, q, sf);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4moe

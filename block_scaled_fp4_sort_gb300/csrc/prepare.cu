@@ -1,0 +1,141 @@
+// prepare.cu -- model-load repack of NVFP4 expert weights into the layout the
+// GEMM kernels stream (the counterpart of the pages' immutable prepared
+// weight panels: alphamoe_nvfp4_routed_moe, w1_data_prepared /
+// prepare_nvfp4_w1_data; and of the MMA scale layout the CuTe-DSL kernels
+// take, cute_dsl_fused_moe, localized_weights).  Pure bit movement.
+//
+// Block (e, f, c) = 256 weight rows x 128 K elements, contiguous:
+//   [0, 16384)      row r: 64 bytes = 16 prepared words, 16-byte chunks
+//                   XOR-swizzled by (r >> 1) & 3 (conflict-free 128-bit
+//                   shared-memory reads when thread r reads row r)
+//   [16384, 18432)  row r: the 8 E4M3 scale bytes of its 128 elements
+// GEMM1 (which = 1): rows 0..127 are gate rows 128f.., rows 128..255 the up
+// rows I+128f..; GEMM2 (which = 2): rows 256f.. of w2, zero past H.
+#include <algorithm>
+
+#include "common.cuh"
+#include "decode.cuh"
+#include "internal.h"
+
+namespace fp4moe {
+namespace {
+
+struct PrepArgs {
+  int which;
+  int64_t EL, F, C, rows_src, K;  // rows_src: rows per expert in the source (2I or H)
+  int64_t I;                      // GEMM1: intermediate size
+  const uint8_t* w;
+  const uint8_t* w_sf;
+  uint8_t* prep;
+  uint16_t* dbg_out;  // debug decode output (bf16 [EL, rows_src, K]) or null
+};
+
+__device__ __forceinline__ int64_t src_row(const PrepArgs& a, int64_t f, int64_t r) {
+  if (a.which == 1) return r < 128 ? 128 * f + r : a.I + 128 * f + (r - 128);
+  const int64_t row = 256 * f + r;
+  return row < a.rows_src ? row : -1;
+}
+
+// one thread per (block, row)
+__global__ void prepare_kernel(PrepArgs a) {
+  const int64_t n = a.EL * a.F * a.C * kRowsPerItem;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i % kRowsPerItem;
+    const int64_t blk = i / kRowsPerItem;
+    const int64_t c = blk % a.C, f = (blk / a.C) % a.F, e = blk / (a.C * a.F);
+    const int64_t sr = src_row(a, f, r);
+    uint8_t* dst = a.prep + blk * kWBlockBytes;
+    const uint32_t* src = sr >= 0 ? reinterpret_cast<const uint32_t*>(
+                                        a.w + (e * a.rows_src + sr) * (a.K / 2) + c * (kBK / 2))
+                                  : nullptr;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (src) {
+        v.x = prep_permute_word(src[4 * q + 0]);
+        v.y = prep_permute_word(src[4 * q + 1]);
+        v.z = prep_permute_word(src[4 * q + 2]);
+        v.w = prep_permute_word(src[4 * q + 3]);
+      }
+      *reinterpret_cast<uint4*>(dst + prep_chunk_offset((uint32_t)r, q)) = v;
+    }
+    uint2 s = make_uint2(0, 0);
+    if (src) s = *reinterpret_cast<const uint2*>(a.w_sf + (e * a.rows_src + sr) * (a.K / 16) + c * 8);
+    *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = s;
+  }
+}
+
+// Decode prepared blocks exactly as the GEMMs do, then undo the 2^-8.
+__global__ void debug_decode_kernel(PrepArgs a) {
+  const int64_t n = a.EL * a.F * a.C * kRowsPerItem;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i % kRowsPerItem;
+    const int64_t blk = i / kRowsPerItem;
+    const int64_t c = blk % a.C, f = (blk / a.C) % a.F, e = blk / (a.C * a.F);
+    const int64_t sr = src_row(a, f, r);
+    if (sr < 0) continue;
+    const uint8_t* b = a.prep + blk * kWBlockBytes;
+    const uint2 sv = *reinterpret_cast<const uint2*>(b + kWDataBytes + r * 8);
+    const uint32_t sbytes[2] = {sv.x, sv.y};
+    uint16_t* out = a.dbg_out + (e * a.rows_src + sr) * a.K + c * kBK;
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = *reinterpret_cast<const uint4*>(b + prep_chunk_offset((uint32_t)r, q));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int k = 0; k < 4; ++k) {
+        const int word = 4 * q + k;                 // elements 8*word .. 8*word+7
+        const uint32_t sb = (sbytes[word / 8] >> (8 * ((word / 2) % 4))) & 0xFFu;
+        uint32_t o[4];
+        decode_word(w[k], scale_bf16x2(sb), o);
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __uint_as_float(o[j] << 16) * 256.0f;
+          const float hi = __uint_as_float(o[j] & 0xFFFF0000u) * 256.0f;
+          __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+          *reinterpret_cast<__nv_bfloat162*>(out + 8 * word + 2 * j) = p;
+        }
+      }
+    }
+  }
+}
+
+PrepArgs make_args(const Shape& s, int which) {
+  PrepArgs a = {};
+  a.which = which;
+  a.EL = s.EL;
+  a.F = row_blocks(s, which);
+  a.C = k_chunks(s, which);
+  a.rows_src = which == 1 ? 2 * s.I : s.H;
+  a.K = which == 1 ? s.H : s.I;
+  a.I = s.I;
+  return a;
+}
+
+}  // namespace
+
+cudaError_t launch_prepare(const Shape& s, int which, const uint8_t* w, const uint8_t* w_sf,
+                           uint8_t* prepared, cudaStream_t st) {
+  PrepArgs a = make_args(s, which);
+  a.w = w;
+  a.w_sf = w_sf;
+  a.prep = prepared;
+  const int64_t n = a.EL * a.F * a.C * kRowsPerItem;
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
+  prepare_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_decode(const Shape& s, int which, const uint8_t* prepared, void* out,
+                                cudaStream_t st) {
+  PrepArgs a = make_args(s, which);
+  a.prep = const_cast<uint8_t*>(prepared);
+  a.dbg_out = static_cast<uint16_t*>(out);
+  const int64_t n = a.EL * a.F * a.C * kRowsPerItem;
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
+  debug_decode_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace fp4moe

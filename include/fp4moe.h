@@ -1,0 +1,252 @@
+/*
+ * fp4moe.h -- C ABI of the GB300 (sm_103a) NVFP4 fused-MoE forward pass.
+ *
+ *   out[t] = sum_j w[t,j] * W2_e(SwiGLU(W1_e x_t)),  e = token_selected_experts[t,j]
+ *
+ * with NVFP4 expert weights: packed E2M1 codes, one E4M3 scale per 16
+ * elements along K, one fp32 alpha per expert.  Argument names, shapes and
+ * dtypes follow the problem statement of the pages this library implements:
+ *   - flashinfer.fused_moe.cute_dsl_fused_moe, "Parameters" (x, x_sf,
+ *     token_selected_experts [M, top_k], token_final_scales [M, top_k],
+ *     w1_weight gate+up fused, w1_alpha, fc2_input_scale, w2_weight, w2_alpha,
+ *     num_local_experts, local_expert_offset, use_fused_finalize, moe_output);
+ *   - flashinfer.fused_moe.alphamoe_nvfp4_routed_moe, description and
+ *     "Parameters" (linear E4M3 scales, caller-owned int32 routing storage,
+ *     routed_scaling_factor, accumulate, everything on the current stream);
+ *   - vllm.models.flint.ops.moe_cute, grouped_moe (moe_sort -> moe_permute ->
+ *     grouped GEMM1 + SwiGLU -> grouped GEMM2 -> weighted top-k reduction,
+ *     and the routing-plan arrays).
+ *
+ * Conventions (all entry points):
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise, and
+ *     must be 16-byte aligned.  All arrays are dense row-major.
+ *   - The caller owns every buffer.  The library never allocates, never
+ *     synchronises the stream and never reads device memory on the host, so
+ *     every compute call may be captured in a CUDA graph.  All work is
+ *     enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Host-side validation failures return a status and enqueue nothing.
+ *   - Data-dependent errors found on the device (an expert id outside
+ *     [0, num_experts), a bounded wait that expired) set an error word: the
+ *     first int32 of the workspace.  It is sticky: zero it once before the
+ *     first call (a zero-filled workspace, or fp4moe_clear_error) and read it
+ *     with fp4moe_read_error() after synchronising.
+ *   - Packed E2M1: element 2i of a row in the low nibble of byte i, 2i+1 in
+ *     the high nibble.  Scales: E4M3 bytes, linear [rows, K/16].  Gate rows
+ *     are w1[:, 0:I), up rows w1[:, I:2I).
+ *   - Routes are numbered r = t*top_k + j.  The permutation is stable: one
+ *     expert's rows appear in ascending r, so at large M each tile gathers
+ *     from a narrow window of tokens (the contiguous-route-window property of
+ *     flashinfer PR #4440).
+ */
+#ifndef FP4MOE_H
+#define FP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FP4MOE_API __attribute__((visibility("default")))
+#else
+#define FP4MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FP4MOE_OK = 0,
+  FP4MOE_ERR_INVALID_ARG = 1,          /* null/misaligned pointer, bad shape or tile */
+  FP4MOE_ERR_UNSUPPORTED = 2,          /* a valid request this build does not implement */
+  FP4MOE_ERR_WORKSPACE_TOO_SMALL = 3,
+  FP4MOE_ERR_CUDA = 4,                 /* a CUDA runtime call failed (launch, memcpy) */
+  FP4MOE_ERR_DEVICE = 5,               /* device error word: invalid expert id */
+  FP4MOE_ERR_DEVICE_TIMEOUT = 6        /* device error word: a bounded wait expired */
+} fp4moe_status;
+
+typedef enum { FP4MOE_W4A16 = 0, FP4MOE_W4A4 = 1 } fp4moe_quant_mode;
+
+typedef enum {
+  FP4MOE_FINALIZE_DETERMINISTIC = 0,   /* GEMM2 writes y; a second pass sums in route order */
+  FP4MOE_FINALIZE_ATOMIC = 1           /* GEMM2's epilogue adds rsf*w*y into out atomically */
+} fp4moe_finalize_mode;
+
+typedef struct {
+  int32_t num_tokens;          /* M >= 0 */
+  int32_t hidden;              /* H, multiple of 128 */
+  int32_t inter;               /* I, multiple of 128 */
+  int32_t num_experts;         /* E >= 1 (global) */
+  int32_t top_k;               /* 1 <= top_k <= num_experts */
+  int32_t num_local_experts;   /* 0 means num_experts */
+  int32_t local_expert_offset; /* offset + num_local_experts <= num_experts */
+  int32_t route_tile;          /* T: 0 = automatic, else 16, 32, 64 or 128 */
+  int32_t mode;                /* fp4moe_quant_mode */
+} fp4moe_problem;
+
+/* ------------------------------------------------------------------ queries */
+
+/* Human-readable name of a status code (static storage). */
+FP4MOE_API const char* fp4moe_status_string(int32_t status);
+
+/* The route tile T the library uses for `p` (resolves route_tile = 0), or a
+ * negative fp4moe_status if `p` is invalid. */
+FP4MOE_API int32_t fp4moe_route_tile(const fp4moe_problem* p);
+
+/* S: number of permuted slots, padding included:
+ *   S = roundup(R + min(E_local, R) * (T - 1), T),  R = M * top_k
+ * (the bound vllm's moe_cute calls get_max_num_permuted_tokens; every expert
+ * wastes fewer than T slots).  Negative fp4moe_status if `p` is invalid. */
+FP4MOE_API int64_t fp4moe_max_permuted_slots(const fp4moe_problem* p);
+
+/* Workspace bytes of moe_route_sort (per-block histogram tables + error word). */
+FP4MOE_API size_t fp4moe_route_workspace_size(const fp4moe_problem* p);
+
+/* Workspace bytes of moe_gemm1_swiglu / moe_gemm2 (error word; for w4a4 also
+ * the BF16 copies of the NVFP4 activations the GEMM consumes). */
+FP4MOE_API size_t fp4moe_gemm_workspace_size(const fp4moe_problem* p, int32_t which /* 1 | 2 */);
+
+/* Workspace bytes of fused_moe_forward: routing plan, FC1 output h [S, I],
+ * GEMM2 output y [S, H] (fp32) and the scratch of the steps above. */
+FP4MOE_API size_t fp4moe_workspace_size(const fp4moe_problem* p);
+
+/* Bytes of the prepared (kernel-layout) weights of GEMM `which` (1 or 2). */
+FP4MOE_API size_t fp4moe_prepared_weight_size(const fp4moe_problem* p, int32_t which);
+
+/* Copy the device error word of a workspace (any of the workspaces above) to
+ * *code (host pointer): 0, FP4MOE_ERR_DEVICE or FP4MOE_ERR_DEVICE_TIMEOUT.
+ * Synchronises `stream`.  Diagnostic use only (not capturable). */
+FP4MOE_API fp4moe_status fp4moe_read_error(const void* workspace, int32_t* code, void* stream);
+
+/* Clear the error word of a workspace (enqueued on `stream`). */
+FP4MOE_API fp4moe_status fp4moe_clear_error(void* workspace, void* stream);
+
+/* ------------------------------------------------------- weight preparation */
+
+/* Model-load repack of one expert weight set from the pages' linear layout
+ * into the layout the GEMM kernels stream (the counterpart of the pages'
+ * immutable prepared weight panels, alphamoe_nvfp4_routed_moe
+ * `w1_data_prepared` and friends, and of the MMA scale layout the CuTe-DSL
+ * kernels require, cute_dsl_fused_moe `localized_weights`).
+ *   which = 1: w = w1 uint8 [E_local, 2I, H/2], w_sf = e4m3 [E_local, 2I, H/16]
+ *   which = 2: w = w2 uint8 [E_local, H, I/2],  w_sf = e4m3 [E_local, H, I/16]
+ * prepared: fp4moe_prepared_weight_size(p, which) bytes.  Bit-exact repack,
+ * no arithmetic.  Inputs are not modified. */
+FP4MOE_API fp4moe_status fp4moe_prepare_weights(const fp4moe_problem* p, int32_t which, const uint8_t* w,
+                                     const uint8_t* w_sf, void* prepared, void* stream);
+
+/* --------------------------------------------------------------- the steps */
+
+/* Routing plan: expert histogram, prefix sum padded to T, stable scatter
+ * (vllm moe_cute grouped_moe -> moe_sort; cute_dsl_fused_moe
+ * num_local_experts / local_expert_offset).
+ *   token_selected_experts  int32 [M, top_k], global ids
+ *   expanded_idx_to_permuted_idx  int32 [M, top_k]: slot of route r, or -1 if
+ *       the expert is not local or the id is invalid (the error word is set
+ *       for ids outside [0, num_experts))
+ *   permuted_idx_to_expanded_idx  int32 [S]: route in slot s, -1 for padding
+ *   tile_idx_to_expert      int32 [S/T]: local expert of tile tau, -1 past the end
+ *   tile_idx_to_mn_limit    int32 [S/T]: exclusive end of tile tau's valid slots
+ *   num_non_exiting_tiles   int32 [1]:   number of tiles in use
+ *   expert_counts           int32 [E_local] or NULL: routes per local expert
+ * Experts are laid out in ascending local id; within an expert, ascending r.
+ * Results are bit-exact and deterministic. */
+FP4MOE_API fp4moe_status moe_route_sort(const fp4moe_problem* p, const int32_t* token_selected_experts,
+                             int32_t* expanded_idx_to_permuted_idx,
+                             int32_t* permuted_idx_to_expanded_idx, int32_t* tile_idx_to_expert,
+                             int32_t* tile_idx_to_mn_limit, int32_t* num_non_exiting_tiles,
+                             int32_t* expert_counts, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* Gather activation rows into permuted order (vllm moe_cute grouped_moe ->
+ * moe_permute):  permuted_x[s] = x[permuted_idx_to_expanded_idx[s] / top_k]
+ * for s < num_non_exiting_tiles * T; padding rows are zero-filled.
+ *   w4a16: x bf16 [M, H] -> permuted_x bf16 [S, H]; x_sf, permuted_x_sf NULL
+ *   w4a4 : x uint8 [M, H/2] + x_sf e4m3 [M, H/16] -> [S, H/2] + [S, H/16]
+ * fused_moe_forward does not call this: its GEMM1 gathers rows by TMA. */
+FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
+                          const int32_t* permuted_idx_to_expanded_idx,
+                          const int32_t* num_non_exiting_tiles, void* permuted_x,
+                          uint8_t* permuted_x_sf, void* stream);
+
+/* Grouped GEMM1 with the SwiGLU epilogue (vllm moe_cute module docstring:
+ * E2M1*E4M3 decoded to BF16, BF16 tcgen05 MMAs, fp32 accumulation, alpha on
+ * the accumulator, silu(g)*u in fp32 rounded once):
+ *   h[s, n] = R( silu(a1_e * G_e[n] . A_s) * (a1_e * U_e[n] . A_s) )
+ * for valid slots s (padding rows of h are zeroed), e = tile_idx_to_expert.
+ *   a: activations.  If gather_rows != NULL it is x itself ([M, H] bf16, or
+ *      [M, H/2] + a_sf [M, H/16] for w4a4) and row s is row
+ *      gather_rows[s] / top_k (gather_rows = permuted_idx_to_expanded_idx);
+ *      otherwise a is already permuted ([S, ...]).
+ *   w1_prepared: fp4moe_prepare_weights(p, 1, ...).  w1_alpha fp32 [E_local].
+ *   w4a16: h bf16 [S, I] (R = round to BF16); h_sf, fc2_input_scale NULL.
+ *   w4a4 : h uint8 [S, I/2] + h_sf e4m3 [S, I/16]: R = NVFP4 quantisation with
+ *          fc2_input_scale fp32 [1]: per 16-block sf = E4M3((amax*s)/6),
+ *          q = E2M1((h*s)/sf), fp32 arithmetic, RNE, saturating. */
+FP4MOE_API fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uint8_t* a_sf,
+                               const int32_t* gather_rows, const void* w1_prepared,
+                               const float* w1_alpha, const float* fc2_input_scale,
+                               const int32_t* tile_idx_to_expert,
+                               const int32_t* tile_idx_to_mn_limit,
+                               const int32_t* num_non_exiting_tiles, void* h, uint8_t* h_sf,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Grouped GEMM2, the down projection, unweighted, in permuted order (vllm
+ * moe_cute grouped_moe: GEMM2 output y [route_slots, H]):
+ *   y[s, n] = a2_e * W2_e[n] . h_s   for valid slots s, stored as fp32 (the
+ *   "FP32 route storage" option of alphamoe_nvfp4_routed_moe; BF16 storage of
+ *   y would put ~0.2% of outputs outside the parity bound through
+ *   cancellation in the weighted sum).  y: fp32 [S, H].
+ *   h: bf16 [S, I] (w4a16) or uint8 [S, I/2] + h_sf [S, I/16] (w4a4).
+ *   w2_prepared: fp4moe_prepare_weights(p, 2, ...).  w2_alpha fp32 [E_local]. */
+FP4MOE_API fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h_sf,
+                        const void* w2_prepared, const float* w2_alpha,
+                        const int32_t* tile_idx_to_expert, const int32_t* tile_idx_to_mn_limit,
+                        const int32_t* num_non_exiting_tiles, void* y, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* Deterministic weighted top-k reduction (cute_dsl_fused_moe
+ * use_fused_finalize=False; alphamoe_nvfp4_routed_moe: route order,
+ * routed_scaling_factor, accumulate):
+ *   out[t] = bf16( seed_t + sum_{j=0..k-1, in order} (rsf * w[t,j]) * y[e2p[t,j]] )
+ * in fp32, seed_t = float(out[t]) if accumulate else +0.0f; routes with
+ * e2p = -1 add nothing.  accumulate = 0 equals accumulate = 1 on a +0 output
+ * bit for bit.  y fp32 [S, H]; token_final_scales fp32 [M, top_k]; out bf16 [M, H]. */
+FP4MOE_API fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y,
+                           const int32_t* expanded_idx_to_permuted_idx,
+                           const float* token_final_scales, float routed_scaling_factor,
+                           int32_t accumulate, void* out, void* stream);
+
+/* The whole forward on `stream`: route sort, GEMM1 (+ SwiGLU, TMA row gather
+ * straight from x), GEMM2, finalize.  Arguments as in the steps above; the
+ * weights are prepared (fp4moe_prepare_weights).  finalize_mode:
+ *   FP4MOE_FINALIZE_DETERMINISTIC: bit-reproducible (default);
+ *   FP4MOE_FINALIZE_ATOMIC: GEMM2's epilogue adds into out (zeroed first when
+ *     accumulate = 0); summation order varies run to run.
+ * workspace: fp4moe_workspace_size(p) bytes. */
+FP4MOE_API fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
+                                const int32_t* token_selected_experts,
+                                const float* token_final_scales, const void* w1_prepared,
+                                const float* w1_alpha, const float* fc2_input_scale,
+                                const void* w2_prepared, const float* w2_alpha,
+                                float routed_scaling_factor, int32_t accumulate,
+                                int32_t finalize_mode, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------ test support */
+
+/* Run the device NVFP4 quantiser of GEMM1's w4a4 epilogue on n fp32 values
+ * (n % 16 == 0): q uint8 [n/2], sf e4m3 [n/16].  Same device function as the
+ * epilogue, exported so that tests can compare it bit for bit. */
+FP4MOE_API fp4moe_status fp4moe_debug_quantize_nvfp4(const float* in, int64_t n, const float* scale,
+                                          uint8_t* q, uint8_t* sf, void* stream);
+
+/* Decode prepared weights back to their BF16 values as the GEMM kernels see
+ * them: out bf16 [E_local, rows, K] for GEMM `which` (rows = 2I or H).
+ * Exported so that tests can check the decode path against the linear input. */
+FP4MOE_API fp4moe_status fp4moe_debug_decode_prepared(const fp4moe_problem* p, int32_t which,
+                                           const void* prepared, void* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP4MOE_H */

@@ -250,6 +250,18 @@ class OracleMoE:
         return out, ex, bool(bad)
 
 
+def route_plan(M, E, top_k, T, ids, E_local=None, offset=0):
+    """Oracle routing plan for ids [M, top_k] (no weights needed)."""
+    E_local = E if E_local is None else E_local
+    z = np.zeros
+    o = OracleMoE(M, 128, 128, E, top_k, np.asarray(ids, np.int32).reshape(M, top_k),
+                  z((M, top_k), np.float32), z((1, 256, 64), np.uint8), z((1, 256, 8), np.uint8),
+                  z(1, np.float32), z((1, 128, 64), np.uint8), z((1, 128, 8), np.uint8),
+                  z(1, np.float32), x=z((max(M, 1), 128), np.uint16), E_local=E_local,
+                  offset=offset, T=T)
+    return o.route_sort()
+
+
 def _bf16():
     import torch
     return torch.bfloat16

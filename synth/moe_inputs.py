@@ -201,6 +201,12 @@ def _routing(cfg: MoEConfig, rng: np.random.Generator):
 # --------------------------------------------------------------------------
 
 
+def generate_routing(cfg: MoEConfig):
+    """Routing draw of `cfg` alone: (ids int32 [M, k], weights fp32 [M, k]) as numpy."""
+    ss_route = np.random.SeedSequence(cfg.seed).spawn(5)[0]
+    return _routing(cfg, np.random.Generator(np.random.PCG64(ss_route)))
+
+
 def _torch_seed(ss: np.random.SeedSequence) -> int:
     return int(ss.generate_state(1, dtype=np.uint64)[0] & ((1 << 62) - 1))
 

@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and validates arguments on the host (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import block_scaled_fp4_sort_gb300 as fm
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp4moe.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    return re.findall(r"^FP4MOE_API [^(]*?\b([a-z_0-9]+)\(", src, flags=re.M)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_scaled_fp4_sort_gb300 import build
+    build.build()
+    return fm.lib()
+
+
+def test_header_declares_the_six_entry_points():
+    names = set(_declared())
+    for n in ("moe_route_sort", "moe_permute", "moe_gemm1_swiglu", "moe_gemm2", "moe_finalize",
+              "fused_moe_forward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert names and set(names) == set(fm.ABI_FUNCTIONS)
+    raw = ctypes.CDLL(fm.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_product_does_not_reach_the_oracle():
+    pkg = os.path.join(ROOT, "block_scaled_fp4_sort_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "fp4moe_oracle" not in text and "orc_" not in text, f
+
+
+@pytest.mark.parametrize("M,E,k,T", [(8, 256, 8, 16), (4096, 256, 8, 128), (2048, 128, 4, 64),
+                                     (131072, 256, 8, 128), (16, 8, 2, 16), (1, 1, 1, 32), (0, 4, 2, 16)])
+def test_slot_bound_matches_oracle(lib, M, E, k, T):
+    p = fm.problem(M, 256, 256, E, k, route_tile=T)
+    assert fm.max_permuted_slots(p) == oracle.max_permuted_slots(M * k, E, T)
+    assert fm.route_tile(p) == T
+
+
+def test_auto_route_tile(lib):
+    assert fm.route_tile(fm.problem(8, 7168, 2048, 256, 8)) == 16
+    assert fm.route_tile(fm.problem(4096, 7168, 2048, 256, 8)) == 128
+    assert fm.route_tile(fm.problem(2048, 4096, 1536, 128, 4)) == 64
+    assert fm.route_tile(fm.problem(131072, 6144, 2048, 256, 8)) == 128
+
+
+def test_sizes(lib):
+    p = fm.problem(8, 7168, 2048, 256, 8)
+    assert fm.workspace_size(p) > 0
+    assert fm.prepared_weight_size(p, 1) == 256 * 16 * 56 * 18432      # I/128 blocks x H/128 chunks
+    assert fm.prepared_weight_size(p, 2) == 256 * 28 * 16 * 18432      # H/256 blocks x I/128 chunks
+    assert fm.gemm_workspace_size(p, 1) >= 256
+    assert fm.prepared_weight_size(p, 3) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(hidden=200), fm.ERR_INVALID_ARG),
+    (dict(inter=100), fm.ERR_INVALID_ARG),
+    (dict(top_k=0), fm.ERR_INVALID_ARG),
+    (dict(route_tile=7), fm.ERR_INVALID_ARG),
+    (dict(route_tile=8), fm.ERR_UNSUPPORTED),
+    (dict(route_tile=256), fm.ERR_UNSUPPORTED),
+    (dict(num_local_experts=300), fm.ERR_INVALID_ARG),
+    (dict(num_local_experts=16, local_expert_offset=250), fm.ERR_INVALID_ARG),
+    (dict(mode=5), fm.ERR_INVALID_ARG),
+])
+def test_invalid_problems_are_rejected_on_the_host(lib, kw, status):
+    base = dict(num_tokens=8, hidden=256, inter=256, num_experts=256, top_k=8)
+    base.update(kw)
+    p = fm.problem(**base)
+    with pytest.raises(fm.Fp4MoeError) as ei:
+        fm.route_tile(p)
+    assert ei.value.status == status
+    assert fm.workspace_size(p) == 0
+
+
+def test_null_pointers_rejected_before_any_launch(lib):
+    p = fm.problem(8, 256, 256, 8, 2)
+
+    class Fake:
+        def __init__(self, n):
+            self.n = n
+
+        def data_ptr(self):
+            return 0
+
+        def numel(self):
+            return self.n
+
+        def element_size(self):
+            return 1
+    ws = Fake(1 << 20)
+    with pytest.raises(fm.Fp4MoeError) as ei:
+        fm.fused_moe_forward(p, None, None, None, None, None, None, None, None, None, 1.0, False, 0,
+                             None, ws, stream=0)
+    assert ei.value.status == fm.ERR_INVALID_ARG
+    with pytest.raises(fm.Fp4MoeError) as ei:
+        fm.moe_route_sort(p, None, None, None, None, None, None, None, ws, stream=0)
+    assert ei.value.status == fm.ERR_INVALID_ARG
+    assert fm.status_string(fm.ERR_DEVICE_TIMEOUT).startswith("device error")
