@@ -88,31 +88,32 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
 }
 
 // out[t] = bf16(seed + sum_j (rsf * w[t,j]) * y[e2p[t,j]]), fp32, route order;
-// y is the fp32 route storage GEMM2 writes.
+// y is the fp32 route storage GEMM2 writes.  One thread per 8 outputs.
 __global__ void finalize_rows(const float4* __restrict__ y, const int32_t* __restrict__ e2p,
                               const float* __restrict__ w, float rsf, int accumulate,
                               uint4* __restrict__ out, int64_t M, int64_t H8, int top_k) {
   grid_dependency_wait();
-  for (int64_t t = blockIdx.x; t < M; t += gridDim.x) {
-    for (int64_t c = threadIdx.x; c < H8; c += blockDim.x) {
-      float acc[8];
-      if (accumulate) {
-        bf16x8_to_f32(out[t * H8 + c], acc);
-      } else {
+  const int64_t n = M * H8;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / H8, c = i % H8;
+    float acc[8];
+    if (accumulate) {
+      bf16x8_to_f32(out[i], acc);
+    } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-      }
-      for (int j = 0; j < top_k; ++j) {
-        const int32_t s = e2p[t * top_k + j];
-        if (s < 0) continue;
-        const float wk = rsf * w[t * top_k + j];
-        const float4 y0 = y[((int64_t)s * H8 + c) * 2], y1 = y[((int64_t)s * H8 + c) * 2 + 1];
-        const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk, yv[i], acc[i]);
-      }
-      out[t * H8 + c] = f32_to_bf16x8(acc);
+      for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
     }
+    for (int j = 0; j < top_k; ++j) {
+      const int32_t s = e2p[t * top_k + j];
+      if (s < 0) continue;
+      const float wk = rsf * w[t * top_k + j];
+      const float4 y0 = y[((int64_t)s * H8 + c) * 2], y1 = y[((int64_t)s * H8 + c) * 2 + 1];
+      const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = fmaf(wk, yv[k], acc[k]);
+    }
+    out[i] = f32_to_bf16x8(acc);
   }
   launch_dependents();
 }
@@ -184,9 +185,9 @@ cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, c
 cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, const float* w,
                             float rsf, int accumulate, void* out, cudaStream_t st, bool pdl) {
   if (s.M == 0) return cudaSuccess;
-  const int64_t blocks = std::min<int64_t>(s.M, (int64_t)num_sms() * 16);
-  const int threads = (int)std::min<int64_t>(256, ((s.H / 8) + 31) / 32 * 32);
-  return launch_pdl(finalize_rows, dim3((unsigned)blocks), dim3(threads), st, pdl,
+  const int64_t n = s.M * (s.H / 8);
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 16);
+  return launch_pdl(finalize_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
                     static_cast<const float4*>(y), e2p, w, rsf, accumulate,
                     static_cast<uint4*>(out), s.M, s.H / 8, (int)s.K);
 }
