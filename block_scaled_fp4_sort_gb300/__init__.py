@@ -23,7 +23,7 @@ ABI_FUNCTIONS = (
     "fp4moe_status_string", "fp4moe_route_tile", "fp4moe_max_permuted_slots",
     "fp4moe_route_workspace_size", "fp4moe_gemm_workspace_size", "fp4moe_workspace_size",
     "fp4moe_prepared_weight_size", "fp4moe_read_error", "fp4moe_clear_error",
-    "fp4moe_prepare_weights", "moe_route_sort", "moe_permute", "moe_gemm1_swiglu", "moe_gemm2",
+    "fp4moe_prepare_weights", "moe_route_sort", "moe_route_sort_noalloc", "moe_permute", "moe_gemm1_swiglu", "moe_gemm2",
     "moe_finalize", "fused_moe_forward", "fp4moe_debug_quantize_nvfp4",
     "fp4moe_debug_decode_prepared",
 )
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
             "fp4moe_clear_error": (i32, [vp, vp]),
             "fp4moe_prepare_weights": (i32, [P, i32, vp, vp, vp, vp]),
             "moe_route_sort": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "moe_route_sort_noalloc": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "moe_permute": (i32, [P, vp, vp, vp, vp, vp, vp, vp]),
             "moe_gemm1_swiglu": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "moe_gemm2": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
@@ -178,6 +179,19 @@ def moe_route_sort(p: Problem, token_selected_experts, expanded_idx_to_permuted_
                                 _p(tile_idx_to_expert), _p(tile_idx_to_mn_limit),
                                 _p(num_non_exiting_tiles), _p(expert_counts), _p(workspace),
                                 _nbytes(workspace), _stream(stream)), "moe_route_sort")
+
+
+def moe_route_sort_noalloc(p: Problem, token_selected_experts, expanded_idx_to_permuted_idx,
+                           permuted_idx_to_expanded_idx, tile_idx_to_expert, tile_idx_to_mn_limit,
+                           num_non_exiting_tiles, expert_counts=None, error_flag=None, stream=None):
+    """moe_route_sort without a workspace: the library keeps its scratch in a
+    static device array (for callers that cannot allocate device memory)."""
+    _check(lib().moe_route_sort_noalloc(ctypes.byref(p), _p(token_selected_experts),
+                                        _p(expanded_idx_to_permuted_idx),
+                                        _p(permuted_idx_to_expanded_idx), _p(tile_idx_to_expert),
+                                        _p(tile_idx_to_mn_limit), _p(num_non_exiting_tiles),
+                                        _p(expert_counts), _p(error_flag), _stream(stream)),
+           "moe_route_sort_noalloc")
 
 
 def moe_permute(p: Problem, x, x_sf, permuted_idx_to_expanded_idx, num_non_exiting_tiles,

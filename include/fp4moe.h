@@ -157,6 +157,33 @@ FP4MOE_API fp4moe_status moe_route_sort(const fp4moe_problem* p, const int32_t* 
                              int32_t* expert_counts, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* moe_route_sort for callers that cannot allocate device memory (a plugin
+ * inside another framework's executor without access to its allocator, or a
+ * runtime that must not grow its footprint after start-up).  No counterpart
+ * in the pages: it exists so that such callers can still build the routing
+ * plan.  Same arguments, results and bit-exactness as moe_route_sort, but no
+ * workspace: the scratch (per-chunk histograms and the error word) lives in a
+ * 1 MiB file-scope device array that every GPU loading the library holds
+ * until the process exits.  The library allocates nothing in this call.
+ *   error_flag  int32 [1] or NULL: if given, zeroed and then set to
+ *               FP4MOE_ERR_DEVICE when an expert id lies outside
+ *               [0, num_experts); if NULL that word lives in the array.
+ * Returns FP4MOE_ERR_UNSUPPORTED if the problem needs more scratch than the
+ * array holds: ceil(M*top_k / 4096) * E_local * 4 bytes + 256 must fit in
+ * 1 MiB (routes up to 4096 need none).  The first call on each device looks
+ * up the array's device address (cudaGetSymbolAddress with that device
+ * current); make it before any stream capture.  Every call shares the array,
+ * so calls that overlap on the GPU (other streams, other threads) race. */
+FP4MOE_API fp4moe_status moe_route_sort_noalloc(const fp4moe_problem* p,
+                                                const int32_t* token_selected_experts,
+                                                int32_t* expanded_idx_to_permuted_idx,
+                                                int32_t* permuted_idx_to_expanded_idx,
+                                                int32_t* tile_idx_to_expert,
+                                                int32_t* tile_idx_to_mn_limit,
+                                                int32_t* num_non_exiting_tiles,
+                                                int32_t* expert_counts, int32_t* error_flag,
+                                                void* stream);
+
 /* Gather activation rows into permuted order (vllm moe_cute grouped_moe ->
  * moe_permute):  permuted_x[s] = x[permuted_idx_to_expanded_idx[s] / top_k]
  * for s < num_non_exiting_tiles * T; padding rows are zero-filled.
