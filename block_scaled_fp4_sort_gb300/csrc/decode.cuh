@@ -58,6 +58,30 @@ __device__ __forceinline__ void decode_word(uint32_t w, uint32_t sc2, uint32_t* 
   o[3] = bf16x2_mul(r3, sc2);
 }
 
+// prepared word -> the 4 BF16x2 registers of an m16n8k16 A fragment: pairs 0
+// and 2 belong to row R0 (scale sc0), pairs 1 and 3 to row R1 = R0 + 8 (sc1)
+__device__ __forceinline__ void decode_word_frag(uint32_t w, uint32_t sc0, uint32_t sc1,
+                                                 uint32_t* o) {
+  const uint32_t r0 = w & (kMagMask | kSignMask);
+  const uint32_t r1 = (__funnelshift_l(w, w, 3) & kMagMask) | (__funnelshift_l(w, w, 4) & kSignMask);
+  const uint32_t r2 = __funnelshift_l(w, w, 6) & (kMagMask | kSignMask);
+  const uint32_t r3 = (__funnelshift_l(w, w, 10) & kMagMask) | (__funnelshift_l(w, w, 5) & kSignMask);
+  o[0] = bf16x2_mul(r0, sc0);
+  o[1] = bf16x2_mul(r1, sc1);
+  o[2] = bf16x2_mul(r2, sc0);
+  o[3] = bf16x2_mul(r3, sc1);
+}
+
+// Fragment layout (decode-size kernel): warp w of the 16 compute warps owns
+// block rows 16w..16w+15; lane l (g = l/4, t = l%4) owns rows R0 = 16w+g and
+// R1 = R0+8 and, for each 16-element K step kk, one prepared word holding
+// (R0,16kk+2t..+1), (R1,16kk+2t..+1), (R0,16kk+8+2t..+1), (R1,16kk+8+2t..+1).
+// A lane's 8 words are 32 contiguous bytes; its two 16-byte halves swap when
+// bit 2 of the lane is set (conflict-free 128-bit shared loads).
+__host__ __device__ constexpr uint32_t frag_half_offset(uint32_t w, uint32_t lane, uint32_t h) {
+  return (w * 32u + lane) * 32u + ((h ^ ((lane >> 2) & 1u)) * 16u);
+}
+
 // byte offset, inside a prepared block's data region, of 16-byte chunk q of row r
 __host__ __device__ constexpr uint32_t prep_chunk_offset(uint32_t r, uint32_t q) {
   return r * 64u + ((q ^ ((r >> 1) & 3u)) * 16u);

@@ -9,7 +9,7 @@
 #include <algorithm>
 #include <cstring>
 
-#include "../../include/fp4moe.h"
+#include "fp4moe.h"
 #include "internal.h"
 
 using namespace fp4moe;

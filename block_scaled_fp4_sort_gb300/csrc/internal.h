@@ -31,6 +31,12 @@ inline int64_t row_blocks(const Shape& s, int which) {
   return which == 1 ? s.I / 128 : (s.H + 255) / 256;
 }
 inline int64_t k_chunks(const Shape& s, int which) { return which == 1 ? s.H / kBK : s.I / kBK; }
+// Decode-size problems (BF16 activations, route tile 16) run on the
+// warp-level MMA kernel, whose prepared blocks hold the codes in MMA fragment
+// order; every other problem uses the row order of the tcgen05 kernel.  Both
+// layouts have the same block size and the same scale region.
+inline bool fragment_layout(const Shape& s) { return s.mode == 0 && s.T == 16; }
+
 inline size_t prepared_bytes(const Shape& s, int which) {
   return (size_t)s.EL * row_blocks(s, which) * k_chunks(s, which) * kWBlockBytes;
 }

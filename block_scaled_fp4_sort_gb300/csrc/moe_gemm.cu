@@ -23,8 +23,8 @@
 //              memory.  After the last chunk the same warps run the epilogue
 //              (tcgen05.ld of the fp32 accumulators).
 //   warp 9     MMA issuer: tcgen05.mma.cta_group::1.kind::f16, A from TMEM,
-//              B from shared memory, D in TMEM; tcgen05.commit releases the
-//              shared-memory stage and the TMEM A stage.
+//              B from shared memory, D in TMEM; one tcgen05.commit per chunk
+//              releases both the shared-memory stage and the TMEM A stage.
 // Every wait is bounded (common.cuh); on timeout the error word is set, the
 // producer waits for its copies in flight, the MMA warp drains, TMEM is freed.
 #include <algorithm>
@@ -86,8 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
   uint64_t* empty = full + C::kStages;
   uint64_t* afull = empty + C::kStages;
-  uint64_t* aempty = afull + C::kAStages;
-  uint64_t* accfull = aempty + C::kAStages;
+  uint64_t* accfull = afull + C::kAStages;
   uint64_t* drain = accfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int32_t* gidx = reinterpret_cast<int32_t*>(smem + C::kStages * C::kStage + C::kBarBytes);
@@ -100,7 +99,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < C::kAStages; ++i) {
       mbar_init(&afull[i], kDecodeWarps);
-      mbar_init(&aempty[i], 1);
     }
     mbar_init(accfull, 1);
     mbar_init(drain, 1);
@@ -199,8 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16_ts(d, abase + kk * 8, bd, kIdesc, (c > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          tc_commit(&aempty[astage]);
-          tc_commit(&empty[stage]);
+          tc_commit(&empty[stage]);   // one commit frees both the SMEM stage and the TMEM A stage
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
@@ -221,13 +218,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile = t >> 7, row = t & 127;
     const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
     int stage = 0, astage = 0;
-    uint32_t phase = 0, aphase = 0, accphase = 0;
+    uint32_t phase = 0, accphase = 0, qd = 0;   // qd: chunks decoded so far by this CTA
     bool ok = true;
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       for (int c = 0; c < a.C; ++c) {
         bool good = mbar_wait(&full[stage], phase, a.err);
-        good = good && mbar_wait(&aempty[astage], aphase ^ 1u, a.err);
+        // TMEM A stage (qd % kAStages) was last read by the MMAs of chunk
+        // qd - kAStages, whose commit completes SMEM stage (qd - kAStages) %
+        // kStages.  That barrier cannot run a further phase ahead: the next one
+        // needs chunk qd - kAStages + kStages, not yet decoded.
+        if (qd >= (uint32_t)C::kAStages) {
+          const uint32_t qp = qd - (uint32_t)C::kAStages;
+          good = good && mbar_wait(&empty[qp % C::kStages], (qp / C::kStages) & 1u, a.err);
+        }
+        ++qd;
         if (!__all_sync(0xffffffffu, good)) {
           ok = false;
           break;
@@ -265,10 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           stage = 0;
           phase ^= 1u;
         }
-        if (++astage == C::kAStages) {
-          astage = 0;
-          aphase ^= 1u;
-        }
+        if (++astage == C::kAStages) astage = 0;
       }
       if (!ok) break;
       // ---------------- epilogue
@@ -341,6 +343,278 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// ===========================================================================
+// Decode-size grouped GEMM: BF16 activations, route tile 16.
+//
+// At decode sizes a tile holds one or two real tokens and the GEMM is a
+// weight-streaming GEMV.  A tcgen05.mma with M=128, K=16 costs >= 46 cycles
+// for N <= 64 (79 with a commit in the stream, ~97 with concurrent TMEM
+// stores, measured on GB300), which caps a 16-column tile well below the HBM
+// rate.  This kernel keeps the TMA producer and the work items of the
+// tcgen05 kernel but multiplies on warp-level MMAs (mma.sync m16n8k16, BF16
+// in, fp32 accumulate): the prepared weights are stored in A-fragment order,
+// so one decoded 32-bit word is a lane's A fragment for one 16-element K step
+// and the decoded weights never leave registers.
+//   warps 0-15  compute: warp w owns block rows 16w..16w+15 (GEMM1: warps
+//               0-7 gate rows, 8-15 the matching up rows); fp32 accumulators
+//               in registers over the whole K range (four chains, summed in a
+//               fixed order); the second 8-column n-block runs only when the
+//               tile holds more than 8 tokens.
+//   warp 16     TMA producer, as in the tcgen05 kernel.
+// SwiGLU pairs gate and up rows through shared memory with two bounded
+// mbarrier handshakes per item.
+// ===========================================================================
+
+constexpr int kGvWarps = 16;
+constexpr int kGvThreads = 32 * (kGvWarps + 1);
+
+struct GvCfg {
+  static constexpr int BN = 16;
+  static constexpr int kBBytes = 2 * BN * 128;
+  static constexpr int kStage = kWBlockBytes + kBBytes;
+  static constexpr int kStages = 8;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kXchgBytes = 128 * BN * 4;
+  static constexpr int kLutBytes = 256 * 4;  // E4M3 byte -> BF16x2 of scale * 2^118
+  static constexpr int kSmem =
+      1024 + kStages * kStage + kBarBytes + 4 * 128 + kXchgBytes + kLutBytes;
+  static_assert(kStage % 1024 == 0, "stage alignment");
+};
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The K loop of one work item for NB n-blocks (1 or 2), a compile-time
+// count so that the eight unrolled K steps of a chunk form one basic block
+// the compiler can interleave.  acc[nb][j] are four independent accumulator
+// chains per n-block (K step kk feeds chain kk & 3).  Returns false on a
+// bounded-wait timeout.
+template <int NB>
+__device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, uint64_t* full,
+                                          uint64_t* empty, const uint32_t* lut,
+                                          const uint32_t (&boff)[8], int w, int lane, uint32_t r0,
+                                          uint32_t r1, int& stage, uint32_t& phase,
+                                          float (&acc)[2][4][4]) {
+  for (int c = 0; c < a.C; ++c) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) return false;
+    const uint8_t* blk = stages + stage * GvCfg::kStage;
+    const uint4 h0 = *reinterpret_cast<const uint4*>(blk + frag_half_offset(w, lane, 0));
+    const uint4 h1 = *reinterpret_cast<const uint4*>(blk + frag_half_offset(w, lane, 1));
+    const uint2 sa = *reinterpret_cast<const uint2*>(blk + kWDataBytes + r0 * 8);
+    const uint2 sb = *reinterpret_cast<const uint2*>(blk + kWDataBytes + r1 * 8);
+    const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    const uint8_t* bt = blk + kWBlockBytes;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t ba = __byte_perm(kk < 4 ? sa.x : sa.y, 0u, 0x4440u + (kk & 3));
+      const uint32_t bb = __byte_perm(kk < 4 ? sb.x : sb.y, 0u, 0x4440u + (kk & 3));
+      uint32_t af[4];
+      decode_word_frag(words[kk], lut[ba], lut[bb], af);
+      const uint8_t* atom = bt + (kk >> 2) * GvCfg::BN * 128;  // K 0..63 or 64..127
+      const int q0 = 2 * (kk & 3);                             // chunks q0, q0+1: k and k+8
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(atom + nb * 1024 + boff[q0]);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(atom + nb * 1024 + boff[q0 + 1]);
+        mma_16816(acc[nb][kk & 3], af, b0, b1);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == GvCfg::kStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  return true;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kGvThreads, 1)
+    moe_gemv_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap) {
+  using C = GvCfg;
+  constexpr int BN = GvCfg::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* xready = empty + C::kStages;
+  uint64_t* xfree = xready + 1;
+  int32_t* gidx = reinterpret_cast<int32_t*>(smem + C::kStages * C::kStage + C::kBarBytes);
+  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kBarBytes + 4 * 128);
+  uint32_t* lut = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(xchg) + C::kXchgBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) lut[i] = scale_bf16x2((uint32_t)i);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kGvWarps);
+    }
+    mbar_init(xready, kGvWarps / 2);
+    mbar_init(xfree, kGvWarps / 2);
+    fence_mbarrier_init();
+  }
+  if (warp == kGvWarps && lane == 0) prefetch_tensormap(&bmap);
+  __syncthreads();
+
+  grid_dependency_wait();
+  const int64_t n_items = (int64_t)a.num_tiles[0] * a.F;
+  const bool gather = a.gather_rows != nullptr;
+
+  if (warp == kGvWarps) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
+    bool ok = true;
+    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
+      const int32_t e = a.tile_expert[tau];
+      if (gather) {
+        __syncwarp();
+        if (lane < BN) {
+          const int32_t r = a.gather_rows[(int64_t)tau * BN + lane];
+          gidx[lane] = r >= 0 ? r / a.top_k : 0;
+        }
+        __syncwarp();
+      }
+      const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kWBlockBytes;
+      for (int c = 0; c < a.C; ++c) {
+        if (lane == 0) {
+          ok = mbar_wait(&empty[stage], phase ^ 1u, a.err);
+          if (ok) {
+            uint8_t* sw = stages + stage * C::kStage;
+            uint8_t* sb = sw + kWBlockBytes;
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWBlockBytes + C::kBBytes));
+            tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &full[stage]);
+#pragma unroll
+            for (int at = 0; at < 2; ++at) {
+              const int32_t kc = c * kBK + at * 64;
+              uint8_t* dst = sb + at * BN * 128;
+              if (gather) {
+#pragma unroll
+                for (int q = 0; q < BN / 4; ++q)
+                  tma_gather4(dst + q * 512, &bmap, kc, gidx[4 * q], gidx[4 * q + 1],
+                              gidx[4 * q + 2], gidx[4 * q + 3], &full[stage]);
+              } else {
+                tma_load_2d(dst, &bmap, kc, tau * BN, &full[stage]);
+              }
+            }
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (lane == 0)
+      for (int q = 0; q < C::kStages; ++q)
+        if (issued_mask & (1u << q)) mbar_wait(&full[q], (issued_parity >> q) & 1u, a.err);
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int w = warp, g = lane >> 2, t = lane & 3;
+    const uint32_t r0 = (uint32_t)(16 * w + g), r1 = r0 + 8;
+    // byte offset of this lane's B-fragment word inside 16-byte chunk q of its
+    // token row g (row 8+g of the second n-block is 1024 bytes further): the
+    // activation tile is 128-byte swizzled, chunk q of row n at chunk q ^ (n & 7)
+    uint32_t boff[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      boff[q] = (uint32_t)g * 128u + (((uint32_t)q ^ (uint32_t)g) << 4) + 4u * (uint32_t)t;
+    int stage = 0;
+    uint32_t phase = 0, xphase = 0;
+    bool ok = true;
+    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
+      const int32_t mn = a.tile_mn[tau];
+      const int64_t s0 = (int64_t)tau * BN;
+      const bool two = mn - s0 > 8;  // second n-block needed (warp-uniform)
+      float acc[2][4][4];
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[nb][p][i] = 0.0f;
+      ok = two ? gv_k_loop<2>(a, stages, full, empty, lut, boff, w, lane, r0, r1, stage, phase, acc)
+               : gv_k_loop<1>(a, stages, full, empty, lut, boff, w, lane, r0, r1, stage, phase, acc);
+      if (!ok) break;
+      // ---------------- epilogue: d[nb][i] at (row i<2 ? r0 : r1, column 8nb + 2t + (i&1))
+      const int32_t e = a.tile_expert[tau];
+      const float scale = a.alpha[e] * 256.0f;  // undo the decode's 2^-8
+      float d[2][4];
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          d[nb][i] = ((acc[nb][0][i] + acc[nb][1][i]) + (acc[nb][2][i] + acc[nb][3][i])) * scale;
+      if (EPI == kEpiPlainBf16) {
+        float* y = static_cast<float*>(a.out);  // fp32 route storage
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int64_t feat = (int64_t)f * 256 + (i < 2 ? r0 : r1);
+            const int64_t s = s0 + 8 * nb + 2 * t + (i & 1);
+            if ((nb == 0 || two) && s < mn && feat < a.valid_rows) y[s * a.out_ld + feat] = d[nb][i];
+          }
+        }
+      } else {
+        // up rows (warps 8-15) hand their values to the gate rows (warps 0-7)
+        if (w >= kGvWarps / 2) {
+          if (!__all_sync(0xffffffffu, mbar_wait(xfree, xphase ^ 1u, a.err))) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              xchg[((i < 2 ? r0 : r1) - 128) * BN + 8 * nb + 2 * t + (i & 1)] = d[nb][i];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(xready);
+        } else {
+          if (!__all_sync(0xffffffffu, mbar_wait(xready, xphase, a.err))) {
+            ok = false;
+            break;
+          }
+          __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t row = i < 2 ? r0 : r1;
+              const int n = 8 * nb + 2 * t + (i & 1);
+              const int64_t s = s0 + n;
+              const float u = xchg[row * BN + n];
+              const float hv = s < mn ? swiglu(d[nb][i], u) : 0.0f;
+              h[s * a.out_ld + (int64_t)f * 128 + row] = __float2bfloat16_rn(hv);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(xfree);
+        }
+        xphase ^= 1u;
+      }
+    }
+  }
+  __syncthreads();
+  launch_dependents();
 }
 
 int sm_count() {
@@ -435,9 +709,54 @@ cudaError_t launch_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
   }
 }
 
+template <int EPI>
+cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  GemmArgs a = {};
+  a.wprep = g.wprep;
+  a.alpha = g.alpha;
+  a.tile_expert = g.tile_expert;
+  a.tile_mn = g.tile_mn;
+  a.num_tiles = g.num_tiles;
+  a.gather_rows = g.gather_rows;
+  a.top_k = (int32_t)s.K;
+  a.F = (int32_t)row_blocks(s, g.which);
+  a.C = (int32_t)k_chunks(s, g.which);
+  a.out_ld = g.which == 1 ? s.I : s.H;
+  a.valid_rows = (int32_t)(g.which == 1 ? 2 * s.I : s.H);
+  a.out = g.out;
+  a.err = g.err;
+  const int64_t Kdim = g.which == 1 ? s.H : s.I;
+  CUtensorMap map;
+  if (!make_act_map(&map, g.act, g.act_rows, Kdim, g.gather_rows ? 1 : GvCfg::BN))
+    return cudaErrorInvalidValue;
+  auto kern = moe_gemv_kernel<EPI>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GvCfg::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(sm_count(), max_items));
+  cfg.blockDim = dim3(kGvThreads);
+  cfg.dynamicSmemBytes = GvCfg::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, map);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  if (fragment_layout(s)) {
+    switch (g.epi) {
+      case kEpiSwigluBf16: return launch_gv<kEpiSwigluBf16>(s, g, st, pdl);
+      case kEpiPlainBf16: return launch_gv<kEpiPlainBf16>(s, g, st, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (s.T) {
     case 16: return launch_bn<16>(s, g, st, pdl);
     case 32: return launch_bn<32>(s, g, st, pdl);

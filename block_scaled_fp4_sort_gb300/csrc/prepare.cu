@@ -11,6 +11,8 @@
 //   [16384, 18432)  row r: the 8 E4M3 scale bytes of its 128 elements
 // GEMM1 (which = 1): rows 0..127 are gate rows 128f.., rows 128..255 the up
 // rows I+128f..; GEMM2 (which = 2): rows 256f.. of w2, zero past H.
+// Decode-size problems store the code bytes in MMA fragment order instead
+// (decode.cuh, frag_half_offset); the scale region is the same.
 #include <algorithm>
 
 #include "common.cuh"
@@ -63,6 +65,80 @@ __global__ void prepare_kernel(PrepArgs a) {
     uint2 s = make_uint2(0, 0);
     if (src) s = *reinterpret_cast<const uint2*>(a.w_sf + (e * a.rows_src + sr) * (a.K / 16) + c * 8);
     *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = s;
+  }
+}
+
+// Fragment layout: one thread per (block, warp slot w, lane).
+__global__ void prepare_fragment_kernel(PrepArgs a) {
+  const int64_t n = a.EL * a.F * a.C * 512;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t lane = (uint32_t)(i & 31), w = (uint32_t)((i >> 5) & 15);
+    const int64_t blk = i >> 9;
+    const int64_t c = blk % a.C, f = (blk / a.C) % a.F, e = blk / (a.C * a.F);
+    const uint32_t g = lane >> 2, t = lane & 3;
+    const int64_t rows[2] = {src_row(a, f, 16 * w + g), src_row(a, f, 16 * w + g + 8)};
+    uint8_t* dst = a.prep + blk * kWBlockBytes;
+    uint32_t words[8];
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t v = 0;
+      for (int j = 0; j < 4; ++j) {  // fragment register j: one byte = codes k, k+1
+        const int64_t row = rows[j & 1];
+        const int64_t k = c * kBK + 16 * kk + 8 * (j >> 1) + 2 * t;
+        uint32_t byte = 0;
+        if (row >= 0) byte = a.w[(e * a.rows_src + row) * (a.K / 2) + k / 2];
+        v |= byte << (8 * j);
+      }
+      words[kk] = prep_permute_word(v);
+    }
+    *reinterpret_cast<uint4*>(dst + frag_half_offset(w, lane, 0)) =
+        make_uint4(words[0], words[1], words[2], words[3]);
+    *reinterpret_cast<uint4*>(dst + frag_half_offset(w, lane, 1)) =
+        make_uint4(words[4], words[5], words[6], words[7]);
+    if (t == 0) {  // scale region: the same row-major layout as the row-order blocks
+      for (int h = 0; h < 2; ++h) {
+        const int64_t row = rows[h];
+        const uint32_t r = 16 * w + g + 8 * h;
+        uint2 sv = make_uint2(0, 0);
+        if (row >= 0)
+          sv = *reinterpret_cast<const uint2*>(a.w_sf + (e * a.rows_src + row) * (a.K / 16) + c * 8);
+        *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = sv;
+      }
+    }
+  }
+}
+
+__global__ void debug_decode_fragment_kernel(PrepArgs a) {
+  const int64_t n = a.EL * a.F * a.C * 512;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t lane = (uint32_t)(i & 31), w = (uint32_t)((i >> 5) & 15);
+    const int64_t blk = i >> 9;
+    const int64_t c = blk % a.C, f = (blk / a.C) % a.F, e = blk / (a.C * a.F);
+    const uint32_t g = lane >> 2, t = lane & 3;
+    const uint32_t r0 = 16 * w + g, r1 = r0 + 8;
+    const int64_t rows[2] = {src_row(a, f, r0), src_row(a, f, r1)};
+    const uint8_t* b = a.prep + blk * kWBlockBytes;
+    const uint4 h0 = *reinterpret_cast<const uint4*>(b + frag_half_offset(w, lane, 0));
+    const uint4 h1 = *reinterpret_cast<const uint4*>(b + frag_half_offset(w, lane, 1));
+    const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    const uint2 s0 = *reinterpret_cast<const uint2*>(b + kWDataBytes + r0 * 8);
+    const uint2 s1 = *reinterpret_cast<const uint2*>(b + kWDataBytes + r1 * 8);
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t b0 = ((kk < 4 ? s0.x : s0.y) >> (8 * (kk & 3))) & 0xFFu;
+      const uint32_t b1 = ((kk < 4 ? s1.x : s1.y) >> (8 * (kk & 3))) & 0xFFu;
+      uint32_t o[4];
+      decode_word_frag(words[kk], scale_bf16x2(b0), scale_bf16x2(b1), o);
+      for (int j = 0; j < 4; ++j) {
+        const int64_t row = rows[j & 1];
+        if (row < 0) continue;
+        const int64_t k = c * kBK + 16 * kk + 8 * (j >> 1) + 2 * t;
+        const float lo = __uint_as_float(o[j] << 16) * 256.0f;
+        const float hi = __uint_as_float(o[j] & 0xFFFF0000u) * 256.0f;
+        *reinterpret_cast<__nv_bfloat162*>(a.dbg_out + (e * a.rows_src + row) * a.K + k) =
+            __floats2bfloat162_rn(lo, hi);
+      }
+    }
   }
 }
 
@@ -119,10 +195,14 @@ cudaError_t launch_prepare(const Shape& s, int which, const uint8_t* w, const ui
   a.w = w;
   a.w_sf = w_sf;
   a.prep = prepared;
-  const int64_t n = a.EL * a.F * a.C * kRowsPerItem;
+  const bool frag = fragment_layout(s);
+  const int64_t n = a.EL * a.F * a.C * (frag ? 512 : kRowsPerItem);
   if (n == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
-  prepare_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  if (frag)
+    prepare_fragment_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  else
+    prepare_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -131,10 +211,14 @@ cudaError_t launch_debug_decode(const Shape& s, int which, const uint8_t* prepar
   PrepArgs a = make_args(s, which);
   a.prep = const_cast<uint8_t*>(prepared);
   a.dbg_out = static_cast<uint16_t*>(out);
-  const int64_t n = a.EL * a.F * a.C * kRowsPerItem;
+  const bool frag = fragment_layout(s);
+  const int64_t n = a.EL * a.F * a.C * (frag ? 512 : kRowsPerItem);
   if (n == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
-  debug_decode_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  if (frag)
+    debug_decode_fragment_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  else
+    debug_decode_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

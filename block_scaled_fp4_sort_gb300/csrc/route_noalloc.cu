@@ -21,7 +21,7 @@
 
 #include <atomic>
 
-#include "../../include/fp4moe.h"
+#include "fp4moe.h"
 #include "internal.h"
 
 namespace fp4moe {

@@ -124,7 +124,8 @@ def test_prepared_weights_decode_exactly():
         assert np.array_equal(f64(out), want)
 
 
-def test_prepared_weights_decode_all_codes_and_scales():
+@pytest.mark.parametrize("T", [16, 32])   # fragment order (decode-size kernel) and row order
+def test_prepared_weights_decode_all_codes_and_scales(T):
     # every code byte against every finite non-negative E4M3 scale
     H, I, E = 256, 128, 1
     codes = np.arange(256, dtype=np.uint8)
@@ -132,7 +133,7 @@ def test_prepared_weights_decode_all_codes_and_scales():
     sfv = np.resize(np.arange(0x7F, dtype=np.uint8), (E, 2 * I, H // 16)).astype(np.uint8)
     w2 = np.resize(codes[::-1], (E, H, I // 2)).astype(np.uint8)
     sf2 = np.resize(np.arange(0x7F, dtype=np.uint8)[::-1], (E, H, I // 16)).astype(np.uint8)
-    p = fm.problem(1, H, I, E, 1)
+    p = fm.problem(1, H, I, E, 1, route_tile=T)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     B = MoEBuffers(p).prepare(t(w1), t(sfv), t(w2), t(sf2))
     for which, w, sf, prep in ((1, w1, sfv, B.w1p), (2, w2, sf2, B.w2p)):
