@@ -6,13 +6,26 @@
 // and mask per field:
 //   r_j = (rotl(w, kMagRot[j]) & magnitude bits) | (rotl(w, kSignRot[j]) & sign bits)
 // with magnitudes landing on BF16 bits 6..8 (+16) and signs on bit 15 (+16).
-// Rotations (0,3,6,10) / (0,4,6,5) tile the 32 bits; pairs 0 and 2 need a
-// single mask, so a word costs 11 integer operations (a search over all
-// layouts of this form finds none cheaper).
+// Rotations (0,3,6,10) / (0,4,6,5) tile the 32 bits.  Only pair 3's
+// magnitudes wrap around, so every other field is a plain left shift, and
+// pairs 0 and 2 need a single mask: 6 logic operations per word.  No layout
+// of this form gives every pair a single rotation (the four translates of the
+// eight target bits cannot tile the word), so 6 is the minimum.
 // Placing the 3 magnitude bits of an E2M1 code at BF16 bits 6..8 yields
 // exactly +-e2m1 * 2^-126 (the E2M1 subnormal 0.5 lands on the BF16
 // subnormal 2^-127), so one BF16x2 multiply by (scale * 2^118) gives the
 // exact weight times 2^-8; the GEMM epilogue multiplies alpha by 2^8.
+// The shifts are written as integer multiplies so that they can issue on the
+// FMA pipe; only the six masks need the integer ALU.
+//
+// Scale codes: the E4M3 scale byte b of each 16-element block is stored as
+// an 8-bit code c with BF16(|scale| * 2^118) == 16 c + 0x7000, so the
+// BF16x2 multiplier is one multiply-add, c * 0x00100010 + 0x70007000.
+// Normal scales map to c = |b| + 112, subnormal ones to their normalised
+// BF16 exponent and mantissa, NaN to c = 255 (a BF16 NaN).  The scale's sign
+// moves into the block's code signs and a zero scale clears the code
+// magnitudes, keeping their signs, so every decoded weight, signed zeros and
+// NaNs included, is the product e2m1(code) * e4m3(b) bit for bit.
 #pragma once
 
 #include "common.cuh"
@@ -39,19 +52,49 @@ __host__ __device__ inline uint32_t prep_permute_word(uint32_t v) {
   return out;
 }
 
-// BF16x2 (both halves) of e4m3(b) * 2^118
-__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t b) {
-  const float f = e4m3_to_float(b) * 0x1p118f;
-  __nv_bfloat162 p = __floats2bfloat162_rn(f, f);
-  return *reinterpret_cast<uint32_t*>(&p);
+// E4M3 scale byte -> prepared scale code (see the header comment)
+__host__ __device__ constexpr uint32_t prep_scale_code(uint32_t b) {
+  const uint32_t m = b & 0x7Fu;
+  if (m == 0x7Fu) return 0xFFu;   // NaN
+  if (m == 0) return 0x70u;       // zero: any finite code, the codes carry the zero
+  if (m >= 8) return m + 112u;    // normal: exponent + 14, same 3 mantissa bits
+  // subnormal m * 2^-9 = 2^p (1 + f) * 2^-9, p = floor(log2 m)
+  const uint32_t p = m >= 4 ? 2u : m >= 2 ? 1u : 0u;
+  return ((12u + p) << 3) | ((m << (3u - p)) & 7u);
+}
+
+// Moves the sign and the zero of scale byte b into linear E2M1 codes
+// (sign_bits: 0x88 for one byte of two codes, 0x88888888 for a word).
+__host__ __device__ constexpr uint32_t prep_fix_codes(uint32_t v, uint32_t b, uint32_t sign_bits) {
+  return (b & 0x7Fu) == 0 ? ((b & 0x80u) ? v ^ sign_bits : v) & sign_bits
+                          : ((b & 0x80u) ? v ^ sign_bits : v);
+}
+
+// BF16x2 (both halves) of |scale| * 2^118 from a prepared scale code
+__device__ __forceinline__ uint32_t scale_code_bf16x2(uint32_t c) {
+  return c * 0x00100010u + 0x70007000u;
+}
+
+// The four BF16x2 bit fields of a prepared word (pairs 0..3).
+__device__ __forceinline__ void decode_fields(uint32_t w, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  constexpr uint32_t M = kMagMask | kSignMask;
+  r0 = w & M;
+  const uint32_t m1 = w & (kMagMask >> 3), s1 = w & (kSignMask >> 4);
+  uint32_t t, w5;
+  uint64_t p;
+  asm("mad.lo.u32 %0, %1, 2, %2;" : "=r"(t) : "r"(s1), "r"(m1));   // fields of pair 1
+  asm("mul.lo.u32 %0, %1, 8;" : "=r"(r1) : "r"(t));                // ... shifted into place
+  asm("mul.lo.u32 %0, %1, 64;" : "=r"(r2) : "r"(w & (M >> 6)));    // pair 2: one shift
+  asm("mul.wide.u32 %0, %1, 1024;" : "=l"(p) : "r"(w));            // pair 3 magnitudes: rotl 10
+  asm("mul.lo.u32 %0, %1, 32;" : "=r"(w5) : "r"(w));               // pair 3 signs: shl 5
+  r3 = (((uint32_t)p | (uint32_t)(p >> 32)) & kMagMask) | (w5 & kSignMask);
 }
 
 // prepared word -> 4 BF16x2 words (K elements 0..7 of the word), times sc2
 __device__ __forceinline__ void decode_word(uint32_t w, uint32_t sc2, uint32_t* o) {
-  const uint32_t r0 = w & (kMagMask | kSignMask);
-  const uint32_t r1 = (__funnelshift_l(w, w, 3) & kMagMask) | (__funnelshift_l(w, w, 4) & kSignMask);
-  const uint32_t r2 = __funnelshift_l(w, w, 6) & (kMagMask | kSignMask);
-  const uint32_t r3 = (__funnelshift_l(w, w, 10) & kMagMask) | (__funnelshift_l(w, w, 5) & kSignMask);
+  uint32_t r0, r1, r2, r3;
+  decode_fields(w, r0, r1, r2, r3);
   o[0] = bf16x2_mul(r0, sc2);
   o[1] = bf16x2_mul(r1, sc2);
   o[2] = bf16x2_mul(r2, sc2);
@@ -62,10 +105,8 @@ __device__ __forceinline__ void decode_word(uint32_t w, uint32_t sc2, uint32_t* 
 // and 2 belong to row R0 (scale sc0), pairs 1 and 3 to row R1 = R0 + 8 (sc1)
 __device__ __forceinline__ void decode_word_frag(uint32_t w, uint32_t sc0, uint32_t sc1,
                                                  uint32_t* o) {
-  const uint32_t r0 = w & (kMagMask | kSignMask);
-  const uint32_t r1 = (__funnelshift_l(w, w, 3) & kMagMask) | (__funnelshift_l(w, w, 4) & kSignMask);
-  const uint32_t r2 = __funnelshift_l(w, w, 6) & (kMagMask | kSignMask);
-  const uint32_t r3 = (__funnelshift_l(w, w, 10) & kMagMask) | (__funnelshift_l(w, w, 5) & kSignMask);
+  uint32_t r0, r1, r2, r3;
+  decode_fields(w, r0, r1, r2, r3);
   o[0] = bf16x2_mul(r0, sc0);
   o[1] = bf16x2_mul(r1, sc1);
   o[2] = bf16x2_mul(r2, sc0);

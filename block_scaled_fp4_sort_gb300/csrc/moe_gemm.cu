@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int sblk = 0; sblk < 8; ++sblk) {
           const uint32_t sbyte = ((sblk < 4 ? sv.x : sv.y) >> (8 * (sblk & 3))) & 0xFFu;
-          const uint32_t sc2 = scale_bf16x2(sbyte);
+          const uint32_t sc2 = scale_code_bf16x2(sbyte);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int word = 2 * sblk + h;
@@ -377,9 +377,7 @@ struct GvCfg {
   static constexpr int kStages = 8;
   static constexpr int kBarBytes = 256;
   static constexpr int kXchgBytes = 128 * BN * 4;
-  static constexpr int kLutBytes = 256 * 4;  // E4M3 byte -> BF16x2 of scale * 2^118
-  static constexpr int kSmem =
-      1024 + kStages * kStage + kBarBytes + 4 * 128 + kXchgBytes + kLutBytes;
+  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes + 4 * 128 + kXchgBytes;
   static_assert(kStage % 1024 == 0, "stage alignment");
 };
 
@@ -399,8 +397,7 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 // bounded-wait timeout.
 template <int NB>
 __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, uint64_t* full,
-                                          uint64_t* empty, const uint32_t* lut,
-                                          const uint32_t (&boff)[8], int w, int lane, uint32_t r0,
+                                          uint64_t* empty, const uint32_t (&boff)[8], int w, int lane, uint32_t r0,
                                           uint32_t r1, int& stage, uint32_t& phase,
                                           float (&acc)[2][4][4]) {
   for (int c = 0; c < a.C; ++c) {
@@ -414,10 +411,10 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
     const uint8_t* bt = blk + kWBlockBytes;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t ba = __byte_perm(kk < 4 ? sa.x : sa.y, 0u, 0x4440u + (kk & 3));
-      const uint32_t bb = __byte_perm(kk < 4 ? sb.x : sb.y, 0u, 0x4440u + (kk & 3));
+      const uint32_t ca = __byte_perm(kk < 4 ? sa.x : sa.y, 0u, 0x4440u + (kk & 3));
+      const uint32_t cb = __byte_perm(kk < 4 ? sb.x : sb.y, 0u, 0x4440u + (kk & 3));
       uint32_t af[4];
-      decode_word_frag(words[kk], lut[ba], lut[bb], af);
+      decode_word_frag(words[kk], scale_code_bf16x2(ca), scale_code_bf16x2(cb), af);
       const uint8_t* atom = bt + (kk >> 2) * GvCfg::BN * 128;  // K 0..63 or 64..127
       const int q0 = 2 * (kk & 3);                             // chunks q0, q0+1: k and k+8
 #pragma unroll
@@ -452,10 +449,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
   uint64_t* xfree = xready + 1;
   int32_t* gidx = reinterpret_cast<int32_t*>(smem + C::kStages * C::kStage + C::kBarBytes);
   float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kBarBytes + 4 * 128);
-  uint32_t* lut = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(xchg) + C::kXchgBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) lut[i] = scale_bf16x2((uint32_t)i);
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
@@ -551,8 +546,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         for (int p = 0; p < 4; ++p)
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[nb][p][i] = 0.0f;
-      ok = two ? gv_k_loop<2>(a, stages, full, empty, lut, boff, w, lane, r0, r1, stage, phase, acc)
-               : gv_k_loop<1>(a, stages, full, empty, lut, boff, w, lane, r0, r1, stage, phase, acc);
+      ok = two ? gv_k_loop<2>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc)
+               : gv_k_loop<1>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc);
       if (!ok) break;
       // ---------------- epilogue: d[nb][i] at (row i<2 ? r0 : r1, column 8nb + 2t + (i&1))
       const int32_t e = a.tile_expert[tau];

@@ -2,13 +2,16 @@
 // GEMM kernels stream (the counterpart of the pages' immutable prepared
 // weight panels: alphamoe_nvfp4_routed_moe, w1_data_prepared /
 // prepare_nvfp4_w1_data; and of the MMA scale layout the CuTe-DSL kernels
-// take, cute_dsl_fused_moe, localized_weights).  Pure bit movement.
+// take, cute_dsl_fused_moe, localized_weights).  Lossless bit re-encoding:
+// every decoded weight equals e2m1(code) * e4m3(scale) bit for bit.
 //
 // Block (e, f, c) = 256 weight rows x 128 K elements, contiguous:
 //   [0, 16384)      row r: 64 bytes = 16 prepared words, 16-byte chunks
 //                   XOR-swizzled by (r >> 1) & 3 (conflict-free 128-bit
 //                   shared-memory reads when thread r reads row r)
-//   [16384, 18432)  row r: the 8 E4M3 scale bytes of its 128 elements
+//   [16384, 18432)  row r: the 8 scale codes of its 128 elements
+//                   (decode.cuh: prep_scale_code; the scale's sign and zero
+//                   are moved into the codes by prep_fix_codes)
 // GEMM1 (which = 1): rows 0..127 are gate rows 128f.., rows 128..255 the up
 // rows I+128f..; GEMM2 (which = 2): rows 256f.. of w2, zero past H.
 // Decode-size problems store the code bytes in MMA fragment order instead
@@ -51,20 +54,26 @@ __global__ void prepare_kernel(PrepArgs a) {
     const uint32_t* src = sr >= 0 ? reinterpret_cast<const uint32_t*>(
                                         a.w + (e * a.rows_src + sr) * (a.K / 2) + c * (kBK / 2))
                                   : nullptr;
+    uint2 s = make_uint2(0, 0);  // rows past the matrix: zero codes under a zero scale
+    if (src) s = *reinterpret_cast<const uint2*>(a.w_sf + (e * a.rows_src + sr) * (a.K / 16) + c * 8);
+    const uint32_t sb[2] = {s.x, s.y};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      uint4 v = make_uint4(0, 0, 0, 0);
+      uint32_t v[4] = {0, 0, 0, 0};
       if (src) {
-        v.x = prep_permute_word(src[4 * q + 0]);
-        v.y = prep_permute_word(src[4 * q + 1]);
-        v.z = prep_permute_word(src[4 * q + 2]);
-        v.w = prep_permute_word(src[4 * q + 3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // word 4q+i: elements 8(4q+i).., scale block (4q+i)/2
+          const int word = 4 * q + i;
+          const uint32_t b = (sb[word >> 3] >> (8 * ((word >> 1) & 3))) & 0xFFu;
+          v[i] = prep_permute_word(prep_fix_codes(src[word], b, 0x88888888u));
+        }
       }
-      *reinterpret_cast<uint4*>(dst + prep_chunk_offset((uint32_t)r, q)) = v;
+      *reinterpret_cast<uint4*>(dst + prep_chunk_offset((uint32_t)r, q)) = make_uint4(v[0], v[1], v[2], v[3]);
     }
-    uint2 s = make_uint2(0, 0);
-    if (src) s = *reinterpret_cast<const uint2*>(a.w_sf + (e * a.rows_src + sr) * (a.K / 16) + c * 8);
-    *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = s;
+    uint32_t codes[2] = {0, 0};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) codes[i >> 2] |= prep_scale_code((sb[i >> 2] >> (8 * (i & 3))) & 0xFFu) << (8 * (i & 3));
+    *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = make_uint2(codes[0], codes[1]);
   }
 }
 
@@ -79,6 +88,10 @@ __global__ void prepare_fragment_kernel(PrepArgs a) {
     const uint32_t g = lane >> 2, t = lane & 3;
     const int64_t rows[2] = {src_row(a, f, 16 * w + g), src_row(a, f, 16 * w + g + 8)};
     uint8_t* dst = a.prep + blk * kWBlockBytes;
+    uint8_t sc[2][8];  // E4M3 scale bytes of the two rows, zero past the matrix
+    for (int h = 0; h < 2; ++h)
+      for (int kk = 0; kk < 8; ++kk)
+        sc[h][kk] = rows[h] >= 0 ? a.w_sf[(e * a.rows_src + rows[h]) * (a.K / 16) + c * 8 + kk] : 0;
     uint32_t words[8];
     for (int kk = 0; kk < 8; ++kk) {
       uint32_t v = 0;
@@ -86,7 +99,7 @@ __global__ void prepare_fragment_kernel(PrepArgs a) {
         const int64_t row = rows[j & 1];
         const int64_t k = c * kBK + 16 * kk + 8 * (j >> 1) + 2 * t;
         uint32_t byte = 0;
-        if (row >= 0) byte = a.w[(e * a.rows_src + row) * (a.K / 2) + k / 2];
+        if (row >= 0) byte = prep_fix_codes(a.w[(e * a.rows_src + row) * (a.K / 2) + k / 2], sc[j & 1][kk], 0x88u);
         v |= byte << (8 * j);
       }
       words[kk] = prep_permute_word(v);
@@ -97,12 +110,10 @@ __global__ void prepare_fragment_kernel(PrepArgs a) {
         make_uint4(words[4], words[5], words[6], words[7]);
     if (t == 0) {  // scale region: the same row-major layout as the row-order blocks
       for (int h = 0; h < 2; ++h) {
-        const int64_t row = rows[h];
         const uint32_t r = 16 * w + g + 8 * h;
-        uint2 sv = make_uint2(0, 0);
-        if (row >= 0)
-          sv = *reinterpret_cast<const uint2*>(a.w_sf + (e * a.rows_src + row) * (a.K / 16) + c * 8);
-        *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = sv;
+        uint32_t codes[2] = {0, 0};
+        for (int kk = 0; kk < 8; ++kk) codes[kk >> 2] |= prep_scale_code(sc[h][kk]) << (8 * (kk & 3));
+        *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = make_uint2(codes[0], codes[1]);
       }
     }
   }
@@ -128,7 +139,7 @@ __global__ void debug_decode_fragment_kernel(PrepArgs a) {
       const uint32_t b0 = ((kk < 4 ? s0.x : s0.y) >> (8 * (kk & 3))) & 0xFFu;
       const uint32_t b1 = ((kk < 4 ? s1.x : s1.y) >> (8 * (kk & 3))) & 0xFFu;
       uint32_t o[4];
-      decode_word_frag(words[kk], scale_bf16x2(b0), scale_bf16x2(b1), o);
+      decode_word_frag(words[kk], scale_code_bf16x2(b0), scale_code_bf16x2(b1), o);
       for (int j = 0; j < 4; ++j) {
         const int64_t row = rows[j & 1];
         if (row < 0) continue;
@@ -163,7 +174,7 @@ __global__ void debug_decode_kernel(PrepArgs a) {
         const int word = 4 * q + k;                 // elements 8*word .. 8*word+7
         const uint32_t sb = (sbytes[word / 8] >> (8 * ((word / 2) % 4))) & 0xFFu;
         uint32_t o[4];
-        decode_word(w[k], scale_bf16x2(sb), o);
+        decode_word(w[k], scale_code_bf16x2(sb), o);
         for (int j = 0; j < 4; ++j) {
           const float lo = __uint_as_float(o[j] << 16) * 256.0f;
           const float hi = __uint_as_float(o[j] & 0xFFFF0000u) * 256.0f;

@@ -124,23 +124,35 @@ def test_prepared_weights_decode_exactly():
         assert np.array_equal(f64(out), want)
 
 
+def _every_code_every_scale(rows, K):
+    """Packed codes [1, rows, K/2] where every 16-element block holds all 16
+    E2M1 codes (rotated by the row), and scales [1, rows, K/16] cycling over
+    all 256 E4M3 bytes: negative, zero, subnormal and NaN scales included."""
+    k = np.arange(K)
+    codes = (k[None, :] + np.arange(rows)[:, None]) % 16
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sf = (np.arange(rows * (K // 16)) % 256).astype(np.uint8).reshape(rows, K // 16)
+    return packed[None], sf[None]
+
+
 @pytest.mark.parametrize("T", [16, 32])   # fragment order (decode-size kernel) and row order
-def test_prepared_weights_decode_all_codes_and_scales(T):
-    # every code byte against every finite non-negative E4M3 scale
+def test_prepared_weights_decode_every_code_under_every_scale(T):
     H, I, E = 256, 128, 1
-    codes = np.arange(256, dtype=np.uint8)
-    w1 = np.resize(codes, (E, 2 * I, H // 2)).astype(np.uint8)
-    sfv = np.resize(np.arange(0x7F, dtype=np.uint8), (E, 2 * I, H // 16)).astype(np.uint8)
-    w2 = np.resize(codes[::-1], (E, H, I // 2)).astype(np.uint8)
-    sf2 = np.resize(np.arange(0x7F, dtype=np.uint8)[::-1], (E, H, I // 16)).astype(np.uint8)
+    w1, sf1 = _every_code_every_scale(2 * I, H)
+    w2, sf2 = _every_code_every_scale(H, I)
+    sf2 = sf2[:, ::-1].copy()
     p = fm.problem(1, H, I, E, 1, route_tile=T)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    B = MoEBuffers(p).prepare(t(w1), t(sfv), t(w2), t(sf2))
-    for which, w, sf, prep in ((1, w1, sfv, B.w1p), (2, w2, sf2, B.w2p)):
+    B = MoEBuffers(p).prepare(t(w1), t(sf1), t(w2), t(sf2))
+    for which, w, sf, prep in ((1, w1, sf1, B.w1p), (2, w2, sf2, B.w2p)):
         out = torch.zeros(E, w.shape[1], w.shape[2] * 2, dtype=torch.bfloat16, device="cuda")
         fm.debug_decode_prepared(p, which, prep, out)
         torch.cuda.synchronize()
-        assert np.array_equal(f64(out), dequant_np(w, sf))
+        got, want = f64(out), dequant_np(w, sf)
+        assert np.isnan(want).sum() > 0 and (want == 0).sum() > 0
+        assert np.array_equal(got, want, equal_nan=True)
+        num = ~np.isnan(want)
+        assert np.array_equal(np.signbit(got[num]), np.signbit(want[num]))   # signed zeros too
 
 
 def test_fc1_quantiser_bit_exact_vs_oracle():
