@@ -116,7 +116,11 @@ __device__ __forceinline__ void decode_word_frag(uint32_t w, uint32_t sc0, uint3
 // Fragment layout (decode-size kernel): warp w of the 16 compute warps owns
 // block rows 16w..16w+15; lane l (g = l/4, t = l%4) owns rows R0 = 16w+g and
 // R1 = R0+8 and, for each 16-element K step kk, one prepared word holding
-// (R0,16kk+2t..+1), (R1,16kk+2t..+1), (R0,16kk+8+2t..+1), (R1,16kk+8+2t..+1).
+// (R0,16kk+4t..+1), (R1,16kk+4t..+1), (R0,16kk+4t+2..+3), (R1,16kk+4t+2..+3):
+// the m16n8k16 fragment's K positions 2t, 2t+1, 8+2t, 8+2t+1 stand for the
+// K elements 4t..4t+3 (a permutation of K inside the step that the
+// activation fragments follow too), so a lane's B fragment is 8 contiguous
+// bytes of one activation row.
 // A lane's 8 words are 32 contiguous bytes; its two 16-byte halves swap when
 // bit 2 of the lane is set (conflict-free 128-bit shared loads).
 __host__ __device__ constexpr uint32_t frag_half_offset(uint32_t w, uint32_t lane, uint32_t h) {

@@ -126,6 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       const int32_t e = a.tile_expert[tau];
+      // gathered tiles fetch only their valid rows, four at a time; the rows
+      // past them feed only output columns the epilogue discards
+      const int32_t nq = gather ? (min(max(a.tile_mn[tau] - tau * BN, 0), BN) + 3) >> 2 : 0;
       if (gather) {
         __syncwarp();
         for (int i = lane; i < BN; i += 32) {
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
+      const uint32_t btx = gather ? (uint32_t)nq * 2u * 512u : (uint32_t)C::kBBytes;
       const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kWBlockBytes;
       for (int c = 0; c < a.C; ++c) {
         if (lane == 0) {
@@ -141,15 +145,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) {
             uint8_t* sw = stages + stage * C::kStage;
             uint8_t* sb = sw + kWBlockBytes;
-            mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWBlockBytes + C::kBBytes));
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)kWBlockBytes + btx);
             tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &full[stage]);
 #pragma unroll
             for (int at = 0; at < 2; ++at) {
               const int32_t kc = c * kBK + at * 64;
               uint8_t* dst = sb + at * BN * 128;
               if (gather) {
-#pragma unroll
-                for (int g = 0; g < BN / 4; ++g)
+                for (int g = 0; g < nq; ++g)
                   tma_gather4(dst + g * 512, &bmap, kc, gidx[4 * g], gidx[4 * g + 1],
                               gidx[4 * g + 2], gidx[4 * g + 3], &full[stage]);
               } else {
@@ -368,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 
 constexpr int kGvWarps = 16;
+constexpr int kGvChains = 2;  // accumulator chains per n-block
 constexpr int kGvThreads = 32 * (kGvWarps + 1);
 
 struct GvCfg {
@@ -392,14 +396,15 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 
 // The K loop of one work item for NB n-blocks (1 or 2), a compile-time
 // count so that the eight unrolled K steps of a chunk form one basic block
-// the compiler can interleave.  acc[nb][j] are four independent accumulator
-// chains per n-block (K step kk feeds chain kk & 3).  Returns false on a
-// bounded-wait timeout.
+// the compiler can interleave.  acc[nb][j] are kGvChains independent
+// accumulator chains per n-block (K step kk feeds chain kk % kGvChains).
+// boff[q]: byte offset of this lane's 8-byte B fragment for K step q of a
+// 64-element activation atom.  Returns false on a bounded-wait timeout.
 template <int NB>
 __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, uint64_t* full,
-                                          uint64_t* empty, const uint32_t (&boff)[8], int w, int lane, uint32_t r0,
+                                          uint64_t* empty, const uint32_t (&boff)[4], int w, int lane, uint32_t r0,
                                           uint32_t r1, int& stage, uint32_t& phase,
-                                          float (&acc)[2][4][4]) {
+                                          float (&acc)[2][kGvChains][4]) {
   for (int c = 0; c < a.C; ++c) {
     if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) return false;
     const uint8_t* blk = stages + stage * GvCfg::kStage;
@@ -416,12 +421,10 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
       uint32_t af[4];
       decode_word_frag(words[kk], scale_code_bf16x2(ca), scale_code_bf16x2(cb), af);
       const uint8_t* atom = bt + (kk >> 2) * GvCfg::BN * 128;  // K 0..63 or 64..127
-      const int q0 = 2 * (kk & 3);                             // chunks q0, q0+1: k and k+8
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(atom + nb * 1024 + boff[q0]);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(atom + nb * 1024 + boff[q0 + 1]);
-        mma_16816(acc[nb][kk & 3], af, b0, b1);
+        const uint2 bv = *reinterpret_cast<const uint2*>(atom + nb * 1024 + boff[kk & 3]);
+        mma_16816(acc[nb][kk % kGvChains], af, bv.x, bv.y);
       }
     }
     __syncwarp();
@@ -475,6 +478,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       const int32_t e = a.tile_expert[tau];
+      // only the valid rows are gathered (see the tcgen05 producer)
+      const int32_t nq = gather ? (min(max(a.tile_mn[tau] - tau * BN, 0), BN) + 3) >> 2 : 0;
       if (gather) {
         __syncwarp();
         if (lane < BN) {
@@ -483,6 +488,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         }
         __syncwarp();
       }
+      const uint32_t btx = gather ? (uint32_t)nq * 2u * 512u : (uint32_t)C::kBBytes;
       const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kWBlockBytes;
       for (int c = 0; c < a.C; ++c) {
         if (lane == 0) {
@@ -490,15 +496,14 @@ __global__ void __launch_bounds__(kGvThreads, 1)
           if (ok) {
             uint8_t* sw = stages + stage * C::kStage;
             uint8_t* sb = sw + kWBlockBytes;
-            mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWBlockBytes + C::kBBytes));
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)kWBlockBytes + btx);
             tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &full[stage]);
 #pragma unroll
             for (int at = 0; at < 2; ++at) {
               const int32_t kc = c * kBK + at * 64;
               uint8_t* dst = sb + at * BN * 128;
               if (gather) {
-#pragma unroll
-                for (int q = 0; q < BN / 4; ++q)
+                for (int q = 0; q < nq; ++q)
                   tma_gather4(dst + q * 512, &bmap, kc, gidx[4 * q], gidx[4 * q + 1],
                               gidx[4 * q + 2], gidx[4 * q + 3], &full[stage]);
               } else {
@@ -524,13 +529,16 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     // ------------------------------------------------------------ compute warps
     const int w = warp, g = lane >> 2, t = lane & 3;
     const uint32_t r0 = (uint32_t)(16 * w + g), r1 = r0 + 8;
-    // byte offset of this lane's B-fragment word inside 16-byte chunk q of its
-    // token row g (row 8+g of the second n-block is 1024 bytes further): the
-    // activation tile is 128-byte swizzled, chunk q of row n at chunk q ^ (n & 7)
-    uint32_t boff[8];
+    // B fragment of K step q (0..3) of a 64-element atom: token row g, K
+    // elements 16q+4t..+3 (the fragment K order of decode.cuh), i.e. bytes
+    // 8(t&1).. of 16-byte chunk 2q+(t>>1); the activation tile is 128-byte
+    // swizzled (chunk j of row n at j ^ (n & 7)); row 8+g of the second
+    // n-block is 1024 bytes further with the same swizzle
+    uint32_t boff[4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      boff[q] = (uint32_t)g * 128u + (((uint32_t)q ^ (uint32_t)g) << 4) + 4u * (uint32_t)t;
+    for (int q = 0; q < 4; ++q)
+      boff[q] = (uint32_t)g * 128u + (((2u * q + ((uint32_t)t >> 1)) ^ (uint32_t)g) << 4) +
+                8u * ((uint32_t)t & 1u);
     int stage = 0;
     uint32_t phase = 0, xphase = 0;
     bool ok = true;
@@ -539,11 +547,11 @@ __global__ void __launch_bounds__(kGvThreads, 1)
       const int32_t mn = a.tile_mn[tau];
       const int64_t s0 = (int64_t)tau * BN;
       const bool two = mn - s0 > 8;  // second n-block needed (warp-uniform)
-      float acc[2][4][4];
+      float acc[2][kGvChains][4];
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-        for (int p = 0; p < 4; ++p)
+        for (int p = 0; p < kGvChains; ++p)
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[nb][p][i] = 0.0f;
       ok = two ? gv_k_loop<2>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc)
@@ -557,7 +565,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
       for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          d[nb][i] = ((acc[nb][0][i] + acc[nb][1][i]) + (acc[nb][2][i] + acc[nb][3][i])) * scale;
+          d[nb][i] = (acc[nb][0][i] + acc[nb][1][i]) * scale;
       if (EPI == kEpiPlainBf16) {
         float* y = static_cast<float*>(a.out);  // fp32 route storage
 #pragma unroll

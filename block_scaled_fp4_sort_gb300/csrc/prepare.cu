@@ -97,7 +97,7 @@ __global__ void prepare_fragment_kernel(PrepArgs a) {
       uint32_t v = 0;
       for (int j = 0; j < 4; ++j) {  // fragment register j: one byte = codes k, k+1
         const int64_t row = rows[j & 1];
-        const int64_t k = c * kBK + 16 * kk + 8 * (j >> 1) + 2 * t;
+        const int64_t k = c * kBK + 16 * kk + 4 * t + 2 * (j >> 1);
         uint32_t byte = 0;
         if (row >= 0) byte = prep_fix_codes(a.w[(e * a.rows_src + row) * (a.K / 2) + k / 2], sc[j & 1][kk], 0x88u);
         v |= byte << (8 * j);
@@ -143,7 +143,7 @@ __global__ void debug_decode_fragment_kernel(PrepArgs a) {
       for (int j = 0; j < 4; ++j) {
         const int64_t row = rows[j & 1];
         if (row < 0) continue;
-        const int64_t k = c * kBK + 16 * kk + 8 * (j >> 1) + 2 * t;
+        const int64_t k = c * kBK + 16 * kk + 4 * t + 2 * (j >> 1);
         const float lo = __uint_as_float(o[j] << 16) * 256.0f;
         const float hi = __uint_as_float(o[j] & 0xFFFF0000u) * 256.0f;
         *reinterpret_cast<__nv_bfloat162*>(a.dbg_out + (e * a.rows_src + row) * a.K + k) =
