@@ -337,7 +337,6 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   const bool w4 = s.mode == FP4MOE_W4A4;
   if (finalize_mode != FP4MOE_FINALIZE_DETERMINISTIC && finalize_mode != FP4MOE_FINALIZE_ATOMIC)
     return FP4MOE_ERR_INVALID_ARG;
-  if (finalize_mode == FP4MOE_FINALIZE_ATOMIC) return FP4MOE_ERR_UNSUPPORTED;
   if (!ok_ptr(w1_prepared) || !ok_ptr(w1_alpha) || !ok_ptr(w2_prepared) || !ok_ptr(w2_alpha) ||
       !ok_ptr(workspace))
     return FP4MOE_ERR_INVALID_ARG;
@@ -355,8 +354,14 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   int32_t* te = reinterpret_cast<int32_t*>(ws + L.tile_expert);
   int32_t* tm = reinterpret_cast<int32_t*>(ws + L.tile_mn);
   int32_t* nt = reinterpret_cast<int32_t*>(ws + L.num_tiles);
-  cudaError_t e = launch_route_sort(s, ids, e2p, p2e, te, tm, nt, nullptr, err, ws + L.route_scratch,
-                                    cs, true);
+  const bool atomic = finalize_mode == FP4MOE_FINALIZE_ATOMIC;
+  // atomic finalize: an fp32 token accumulator [M, H] in the y region (unused
+  // in that mode; S >= M * top_k >= M rows), seeded before GEMM2
+  float* acc = reinterpret_cast<float*>(ws + L.y);
+  cudaError_t e = atomic ? launch_seed_acc(s, out, accumulate ? 1 : 0, acc, cs, true) : cudaSuccess;
+  if (e == cudaSuccess)
+    e = launch_route_sort(s, ids, e2p, p2e, te, tm, nt, nullptr, err, ws + L.route_scratch, cs,
+                          true);
   const void* xb = x;
   if (e == cudaSuccess && w4) {
     e = launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.M, s.H, nullptr, s.T,
@@ -386,7 +391,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   }
   GemmLaunch g2 = {};
   g2.which = 2;
-  g2.epi = kEpiPlainBf16;
+  g2.epi = atomic ? kEpiAtomicFinal : kEpiPlainBf16;
   g2.wprep = static_cast<const uint8_t*>(w2_prepared);
   g2.alpha = w2_alpha;
   g2.tile_expert = te;
@@ -395,10 +400,14 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g2.act = hin;
   g2.act_rows = s.S;
   g2.out = ws + L.y;
+  g2.p2e = p2e;
+  g2.route_w = wts;
+  g2.rsf = rsf;
   g2.err = err;
   if (e == cudaSuccess) e = launch_gemm(s, g2, cs, true);
   if (e == cudaSuccess)
-    e = launch_finalize(s, ws + L.y, e2p, wts, rsf, accumulate ? 1 : 0, out, cs, true);
+    e = atomic ? launch_round_acc(s, acc, out, cs, true)
+               : launch_finalize(s, ws + L.y, e2p, wts, rsf, accumulate ? 1 : 0, out, cs, true);
   return cuda_status(e);
 }
 

@@ -55,6 +55,11 @@ cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, c
                            bool pdl);
 cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, const float* w,
                             float rsf, int accumulate, void* out, cudaStream_t st, bool pdl);
+// atomic finalize: fp32 accumulator [M, H] seeded from out (or +0), rounded into out
+cudaError_t launch_seed_acc(const Shape& s, const void* out, int accumulate, float* acc,
+                            cudaStream_t st, bool pdl);
+cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaStream_t st,
+                             bool pdl);
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
                                 const int32_t* row_limit_tiles, int64_t T, void* out,
                                 cudaStream_t st, bool pdl);

@@ -58,8 +58,22 @@ struct GemmArgs {
   void* out;
   uint8_t* out_sf;
   const float* fc2_scale;
+  const int32_t* p2e;          // atomic finalize: route of each slot
+  const float* route_w;        //   token_final_scales [M, top_k]
+  float rsf;                   //   routed_scaling_factor
   int* err;
 };
+
+// Atomic finalize (kEpiAtomicFinal): the GEMM2 value of slot s at output
+// column n goes straight into the fp32 token accumulator,
+//   acc[t, n] += (rsf * w[r]) * y,   r = p2e[s], t = r / top_k,
+// the same terms the deterministic finalize sums, in arrival order.
+__device__ __forceinline__ void atomic_final_add(const GemmArgs& a, int64_t s, int64_t n, float yv) {
+  const int32_t r = a.p2e[s];
+  if (r >= 0)
+    atomicAdd(static_cast<float*>(a.out) + (int64_t)(r / a.top_k) * a.out_ld + n,
+              (a.rsf * a.route_w[r]) * yv);
+}
 
 template <int BN>
 struct Cfg {
@@ -287,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t mn = a.tile_mn[tau];
       const float scale = a.alpha[e] * 256.0f;  // undo the decode's 2^-8
       const int64_t s0 = (int64_t)tau * BN;
-      if (EPI == kEpiPlainBf16) {
+      if (EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal) {
         const int64_t n = (int64_t)f * 256 + tile * 128 + row;
         float* y = static_cast<float*>(a.out);   // fp32 route storage
 #pragma unroll 1
@@ -299,7 +313,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int64_t s = s0 + cc + i;
-              if (s < mn) y[s * a.out_ld + n] = __uint_as_float(v[i]) * scale;
+              if (s >= mn) continue;
+              const float yv = __uint_as_float(v[i]) * scale;
+              if (EPI == kEpiPlainBf16)
+                y[s * a.out_ld + n] = yv;
+              else
+                atomic_final_add(a, s, n, yv);
             }
           }
         }
@@ -566,7 +585,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           d[nb][i] = (acc[nb][0][i] + acc[nb][1][i]) * scale;
-      if (EPI == kEpiPlainBf16) {
+      if (EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal) {
         float* y = static_cast<float*>(a.out);  // fp32 route storage
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb) {
@@ -574,7 +593,11 @@ __global__ void __launch_bounds__(kGvThreads, 1)
           for (int i = 0; i < 4; ++i) {
             const int64_t feat = (int64_t)f * 256 + (i < 2 ? r0 : r1);
             const int64_t s = s0 + 8 * nb + 2 * t + (i & 1);
-            if ((nb == 0 || two) && s < mn && feat < a.valid_rows) y[s * a.out_ld + feat] = d[nb][i];
+            if (!((nb == 0 || two) && s < mn && feat < a.valid_rows)) continue;
+            if (EPI == kEpiPlainBf16)
+              y[s * a.out_ld + feat] = d[nb][i];
+            else
+              atomic_final_add(a, s, feat, d[nb][i]);
           }
         }
       } else {
@@ -680,6 +703,9 @@ cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool 
   a.out = g.out;
   a.out_sf = g.out_sf;
   a.fc2_scale = g.fc2_scale;
+  a.p2e = g.p2e;
+  a.route_w = g.route_w;
+  a.rsf = g.rsf;
   a.err = g.err;
   const int64_t Kdim = g.which == 1 ? s.H : s.I;
   CUtensorMap map;
@@ -708,6 +734,7 @@ cudaError_t launch_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
     case kEpiSwigluBf16: return launch_t<BN, kEpiSwigluBf16>(s, g, st, pdl);
     case kEpiSwigluNvfp4: return launch_t<BN, kEpiSwigluNvfp4>(s, g, st, pdl);
     case kEpiPlainBf16: return launch_t<BN, kEpiPlainBf16>(s, g, st, pdl);
+    case kEpiAtomicFinal: return launch_t<BN, kEpiAtomicFinal>(s, g, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -727,6 +754,9 @@ cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
   a.out_ld = g.which == 1 ? s.I : s.H;
   a.valid_rows = (int32_t)(g.which == 1 ? 2 * s.I : s.H);
   a.out = g.out;
+  a.p2e = g.p2e;
+  a.route_w = g.route_w;
+  a.rsf = g.rsf;
   a.err = g.err;
   const int64_t Kdim = g.which == 1 ? s.H : s.I;
   CUtensorMap map;
@@ -757,6 +787,7 @@ cudaError_t launch_gemm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bo
     switch (g.epi) {
       case kEpiSwigluBf16: return launch_gv<kEpiSwigluBf16>(s, g, st, pdl);
       case kEpiPlainBf16: return launch_gv<kEpiPlainBf16>(s, g, st, pdl);
+      case kEpiAtomicFinal: return launch_gv<kEpiAtomicFinal>(s, g, st, pdl);
       default: return cudaErrorInvalidValue;
     }
   }

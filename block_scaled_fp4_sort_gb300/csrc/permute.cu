@@ -118,6 +118,38 @@ __global__ void finalize_rows(const float4* __restrict__ y, const int32_t* __res
   launch_dependents();
 }
 
+// Atomic finalize, before GEMM2: acc = float(out) (accumulate) or +0.
+// One thread per 8 elements.
+__global__ void seed_acc(const uint4* __restrict__ out, int accumulate, float4* __restrict__ acc,
+                         int64_t n8) {
+  grid_dependency_wait();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+    if (accumulate) {
+      bf16x8_to_f32(out[i], v);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+    }
+    acc[2 * i] = make_float4(v[0], v[1], v[2], v[3]);
+    acc[2 * i + 1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+  launch_dependents();
+}
+
+// Atomic finalize, after GEMM2: out = bf16(acc), round to nearest even.
+__global__ void round_acc(const float4* __restrict__ acc, uint4* __restrict__ out, int64_t n8) {
+  grid_dependency_wait();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    out[i] = f32_to_bf16x8(v);
+  }
+  launch_dependents();
+}
+
 __constant__ float kE2M1[16] = {0.0f,  0.5f,  1.0f,  1.5f,  2.0f,  3.0f,  4.0f,  6.0f,
                                 -0.0f, -0.5f, -1.0f, -1.5f, -2.0f, -3.0f, -4.0f, -6.0f};
 
@@ -190,6 +222,24 @@ cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, c
   return launch_pdl(finalize_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
                     static_cast<const float4*>(y), e2p, w, rsf, accumulate,
                     static_cast<uint4*>(out), s.M, s.H / 8, (int)s.K);
+}
+
+cudaError_t launch_seed_acc(const Shape& s, const void* out, int accumulate, float* acc,
+                            cudaStream_t st, bool pdl) {
+  const int64_t n8 = s.M * (s.H / 8);
+  if (n8 == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, (int64_t)num_sms() * 16);
+  return launch_pdl(seed_acc, dim3((unsigned)blocks), dim3(256), st, pdl,
+                    static_cast<const uint4*>(out), accumulate, reinterpret_cast<float4*>(acc), n8);
+}
+
+cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaStream_t st,
+                             bool pdl) {
+  const int64_t n8 = s.M * (s.H / 8);
+  if (n8 == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, (int64_t)num_sms() * 16);
+  return launch_pdl(round_acc, dim3((unsigned)blocks), dim3(256), st, pdl,
+                    reinterpret_cast<const float4*>(acc), static_cast<uint4*>(out), n8);
 }
 
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,

@@ -247,8 +247,12 @@ FP4MOE_API fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y,
  * straight from x), GEMM2, finalize.  Arguments as in the steps above; the
  * weights are prepared (fp4moe_prepare_weights).  finalize_mode:
  *   FP4MOE_FINALIZE_DETERMINISTIC: bit-reproducible (default);
- *   FP4MOE_FINALIZE_ATOMIC: GEMM2's epilogue adds into out (zeroed first when
- *     accumulate = 0); summation order varies run to run.
+ *   FP4MOE_FINALIZE_ATOMIC (cute_dsl_fused_moe use_fused_finalize): no y
+ *     round trip.  An fp32 token accumulator in the workspace is seeded with
+ *     float(out) (accumulate = 1) or +0, GEMM2's epilogue adds each
+ *     (rsf * w[t,j]) * y term into it with fp32 atomic adds, and a last pass
+ *     rounds it into out (RNE).  The terms are those of the deterministic
+ *     path; only their summation order varies from run to run.
  * workspace: fp4moe_workspace_size(p) bytes. */
 FP4MOE_API fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
                                 const int32_t* token_selected_experts,

@@ -183,7 +183,7 @@ def _setup(cfg, T=None):
     return inp, p, B, orc
 
 
-def _fused(inp, B, rsf=1.0, accumulate=False, out=None):
+def _fused(inp, B, rsf=1.0, accumulate=False, out=None, mode=fm.FINALIZE_DETERMINISTIC):
     cfg = inp.cfg
     ids = inp.token_selected_experts.cuda()
     w = inp.token_final_scales.cuda()
@@ -191,7 +191,7 @@ def _fused(inp, B, rsf=1.0, accumulate=False, out=None):
         out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device="cuda")
     x = inp.x if inp.x is not None else inp.x_q
     B.forward(x, inp.x_sf, ids, w, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale, rsf,
-              accumulate)
+              accumulate, finalize_mode=mode)
     torch.cuda.synchronize()
     assert fm.read_error(B.fused_ws) == 0
     return out
@@ -257,6 +257,61 @@ def test_accumulate_false_equals_zero_seed_bitwise():
     c = _fused(inp, B, rsf=0.75, accumulate=True, out=a.clone())
     _, exact, _ = orc.forward(rsf=0.75, accumulate=True, out_old=bits(a))
     check_out(f64(c), exact, 5e-3, what="accumulate")
+
+
+# ------------------------------------------------------------------ atomic finalize
+
+ATOMIC = fm.FINALIZE_ATOMIC
+
+
+@pytest.mark.parametrize("name,T", [("tiny_w4a16", 16), ("tiny_w4a16", 32), ("decode_w4a16", 16),
+                                    ("skewed_w4a16", 64)])
+def test_atomic_finalize_matches_oracle(name, T):
+    # warp-MMA kernel at T = 16, tcgen05 kernel otherwise; same bar as the
+    # deterministic path (the terms are the same, only their order varies)
+    cfg = synth.CONFIGS[name]
+    inp, p, B, orc = _setup(cfg, T)
+    out = _fused(inp, B, rsf=0.5, mode=ATOMIC)
+    _, exact, _ = orc.forward(rsf=0.5, nthreads=NTHREADS)
+    check_out(f64(out), exact, 5e-3, what="atomic %s T=%d" % (name, T))
+    det = _fused(inp, B, rsf=0.5)
+    d = f64(det)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(d), 1e-30))) - 7)
+    close = np.abs(f64(out) - d) <= ulp
+    print("atomic vs deterministic: %d of %d within one bf16 ulp" % (close.sum(), close.size))
+    assert close.mean() > 0.99
+
+
+@pytest.mark.parametrize("T", [16, 32])
+def test_atomic_finalize_accumulate(T):
+    cfg = synth.CONFIGS["tiny_w4a16"]
+    inp, p, B, orc = _setup(cfg, T)
+    garbage = torch.full((cfg.M, cfg.H), 3.0, dtype=torch.bfloat16, device="cuda")
+    a = _fused(inp, B, rsf=0.75, accumulate=False, out=garbage, mode=ATOMIC)
+    _, exact, _ = orc.forward(rsf=0.75)
+    check_out(f64(a), exact, 5e-3, what="atomic, accumulate=False over garbage")
+    c = _fused(inp, B, rsf=0.75, accumulate=True, out=a.clone(), mode=ATOMIC)
+    _, exact, _ = orc.forward(rsf=0.75, accumulate=True, out_old=bits(a))
+    check_out(f64(c), exact, 5e-3, what="atomic accumulate")
+
+
+def test_atomic_finalize_expert_parallel_halves():
+    cfg = synth.CONFIGS["tiny_w4a16"]
+    inp = synth.generate(cfg, device="cuda")
+    ids = inp.token_selected_experts.cuda()
+    w = inp.token_final_scales.cuda()
+    out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device="cuda")
+    half = cfg.E // 2
+    for i, off in enumerate((0, half)):
+        p = problem_for(cfg, 32, half, off)
+        sl = slice(off, off + half)
+        B = MoEBuffers(p).prepare(inp.w1[sl].contiguous(), inp.w1_sf[sl].contiguous(),
+                                  inp.w2[sl].contiguous(), inp.w2_sf[sl].contiguous())
+        B.forward(inp.x, None, ids, w, inp.w1_alpha[sl].contiguous(), inp.w2_alpha[sl].contiguous(),
+                  out, accumulate=(i == 1), finalize_mode=ATOMIC)
+    torch.cuda.synchronize()
+    _, exact, _ = oracle.OracleMoE.from_inputs(inp).forward()
+    check_out(f64(out), exact, 5e-3, what="atomic EP halves")
 
 
 def test_expert_parallel_halves_sum_to_full():
