@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_w4a16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--locality", action="store_true",
+                    help="print the GEMM1 gather-locality measurement instead of the bench line")
     return ap.parse_args()
 
 
@@ -46,6 +48,26 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def max_over_ranks(v, world, device=None):
+    """Max of a per-rank float over all ranks (the job's time is its slowest rank)."""
+    if world == 1:
+        return float(v)
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_cfg(cfg, rank):
+    """Rank r's replica draws its own batch and weights (seed + r): weak scaling."""
+    return cfg.with_(seed=cfg.seed + rank) if rank else cfg
+
+
+def tokens_per_s(world, tokens_per_rank, ms):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms * 1e-3)
 
 
 def workload_config(cfg, T):
@@ -158,7 +180,7 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     fbuild.build()
-    cfg = synth.CONFIGS[args.workload]
+    cfg = replica_cfg(synth.CONFIGS[args.workload], rank)
     T = synth.route_tile_for(cfg)
     inp = synth.generate(cfg, device=dev)
     p = problem_for(cfg, T)
@@ -187,15 +209,26 @@ def run_ours(args, rank, world, local):
             step()
         e1.record(stream)
         torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
         torch.distributed.barrier()
     err = fm.read_error(B.fused_ws)
     if err:
         raise RuntimeError("device error word %d" % err)
+
+    # ---------------- the same step with the atomic finalize (y never stored)
+    def step_atomic():
+        B.forward(x, inp.x_sf, ids, wts, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale,
+                  finalize_mode=fm.FINALIZE_ATOMIC, stream=stream)
+    for _ in range(max(args.warmup, 3)):
+        step_atomic()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_atomic()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_atomic = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     # ---------------- per-kernel breakdown through the staged entry points
     # (same kernels as the fused call, events around each launch)
@@ -265,13 +298,9 @@ def run_ours(args, rank, world, local):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hw) + ((hxsf,) if hxsf is not None else ()))
     d2h = hout.numel() * hout.element_size()
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
 
     # ---------------- roofline of the dominant kernel (GEMM1)
     peaks, peak_src = load_peaks()
@@ -292,7 +321,7 @@ def run_ours(args, rank, world, local):
             tj = json.load(f)
         if tj.get("workload") == cfg.name:
             traffic = tj.get("dram_bytes_per_launch")
-    tokens_s = world * cfg.M / (ms * 1e-3)
+    tokens_s = tokens_per_s(world, cfg.M, ms)
     line = {
         "metric": METRIC, "value": tokens_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
@@ -308,17 +337,133 @@ def run_ours(args, rank, world, local):
                      "algorithmic_bytes": g1_bytes, "peak_source": peak_src,
                      "touched_experts": touched},
         "kernels_ms": kernels,
-        "e2e": {"value": world * cfg.M / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "atomic_finalize": {"ms_per_step": ms_atomic, "value": tokens_per_s(world, cfg.M, ms_atomic),
+                            "unit": UNIT},
+        "e2e": {"value": tokens_per_s(world, cfg.M, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
-        "gpu_launches": args.steps * (4 if cfg.mode == "w4a16" else 6),
+        # per fused step: routing (1 kernel up to 4096 routes, else 3), x in slot
+        # order (all but the w4a16 route-tile-16 path), GEMM1, the w4a4 h -> BF16
+        # expansion, GEMM2, finalize
+        "gpu_launches": args.steps * ((1 if cfg.routes <= 4096 else 3) +
+                                      (0 if cfg.mode == "w4a16" and T == 16 else 1) + 3 +
+                                      (0 if cfg.mode == "w4a16" else 1)),
     }
     return line, inp, T
+
+
+def pages_per_tile(groups, top_k, row_bytes, page=2 << 20):
+    """Distinct `page`-byte pages of the activation matrix that each group of
+    route slots (one GEMM1 tile) gathers from; a row may straddle two pages."""
+    import numpy as np
+    out = []
+    for g in groups:
+        rows = g[g >= 0].astype(np.int64) // top_k
+        if rows.size == 0:
+            continue
+        lo = rows * row_bytes // page
+        hi = (rows * row_bytes + row_bytes - 1) // page
+        out.append(np.unique(np.concatenate([lo, hi])).size)
+    return np.array(out)
+
+
+def expert_groups(p2e, tile_expert, tile_mn, num_tiles, T, group):
+    """Each local expert's valid slots in slot order, cut into groups of `group` routes."""
+    import numpy as np
+    by_e = {}
+    for tau in range(num_tiles):
+        e = int(tile_expert[tau])
+        sl = p2e[tau * T:min(tau * T + T, int(tile_mn[tau]))]
+        by_e.setdefault(e, []).append(sl)
+    groups = []
+    for e, parts in by_e.items():
+        v = np.concatenate(parts)
+        groups += [v[i:i + group] for i in range(0, v.size, group)]
+    return groups
+
+
+def shuffled_within_experts(p2e, tile_expert, tile_mn, num_tiles, T, seed=0):
+    """Arrival-order model: each expert's routes in a seeded random order."""
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    out = p2e.copy()
+    start = {}
+    for tau in range(num_tiles):
+        start.setdefault(int(tile_expert[tau]), []).append(tau)
+    for e, taus in start.items():
+        idx = np.concatenate([np.arange(t * T, min(t * T + T, int(tile_mn[t]))) for t in taus])
+        out[idx] = rng.permutation(p2e[idx])
+    return out
+
+
+def run_locality(args):
+    """Gather locality of GEMM1 (the pages' M1/M2 table): 2 MiB pages of x per
+    tile under this build's stable routing order and under an arrival-order
+    model, plus GEMM1 time with either order at the large batch."""
+    import numpy as np
+    import torch
+
+    import block_scaled_fp4_sort_gb300 as fm
+    import synth
+    from block_scaled_fp4_sort_gb300 import build as fbuild
+    from block_scaled_fp4_sort_gb300.buffers import MoEBuffers, problem_for
+
+    fbuild.build()
+    base = synth.CONFIGS["large_w4a16"]
+    res = {"metric": "2 MiB pages of x per GEMM1 tile", "unit": "pages", "rows": []}
+    for M in (65536, 131072, 262144):
+        cfg = base.with_(M=M)
+        ids, _ = synth.generate_routing(cfg)
+        for EL, group in ((32, 256), (256, 128)):   # the pages' setting; this build's large config
+            p = problem_for(cfg, 128, EL, 0)
+            B = MoEBuffers(p)
+            B.route(torch.from_numpy(ids).cuda())
+            torch.cuda.synchronize()
+            nt = int(B.num_tiles[0])
+            p2e, te, tm = B.p2e.cpu().numpy(), B.tile_expert.cpu().numpy(), B.tile_mn.cpu().numpy()
+            row = {"M": M, "local_experts": EL, "tile_routes": group}
+            for name, order in (("stable", p2e),
+                                ("arrival_model", shuffled_within_experts(p2e, te, tm, nt, 128))):
+                pg = pages_per_tile(expert_groups(order, te, tm, nt, 128, group), cfg.top_k,
+                                    cfg.H * 2)
+                row[name] = {"mean": float(pg.mean()), "max": int(pg.max()), "tiles": int(pg.size)}
+            res["rows"].append(row)
+            del B
+    # GEMM1 with the stable against the shuffled permutation, M = 131072
+    cfg = base
+    inp = synth.generate(cfg, device="cuda")
+    p = problem_for(cfg, 128)
+    B = MoEBuffers(p).prepare(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+    B.route(inp.token_selected_experts.cuda())
+    torch.cuda.synchronize()
+    nt = int(B.num_tiles[0])
+    shuf = torch.from_numpy(shuffled_within_experts(B.p2e.cpu().numpy(), B.tile_expert.cpu().numpy(),
+                                                    B.tile_mn.cpu().numpy(), nt, 128)).cuda()
+    h = torch.zeros(B.S, cfg.I, dtype=torch.bfloat16, device="cuda")
+    times = {}
+    for name, rows in (("stable", B.p2e), ("arrival_model", shuf)):
+        def g1():
+            fm.moe_gemm1_swiglu(p, inp.x, None, rows, B.w1p, inp.w1_alpha, None, B.tile_expert,
+                                B.tile_mn, B.num_tiles, h, None, B.gemm1_ws)
+        for _ in range(3):
+            g1()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            g1()
+        e1.record()
+        torch.cuda.synchronize()
+        times[name] = e0.elapsed_time(e1) / args.steps
+    res["gemm1_ms_at_131072"] = times
+    print(json.dumps(res))
 
 
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.locality:
+        return run_locality(args)
     if world > 1:
         import torch
         backend = "nccl" if args.impl == "ours" else "gloo"

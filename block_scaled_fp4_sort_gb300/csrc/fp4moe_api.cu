@@ -82,18 +82,26 @@ RouteWs route_ws(const Shape& s) {
   return w;
 }
 
-size_t gemm_ws_bytes(const Shape& s, int which) {
+// staged GEMM workspace: header | BF16 activations in slot order (w4a4, or
+// gathered rows for the tcgen05 GEMM) | warp-MMA K-split scratch
+size_t gemm_split_offset(const Shape& s, int which) {
   size_t b = kWsHeader;
-  if (s.mode == FP4MOE_W4A4) {
+  if (s.mode == FP4MOE_W4A4 || (which == 1 && !fragment_layout(s))) {
     const int64_t rows = which == 1 ? std::max(s.M, s.S) : s.S;
     const int64_t K = which == 1 ? s.H : s.I;
     b += up((size_t)rows * K * 2);
   }
   return up(b);
 }
+size_t gemm_ws_bytes(const Shape& s, int which) {
+  return gemm_split_offset(s, which) + (fragment_layout(s) ? up(kSplitBytes) : 0);
+}
+void* gemm_split(const Shape& s, int which, uint8_t* ws) {
+  return fragment_layout(s) ? ws + gemm_split_offset(s, which) : nullptr;
+}
 
 struct FusedWs {
-  size_t e2p, p2e, tile_expert, tile_mn, num_tiles, route_scratch, h, h_sf, y, deq1, deq2, total;
+  size_t e2p, p2e, tile_expert, tile_mn, num_tiles, route_scratch, h, h_sf, y, deq2, split, total;
 };
 FusedWs fused_ws(const Shape& s) {
   FusedWs w = {};
@@ -109,10 +117,14 @@ FusedWs fused_ws(const Shape& s) {
   } else {
     w.h = o; o = up(o + (size_t)s.S * s.I / 2);
     w.h_sf = o; o = up(o + (size_t)s.S * s.I / 16);
-    w.deq1 = o; o = up(o + (size_t)s.M * s.H * 2);     // x in BF16 (exact)
     w.deq2 = o; o = up(o + (size_t)s.S * s.I * 2);     // h in BF16 (exact)
   }
-  w.y = o; o = up(o + (size_t)s.S * s.H * 4);  // fp32 route storage
+  // fp32 route storage; until GEMM2 it holds x in slot order (BF16, 2 S H
+  // bytes) for the tcgen05 GEMM1, in atomic mode the fp32 [M, H] accumulator
+  w.y = o; o = up(o + (size_t)s.S * s.H * 4);
+  if (fragment_layout(s)) {                     // K-split scratch, shared by GEMM1 and GEMM2
+    w.split = o; o = up(o + kSplitBytes);
+  }
   w.total = o;
   return w;
 }
@@ -251,14 +263,22 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   if (workspace_bytes < gemm_ws_bytes(s, 1)) return FP4MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // The tcgen05 GEMM reads plain row tiles: gathered rows are first written in
+  // slot order (its TMA four-row gather needs one instruction per four rows,
+  // which limited GEMM1 at large tiles); the decode-size kernel gathers itself.
+  const bool slot_order = gather_rows != nullptr && !fragment_layout(s);
   const void* act = a;
+  cudaError_t e = cudaSuccess;
   if (w4) {
+    e = launch_dequant_rows(static_cast<const uint8_t*>(a), a_sf, slot_order ? s.S : act_rows, s.H,
+                            gather_rows && !slot_order ? nullptr : num_tiles, s.T, ws + kWsHeader,
+                            cs, false, slot_order ? gather_rows : nullptr, s.K);
     act = ws + kWsHeader;
-    cudaError_t e = launch_dequant_rows(static_cast<const uint8_t*>(a), a_sf, act_rows, s.H,
-                                        gather_rows ? nullptr : num_tiles, s.T, ws + kWsHeader, cs,
-                                        false);
-    if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
+  } else if (slot_order) {
+    e = launch_permute(s, a, nullptr, gather_rows, num_tiles, ws + kWsHeader, nullptr, cs, false);
+    act = ws + kWsHeader;
   }
+  if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
   GemmLaunch g = {};
   g.which = 1;
   g.epi = w4 ? kEpiSwigluNvfp4 : kEpiSwigluBf16;
@@ -267,14 +287,15 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   g.tile_expert = tile_expert;
   g.tile_mn = tile_mn;
   g.num_tiles = num_tiles;
-  g.gather_rows = gather_rows;
+  g.gather_rows = slot_order ? nullptr : gather_rows;
   g.act = act;
-  g.act_rows = act_rows;
+  g.act_rows = slot_order ? s.S : act_rows;
   g.out = h;
   g.out_sf = h_sf;
   g.fc2_scale = fc2_input_scale;
+  g.split = gemm_split(s, 1, ws);
   g.err = err_word(ws);
-  return cuda_status(launch_gemm(s, g, cs, w4));
+  return cuda_status(launch_gemm(s, g, cs, w4 || slot_order));
 }
 
 fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h_sf,
@@ -310,6 +331,7 @@ fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h
   g.act = act;
   g.act_rows = s.S;
   g.out = y;
+  g.split = gemm_split(s, 2, ws);
   g.err = err_word(ws);
   return cuda_status(launch_gemm(s, g, cs, w4));
 }
@@ -356,17 +378,20 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   int32_t* nt = reinterpret_cast<int32_t*>(ws + L.num_tiles);
   const bool atomic = finalize_mode == FP4MOE_FINALIZE_ATOMIC;
   // atomic finalize: an fp32 token accumulator [M, H] in the y region (unused
-  // in that mode; S >= M * top_k >= M rows), seeded before GEMM2
+  // in that mode; S >= M * top_k >= M rows), seeded after GEMM1
   float* acc = reinterpret_cast<float*>(ws + L.y);
-  cudaError_t e = atomic ? launch_seed_acc(s, out, accumulate ? 1 : 0, acc, cs, true) : cudaSuccess;
-  if (e == cudaSuccess)
-    e = launch_route_sort(s, ids, e2p, p2e, te, tm, nt, nullptr, err, ws + L.route_scratch, cs,
-                          true);
+  cudaError_t e = launch_route_sort(s, ids, e2p, p2e, te, tm, nt, nullptr, err,
+                                    ws + L.route_scratch, cs, true);
+  // x in slot order for the tcgen05 GEMM1 (w4a4: expanded to BF16 on the way),
+  // in the y region, which GEMM2 overwrites only after GEMM1 has read it; the
+  // decode-size kernel gathers its few rows itself
+  const bool slot_order = !fragment_layout(s);
   const void* xb = x;
-  if (e == cudaSuccess && w4) {
-    e = launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.M, s.H, nullptr, s.T,
-                            ws + L.deq1, cs, true);
-    xb = ws + L.deq1;
+  if (e == cudaSuccess && slot_order) {
+    e = w4 ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
+                                 ws + L.y, cs, true, p2e, s.K)
+           : launch_permute(s, x, nullptr, p2e, nt, ws + L.y, nullptr, cs, true);
+    xb = ws + L.y;
   }
   GemmLaunch g1 = {};
   g1.which = 1;
@@ -376,12 +401,13 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g1.tile_expert = te;
   g1.tile_mn = tm;
   g1.num_tiles = nt;
-  g1.gather_rows = p2e;      // rows gathered by TMA straight from x
+  g1.gather_rows = slot_order ? nullptr : p2e;   // else rows gathered by TMA straight from x
   g1.act = xb;
-  g1.act_rows = s.M;
+  g1.act_rows = slot_order ? s.S : s.M;
   g1.out = ws + L.h;
   g1.out_sf = w4 ? ws + L.h_sf : nullptr;
   g1.fc2_scale = fc2_input_scale;
+  g1.split = fragment_layout(s) ? ws + L.split : nullptr;
   g1.err = err;
   if (e == cudaSuccess) e = launch_gemm(s, g1, cs, true);
   const void* hin = ws + L.h;
@@ -389,6 +415,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
     e = launch_dequant_rows(ws + L.h, ws + L.h_sf, s.S, s.I, nt, s.T, ws + L.deq2, cs, true);
     hin = ws + L.deq2;
   }
+  if (e == cudaSuccess && atomic) e = launch_seed_acc(s, out, accumulate ? 1 : 0, acc, cs, true);
   GemmLaunch g2 = {};
   g2.which = 2;
   g2.epi = atomic ? kEpiAtomicFinal : kEpiPlainBf16;
@@ -403,6 +430,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g2.p2e = p2e;
   g2.route_w = wts;
   g2.rsf = rsf;
+  g2.split = fragment_layout(s) ? ws + L.split : nullptr;
   g2.err = err;
   if (e == cudaSuccess) e = launch_gemm(s, g2, cs, true);
   if (e == cudaSuccess)

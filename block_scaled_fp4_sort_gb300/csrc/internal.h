@@ -21,6 +21,11 @@ constexpr int kWBlockBytes = kWDataBytes + kWScaleBytes;
 
 // error word lives at offset 0 of every workspace; the header is 256 bytes
 constexpr size_t kWsHeader = 256;
+// K-split tail of the warp-MMA GEMM: a counter per tail item, then one
+// 16 KB block of fp32 partial sums per unit (at most one unit per CTA)
+constexpr int64_t kSplitMaxUnits = 256;
+constexpr size_t kSplitCountBytes = kSplitMaxUnits * 4;
+constexpr size_t kSplitBytes = kSplitCountBytes + kSplitMaxUnits * 16 * 32 * 8 * 4;
 
 struct Shape {
   int64_t M, H, I, E, K, EL, off, T, mode;
@@ -62,7 +67,8 @@ cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaSt
                              bool pdl);
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
                                 const int32_t* row_limit_tiles, int64_t T, void* out,
-                                cudaStream_t st, bool pdl);
+                                cudaStream_t st, bool pdl, const int32_t* gather = nullptr,
+                                int64_t top_k = 1);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl);
 cudaError_t launch_debug_quantize(const float* in, int64_t n, const float* scale, uint8_t* q,
                                   uint8_t* sf, cudaStream_t st);
@@ -90,6 +96,7 @@ struct GemmLaunch {
   void* out;                   // h bf16 [S, I] | hq [S, I/2] | y bf16 [S, H] | out bf16 [M, H]
   uint8_t* out_sf;             // hsf [S, I/16]
   const float* fc2_scale;      // [1]
+  void* split;                 // warp-MMA K-split tail scratch (kSplitBytes, zero-filled once) or null
   // atomic finalize epilogue
   const int32_t* p2e;
   const float* route_w;

@@ -58,6 +58,8 @@ struct GemmArgs {
   void* out;
   uint8_t* out_sf;
   const float* fc2_scale;
+  float* part;                 // K-split tail (warp-MMA kernel): partial sums, or null
+  int32_t* split_cnt;          //   per tail item: pieces done (zero between launches)
   const int32_t* p2e;          // atomic finalize: route of each slot
   const float* route_w;        //   token_final_scales [M, top_k]
   float rsf;                   //   routed_scaling_factor
@@ -418,13 +420,14 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 // the compiler can interleave.  acc[nb][j] are kGvChains independent
 // accumulator chains per n-block (K step kk feeds chain kk % kGvChains).
 // boff[q]: byte offset of this lane's 8-byte B fragment for K step q of a
-// 64-element activation atom.  Returns false on a bounded-wait timeout.
+// 64-element activation atom.  Runs nchunks consecutive chunks of the
+// stage ring.  Returns false on a bounded-wait timeout.
 template <int NB>
 __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, uint64_t* full,
                                           uint64_t* empty, const uint32_t (&boff)[4], int w, int lane, uint32_t r0,
                                           uint32_t r1, int& stage, uint32_t& phase,
-                                          float (&acc)[2][kGvChains][4]) {
-  for (int c = 0; c < a.C; ++c) {
+                                          float (&acc)[2][kGvChains][4], int nchunks) {
+  for (int c = 0; c < nchunks; ++c) {
     if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) return false;
     const uint8_t* blk = stages + stage * GvCfg::kStage;
     const uint4 h0 = *reinterpret_cast<const uint4*>(blk + frag_half_offset(w, lane, 0));
@@ -456,6 +459,106 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
   return true;
 }
 
+// Work schedule of one CTA (identical in the producer and the compute warps).
+// Items (tile, 256-row block) go round-robin over the G CTAs.  When the last
+// round is partial, its `tail` items are instead cut along K into KS pieces
+// each (tail * KS <= G units, one per CTA): every piece stores its fp32
+// partial sums, and the CTA that completes an item's last piece (a counter
+// per item) adds the KS partials in piece order -- deterministic, the sum
+// does not depend on which CTA finishes last -- and runs the epilogue.
+struct GvSchedule {
+  int64_t n_items, main_end, tail;
+  int32_t KS;
+  __device__ GvSchedule(const GemmArgs& a) {
+    const int64_t G = gridDim.x;
+    n_items = (int64_t)a.num_tiles[0] * a.F;
+    const int64_t rounds = n_items / G;
+    tail = n_items - rounds * G;
+    KS = 1;
+    if (tail > 0 && a.part != nullptr) {
+      const int64_t ks = G / tail;  // >= 1
+      KS = (int32_t)(ks < a.C ? ks : a.C);
+    }
+    main_end = KS > 1 ? rounds * G : n_items;
+    if (KS == 1) tail = 0;
+  }
+  // this CTA's K-split unit: item, chunk range [c0, c1); false if none
+  __device__ bool unit(const GemmArgs& a, int64_t& item, int32_t& c0, int32_t& c1) const {
+    const int64_t u = blockIdx.x;
+    if (KS == 1 || u >= tail * KS) return false;
+    item = main_end + u / KS;
+    const int32_t ks = (int32_t)(u % KS);
+    c0 = (int32_t)((int64_t)ks * a.C / KS);
+    c1 = (int32_t)((int64_t)(ks + 1) * a.C / KS);
+    return true;
+  }
+};
+
+// The epilogue of one item from its scaled sums d[nb][i] at (row i<2 ? r0 : r1,
+// column 8nb + 2t + (i&1)).  Returns false on a bounded-wait timeout.
+template <int EPI>
+__device__ __forceinline__ bool gv_epilogue(const GemmArgs& a, int32_t tau, int32_t f, int w,
+                                            int lane, uint32_t r0, uint32_t r1,
+                                            const float (&d)[2][4], float* xchg, uint64_t* xready,
+                                            uint64_t* xfree, uint32_t& xphase) {
+  constexpr int BN = GvCfg::BN;
+  const int t = lane & 3;
+  const int32_t mn = a.tile_mn[tau];
+  const int64_t s0 = (int64_t)tau * BN;
+  const bool two = mn - s0 > 8;
+  if (EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal) {
+    float* y = static_cast<float*>(a.out);  // fp32 route storage
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t feat = (int64_t)f * 256 + (i < 2 ? r0 : r1);
+        const int64_t s = s0 + 8 * nb + 2 * t + (i & 1);
+        if (!((nb == 0 || two) && s < mn && feat < a.valid_rows)) continue;
+        if (EPI == kEpiPlainBf16)
+          y[s * a.out_ld + feat] = d[nb][i];
+        else
+          atomic_final_add(a, s, feat, d[nb][i]);
+      }
+    }
+    return true;
+  }
+  // up rows (warps 8-15) hand their values to the gate rows (warps 0-7)
+  if (w >= kGvWarps / 2) {
+    if (!__all_sync(0xffffffffu, mbar_wait(xfree, xphase ^ 1u, a.err))) return false;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        xchg[((i < 2 ? r0 : r1) - 128) * BN + 8 * nb + 2 * t + (i & 1)] = d[nb][i];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(xready);
+  } else {
+    if (!__all_sync(0xffffffffu, mbar_wait(xready, xphase, a.err))) return false;
+    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t row = i < 2 ? r0 : r1;
+        const int n = 8 * nb + 2 * t + (i & 1);
+        const int64_t s = s0 + n;
+        const float u = xchg[row * BN + n];
+        const float hv = s < mn ? swiglu(d[nb][i], u) : 0.0f;
+        h[s * a.out_ld + (int64_t)f * 128 + row] = __float2bfloat16_rn(hv);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(xfree);
+  }
+  xphase ^= 1u;
+  return true;
+}
+
+__device__ __forceinline__ void compute_bar_sync() {  // the 16 compute warps only
+  asm volatile("bar.sync 1, %0;" ::"n"(kGvWarps * 32) : "memory");
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kGvThreads, 1)
     moe_gemv_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap) {
@@ -469,6 +572,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
   uint64_t* empty = full + C::kStages;
   uint64_t* xready = empty + C::kStages;
   uint64_t* xfree = xready + 1;
+  int32_t* last_flag = reinterpret_cast<int32_t*>(xfree + 1);
   int32_t* gidx = reinterpret_cast<int32_t*>(smem + C::kStages * C::kStage + C::kBarBytes);
   float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kBarBytes + 4 * 128);
 
@@ -486,15 +590,15 @@ __global__ void __launch_bounds__(kGvThreads, 1)
   __syncthreads();
 
   grid_dependency_wait();
-  const int64_t n_items = (int64_t)a.num_tiles[0] * a.F;
+  const GvSchedule sch(a);
   const bool gather = a.gather_rows != nullptr;
 
   if (warp == kGvWarps) {
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
-    bool ok = true;
-    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    // stream chunks [c0, c1) of one item through the stage ring
+    auto produce = [&](int64_t item, int32_t c0, int32_t c1) -> bool {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       const int32_t e = a.tile_expert[tau];
       // only the valid rows are gathered (see the tcgen05 producer)
@@ -509,7 +613,8 @@ __global__ void __launch_bounds__(kGvThreads, 1)
       }
       const uint32_t btx = gather ? (uint32_t)nq * 2u * 512u : (uint32_t)C::kBBytes;
       const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kWBlockBytes;
-      for (int c = 0; c < a.C; ++c) {
+      for (int c = c0; c < c1; ++c) {
+        bool ok = true;
         if (lane == 0) {
           ok = mbar_wait(&empty[stage], phase ^ 1u, a.err);
           if (ok) {
@@ -533,14 +638,20 @@ __global__ void __launch_bounds__(kGvThreads, 1)
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+        if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return false;
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
-    }
+      return true;
+    };
+    bool ok = true;
+    for (int64_t item = blockIdx.x; item < sch.main_end && ok; item += gridDim.x)
+      ok = produce(item, 0, a.C);
+    int64_t item;
+    int32_t c0, c1;
+    if (ok && sch.unit(a, item, c0, c1)) produce(item, c0, c1);
     if (lane == 0)
       for (int q = 0; q < C::kStages; ++q)
         if (issued_mask & (1u << q)) mbar_wait(&full[q], (issued_parity >> q) & 1u, a.err);
@@ -560,12 +671,10 @@ __global__ void __launch_bounds__(kGvThreads, 1)
                 8u * ((uint32_t)t & 1u);
     int stage = 0;
     uint32_t phase = 0, xphase = 0;
-    bool ok = true;
-    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      const int32_t mn = a.tile_mn[tau];
-      const int64_t s0 = (int64_t)tau * BN;
-      const bool two = mn - s0 > 8;  // second n-block needed (warp-uniform)
+    // unscaled sums of chunks [c0, c1) of one item: raw[nb][i]
+    auto k_range = [&](int64_t item, int32_t c0, int32_t c1, float (&raw)[2][4]) -> bool {
+      const int32_t tau = (int32_t)(item / a.F);
+      const bool two = a.tile_mn[tau] - (int64_t)tau * BN > 8;  // second n-block (warp-uniform)
       float acc[2][kGvChains][4];
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
@@ -573,69 +682,63 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         for (int p = 0; p < kGvChains; ++p)
 #pragma unroll
           for (int i = 0; i < 4; ++i) acc[nb][p][i] = 0.0f;
-      ok = two ? gv_k_loop<2>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc)
-               : gv_k_loop<1>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc);
-      if (!ok) break;
-      // ---------------- epilogue: d[nb][i] at (row i<2 ? r0 : r1, column 8nb + 2t + (i&1))
-      const int32_t e = a.tile_expert[tau];
-      const float scale = a.alpha[e] * 256.0f;  // undo the decode's 2^-8
+      const bool ok =
+          two ? gv_k_loop<2>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc, c1 - c0)
+              : gv_k_loop<1>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc, c1 - c0);
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) raw[nb][i] = acc[nb][0][i] + acc[nb][1][i];
+      return ok;
+    };
+    auto finish = [&](int64_t item, const float (&raw)[2][4]) -> bool {
+      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
+      const float scale = a.alpha[a.tile_expert[tau]] * 256.0f;  // undo the decode's 2^-8
       float d[2][4];
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          d[nb][i] = (acc[nb][0][i] + acc[nb][1][i]) * scale;
-      if (EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal) {
-        float* y = static_cast<float*>(a.out);  // fp32 route storage
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int64_t feat = (int64_t)f * 256 + (i < 2 ? r0 : r1);
-            const int64_t s = s0 + 8 * nb + 2 * t + (i & 1);
-            if (!((nb == 0 || two) && s < mn && feat < a.valid_rows)) continue;
-            if (EPI == kEpiPlainBf16)
-              y[s * a.out_ld + feat] = d[nb][i];
-            else
-              atomic_final_add(a, s, feat, d[nb][i]);
-          }
+        for (int i = 0; i < 4; ++i) d[nb][i] = raw[nb][i] * scale;
+      return gv_epilogue<EPI>(a, tau, f, w, lane, r0, r1, d, xchg, xready, xfree, xphase);
+    };
+    bool ok = true;
+    for (int64_t item = blockIdx.x; item < sch.main_end && ok; item += gridDim.x) {
+      float raw[2][4];
+      ok = k_range(item, 0, a.C, raw) && finish(item, raw);
+    }
+    int64_t item;
+    int32_t c0, c1;
+    // entered by all 16 compute warps alike (the named barriers below need
+    // every one of them); a warp whose earlier wait expired skips the work
+    if (sch.unit(a, item, c0, c1)) {
+      float raw[2][4] = {};
+      if (ok) ok = k_range(item, c0, c1, raw);
+      // this piece's partial sums: unit u, warp w, lane -> 8 floats
+      const int64_t u = blockIdx.x;
+      float4* mine = reinterpret_cast<float4*>(a.part + ((u * kGvWarps + w) * 32 + lane) * 8);
+      mine[0] = make_float4(raw[0][0], raw[0][1], raw[0][2], raw[0][3]);
+      mine[1] = make_float4(raw[1][0], raw[1][1], raw[1][2], raw[1][3]);
+      __threadfence();
+      compute_bar_sync();
+      if (threadIdx.x == 0) {
+        int32_t* cnt = a.split_cnt + (item - sch.main_end);
+        const int32_t old = atomicAdd(cnt, 1);
+        *last_flag = old == sch.KS - 1;
+        if (old == sch.KS - 1) *cnt = 0;  // ready for the next launch
+      }
+      compute_bar_sync();
+      if (*last_flag && ok) {
+        __threadfence();
+        const int64_t u0 = (item - sch.main_end) * sch.KS;
+        float sum[2][4] = {};
+        for (int ks = 0; ks < sch.KS; ++ks) {  // fixed piece order
+          const float4* pp =
+              reinterpret_cast<const float4*>(a.part + (((u0 + ks) * kGvWarps + w) * 32 + lane) * 8);
+          const float4 p0 = __ldcg(pp), p1 = __ldcg(pp + 1);
+          sum[0][0] += p0.x; sum[0][1] += p0.y; sum[0][2] += p0.z; sum[0][3] += p0.w;
+          sum[1][0] += p1.x; sum[1][1] += p1.y; sum[1][2] += p1.z; sum[1][3] += p1.w;
         }
-      } else {
-        // up rows (warps 8-15) hand their values to the gate rows (warps 0-7)
-        if (w >= kGvWarps / 2) {
-          if (!__all_sync(0xffffffffu, mbar_wait(xfree, xphase ^ 1u, a.err))) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              xchg[((i < 2 ? r0 : r1) - 128) * BN + 8 * nb + 2 * t + (i & 1)] = d[nb][i];
-          __syncwarp();
-          if (lane == 0) mbar_arrive(xready);
-        } else {
-          if (!__all_sync(0xffffffffu, mbar_wait(xready, xphase, a.err))) {
-            ok = false;
-            break;
-          }
-          __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t row = i < 2 ? r0 : r1;
-              const int n = 8 * nb + 2 * t + (i & 1);
-              const int64_t s = s0 + n;
-              const float u = xchg[row * BN + n];
-              const float hv = s < mn ? swiglu(d[nb][i], u) : 0.0f;
-              h[s * a.out_ld + (int64_t)f * 128 + row] = __float2bfloat16_rn(hv);
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(xfree);
-        }
-        xphase ^= 1u;
+        ok = finish(item, sum);
       }
     }
   }
@@ -758,6 +861,11 @@ cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
   a.route_w = g.route_w;
   a.rsf = g.rsf;
   a.err = g.err;
+  const int64_t grid = std::min<int64_t>(sm_count(), std::max<int64_t>(1, s.tiles * a.F));
+  if (g.split != nullptr && grid <= kSplitMaxUnits) {
+    a.split_cnt = static_cast<int32_t*>(g.split);
+    a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(g.split) + kSplitCountBytes);
+  }
   const int64_t Kdim = g.which == 1 ? s.H : s.I;
   CUtensorMap map;
   if (!make_act_map(&map, g.act, g.act_rows, Kdim, g.gather_rows ? 1 : GvCfg::BN))
@@ -766,9 +874,8 @@ cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GvCfg::kSmem);
   if (e != cudaSuccess) return e;
-  const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)std::min<int64_t>(sm_count(), max_items));
+  cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kGvThreads);
   cfg.dynamicSmemBytes = GvCfg::kSmem;
   cfg.stream = st;

@@ -154,10 +154,12 @@ __constant__ float kE2M1[16] = {0.0f,  0.5f,  1.0f,  1.5f,  2.0f,  3.0f,  4.0f, 
                                 -0.0f, -0.5f, -1.0f, -1.5f, -2.0f, -3.0f, -4.0f, -6.0f};
 
 // NVFP4 rows -> BF16 rows (exact: every E2M1*E4M3 product is a BF16 value).
-// One thread per 8 elements.
+// With `gather` (permuted_idx_to_expanded_idx), output row s is source row
+// gather[s] / top_k, or zeros for a padding slot.  One thread per 8 elements.
 __global__ void dequant_rows(const uint32_t* __restrict__ q, const uint8_t* __restrict__ sf,
                              int64_t rows, int64_t K, const int32_t* __restrict__ num_tiles,
-                             int64_t T, uint4* __restrict__ out) {
+                             int64_t T, const int32_t* __restrict__ gather, int64_t top_k,
+                             uint4* __restrict__ out) {
   grid_dependency_wait();
   const int64_t nrows = num_tiles ? min(rows, (int64_t)num_tiles[0] * T) : rows;
   const int64_t per_row = K / 8;
@@ -165,11 +167,21 @@ __global__ void dequant_rows(const uint32_t* __restrict__ q, const uint8_t* __re
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i / per_row, c = i % per_row;
-    const uint32_t codes = q[r * (K / 8) + c];
-    const float s = e4m3_to_float(sf[r * (K / 16) + c / 2]);
+    int64_t src = r;
+    if (gather) {
+      const int32_t g = gather[r];
+      src = g >= 0 ? g / top_k : -1;
+    }
     float f[8];
+    if (src >= 0) {
+      const uint32_t codes = q[src * (K / 8) + c];
+      const float s = e4m3_to_float(sf[src * (K / 16) + c / 2]);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) f[k] = kE2M1[(codes >> (4 * k)) & 15u] * s;
+      for (int k = 0; k < 8; ++k) f[k] = kE2M1[(codes >> (4 * k)) & 15u] * s;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f[k] = 0.0f;
+    }
     out[r * per_row + c] = f32_to_bf16x8(f);
   }
   launch_dependents();
@@ -244,13 +256,13 @@ cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaSt
 
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
                                 const int32_t* row_limit_tiles, int64_t T, void* out,
-                                cudaStream_t st, bool pdl) {
+                                cudaStream_t st, bool pdl, const int32_t* gather, int64_t top_k) {
   const int64_t n = rows * (K / 8);
   if (n == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 16);
   return launch_pdl(dequant_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
-                    reinterpret_cast<const uint32_t*>(q), sf, rows, K, row_limit_tiles, T,
-                    static_cast<uint4*>(out));
+                    reinterpret_cast<const uint32_t*>(q), sf, rows, K, row_limit_tiles, T, gather,
+                    top_k, static_cast<uint4*>(out));
 }
 
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl) {

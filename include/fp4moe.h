@@ -25,11 +25,14 @@
  *     every compute call may be captured in a CUDA graph.  All work is
  *     enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
  *   - Host-side validation failures return a status and enqueue nothing.
+ *   - Workspaces are zero-filled by the caller once, before their first use;
+ *     the library leaves the counters it keeps there at zero after every
+ *     call, so a workspace is reusable without clearing.
  *   - Data-dependent errors found on the device (an expert id outside
  *     [0, num_experts), a bounded wait that expired) set an error word: the
- *     first int32 of the workspace.  It is sticky: zero it once before the
- *     first call (a zero-filled workspace, or fp4moe_clear_error) and read it
- *     with fp4moe_read_error() after synchronising.
+ *     first int32 of the workspace.  It is sticky: read it with
+ *     fp4moe_read_error() after synchronising, reset it with
+ *     fp4moe_clear_error().
  *   - Packed E2M1: element 2i of a row in the low nibble of byte i, 2i+1 in
  *     the high nibble.  Scales: E4M3 bytes, linear [rows, K/16].  Gate rows
  *     are w1[:, 0:I), up rows w1[:, I:2I).
@@ -189,7 +192,7 @@ FP4MOE_API fp4moe_status moe_route_sort_noalloc(const fp4moe_problem* p,
  * for s < num_non_exiting_tiles * T; padding rows are zero-filled.
  *   w4a16: x bf16 [M, H] -> permuted_x bf16 [S, H]; x_sf, permuted_x_sf NULL
  *   w4a4 : x uint8 [M, H/2] + x_sf e4m3 [M, H/16] -> [S, H/2] + [S, H/16]
- * fused_moe_forward does not call this: its GEMM1 gathers rows by TMA. */
+ * fused_moe_forward does its own gather (see there). */
 FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
                           const int32_t* permuted_idx_to_expanded_idx,
                           const int32_t* num_non_exiting_tiles, void* permuted_x,
@@ -203,7 +206,10 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
  *   a: activations.  If gather_rows != NULL it is x itself ([M, H] bf16, or
  *      [M, H/2] + a_sf [M, H/16] for w4a4) and row s is row
  *      gather_rows[s] / top_k (gather_rows = permuted_idx_to_expanded_idx);
- *      otherwise a is already permuted ([S, ...]).
+ *      otherwise a is already permuted ([S, ...]).  Gathered rows go through
+ *      the workspace in slot order when route_tile >= 32 (the tcgen05 GEMM
+ *      reads plain row tiles) and are fetched by TMA inside the decode-size
+ *      GEMM (route_tile 16); the result is the same bit for bit.
  *   w1_prepared: fp4moe_prepare_weights(p, 1, ...).  w1_alpha fp32 [E_local].
  *   w4a16: h bf16 [S, I] (R = round to BF16); h_sf, fc2_input_scale NULL.
  *   w4a4 : h uint8 [S, I/2] + h_sf e4m3 [S, I/16]: R = NVFP4 quantisation with
@@ -243,8 +249,10 @@ FP4MOE_API fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y,
                            const float* token_final_scales, float routed_scaling_factor,
                            int32_t accumulate, void* out, void* stream);
 
-/* The whole forward on `stream`: route sort, GEMM1 (+ SwiGLU, TMA row gather
- * straight from x), GEMM2, finalize.  Arguments as in the steps above; the
+/* The whole forward on `stream`: route sort, x gathered into slot order in the
+ * workspace (route_tile >= 32; w4a4 rows expanded to BF16 on the way) or by
+ * TMA inside GEMM1 (route_tile 16), GEMM1 (+ SwiGLU), GEMM2, finalize,
+ * chained with programmatic dependent launch.  Arguments as in the steps above; the
  * weights are prepared (fp4moe_prepare_weights).  finalize_mode:
  *   FP4MOE_FINALIZE_DETERMINISTIC: bit-reproducible (default);
  *   FP4MOE_FINALIZE_ATOMIC (cute_dsl_fused_moe use_fused_finalize): no y
