@@ -331,7 +331,10 @@ def run_ours(args, rank, world, local):
                        "per step vs 126 MB L2" % (step_bytes / 1e9), parallelism="replicas" if world > 1 else "1 GPU"),
         "tflops": world * cfg.flops() / (ms * 1e-3) / 1e12,
         "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
-        "roofline": {"kernel": "moe_gemm_kernel (GEMM1 + SwiGLU)", "bound": "hbm",
+        "roofline": {"kernel": ("moe_gemv_kernel<0> (GEMM1 + SwiGLU, warp MMA)"
+                               if cfg.mode == "w4a16" and T == 16 else
+                               "moe_gemm_kernel<%d, %d> (GEMM1 + SwiGLU, tcgen05)"
+                               % (T, 0 if cfg.mode == "w4a16" else 1)), "bound": "hbm",
                      "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "algorithmic_bytes": g1_bytes, "peak_source": peak_src,
