@@ -113,16 +113,23 @@ __device__ __forceinline__ void decode_word_frag(uint32_t w, uint32_t sc0, uint3
   o[3] = bf16x2_mul(r3, sc1);
 }
 
-// Fragment layout (decode-size kernel): warp w of the 16 compute warps owns
-// block rows 16w..16w+15; lane l (g = l/4, t = l%4) owns rows R0 = 16w+g and
+// Fragment layout (decode-size kernel): fragment slot w (0..15) holds block
+// rows 16w..16w+15; lane l (g = l/4, t = l%4) owns rows R0 = 16w+g and
 // R1 = R0+8 and, for each 16-element K step kk, one prepared word holding
-// (R0,16kk+4t..+1), (R1,16kk+4t..+1), (R0,16kk+4t+2..+3), (R1,16kk+4t+2..+3):
-// the m16n8k16 fragment's K positions 2t, 2t+1, 8+2t, 8+2t+1 stand for the
-// K elements 4t..4t+3 (a permutation of K inside the step that the
-// activation fragments follow too), so a lane's B fragment is 8 contiguous
-// bytes of one activation row.
+// (R0,e0..e1), (R1,e0..e1), (R0,e2..e3), (R1,e2..e3): the m16n8k16
+// fragment's K positions 2t, 2t+1, 8+2t, 9+2t stand for the four K elements
+//   e0..e3 = 64a + 16t + 4 (q ^ (t & 1)) + 0..3,   a = kk / 4, q = kk % 4
+// of the 128-element chunk (a permutation of K that the activation
+// fragments follow too).  Over the four steps of a 64-element atom lane t
+// thus covers exactly the 16-element scale block 4a + t of its two rows (one
+// scale multiplier per row per atom), its B fragment is 8 contiguous bytes
+// of one activation row, and the four lanes of a row fall in distinct
+// (swizzle coset, half chunk) pairs: conflict-free 8-byte shared loads.
 // A lane's 8 words are 32 contiguous bytes; its two 16-byte halves swap when
 // bit 2 of the lane is set (conflict-free 128-bit shared loads).
+__host__ __device__ constexpr uint32_t frag_k(uint32_t kk, uint32_t t) {
+  return 64u * (kk >> 2) + 16u * t + 4u * ((kk & 3u) ^ (t & 1u));
+}
 __host__ __device__ constexpr uint32_t frag_half_offset(uint32_t w, uint32_t lane, uint32_t h) {
   return (w * 32u + lane) * 32u + ((h ^ ((lane >> 2) & 1u)) * 16u);
 }

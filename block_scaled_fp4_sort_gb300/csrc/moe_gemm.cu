@@ -435,13 +435,17 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
     const uint2 sa = *reinterpret_cast<const uint2*>(blk + kWDataBytes + r0 * 8);
     const uint2 sb = *reinterpret_cast<const uint2*>(blk + kWDataBytes + r1 * 8);
     const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+    // one scale multiplier per row per atom: block 4a + t (fragment K order)
+    const uint32_t sel = 0x4440u + ((uint32_t)lane & 3u);
+    const uint32_t sc0[2] = {scale_code_bf16x2(__byte_perm(sa.x, 0u, sel)),
+                             scale_code_bf16x2(__byte_perm(sa.y, 0u, sel))};
+    const uint32_t sc1[2] = {scale_code_bf16x2(__byte_perm(sb.x, 0u, sel)),
+                             scale_code_bf16x2(__byte_perm(sb.y, 0u, sel))};
     const uint8_t* bt = blk + kWBlockBytes;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t ca = __byte_perm(kk < 4 ? sa.x : sa.y, 0u, 0x4440u + (kk & 3));
-      const uint32_t cb = __byte_perm(kk < 4 ? sb.x : sb.y, 0u, 0x4440u + (kk & 3));
       uint32_t af[4];
-      decode_word_frag(words[kk], scale_code_bf16x2(ca), scale_code_bf16x2(cb), af);
+      decode_word_frag(words[kk], sc0[kk >> 2], sc1[kk >> 2], af);
       const uint8_t* atom = bt + (kk >> 2) * GvCfg::BN * 128;  // K 0..63 or 64..127
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) {
@@ -660,15 +664,16 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     const int w = warp, g = lane >> 2, t = lane & 3;
     const uint32_t r0 = (uint32_t)(16 * w + g), r1 = r0 + 8;
     // B fragment of K step q (0..3) of a 64-element atom: token row g, K
-    // elements 16q+4t..+3 (the fragment K order of decode.cuh), i.e. bytes
-    // 8(t&1).. of 16-byte chunk 2q+(t>>1); the activation tile is 128-byte
+    // elements k = frag_k(q, t)..+3 (the fragment K order of decode.cuh), at
+    // byte 2 (k % 8) of 16-byte chunk k / 8; the activation tile is 128-byte
     // swizzled (chunk j of row n at j ^ (n & 7)); row 8+g of the second
     // n-block is 1024 bytes further with the same swizzle
     uint32_t boff[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      boff[q] = (uint32_t)g * 128u + (((2u * q + ((uint32_t)t >> 1)) ^ (uint32_t)g) << 4) +
-                8u * ((uint32_t)t & 1u);
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t k = frag_k((uint32_t)q, (uint32_t)t);
+      boff[q] = (uint32_t)g * 128u + (((k >> 3) ^ (uint32_t)g) << 4) + 2u * (k & 7u);
+    }
     int stage = 0;
     uint32_t phase = 0, xphase = 0;
     // unscaled sums of chunks [c0, c1) of one item: raw[nb][i]

@@ -97,9 +97,10 @@ __global__ void prepare_fragment_kernel(PrepArgs a) {
       uint32_t v = 0;
       for (int j = 0; j < 4; ++j) {  // fragment register j: one byte = codes k, k+1
         const int64_t row = rows[j & 1];
-        const int64_t k = c * kBK + 16 * kk + 4 * t + 2 * (j >> 1);
+        const int64_t k = c * kBK + frag_k((uint32_t)kk, t) + 2 * (j >> 1);
         uint32_t byte = 0;
-        if (row >= 0) byte = prep_fix_codes(a.w[(e * a.rows_src + row) * (a.K / 2) + k / 2], sc[j & 1][kk], 0x88u);
+        if (row >= 0)
+          byte = prep_fix_codes(a.w[(e * a.rows_src + row) * (a.K / 2) + k / 2], sc[j & 1][(k / 16) % 8], 0x88u);
         v |= byte << (8 * j);
       }
       words[kk] = prep_permute_word(v);
@@ -136,14 +137,15 @@ __global__ void debug_decode_fragment_kernel(PrepArgs a) {
     const uint2 s0 = *reinterpret_cast<const uint2*>(b + kWDataBytes + r0 * 8);
     const uint2 s1 = *reinterpret_cast<const uint2*>(b + kWDataBytes + r1 * 8);
     for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t b0 = ((kk < 4 ? s0.x : s0.y) >> (8 * (kk & 3))) & 0xFFu;
-      const uint32_t b1 = ((kk < 4 ? s1.x : s1.y) >> (8 * (kk & 3))) & 0xFFu;
+      // scale block 4 (kk / 4) + t of the chunk (fragment K order)
+      const uint32_t b0 = ((kk < 4 ? s0.x : s0.y) >> (8 * t)) & 0xFFu;
+      const uint32_t b1 = ((kk < 4 ? s1.x : s1.y) >> (8 * t)) & 0xFFu;
       uint32_t o[4];
       decode_word_frag(words[kk], scale_code_bf16x2(b0), scale_code_bf16x2(b1), o);
       for (int j = 0; j < 4; ++j) {
         const int64_t row = rows[j & 1];
         if (row < 0) continue;
-        const int64_t k = c * kBK + 16 * kk + 4 * t + 2 * (j >> 1);
+        const int64_t k = c * kBK + frag_k((uint32_t)kk, t) + 2 * (j >> 1);
         const float lo = __uint_as_float(o[j] << 16) * 256.0f;
         const float hi = __uint_as_float(o[j] & 0xFFFF0000u) * 256.0f;
         *reinterpret_cast<__nv_bfloat162*>(a.dbg_out + (e * a.rows_src + row) * a.K + k) =
