@@ -231,10 +231,16 @@ def run_ours(args, rank, world, local):
     ms_atomic = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     # ---------------- per-kernel breakdown through the staged entry points
-    # (same kernels as the fused call, events around each launch)
+    # (the fused call's kernels in its order: x into slot order, then GEMM1 on
+    # plain row tiles; events around each launch)
     kernels = {}
-    names = ["route_sort", "gemm1_swiglu", "gemm2", "finalize"]
+    names = ["route_sort", "permute", "gemm1_swiglu", "gemm2", "finalize"]
     ev = {n: [] for n in names}
+    if cfg.mode == "w4a16":
+        px, pxsf = torch.zeros(B.S, cfg.H, dtype=torch.bfloat16, device=dev), None
+    else:
+        px = torch.zeros(B.S, cfg.H // 2, dtype=torch.uint8, device=dev)
+        pxsf = torch.zeros(B.S, cfg.H // 16, dtype=torch.uint8, device=dev)
 
     if cfg.mode == "w4a16":
         h = torch.zeros(B.S, cfg.I, dtype=torch.bfloat16, device=dev)
@@ -248,8 +254,10 @@ def run_ours(args, rank, world, local):
         if name == "route_sort":
             fm.moe_route_sort(p, ids, B.e2p, B.p2e, B.tile_expert, B.tile_mn, B.num_tiles, None,
                               B.route_ws, stream)
+        elif name == "permute":
+            fm.moe_permute(p, x, inp.x_sf, B.p2e, B.num_tiles, px, pxsf, stream)
         elif name == "gemm1_swiglu":
-            fm.moe_gemm1_swiglu(p, x, inp.x_sf, B.p2e, B.w1p, inp.w1_alpha, inp.fc2_input_scale,
+            fm.moe_gemm1_swiglu(p, px, pxsf, None, B.w1p, inp.w1_alpha, inp.fc2_input_scale,
                                 B.tile_expert, B.tile_mn, B.num_tiles, h, hsf, B.gemm1_ws, stream)
         elif name == "gemm2":
             fm.moe_gemm2(p, h, hsf, B.w2p, inp.w2_alpha, B.tile_expert, B.tile_mn, B.num_tiles, y,
@@ -346,10 +354,8 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
         # per fused step: routing (1 kernel up to 4096 routes, else 3), x in slot
-        # order (all but the w4a16 route-tile-16 path), GEMM1, the w4a4 h -> BF16
-        # expansion, GEMM2, finalize
-        "gpu_launches": args.steps * ((1 if cfg.routes <= 4096 else 3) +
-                                      (0 if cfg.mode == "w4a16" and T == 16 else 1) + 3 +
+        # order, GEMM1, the w4a4 h -> BF16 expansion, GEMM2, finalize
+        "gpu_launches": args.steps * ((1 if cfg.routes <= 4096 else 3) + 1 + 3 +
                                       (0 if cfg.mode == "w4a16" else 1)),
     }
     return line, inp, T

@@ -36,12 +36,13 @@ class MoEBuffers:
         E_local = p.num_local_experts or p.num_experts
         d = self.device
         i32 = torch.int32
-        self.e2p = _empty(M * k, i32, d)
-        self.p2e = _empty(self.S, i32, d)
-        self.tile_expert = _empty(self.tiles, i32, d)
-        self.tile_mn = _empty(self.tiles, i32, d)
-        self.num_tiles = _empty(4, i32, d)
-        self.counts = _empty(E_local, i32, d)
+        # the plan starts empty (zero tiles) until route() writes it
+        self.e2p = _zeros(M * k, i32, d)
+        self.p2e = _zeros(self.S, i32, d)
+        self.tile_expert = _zeros(self.tiles, i32, d)
+        self.tile_mn = _zeros(self.tiles, i32, d)
+        self.num_tiles = _zeros(4, i32, d)
+        self.counts = _zeros(E_local, i32, d)
         self.route_ws = _zeros(route_workspace_size(p), torch.uint8, d)
         self.gemm1_ws = _zeros(gemm_workspace_size(p, 1), torch.uint8, d)
         self.gemm2_ws = _zeros(gemm_workspace_size(p, 2), torch.uint8, d)

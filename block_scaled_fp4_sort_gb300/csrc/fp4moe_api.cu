@@ -272,7 +272,7 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   if (w4) {
     e = launch_dequant_rows(static_cast<const uint8_t*>(a), a_sf, slot_order ? s.S : act_rows, s.H,
                             gather_rows && !slot_order ? nullptr : num_tiles, s.T, ws + kWsHeader,
-                            cs, false, slot_order ? gather_rows : nullptr, s.K);
+                            cs, false, slot_order ? gather_rows : nullptr, s.K, s.M);
     act = ws + kWsHeader;
   } else if (slot_order) {
     e = launch_permute(s, a, nullptr, gather_rows, num_tiles, ws + kWsHeader, nullptr, cs, false);
@@ -382,17 +382,15 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   float* acc = reinterpret_cast<float*>(ws + L.y);
   cudaError_t e = launch_route_sort(s, ids, e2p, p2e, te, tm, nt, nullptr, err,
                                     ws + L.route_scratch, cs, true);
-  // x in slot order for the tcgen05 GEMM1 (w4a4: expanded to BF16 on the way),
-  // in the y region, which GEMM2 overwrites only after GEMM1 has read it; the
-  // decode-size kernel gathers its few rows itself
-  const bool slot_order = !fragment_layout(s);
-  const void* xb = x;
-  if (e == cudaSuccess && slot_order) {
+  // x in slot order for GEMM1 (w4a4: expanded to BF16 on the way), in the y
+  // region, which GEMM2 overwrites only after GEMM1 has read it; padding rows
+  // are left unwritten (no result of a padding slot is stored).  Plain row
+  // tiles beat the TMA four-row gather in both GEMM kernels.
+  const void* xb = ws + L.y;
+  if (e == cudaSuccess)
     e = w4 ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
-                                 ws + L.y, cs, true, p2e, s.K)
-           : launch_permute(s, x, nullptr, p2e, nt, ws + L.y, nullptr, cs, true);
-    xb = ws + L.y;
-  }
+                                 ws + L.y, cs, true, p2e, s.K, s.M)
+           : launch_permute(s, x, nullptr, p2e, nt, ws + L.y, nullptr, cs, true, false);
   GemmLaunch g1 = {};
   g1.which = 1;
   g1.epi = w4 ? kEpiSwigluNvfp4 : kEpiSwigluBf16;
@@ -401,9 +399,9 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g1.tile_expert = te;
   g1.tile_mn = tm;
   g1.num_tiles = nt;
-  g1.gather_rows = slot_order ? nullptr : p2e;   // else rows gathered by TMA straight from x
+  g1.gather_rows = nullptr;
   g1.act = xb;
-  g1.act_rows = slot_order ? s.S : s.M;
+  g1.act_rows = s.S;
   g1.out = ws + L.h;
   g1.out_sf = w4 ? ws + L.h_sf : nullptr;
   g1.fc2_scale = fc2_input_scale;

@@ -57,7 +57,7 @@ cudaError_t launch_route_sort(const Shape& s, const int32_t* ids, int32_t* e2p, 
 // ---- elementwise steps (permute.cu) ----
 cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, const int32_t* p2e,
                            const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
-                           bool pdl);
+                           bool pdl, bool zero_pad = true);
 cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, const float* w,
                             float rsf, int accumulate, void* out, cudaStream_t st, bool pdl);
 // atomic finalize: fp32 accumulator [M, H] seeded from out (or +0), rounded into out
@@ -68,7 +68,7 @@ cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaSt
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
                                 const int32_t* row_limit_tiles, int64_t T, void* out,
                                 cudaStream_t st, bool pdl, const int32_t* gather = nullptr,
-                                int64_t top_k = 1);
+                                int64_t top_k = 1, int64_t src_rows = 0);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl);
 cudaError_t launch_debug_quantize(const float* in, int64_t n, const float* scale, uint8_t* q,
                                   uint8_t* sf, cudaStream_t st);

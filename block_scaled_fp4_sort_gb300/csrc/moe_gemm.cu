@@ -58,6 +58,9 @@ struct GemmArgs {
   void* out;
   uint8_t* out_sf;
   const float* fc2_scale;
+  int32_t max_tiles;           // S / T: bound on num_tiles[0]
+  int32_t EL;                  // local experts: bound on tile_idx_to_expert
+  int64_t R;                   // routes M * top_k: bound on slot entries
   float* part;                 // K-split tail (warp-MMA kernel): partial sums, or null
   int32_t* split_cnt;          //   per tail item: pieces done (zero between launches)
   const int32_t* p2e;          // atomic finalize: route of each slot
@@ -72,9 +75,28 @@ struct GemmArgs {
 // the same terms the deterministic finalize sums, in arrival order.
 __device__ __forceinline__ void atomic_final_add(const GemmArgs& a, int64_t s, int64_t n, float yv) {
   const int32_t r = a.p2e[s];
-  if (r >= 0)
+  if (r >= 0 && r < a.R)
     atomicAdd(static_cast<float*>(a.out) + (int64_t)(r / a.top_k) * a.out_ld + n,
               (a.rsf * a.route_w[r]) * yv);
+}
+
+// Work items from the routing plan: the tile count is clamped to S / T and an
+// expert id outside [0, E_local) sets the error word and reads expert 0, so a
+// malformed plan cannot send a load outside the buffers.
+__device__ __forceinline__ int64_t plan_items(const GemmArgs& a) {
+  const int32_t nt = a.num_tiles[0];
+  return (int64_t)(nt < 0 ? 0 : nt < a.max_tiles ? nt : a.max_tiles) * a.F;
+}
+__device__ __forceinline__ int32_t plan_expert(const GemmArgs& a, int32_t tau) {
+  const int32_t e = a.tile_expert[tau];
+  if (e >= 0 && e < a.EL) return e;
+  set_error(a.err, kErrDevice);
+  return 0;
+}
+// the same clamp without the report (the producer reports it for the tile)
+__device__ __forceinline__ int32_t plan_expert_quiet(const GemmArgs& a, int32_t tau) {
+  const int32_t e = a.tile_expert[tau];
+  return (uint32_t)e < (uint32_t)a.EL ? e : 0;
 }
 
 template <int BN>
@@ -131,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   grid_dependency_wait();
-  const int64_t n_items = (int64_t)a.num_tiles[0] * a.F;
+  const int64_t n_items = plan_items(a);
   const bool gather = a.gather_rows != nullptr;
 
   if (warp == kTmaWarp) {
@@ -141,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      const int32_t e = a.tile_expert[tau];
+      const int32_t e = plan_expert(a, tau);
       // gathered tiles fetch only their valid rows, four at a time; the rows
       // past them feed only output columns the epilogue discards
       const int32_t nq = gather ? (min(max(a.tile_mn[tau] - tau * BN, 0), BN) + 3) >> 2 : 0;
@@ -149,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         for (int i = lane; i < BN; i += 32) {
           const int32_t r = a.gather_rows[(int64_t)tau * BN + i];
-          gidx[i] = r >= 0 ? r / a.top_k : 0;
+          gidx[i] = r >= 0 && r < a.R ? r / a.top_k : 0;
         }
         __syncwarp();
       }
@@ -299,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       accphase ^= 1u;
       tc_fence_after();
-      const int32_t e = a.tile_expert[tau];
+      const int32_t e = plan_expert_quiet(a, tau);
       const int32_t mn = a.tile_mn[tau];
       const float scale = a.alpha[e] * 256.0f;  // undo the decode's 2^-8
       const int64_t s0 = (int64_t)tau * BN;
@@ -475,7 +497,7 @@ struct GvSchedule {
   int32_t KS;
   __device__ GvSchedule(const GemmArgs& a) {
     const int64_t G = gridDim.x;
-    n_items = (int64_t)a.num_tiles[0] * a.F;
+    n_items = plan_items(a);
     const int64_t rounds = n_items / G;
     tail = n_items - rounds * G;
     KS = 1;
@@ -604,14 +626,14 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     // stream chunks [c0, c1) of one item through the stage ring
     auto produce = [&](int64_t item, int32_t c0, int32_t c1) -> bool {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      const int32_t e = a.tile_expert[tau];
+      const int32_t e = plan_expert(a, tau);
       // only the valid rows are gathered (see the tcgen05 producer)
       const int32_t nq = gather ? (min(max(a.tile_mn[tau] - tau * BN, 0), BN) + 3) >> 2 : 0;
       if (gather) {
         __syncwarp();
         if (lane < BN) {
           const int32_t r = a.gather_rows[(int64_t)tau * BN + lane];
-          gidx[lane] = r >= 0 ? r / a.top_k : 0;
+          gidx[lane] = r >= 0 && r < a.R ? r / a.top_k : 0;
         }
         __syncwarp();
       }
@@ -698,7 +720,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     };
     auto finish = [&](int64_t item, const float (&raw)[2][4]) -> bool {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      const float scale = a.alpha[a.tile_expert[tau]] * 256.0f;  // undo the decode's 2^-8
+      const float scale = a.alpha[plan_expert_quiet(a, tau)] * 256.0f;  // undo the decode's 2^-8
       float d[2][4];
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
@@ -811,6 +833,9 @@ cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool 
   a.out = g.out;
   a.out_sf = g.out_sf;
   a.fc2_scale = g.fc2_scale;
+  a.max_tiles = (int32_t)s.tiles;
+  a.EL = (int32_t)s.EL;
+  a.R = s.R;
   a.p2e = g.p2e;
   a.route_w = g.route_w;
   a.rsf = g.rsf;
@@ -862,6 +887,9 @@ cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
   a.out_ld = g.which == 1 ? s.I : s.H;
   a.valid_rows = (int32_t)(g.which == 1 ? 2 * s.I : s.H);
   a.out = g.out;
+  a.max_tiles = (int32_t)s.tiles;
+  a.EL = (int32_t)s.EL;
+  a.R = s.R;
   a.p2e = g.p2e;
   a.route_w = g.route_w;
   a.rsf = g.rsf;

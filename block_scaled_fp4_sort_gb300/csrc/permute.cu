@@ -43,19 +43,24 @@ int num_sms() {
   return n;
 }
 
-// One warp per permuted row; rows past num_tiles*T are not touched.
+// One warp per permuted row; rows past num_tiles*T are not touched, padding
+// rows are zero-filled when zero_pad is set and left as they are otherwise
+// (the GEMMs never store results for padding slots).
 __global__ void permute_rows(const uint8_t* __restrict__ x, const uint8_t* __restrict__ x_sf,
                              const int32_t* __restrict__ p2e, const int32_t* __restrict__ num_tiles,
                              int64_t T, int64_t top_k, int64_t row_bytes, int64_t sf_bytes,
-                             uint8_t* __restrict__ px, uint8_t* __restrict__ px_sf) {
+                             int zero_pad, int64_t S, int64_t M, uint8_t* __restrict__ px,
+                             uint8_t* __restrict__ px_sf) {
   grid_dependency_wait();
-  const int64_t rows = (int64_t)num_tiles[0] * T;
+  // a tile count or slot entry from outside [0, S) / [0, M*top_k) is not followed
+  const int64_t rows = min(max((int64_t)num_tiles[0], (int64_t)0) * T, S);
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t s = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); s < rows;
        s += warps) {
     const int32_t r = p2e[s];
-    const int64_t src = r >= 0 ? r / top_k : -1;
+    const int64_t src = r >= 0 && r < M * top_k ? r / top_k : -1;
+    if (src < 0 && !zero_pad) continue;
     uint4* dst = reinterpret_cast<uint4*>(px + s * row_bytes);
     const uint4* sp = reinterpret_cast<const uint4*>(x + src * row_bytes);
     for (int64_t i = lane; i < row_bytes / 16; i += 32) dst[i] = src >= 0 ? sp[i] : make_uint4(0, 0, 0, 0);
@@ -91,7 +96,8 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
 // y is the fp32 route storage GEMM2 writes.  One thread per 8 outputs.
 __global__ void finalize_rows(const float4* __restrict__ y, const int32_t* __restrict__ e2p,
                               const float* __restrict__ w, float rsf, int accumulate,
-                              uint4* __restrict__ out, int64_t M, int64_t H8, int top_k) {
+                              uint4* __restrict__ out, int64_t M, int64_t H8, int top_k,
+                              int64_t S) {
   grid_dependency_wait();
   const int64_t n = M * H8;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -106,7 +112,7 @@ __global__ void finalize_rows(const float4* __restrict__ y, const int32_t* __res
     }
     for (int j = 0; j < top_k; ++j) {
       const int32_t s = e2p[t * top_k + j];
-      if (s < 0) continue;
+      if (s < 0 || s >= S) continue;
       const float wk = rsf * w[t * top_k + j];
       const float4 y0 = y[((int64_t)s * H8 + c) * 2], y1 = y[((int64_t)s * H8 + c) * 2 + 1];
       const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
@@ -159,9 +165,10 @@ __constant__ float kE2M1[16] = {0.0f,  0.5f,  1.0f,  1.5f,  2.0f,  3.0f,  4.0f, 
 __global__ void dequant_rows(const uint32_t* __restrict__ q, const uint8_t* __restrict__ sf,
                              int64_t rows, int64_t K, const int32_t* __restrict__ num_tiles,
                              int64_t T, const int32_t* __restrict__ gather, int64_t top_k,
-                             uint4* __restrict__ out) {
+                             int64_t src_rows, uint4* __restrict__ out) {
   grid_dependency_wait();
-  const int64_t nrows = num_tiles ? min(rows, (int64_t)num_tiles[0] * T) : rows;
+  const int64_t nrows =
+      num_tiles ? min(rows, max((int64_t)num_tiles[0], (int64_t)0) * T) : rows;
   const int64_t per_row = K / 8;
   const int64_t n = nrows * per_row;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -170,7 +177,7 @@ __global__ void dequant_rows(const uint32_t* __restrict__ q, const uint8_t* __re
     int64_t src = r;
     if (gather) {
       const int32_t g = gather[r];
-      src = g >= 0 ? g / top_k : -1;
+      src = g >= 0 && g < src_rows * top_k ? g / top_k : -1;
     }
     float f[8];
     if (src >= 0) {
@@ -216,13 +223,13 @@ __global__ void debug_quantize(const float* __restrict__ in, int64_t n, const fl
 
 cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, const int32_t* p2e,
                            const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
-                           bool pdl) {
+                           bool pdl, bool zero_pad) {
   const int64_t row_bytes = s.mode == 0 ? s.H * 2 : s.H / 2;
   const int64_t sf_bytes = s.mode == 0 ? 0 : s.H / 16;
   const int64_t blocks = std::min<int64_t>((s.S + 7) / 8, (int64_t)num_sms() * 8);
   return launch_pdl(permute_rows, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), st, pdl,
                     static_cast<const uint8_t*>(x), s.mode == 0 ? nullptr : x_sf, p2e, num_tiles,
-                    s.T, s.K, row_bytes, sf_bytes, static_cast<uint8_t*>(px),
+                    s.T, s.K, row_bytes, sf_bytes, zero_pad ? 1 : 0, s.S, s.M, static_cast<uint8_t*>(px),
                     s.mode == 0 ? nullptr : px_sf);
 }
 
@@ -233,7 +240,7 @@ cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, c
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 16);
   return launch_pdl(finalize_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
                     static_cast<const float4*>(y), e2p, w, rsf, accumulate,
-                    static_cast<uint4*>(out), s.M, s.H / 8, (int)s.K);
+                    static_cast<uint4*>(out), s.M, s.H / 8, (int)s.K, s.S);
 }
 
 cudaError_t launch_seed_acc(const Shape& s, const void* out, int accumulate, float* acc,
@@ -256,13 +263,14 @@ cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaSt
 
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
                                 const int32_t* row_limit_tiles, int64_t T, void* out,
-                                cudaStream_t st, bool pdl, const int32_t* gather, int64_t top_k) {
+                                cudaStream_t st, bool pdl, const int32_t* gather, int64_t top_k,
+                                int64_t src_rows) {
   const int64_t n = rows * (K / 8);
   if (n == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 16);
   return launch_pdl(dequant_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
                     reinterpret_cast<const uint32_t*>(q), sf, rows, K, row_limit_tiles, T, gather,
-                    top_k, static_cast<uint4*>(out));
+                    top_k, src_rows, static_cast<uint4*>(out));
 }
 
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl) {

@@ -250,9 +250,9 @@ FP4MOE_API fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y,
                            int32_t accumulate, void* out, void* stream);
 
 /* The whole forward on `stream`: route sort, x gathered into slot order in the
- * workspace (route_tile >= 32; w4a4 rows expanded to BF16 on the way) or by
- * TMA inside GEMM1 (route_tile 16), GEMM1 (+ SwiGLU), GEMM2, finalize,
- * chained with programmatic dependent launch.  Arguments as in the steps above; the
+ * workspace (w4a4 rows expanded to BF16 on the way; padding rows unwritten),
+ * GEMM1 (+ SwiGLU), GEMM2, finalize, chained with programmatic dependent
+ * launch.  Arguments as in the steps above; the
  * weights are prepared (fp4moe_prepare_weights).  finalize_mode:
  *   FP4MOE_FINALIZE_DETERMINISTIC: bit-reproducible (default);
  *   FP4MOE_FINALIZE_ATOMIC (cute_dsl_fused_moe use_fused_finalize): no y
