@@ -35,18 +35,48 @@ class Fp4MoeError(RuntimeError):
         super().__init__("%s: %s (status %d)" % (where, status_string(status), status))
 
 
+ACT_SWIGLU, ACT_GEGLU_TANH, ACT_RELU2 = 0, 1, 2
+ACT_F_SWIGLU_OAI, ACT_F_SITU, ACT_F_SITU_LINEAR = 1, 2, 4
+
+
+class Activation(ctypes.Structure):
+    _fields_ = [("type", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("swiglu_alpha", ctypes.c_float), ("swiglu_beta", ctypes.c_float),
+                ("swiglu_limit", ctypes.c_float), ("situ_beta", ctypes.c_float),
+                ("situ_linear_beta", ctypes.c_float)]
+
+
 class Problem(ctypes.Structure):
     _fields_ = [("num_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32),
                 ("inter", ctypes.c_int32), ("num_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("num_local_experts", ctypes.c_int32),
                 ("local_expert_offset", ctypes.c_int32), ("route_tile", ctypes.c_int32),
-                ("mode", ctypes.c_int32)]
+                ("mode", ctypes.c_int32), ("activation", Activation)]
+
+
+def activation(type=ACT_SWIGLU, swiglu_alpha=None, swiglu_beta=None, swiglu_limit=None,
+               situ_beta=None, situ_linear_beta=None) -> Activation:
+    """The FC1 activation; swiglu_* parameters select swiglu_oai (defaults 1, 0,
+    +inf), situ_beta selects SiTU, situ_linear_beta adds its up-branch clamp."""
+    a = Activation(type, 0, 1.0, 0.0, float("inf"), 0.0, 0.0)
+    if swiglu_alpha is not None or swiglu_beta is not None or swiglu_limit is not None:
+        a.flags |= ACT_F_SWIGLU_OAI
+        a.swiglu_alpha = 1.0 if swiglu_alpha is None else swiglu_alpha
+        a.swiglu_beta = 0.0 if swiglu_beta is None else swiglu_beta
+        a.swiglu_limit = float("inf") if swiglu_limit is None else swiglu_limit
+    if situ_beta is not None:
+        a.flags |= ACT_F_SITU
+        a.situ_beta = situ_beta
+    if situ_linear_beta is not None:
+        a.flags |= ACT_F_SITU_LINEAR
+        a.situ_linear_beta = situ_linear_beta
+    return a
 
 
 def problem(num_tokens, hidden, inter, num_experts, top_k, num_local_experts=0,
-            local_expert_offset=0, route_tile=0, mode=W4A16) -> Problem:
+            local_expert_offset=0, route_tile=0, mode=W4A16, act=None) -> Problem:
     return Problem(num_tokens, hidden, inter, num_experts, top_k, num_local_experts,
-                   local_expert_offset, route_tile, mode)
+                   local_expert_offset, route_tile, mode, act if act is not None else Activation())
 
 
 _lib = None
@@ -76,11 +106,12 @@ def lib() -> ctypes.CDLL:
             "moe_route_sort": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "moe_route_sort_noalloc": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "moe_permute": (i32, [P, vp, vp, vp, vp, vp, vp, vp]),
-            "moe_gemm1_swiglu": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+            "moe_gemm1_swiglu": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                       vp]),
             "moe_gemm2": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
             "moe_finalize": (i32, [P, vp, vp, vp, f32, i32, vp, vp]),
-            "fused_moe_forward": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp, vp,
-                                        sz, vp]),
+            "fused_moe_forward": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp,
+                                        vp, sz, vp]),
             "fp4moe_debug_quantize_nvfp4": (i32, [vp, i64, vp, vp, vp, vp]),
             "fp4moe_debug_decode_prepared": (i32, [P, i32, vp, vp, vp]),
         }
@@ -203,10 +234,10 @@ def moe_permute(p: Problem, x, x_sf, permuted_idx_to_expanded_idx, num_non_exiti
 
 def moe_gemm1_swiglu(p: Problem, a, a_sf, gather_rows, w1_prepared, w1_alpha, fc2_input_scale,
                      tile_idx_to_expert, tile_idx_to_mn_limit, num_non_exiting_tiles, h, h_sf,
-                     workspace, stream=None):
+                     workspace, stream=None, per_token_scale=None):
     _check(lib().moe_gemm1_swiglu(ctypes.byref(p), _p(a), _p(a_sf), _p(gather_rows),
                                   _p(w1_prepared), _p(w1_alpha), _p(fc2_input_scale),
-                                  _p(tile_idx_to_expert), _p(tile_idx_to_mn_limit),
+                                  _p(per_token_scale), _p(tile_idx_to_expert), _p(tile_idx_to_mn_limit),
                                   _p(num_non_exiting_tiles), _p(h), _p(h_sf), _p(workspace),
                                   _nbytes(workspace), _stream(stream)), "moe_gemm1_swiglu")
 
@@ -229,10 +260,11 @@ def moe_finalize(p: Problem, y, expanded_idx_to_permuted_idx, token_final_scales
 def fused_moe_forward(p: Problem, x, x_sf, token_selected_experts, token_final_scales,
                       w1_prepared, w1_alpha, fc2_input_scale, w2_prepared, w2_alpha,
                       routed_scaling_factor, accumulate, finalize_mode, out, workspace,
-                      stream=None):
+                      stream=None, per_token_scale=None):
     _check(lib().fused_moe_forward(ctypes.byref(p), _p(x), _p(x_sf), _p(token_selected_experts),
                                    _p(token_final_scales), _p(w1_prepared), _p(w1_alpha),
-                                   _p(fc2_input_scale), _p(w2_prepared), _p(w2_alpha),
+                                   _p(fc2_input_scale), _p(per_token_scale), _p(w2_prepared),
+                                   _p(w2_alpha),
                                    float(routed_scaling_factor), int(bool(accumulate)),
                                    int(finalize_mode), _p(out), _p(workspace), _nbytes(workspace),
                                    _stream(stream)), "fused_moe_forward")

@@ -8,10 +8,10 @@ from __future__ import annotations
 
 import torch
 
-from . import (W4A4, W4A16, FINALIZE_DETERMINISTIC, fused_moe_forward, gemm_workspace_size,
-               max_permuted_slots, moe_finalize, moe_gemm1_swiglu, moe_gemm2, moe_permute,
-               moe_route_sort, prepare_weights, prepared_weight_size, problem, route_tile,
-               route_workspace_size, workspace_size)
+from . import (W4A4, W4A16, FINALIZE_DETERMINISTIC, activation, fused_moe_forward,
+               gemm_workspace_size, max_permuted_slots, moe_finalize, moe_gemm1_swiglu, moe_gemm2,
+               moe_permute, moe_route_sort, prepare_weights, prepared_weight_size, problem,
+               route_tile, route_workspace_size, workspace_size)
 
 
 def _empty(n, dtype, device):
@@ -80,7 +80,8 @@ class MoEBuffers:
         moe_permute(p, x, x_sf, self.p2e, self.num_tiles, px, psf, stream)
         return px, psf
 
-    def gemm1(self, a, a_sf, w1_alpha, fc2_input_scale=None, gather=True, stream=None):
+    def gemm1(self, a, a_sf, w1_alpha, fc2_input_scale=None, gather=True, stream=None,
+              per_token_scale=None):
         p = self.p
         if p.mode == W4A16:
             h = torch.zeros(self.S, p.inter, dtype=torch.bfloat16, device=self.device)
@@ -90,7 +91,7 @@ class MoEBuffers:
             hsf = torch.zeros(self.S, p.inter // 16, dtype=torch.uint8, device=self.device)
         moe_gemm1_swiglu(p, a, a_sf, self.p2e if gather else None, self.w1p, w1_alpha,
                          fc2_input_scale, self.tile_expert, self.tile_mn, self.num_tiles, h, hsf,
-                         self.gemm1_ws, stream)
+                         self.gemm1_ws, stream, per_token_scale=per_token_scale)
         return h, hsf
 
     def gemm2(self, h, hsf, w2_alpha, stream=None):
@@ -107,15 +108,18 @@ class MoEBuffers:
     # -- fused path
     def forward(self, x, x_sf, ids, token_final_scales, w1_alpha, w2_alpha, out,
                 fc2_input_scale=None, rsf=1.0, accumulate=False,
-                finalize_mode=FINALIZE_DETERMINISTIC, stream=None):
+                finalize_mode=FINALIZE_DETERMINISTIC, stream=None, per_token_scale=None):
         ws = self.ensure_fused_ws()
         fused_moe_forward(self.p, x, x_sf, ids, token_final_scales, self.w1p, w1_alpha,
                           fc2_input_scale, self.w2p, w2_alpha, rsf, accumulate, finalize_mode, out,
-                          ws, stream)
+                          ws, stream, per_token_scale=per_token_scale)
         return out
 
 
 def problem_for(cfg, route_tile_=0, num_local_experts=0, local_expert_offset=0):
-    """fp4moe_problem for a synth.MoEConfig."""
+    """fp4moe_problem for a synth.MoEConfig (its activation included)."""
+    import synth
+    kind, params = synth.activation_spec(cfg)
     return problem(cfg.M, cfg.H, cfg.I, cfg.E, cfg.top_k, num_local_experts, local_expert_offset,
-                   route_tile_, W4A4 if cfg.mode == "w4a4" else W4A16)
+                   route_tile_, W4A4 if cfg.mode == "w4a4" else W4A16,
+                   activation(kind, **params))

@@ -7,6 +7,7 @@
 // Nothing here allocates, synchronises or reads device memory, except
 // fp4moe_read_error, which is documented as a synchronising diagnostic.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "fp4moe.h"
@@ -54,6 +55,24 @@ fp4moe_status validate(const fp4moe_problem* p, Shape* s) {
   int64_t S = (R + ne * (T - 1) + T - 1) / T * T;
   if (S < T) S = T;
   if (R > INT32_MAX || S > INT32_MAX) return FP4MOE_ERR_UNSUPPORTED;
+  // FC1 activation
+  const fp4moe_activation& a = p->activation;
+  const auto pos_finite = [](float v) { return std::isfinite(v) && v > 0.0f; };
+  if (a.type != FP4MOE_ACT_SWIGLU && a.type != FP4MOE_ACT_GEGLU_TANH && a.type != FP4MOE_ACT_RELU2)
+    return FP4MOE_ERR_INVALID_ARG;
+  const int32_t known = FP4MOE_ACT_F_SWIGLU_OAI | FP4MOE_ACT_F_SITU | FP4MOE_ACT_F_SITU_LINEAR;
+  if ((a.flags & ~known) != 0 || (a.flags != 0 && a.type != FP4MOE_ACT_SWIGLU))
+    return FP4MOE_ERR_INVALID_ARG;
+  if ((a.flags & FP4MOE_ACT_F_SWIGLU_OAI) && (a.flags & FP4MOE_ACT_F_SITU)) return FP4MOE_ERR_INVALID_ARG;
+  if ((a.flags & FP4MOE_ACT_F_SITU_LINEAR) && !(a.flags & FP4MOE_ACT_F_SITU)) return FP4MOE_ERR_INVALID_ARG;
+  if ((a.flags & FP4MOE_ACT_F_SWIGLU_OAI) &&
+      (!std::isfinite(a.swiglu_alpha) || !std::isfinite(a.swiglu_beta) || !(a.swiglu_limit > 0.0f)))
+    return FP4MOE_ERR_INVALID_ARG;
+  if ((a.flags & FP4MOE_ACT_F_SITU) && !pos_finite(a.situ_beta)) return FP4MOE_ERR_INVALID_ARG;
+  if ((a.flags & FP4MOE_ACT_F_SITU_LINEAR) && !pos_finite(a.situ_linear_beta))
+    return FP4MOE_ERR_INVALID_ARG;
+  s->act = Act{a.type, a.flags, a.swiglu_alpha, a.swiglu_beta, a.swiglu_limit, a.situ_beta,
+               a.situ_linear_beta};
   s->M = p->num_tokens;
   s->H = p->hidden;
   s->I = p->inter;
@@ -130,6 +149,13 @@ FusedWs fused_ws(const Shape& s) {
 }
 
 inline int* err_word(void* ws) { return static_cast<int*>(ws); }
+
+// GEMM1 epilogue for the activation and the FC1 output format
+Epilogue gemm1_epilogue(const Shape& s) {
+  const bool w4 = s.mode == FP4MOE_W4A4;
+  if (!gated(s)) return w4 ? kEpiRelu2Nvfp4 : kEpiRelu2Bf16;
+  return w4 ? kEpiSwigluNvfp4 : kEpiSwigluBf16;
+}
 
 }  // namespace
 
@@ -246,7 +272,7 @@ fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, const uint8_t*
 fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uint8_t* a_sf,
                                const int32_t* gather_rows, const void* w1_prepared,
                                const float* w1_alpha, const float* fc2_input_scale,
-                               const int32_t* tile_expert, const int32_t* tile_mn,
+                               const float* per_token_scale, const int32_t* tile_expert, const int32_t* tile_mn,
                                const int32_t* num_tiles, void* h, uint8_t* h_sf, void* workspace,
                                size_t workspace_bytes, void* stream) {
   Shape s;
@@ -255,6 +281,9 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   const bool w4 = s.mode == FP4MOE_W4A4;
   if (!ok_ptr(w1_prepared) || !ok_ptr(w1_alpha) || !ok_ptr(tile_expert) || !ok_ptr(tile_mn) ||
       !ok_ptr(num_tiles) || !ok_ptr(h) || !ok_ptr(workspace) || (gather_rows && !ok_ptr(gather_rows)))
+    return FP4MOE_ERR_INVALID_ARG;
+  // the per-token scale reaches a slot through its route (gather_rows)
+  if (per_token_scale && (!gather_rows || (s.M > 0 && !ok_ptr(per_token_scale))))
     return FP4MOE_ERR_INVALID_ARG;
   const int64_t act_rows = gather_rows ? s.M : s.S;
   if (act_rows > 0 && !ok_ptr(a)) return FP4MOE_ERR_INVALID_ARG;
@@ -281,7 +310,7 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
   GemmLaunch g = {};
   g.which = 1;
-  g.epi = w4 ? kEpiSwigluNvfp4 : kEpiSwigluBf16;
+  g.epi = gemm1_epilogue(s);
   g.wprep = static_cast<const uint8_t*>(w1_prepared);
   g.alpha = w1_alpha;
   g.tile_expert = tile_expert;
@@ -293,6 +322,8 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   g.out = h;
   g.out_sf = h_sf;
   g.fc2_scale = fc2_input_scale;
+  g.token_scale = per_token_scale;
+  g.p2e = gather_rows;
   g.split = gemm_split(s, 1, ws);
   g.err = err_word(ws);
   return cuda_status(launch_gemm(s, g, cs, w4 || slot_order));
@@ -350,7 +381,7 @@ fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y, const int32_t
 fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
                                 const int32_t* ids, const float* wts, const void* w1_prepared,
                                 const float* w1_alpha, const float* fc2_input_scale,
-                                const void* w2_prepared, const float* w2_alpha, float rsf,
+                                const float* per_token_scale, const void* w2_prepared, const float* w2_alpha, float rsf,
                                 int32_t accumulate, int32_t finalize_mode, void* out,
                                 void* workspace, size_t workspace_bytes, void* stream) {
   Shape s;
@@ -365,6 +396,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   if (s.M > 0 && (!ok_ptr(x) || !ok_ptr(ids) || !ok_ptr(wts) || !ok_ptr(out)))
     return FP4MOE_ERR_INVALID_ARG;
   if (w4 && ((s.M > 0 && !ok_ptr(x_sf)) || !ok_ptr(fc2_input_scale))) return FP4MOE_ERR_INVALID_ARG;
+  if (per_token_scale && s.M > 0 && !ok_ptr(per_token_scale)) return FP4MOE_ERR_INVALID_ARG;
   const FusedWs L = fused_ws(s);
   if (workspace_bytes < L.total) return FP4MOE_ERR_WORKSPACE_TOO_SMALL;
   if (s.M == 0) return FP4MOE_OK;
@@ -393,7 +425,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
            : launch_permute(s, x, nullptr, p2e, nt, ws + L.y, nullptr, cs, true, false);
   GemmLaunch g1 = {};
   g1.which = 1;
-  g1.epi = w4 ? kEpiSwigluNvfp4 : kEpiSwigluBf16;
+  g1.epi = gemm1_epilogue(s);
   g1.wprep = static_cast<const uint8_t*>(w1_prepared);
   g1.alpha = w1_alpha;
   g1.tile_expert = te;
@@ -405,6 +437,8 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g1.out = ws + L.h;
   g1.out_sf = w4 ? ws + L.h_sf : nullptr;
   g1.fc2_scale = fc2_input_scale;
+  g1.token_scale = per_token_scale;
+  g1.p2e = p2e;
   g1.split = fragment_layout(s) ? ws + L.split : nullptr;
   g1.err = err;
   if (e == cudaSuccess) e = launch_gemm(s, g1, cs, true);

@@ -27,13 +27,26 @@ constexpr int64_t kSplitMaxUnits = 256;
 constexpr size_t kSplitCountBytes = kSplitMaxUnits * 4;
 constexpr size_t kSplitBytes = kSplitCountBytes + kSplitMaxUnits * 16 * 32 * 8 * 4;
 
+// FC1 activation (the header's fp4moe_activation, validated)
+struct Act {
+  int32_t type, flags;
+  float alpha, beta, limit, situ_beta, situ_lin;
+};
+
 struct Shape {
   int64_t M, H, I, E, K, EL, off, T, mode;
   int64_t R, S, tiles;  // routes, permuted slots, S / T
+  Act act;
 };
 
+// GEMM1 is gated (gate and up rows) for every activation but ReLU^2
+inline bool gated(const Shape& s) { return s.act.type != 2; }
+
+// 256-row weight blocks per expert: gated GEMM1 pairs 128 gate rows with the
+// matching 128 up rows; ReLU^2 GEMM1 and GEMM2 take 256 consecutive rows
 inline int64_t row_blocks(const Shape& s, int which) {
-  return which == 1 ? s.I / 128 : (s.H + 255) / 256;
+  if (which == 1) return gated(s) ? s.I / 128 : (s.I + 255) / 256;
+  return (s.H + 255) / 256;
 }
 inline int64_t k_chunks(const Shape& s, int which) { return which == 1 ? s.H / kBK : s.I / kBK; }
 // Decode-size problems (BF16 activations, route tile 16) run on the
@@ -80,7 +93,12 @@ cudaError_t launch_debug_decode(const Shape& s, int which, const uint8_t* prepar
                                 cudaStream_t st);
 
 // ---- grouped GEMM (moe_gemm.cu) ----
-enum Epilogue { kEpiSwigluBf16 = 0, kEpiSwigluNvfp4 = 1, kEpiPlainBf16 = 2, kEpiAtomicFinal = 3 };
+// GEMM epilogues: gated activation -> BF16 h / NVFP4 h; fp32 y; atomic
+// finalize; non-gated ReLU^2 -> BF16 h / NVFP4 h
+enum Epilogue {
+  kEpiSwigluBf16 = 0, kEpiSwigluNvfp4 = 1, kEpiPlainBf16 = 2, kEpiAtomicFinal = 3,
+  kEpiRelu2Bf16 = 4, kEpiRelu2Nvfp4 = 5
+};
 
 struct GemmLaunch {
   int which;                   // 1 = GEMM1 (+SwiGLU), 2 = GEMM2
@@ -96,6 +114,7 @@ struct GemmLaunch {
   void* out;                   // h bf16 [S, I] | hq [S, I/2] | y bf16 [S, H] | out bf16 [M, H]
   uint8_t* out_sf;             // hsf [S, I/16]
   const float* fc2_scale;      // [1]
+  const float* token_scale;    // per_token_scale [M] (GEMM1) or null; needs p2e
   void* split;                 // warp-MMA K-split tail scratch (kSplitBytes, zero-filled once) or null
   // atomic finalize epilogue
   const int32_t* p2e;

@@ -58,6 +58,8 @@ struct GemmArgs {
   void* out;
   uint8_t* out_sf;
   const float* fc2_scale;
+  const float* token_scale;    // GEMM1 per_token_scale [M] (token of slot s: p2e[s] / top_k) or null
+  Act act;                     // GEMM1 activation
   int32_t max_tiles;           // S / T: bound on num_tiles[0]
   int32_t EL;                  // local experts: bound on tile_idx_to_expert
   int64_t R;                   // routes M * top_k: bound on slot entries
@@ -78,6 +80,18 @@ __device__ __forceinline__ void atomic_final_add(const GemmArgs& a, int64_t s, i
   if (r >= 0 && r < a.R)
     atomicAdd(static_cast<float*>(a.out) + (int64_t)(r / a.top_k) * a.out_ld + n,
               (a.rsf * a.route_w[r]) * yv);
+}
+
+// GEMM1's activation of one (gate, up) pair, and the per-token input scale of
+// slot s (1 without per_token_scale)
+__device__ __forceinline__ float gemm1_act(const GemmArgs& a, float g, float u) {
+  return act_gated(a.act.type, a.act.flags, a.act.alpha, a.act.beta, a.act.limit, a.act.situ_beta,
+                   a.act.situ_lin, g, u);
+}
+__device__ __forceinline__ float token_factor(const GemmArgs& a, int64_t s) {
+  if (a.token_scale == nullptr) return 1.0f;
+  const int32_t r = a.p2e[s];
+  return r >= 0 && r < a.R ? a.token_scale[r / a.top_k] : 1.0f;
 }
 
 // Work items from the routing plan: the tile count is clamped to S / T and an
@@ -346,6 +360,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      } else if (EPI == kEpiRelu2Bf16 || EPI == kEpiRelu2Nvfp4) {
+        // non-gated FC1: both 128-row tiles are outputs, feature n per thread
+        const int64_t n = (int64_t)f * 256 + tile * 128 + row;
+        const float fs = EPI == kEpiRelu2Nvfp4 ? a.fc2_scale[0] : 0.0f;
+        if (n < a.valid_rows) {  // warp-uniform: I is a multiple of 128
+#pragma unroll 1
+          for (int cc = 0; cc < BN; cc += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc), v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int64_t s = s0 + cc + i;
+              const float hv = s < mn ? relu2(__uint_as_float(v[i]) * scale * token_factor(a, s)) : 0.0f;
+              if (EPI == kEpiRelu2Bf16) {
+                static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] = __float2bfloat16_rn(hv);
+              } else {
+                uint32_t sf;
+                const uint32_t code = nvfp4_quant_lane16(hv, fs, &sf);
+                const uint32_t other = __shfl_down_sync(0xffffffffu, code, 1);
+                if ((lane & 1) == 0)
+                  static_cast<uint8_t*>(a.out)[s * (a.out_ld / 2) + n / 2] = (uint8_t)(code | (other << 4));
+                if ((lane & 15) == 0) a.out_sf[s * (a.out_ld / 16) + n / 16] = (uint8_t)sf;
+              }
+            }
+          }
+        }
       } else {
         constexpr int kCols = BN >= 32 ? BN / 2 : BN;
         if (BN >= 32 || warp < 4) {
@@ -361,9 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int64_t s = s0 + cbase + cc + i;
-              const float hv = s < mn ? swiglu(__uint_as_float(g[i]) * scale,
-                                               __uint_as_float(u[i]) * scale)
-                                      : 0.0f;
+              float hv = 0.0f;
+              if (s < mn) {
+                const float sc = scale * token_factor(a, s);
+                hv = gemm1_act(a, __uint_as_float(g[i]) * sc, __uint_as_float(u[i]) * sc);
+              }
               if (EPI == kEpiSwigluBf16) {
                 static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] = __float2bfloat16_rn(hv);
               } else {
@@ -549,6 +592,21 @@ __device__ __forceinline__ bool gv_epilogue(const GemmArgs& a, int32_t tau, int3
     }
     return true;
   }
+  if (EPI == kEpiRelu2Bf16) {  // non-gated FC1: every row is an output
+    __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t feat = (int64_t)f * 256 + (i < 2 ? r0 : r1);
+        const int64_t s = s0 + 8 * nb + 2 * t + (i & 1);
+        if (feat >= a.valid_rows) continue;
+        const float hv = s < mn ? relu2(d[nb][i] * token_factor(a, s)) : 0.0f;
+        h[s * a.out_ld + feat] = __float2bfloat16_rn(hv);
+      }
+    }
+    return true;
+  }
   // up rows (warps 8-15) hand their values to the gate rows (warps 0-7)
   if (w >= kGvWarps / 2) {
     if (!__all_sync(0xffffffffu, mbar_wait(xfree, xphase ^ 1u, a.err))) return false;
@@ -569,8 +627,11 @@ __device__ __forceinline__ bool gv_epilogue(const GemmArgs& a, int32_t tau, int3
         const uint32_t row = i < 2 ? r0 : r1;
         const int n = 8 * nb + 2 * t + (i & 1);
         const int64_t s = s0 + n;
-        const float u = xchg[row * BN + n];
-        const float hv = s < mn ? swiglu(d[nb][i], u) : 0.0f;
+        float hv = 0.0f;
+        if (s < mn) {
+          const float c = token_factor(a, s);
+          hv = gemm1_act(a, d[nb][i] * c, xchg[row * BN + n] * c);
+        }
         h[s * a.out_ld + (int64_t)f * 128 + row] = __float2bfloat16_rn(hv);
       }
     }
@@ -829,7 +890,9 @@ cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool 
   a.F = (int32_t)row_blocks(s, g.which);
   a.C = (int32_t)k_chunks(s, g.which);
   a.out_ld = g.which == 1 ? s.I : s.H;
-  a.valid_rows = (int32_t)(g.which == 1 ? 2 * s.I : s.H);
+  a.valid_rows = (int32_t)(g.which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H);
+  a.act = s.act;
+  a.token_scale = g.token_scale;
   a.out = g.out;
   a.out_sf = g.out_sf;
   a.fc2_scale = g.fc2_scale;
@@ -868,6 +931,8 @@ cudaError_t launch_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
     case kEpiSwigluNvfp4: return launch_t<BN, kEpiSwigluNvfp4>(s, g, st, pdl);
     case kEpiPlainBf16: return launch_t<BN, kEpiPlainBf16>(s, g, st, pdl);
     case kEpiAtomicFinal: return launch_t<BN, kEpiAtomicFinal>(s, g, st, pdl);
+    case kEpiRelu2Bf16: return launch_t<BN, kEpiRelu2Bf16>(s, g, st, pdl);
+    case kEpiRelu2Nvfp4: return launch_t<BN, kEpiRelu2Nvfp4>(s, g, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -885,7 +950,9 @@ cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
   a.F = (int32_t)row_blocks(s, g.which);
   a.C = (int32_t)k_chunks(s, g.which);
   a.out_ld = g.which == 1 ? s.I : s.H;
-  a.valid_rows = (int32_t)(g.which == 1 ? 2 * s.I : s.H);
+  a.valid_rows = (int32_t)(g.which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H);
+  a.act = s.act;
+  a.token_scale = g.token_scale;
   a.out = g.out;
   a.max_tiles = (int32_t)s.tiles;
   a.EL = (int32_t)s.EL;
@@ -928,6 +995,7 @@ cudaError_t launch_gemm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bo
       case kEpiSwigluBf16: return launch_gv<kEpiSwigluBf16>(s, g, st, pdl);
       case kEpiPlainBf16: return launch_gv<kEpiPlainBf16>(s, g, st, pdl);
       case kEpiAtomicFinal: return launch_gv<kEpiAtomicFinal>(s, g, st, pdl);
+      case kEpiRelu2Bf16: return launch_gv<kEpiRelu2Bf16>(s, g, st, pdl);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -50,4 +50,47 @@ __device__ __forceinline__ float swiglu(float g, float u) {
   return g * r * u;
 }
 
+// 1 / (1 + exp(-v)), the same approximate exponential and reciprocal
+__device__ __forceinline__ float sigmoid_approx(float v) {
+  float e, r;
+  const float z = -v * 1.4426950408889634f;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(z));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return r;
+}
+
+__device__ __forceinline__ float tanh_approx(float v) {
+  float r;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// FC1 activations (cute_dsl_fused_moe activation_type; fp4moe.h,
+// fp4moe_activation): type 0 with flags 0 = SwiGLU, flag 1 = swiglu_oai
+// (alpha, beta, limit), flag 2 = SiTU gate, flag 4 = SiTU tanh clamp of the
+// up branch; type 1 = GeGLU with the tanh approximation of GELU.
+__device__ __forceinline__ float act_gated(int32_t type, int32_t flags, float alpha, float beta,
+                                           float limit, float situ_beta, float situ_lin, float g,
+                                           float u) {
+  if (type == 0 && flags == 0) return swiglu(g, u);
+  if (type == 1) {
+    const float c = 0.7978845608028654f;  // sqrt(2 / pi)
+    return 0.5f * g * (1.0f + tanh_approx(c * (g + 0.044715f * g * g * g))) * u;
+  }
+  if (flags & 1) {
+    const float gc = fminf(g, limit);
+    const float uc = fminf(fmaxf(u, -limit), limit);
+    return gc * sigmoid_approx(alpha * gc) * (uc + beta);
+  }
+  const float gate = situ_beta * tanh_approx(__fdividef(g, situ_beta)) * sigmoid_approx(g);
+  const float up = (flags & 4) ? situ_lin * tanh_approx(__fdividef(u, situ_lin)) : u;
+  return gate * up;
+}
+
+// non-gated ReLU^2
+__device__ __forceinline__ float relu2(float u) {
+  const float r = fmaxf(u, 0.0f);
+  return r * r;
+}
+
 }  // namespace fp4moe

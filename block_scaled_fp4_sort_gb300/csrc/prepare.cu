@@ -27,7 +27,8 @@ namespace {
 
 struct PrepArgs {
   int which;
-  int64_t EL, F, C, rows_src, K;  // rows_src: rows per expert in the source (2I or H)
+  int64_t EL, F, C, rows_src, K;  // rows_src: rows per expert in the source (2I, I or H)
+  int gated;                      // GEMM1 with gate and up rows
   int64_t I;                      // GEMM1: intermediate size
   const uint8_t* w;
   const uint8_t* w_sf;
@@ -36,7 +37,7 @@ struct PrepArgs {
 };
 
 __device__ __forceinline__ int64_t src_row(const PrepArgs& a, int64_t f, int64_t r) {
-  if (a.which == 1) return r < 128 ? 128 * f + r : a.I + 128 * f + (r - 128);
+  if (a.which == 1 && a.gated) return r < 128 ? 128 * f + r : a.I + 128 * f + (r - 128);
   const int64_t row = 256 * f + r;
   return row < a.rows_src ? row : -1;
 }
@@ -194,7 +195,8 @@ PrepArgs make_args(const Shape& s, int which) {
   a.EL = s.EL;
   a.F = row_blocks(s, which);
   a.C = k_chunks(s, which);
-  a.rows_src = which == 1 ? 2 * s.I : s.H;
+  a.gated = gated(s) ? 1 : 0;
+  a.rows_src = which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H;
   a.K = which == 1 ? s.H : s.I;
   a.I = s.I;
   return a;

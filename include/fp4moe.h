@@ -74,6 +74,41 @@ typedef enum {
   FP4MOE_FINALIZE_ATOMIC = 1           /* GEMM2's epilogue adds rsf*w*y into out atomically */
 } fp4moe_finalize_mode;
 
+/* FC1 activation (cute_dsl_fused_moe: activation_type, swiglu_alpha /
+ * swiglu_beta / swiglu_limit, situ_beta, situ_linear_beta).  g and u are
+ * the alpha-scaled gate and up pre-activations of one FC1 output:
+ *   FP4MOE_ACT_SWIGLU, flags 0   silu(g) * u  (the default; an all-zero
+ *                                struct selects it)
+ *     | FP4MOE_ACT_F_SWIGLU_OAI  gc * sigmoid(swiglu_alpha * gc) * (uc + swiglu_beta),
+ *                                gc = min(g, L), uc = clamp(u, -L, L), L = swiglu_limit
+ *                                (+inf allowed)
+ *     | FP4MOE_ACT_F_SITU        situ_beta * tanh(g / situ_beta) * sigmoid(g) * u'
+ *     | FP4MOE_ACT_F_SITU_LINEAR   u' = situ_linear_beta * tanh(u / situ_linear_beta)
+ *                                  (else u' = u)
+ *   FP4MOE_ACT_GEGLU_TANH        0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) * u
+ *   FP4MOE_ACT_RELU2             max(u, 0)^2, non-gated: w1 is [E, I, H/2] + [E, I, H/16]
+ * The oai and SiTU flags exclude each other; betas must be finite and > 0,
+ * swiglu_alpha finite, swiglu_limit > 0.  Other combinations return
+ * FP4MOE_ERR_INVALID_ARG. */
+typedef enum {
+  FP4MOE_ACT_SWIGLU = 0,
+  FP4MOE_ACT_GEGLU_TANH = 1,
+  FP4MOE_ACT_RELU2 = 2
+} fp4moe_activation_type;
+
+enum {
+  FP4MOE_ACT_F_SWIGLU_OAI = 1,
+  FP4MOE_ACT_F_SITU = 2,
+  FP4MOE_ACT_F_SITU_LINEAR = 4
+};
+
+typedef struct {
+  int32_t type;                /* fp4moe_activation_type */
+  int32_t flags;               /* FP4MOE_ACT_F_*, with FP4MOE_ACT_SWIGLU only */
+  float swiglu_alpha, swiglu_beta, swiglu_limit;
+  float situ_beta, situ_linear_beta;
+} fp4moe_activation;
+
 typedef struct {
   int32_t num_tokens;          /* M >= 0 */
   int32_t hidden;              /* H, multiple of 128 */
@@ -84,6 +119,7 @@ typedef struct {
   int32_t local_expert_offset; /* offset + num_local_experts <= num_experts */
   int32_t route_tile;          /* T: 0 = automatic, else 16, 32, 64 or 128 */
   int32_t mode;                /* fp4moe_quant_mode */
+  fp4moe_activation activation;  /* FC1 activation; all zero = SwiGLU */
 } fp4moe_problem;
 
 /* ------------------------------------------------------------------ queries */
@@ -131,9 +167,11 @@ FP4MOE_API fp4moe_status fp4moe_clear_error(void* workspace, void* stream);
  * `w1_data_prepared` and friends, and of the MMA scale layout the CuTe-DSL
  * kernels require, cute_dsl_fused_moe `localized_weights`).
  *   which = 1: w = w1 uint8 [E_local, 2I, H/2], w_sf = e4m3 [E_local, 2I, H/16]
+ *              (FP4MOE_ACT_RELU2: [E_local, I, H/2] and [E_local, I, H/16])
  *   which = 2: w = w2 uint8 [E_local, H, I/2],  w_sf = e4m3 [E_local, H, I/16]
- * prepared: fp4moe_prepared_weight_size(p, which) bytes.  Bit-exact repack,
- * no arithmetic.  Inputs are not modified. */
+ * prepared: fp4moe_prepared_weight_size(p, which) bytes.  A lossless
+ * re-encoding: every weight the kernels decode equals e2m1(code) *
+ * e4m3(scale) bit for bit.  Inputs are not modified. */
 FP4MOE_API fp4moe_status fp4moe_prepare_weights(const fp4moe_problem* p, int32_t which, const uint8_t* w,
                                      const uint8_t* w_sf, void* prepared, void* stream);
 
@@ -198,11 +236,15 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
                           const int32_t* num_non_exiting_tiles, void* permuted_x,
                           uint8_t* permuted_x_sf, void* stream);
 
-/* Grouped GEMM1 with the SwiGLU epilogue (vllm moe_cute module docstring:
- * E2M1*E4M3 decoded to BF16, BF16 tcgen05 MMAs, fp32 accumulation, alpha on
- * the accumulator, silu(g)*u in fp32 rounded once):
- *   h[s, n] = R( silu(a1_e * G_e[n] . A_s) * (a1_e * U_e[n] . A_s) )
- * for valid slots s (padding rows of h are zeroed), e = tile_idx_to_expert.
+/* Grouped GEMM1 with the activation epilogue (vllm moe_cute module docstring:
+ * E2M1*E4M3 decoded to BF16, BF16 MMAs, fp32 accumulation, alpha on the
+ * accumulator, the activation in fp32 rounded once):
+ *   h[s, n] = R( act(c_s a1_e G_e[n] . A_s, c_s a1_e U_e[n] . A_s) )
+ * for valid slots s (padding rows of h are zeroed), e = tile_idx_to_expert,
+ * act = p->activation (default silu(g) * u; ReLU^2 has no gate rows), and
+ * c_s = per_token_scale[t] of the slot's token t = gather_rows[s] / top_k
+ * (cute_dsl_fused_moe per_token_scale) or 1 when per_token_scale is NULL;
+ * per_token_scale needs gather_rows.
  *   a: activations.  If gather_rows != NULL it is x itself ([M, H] bf16, or
  *      [M, H/2] + a_sf [M, H/16] for w4a4) and row s is row
  *      gather_rows[s] / top_k (gather_rows = permuted_idx_to_expanded_idx);
@@ -218,6 +260,7 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
 FP4MOE_API fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uint8_t* a_sf,
                                const int32_t* gather_rows, const void* w1_prepared,
                                const float* w1_alpha, const float* fc2_input_scale,
+                               const float* per_token_scale,
                                const int32_t* tile_idx_to_expert,
                                const int32_t* tile_idx_to_mn_limit,
                                const int32_t* num_non_exiting_tiles, void* h, uint8_t* h_sf,
@@ -251,7 +294,7 @@ FP4MOE_API fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y,
 
 /* The whole forward on `stream`: route sort, x gathered into slot order in the
  * workspace (w4a4 rows expanded to BF16 on the way; padding rows unwritten),
- * GEMM1 (+ SwiGLU), GEMM2, finalize, chained with programmatic dependent
+ * GEMM1 (+ activation), GEMM2, finalize, chained with programmatic dependent
  * launch.  Arguments as in the steps above; the
  * weights are prepared (fp4moe_prepare_weights).  finalize_mode:
  *   FP4MOE_FINALIZE_DETERMINISTIC: bit-reproducible (default);
@@ -261,11 +304,13 @@ FP4MOE_API fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y,
  *     (rsf * w[t,j]) * y term into it with fp32 atomic adds, and a last pass
  *     rounds it into out (RNE).  The terms are those of the deterministic
  *     path; only their summation order varies from run to run.
+ * per_token_scale: fp32 [M] or NULL, as in moe_gemm1_swiglu.
  * workspace: fp4moe_workspace_size(p) bytes. */
 FP4MOE_API fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
                                 const int32_t* token_selected_experts,
                                 const float* token_final_scales, const void* w1_prepared,
                                 const float* w1_alpha, const float* fc2_input_scale,
+                                const float* per_token_scale,
                                 const void* w2_prepared, const float* w2_alpha,
                                 float routed_scaling_factor, int32_t accumulate,
                                 int32_t finalize_mode, void* out, void* workspace,

@@ -38,7 +38,10 @@ def build(force: bool = False) -> str:
 
 class Problem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("M", "H", "I", "E", "top_k", "E_local", "offset", "T", "mode")]
+                ("M", "H", "I", "E", "top_k", "E_local", "offset", "T", "mode", "act_type",
+                 "act_flags")] + [(n, ctypes.c_double) for n in
+                                  ("swiglu_alpha", "swiglu_beta", "swiglu_limit", "situ_beta",
+                                   "situ_linear_beta")]
 
 
 class Inputs(ctypes.Structure):
@@ -46,7 +49,7 @@ class Inputs(ctypes.Structure):
                 ("ids", ctypes.c_void_p), ("wts", ctypes.c_void_p),
                 ("w1", ctypes.c_void_p), ("w1_sf", ctypes.c_void_p), ("w1_alpha", ctypes.c_void_p),
                 ("w2", ctypes.c_void_p), ("w2_sf", ctypes.c_void_p), ("w2_alpha", ctypes.c_void_p),
-                ("fc2_input_scale", ctypes.c_void_p)]
+                ("fc2_input_scale", ctypes.c_void_p), ("per_token_scale", ctypes.c_void_p)]
 
 
 def lib():
@@ -148,7 +151,11 @@ class OracleMoE:
     """Holds host copies (numpy) of one workload and evaluates the oracle on it."""
 
     def __init__(self, M, H, I, E, top_k, ids, wts, w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha,
-                 x=None, x_q=None, x_sf=None, fc2_input_scale=None, E_local=None, offset=0, T=16):
+                 x=None, x_q=None, x_sf=None, fc2_input_scale=None, E_local=None, offset=0, T=16,
+                 act_type=0, act_params=None, per_token_scale=None):
+        """act_type / act_params: the FC1 activation (0 SwiGLU family with optional
+        swiglu_alpha/beta/limit or situ_beta/situ_linear_beta, 1 GeGLU-tanh,
+        2 non-gated ReLU^2); per_token_scale: fp32 [M] or None."""
         c = np.ascontiguousarray
         self.arrays = dict(
             x=None if x is None else c(x, dtype=np.uint16),
@@ -159,10 +166,22 @@ class OracleMoE:
             w1_alpha=c(w1_alpha, dtype=np.float32),
             w2=c(w2, dtype=np.uint8), w2_sf=c(w2_sf, dtype=np.uint8),
             w2_alpha=c(w2_alpha, dtype=np.float32),
-            fc2_input_scale=None if fc2_input_scale is None else c(fc2_input_scale, dtype=np.float32))
+            fc2_input_scale=None if fc2_input_scale is None else c(fc2_input_scale, dtype=np.float32),
+            per_token_scale=None if per_token_scale is None else c(per_token_scale, dtype=np.float32))
         mode = 0 if x is not None else 1
         E_local = E if E_local is None else E_local
-        self.p = Problem(M, H, I, E, top_k, E_local, offset, T, mode)
+        ap = dict(act_params or {})
+        flags = 0
+        if {"swiglu_alpha", "swiglu_beta", "swiglu_limit"} & set(ap):
+            flags |= 1
+        if "situ_beta" in ap:
+            flags |= 2
+        if "situ_linear_beta" in ap:
+            flags |= 4
+        self.p = Problem(M, H, I, E, top_k, E_local, offset, T, mode, act_type, flags,
+                         float(ap.get("swiglu_alpha", 1.0)), float(ap.get("swiglu_beta", 0.0)),
+                         float(ap.get("swiglu_limit", float("inf"))), float(ap.get("situ_beta", 0.0)),
+                         float(ap.get("situ_linear_beta", 0.0)))
         self.inp = Inputs(**{k: _ptr(v) for k, v in self.arrays.items()})
 
     @classmethod
@@ -177,10 +196,14 @@ class OracleMoE:
             if t.dtype == _bf16():
                 return t.view(_i16()).numpy().view(np.uint16)
             return t.numpy()
+        import synth
+        act_type, act_params = synth.activation_spec(cfg)
         return cls(cfg.M, cfg.H, cfg.I, cfg.E, cfg.top_k, h(inp.token_selected_experts),
                    h(inp.token_final_scales), h(inp.w1), h(inp.w1_sf), h(inp.w1_alpha), h(inp.w2),
                    h(inp.w2_sf), h(inp.w2_alpha), x=h(inp.x), x_q=h(inp.x_q), x_sf=h(inp.x_sf),
-                   fc2_input_scale=h(inp.fc2_input_scale), E_local=E_local, offset=offset, T=T)
+                   fc2_input_scale=h(inp.fc2_input_scale), E_local=E_local, offset=offset, T=T,
+                   act_type=act_type, act_params=act_params,
+                   per_token_scale=h(getattr(inp, "per_token_scale", None)))
 
     @property
     def H(self):

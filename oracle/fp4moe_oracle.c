@@ -264,9 +264,40 @@ void orc_xhat(const orc_problem* p, const orc_inputs* in, int64_t t, double* xha
     for (int64_t k = 0; k < H; ++k)
       xhat[k] = dec_packed(in->x_q + t * (H / 2), in->x_sf + t * (H / 16), k);
   }
+  /* reading: the per-token input row scale multiplies the decoded row */
+  if (in->per_token_scale)
+    for (int64_t k = 0; k < H; ++k) xhat[k] *= (double)in->per_token_scale[t];
 }
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
+static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+/* gated FC1 activations (act_type 0 and 1), see the header */
+static double act_gated(const orc_problem* p, double g, double u) {
+  if (p->act_type == 1) {
+    const double c = sqrt(2.0 / 3.14159265358979323846);
+    return 0.5 * g * (1.0 + tanh(c * (g + 0.044715 * g * g * g))) * u;
+  }
+  if (p->act_flags & 1) {
+    const double L = p->swiglu_limit;
+    const double gc = g < L ? g : L;
+    const double uc = u > L ? L : (u < -L ? -L : u);
+    return gc * sigmoid(p->swiglu_alpha * gc) * (uc + p->swiglu_beta);
+  }
+  if (p->act_flags & 2) {
+    const double gate = p->situ_beta * tanh(g / p->situ_beta) * sigmoid(g);
+    const double up = (p->act_flags & 4) ? p->situ_linear_beta * tanh(u / p->situ_linear_beta) : u;
+    return gate * up;
+  }
+  return silu(g) * u;
+}
+
+/* sum_k dec(W[row])[k] * v[k] in ascending k */
+static double dot1(const uint8_t* q, const uint8_t* sf, const double* v, int64_t K) {
+  double acc = 0.0;
+  for (int64_t k = 0; k < K; ++k) acc += dec_packed(q, sf, k) * v[k];
+  return acc;
+}
 
 static void down_proj(const orc_problem* p, const orc_inputs* in, int32_t e, const double* hin,
                       double* y) {
@@ -288,8 +319,10 @@ void orc_expert_ffn(const orc_problem* p, const orc_inputs* in, int32_t e, const
                     uint8_t* hsf, double* y) {
   int64_t H = p->H, I = p->I;
   pthread_once(&g_tab_once, build_tables);
-  const uint8_t* W1 = in->w1 + (int64_t)e * 2 * I * (H / 2);
-  const uint8_t* S1 = in->w1_sf + (int64_t)e * 2 * I * (H / 16);
+  const int gated = p->act_type != 2;
+  const int64_t rows1 = gated ? 2 * I : I;   /* FC1 rows per expert */
+  const uint8_t* W1 = in->w1 + (int64_t)e * rows1 * (H / 2);
+  const uint8_t* S1 = in->w1_sf + (int64_t)e * rows1 * (H / 16);
   double a1 = (double)in->w1_alpha[e];
   double* h = (double*)malloc(sizeof(double) * (size_t)I);
   double* hi = (double*)malloc(sizeof(double) * (size_t)I);
@@ -297,14 +330,21 @@ void orc_expert_ffn(const orc_problem* p, const orc_inputs* in, int32_t e, const
   uint8_t* q = (uint8_t*)malloc((size_t)I / 2);
   uint8_t* sf = (uint8_t*)malloc((size_t)I / 16);
   for (int64_t n = 0; n < I; ++n) {
-    /* reading: rows [0, I) of w1 are the gate, rows [I, 2I) the up projection */
-    double gacc, uacc;
-    dot2(W1 + n * (H / 2), S1 + n * (H / 16), W1 + (I + n) * (H / 2), S1 + (I + n) * (H / 16),
-         xhat, H, &gacc, &uacc);
-    double g = a1 * gacc, u = a1 * uacc;   /* alpha on the accumulator */
-    if (g_out) g_out[n] = g;
-    if (u_out) u_out[n] = u;
-    h[n] = silu(g) * u;                     /* default swiglu alpha=1, beta=0, limit=FLT_MAX */
+    if (gated) {
+      /* reading: rows [0, I) of w1 are the gate, rows [I, 2I) the up projection */
+      double gacc, uacc;
+      dot2(W1 + n * (H / 2), S1 + n * (H / 16), W1 + (I + n) * (H / 2), S1 + (I + n) * (H / 16),
+           xhat, H, &gacc, &uacc);
+      double g = a1 * gacc, u = a1 * uacc;   /* alpha on the accumulator */
+      if (g_out) g_out[n] = g;
+      if (u_out) u_out[n] = u;
+      h[n] = act_gated(p, g, u);
+    } else {
+      double u = a1 * dot1(W1 + n * (H / 2), S1 + n * (H / 16), xhat, H);
+      if (g_out) g_out[n] = 0.0;
+      if (u_out) u_out[n] = u;
+      h[n] = u > 0.0 ? u * u : 0.0;            /* ReLU^2 */
+    }
     if (h_pre) h_pre[n] = h[n];
   }
   if (p->mode == 0) {

@@ -27,9 +27,20 @@
 extern "C" {
 #endif
 
+/* FC1 activation (cute_dsl_fused_moe: activation_type, swiglu_alpha/beta/
+ * limit, situ_beta, situ_linear_beta), with g, u the alpha-scaled gate and
+ * up pre-activations:
+ *   act_type 0, act_flags 0 : silu(g) * u
+ *   act_type 0, flags & 1   : swiglu_oai  min(g, L) * sigmoid(a * min(g, L)) * (clamp(u, -L, L) + b)
+ *   act_type 0, flags & 2   : SiTU        sb * tanh(g / sb) * sigmoid(g) * u', u' = u, or
+ *                             slb * tanh(u / slb) when flags & 4
+ *   act_type 1              : GeGLU, tanh approximation  0.5 g (1 + tanh(sqrt(2/pi) (g + 0.044715 g^3))) * u
+ *   act_type 2              : non-gated ReLU^2  max(u, 0)^2, w1 has I rows (no gate rows) */
 typedef struct {
   int32_t M, H, I, E, top_k, E_local, offset, T;
   int32_t mode; /* 0 = w4a16 (BF16 x), 1 = w4a4 (NVFP4 x) */
+  int32_t act_type, act_flags;
+  double swiglu_alpha, swiglu_beta, swiglu_limit, situ_beta, situ_linear_beta;
 } orc_problem;
 
 typedef struct {
@@ -45,6 +56,7 @@ typedef struct {
   const uint8_t* w2_sf;     /* [E_local, H, I/16]                    */
   const float* w2_alpha;    /* [E_local]                             */
   const float* fc2_input_scale; /* [1] (w4a4) or NULL                */
+  const float* per_token_scale; /* [M] or NULL: x row t is scaled by it  */
 } orc_inputs;
 
 /* ---- scalar codecs (OCP FP8 E4M3, FP4 E2M1, bfloat16) ---- */
@@ -75,7 +87,8 @@ int32_t orc_route_sort(const orc_problem* p, const int32_t* ids,
 
 /* ---- per-route expert FFN (one token through one local expert) ----
  * xhat [H] is the decoded activation row.  Outputs (each may be NULL):
- *   g, u [I]  : alpha-scaled gate / up pre-activations
+ *   g, u [I]  : alpha-scaled gate / up pre-activations (ReLU^2: g unused,
+ *               u the single FC1 row)
  *   h_pre [I] : silu(g)*u before rounding
  *   h_in [I]  : the GEMM2 input value (BF16-rounded h; or dequantised NVFP4 h
  *               times 1 -- i.e. dec(q)*dec(sf), the fc2 scale stays in a2)
@@ -89,7 +102,7 @@ void orc_expert_ffn(const orc_problem* p, const orc_inputs* in, int32_t e_local,
 void orc_expert_down_nvfp4(const orc_problem* p, const orc_inputs* in, int32_t e_local,
                            const uint8_t* hq, const uint8_t* hsf, double* y);
 
-/* decoded activation row of token t */
+/* decoded activation row of token t, times per_token_scale[t] when given */
 void orc_xhat(const orc_problem* p, const orc_inputs* in, int64_t t, double* xhat);
 
 /* Whole forward for a list of tokens.  out_old_rows [ntok, H] bf16 bits is

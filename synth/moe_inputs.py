@@ -46,6 +46,8 @@ class MoEConfig:
     routing: str    # "softmax", "skewed" or "uniform"
     sample: int = 0  # 0: check every token; else number of sampled tokens
     seed: int = 0
+    act: str = "swiglu"           # FC1 activation, see ACTIVATIONS
+    per_token_scale: bool = False  # draw a per-token input row scale (w4a4)
 
     @property
     def routes(self) -> int:
@@ -57,6 +59,25 @@ class MoEConfig:
 
     def with_(self, **kw) -> "MoEConfig":
         return dataclasses.replace(self, **kw)
+
+
+# FC1 activations of the tests: name -> (type, parameters).  Type 0 = the
+# SwiGLU family, 1 = GeGLU with tanh, 2 = non-gated ReLU^2; parameter values
+# are picked so that the clamps and the tanh saturation are reached at the
+# tests' pre-activation scale (g, u ~ N(0, 0.02^2 H / gs^2), |g| up to ~1).
+ACTIVATIONS = {
+    "swiglu": (0, {}),
+    "swiglu_oai": (0, {"swiglu_alpha": 1.702, "swiglu_beta": 1.0, "swiglu_limit": 0.25}),
+    "situ": (0, {"situ_beta": 0.3}),
+    "situ_linear": (0, {"situ_beta": 0.3, "situ_linear_beta": 0.2}),
+    "geglu_tanh": (1, {}),
+    "relu2": (2, {}),
+}
+
+
+def activation_spec(cfg: "MoEConfig"):
+    """(type, parameter dict) of cfg's FC1 activation (configuration only)."""
+    return ACTIVATIONS[cfg.act]
 
 
 CONFIGS = {
@@ -91,14 +112,15 @@ class MoEInputs:
     x: Optional[torch.Tensor]              # bf16 [M, H]         (w4a16)
     x_q: Optional[torch.Tensor]            # uint8 [M, H/2]      (w4a4)
     x_sf: Optional[torch.Tensor]           # uint8 e4m3 [M, H/16](w4a4)
-    w1: torch.Tensor                       # uint8 [E, 2I, H/2]
-    w1_sf: torch.Tensor                    # uint8 [E, 2I, H/16]
+    w1: torch.Tensor                       # uint8 [E, 2I, H/2]  (ReLU^2: [E, I, H/2])
+    w1_sf: torch.Tensor                    # uint8 [E, 2I, H/16] (ReLU^2: [E, I, H/16])
     w1_alpha: torch.Tensor                 # fp32 [E]
     w2: torch.Tensor                       # uint8 [E, H, I/2]
     w2_sf: torch.Tensor                    # uint8 [E, H, I/16]
     w2_alpha: torch.Tensor                 # fp32 [E]
     fc2_input_scale: Optional[torch.Tensor]  # fp32 [1] (w4a4)
     sample_tokens: np.ndarray              # int64 sorted token ids to check
+    per_token_scale: Optional[torch.Tensor] = None  # fp32 [M] or None
 
     def to(self, device) -> "MoEInputs":
         def mv(t):
@@ -107,7 +129,7 @@ class MoEInputs:
             self, x=mv(self.x), x_q=mv(self.x_q), x_sf=mv(self.x_sf), w1=mv(self.w1),
             w1_sf=mv(self.w1_sf), w1_alpha=mv(self.w1_alpha), w2=mv(self.w2),
             w2_sf=mv(self.w2_sf), w2_alpha=mv(self.w2_alpha),
-            fc2_input_scale=mv(self.fc2_input_scale))
+            fc2_input_scale=mv(self.fc2_input_scale), per_token_scale=mv(self.per_token_scale))
 
 
 # --------------------------------------------------------------------------
@@ -234,8 +256,9 @@ def generate(cfg: MoEConfig, device="cpu", experts: Optional[int] = None) -> MoE
     del xf
 
     n_gen = E if experts is None else experts
-    w1 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
-    w1_sf = torch.empty(E, 2 * I, H // 16, dtype=torch.uint8, device=device)
+    rows1 = I if activation_spec(cfg)[0] == 2 else 2 * I   # ReLU^2 has no gate rows
+    w1 = torch.empty(E, rows1, H // 2, dtype=torch.uint8, device=device)
+    w1_sf = torch.empty(E, rows1, H // 16, dtype=torch.uint8, device=device)
     w2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
     w2_sf = torch.empty(E, H, I // 16, dtype=torch.uint8, device=device)
     gs1 = torch.ones(E, dtype=torch.float32, device=device)
@@ -244,7 +267,7 @@ def generate(cfg: MoEConfig, device="cpu", experts: Optional[int] = None) -> MoE
     g = torch.Generator(device=device)
     for e in range(n_gen):
         g.manual_seed(base1 + e)
-        W = torch.randn(2 * I, H, generator=g, device=device, dtype=torch.float32) * 0.02
+        W = torch.randn(rows1, H, generator=g, device=device, dtype=torch.float32) * 0.02
         w1[e], w1_sf[e], gs1[e] = quantize_nvfp4(W)
         g.manual_seed(base2 + e)
         W = torch.randn(H, I, generator=g, device=device, dtype=torch.float32) * 0.02
@@ -273,6 +296,11 @@ def generate(cfg: MoEConfig, device="cpu", experts: Optional[int] = None) -> MoE
         sample = np.sort(srng.choice(M, size=cfg.sample, replace=False)).astype(np.int64)
     else:
         sample = np.arange(M, dtype=np.int64)
+    pts = None
+    if cfg.per_token_scale:
+        # per-token row scales 2^U(-1, 1), from their own sub-stream of x's seed
+        prng = np.random.Generator(np.random.PCG64(ss_x.spawn(1)[0]))
+        pts = torch.from_numpy(np.exp2(prng.uniform(-1.0, 1.0, M)).astype(np.float32)).to(device)
 
     return MoEInputs(
         cfg=cfg,
@@ -281,4 +309,4 @@ def generate(cfg: MoEConfig, device="cpu", experts: Optional[int] = None) -> MoE
         x=x, x_q=x_q, x_sf=x_sf,
         w1=w1, w1_sf=w1_sf, w1_alpha=a1.to(torch.float32).contiguous(),
         w2=w2, w2_sf=w2_sf, w2_alpha=a2.to(torch.float32).contiguous(),
-        fc2_input_scale=fc2, sample_tokens=sample)
+        fc2_input_scale=fc2, sample_tokens=sample, per_token_scale=pts)

@@ -120,3 +120,62 @@ def test_null_pointers_rejected_before_any_launch(lib):
         fm.moe_route_sort(p, None, None, None, None, None, None, None, ws, stream=0)
     assert ei.value.status == fm.ERR_INVALID_ARG
     assert fm.status_string(fm.ERR_DEVICE_TIMEOUT).startswith("device error")
+
+
+@pytest.mark.parametrize("act", [
+    dict(type=3),                                                  # unknown type
+    dict(type=fm.ACT_GEGLU_TANH, flags=fm.ACT_F_SITU, situ_beta=1.0),  # flags only with SwiGLU
+    dict(flags=fm.ACT_F_SWIGLU_OAI | fm.ACT_F_SITU, situ_beta=1.0, swiglu_limit=1.0),
+    dict(flags=fm.ACT_F_SITU_LINEAR, situ_linear_beta=1.0),         # linear clamp needs SiTU
+    dict(flags=fm.ACT_F_SITU, situ_beta=0.0),
+    dict(flags=fm.ACT_F_SITU | fm.ACT_F_SITU_LINEAR, situ_beta=1.0, situ_linear_beta=float("inf")),
+    dict(flags=fm.ACT_F_SWIGLU_OAI, swiglu_alpha=float("nan"), swiglu_limit=1.0),
+    dict(flags=fm.ACT_F_SWIGLU_OAI, swiglu_limit=0.0),
+    dict(flags=8),
+])
+def test_invalid_activations_are_rejected(lib, act):
+    a = fm.Activation()
+    for k, v in act.items():
+        setattr(a, k, v)
+    p = fm.problem(8, 256, 256, 8, 2, act=a)
+    with pytest.raises(fm.Fp4MoeError) as ei:
+        fm.route_tile(p)
+    assert ei.value.status == fm.ERR_INVALID_ARG
+
+
+def test_activation_helper_and_relu2_sizes(lib):
+    assert fm.activation().flags == 0
+    a = fm.activation(swiglu_alpha=1.702, swiglu_beta=1.0, swiglu_limit=7.0)
+    assert a.flags == fm.ACT_F_SWIGLU_OAI
+    a = fm.activation(situ_beta=2.0, situ_linear_beta=1.0)
+    assert a.flags == fm.ACT_F_SITU | fm.ACT_F_SITU_LINEAR
+    for T in (16, 32):
+        p = fm.problem(8, 7168, 2048, 256, 8, route_tile=T, act=fm.activation(fm.ACT_RELU2))
+        assert fm.route_tile(p) == T
+        assert fm.prepared_weight_size(p, 1) == 256 * 8 * 56 * 18432     # I/256 blocks, no gate rows
+        p = fm.problem(8, 7168, 384, 256, 8, route_tile=T, act=fm.activation(fm.ACT_RELU2))
+        assert fm.prepared_weight_size(p, 1) == 256 * 2 * 56 * 18432     # a half-empty last block
+        g = fm.problem(8, 7168, 2048, 256, 8, route_tile=T, act=fm.activation(fm.ACT_GEGLU_TANH))
+        assert fm.prepared_weight_size(g, 1) == 256 * 16 * 56 * 18432
+
+
+def test_per_token_scale_needs_the_slot_map(lib):
+    p = fm.problem(8, 256, 256, 8, 2, mode=fm.W4A4)
+
+    class Fake:
+        def __init__(self, addr, n):
+            self.addr, self.n = addr, n
+
+        def data_ptr(self):
+            return self.addr
+
+        def numel(self):
+            return self.n
+
+        def element_size(self):
+            return 1
+    dev = Fake(1 << 20, 1 << 24)                      # an aligned address; never dereferenced
+    with pytest.raises(fm.Fp4MoeError) as ei:
+        fm.moe_gemm1_swiglu(p, dev, dev, None, dev, dev, dev, dev, dev, dev, dev, dev, dev,
+                            stream=0, per_token_scale=dev)
+    assert ei.value.status == fm.ERR_INVALID_ARG

@@ -259,6 +259,71 @@ def test_accumulate_false_equals_zero_seed_bitwise():
     check_out(f64(c), exact, 5e-3, what="accumulate")
 
 
+# ------------------------------------------------------------------ FC1 activations
+
+@pytest.mark.parametrize("act", ["swiglu_oai", "situ", "situ_linear", "geglu_tanh", "relu2"])
+@pytest.mark.parametrize("T", [16, 32])   # warp-MMA kernel, tcgen05 kernel
+def test_activation_variants_match_oracle(act, T):
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(act=act)
+    inp, p, B, orc = _setup(cfg, T)
+    out = _fused(inp, B, rsf=0.5)
+    _, exact, _ = orc.forward(rsf=0.5, nthreads=NTHREADS)
+    check_out(f64(out), exact, 5e-3, what="%s T=%d" % (act, T))
+
+
+@pytest.mark.parametrize("T", [16, 32])
+def test_relu2_partial_row_block_and_staged_h(T):
+    # I = 384: the second 256-row block of the non-gated FC1 is half empty
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(act="relu2", I=384)
+    inp, p, B, orc = _setup(cfg, T)
+    out = _fused(inp, B)
+    _, exact, _ = orc.forward(nthreads=NTHREADS)
+    check_out(f64(out), exact, 5e-3, what="relu2 I=384 T=%d" % T)
+    B.route(inp.token_selected_experts.cuda())
+    h, _ = B.gemm1(inp.x, None, inp.w1_alpha, gather=True)
+    torch.cuda.synchronize()
+    p2e = B.p2e.cpu().numpy()
+    hv = f64(h)
+    for s in np.nonzero(p2e >= 0)[0][:12]:
+        t, j = divmod(int(p2e[s]), cfg.top_k)
+        st = orc.expert_ffn(int(inp.token_selected_experts[t, j]), t)
+        check_out(hv[s], st["h_in"], 5e-3, what="relu2 h slot %d" % s)
+
+
+def test_relu2_prepared_weights_decode_exactly():
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(act="relu2", I=384)
+    inp = synth.generate(cfg, device="cuda")
+    for T in (16, 32):
+        p = problem_for(cfg, T)
+        B = MoEBuffers(p).prepare(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+        out = torch.zeros(cfg.E, cfg.I, cfg.H, dtype=torch.bfloat16, device="cuda")
+        fm.debug_decode_prepared(p, 1, B.w1p, out)
+        torch.cuda.synchronize()
+        assert np.array_equal(f64(out), dequant_np(inp.w1.cpu().numpy(), inp.w1_sf.cpu().numpy()))
+
+
+@pytest.mark.parametrize("act", ["swiglu", "relu2", "geglu_tanh"])
+def test_w4a4_activation_and_per_token_scale(act):
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a4", act=act, per_token_scale=True)
+    inp, p, B, orc = _setup(cfg, 32)
+    ids = inp.token_selected_experts.cuda()
+    out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device="cuda")
+    B.forward(inp.x_q, inp.x_sf, ids, inp.token_final_scales.cuda(), inp.w1_alpha, inp.w2_alpha,
+              out, inp.fc2_input_scale, per_token_scale=inp.per_token_scale)
+    torch.cuda.synchronize()
+    assert fm.read_error(B.fused_ws) == 0
+    _, exact, _ = orc.forward(nthreads=NTHREADS)
+    check_out(f64(out), exact, 2e-2, strict=False, what="w4a4 %s per-token scale" % act)
+
+
+def test_decode_size_geglu_full():
+    cfg = synth.CONFIGS["decode_w4a16"].with_(act="geglu_tanh")
+    inp, p, B, orc = _setup(cfg, 16)
+    out = _fused(inp, B)
+    _, exact, _ = orc.forward(nthreads=NTHREADS)
+    check_out(f64(out), exact, 5e-3, what="decode geglu")
+
+
 # ------------------------------------------------------------------ atomic finalize
 
 ATOMIC = fm.FINALIZE_ATOMIC
