@@ -320,6 +320,10 @@ def run_ours(args, rank, world, local):
     act1 = M * H * 2 if cfg.mode == "w4a16" else M * H // 2 + M * H // 16
     g1_bytes = touched * w1_bytes_per_expert + act1 + R * I * 2
     g1_ms = kernels["gemm1_swiglu"]
+    g1_flops = 4.0 * R * H * I
+    # the roofline of GEMM1 is the HBM rate below the ridge (peak flops / peak
+    # bytes) and the BF16 tensor rate above it (the MMAs run on decoded BF16)
+    tensor_bound = g1_flops / g1_bytes > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     achieved = g1_bytes / (g1_ms * 1e-3) / 1e9
     step_bytes = touched * (w1_bytes_per_expert + w2_bytes_per_expert) + act1 + M * H * 2
     traffic_path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
@@ -339,14 +343,19 @@ def run_ours(args, rank, world, local):
                        "per step vs 126 MB L2" % (step_bytes / 1e9), parallelism="replicas" if world > 1 else "1 GPU"),
         "tflops": world * cfg.flops() / (ms * 1e-3) / 1e12,
         "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
-        "roofline": {"kernel": ("moe_gemv_kernel<0> (GEMM1 + SwiGLU, warp MMA)"
-                               if cfg.mode == "w4a16" and T == 16 else
-                               "moe_gemm_kernel<%d, %d> (GEMM1 + SwiGLU, tcgen05)"
-                               % (T, 0 if cfg.mode == "w4a16" else 1)), "bound": "hbm",
-                     "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "algorithmic_bytes": g1_bytes, "peak_source": peak_src,
-                     "touched_experts": touched},
+        "roofline": dict({"kernel": ("moe_gemv_kernel<0> (GEMM1 + SwiGLU, warp MMA)"
+                                     if cfg.mode == "w4a16" and T == 16 else
+                                     "moe_gemm_kernel<%d, %d> (GEMM1 + SwiGLU, tcgen05)"
+                                     % (T, 0 if cfg.mode == "w4a16" else 1))},
+                         **({"bound": "tensor", "achieved": g1_flops / (g1_ms * 1e-3) / 1e12,
+                             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": g1_flops / (g1_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                             "algorithmic_flops": g1_flops}
+                            if tensor_bound else
+                            {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                             "algorithmic_bytes": g1_bytes}),
+                         traffic=traffic, peak_source=peak_src, touched_experts=touched),
         "kernels_ms": kernels,
         "atomic_finalize": {"ms_per_step": ms_atomic, "value": tokens_per_s(world, cfg.M, ms_atomic),
                             "unit": UNIT},
