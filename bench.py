@@ -236,18 +236,8 @@ def run_ours(args, rank, world, local):
     kernels = {}
     names = ["route_sort", "permute", "gemm1_swiglu", "gemm2", "finalize"]
     ev = {n: [] for n in names}
-    if cfg.mode == "w4a16":
-        px, pxsf = torch.zeros(B.S, cfg.H, dtype=torch.bfloat16, device=dev), None
-    else:
-        px = torch.zeros(B.S, cfg.H // 2, dtype=torch.uint8, device=dev)
-        pxsf = torch.zeros(B.S, cfg.H // 16, dtype=torch.uint8, device=dev)
-
-    if cfg.mode == "w4a16":
-        h = torch.zeros(B.S, cfg.I, dtype=torch.bfloat16, device=dev)
-        hsf = None
-    else:
-        h = torch.zeros(B.S, cfg.I // 2, dtype=torch.uint8, device=dev)
-        hsf = torch.zeros(B.S, cfg.I // 16, dtype=torch.uint8, device=dev)
+    px, pxsf = B.alloc_permuted()
+    h, hsf = B.alloc_h()
     y = torch.zeros(B.S, cfg.H, dtype=torch.float32, device=dev)
 
     def launch(name):
@@ -315,9 +305,11 @@ def run_ours(args, rank, world, local):
     ids_np = inp.token_selected_experts.numpy()
     touched = len(np.unique(ids_np))
     H, I, M, R = cfg.H, cfg.I, cfg.M, cfg.routes
-    w1_bytes_per_expert = 2 * I * H // 2 + 2 * I * H // 16
-    w2_bytes_per_expert = H * I // 2 + H * I // 16
-    act1 = M * H * 2 if cfg.mode == "w4a16" else M * H // 2 + M * H // 16
+    sb = 32 if cfg.mode == "w4a8" else 16       # weight scale block: MXFP4 / NVFP4
+    w1_bytes_per_expert = 2 * I * H // 2 + 2 * I * H // sb
+    w2_bytes_per_expert = H * I // 2 + H * I // sb
+    act1 = {"w4a16": M * H * 2, "w4a4": M * H // 2 + M * H // 16,
+            "w4a8": M * H + M * H // 32}[cfg.mode]
     g1_bytes = touched * w1_bytes_per_expert + act1 + R * I * 2
     g1_ms = kernels["gemm1_swiglu"]
     g1_flops = 4.0 * R * H * I
@@ -337,7 +329,8 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": tokens_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.mode == "w4a16" else "nvfp4->bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"w4a16": "bf16", "w4a4": "nvfp4->bf16", "w4a8": "mxfp8->bf16"}[cfg.mode],
         "data": "synthetic (seeded generator; random NVFP4 weights)",
         "config": dict(workload_config(cfg, T), l2="inputs larger than L2: %.2f GB of weights "
                        "per step vs 126 MB L2" % (step_bytes / 1e9), parallelism="replicas" if world > 1 else "1 GPU"),
@@ -346,7 +339,7 @@ def run_ours(args, rank, world, local):
         "roofline": dict({"kernel": ("moe_gemv_kernel<0> (GEMM1 + SwiGLU, warp MMA)"
                                      if cfg.mode == "w4a16" and T == 16 else
                                      "moe_gemm_kernel<%d, %d> (GEMM1 + SwiGLU, tcgen05)"
-                                     % (T, 0 if cfg.mode == "w4a16" else 1))},
+                                     % (T, {"w4a16": 0, "w4a4": 1, "w4a8": 6}[cfg.mode]))},
                          **({"bound": "tensor", "achieved": g1_flops / (g1_ms * 1e-3) / 1e12,
                              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                              "frac": g1_flops / (g1_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
@@ -363,7 +356,7 @@ def run_ours(args, rank, world, local):
                 "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),
         # per fused step: routing (1 kernel up to 4096 routes, else 3), x in slot
-        # order, GEMM1, the w4a4 h -> BF16 expansion, GEMM2, finalize
+        # order, GEMM1, the w4a4 / w4a8 h -> BF16 expansion, GEMM2, finalize
         "gpu_launches": args.steps * ((1 if cfg.routes <= 4096 else 3) + 1 + 3 +
                                       (0 if cfg.mode == "w4a16" else 1)),
     }

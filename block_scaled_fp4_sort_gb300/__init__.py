@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp4moe.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_DEVICE, ERR_DEVICE_TIMEOUT = range(7)
-W4A16, W4A4 = 0, 1
+W4A16, W4A4, W4A8 = 0, 1, 2
 FINALIZE_DETERMINISTIC, FINALIZE_ATOMIC = 0, 1
 
 ABI_FUNCTIONS = (
@@ -25,7 +25,7 @@ ABI_FUNCTIONS = (
     "fp4moe_prepared_weight_size", "fp4moe_read_error", "fp4moe_clear_error",
     "fp4moe_prepare_weights", "moe_route_sort", "moe_route_sort_noalloc", "moe_permute", "moe_gemm1_swiglu", "moe_gemm2",
     "moe_finalize", "fused_moe_forward", "fp4moe_debug_quantize_nvfp4",
-    "fp4moe_debug_decode_prepared",
+    "fp4moe_debug_quantize_mxfp8", "fp4moe_debug_decode_prepared",
 )
 
 
@@ -113,6 +113,7 @@ def lib() -> ctypes.CDLL:
             "fused_moe_forward": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp,
                                         vp, sz, vp]),
             "fp4moe_debug_quantize_nvfp4": (i32, [vp, i64, vp, vp, vp, vp]),
+            "fp4moe_debug_quantize_mxfp8": (i32, [vp, i64, vp, vp, vp]),
             "fp4moe_debug_decode_prepared": (i32, [P, i32, vp, vp, vp]),
         }
         for name, (res, args) in sig.items():
@@ -268,6 +269,11 @@ def fused_moe_forward(p: Problem, x, x_sf, token_selected_experts, token_final_s
                                    float(routed_scaling_factor), int(bool(accumulate)),
                                    int(finalize_mode), _p(out), _p(workspace), _nbytes(workspace),
                                    _stream(stream)), "fused_moe_forward")
+
+
+def debug_quantize_mxfp8(x, q, sf, stream=None):
+    _check(lib().fp4moe_debug_quantize_mxfp8(_p(x), x.numel(), _p(q), _p(sf), _stream(stream)),
+           "fp4moe_debug_quantize_mxfp8")
 
 
 def debug_quantize_nvfp4(x, scale, q, sf, stream=None):

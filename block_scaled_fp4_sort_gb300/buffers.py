@@ -8,7 +8,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (W4A4, W4A16, FINALIZE_DETERMINISTIC, activation, fused_moe_forward,
+from . import (W4A4, W4A8, W4A16, FINALIZE_DETERMINISTIC, activation, fused_moe_forward,
                gemm_workspace_size, max_permuted_slots, moe_finalize, moe_gemm1_swiglu, moe_gemm2,
                moe_permute, moe_route_sort, prepare_weights, prepared_weight_size, problem,
                route_tile, route_workspace_size, workspace_size)
@@ -69,26 +69,34 @@ class MoEBuffers:
         moe_route_sort(self.p, ids, self.e2p, self.p2e, self.tile_expert, self.tile_mn,
                        self.num_tiles, self.counts, self.route_ws, stream)
 
-    def permute(self, x, x_sf=None, stream=None):
-        p = self.p
+    def _rows(self, K):
+        """Zeroed [S, K] activation rows and scales in the problem's format."""
+        p, d, S = self.p, self.device, self.S
         if p.mode == W4A16:
-            px = torch.zeros(self.S, p.hidden, dtype=torch.bfloat16, device=self.device)
-            psf = None
-        else:
-            px = torch.zeros(self.S, p.hidden // 2, dtype=torch.uint8, device=self.device)
-            psf = torch.zeros(self.S, p.hidden // 16, dtype=torch.uint8, device=self.device)
-        moe_permute(p, x, x_sf, self.p2e, self.num_tiles, px, psf, stream)
+            return torch.zeros(S, K, dtype=torch.bfloat16, device=d), None
+        if p.mode == W4A8:   # MXFP8: E4M3 bytes + E8M0 block-32 scales
+            return (torch.zeros(S, K, dtype=torch.uint8, device=d),
+                    torch.zeros(S, K // 32, dtype=torch.uint8, device=d))
+        return (torch.zeros(S, K // 2, dtype=torch.uint8, device=d),     # NVFP4
+                torch.zeros(S, K // 16, dtype=torch.uint8, device=d))
+
+    def alloc_permuted(self):
+        """Buffers for x in slot order (moe_permute's output)."""
+        return self._rows(self.p.hidden)
+
+    def alloc_h(self):
+        """Buffers for GEMM1's output h."""
+        return self._rows(self.p.inter)
+
+    def permute(self, x, x_sf=None, stream=None):
+        px, psf = self.alloc_permuted()
+        moe_permute(self.p, x, x_sf, self.p2e, self.num_tiles, px, psf, stream)
         return px, psf
 
     def gemm1(self, a, a_sf, w1_alpha, fc2_input_scale=None, gather=True, stream=None,
               per_token_scale=None):
         p = self.p
-        if p.mode == W4A16:
-            h = torch.zeros(self.S, p.inter, dtype=torch.bfloat16, device=self.device)
-            hsf = None
-        else:
-            h = torch.zeros(self.S, p.inter // 2, dtype=torch.uint8, device=self.device)
-            hsf = torch.zeros(self.S, p.inter // 16, dtype=torch.uint8, device=self.device)
+        h, hsf = self.alloc_h()
         moe_gemm1_swiglu(p, a, a_sf, self.p2e if gather else None, self.w1p, w1_alpha,
                          fc2_input_scale, self.tile_expert, self.tile_mn, self.num_tiles, h, hsf,
                          self.gemm1_ws, stream, per_token_scale=per_token_scale)
@@ -121,5 +129,5 @@ def problem_for(cfg, route_tile_=0, num_local_experts=0, local_expert_offset=0):
     import synth
     kind, params = synth.activation_spec(cfg)
     return problem(cfg.M, cfg.H, cfg.I, cfg.E, cfg.top_k, num_local_experts, local_expert_offset,
-                   route_tile_, W4A4 if cfg.mode == "w4a4" else W4A16,
+                   route_tile_, {"w4a16": W4A16, "w4a4": W4A4, "w4a8": W4A8}[cfg.mode],
                    activation(kind, **params))

@@ -63,6 +63,16 @@ __host__ __device__ constexpr uint32_t prep_scale_code(uint32_t b) {
   return ((12u + p) << 3) | ((m << (3u - p)) & 7u);
 }
 
+// MXFP4 (E8M0 block-32 scales, w4a8) -> prepared scale code of one 16-element
+// half block: 2^(e - 127) * 2^118 = 2^(e - 9) is a code for e in [106, 136]
+// (c = 8e - 848); e = 255 (NaN) and an out-of-range e under non-zero codes
+// give the NaN code, an out-of-range e over zero codes any finite code.
+__host__ __device__ constexpr uint32_t prep_scale_code_mx(uint32_t e, bool zero_codes) {
+  return e == 255u ? 0xFFu
+         : (e >= 106u && e <= 136u) ? 8u * e - 848u
+         : zero_codes ? 0x70u : 0xFFu;
+}
+
 // Moves the sign and the zero of scale byte b into linear E2M1 codes
 // (sign_bits: 0x88 for one byte of two codes, 0x88888888 for a word).
 __host__ __device__ constexpr uint32_t prep_fix_codes(uint32_t v, uint32_t b, uint32_t sign_bits) {

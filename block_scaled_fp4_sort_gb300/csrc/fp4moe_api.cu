@@ -40,7 +40,8 @@ fp4moe_status validate(const fp4moe_problem* p, Shape* s) {
       p->local_expert_offset + EL > p->num_experts)
     return FP4MOE_ERR_INVALID_ARG;
   if (p->top_k > p->num_experts) return FP4MOE_ERR_INVALID_ARG;
-  if (p->mode != FP4MOE_W4A16 && p->mode != FP4MOE_W4A4) return FP4MOE_ERR_INVALID_ARG;
+  if (p->mode != FP4MOE_W4A16 && p->mode != FP4MOE_W4A4 && p->mode != FP4MOE_W4A8)
+    return FP4MOE_ERR_INVALID_ARG;
   if (EL > kMaxLocalExperts) return FP4MOE_ERR_UNSUPPORTED;
   const int64_t R = (int64_t)p->num_tokens * p->top_k;
   int32_t T = p->route_tile;
@@ -105,7 +106,7 @@ RouteWs route_ws(const Shape& s) {
 // gathered rows for the tcgen05 GEMM) | warp-MMA K-split scratch
 size_t gemm_split_offset(const Shape& s, int which) {
   size_t b = kWsHeader;
-  if (s.mode == FP4MOE_W4A4 || (which == 1 && !fragment_layout(s))) {
+  if (s.mode != FP4MOE_W4A16 || (which == 1 && !fragment_layout(s))) {
     const int64_t rows = which == 1 ? std::max(s.M, s.S) : s.S;
     const int64_t K = which == 1 ? s.H : s.I;
     b += up((size_t)rows * K * 2);
@@ -133,10 +134,11 @@ FusedWs fused_ws(const Shape& s) {
   w.route_scratch = o; o = up(o + route_scratch_bytes(s));
   if (s.mode == FP4MOE_W4A16) {
     w.h = o; o = up(o + (size_t)s.S * s.I * 2);
-  } else {
-    w.h = o; o = up(o + (size_t)s.S * s.I / 2);
-    w.h_sf = o; o = up(o + (size_t)s.S * s.I / 16);
-    w.deq2 = o; o = up(o + (size_t)s.S * s.I * 2);     // h in BF16 (exact)
+  } else {  // NVFP4 (w4a4) or MXFP8 (w4a8) h, and h expanded to BF16 for GEMM2
+    const bool mx = s.mode == FP4MOE_W4A8;
+    w.h = o; o = up(o + (size_t)s.S * s.I / (mx ? 1 : 2));
+    w.h_sf = o; o = up(o + (size_t)s.S * s.I / (mx ? 32 : 16));
+    w.deq2 = o; o = up(o + (size_t)s.S * s.I * 2);
   }
   // fp32 route storage; until GEMM2 it holds x in slot order (BF16, 2 S H
   // bytes) for the tcgen05 GEMM1, in atomic mode the fp32 [M, H] accumulator
@@ -152,6 +154,7 @@ inline int* err_word(void* ws) { return static_cast<int*>(ws); }
 
 // GEMM1 epilogue for the activation and the FC1 output format
 Epilogue gemm1_epilogue(const Shape& s) {
+  if (s.mode == FP4MOE_W4A8) return gated(s) ? kEpiSwigluMxfp8 : kEpiRelu2Mxfp8;
   const bool w4 = s.mode == FP4MOE_W4A4;
   if (!gated(s)) return w4 ? kEpiRelu2Nvfp4 : kEpiRelu2Bf16;
   return w4 ? kEpiSwigluNvfp4 : kEpiSwigluBf16;
@@ -263,7 +266,7 @@ fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, const uint8_t*
   if (st != FP4MOE_OK) return st;
   if ((s.M > 0 && !ok_ptr(x)) || !ok_ptr(p2e) || !ok_ptr(num_tiles) || !ok_ptr(px))
     return FP4MOE_ERR_INVALID_ARG;
-  if (s.mode == FP4MOE_W4A4 && ((s.M > 0 && !ok_ptr(x_sf)) || !ok_ptr(px_sf)))
+  if (s.mode != FP4MOE_W4A16 && ((s.M > 0 && !ok_ptr(x_sf)) || !ok_ptr(px_sf)))
     return FP4MOE_ERR_INVALID_ARG;
   return cuda_status(launch_permute(s, x, x_sf, p2e, num_tiles, px, px_sf,
                                     static_cast<cudaStream_t>(stream), false));
@@ -278,7 +281,8 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   Shape s;
   fp4moe_status st = validate(p, &s);
   if (st != FP4MOE_OK) return st;
-  const bool w4 = s.mode == FP4MOE_W4A4;
+  const bool w4 = s.mode != FP4MOE_W4A16;   // packed activations: NVFP4 (w4a4) or MXFP8 (w4a8)
+  const bool mx = s.mode == FP4MOE_W4A8;
   if (!ok_ptr(w1_prepared) || !ok_ptr(w1_alpha) || !ok_ptr(tile_expert) || !ok_ptr(tile_mn) ||
       !ok_ptr(num_tiles) || !ok_ptr(h) || !ok_ptr(workspace) || (gather_rows && !ok_ptr(gather_rows)))
     return FP4MOE_ERR_INVALID_ARG;
@@ -287,7 +291,9 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
     return FP4MOE_ERR_INVALID_ARG;
   const int64_t act_rows = gather_rows ? s.M : s.S;
   if (act_rows > 0 && !ok_ptr(a)) return FP4MOE_ERR_INVALID_ARG;
-  if (w4 && ((act_rows > 0 && !ok_ptr(a_sf)) || !ok_ptr(h_sf) || !ok_ptr(fc2_input_scale)))
+  if (w4 && ((act_rows > 0 && !ok_ptr(a_sf)) || !ok_ptr(h_sf))) return FP4MOE_ERR_INVALID_ARG;
+  // fc2_input_scale: the w4a4 GEMM2 input scale; none for w4a8 (MX scales)
+  if (s.mode == FP4MOE_W4A4 ? !ok_ptr(fc2_input_scale) : (mx && fc2_input_scale != nullptr))
     return FP4MOE_ERR_INVALID_ARG;
   if (workspace_bytes < gemm_ws_bytes(s, 1)) return FP4MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -301,7 +307,7 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   if (w4) {
     e = launch_dequant_rows(static_cast<const uint8_t*>(a), a_sf, slot_order ? s.S : act_rows, s.H,
                             gather_rows && !slot_order ? nullptr : num_tiles, s.T, ws + kWsHeader,
-                            cs, false, slot_order ? gather_rows : nullptr, s.K, s.M);
+                            cs, false, slot_order ? gather_rows : nullptr, s.K, s.M, mx);
     act = ws + kWsHeader;
   } else if (slot_order) {
     e = launch_permute(s, a, nullptr, gather_rows, num_tiles, ws + kWsHeader, nullptr, cs, false);
@@ -336,7 +342,7 @@ fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h
   Shape s;
   fp4moe_status st = validate(p, &s);
   if (st != FP4MOE_OK) return st;
-  const bool w4 = s.mode == FP4MOE_W4A4;
+  const bool w4 = s.mode != FP4MOE_W4A16;   // packed h: NVFP4 (w4a4) or MXFP8 (w4a8)
   if (!ok_ptr(h) || !ok_ptr(w2_prepared) || !ok_ptr(w2_alpha) || !ok_ptr(tile_expert) ||
       !ok_ptr(tile_mn) || !ok_ptr(num_tiles) || !ok_ptr(y) || !ok_ptr(workspace) ||
       (w4 && !ok_ptr(h_sf)))
@@ -348,7 +354,8 @@ fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h
   if (w4) {
     act = ws + kWsHeader;
     cudaError_t e = launch_dequant_rows(static_cast<const uint8_t*>(h), h_sf, s.S, s.I, num_tiles,
-                                        s.T, ws + kWsHeader, cs, false);
+                                        s.T, ws + kWsHeader, cs, false, nullptr, 1, 0,
+                                        s.mode == FP4MOE_W4A8);
     if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
   }
   GemmLaunch g = {};
@@ -387,7 +394,8 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   Shape s;
   fp4moe_status st = validate(p, &s);
   if (st != FP4MOE_OK) return st;
-  const bool w4 = s.mode == FP4MOE_W4A4;
+  const bool w4 = s.mode != FP4MOE_W4A16;   // packed activations
+  const bool mx = s.mode == FP4MOE_W4A8;
   if (finalize_mode != FP4MOE_FINALIZE_DETERMINISTIC && finalize_mode != FP4MOE_FINALIZE_ATOMIC)
     return FP4MOE_ERR_INVALID_ARG;
   if (!ok_ptr(w1_prepared) || !ok_ptr(w1_alpha) || !ok_ptr(w2_prepared) || !ok_ptr(w2_alpha) ||
@@ -395,7 +403,9 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
     return FP4MOE_ERR_INVALID_ARG;
   if (s.M > 0 && (!ok_ptr(x) || !ok_ptr(ids) || !ok_ptr(wts) || !ok_ptr(out)))
     return FP4MOE_ERR_INVALID_ARG;
-  if (w4 && ((s.M > 0 && !ok_ptr(x_sf)) || !ok_ptr(fc2_input_scale))) return FP4MOE_ERR_INVALID_ARG;
+  if (w4 && s.M > 0 && !ok_ptr(x_sf)) return FP4MOE_ERR_INVALID_ARG;
+  if (s.mode == FP4MOE_W4A4 ? !ok_ptr(fc2_input_scale) : (mx && fc2_input_scale != nullptr))
+    return FP4MOE_ERR_INVALID_ARG;
   if (per_token_scale && s.M > 0 && !ok_ptr(per_token_scale)) return FP4MOE_ERR_INVALID_ARG;
   const FusedWs L = fused_ws(s);
   if (workspace_bytes < L.total) return FP4MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -421,7 +431,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   const void* xb = ws + L.y;
   if (e == cudaSuccess)
     e = w4 ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
-                                 ws + L.y, cs, true, p2e, s.K, s.M)
+                                 ws + L.y, cs, true, p2e, s.K, s.M, mx)
            : launch_permute(s, x, nullptr, p2e, nt, ws + L.y, nullptr, cs, true, false);
   GemmLaunch g1 = {};
   g1.which = 1;
@@ -444,7 +454,8 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   if (e == cudaSuccess) e = launch_gemm(s, g1, cs, true);
   const void* hin = ws + L.h;
   if (e == cudaSuccess && w4) {
-    e = launch_dequant_rows(ws + L.h, ws + L.h_sf, s.S, s.I, nt, s.T, ws + L.deq2, cs, true);
+    e = launch_dequant_rows(ws + L.h, ws + L.h_sf, s.S, s.I, nt, s.T, ws + L.deq2, cs, true,
+                            nullptr, 1, 0, mx);
     hin = ws + L.deq2;
   }
   if (e == cudaSuccess && atomic) e = launch_seed_acc(s, out, accumulate ? 1 : 0, acc, cs, true);
@@ -476,6 +487,13 @@ fp4moe_status fp4moe_debug_quantize_nvfp4(const float* in, int64_t n, const floa
   if (n < 0 || n % 16 != 0 || (n > 0 && (!ok_ptr(in) || !ok_ptr(q) || !ok_ptr(sf))) || !scale)
     return FP4MOE_ERR_INVALID_ARG;
   return cuda_status(launch_debug_quantize(in, n, scale, q, sf, static_cast<cudaStream_t>(stream)));
+}
+
+fp4moe_status fp4moe_debug_quantize_mxfp8(const float* in, int64_t n, uint8_t* q, uint8_t* sf,
+                                          void* stream) {
+  if (n < 0 || n % 32 != 0 || (n > 0 && (!ok_ptr(in) || !ok_ptr(q) || !ok_ptr(sf))))
+    return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_debug_quantize_mx(in, n, q, sf, static_cast<cudaStream_t>(stream)));
 }
 
 fp4moe_status fp4moe_debug_decode_prepared(const fp4moe_problem* p, int32_t which,

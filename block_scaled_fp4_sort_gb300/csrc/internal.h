@@ -81,7 +81,9 @@ cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaSt
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
                                 const int32_t* row_limit_tiles, int64_t T, void* out,
                                 cudaStream_t st, bool pdl, const int32_t* gather = nullptr,
-                                int64_t top_k = 1, int64_t src_rows = 0);
+                                int64_t top_k = 1, int64_t src_rows = 0, bool mx = false);
+cudaError_t launch_debug_quantize_mx(const float* in, int64_t n, uint8_t* q, uint8_t* sf,
+                                     cudaStream_t st);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl);
 cudaError_t launch_debug_quantize(const float* in, int64_t n, const float* scale, uint8_t* q,
                                   uint8_t* sf, cudaStream_t st);
@@ -94,10 +96,10 @@ cudaError_t launch_debug_decode(const Shape& s, int which, const uint8_t* prepar
 
 // ---- grouped GEMM (moe_gemm.cu) ----
 // GEMM epilogues: gated activation -> BF16 h / NVFP4 h; fp32 y; atomic
-// finalize; non-gated ReLU^2 -> BF16 h / NVFP4 h
+// finalize; non-gated ReLU^2 -> BF16 h / NVFP4 h; gated / ReLU^2 -> MXFP8 h
 enum Epilogue {
   kEpiSwigluBf16 = 0, kEpiSwigluNvfp4 = 1, kEpiPlainBf16 = 2, kEpiAtomicFinal = 3,
-  kEpiRelu2Bf16 = 4, kEpiRelu2Nvfp4 = 5
+  kEpiRelu2Bf16 = 4, kEpiRelu2Nvfp4 = 5, kEpiSwigluMxfp8 = 6, kEpiRelu2Mxfp8 = 7
 };
 
 struct GemmLaunch {

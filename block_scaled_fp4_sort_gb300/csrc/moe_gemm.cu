@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else if (EPI == kEpiRelu2Bf16 || EPI == kEpiRelu2Nvfp4) {
+      } else if (EPI == kEpiRelu2Bf16 || EPI == kEpiRelu2Nvfp4 || EPI == kEpiRelu2Mxfp8) {
         // non-gated FC1: both 128-row tiles are outputs, feature n per thread
         const int64_t n = (int64_t)f * 256 + tile * 128 + row;
         const float fs = EPI == kEpiRelu2Nvfp4 ? a.fc2_scale[0] : 0.0f;
@@ -376,6 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float hv = s < mn ? relu2(__uint_as_float(v[i]) * scale * token_factor(a, s)) : 0.0f;
               if (EPI == kEpiRelu2Bf16) {
                 static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] = __float2bfloat16_rn(hv);
+              } else if (EPI == kEpiRelu2Mxfp8) {  // the warp's 32 rows are one MXFP8 block
+                uint32_t sf;
+                const uint32_t code = mxfp8_quant_warp(hv, &sf);
+                static_cast<uint8_t*>(a.out)[s * a.out_ld + n] = (uint8_t)code;
+                if (lane == 0) a.out_sf[s * (a.out_ld / 32) + n / 32] = (uint8_t)sf;
               } else {
                 uint32_t sf;
                 const uint32_t code = nvfp4_quant_lane16(hv, fs, &sf);
@@ -409,6 +414,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               if (EPI == kEpiSwigluBf16) {
                 static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] = __float2bfloat16_rn(hv);
+              } else if (EPI == kEpiSwigluMxfp8) {  // the warp's 32 rows are one MXFP8 block
+                uint32_t sf;
+                const uint32_t code = mxfp8_quant_warp(hv, &sf);
+                static_cast<uint8_t*>(a.out)[s * a.out_ld + n] = (uint8_t)code;
+                if (lane == 0) a.out_sf[s * (a.out_ld / 32) + n / 32] = (uint8_t)sf;
               } else {
                 uint32_t sf;
                 const uint32_t code = nvfp4_quant_lane16(hv, fs, &sf);
@@ -933,6 +943,8 @@ cudaError_t launch_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
     case kEpiAtomicFinal: return launch_t<BN, kEpiAtomicFinal>(s, g, st, pdl);
     case kEpiRelu2Bf16: return launch_t<BN, kEpiRelu2Bf16>(s, g, st, pdl);
     case kEpiRelu2Nvfp4: return launch_t<BN, kEpiRelu2Nvfp4>(s, g, st, pdl);
+    case kEpiSwigluMxfp8: return launch_t<BN, kEpiSwigluMxfp8>(s, g, st, pdl);
+    case kEpiRelu2Mxfp8: return launch_t<BN, kEpiRelu2Mxfp8>(s, g, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

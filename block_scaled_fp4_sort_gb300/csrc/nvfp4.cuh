@@ -40,6 +40,32 @@ __device__ __forceinline__ uint32_t nvfp4_quant_lane16(float h, float s, uint32_
   return f32_to_e2m1_satfinite(__fdiv_rn(__fmul_rn(h, s), dsf));
 }
 
+// Quantise one value of a 32-element MXFP8 block held by the 32 lanes of the
+// warp (the w4a8 FC1 intermediate, FlashInfer PR #4440; the OCP MX recipe):
+//   X = clamp(floor(log2(amax)) - 8, -127, 127), amax = 0 giving -127
+//   sf = X + 127 (E8M0);  q = E4M3_RNE_satfinite(h * 2^-X), the product in fp32
+// A block holding a NaN or an infinity gets sf 255 and q 0x7F.  Every lane
+// returns its own E4M3 byte; *sf receives the block's E8M0 code.
+__device__ __forceinline__ uint32_t mxfp8_quant_warp(float h, uint32_t* sf) {
+  const float a = fabsf(h);
+  const bool special = !(a <= 3.402823466e38f);  // NaN or infinity
+  float amax = special ? 0.0f : a;
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  if (__any_sync(0xffffffffu, special)) {
+    *sf = 255u;
+    return 0x7Fu;
+  }
+  // floor(log2(amax)) of a normal amax is its unbiased exponent; zero and
+  // subnormal amax (exponent field 0) fall below the clamp
+  const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  int X = eb - 127 - 8;
+  X = X < -127 ? -127 : X;                        // fp32 amax keeps X <= 119
+  *sf = (uint32_t)(X + 127);
+  const float inv = __uint_as_float((uint32_t)(127 - X) << 23);   // 2^-X, exponent field 8..254
+  return f32_to_e4m3_satfinite(__fmul_rn(h, inv));
+}
+
 // silu(g) * u with the sigmoid from ex2.approx and rcp.approx
 // (vllm.models.flint.ops.moe_cute, module docstring).
 __device__ __forceinline__ float swiglu(float g, float u) {

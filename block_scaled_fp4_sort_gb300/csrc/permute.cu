@@ -64,10 +64,10 @@ __global__ void permute_rows(const uint8_t* __restrict__ x, const uint8_t* __res
     uint4* dst = reinterpret_cast<uint4*>(px + s * row_bytes);
     const uint4* sp = reinterpret_cast<const uint4*>(x + src * row_bytes);
     for (int64_t i = lane; i < row_bytes / 16; i += 32) dst[i] = src >= 0 ? sp[i] : make_uint4(0, 0, 0, 0);
-    if (x_sf != nullptr) {
-      uint2* dsf = reinterpret_cast<uint2*>(px_sf + s * sf_bytes);
-      const uint2* ssf = reinterpret_cast<const uint2*>(x_sf + src * sf_bytes);
-      for (int64_t i = lane; i < sf_bytes / 8; i += 32) dsf[i] = src >= 0 ? ssf[i] : make_uint2(0, 0);
+    if (x_sf != nullptr) {  // 4-byte units: H/16 (NVFP4) and H/32 (MXFP8) scale bytes
+      uint32_t* dsf = reinterpret_cast<uint32_t*>(px_sf + s * sf_bytes);
+      const uint32_t* ssf = reinterpret_cast<const uint32_t*>(x_sf + src * sf_bytes);
+      for (int64_t i = lane; i < sf_bytes / 4; i += 32) dsf[i] = src >= 0 ? ssf[i] : 0u;
     }
   }
   launch_dependents();
@@ -159,13 +159,21 @@ __global__ void round_acc(const float4* __restrict__ acc, uint4* __restrict__ ou
 __constant__ float kE2M1[16] = {0.0f,  0.5f,  1.0f,  1.5f,  2.0f,  3.0f,  4.0f,  6.0f,
                                 -0.0f, -0.5f, -1.0f, -1.5f, -2.0f, -3.0f, -4.0f, -6.0f};
 
-// NVFP4 rows -> BF16 rows (exact: every E2M1*E4M3 product is a BF16 value).
-// With `gather` (permuted_idx_to_expanded_idx), output row s is source row
-// gather[s] / top_k, or zeros for a padding slot.  One thread per 8 elements.
-__global__ void dequant_rows(const uint32_t* __restrict__ q, const uint8_t* __restrict__ sf,
+// 2^(e - 127) of an E8M0 code, NaN for 255
+__device__ __forceinline__ float e8m0_to_float(uint32_t e) {
+  return e == 255u ? __uint_as_float(0x7FC00000u)
+                   : e == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(e << 23);
+}
+
+// NVFP4 rows (mx = 0) or MXFP8 rows (mx = 1: E4M3 bytes [rows, K] + E8M0
+// block-32 scales) -> BF16 rows.  Exact for NVFP4 (every E2M1*E4M3 product is
+// a BF16 value) and for MXFP8 products in the BF16 range.  With `gather`
+// (permuted_idx_to_expanded_idx), output row s is source row gather[s] /
+// top_k, or zeros for a padding slot.  One thread per 8 elements.
+__global__ void dequant_rows(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
                              int64_t rows, int64_t K, const int32_t* __restrict__ num_tiles,
                              int64_t T, const int32_t* __restrict__ gather, int64_t top_k,
-                             int64_t src_rows, uint4* __restrict__ out) {
+                             int64_t src_rows, int mx, uint4* __restrict__ out) {
   grid_dependency_wait();
   const int64_t nrows =
       num_tiles ? min(rows, max((int64_t)num_tiles[0], (int64_t)0) * T) : rows;
@@ -180,8 +188,14 @@ __global__ void dequant_rows(const uint32_t* __restrict__ q, const uint8_t* __re
       src = g >= 0 && g < src_rows * top_k ? g / top_k : -1;
     }
     float f[8];
-    if (src >= 0) {
-      const uint32_t codes = q[src * (K / 8) + c];
+    if (src >= 0 && mx) {
+      const uint2 b = *reinterpret_cast<const uint2*>(q + src * K + 8 * c);
+      const float s = e8m0_to_float(sf[src * (K / 32) + c / 4]);
+      const uint32_t w[2] = {b.x, b.y};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) f[k] = e4m3_to_float((w[k >> 2] >> (8 * (k & 3))) & 0xFFu) * s;
+    } else if (src >= 0) {
+      const uint32_t codes = reinterpret_cast<const uint32_t*>(q)[src * (K / 8) + c];
       const float s = e4m3_to_float(sf[src * (K / 16) + c / 2]);
 #pragma unroll
       for (int k = 0; k < 8; ++k) f[k] = kE2M1[(codes >> (4 * k)) & 15u] * s;
@@ -219,13 +233,35 @@ __global__ void debug_quantize(const float* __restrict__ in, int64_t n, const fl
   }
 }
 
+// 32 lanes per 32-element block
+__global__ void debug_quantize_mx(const float* __restrict__ in, int64_t n, uint8_t* __restrict__ q,
+                                  uint8_t* __restrict__ sf) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t base = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) & ~31ll; base < n;
+       base += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t sc;
+    const uint32_t code = mxfp8_quant_warp(in[base + lane], &sc);
+    q[base + lane] = (uint8_t)code;
+    if (lane == 0) sf[base / 32] = (uint8_t)sc;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_debug_quantize_mx(const float* in, int64_t n, uint8_t* q, uint8_t* sf,
+                                     cudaStream_t st) {
+  if (n == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4096);
+  debug_quantize_mx<<<(unsigned)blocks, 256, 0, st>>>(in, n, q, sf);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, const int32_t* p2e,
                            const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
                            bool pdl, bool zero_pad) {
-  const int64_t row_bytes = s.mode == 0 ? s.H * 2 : s.H / 2;
-  const int64_t sf_bytes = s.mode == 0 ? 0 : s.H / 16;
+  // w4a16 BF16 rows; w4a4 NVFP4 (H/2 + H/16 bytes); w4a8 MXFP8 (H + H/32 bytes)
+  const int64_t row_bytes = s.mode == 0 ? s.H * 2 : s.mode == 2 ? s.H : s.H / 2;
+  const int64_t sf_bytes = s.mode == 0 ? 0 : s.mode == 2 ? s.H / 32 : s.H / 16;
   const int64_t blocks = std::min<int64_t>((s.S + 7) / 8, (int64_t)num_sms() * 8);
   return launch_pdl(permute_rows, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), st, pdl,
                     static_cast<const uint8_t*>(x), s.mode == 0 ? nullptr : x_sf, p2e, num_tiles,
@@ -264,13 +300,13 @@ cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaSt
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
                                 const int32_t* row_limit_tiles, int64_t T, void* out,
                                 cudaStream_t st, bool pdl, const int32_t* gather, int64_t top_k,
-                                int64_t src_rows) {
+                                int64_t src_rows, bool mx) {
   const int64_t n = rows * (K / 8);
   if (n == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 16);
   return launch_pdl(dequant_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
-                    reinterpret_cast<const uint32_t*>(q), sf, rows, K, row_limit_tiles, T, gather,
-                    top_k, src_rows, static_cast<uint4*>(out));
+                    q, sf, rows, K, row_limit_tiles, T, gather, top_k, src_rows, mx ? 1 : 0,
+                    static_cast<uint4*>(out));
 }
 
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl) {

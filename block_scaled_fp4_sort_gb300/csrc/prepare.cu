@@ -29,6 +29,7 @@ struct PrepArgs {
   int which;
   int64_t EL, F, C, rows_src, K;  // rows_src: rows per expert in the source (2I, I or H)
   int gated;                      // GEMM1 with gate and up rows
+  int mx;                         // MXFP4 weights: E8M0 block-32 scales (w4a8)
   int64_t I;                      // GEMM1: intermediate size
   const uint8_t* w;
   const uint8_t* w_sf;
@@ -40,6 +41,23 @@ __device__ __forceinline__ int64_t src_row(const PrepArgs& a, int64_t f, int64_t
   if (a.which == 1 && a.gated) return r < 128 ? 128 * f + r : a.I + 128 * f + (r - 128);
   const int64_t row = 256 * f + r;
   return row < a.rows_src ? row : -1;
+}
+
+// Scale code of 16-element block `blk` (0..7) of chunk c of source row `row`
+// (-1: a row past the matrix, zero codes).
+__device__ uint32_t block_scale_code(const PrepArgs& a, int64_t e, int64_t row, int64_t c, int blk) {
+  if (row < 0) return prep_scale_code(0);
+  const int64_t r = e * a.rows_src + row;
+  if (!a.mx) return prep_scale_code(a.w_sf[r * (a.K / 16) + c * 8 + blk]);
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(a.w + r * (a.K / 2) + c * (kBK / 2) + blk * 8);
+  const bool zero = ((q[0] | q[1]) & 0x77777777u) == 0u;
+  return prep_scale_code_mx(a.w_sf[r * (a.K / 32) + c * 4 + blk / 2], zero);
+}
+
+// the E4M3 scale byte whose sign and zero move into the codes (NVFP4 only)
+__device__ uint32_t block_scale_byte(const PrepArgs& a, int64_t e, int64_t row, int64_t c, int blk) {
+  if (row < 0 || a.mx) return 1u;   // a positive non-zero scale: codes unchanged
+  return a.w_sf[(e * a.rows_src + row) * (a.K / 16) + c * 8 + blk];
 }
 
 // one thread per (block, row)
@@ -55,9 +73,7 @@ __global__ void prepare_kernel(PrepArgs a) {
     const uint32_t* src = sr >= 0 ? reinterpret_cast<const uint32_t*>(
                                         a.w + (e * a.rows_src + sr) * (a.K / 2) + c * (kBK / 2))
                                   : nullptr;
-    uint2 s = make_uint2(0, 0);  // rows past the matrix: zero codes under a zero scale
-    if (src) s = *reinterpret_cast<const uint2*>(a.w_sf + (e * a.rows_src + sr) * (a.K / 16) + c * 8);
-    const uint32_t sb[2] = {s.x, s.y};
+    // rows past the matrix: zero codes under a finite scale code
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint32_t v[4] = {0, 0, 0, 0};
@@ -65,7 +81,7 @@ __global__ void prepare_kernel(PrepArgs a) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {  // word 4q+i: elements 8(4q+i).., scale block (4q+i)/2
           const int word = 4 * q + i;
-          const uint32_t b = (sb[word >> 3] >> (8 * ((word >> 1) & 3))) & 0xFFu;
+          const uint32_t b = block_scale_byte(a, e, sr, c, word >> 1);
           v[i] = prep_permute_word(prep_fix_codes(src[word], b, 0x88888888u));
         }
       }
@@ -73,7 +89,7 @@ __global__ void prepare_kernel(PrepArgs a) {
     }
     uint32_t codes[2] = {0, 0};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) codes[i >> 2] |= prep_scale_code((sb[i >> 2] >> (8 * (i & 3))) & 0xFFu) << (8 * (i & 3));
+    for (int i = 0; i < 8; ++i) codes[i >> 2] |= block_scale_code(a, e, sr, c, i) << (8 * (i & 3));
     *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = make_uint2(codes[0], codes[1]);
   }
 }
@@ -89,10 +105,9 @@ __global__ void prepare_fragment_kernel(PrepArgs a) {
     const uint32_t g = lane >> 2, t = lane & 3;
     const int64_t rows[2] = {src_row(a, f, 16 * w + g), src_row(a, f, 16 * w + g + 8)};
     uint8_t* dst = a.prep + blk * kWBlockBytes;
-    uint8_t sc[2][8];  // E4M3 scale bytes of the two rows, zero past the matrix
+    uint8_t sc[2][8];  // E4M3 scale bytes of the two rows (sign / zero into the codes)
     for (int h = 0; h < 2; ++h)
-      for (int kk = 0; kk < 8; ++kk)
-        sc[h][kk] = rows[h] >= 0 ? a.w_sf[(e * a.rows_src + rows[h]) * (a.K / 16) + c * 8 + kk] : 0;
+      for (int kk = 0; kk < 8; ++kk) sc[h][kk] = (uint8_t)block_scale_byte(a, e, rows[h], c, kk);
     uint32_t words[8];
     for (int kk = 0; kk < 8; ++kk) {
       uint32_t v = 0;
@@ -114,7 +129,8 @@ __global__ void prepare_fragment_kernel(PrepArgs a) {
       for (int h = 0; h < 2; ++h) {
         const uint32_t r = 16 * w + g + 8 * h;
         uint32_t codes[2] = {0, 0};
-        for (int kk = 0; kk < 8; ++kk) codes[kk >> 2] |= prep_scale_code(sc[h][kk]) << (8 * (kk & 3));
+        for (int kk = 0; kk < 8; ++kk)
+          codes[kk >> 2] |= block_scale_code(a, e, rows[h], c, kk) << (8 * (kk & 3));
         *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = make_uint2(codes[0], codes[1]);
       }
     }
@@ -196,6 +212,7 @@ PrepArgs make_args(const Shape& s, int which) {
   a.F = row_blocks(s, which);
   a.C = k_chunks(s, which);
   a.gated = gated(s) ? 1 : 0;
+  a.mx = s.mode == 2 ? 1 : 0;
   a.rows_src = which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H;
   a.K = which == 1 ? s.H : s.I;
   a.I = s.I;

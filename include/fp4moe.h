@@ -67,7 +67,16 @@ typedef enum {
   FP4MOE_ERR_DEVICE_TIMEOUT = 6        /* device error word: a bounded wait expired */
 } fp4moe_status;
 
-typedef enum { FP4MOE_W4A16 = 0, FP4MOE_W4A4 = 1 } fp4moe_quant_mode;
+/* Quantisation modes (cute_dsl_fused_moe quant_mode):
+ *   FP4MOE_W4A16: BF16 x; NVFP4 weights (E2M1, E4M3 block-16 scales)
+ *   FP4MOE_W4A4 : NVFP4 x [M, H/2] + E4M3 [M, H/16]; NVFP4 weights; NVFP4 FC1
+ *                 intermediate through fc2_input_scale
+ *   FP4MOE_W4A8 : MXFP8 x, E4M3 [M, H] + E8M0 block-32 scales [M, H/32];
+ *                 MXFP4 weights, E2M1 + E8M0 block-32 scales ([.., K/32]);
+ *                 MXFP8 FC1 intermediate (FlashInfer PR #4440).  Weight scale
+ *                 exponents must lie in [106, 136] (2^-21 .. 2^9): a block
+ *                 outside that range with non-zero codes decodes as NaN. */
+typedef enum { FP4MOE_W4A16 = 0, FP4MOE_W4A4 = 1, FP4MOE_W4A8 = 2 } fp4moe_quant_mode;
 
 typedef enum {
   FP4MOE_FINALIZE_DETERMINISTIC = 0,   /* GEMM2 writes y; a second pass sums in route order */
@@ -230,6 +239,7 @@ FP4MOE_API fp4moe_status moe_route_sort_noalloc(const fp4moe_problem* p,
  * for s < num_non_exiting_tiles * T; padding rows are zero-filled.
  *   w4a16: x bf16 [M, H] -> permuted_x bf16 [S, H]; x_sf, permuted_x_sf NULL
  *   w4a4 : x uint8 [M, H/2] + x_sf e4m3 [M, H/16] -> [S, H/2] + [S, H/16]
+ *   w4a8 : x e4m3 [M, H] + x_sf e8m0 [M, H/32] -> [S, H] + [S, H/32]
  * fused_moe_forward does its own gather (see there). */
 FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
                           const int32_t* permuted_idx_to_expanded_idx,
@@ -254,6 +264,10 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
  *      GEMM (route_tile 16); the result is the same bit for bit.
  *   w1_prepared: fp4moe_prepare_weights(p, 1, ...).  w1_alpha fp32 [E_local].
  *   w4a16: h bf16 [S, I] (R = round to BF16); h_sf, fc2_input_scale NULL.
+ *   w4a8 : h e4m3 [S, I] + h_sf e8m0 [S, I/32]: R = MXFP8 quantisation (OCP MX
+ *          recipe): per 32-block X = clamp(floor(log2(amax)) - 8, -127, 127)
+ *          (amax = 0: -127), h_sf = X + 127, h = E4M3_RNE_satfinite(h * 2^-X)
+ *          in fp32; fc2_input_scale NULL.
  *   w4a4 : h uint8 [S, I/2] + h_sf e4m3 [S, I/16]: R = NVFP4 quantisation with
  *          fc2_input_scale fp32 [1]: per 16-block sf = E4M3((amax*s)/6),
  *          q = E2M1((h*s)/sf), fp32 arithmetic, RNE, saturating. */
@@ -272,7 +286,8 @@ FP4MOE_API fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a
  *   "FP32 route storage" option of alphamoe_nvfp4_routed_moe; BF16 storage of
  *   y would put ~0.2% of outputs outside the parity bound through
  *   cancellation in the weighted sum).  y: fp32 [S, H].
- *   h: bf16 [S, I] (w4a16) or uint8 [S, I/2] + h_sf [S, I/16] (w4a4).
+ *   h: bf16 [S, I] (w4a16), uint8 [S, I/2] + h_sf [S, I/16] (w4a4) or e4m3
+ *   [S, I] + h_sf e8m0 [S, I/32] (w4a8).
  *   w2_prepared: fp4moe_prepare_weights(p, 2, ...).  w2_alpha fp32 [E_local]. */
 FP4MOE_API fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h_sf,
                         const void* w2_prepared, const float* w2_alpha,
@@ -323,6 +338,11 @@ FP4MOE_API fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* 
  * epilogue, exported so that tests can compare it bit for bit. */
 FP4MOE_API fp4moe_status fp4moe_debug_quantize_nvfp4(const float* in, int64_t n, const float* scale,
                                           uint8_t* q, uint8_t* sf, void* stream);
+
+/* Run the device MXFP8 quantiser of GEMM1's w4a8 epilogue on n fp32 values
+ * (n multiple of 32, device pointers): q gets n E4M3 bytes, sf n/32 E8M0. */
+FP4MOE_API fp4moe_status fp4moe_debug_quantize_mxfp8(const float* in, int64_t n, uint8_t* q,
+                                                  uint8_t* sf, void* stream);
 
 /* Decode prepared weights back to their BF16 values as the GEMM kernels see
  * them: out bf16 [E_local, rows, K] for GEMM `which` (rows = 2I or H).

@@ -70,6 +70,10 @@ def lib():
                 getattr(L, name).argtypes = [d]
             L.orc_nvfp4_quantize_f32.restype = None
             L.orc_nvfp4_quantize_f32.argtypes = [vp, i64, ctypes.c_float, vp, vp]
+            L.orc_ue8m0_value.restype = d
+            L.orc_ue8m0_value.argtypes = [u32]
+            L.orc_mxfp8_quantize_f32.restype = None
+            L.orc_mxfp8_quantize_f32.argtypes = [vp, i64, vp, vp]
             L.orc_max_permuted_slots.restype = i64
             L.orc_max_permuted_slots.argtypes = [i64, i32, i32]
             L.orc_route_sort.restype = i32
@@ -143,6 +147,20 @@ def nvfp4_quantize_f32(h: np.ndarray, s: float):
     return q.reshape(h.shape[:-1] + (h.shape[-1] // 2,)), sf.reshape(h.shape[:-1] + (h.shape[-1] // 16,))
 
 
+def ue8m0_value(code: int) -> float:
+    return lib().orc_ue8m0_value(code)
+
+
+def mxfp8_quantize_f32(h: np.ndarray):
+    """fp32 MXFP8 quantiser of the w4a8 FC1 output.  h: float32 [..., n], n % 32 == 0."""
+    h = np.ascontiguousarray(h, dtype=np.float32)
+    n = h.size
+    q = np.zeros(n, np.uint8)
+    sf = np.zeros(n // 32, np.uint8)
+    lib().orc_mxfp8_quantize_f32(_ptr(h), n, _ptr(q), _ptr(sf))
+    return q.reshape(h.shape), sf.reshape(h.shape[:-1] + (h.shape[-1] // 32,))
+
+
 def max_permuted_slots(routes: int, E_local: int, T: int) -> int:
     return int(lib().orc_max_permuted_slots(routes, E_local, T))
 
@@ -152,7 +170,7 @@ class OracleMoE:
 
     def __init__(self, M, H, I, E, top_k, ids, wts, w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha,
                  x=None, x_q=None, x_sf=None, fc2_input_scale=None, E_local=None, offset=0, T=16,
-                 act_type=0, act_params=None, per_token_scale=None):
+                 act_type=0, act_params=None, per_token_scale=None, mode=None):
         """act_type / act_params: the FC1 activation (0 SwiGLU family with optional
         swiglu_alpha/beta/limit or situ_beta/situ_linear_beta, 1 GeGLU-tanh,
         2 non-gated ReLU^2); per_token_scale: fp32 [M] or None."""
@@ -168,7 +186,8 @@ class OracleMoE:
             w2_alpha=c(w2_alpha, dtype=np.float32),
             fc2_input_scale=None if fc2_input_scale is None else c(fc2_input_scale, dtype=np.float32),
             per_token_scale=None if per_token_scale is None else c(per_token_scale, dtype=np.float32))
-        mode = 0 if x is not None else 1
+        if mode is None:                     # 0 w4a16, 1 w4a4, 2 w4a8 (MXFP8 x, MXFP4 weights)
+            mode = 0 if x is not None else 1
         E_local = E if E_local is None else E_local
         ap = dict(act_params or {})
         flags = 0
@@ -203,7 +222,8 @@ class OracleMoE:
                    h(inp.w2_sf), h(inp.w2_alpha), x=h(inp.x), x_q=h(inp.x_q), x_sf=h(inp.x_sf),
                    fc2_input_scale=h(inp.fc2_input_scale), E_local=E_local, offset=offset, T=T,
                    act_type=act_type, act_params=act_params,
-                   per_token_scale=h(getattr(inp, "per_token_scale", None)))
+                   per_token_scale=h(getattr(inp, "per_token_scale", None)),
+                   mode={"w4a16": 0, "w4a4": 1, "w4a8": 2}[cfg.mode])
 
     @property
     def H(self):
@@ -241,8 +261,9 @@ class OracleMoE:
         xh = self.xhat(t)
         g = np.zeros(p.I); u = np.zeros(p.I); hp = np.zeros(p.I); hi = np.zeros(p.I)
         y = np.zeros(p.H)
-        hq = np.zeros(p.I // 2, np.uint8)
-        hsf = np.zeros(p.I // 16, np.uint8)
+        mx = p.mode == 2                      # w4a8: MXFP8 codes of h
+        hq = np.zeros(p.I if mx else p.I // 2, np.uint8)
+        hsf = np.zeros(p.I // (32 if mx else 16), np.uint8)
         lib().orc_expert_ffn(ctypes.byref(p), ctypes.byref(self.inp), int(e_local), _ptr(xh),
                              _ptr(g), _ptr(u), _ptr(hp), _ptr(hi), _ptr(hq), _ptr(hsf), _ptr(y))
         return dict(g=g, u=u, h_pre=hp, h_in=hi, hq=hq, hsf=hsf, y=y)

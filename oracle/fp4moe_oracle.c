@@ -12,6 +12,7 @@
  */
 #include "fp4moe_oracle.h"
 
+#include <float.h>
 #include <math.h>
 #include <pthread.h>
 #include <stdlib.h>
@@ -156,6 +157,50 @@ void orc_nvfp4_quantize_f32(const float* h, int64_t n, float s, uint8_t* q_packe
   }
 }
 
+/* OCP MX E8M0 scale: 2^(code - 127), code 255 = NaN (FlashInfer PR #4440:
+ * "linear block-32 E8M0" scales of MXFP8 activations and MXFP4 weights). */
+double orc_ue8m0_value(uint32_t code) {
+  code &= 255u;
+  if (code == 255u) return NAN;
+  return ldexp(1.0, (int)code - 127);
+}
+
+/* MXFP8 quantiser of the w4a8 FC1 output (reading: the OCP MX recipe).  Per
+ * 32-element block: X = floor(log2(amax)) - 8 (8 = exponent of the largest
+ * E4M3 value, 448), clamped to [-127, 127], amax = 0 giving -127; scale code
+ * X + 127; q_i = E4M3_RNE_satfinite(h_i * 2^-X) with the product in fp32.  A
+ * block holding a NaN or an infinity gets code 255 and NaN elements. */
+void orc_mxfp8_quantize_f32(const float* h, int64_t n, uint8_t* q, uint8_t* sf) {
+  for (int64_t b = 0; b < n / 32; ++b) {
+    float amax = 0.0f;
+    int special = 0;
+    for (int i = 0; i < 32; ++i) {
+      float a = fabsf(h[b * 32 + i]);
+      if (!(a <= FLT_MAX)) special = 1;   /* NaN or infinity */
+      else if (a > amax) amax = a;
+    }
+    if (special) {
+      sf[b] = 255u;
+      for (int i = 0; i < 32; ++i) q[b * 32 + i] = 0x7Fu;
+      continue;
+    }
+    int X = -127;
+    if (amax > 0.0f) {
+      int e;
+      (void)frexpf(amax, &e);               /* amax = m 2^e, m in [0.5, 1) */
+      X = (e - 1) - 8;
+      if (X < -127) X = -127;
+      if (X > 127) X = 127;
+    }
+    sf[b] = (uint8_t)(X + 127);
+    const float inv = ldexpf(1.0f, -X);     /* exact power of two */
+    for (int i = 0; i < 32; ++i) {
+      volatile float v = h[b * 32 + i] * inv;
+      q[b * 32 + i] = (uint8_t)orc_e4m3_code_satfinite((double)v);
+    }
+  }
+}
+
 /* ------------------------------------------------------------------------
  * Routing plan (cute_dsl_fused_moe `num_local_experts`/`local_expert_offset`;
  * vllm moe_cute grouped_moe: moe_sort -> tile_idx_to_expert_idx,
@@ -236,6 +281,14 @@ static void build_tables(void) {
   for (uint32_t c = 0; c < 256; ++c) g_e4m3[c] = orc_e4m3_value(c);
 }
 
+/* packed E2M1 element k of a row under E4M3 block-16 scales (NVFP4, mx = 0)
+ * or E8M0 block-32 scales (MXFP4, mx = 1) */
+static double dec_w(int mx, const uint8_t* row_q, const uint8_t* row_sf, int64_t k) {
+  uint8_t byte = row_q[k / 2];
+  uint32_t code = (k & 1) ? (uint32_t)(byte >> 4) : (uint32_t)(byte & 15u);
+  return g_e2m1[code] * (mx ? orc_ue8m0_value(row_sf[k / 32]) : g_e4m3[row_sf[k / 16]]);
+}
+
 static double dec_packed(const uint8_t* row_q, const uint8_t* row_sf, int64_t k) {
   uint8_t byte = row_q[k / 2];
   uint32_t code = (k & 1) ? (uint32_t)(byte >> 4) : (uint32_t)(byte & 15u); /* reading: 2i low nibble */
@@ -244,12 +297,12 @@ static double dec_packed(const uint8_t* row_q, const uint8_t* row_sf, int64_t k)
 
 /* sum_k dec(W[row a])[k] * v[k] and the same for row b, each summed in
  * ascending k (two rows at a time only to overlap their latencies). */
-static void dot2(const uint8_t* qa, const uint8_t* sa, const uint8_t* qb, const uint8_t* sb,
-                 const double* v, int64_t K, double* ra, double* rb) {
+static void dot2(int mx, const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
+                 const uint8_t* sb, const double* v, int64_t K, double* ra, double* rb) {
   double acc_a = 0.0, acc_b = 0.0;
   for (int64_t k = 0; k < K; ++k) {
-    acc_a += dec_packed(qa, sa, k) * v[k];
-    acc_b += dec_packed(qb, sb, k) * v[k];
+    acc_a += dec_w(mx, qa, sa, k) * v[k];
+    acc_b += dec_w(mx, qb, sb, k) * v[k];
   }
   *ra = acc_a;
   *rb = acc_b;
@@ -260,6 +313,9 @@ void orc_xhat(const orc_problem* p, const orc_inputs* in, int64_t t, double* xha
   int64_t H = p->H;
   if (p->mode == 0) {
     for (int64_t k = 0; k < H; ++k) xhat[k] = orc_bf16_value(in->x[t * H + k]);
+  } else if (p->mode == 2) {  /* MXFP8: E4M3 elements, E8M0 block-32 scales */
+    for (int64_t k = 0; k < H; ++k)
+      xhat[k] = g_e4m3[in->x_q[t * H + k]] * orc_ue8m0_value(in->x_sf[t * (H / 32) + k / 32]);
   } else {
     for (int64_t k = 0; k < H; ++k)
       xhat[k] = dec_packed(in->x_q + t * (H / 2), in->x_sf + t * (H / 16), k);
@@ -293,22 +349,25 @@ static double act_gated(const orc_problem* p, double g, double u) {
 }
 
 /* sum_k dec(W[row])[k] * v[k] in ascending k */
-static double dot1(const uint8_t* q, const uint8_t* sf, const double* v, int64_t K) {
+static double dot1(int mx, const uint8_t* q, const uint8_t* sf, const double* v, int64_t K) {
   double acc = 0.0;
-  for (int64_t k = 0; k < K; ++k) acc += dec_packed(q, sf, k) * v[k];
+  for (int64_t k = 0; k < K; ++k) acc += dec_w(mx, q, sf, k) * v[k];
   return acc;
 }
 
 static void down_proj(const orc_problem* p, const orc_inputs* in, int32_t e, const double* hin,
                       double* y) {
   int64_t H = p->H, I = p->I;
+  const int mx = p->mode == 2;
+  const int64_t sb = mx ? 32 : 16;   /* elements per weight scale */
   const uint8_t* W2 = in->w2 + (int64_t)e * H * (I / 2);
-  const uint8_t* S2 = in->w2_sf + (int64_t)e * H * (I / 16);
+  const uint8_t* S2 = in->w2_sf + (int64_t)e * H * (I / sb);
   double a2 = (double)in->w2_alpha[e];
   for (int64_t n = 0; n < H; n += 2) {
     double ya, yb;
     int64_t m = n + 1 < H ? n + 1 : n;
-    dot2(W2 + n * (I / 2), S2 + n * (I / 16), W2 + m * (I / 2), S2 + m * (I / 16), hin, I, &ya, &yb);
+    dot2(mx, W2 + n * (I / 2), S2 + n * (I / sb), W2 + m * (I / 2), S2 + m * (I / sb), hin, I, &ya,
+         &yb);
     y[n] = a2 * ya;
     if (m != n) y[m] = a2 * yb;
   }
@@ -320,9 +379,11 @@ void orc_expert_ffn(const orc_problem* p, const orc_inputs* in, int32_t e, const
   int64_t H = p->H, I = p->I;
   pthread_once(&g_tab_once, build_tables);
   const int gated = p->act_type != 2;
+  const int mx = p->mode == 2;
+  const int64_t sb = mx ? 32 : 16;          /* elements per weight scale */
   const int64_t rows1 = gated ? 2 * I : I;   /* FC1 rows per expert */
   const uint8_t* W1 = in->w1 + (int64_t)e * rows1 * (H / 2);
-  const uint8_t* S1 = in->w1_sf + (int64_t)e * rows1 * (H / 16);
+  const uint8_t* S1 = in->w1_sf + (int64_t)e * rows1 * (H / sb);
   double a1 = (double)in->w1_alpha[e];
   double* h = (double*)malloc(sizeof(double) * (size_t)I);
   double* hi = (double*)malloc(sizeof(double) * (size_t)I);
@@ -333,14 +394,14 @@ void orc_expert_ffn(const orc_problem* p, const orc_inputs* in, int32_t e, const
     if (gated) {
       /* reading: rows [0, I) of w1 are the gate, rows [I, 2I) the up projection */
       double gacc, uacc;
-      dot2(W1 + n * (H / 2), S1 + n * (H / 16), W1 + (I + n) * (H / 2), S1 + (I + n) * (H / 16),
+      dot2(mx, W1 + n * (H / 2), S1 + n * (H / sb), W1 + (I + n) * (H / 2), S1 + (I + n) * (H / sb),
            xhat, H, &gacc, &uacc);
       double g = a1 * gacc, u = a1 * uacc;   /* alpha on the accumulator */
       if (g_out) g_out[n] = g;
       if (u_out) u_out[n] = u;
       h[n] = act_gated(p, g, u);
     } else {
-      double u = a1 * dot1(W1 + n * (H / 2), S1 + n * (H / 16), xhat, H);
+      double u = a1 * dot1(mx, W1 + n * (H / 2), S1 + n * (H / sb), xhat, H);
       if (g_out) g_out[n] = 0.0;
       if (u_out) u_out[n] = u;
       h[n] = u > 0.0 ? u * u : 0.0;            /* ReLU^2 */
@@ -349,6 +410,16 @@ void orc_expert_ffn(const orc_problem* p, const orc_inputs* in, int32_t e, const
   }
   if (p->mode == 0) {
     for (int64_t n = 0; n < I; ++n) hi[n] = orc_round_bf16(h[n]);   /* rounded once */
+  } else if (p->mode == 2) {
+    /* w4a8: MXFP8 FC1 intermediate, decision in fp32 as in the kernel */
+    uint8_t* q8 = (uint8_t*)malloc((size_t)I);
+    uint8_t* sf8 = (uint8_t*)malloc((size_t)I / 32);
+    for (int64_t n = 0; n < I; ++n) hf[n] = (float)h[n];
+    orc_mxfp8_quantize_f32(hf, I, q8, sf8);
+    for (int64_t n = 0; n < I; ++n) hi[n] = g_e4m3[q8[n]] * orc_ue8m0_value(sf8[n / 32]);
+    if (hq) memcpy(hq, q8, (size_t)I);
+    if (hsf) memcpy(hsf, sf8, (size_t)I / 32);
+    free(q8); free(sf8);
   } else {
     /* the quantisation decision is taken in fp32, as in the kernel */
     for (int64_t n = 0; n < I; ++n) hf[n] = (float)h[n];
@@ -367,7 +438,8 @@ void orc_expert_down_nvfp4(const orc_problem* p, const orc_inputs* in, int32_t e
   int64_t I = p->I;
   pthread_once(&g_tab_once, build_tables);
   double* hi = (double*)malloc(sizeof(double) * (size_t)I);
-  for (int64_t n = 0; n < I; ++n) hi[n] = dec_packed(hq, hsf, n);
+  for (int64_t n = 0; n < I; ++n)
+    hi[n] = p->mode == 2 ? g_e4m3[hq[n]] * orc_ue8m0_value(hsf[n / 32]) : dec_packed(hq, hsf, n);
   down_proj(p, in, e, hi, y);
   free(hi);
 }

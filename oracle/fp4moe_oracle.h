@@ -38,22 +38,22 @@ extern "C" {
  *   act_type 2              : non-gated ReLU^2  max(u, 0)^2, w1 has I rows (no gate rows) */
 typedef struct {
   int32_t M, H, I, E, top_k, E_local, offset, T;
-  int32_t mode; /* 0 = w4a16 (BF16 x), 1 = w4a4 (NVFP4 x) */
+  int32_t mode; /* 0 = w4a16 (BF16 x), 1 = w4a4 (NVFP4 x), 2 = w4a8 (MXFP8 x, MXFP4 w) */
   int32_t act_type, act_flags;
   double swiglu_alpha, swiglu_beta, swiglu_limit, situ_beta, situ_linear_beta;
 } orc_problem;
 
 typedef struct {
   const uint16_t* x;        /* bf16 bits [M, H]              (w4a16) */
-  const uint8_t* x_q;       /* packed e2m1 [M, H/2]          (w4a4)  */
-  const uint8_t* x_sf;      /* e4m3 [M, H/16]                (w4a4)  */
+  const uint8_t* x_q;       /* packed e2m1 [M, H/2] (w4a4); e4m3 [M, H] (w4a8) */
+  const uint8_t* x_sf;      /* e4m3 [M, H/16] (w4a4); e8m0 [M, H/32] (w4a8)    */
   const int32_t* ids;       /* [M, top_k] global expert ids          */
   const float* wts;         /* [M, top_k] routing weights            */
   const uint8_t* w1;        /* [E_local, 2I, H/2]                    */
-  const uint8_t* w1_sf;     /* [E_local, 2I, H/16]                   */
+  const uint8_t* w1_sf;     /* [E_local, 2I, H/16]; w4a8: e8m0 [., ., H/32] */
   const float* w1_alpha;    /* [E_local]                             */
   const uint8_t* w2;        /* [E_local, H, I/2]                     */
-  const uint8_t* w2_sf;     /* [E_local, H, I/16]                    */
+  const uint8_t* w2_sf;     /* [E_local, H, I/16]; w4a8: e8m0 [., ., I/32]  */
   const float* w2_alpha;    /* [E_local]                             */
   const float* fc2_input_scale; /* [1] (w4a4) or NULL                */
   const float* per_token_scale; /* [M] or NULL: x row t is scaled by it  */
@@ -76,6 +76,15 @@ uint32_t orc_e2m1_code_satfinite(double v);
  * n/2 bytes (element 2i in the low nibble), sf gets n/16 bytes. */
 void orc_nvfp4_quantize_f32(const float* h, int64_t n, float s, uint8_t* q_packed, uint8_t* sf);
 
+/* OCP MX E8M0 scale value 2^(code - 127); code 255 is NaN. */
+double orc_ue8m0_value(uint32_t code);
+
+/* MXFP8 quantiser for the w4a8 FC1 output, fp32 decisions (OCP MX recipe):
+ * per 32-block X = clamp(floor(log2(amax)) - 8, -127, 127) (amax = 0: -127),
+ * sf = X + 127, q_i = E4M3_RNE_satfinite(h_i * 2^-X); a block holding a NaN or
+ * an infinity gets sf 255 and q 0x7F.  n multiple of 32; q gets n bytes. */
+void orc_mxfp8_quantize_f32(const float* h, int64_t n, uint8_t* q, uint8_t* sf);
+
 /* ---- routing plan ---- */
 int64_t orc_max_permuted_slots(int64_t routes, int32_t E_local, int32_t T);
 /* Stable counting sort of routes r = t*top_k + j by local expert.  Returns
@@ -92,13 +101,14 @@ int32_t orc_route_sort(const orc_problem* p, const int32_t* ids,
  *   h_pre [I] : silu(g)*u before rounding
  *   h_in [I]  : the GEMM2 input value (BF16-rounded h; or dequantised NVFP4 h
  *               times 1 -- i.e. dec(q)*dec(sf), the fc2 scale stays in a2)
- *   hq [I/2], hsf [I/16] : NVFP4 codes of h (w4a4 only)
+ *   hq [I/2], hsf [I/16] : NVFP4 codes of h (w4a4); w4a8: MXFP8 hq [I], hsf [I/32]
  *   y [H]     : alpha2-scaled down projection, unrounded */
 void orc_expert_ffn(const orc_problem* p, const orc_inputs* in, int32_t e_local,
                     const double* xhat, double* g, double* u, double* h_pre,
                     double* h_in, uint8_t* hq, uint8_t* hsf, double* y);
 
-/* GEMM2 half alone, from given NVFP4 FC1 codes (staged w4a4 check). */
+/* GEMM2 half alone, from given FC1 codes (staged checks): NVFP4 (w4a4) or
+ * MXFP8 (w4a8). */
 void orc_expert_down_nvfp4(const orc_problem* p, const orc_inputs* in, int32_t e_local,
                            const uint8_t* hq, const uint8_t* hsf, double* y);
 

@@ -42,7 +42,7 @@ class MoEConfig:
     I: int          # intermediate (per gate / up half)
     E: int          # experts (all local)
     top_k: int
-    mode: str       # "w4a16" or "w4a4"
+    mode: str       # "w4a16", "w4a4" or "w4a8"
     routing: str    # "softmax", "skewed" or "uniform"
     sample: int = 0  # 0: check every token; else number of sampled tokens
     seed: int = 0
@@ -89,6 +89,8 @@ CONFIGS = {
                               mode="w4a4", routing="softmax", sample=1024),
     "skewed_w4a16": MoEConfig("skewed_w4a16", M=2048, H=4096, I=1536, E=128, top_k=4,
                               mode="w4a16", routing="skewed"),
+    "prefill_w4a8": MoEConfig("prefill_w4a8", M=4096, H=7168, I=2048, E=256, top_k=8,
+                              mode="w4a8", routing="softmax", sample=1024),
     "large_w4a16": MoEConfig("large_w4a16", M=131072, H=6144, I=2048, E=256, top_k=8,
                              mode="w4a16", routing="uniform", sample=1024),
 }
@@ -178,6 +180,37 @@ def quantize_nvfp4(w: torch.Tensor, gs: Optional[torch.Tensor] = None):
     return _pack_nibbles(codes), sf.view(torch.uint8), gs
 
 
+def _mx_exponents(w: torch.Tensor, emax: int) -> torch.Tensor:
+    """OCP MX shared exponents of [rows, K] along K (block 32): floor(log2 amax) -
+    emax, clamped to [-127, 127]; -127 for an all-zero block."""
+    rows, K = w.shape
+    amax = w.reshape(rows, K // 32, 32).abs().amax(dim=-1)
+    _, e = torch.frexp(amax)                                # amax = m 2^e, m in [0.5, 1)
+    X = (e.to(torch.int32) - 1) - emax
+    X = torch.where(amax > 0, X, torch.full_like(X, -127))
+    return X.clamp(-127, 127)
+
+
+def quantize_mxfp4(w: torch.Tensor):
+    """MXFP4-quantise [rows, K] along K: E2M1 codes with E8M0 block-32 scales
+    2^X, X = floor(log2 amax) - 2.  Returns (packed uint8 [rows, K/2], e8m0 [rows, K/32])."""
+    rows, K = w.shape
+    X = _mx_exponents(w, 2)
+    scaled = w.reshape(rows, K // 32, 32) * torch.exp2(-X.to(torch.float32)).unsqueeze(-1)
+    codes = _e2m1_codes(scaled.reshape(rows, K))
+    return _pack_nibbles(codes), (X + 127).to(torch.uint8)
+
+
+def quantize_mxfp8(x: torch.Tensor):
+    """MXFP8-quantise [rows, K] along K: E4M3 elements (saturating) with E8M0
+    block-32 scales 2^X, X = floor(log2 amax) - 8.  Returns (e4m3 [rows, K], e8m0 [rows, K/32])."""
+    rows, K = x.shape
+    X = _mx_exponents(x, 8)
+    scaled = x.reshape(rows, K // 32, 32) * torch.exp2(-X.to(torch.float32)).unsqueeze(-1)
+    q = scaled.clamp(-448.0, 448.0).reshape(rows, K).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), (X + 127).to(torch.uint8)
+
+
 # --------------------------------------------------------------------------
 # routing draws
 # --------------------------------------------------------------------------
@@ -251,16 +284,19 @@ def generate(cfg: MoEConfig, device="cpu", experts: Optional[int] = None) -> MoE
     gs_x = None
     if cfg.mode == "w4a16":
         x = xf.to(torch.bfloat16)
+    elif cfg.mode == "w4a8":
+        x_q, x_sf = quantize_mxfp8(xf)
     else:
         x_q, x_sf, gs_x = quantize_nvfp4(xf)
     del xf
 
     n_gen = E if experts is None else experts
     rows1 = I if activation_spec(cfg)[0] == 2 else 2 * I   # ReLU^2 has no gate rows
+    sb = 32 if cfg.mode == "w4a8" else 16                  # MXFP4 / NVFP4 scale block
     w1 = torch.empty(E, rows1, H // 2, dtype=torch.uint8, device=device)
-    w1_sf = torch.empty(E, rows1, H // 16, dtype=torch.uint8, device=device)
+    w1_sf = torch.empty(E, rows1, H // sb, dtype=torch.uint8, device=device)
     w2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
-    w2_sf = torch.empty(E, H, I // 16, dtype=torch.uint8, device=device)
+    w2_sf = torch.empty(E, H, I // sb, dtype=torch.uint8, device=device)
     gs1 = torch.ones(E, dtype=torch.float32, device=device)
     gs2 = torch.ones(E, dtype=torch.float32, device=device)
     base1, base2 = _torch_seed(ss_w1), _torch_seed(ss_w2)
@@ -268,17 +304,23 @@ def generate(cfg: MoEConfig, device="cpu", experts: Optional[int] = None) -> MoE
     for e in range(n_gen):
         g.manual_seed(base1 + e)
         W = torch.randn(rows1, H, generator=g, device=device, dtype=torch.float32) * 0.02
-        w1[e], w1_sf[e], gs1[e] = quantize_nvfp4(W)
+        if cfg.mode == "w4a8":
+            w1[e], w1_sf[e] = quantize_mxfp4(W)
+        else:
+            w1[e], w1_sf[e], gs1[e] = quantize_nvfp4(W)
         g.manual_seed(base2 + e)
         W = torch.randn(H, I, generator=g, device=device, dtype=torch.float32) * 0.02
-        w2[e], w2_sf[e], gs2[e] = quantize_nvfp4(W)
+        if cfg.mode == "w4a8":
+            w2[e], w2_sf[e] = quantize_mxfp4(W)
+        else:
+            w2[e], w2_sf[e], gs2[e] = quantize_nvfp4(W)
         del W
     if n_gen < E:
         for t in (w1, w1_sf, w2, w2_sf):
             t[n_gen:].zero_()
 
     fc2 = None
-    if cfg.mode == "w4a16":
+    if cfg.mode in ("w4a16", "w4a8"):   # MX formats carry no global scale: gs = 1
         a1 = 1.0 / gs1
         a2 = 1.0 / gs2
     else:

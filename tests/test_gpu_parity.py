@@ -324,6 +324,92 @@ def test_decode_size_geglu_full():
     check_out(f64(out), exact, 5e-3, what="decode geglu")
 
 
+# ------------------------------------------------------------------ w4a8 (MXFP8 x MXFP4)
+
+def test_mxfp8_quantiser_bit_exact_vs_oracle():
+    rng = np.random.default_rng(12)
+    n = 32 * 4096
+    mags = np.exp2(rng.integers(-40, 40, n // 32)).repeat(32)
+    h = (rng.standard_normal(n) * mags).astype(np.float32)
+    h[:32] = 0.0
+    h[32:64] = np.float32(1e-42)          # subnormal block
+    h[64] = 500.0                         # saturating block
+    h[96] = np.nan
+    h[128] = np.inf
+    q = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(n // 32, dtype=torch.uint8, device="cuda")
+    fm.debug_quantize_mxfp8(torch.from_numpy(h).cuda(), q, sf)
+    torch.cuda.synchronize()
+    oq, osf = oracle.mxfp8_quantize_f32(h)
+    assert np.array_equal(sf.cpu().numpy(), osf)
+    assert np.array_equal(q.cpu().numpy(), oq)
+
+
+@pytest.mark.parametrize("T", [16, 32])
+def test_mxfp4_prepared_weights_decode_every_code_under_every_scale(T):
+    H, I, E = 256, 256, 1
+    k = np.arange(H)
+    rows = 2 * I
+    codes = (k[None, :] + np.arange(rows)[:, None]) % 16
+    codes[::7, :32] = np.where(codes[::7, :32] >= 8, 8, 0)      # some all-zero-magnitude blocks
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)[None]
+    sf = (np.arange(rows * (H // 32)) % 256).astype(np.uint8).reshape(1, rows, H // 32)
+    w2 = np.zeros((E, H, I // 2), np.uint8)
+    sf2 = np.full((E, H, I // 32), 120, np.uint8)
+    p = fm.problem(1, H, I, E, 1, route_tile=T, mode=fm.W4A8)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    B = MoEBuffers(p).prepare(t(packed), t(sf), t(w2), t(sf2))
+    out = torch.zeros(E, rows, H, dtype=torch.bfloat16, device="cuda")
+    fm.debug_decode_prepared(p, 1, B.w1p, out)
+    torch.cuda.synchronize()
+    got = f64(out)[0]
+    from ref_decode import E2M1_TABLE
+    e = np.repeat(sf[0].astype(np.int64), 32, axis=1)
+    val = E2M1_TABLE[codes] * np.exp2((e - 127).astype(np.float64))
+    mag = (codes & 7) != 0
+    half_nonzero = mag.reshape(rows, H // 16, 16).any(-1).repeat(16, axis=1)
+    nan = (e == 255) | (((e < 106) | (e > 136)) & half_nonzero)
+    want = np.where(nan, np.nan, np.where(((e < 106) | (e > 136)) & ~half_nonzero, val * 0, val))
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(want[ok]))
+
+
+@pytest.mark.parametrize("T,act", [(16, "swiglu"), (32, "swiglu"), (32, "relu2")])
+def test_w4a8_fused_forward_tiny(T, act):
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a8", act=act)
+    inp, p, B, orc = _setup(cfg, T)
+    out = _fused(inp, B, rsf=0.5)
+    _, exact, _ = orc.forward(rsf=0.5, nthreads=NTHREADS)
+    check_out(f64(out), exact, 1e-2, strict=False, what="w4a8 %s T=%d" % (act, T))
+    # staged: the GPU's MXFP8 FC1 codes fed to the oracle's GEMM2 meet the w4a16 bar
+    ids = inp.token_selected_experts.cuda()
+    B.route(ids)
+    h, hsf = B.gemm1(inp.x_q, inp.x_sf, inp.w1_alpha, gather=True)
+    y = B.gemm2(h, hsf, inp.w2_alpha)
+    torch.cuda.synchronize()
+    p2e = B.p2e.cpu().numpy()
+    hq, hs, yv = h.cpu().numpy(), hsf.cpu().numpy(), f64(y)
+    flips = 0
+    for s in np.nonzero(p2e >= 0)[0][:16]:
+        t, j = divmod(int(p2e[s]), cfg.top_k)
+        e = int(inp.token_selected_experts[t, j])
+        st = orc.expert_ffn(e, t)
+        flips += int(np.sum(st["hq"] != hq[s]))
+        check_out(yv[s], orc.expert_down_nvfp4(e, hq[s], hs[s]), 5e-3, what="w4a8 GEMM2 slot %d" % s)
+    print("w4a8 FC1 code bytes differing from the oracle: %d" % flips)
+
+
+def test_prefill_w4a8_sampled():
+    cfg = synth.CONFIGS["prefill_w4a8"].with_(sample=256)
+    inp, p, B, orc = _setup(cfg)
+    out = _fused(inp, B)
+    toks = inp.sample_tokens
+    _, exact, _ = orc.forward(toks, nthreads=NTHREADS)
+    check_out(f64(out)[toks], exact, 1e-2, strict=False, what="prefill w4a8")
+
+
 # ------------------------------------------------------------------ atomic finalize
 
 ATOMIC = fm.FINALIZE_ATOMIC
