@@ -1,6 +1,6 @@
 """CUDA path vs the CPU oracle, through the C ABI (needs a GB300).
 
-Bars (BASELINE's north star): routing indices bit-exact; outputs per element
+Bars: routing indices bit-exact; outputs per element
 |gpu - oracle| <= 1e-2*|oracle| + 2e-3 with relative L2 <= 5e-3 (w4a16) or
 <= 2e-2 (w4a4, where the per-element count outside the bound is reported);
 large configs on the 1024 seeded sampled tokens, plus row independence.
@@ -408,6 +408,51 @@ def test_prefill_w4a8_sampled():
     toks = inp.sample_tokens
     _, exact, _ = orc.forward(toks, nthreads=NTHREADS)
     check_out(f64(out)[toks], exact, 1e-2, strict=False, what="prefill w4a8")
+
+
+# ------------------------------------------------------------------ CUDA graphs
+
+@pytest.mark.parametrize("name,T,mode", [("tiny_w4a16", 16, fm.FINALIZE_DETERMINISTIC),
+                                         ("tiny_w4a16", 32, fm.FINALIZE_DETERMINISTIC),
+                                         ("skewed_w4a16", 64, fm.FINALIZE_ATOMIC)])
+def test_fused_forward_replays_from_a_cuda_graph(name, T, mode):
+    # the library never allocates, synchronises or reads device memory on the
+    # host, so the whole forward can be captured once and replayed
+    cfg = synth.CONFIGS[name]
+    inp, p, B, orc = _setup(cfg, T)
+    ids = inp.token_selected_experts.cuda()
+    w = inp.token_final_scales.cuda()
+    x = inp.x.clone()
+    out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device="cuda")
+    B.ensure_fused_ws()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):      # warm-up outside the capture
+        B.forward(x, None, ids, w, inp.w1_alpha, inp.w2_alpha, out, finalize_mode=mode)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.forward(x, None, ids, w, inp.w1_alpha, inp.w2_alpha, out, finalize_mode=mode)
+    # new inputs in the captured buffers, then replay
+    x.copy_(torch.flip(inp.x, dims=[0]))
+    ids.copy_(torch.flip(inp.token_selected_experts, dims=[0]).cuda())
+    w.copy_(torch.flip(inp.token_final_scales, dims=[0]).cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    assert fm.read_error(B.fused_ws) == 0
+    replayed = out.clone()
+    eager = torch.zeros_like(out)
+    B.forward(x, None, ids, w, inp.w1_alpha, inp.w2_alpha, eager, finalize_mode=mode)
+    torch.cuda.synchronize()
+    if mode == fm.FINALIZE_DETERMINISTIC:
+        assert np.array_equal(bits(replayed), bits(eager))
+    else:   # atomic summation order varies; the flipped batch must still be right
+        import dataclasses
+        flipped = dataclasses.replace(inp, x=x, token_selected_experts=ids.cpu(),
+                                      token_final_scales=w.cpu())
+        _, exact, _ = oracle.OracleMoE.from_inputs(flipped, T=T).forward(nthreads=NTHREADS)
+        check_out(f64(replayed), exact, 5e-3, what="graph replay atomic")
 
 
 # ------------------------------------------------------------------ atomic finalize
