@@ -23,21 +23,55 @@ __device__ __forceinline__ uint32_t f32_to_e2m1_satfinite(float v) {
   return r & 0xFu;
 }
 
+// fp32 pair -> two E4M3 bytes / two E2M1 codes in one conversion (round to
+// nearest even, saturating): lo in bits 0..7 / 0..3, hi above
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2_satfinite(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2_satfinite(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
+      : "=h"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// The E4M3 byte (e2m1 = false) or E2M1 code (true) of RN_fp32(v / d), exactly
+// as an IEEE division followed by the conversion would give it.  Fast path:
+// t = v * RN(1/d) is within ~2^-22 (relative) of RN(v / d); when t (1 - 2^-20)
+// and t (1 + 2^-20) convert to the same code, every value between them does
+// (rounding is monotonic), RN(v / d) included.  Otherwise -- RN(v / d) next to
+// a rounding boundary or exactly on a tie, or t not finite -- divide.
+template <bool kE2M1>
+__device__ __forceinline__ uint32_t code_of_quotient(float v, float d, float rcp_d) {
+  const float t = __fmul_rn(v, rcp_d);
+  const float lo = __fmul_rn(t, 0.99999904632568359375f);  // 1 - 2^-20
+  const float hi = __fmul_rn(t, 1.00000095367431640625f);  // 1 + 2^-20
+  const uint32_t two = kE2M1 ? f32x2_to_e2m1x2_satfinite(lo, hi) : f32x2_to_e4m3x2_satfinite(lo, hi);
+  const uint32_t a = kE2M1 ? (two & 0xFu) : (two & 0xFFu);
+  const uint32_t b = kE2M1 ? ((two >> 4) & 0xFu) : ((two >> 8) & 0xFFu);
+  if (a == b && fabsf(t) <= 3.402823466e38f) return a;
+  const float q = __fdiv_rn(v, d);
+  return kE2M1 ? f32_to_e2m1_satfinite(q) : f32_to_e4m3_satfinite(q);
+}
+
 // Quantise one value of a 16-element block held by 16 consecutive lanes
 // (lanes 0-15 or 16-31 of the warp).  Every lane returns its own E2M1 code;
 // *sf receives the block's E4M3 scale byte (same in all 16 lanes).
 //   sf = E4M3((amax * s) / 6);  q = E2M1((h * s) / dec(sf));  q = 0 if dec(sf) == 0
-// Every step is an fp32 round-to-nearest operation (IEEE division).
+// Every step is an fp32 round-to-nearest operation (IEEE division), computed
+// through code_of_quotient.
 __device__ __forceinline__ uint32_t nvfp4_quant_lane16(float h, float s, uint32_t* sf) {
   float amax = fabsf(h);
 #pragma unroll
   for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-  const float t = __fdiv_rn(__fmul_rn(amax, s), 6.0f);
-  const uint32_t sc = f32_to_e4m3_satfinite(t);
+  const uint32_t sc = code_of_quotient<false>(__fmul_rn(amax, s), 6.0f, 0.16666667163372039795f);
   *sf = sc;
   const float dsf = e4m3_to_float(sc);
   if (dsf == 0.0f) return 0u;
-  return f32_to_e2m1_satfinite(__fdiv_rn(__fmul_rn(h, s), dsf));
+  return code_of_quotient<true>(__fmul_rn(h, s), dsf, __frcp_rn(dsf));
 }
 
 // Quantise one value of a 32-element MXFP8 block held by the 32 lanes of the

@@ -156,8 +156,15 @@ __global__ void round_acc(const float4* __restrict__ acc, uint4* __restrict__ ou
   launch_dependents();
 }
 
-__constant__ float kE2M1[16] = {0.0f,  0.5f,  1.0f,  1.5f,  2.0f,  3.0f,  4.0f,  6.0f,
-                                -0.0f, -0.5f, -1.0f, -1.5f, -2.0f, -3.0f, -4.0f, -6.0f};
+// E2M1 code -> its fp32 value, built from the bits: magnitude code 2e + m is
+// (1 + m/2) 2^(e-1) for e >= 1 and m/2 for e = 0 (0.5 = 2^-1: exponent field
+// 126), the sign from bit 3.  Integer operations only: no table lookup whose
+// address differs across the warp.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const uint32_t mag = e ? ((e + 126u) << 23) | (m << 22) : (m ? (126u << 23) : 0u);
+  return __uint_as_float(mag | ((c & 8u) << 28));
+}
 
 // 2^(e - 127) of an E8M0 code, NaN for 255
 __device__ __forceinline__ float e8m0_to_float(uint32_t e) {
@@ -198,7 +205,7 @@ __global__ void dequant_rows(const uint8_t* __restrict__ q, const uint8_t* __res
       const uint32_t codes = reinterpret_cast<const uint32_t*>(q)[src * (K / 8) + c];
       const float s = e4m3_to_float(sf[src * (K / 16) + c / 2]);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) f[k] = kE2M1[(codes >> (4 * k)) & 15u] * s;
+      for (int k = 0; k < 8; ++k) f[k] = e2m1_value((codes >> (4 * k)) & 15u) * s;
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k) f[k] = 0.0f;

@@ -162,6 +162,11 @@ def test_fc1_quantiser_bit_exact_vs_oracle():
     h = (rng.standard_normal(n) * mags).astype(np.float32)
     h[:16] = 0.0
     h[16:32] = np.array([6, -3, 1.5, 0.5, 0, 2, 4, -6, 1, -1, 0.25, 0.75, 5, 3.5, -2.5, 1.25])
+    # ties of both roundings: amax*s/6 = 1.0625 (an E4M3 midpoint, s = 1), and
+    # quotients on E2M1 midpoints under the non-unit block scale 1.125
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.75, -2.5, 0.5, 1, 2, 3, 4, 5.5, 6]) * 1.125
+    h[32:48] = ties
+    h[48:64] = np.array([6.375, 1.0, -1.0] + [0.5] * 13)
     for s in (1.0, 16.0, 0.0625, 3.0):
         q = torch.zeros(n // 2, dtype=torch.uint8, device="cuda")
         sf = torch.zeros(n // 16, dtype=torch.uint8, device="cuda")
