@@ -268,7 +268,9 @@ class OracleMoE:
                              _ptr(g), _ptr(u), _ptr(hp), _ptr(hi), _ptr(hq), _ptr(hsf), _ptr(y))
         return dict(g=g, u=u, h_pre=hp, h_in=hi, hq=hq, hsf=hsf, y=y)
 
-    def expert_down_nvfp4(self, e_local, hq, hsf):
+    def expert_down_codes(self, e_local, hq, hsf):
+        """GEMM2 alone from FC1 codes: NVFP4 (w4a4: hq [I/2], hsf [I/16]) or MXFP8
+        (w4a8: hq [I], hsf [I/32])."""
         y = np.zeros(self.p.H)
         hq = np.ascontiguousarray(hq, np.uint8)
         hsf = np.ascontiguousarray(hsf, np.uint8)

@@ -402,7 +402,7 @@ def test_w4a8_fused_forward_tiny(T, act):
         e = int(inp.token_selected_experts[t, j])
         st = orc.expert_ffn(e, t)
         flips += int(np.sum(st["hq"] != hq[s]))
-        check_out(yv[s], orc.expert_down_nvfp4(e, hq[s], hs[s]), 5e-3, what="w4a8 GEMM2 slot %d" % s)
+        check_out(yv[s], orc.expert_down_codes(e, hq[s], hs[s]), 5e-3, what="w4a8 GEMM2 slot %d" % s)
     print("w4a8 FC1 code bytes differing from the oracle: %d" % flips)
 
 
@@ -558,7 +558,7 @@ def test_prefill_w4a4_sampled():
         e = int(inp.token_selected_experts[t, j])
         st = orc.expert_ffn(e, t)
         flips += int(np.sum(st["hq"] != hq[s]))
-        y_ref = orc.expert_down_nvfp4(e, hq[s], hs[s])
+        y_ref = orc.expert_down_codes(e, hq[s], hs[s])
         check_out(yv[s], y_ref, 5e-3, what="w4a4 GEMM2 on GPU codes, slot %d" % s)
     print("FC1 code bytes differing from the oracle: %d of %d" % (flips, len(slots) * cfg.I // 2))
 
