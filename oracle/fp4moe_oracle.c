@@ -281,12 +281,17 @@ static void build_tables(void) {
   for (uint32_t c = 0; c < 256; ++c) g_e4m3[c] = orc_e4m3_value(c);
 }
 
-/* packed E2M1 element k of a row under E4M3 block-16 scales (NVFP4, mx = 0)
- * or E8M0 block-32 scales (MXFP4, mx = 1) */
-static double dec_w(int mx, const uint8_t* row_q, const uint8_t* row_sf, int64_t k) {
+/* the E2M1 value of packed element k of a row (element 2i in the low nibble
+ * of byte i) */
+static double e2m1_at(const uint8_t* row_q, int64_t k) {
   uint8_t byte = row_q[k / 2];
-  uint32_t code = (k & 1) ? (uint32_t)(byte >> 4) : (uint32_t)(byte & 15u);
-  return g_e2m1[code] * (mx ? orc_ue8m0_value(row_sf[k / 32]) : g_e4m3[row_sf[k / 16]]);
+  return g_e2m1[(k & 1) ? (uint32_t)(byte >> 4) : (uint32_t)(byte & 15u)];
+}
+
+/* the scale of weight block b of a row: E4M3 per 16 elements (NVFP4,
+ * mx = 0) or E8M0 per 32 elements (MXFP4, mx = 1) */
+static double w_block_scale(int mx, const uint8_t* row_sf, int64_t b) {
+  return mx ? orc_ue8m0_value(row_sf[b]) : g_e4m3[row_sf[b]];
 }
 
 static double dec_packed(const uint8_t* row_q, const uint8_t* row_sf, int64_t k) {
@@ -296,13 +301,19 @@ static double dec_packed(const uint8_t* row_q, const uint8_t* row_sf, int64_t k)
 }
 
 /* sum_k dec(W[row a])[k] * v[k] and the same for row b, each summed in
- * ascending k (two rows at a time only to overlap their latencies). */
+ * ascending k, where dec(W)[k] = E2M1 value * the scale of k's block (two
+ * rows at a time only to overlap their latencies). */
 static void dot2(int mx, const uint8_t* qa, const uint8_t* sa, const uint8_t* qb,
                  const uint8_t* sb, const double* v, int64_t K, double* ra, double* rb) {
+  const int64_t bs = mx ? 32 : 16;
   double acc_a = 0.0, acc_b = 0.0;
-  for (int64_t k = 0; k < K; ++k) {
-    acc_a += dec_w(mx, qa, sa, k) * v[k];
-    acc_b += dec_w(mx, qb, sb, k) * v[k];
+  for (int64_t k0 = 0; k0 < K; k0 += bs) {
+    const double s_a = w_block_scale(mx, sa, k0 / bs), s_b = w_block_scale(mx, sb, k0 / bs);
+    const int64_t k1 = k0 + bs < K ? k0 + bs : K;
+    for (int64_t k = k0; k < k1; ++k) {
+      acc_a += e2m1_at(qa, k) * s_a * v[k];
+      acc_b += e2m1_at(qb, k) * s_b * v[k];
+    }
   }
   *ra = acc_a;
   *rb = acc_b;
@@ -350,8 +361,13 @@ static double act_gated(const orc_problem* p, double g, double u) {
 
 /* sum_k dec(W[row])[k] * v[k] in ascending k */
 static double dot1(int mx, const uint8_t* q, const uint8_t* sf, const double* v, int64_t K) {
+  const int64_t bs = mx ? 32 : 16;
   double acc = 0.0;
-  for (int64_t k = 0; k < K; ++k) acc += dec_w(mx, q, sf, k) * v[k];
+  for (int64_t k0 = 0; k0 < K; k0 += bs) {
+    const double s = w_block_scale(mx, sf, k0 / bs);
+    const int64_t k1 = k0 + bs < K ? k0 + bs : K;
+    for (int64_t k = k0; k < k1; ++k) acc += e2m1_at(q, k) * s * v[k];
+  }
   return acc;
 }
 
