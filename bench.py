@@ -230,6 +230,39 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     ms_atomic = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
+    # ---------------- the same step over two locality domains: FC1 split on I,
+    # FC2 on H, each half on a green context holding half of the SMs
+    localized = None
+    if cfg.I % 256 == 0 and cfg.H % 256 == 0:
+        try:
+            doms = fm.Domains(local)
+        except fm.Fp4MoeError as exc:
+            localized = {"unavailable": str(exc)}
+        else:
+            B.prepare_domains(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+
+            def step_local():
+                B.forward_localized(x, inp.x_sf, ids, wts, inp.w1_alpha, inp.w2_alpha, out,
+                                    doms.streams, doms.sm_count, None, inp.fc2_input_scale,
+                                    stream=stream)
+            for _ in range(max(args.warmup, 3)):
+                step_local()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(args.steps):
+                step_local()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms_local = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+            if fm.read_error(B.local_ws):
+                raise RuntimeError("device error word in the localized forward")
+            localized = {"ms_per_step": ms_local, "value": tokens_per_s(world, cfg.M, ms_local),
+                         "unit": UNIT, "sm_per_domain": doms.sm_count,
+                         "streams": "green contexts"}
+            B.w1d = B.w2d = None
+            torch.cuda.synchronize()
+            doms.close()
+
     # ---------------- per-kernel breakdown through the staged entry points
     # (the fused call's kernels in its order: x into slot order, then GEMM1 on
     # plain row tiles; events around each launch)
@@ -352,6 +385,7 @@ def run_ours(args, rank, world, local):
         "kernels_ms": kernels,
         "atomic_finalize": {"ms_per_step": ms_atomic, "value": tokens_per_s(world, cfg.M, ms_atomic),
                             "unit": UNIT},
+        "localized": localized,
         "e2e": {"value": tokens_per_s(world, cfg.M, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clk.summary(),

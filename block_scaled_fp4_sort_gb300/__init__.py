@@ -26,6 +26,9 @@ ABI_FUNCTIONS = (
     "fp4moe_prepare_weights", "moe_route_sort", "moe_route_sort_noalloc", "moe_permute", "moe_gemm1_swiglu", "moe_gemm2",
     "moe_finalize", "fused_moe_forward", "fp4moe_debug_quantize_nvfp4",
     "fp4moe_debug_quantize_mxfp8", "fp4moe_debug_decode_prepared",
+    "fp4moe_domain_weight_size", "fp4moe_prepare_domain_weights",
+    "fp4moe_localized_workspace_size", "fused_moe_forward_localized", "fp4moe_domains_create",
+    "fp4moe_domains_stream", "fp4moe_domains_destroy",
 )
 
 
@@ -52,6 +55,13 @@ class Problem(ctypes.Structure):
                 ("top_k", ctypes.c_int32), ("num_local_experts", ctypes.c_int32),
                 ("local_expert_offset", ctypes.c_int32), ("route_tile", ctypes.c_int32),
                 ("mode", ctypes.c_int32), ("activation", Activation)]
+
+
+class Localized(ctypes.Structure):
+    """fp4moe_localized: the two domains' prepared shards and streams."""
+    _fields_ = [("w1_prepared", ctypes.c_void_p * 2), ("w2_prepared", ctypes.c_void_p * 2),
+                ("streams", ctypes.c_void_p * 2), ("sm_count", ctypes.c_int32),
+                ("memset_stream", ctypes.c_void_p)]
 
 
 def activation(type=ACT_SWIGLU, swiglu_alpha=None, swiglu_beta=None, swiglu_limit=None,
@@ -115,6 +125,14 @@ def lib() -> ctypes.CDLL:
             "fp4moe_debug_quantize_nvfp4": (i32, [vp, i64, vp, vp, vp, vp]),
             "fp4moe_debug_quantize_mxfp8": (i32, [vp, i64, vp, vp, vp]),
             "fp4moe_debug_decode_prepared": (i32, [P, i32, vp, vp, vp]),
+            "fp4moe_domain_weight_size": (sz, [P, i32]),
+            "fp4moe_prepare_domain_weights": (i32, [P, i32, vp, vp, vp, vp]),
+            "fp4moe_localized_workspace_size": (sz, [P]),
+            "fused_moe_forward_localized": (i32, [P, vp, vp, vp, vp, ctypes.POINTER(Localized), vp,
+                                                  vp, vp, vp, f32, i32, i32, vp, vp, sz, vp]),
+            "fp4moe_domains_create": (i32, [i32, i32, ctypes.POINTER(vp)]),
+            "fp4moe_domains_stream": (i32, [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(i32)]),
+            "fp4moe_domains_destroy": (i32, [vp]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -284,3 +302,73 @@ def debug_quantize_nvfp4(x, scale, q, sf, stream=None):
 def debug_decode_prepared(p: Problem, which: int, prepared, out, stream=None):
     _check(lib().fp4moe_debug_decode_prepared(ctypes.byref(p), which, _p(prepared), _p(out),
                                               _stream(stream)), "fp4moe_debug_decode_prepared")
+
+
+# ------------------------------------------------ two locality domains
+
+def domain_weight_size(p: Problem, which: int) -> int:
+    return lib().fp4moe_domain_weight_size(ctypes.byref(p), which)
+
+
+def localized_workspace_size(p: Problem) -> int:
+    return lib().fp4moe_localized_workspace_size(ctypes.byref(p))
+
+
+def prepare_domain_weights(p: Problem, which: int, w_shard, w_sf_shard, prepared, stream=None):
+    _check(lib().fp4moe_prepare_domain_weights(ctypes.byref(p), which, _p(w_shard), _p(w_sf_shard),
+                                               _p(prepared), _stream(stream)),
+           "fp4moe_prepare_domain_weights")
+
+
+def localized(w1_prepared, w2_prepared, streams, sm_count=0, memset_stream=None) -> Localized:
+    """Localized from two prepared shards per GEMM and two streams (torch
+    streams or raw cudaStream_t handles)."""
+    raw = lambda st: None if st is None else (st if isinstance(st, int) else st.cuda_stream)
+    L = Localized()
+    for d in range(2):
+        L.w1_prepared[d] = _p(w1_prepared[d])
+        L.w2_prepared[d] = _p(w2_prepared[d])
+        L.streams[d] = raw(streams[d])
+    L.sm_count = int(sm_count)
+    L.memset_stream = raw(memset_stream)
+    return L
+
+
+def fused_moe_forward_localized(p: Problem, x, x_sf, token_selected_experts, token_final_scales,
+                                loc: Localized, w1_alpha, fc2_input_scale, w2_alpha,
+                                routed_scaling_factor, accumulate, finalize_mode, out, workspace,
+                                stream=None, per_token_scale=None):
+    _check(lib().fused_moe_forward_localized(
+        ctypes.byref(p), _p(x), _p(x_sf), _p(token_selected_experts), _p(token_final_scales),
+        ctypes.byref(loc), _p(w1_alpha), _p(fc2_input_scale), _p(per_token_scale), _p(w2_alpha),
+        float(routed_scaling_factor), int(bool(accumulate)), int(finalize_mode), _p(out),
+        _p(workspace), _nbytes(workspace), _stream(stream)), "fused_moe_forward_localized")
+
+
+class Domains:
+    """Two green-context locality domains of one device (fp4moe_domains_*)."""
+
+    def __init__(self, device: int = 0, min_sm_count: int = 0):
+        h = ctypes.c_void_p()
+        _check(lib().fp4moe_domains_create(int(device), int(min_sm_count), ctypes.byref(h)),
+               "fp4moe_domains_create")
+        self._h = h
+        self.streams = []
+        self.sm_count = 0
+        for i in range(2):
+            st, n = ctypes.c_void_p(), ctypes.c_int32()
+            _check(lib().fp4moe_domains_stream(h, i, ctypes.byref(st), ctypes.byref(n)),
+                   "fp4moe_domains_stream")
+            self.streams.append(int(st.value))
+            self.sm_count = int(n.value)
+
+    def close(self):
+        if self._h is not None:
+            _check(lib().fp4moe_domains_destroy(self._h), "fp4moe_domains_destroy")
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

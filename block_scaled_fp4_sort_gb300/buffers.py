@@ -8,10 +8,12 @@ from __future__ import annotations
 
 import torch
 
-from . import (W4A4, W4A8, W4A16, FINALIZE_DETERMINISTIC, activation, fused_moe_forward,
-               gemm_workspace_size, max_permuted_slots, moe_finalize, moe_gemm1_swiglu, moe_gemm2,
-               moe_permute, moe_route_sort, prepare_weights, prepared_weight_size, problem,
-               route_tile, route_workspace_size, workspace_size)
+from . import (ACT_RELU2, W4A4, W4A8, W4A16, FINALIZE_DETERMINISTIC, activation,
+               domain_weight_size, fused_moe_forward, fused_moe_forward_localized,
+               gemm_workspace_size, localized, localized_workspace_size, max_permuted_slots,
+               moe_finalize, moe_gemm1_swiglu, moe_gemm2, moe_permute, moe_route_sort,
+               prepare_domain_weights, prepare_weights, prepared_weight_size, problem, route_tile,
+               route_workspace_size, workspace_size)
 
 
 def _empty(n, dtype, device):
@@ -47,8 +49,11 @@ class MoEBuffers:
         self.gemm1_ws = _zeros(gemm_workspace_size(p, 1), torch.uint8, d)
         self.gemm2_ws = _zeros(gemm_workspace_size(p, 2), torch.uint8, d)
         self.fused_ws = None
+        self.local_ws = None
         self.w1p = None
         self.w2p = None
+        self.w1d = None     # per-domain prepared shards (prepare_domains)
+        self.w2d = None
 
     # -- weights
     def prepare(self, w1, w1_sf, w2, w2_sf, stream=None):
@@ -57,6 +62,28 @@ class MoEBuffers:
         self.w2p = _empty(prepared_weight_size(p, 2), torch.uint8, d)
         prepare_weights(p, 1, w1, w1_sf, self.w1p, stream)
         prepare_weights(p, 2, w2, w2_sf, self.w2p, stream)
+        return self
+
+    def prepare_domains(self, w1, w1_sf, w2, w2_sf):
+        """Split the linear weights into the two locality domains' shards
+        (FC1 on I: gate rows then the matching up rows; FC2 on H) and prepare
+        each, on the current stream."""
+        p, d = self.p, self.device
+        I, H = p.inter, p.hidden
+        self.w1d, self.w2d = [], []
+        for k in range(2):
+            half = torch.arange(k * I // 2, (k + 1) * I // 2, device=w1.device)
+            rows = half if p.activation.type == ACT_RELU2 else torch.cat([half, half + I])
+            w1s = w1.index_select(1, rows).contiguous()
+            w1s_sf = w1_sf.index_select(1, rows).contiguous()
+            w2s = w2[:, k * H // 2:(k + 1) * H // 2].contiguous()
+            w2s_sf = w2_sf[:, k * H // 2:(k + 1) * H // 2].contiguous()
+            p1 = _empty(domain_weight_size(p, 1), torch.uint8, d)
+            p2 = _empty(domain_weight_size(p, 2), torch.uint8, d)
+            prepare_domain_weights(p, 1, w1s, w1s_sf, p1)
+            prepare_domain_weights(p, 2, w2s, w2s_sf, p2)
+            self.w1d.append(p1)
+            self.w2d.append(p2)
         return self
 
     def ensure_fused_ws(self):
@@ -121,6 +148,18 @@ class MoEBuffers:
         fused_moe_forward(self.p, x, x_sf, ids, token_final_scales, self.w1p, w1_alpha,
                           fc2_input_scale, self.w2p, w2_alpha, rsf, accumulate, finalize_mode, out,
                           ws, stream, per_token_scale=per_token_scale)
+        return out
+
+    def forward_localized(self, x, x_sf, ids, token_final_scales, w1_alpha, w2_alpha, out, streams,
+                          sm_count=0, memset_stream=None, fc2_input_scale=None, rsf=1.0,
+                          accumulate=False, finalize_mode=FINALIZE_DETERMINISTIC, stream=None,
+                          per_token_scale=None):
+        if self.local_ws is None:
+            self.local_ws = _zeros(localized_workspace_size(self.p), torch.uint8, self.device)
+        loc = localized(self.w1d, self.w2d, streams, sm_count, memset_stream)
+        fused_moe_forward_localized(self.p, x, x_sf, ids, token_final_scales, loc, w1_alpha,
+                                    fc2_input_scale, w2_alpha, rsf, accumulate, finalize_mode, out,
+                                    self.local_ws, stream, per_token_scale=per_token_scale)
         return out
 
 

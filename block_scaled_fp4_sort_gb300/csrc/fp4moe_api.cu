@@ -160,6 +160,57 @@ Epilogue gemm1_epilogue(const Shape& s) {
   return w4 ? kEpiSwigluNvfp4 : kEpiSwigluBf16;
 }
 
+// ---- two locality domains: FC1 shards split I, FC2 shards split H ----
+bool splits(const Shape& s) { return s.I % 256 == 0 && s.H % 256 == 0; }
+
+// the problem one shard computes: FC1 of intermediate size I/2 (its h
+// columns), FC2 of hidden size H/2 (its output columns) over the full I
+Shape domain_shape(const Shape& s, int which) {
+  Shape d = s;
+  if (which == 1) d.I = s.I / 2;
+  else d.H = s.H / 2;
+  return d;
+}
+
+// the fused workspace, a second K-split scratch (the domains' GEMMs run
+// concurrently) and an fp32 accumulator [M, H] of its own, so that the
+// atomic finalize's seed overlaps FC1
+struct LocalWs {
+  FusedWs f;
+  size_t split2, acc, total;
+};
+LocalWs local_ws(const Shape& s) {
+  LocalWs w;
+  w.f = fused_ws(s);
+  size_t o = w.f.total;
+  w.split2 = 0;
+  if (fragment_layout(s)) {
+    w.split2 = o;
+    o = up(o + kSplitBytes);
+  }
+  w.acc = o;
+  o = up(o + (size_t)s.M * s.H * 4);
+  w.total = o;
+  return w;
+}
+
+struct DomainLock {
+  DomainLock() { domain_lock(); }
+  ~DomainLock() { domain_unlock(); }
+};
+
+cudaError_t record_on(cudaStream_t st, int slot, cudaEvent_t* ev) {
+  cudaError_t e = stream_event(st, slot, ev);
+  if (e != cudaSuccess) return e;
+  StreamCtxGuard g(st);
+  return g.ok() ? cudaEventRecord(*ev, st) : cudaErrorDeviceUninitialized;
+}
+
+cudaError_t wait_on(cudaStream_t st, cudaEvent_t ev) {
+  StreamCtxGuard g(st);
+  return g.ok() ? cudaStreamWaitEvent(st, ev, 0) : cudaErrorDeviceUninitialized;
+}
+
 }  // namespace
 
 extern "C" {
@@ -479,6 +530,190 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   if (e == cudaSuccess)
     e = atomic ? launch_round_acc(s, acc, out, cs, true)
                : launch_finalize(s, ws + L.y, e2p, wts, rsf, accumulate ? 1 : 0, out, cs, true);
+  return cuda_status(e);
+}
+
+size_t fp4moe_domain_weight_size(const fp4moe_problem* p, int32_t which) {
+  Shape s;
+  if (validate(p, &s) != FP4MOE_OK || (which != 1 && which != 2) || !splits(s)) return 0;
+  return prepared_bytes(domain_shape(s, which), which);
+}
+
+fp4moe_status fp4moe_prepare_domain_weights(const fp4moe_problem* p, int32_t which,
+                                            const uint8_t* w, const uint8_t* w_sf, void* prepared,
+                                            void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  if ((which != 1 && which != 2) || !ok_ptr(w) || !ok_ptr(w_sf) || !ok_ptr(prepared))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (!splits(s)) return FP4MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_prepare(domain_shape(s, which), which, w, w_sf,
+                                    static_cast<uint8_t*>(prepared),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+size_t fp4moe_localized_workspace_size(const fp4moe_problem* p) {
+  Shape s;
+  if (validate(p, &s) != FP4MOE_OK || !splits(s)) return 0;
+  return local_ws(s).total;
+}
+
+fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x,
+                                          const uint8_t* x_sf, const int32_t* ids,
+                                          const float* wts, const fp4moe_localized* loc,
+                                          const float* w1_alpha, const float* fc2_input_scale,
+                                          const float* per_token_scale, const float* w2_alpha,
+                                          float rsf, int32_t accumulate, int32_t finalize_mode,
+                                          void* out, void* workspace, size_t workspace_bytes,
+                                          void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  const bool w4 = s.mode != FP4MOE_W4A16;
+  const bool mx = s.mode == FP4MOE_W4A8;
+  if (finalize_mode != FP4MOE_FINALIZE_DETERMINISTIC && finalize_mode != FP4MOE_FINALIZE_ATOMIC)
+    return FP4MOE_ERR_INVALID_ARG;
+  if (!loc || loc->sm_count < 0 || !ok_ptr(w1_alpha) || !ok_ptr(w2_alpha) || !ok_ptr(workspace))
+    return FP4MOE_ERR_INVALID_ARG;
+  for (int d = 0; d < 2; ++d)
+    if (!ok_ptr(loc->w1_prepared[d]) || !ok_ptr(loc->w2_prepared[d])) return FP4MOE_ERR_INVALID_ARG;
+  if (s.M > 0 && (!ok_ptr(x) || !ok_ptr(ids) || !ok_ptr(wts) || !ok_ptr(out)))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (w4 && s.M > 0 && !ok_ptr(x_sf)) return FP4MOE_ERR_INVALID_ARG;
+  if (s.mode == FP4MOE_W4A4 ? !ok_ptr(fc2_input_scale) : (mx && fc2_input_scale != nullptr))
+    return FP4MOE_ERR_INVALID_ARG;
+  if (per_token_scale && s.M > 0 && !ok_ptr(per_token_scale)) return FP4MOE_ERR_INVALID_ARG;
+  if (!splits(s)) return FP4MOE_ERR_UNSUPPORTED;
+  const LocalWs L = local_ws(s);
+  if (workspace_bytes < L.total) return FP4MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (s.M == 0) return FP4MOE_OK;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaStream_t ds[2] = {static_cast<cudaStream_t>(loc->streams[0]),
+                        static_cast<cudaStream_t>(loc->streams[1])};
+  const bool atomic = finalize_mode == FP4MOE_FINALIZE_ATOMIC;
+  cudaStream_t ms = loc->memset_stream ? static_cast<cudaStream_t>(loc->memset_stream) : cs;
+  const bool side_seed = atomic && ms != cs;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* err = err_word(ws);
+  int32_t* e2p = reinterpret_cast<int32_t*>(ws + L.f.e2p);
+  int32_t* p2e = reinterpret_cast<int32_t*>(ws + L.f.p2e);
+  int32_t* te = reinterpret_cast<int32_t*>(ws + L.f.tile_expert);
+  int32_t* tm = reinterpret_cast<int32_t*>(ws + L.f.tile_mn);
+  int32_t* nt = reinterpret_cast<int32_t*>(ws + L.f.num_tiles);
+  float* acc = reinterpret_cast<float*>(ws + L.acc);
+  float* y = reinterpret_cast<float*>(ws + L.f.y);
+  const int64_t c1 = s.I / 2, c2 = s.H / 2;   // h columns, output columns per domain
+  const Shape s1 = domain_shape(s, 1), s2 = domain_shape(s, 2);
+
+  DomainLock lock;
+  cudaError_t e = cudaSuccess;
+  cudaEvent_t ev_start = nullptr, ev_fork = nullptr, ev_seed = nullptr, ev_fc1[2], ev_fc2[2];
+  {
+    StreamCtxGuard g(cs);
+    if (!g.ok()) return FP4MOE_ERR_CUDA;
+    // the side seed reads `out` after the caller's earlier work on it
+    if (side_seed) e = record_on(cs, kEvStart, &ev_start);
+    if (e == cudaSuccess)
+      e = launch_route_sort(s, ids, e2p, p2e, te, tm, nt, nullptr, err, ws + L.f.route_scratch, cs,
+                            true);
+    // x in slot order (w4a4 / w4a8 rows expanded to BF16), as in the fused path
+    if (e == cudaSuccess)
+      e = w4 ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T, y, cs,
+                                   true, p2e, s.K, s.M, mx)
+             : launch_permute(s, x, nullptr, p2e, nt, y, nullptr, cs, true, false);
+    if (e == cudaSuccess && atomic && !side_seed)
+      e = launch_seed_acc(s, out, accumulate ? 1 : 0, acc, cs, true);
+    if (e == cudaSuccess) e = record_on(cs, kEvFork, &ev_fork);
+  }
+  if (e == cudaSuccess && side_seed) {
+    e = wait_on(ms, ev_start);
+    if (e == cudaSuccess) {
+      StreamCtxGuard g(ms);
+      e = g.ok() ? launch_seed_acc(s, out, accumulate ? 1 : 0, acc, ms, false) : cudaErrorDeviceUninitialized;
+    }
+    if (e == cudaSuccess) e = record_on(ms, kEvSeed, &ev_seed);
+  }
+  // FC1 shard d -> h columns [d c1, (d+1) c1); w4a4 / w4a8: those columns
+  // expanded to BF16 for FC2
+  for (int d = 0; d < 2 && e == cudaSuccess; ++d) {
+    e = wait_on(ds[d], ev_fork);
+    if (e != cudaSuccess) break;
+    {
+      StreamCtxGuard g(ds[d]);
+      if (!g.ok()) {
+        e = cudaErrorDeviceUninitialized;
+        break;
+      }
+      uint8_t* hq = ws + L.f.h + (s.mode == FP4MOE_W4A16 ? d * c1 * 2 : mx ? d * c1 : d * c1 / 2);
+      uint8_t* hsf = w4 ? ws + L.f.h_sf + d * c1 / (mx ? 32 : 16) : nullptr;
+      GemmLaunch g1 = {};
+      g1.which = 1;
+      g1.epi = gemm1_epilogue(s);
+      g1.wprep = static_cast<const uint8_t*>(loc->w1_prepared[d]);
+      g1.alpha = w1_alpha;
+      g1.tile_expert = te;
+      g1.tile_mn = tm;
+      g1.num_tiles = nt;
+      g1.act = y;
+      g1.act_rows = s.S;
+      g1.out = hq;
+      g1.out_sf = hsf;
+      g1.out_ld = s.I;
+      g1.fc2_scale = fc2_input_scale;
+      g1.token_scale = per_token_scale;
+      g1.p2e = p2e;
+      g1.split = fragment_layout(s) ? ws + (d == 0 ? L.f.split : L.split2) : nullptr;
+      g1.grid_limit = loc->sm_count;
+      g1.err = err;
+      e = launch_gemm(s1, g1, ds[d], false);
+      if (e == cudaSuccess && w4)
+        e = launch_dequant_rows(hq, hsf, s.S, c1, nt, s.T, ws + L.f.deq2 + d * c1 * 2, ds[d], false,
+                                nullptr, 1, 0, mx, s.I);
+    }
+    if (e == cudaSuccess) e = record_on(ds[d], kEvFc1 + d, &ev_fc1[d]);
+  }
+  // FC2 shard d -> output columns [d c2, (d+1) c2), after both FC1 shards
+  for (int d = 0; d < 2 && e == cudaSuccess; ++d) {
+    e = wait_on(ds[d], ev_fc1[1 - d]);
+    if (e == cudaSuccess && side_seed) e = wait_on(ds[d], ev_seed);
+    if (e != cudaSuccess) break;
+    {
+      StreamCtxGuard g(ds[d]);
+      if (!g.ok()) {
+        e = cudaErrorDeviceUninitialized;
+        break;
+      }
+      GemmLaunch g2 = {};
+      g2.which = 2;
+      g2.epi = atomic ? kEpiAtomicFinal : kEpiPlainBf16;
+      g2.wprep = static_cast<const uint8_t*>(loc->w2_prepared[d]);
+      g2.alpha = w2_alpha;
+      g2.tile_expert = te;
+      g2.tile_mn = tm;
+      g2.num_tiles = nt;
+      g2.act = w4 ? ws + L.f.deq2 : ws + L.f.h;
+      g2.act_rows = s.S;
+      g2.out = atomic ? acc + d * c2 : y + d * c2;
+      g2.out_ld = s.H;
+      g2.p2e = p2e;
+      g2.route_w = wts;
+      g2.rsf = rsf;
+      g2.split = fragment_layout(s) ? ws + (d == 0 ? L.f.split : L.split2) : nullptr;
+      g2.grid_limit = loc->sm_count;
+      g2.err = err;
+      e = launch_gemm(s2, g2, ds[d], false);
+    }
+    if (e == cudaSuccess) e = record_on(ds[d], kEvFc2 + d, &ev_fc2[d]);
+  }
+  for (int d = 0; d < 2 && e == cudaSuccess; ++d) e = wait_on(cs, ev_fc2[d]);
+  if (e == cudaSuccess) {
+    StreamCtxGuard g(cs);
+    if (!g.ok()) return FP4MOE_ERR_CUDA;
+    e = atomic ? launch_round_acc(s, acc, out, cs, false)
+               : launch_finalize(s, y, e2p, wts, rsf, accumulate ? 1 : 0, out, cs, false);
+  }
   return cuda_status(e);
 }
 

@@ -81,7 +81,8 @@ cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaSt
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
                                 const int32_t* row_limit_tiles, int64_t T, void* out,
                                 cudaStream_t st, bool pdl, const int32_t* gather = nullptr,
-                                int64_t top_k = 1, int64_t src_rows = 0, bool mx = false);
+                                int64_t top_k = 1, int64_t src_rows = 0, bool mx = false,
+                                int64_t ld = 0);   // row stride of q/sf/out in elements (0 = K)
 cudaError_t launch_debug_quantize_mx(const float* in, int64_t n, uint8_t* q, uint8_t* sf,
                                      cudaStream_t st);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl);
@@ -118,6 +119,8 @@ struct GemmLaunch {
   const float* fc2_scale;      // [1]
   const float* token_scale;    // per_token_scale [M] (GEMM1) or null; needs p2e
   void* split;                 // warp-MMA K-split tail scratch (kSplitBytes, zero-filled once) or null
+  int64_t out_ld;              // output row stride in elements (0: I for GEMM1, H for GEMM2)
+  int grid_limit;              // CTAs of the persistent grid at most (0: the device's SMs)
   // atomic finalize epilogue
   const int32_t* p2e;
   const float* route_w;
@@ -125,5 +128,29 @@ struct GemmLaunch {
   int* err;
 };
 cudaError_t launch_gemm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl);
+
+// ---- locality domains (domains.cu) ----
+// Runtime launches on a stream of another context (a green context's
+// stream) are made with that context current: the guard pushes the
+// stream's context when it is not the current one and pops it on exit.
+class StreamCtxGuard {
+ public:
+  explicit StreamCtxGuard(cudaStream_t st);
+  ~StreamCtxGuard();
+  bool ok() const { return ok_; }
+  StreamCtxGuard(const StreamCtxGuard&) = delete;
+  StreamCtxGuard& operator=(const StreamCtxGuard&) = delete;
+
+ private:
+  bool pushed_ = false, ok_ = true;
+};
+// An event made in the context of `st` (an event is recorded only on streams
+// of its own context), cached per context and slot; callers serialise
+// through domain_lock().
+constexpr int kEventSlots = 8;
+enum EventSlot { kEvStart = 0, kEvFork = 1, kEvSeed = 2, kEvFc1 = 3, kEvFc2 = 5 };  // Fc1/Fc2 + domain
+cudaError_t stream_event(cudaStream_t st, int slot, cudaEvent_t* ev);
+void domain_lock();
+void domain_unlock();
 
 }  // namespace fp4moe

@@ -855,6 +855,11 @@ int sm_count() {
   return n;
 }
 
+// persistent grid: one CTA per SM of the device, or of the caller's SM partition
+int64_t grid_ctas(const GemmLaunch& g) {
+  return g.grid_limit > 0 ? std::min<int64_t>(g.grid_limit, sm_count()) : sm_count();
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -899,7 +904,7 @@ cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool 
   a.top_k = (int32_t)s.K;
   a.F = (int32_t)row_blocks(s, g.which);
   a.C = (int32_t)k_chunks(s, g.which);
-  a.out_ld = g.which == 1 ? s.I : s.H;
+  a.out_ld = g.out_ld > 0 ? g.out_ld : (g.which == 1 ? s.I : s.H);
   a.valid_rows = (int32_t)(g.which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H);
   a.act = s.act;
   a.token_scale = g.token_scale;
@@ -922,7 +927,7 @@ cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool 
   if (e != cudaSuccess) return e;
   const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)std::min<int64_t>(sm_count(), max_items));
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(grid_ctas(g), max_items));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Cf::kSmem;
   cfg.stream = st;
@@ -961,7 +966,7 @@ cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
   a.top_k = (int32_t)s.K;
   a.F = (int32_t)row_blocks(s, g.which);
   a.C = (int32_t)k_chunks(s, g.which);
-  a.out_ld = g.which == 1 ? s.I : s.H;
+  a.out_ld = g.out_ld > 0 ? g.out_ld : (g.which == 1 ? s.I : s.H);
   a.valid_rows = (int32_t)(g.which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H);
   a.act = s.act;
   a.token_scale = g.token_scale;
@@ -973,7 +978,7 @@ cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
   a.route_w = g.route_w;
   a.rsf = g.rsf;
   a.err = g.err;
-  const int64_t grid = std::min<int64_t>(sm_count(), std::max<int64_t>(1, s.tiles * a.F));
+  const int64_t grid = std::min<int64_t>(grid_ctas(g), std::max<int64_t>(1, s.tiles * a.F));
   if (g.split != nullptr && grid <= kSplitMaxUnits) {
     a.split_cnt = static_cast<int32_t*>(g.split);
     a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(g.split) + kSplitCountBytes);

@@ -180,11 +180,12 @@ __device__ __forceinline__ float e8m0_to_float(uint32_t e) {
 __global__ void dequant_rows(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
                              int64_t rows, int64_t K, const int32_t* __restrict__ num_tiles,
                              int64_t T, const int32_t* __restrict__ gather, int64_t top_k,
-                             int64_t src_rows, int mx, uint4* __restrict__ out) {
+                             int64_t src_rows, int mx, int64_t ld, uint4* __restrict__ out) {
   grid_dependency_wait();
   const int64_t nrows =
       num_tiles ? min(rows, max((int64_t)num_tiles[0], (int64_t)0) * T) : rows;
-  const int64_t per_row = K / 8;
+  const int64_t per_row = K / 8;   // 8-element groups converted per row
+  const int64_t ld8 = ld / 8;      // row stride in 8-element groups
   const int64_t n = nrows * per_row;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -196,21 +197,21 @@ __global__ void dequant_rows(const uint8_t* __restrict__ q, const uint8_t* __res
     }
     float f[8];
     if (src >= 0 && mx) {
-      const uint2 b = *reinterpret_cast<const uint2*>(q + src * K + 8 * c);
-      const float s = e8m0_to_float(sf[src * (K / 32) + c / 4]);
+      const uint2 b = *reinterpret_cast<const uint2*>(q + src * ld + 8 * c);
+      const float s = e8m0_to_float(sf[src * (ld / 32) + c / 4]);
       const uint32_t w[2] = {b.x, b.y};
 #pragma unroll
       for (int k = 0; k < 8; ++k) f[k] = e4m3_to_float((w[k >> 2] >> (8 * (k & 3))) & 0xFFu) * s;
     } else if (src >= 0) {
-      const uint32_t codes = reinterpret_cast<const uint32_t*>(q)[src * (K / 8) + c];
-      const float s = e4m3_to_float(sf[src * (K / 16) + c / 2]);
+      const uint32_t codes = reinterpret_cast<const uint32_t*>(q)[src * ld8 + c];
+      const float s = e4m3_to_float(sf[src * (ld / 16) + c / 2]);
 #pragma unroll
       for (int k = 0; k < 8; ++k) f[k] = e2m1_value((codes >> (4 * k)) & 15u) * s;
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k) f[k] = 0.0f;
     }
-    out[r * per_row + c] = f32_to_bf16x8(f);
+    out[r * ld8 + c] = f32_to_bf16x8(f);
   }
   launch_dependents();
 }
@@ -307,12 +308,13 @@ cudaError_t launch_round_acc(const Shape& s, const float* acc, void* out, cudaSt
 cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t rows, int64_t K,
                                 const int32_t* row_limit_tiles, int64_t T, void* out,
                                 cudaStream_t st, bool pdl, const int32_t* gather, int64_t top_k,
-                                int64_t src_rows, bool mx) {
+                                int64_t src_rows, bool mx, int64_t ld) {
   const int64_t n = rows * (K / 8);
+  if (ld <= 0) ld = K;
   if (n == 0) return cudaSuccess;
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 16);
   return launch_pdl(dequant_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
-                    q, sf, rows, K, row_limit_tiles, T, gather, top_k, src_rows, mx ? 1 : 0,
+                    q, sf, rows, K, row_limit_tiles, T, gather, top_k, src_rows, mx ? 1 : 0, ld,
                     static_cast<uint4*>(out));
 }
 

@@ -331,6 +331,84 @@ FP4MOE_API fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* 
                                 int32_t finalize_mode, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------- two locality domains of one GPU */
+
+/* Localised execution (cute_dsl_fused_moe: localized_weights,
+ * localized_streams, localized_sm_count, localized_memset_stream): the
+ * weights are split into two equal-width shards, one per locality domain,
+ * and each domain runs its shard's GEMMs on its own stream:
+ *   FC1 shard d computes h columns [d*I/2, (d+1)*I/2).  Its w1 is the gate
+ *     rows d*I/2 .. (d+1)*I/2-1 followed by the matching up rows I + d*I/2 ..,
+ *     uint8 [E_local, I, H/2] with scales [E_local, I, H/16] (w4a8:
+ *     [.., H/32]); for FP4MOE_ACT_RELU2 the rows d*I/2 .. (d+1)*I/2-1 of w1,
+ *     [E_local, I/2, H/2].
+ *   FC2 shard d computes output columns [d*H/2, (d+1)*H/2) over the full
+ *     reduction dimension: w2 rows d*H/2 .., uint8 [E_local, H/2, I/2] with
+ *     scales [E_local, H/2, I/16] (w4a8: [.., I/32]).
+ * FC2 of either domain reads all of h, so each domain's FC2 waits for both
+ * FC1 shards.  w1_alpha, w2_alpha, fc2_input_scale and per_token_scale are
+ * shared.  Requires I and H to be multiples of 256.  Where the shards live is
+ * the caller's choice (allocate each in its domain's memory where the
+ * platform offers such placement). */
+typedef struct {
+  const void* w1_prepared[2];   /* fp4moe_prepare_domain_weights(p, 1, shard d) */
+  const void* w2_prepared[2];   /* fp4moe_prepare_domain_weights(p, 2, shard d) */
+  void* streams[2];             /* the domains' streams (cudaStream_t), e.g. fp4moe_domains_stream */
+  int32_t sm_count;             /* SMs of each domain: caps each GEMM's persistent grid; 0 = all SMs */
+  void* memset_stream;          /* FP4MOE_FINALIZE_ATOMIC: the accumulator is seeded on this stream,
+                                   overlapping FC1; NULL = the caller's stream */
+} fp4moe_localized;
+
+/* Bytes of one prepared shard of GEMM `which` (1 or 2); 0 if `p` is invalid
+ * or does not split (I or H not a multiple of 256). */
+FP4MOE_API size_t fp4moe_domain_weight_size(const fp4moe_problem* p, int32_t which);
+
+/* Prepare one shard (layouts above) into the kernel layout: the same
+ * lossless re-encoding as fp4moe_prepare_weights. */
+FP4MOE_API fp4moe_status fp4moe_prepare_domain_weights(const fp4moe_problem* p, int32_t which,
+                                                       const uint8_t* w_shard,
+                                                       const uint8_t* w_sf_shard, void* prepared,
+                                                       void* stream);
+
+/* Workspace bytes of fused_moe_forward_localized (the fused workspace, a
+ * second K-split scratch and an fp32 [M, H] accumulator). */
+FP4MOE_API size_t fp4moe_localized_workspace_size(const fp4moe_problem* p);
+
+/* fused_moe_forward over two domains.  On `stream`: route sort and x in slot
+ * order; then on domain stream d: FC1 shard d (+ its columns of h expanded to
+ * BF16 for w4a4 / w4a8), a wait for the other domain's FC1, FC2 shard d; then
+ * on `stream` again, after both domains: the finalize.  The results equal
+ * fused_moe_forward's: bit for bit for route_tile >= 32 with the
+ * deterministic finalize; for route_tile 16 the warp-MMA GEMM's K-split tail
+ * depends on the grid, so the summation order (not the terms) may differ.
+ * The first call per CUDA context creates and caches a few events in it
+ * (events are recorded only on streams of their own context).  Calls are
+ * serialised by a library lock.  Streams of green contexts are accepted:
+ * launches on them are made with their context current.  Not capturable in a
+ * CUDA graph when the domain streams belong to green contexts. */
+FP4MOE_API fp4moe_status fused_moe_forward_localized(
+    const fp4moe_problem* p, const void* x, const uint8_t* x_sf,
+    const int32_t* token_selected_experts, const float* token_final_scales,
+    const fp4moe_localized* loc, const float* w1_alpha, const float* fc2_input_scale,
+    const float* per_token_scale, const float* w2_alpha, float routed_scaling_factor,
+    int32_t accumulate, int32_t finalize_mode, void* out, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/* Two locality domains as green contexts: disjoint SM partitions of `device`
+ * of at least min_sm_count SMs each (0 = half of the SMs; the driver rounds
+ * to its partition granularity), each with a non-blocking stream.  Setup at
+ * model load: allocates the handle and the contexts.  FP4MOE_ERR_UNSUPPORTED
+ * if the driver cannot make two such partitions.  CUDA 13.0 places a
+ * partition's SMs as the driver chooses; it offers no choice of die. */
+typedef struct fp4moe_domains fp4moe_domains;
+FP4MOE_API fp4moe_status fp4moe_domains_create(int32_t device, int32_t min_sm_count,
+                                               fp4moe_domains** out);
+/* Stream of domain i (0 or 1) and the SM count of the smaller partition. */
+FP4MOE_API fp4moe_status fp4moe_domains_stream(const fp4moe_domains* d, int32_t i, void** stream,
+                                               int32_t* sm_count);
+/* Destroy the streams and contexts (no work may be pending on them). */
+FP4MOE_API fp4moe_status fp4moe_domains_destroy(fp4moe_domains* d);
+
 /* ------------------------------------------------------------ test support */
 
 /* Run the device NVFP4 quantiser of GEMM1's w4a4 epilogue on n fp32 values

@@ -179,3 +179,64 @@ def test_per_token_scale_needs_the_slot_map(lib):
         fm.moe_gemm1_swiglu(p, dev, dev, None, dev, dev, dev, dev, dev, dev, dev, dev, dev,
                             stream=0, per_token_scale=dev)
     assert ei.value.status == fm.ERR_INVALID_ARG
+
+
+def test_domain_shard_sizes(lib):
+    # FC1 shard: I/2 h columns; FC2 shard: H/2 output rows over the full I
+    for T in (16, 32):
+        p = fm.problem(8, 7168, 2048, 256, 8, route_tile=T)
+        assert 2 * fm.domain_weight_size(p, 1) == fm.prepared_weight_size(p, 1)
+        assert 2 * fm.domain_weight_size(p, 2) == fm.prepared_weight_size(p, 2)
+        # the fused workspace plus an fp32 [M, H] accumulator (and, for the
+        # warp-MMA route tile, a second K-split scratch)
+        assert fm.localized_workspace_size(p) >= fm.workspace_size(p) + 8 * 7168 * 4
+    r = fm.problem(8, 7168, 2048, 256, 8, route_tile=32, act=fm.activation(fm.ACT_RELU2))
+    assert fm.domain_weight_size(r, 1) == 256 * 4 * 56 * 18432        # I/2 rows, no gate rows
+    m = fm.problem(8, 6144, 2048, 256, 8, route_tile=32, mode=fm.W4A8)
+    assert 2 * fm.domain_weight_size(m, 2) == fm.prepared_weight_size(m, 2)
+    # I or H not a multiple of 256 does not split
+    for I, H in ((384, 7168), (2048, 384)):
+        q = fm.problem(8, H, I, 256, 8)
+        assert fm.domain_weight_size(q, 1) == 0 and fm.domain_weight_size(q, 2) == 0
+        assert fm.localized_workspace_size(q) == 0
+
+
+def test_localized_forward_rejected_on_the_host(lib):
+    class Fake:
+        def __init__(self, addr, n):
+            self.addr, self.n = addr, n
+
+        def data_ptr(self):
+            return self.addr
+
+        def numel(self):
+            return self.n
+
+        def element_size(self):
+            return 1
+    dev = Fake(1 << 20, 1 << 24)                      # an aligned address; never dereferenced
+    small_ws = Fake(1 << 20, 1024)
+    p = fm.problem(8, 256, 256, 8, 2, route_tile=32)
+    shards = [dev, dev]
+
+    def call(p, loc, ws=small_ws, fc2=None, mode=0):
+        with pytest.raises(fm.Fp4MoeError) as ei:
+            fm.fused_moe_forward_localized(p, dev, dev, dev, dev, loc, dev, fc2, dev, 1.0, False,
+                                           mode, dev, ws, stream=0)
+        return ei.value.status
+    assert call(p, fm.Localized()) == fm.ERR_INVALID_ARG                  # null shards
+    loc = fm.localized(shards, shards, [0, 0])
+    assert call(p, loc, mode=7) == fm.ERR_INVALID_ARG                      # finalize mode
+    bad = fm.localized(shards, [dev, Fake((1 << 20) + 8, 1)], [0, 0])
+    assert call(p, bad) == fm.ERR_INVALID_ARG                              # misaligned shard
+    neg = fm.localized(shards, shards, [0, 0], sm_count=-1)
+    assert call(p, neg) == fm.ERR_INVALID_ARG
+    assert call(fm.problem(8, 256, 384, 8, 2, route_tile=32), loc) == fm.ERR_UNSUPPORTED   # I % 256
+    assert call(p, loc) == fm.ERR_WORKSPACE_TOO_SMALL
+    # w4a4 needs fc2_input_scale; w4a8 takes none
+    assert call(fm.problem(8, 256, 256, 8, 2, route_tile=32, mode=fm.W4A4), loc) == fm.ERR_INVALID_ARG
+    assert call(fm.problem(8, 256, 256, 8, 2, route_tile=32, mode=fm.W4A8), loc,
+                fc2=dev) == fm.ERR_INVALID_ARG
+    with pytest.raises(fm.Fp4MoeError) as ei:
+        fm.prepare_domain_weights(fm.problem(8, 256, 384, 8, 2), 1, dev, dev, dev, stream=0)
+    assert ei.value.status == fm.ERR_UNSUPPORTED

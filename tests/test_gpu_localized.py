@@ -1,0 +1,185 @@
+"""Two-domain localised forward (cute_dsl_fused_moe: localized_weights,
+localized_streams, localized_sm_count, localized_memset_stream) through the C
+ABI, against the single-domain fused forward and the CPU oracle (needs a
+GB300).
+
+FC1 shard d computes h columns [d I/2, (d+1) I/2) and FC2 shard d output
+columns [d H/2, (d+1) H/2) over the full I, so with the tcgen05 GEMMs (route
+tile >= 32), whose K loop does not depend on the grid, every output element
+has the same terms in the same order as in the fused forward: bit-identical.
+The warp-MMA GEMM (route tile 16) splits its last K rounds by grid size, so
+there only the oracle bar applies."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_fp4_sort_gb300 as fm
+import oracle
+import synth
+from block_scaled_fp4_sort_gb300.buffers import MoEBuffers, problem_for
+
+pytestmark = pytest.mark.gpu
+NTHREADS = os.cpu_count() or 4
+ATOL, RTOL = 2e-3, 1e-2
+DET, ATOMIC = fm.FINALIZE_DETERMINISTIC, fm.FINALIZE_ATOMIC
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from block_scaled_fp4_sort_gb300 import build
+    build.build()
+    oracle.build()
+
+
+@pytest.fixture(scope="module")
+def domains():
+    d = fm.Domains(0)
+    yield d
+    torch.cuda.synchronize()
+    d.close()
+
+
+def bits(t):
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def f64(t):
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def check_out(gpu, ref, rel_l2_max, strict=True, what=""):
+    err = np.abs(gpu - ref)
+    bound = RTOL * np.abs(ref) + ATOL
+    rel = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-30)
+    nbad = int(np.sum(err > bound))
+    print("%s: rel_l2=%.3e max_err=%.3e outside=%d/%d" % (what, rel, err.max(), nbad, err.size))
+    assert np.all(np.isfinite(gpu)), what
+    assert rel <= rel_l2_max, (what, rel)
+    if strict:
+        assert nbad == 0, (what, nbad)
+
+
+def _setup(cfg, T):
+    inp = synth.generate(cfg, device="cuda")
+    p = problem_for(cfg, T)
+    B = MoEBuffers(p).prepare(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+    B.prepare_domains(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+    return inp, B
+
+
+def _args(inp):
+    x = inp.x if inp.x is not None else inp.x_q
+    return x, inp.x_sf, inp.token_selected_experts.cuda(), inp.token_final_scales.cuda()
+
+
+def _fused(inp, B, mode=DET, rsf=1.0, accumulate=False, out=None):
+    x, x_sf, ids, w = _args(inp)
+    out = torch.zeros(inp.cfg.M, inp.cfg.H, dtype=torch.bfloat16, device="cuda") if out is None else out
+    B.forward(x, x_sf, ids, w, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale, rsf, accumulate,
+              finalize_mode=mode, per_token_scale=inp.per_token_scale)
+    torch.cuda.synchronize()
+    assert fm.read_error(B.fused_ws) == 0
+    return out
+
+
+def _local(inp, B, streams, sm_count=0, memset_stream=None, mode=DET, rsf=1.0, accumulate=False,
+           out=None):
+    x, x_sf, ids, w = _args(inp)
+    out = torch.zeros(inp.cfg.M, inp.cfg.H, dtype=torch.bfloat16, device="cuda") if out is None else out
+    B.forward_localized(x, x_sf, ids, w, inp.w1_alpha, inp.w2_alpha, out, streams, sm_count,
+                        memset_stream, inp.fc2_input_scale, rsf, accumulate, mode,
+                        per_token_scale=inp.per_token_scale)
+    torch.cuda.synchronize()
+    assert fm.read_error(B.local_ws) == 0
+    return out
+
+
+def _side_streams():
+    return [torch.cuda.Stream(), torch.cuda.Stream()]
+
+
+@pytest.mark.parametrize("mode,act,T", [("w4a16", "swiglu", 32), ("w4a16", "swiglu", 128),
+                                        ("w4a4", "swiglu", 64), ("w4a8", "swiglu", 32),
+                                        ("w4a16", "relu2", 32), ("w4a4", "geglu_tanh", 32),
+                                        ("w4a16", "swiglu_oai", 64)])
+def test_localized_equals_fused_bitwise(mode, act, T):
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode=mode, act=act)
+    inp, B = _setup(cfg, T)
+    ref = _fused(inp, B, rsf=0.5)
+    for sm in (0, 40):
+        got = _local(inp, B, _side_streams(), sm_count=sm, rsf=0.5)
+        assert np.array_equal(bits(got), bits(ref)), (mode, act, T, sm)
+    _, exact, _ = oracle.OracleMoE.from_inputs(inp, T=T).forward(rsf=0.5, nthreads=NTHREADS)
+    check_out(f64(ref), exact, 5e-3 if mode == "w4a16" else 2e-2, strict=mode == "w4a16",
+              what="localized %s %s T=%d" % (mode, act, T))
+
+
+def test_localized_on_green_contexts_prefill_w4a4(domains):
+    # the pages' localised mode is W4A4: the full prefill batch on the two
+    # green-context domains equals the single-domain forward bit for bit
+    assert domains.sm_count > 0
+    cfg = synth.CONFIGS["prefill_w4a4"]
+    T = synth.route_tile_for(cfg)
+    inp, B = _setup(cfg, T)
+    ref = _fused(inp, B)
+    got = _local(inp, B, domains.streams, sm_count=domains.sm_count)
+    assert np.array_equal(bits(got), bits(ref))
+    print("domains: %d SMs each" % domains.sm_count)
+
+
+def test_localized_decode_on_green_contexts_matches_oracle(domains):
+    cfg = synth.CONFIGS["decode_w4a16"]
+    inp, B = _setup(cfg, 16)
+    got = _local(inp, B, domains.streams, sm_count=domains.sm_count)
+    _, exact, _ = oracle.OracleMoE.from_inputs(inp, T=16).forward(nthreads=NTHREADS)
+    check_out(f64(got), exact, 5e-3, what="localized decode (green contexts)")
+    again = _local(inp, B, domains.streams, sm_count=domains.sm_count)
+    assert np.array_equal(bits(got), bits(again))   # deterministic for a fixed grid
+
+
+@pytest.mark.parametrize("T", [16, 32])
+def test_localized_atomic_with_memset_stream(T, domains):
+    cfg = synth.CONFIGS["tiny_w4a16"]
+    inp, B = _setup(cfg, T)
+    ms = torch.cuda.Stream()
+    garbage = torch.full((cfg.M, cfg.H), 3.0, dtype=torch.bfloat16, device="cuda")
+    a = _local(inp, B, domains.streams, domains.sm_count, ms, mode=ATOMIC, rsf=0.75, out=garbage)
+    orc = oracle.OracleMoE.from_inputs(inp, T=T)
+    _, exact, _ = orc.forward(rsf=0.75)
+    check_out(f64(a), exact, 5e-3, what="localized atomic T=%d" % T)
+    c = _local(inp, B, domains.streams, domains.sm_count, ms, mode=ATOMIC, rsf=0.75,
+               accumulate=True, out=a.clone())
+    _, exact, _ = orc.forward(rsf=0.75, accumulate=True, out_old=bits(a))
+    check_out(f64(c), exact, 5e-3, what="localized atomic accumulate T=%d" % T)
+    # the caller's stream as the memset stream gives the same (deterministic-term) result bar
+    d = _local(inp, B, _side_streams(), 0, None, mode=ATOMIC, rsf=0.75)
+    _, exact, _ = orc.forward(rsf=0.75)
+    check_out(f64(d), exact, 5e-3, what="localized atomic, seed on the caller stream")
+
+
+def test_localized_per_token_scale_w4a4():
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a4", per_token_scale=True)
+    inp, B = _setup(cfg, 32)
+    assert inp.per_token_scale is not None
+    ref = _fused(inp, B)
+    got = _local(inp, B, _side_streams())
+    assert np.array_equal(bits(got), bits(ref))
+
+
+def test_localized_back_to_back_calls_reuse_events(domains):
+    # consecutive calls without a host synchronisation in between: the cached
+    # per-context events are re-recorded only after the waits that use them
+    cfg = synth.CONFIGS["tiny_w4a16"]
+    inp, B = _setup(cfg, 32)
+    ref = _fused(inp, B)
+    x, x_sf, ids, w = _args(inp)
+    outs = [torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device="cuda") for _ in range(6)]
+    for o in outs:
+        B.forward_localized(x, x_sf, ids, w, inp.w1_alpha, inp.w2_alpha, o, domains.streams,
+                            domains.sm_count)
+    torch.cuda.synchronize()
+    assert fm.read_error(B.local_ws) == 0
+    for o in outs:
+        assert np.array_equal(bits(o), bits(ref))
