@@ -346,9 +346,15 @@ def run_ours(args, rank, world, local):
     g1_bytes = touched * w1_bytes_per_expert + act1 + R * I * 2
     g1_ms = kernels["gemm1_swiglu"]
     g1_flops = 4.0 * R * H * I
+    # w4a4 with K a multiple of 256 and route tile >= 32 multiplies on the
+    # native NVFP4 tensor-core MMA; everything else on BF16 MMAs of decoded
+    # weights.  The FP4 peak is the measured BF16 peak times the nominal
+    # dense ratio 13.5 / 2.25 PFLOP/s.
+    native = cfg.mode == "w4a4" and T >= 32 and H % 256 == 0
+    mma_peak = peaks["bf16_tflops"] * (13.5 / 2.25 if native else 1.0)
     # the roofline of GEMM1 is the HBM rate below the ridge (peak flops / peak
-    # bytes) and the BF16 tensor rate above it (the MMAs run on decoded BF16)
-    tensor_bound = g1_flops / g1_bytes > peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    # bytes) and the tensor rate of its MMA dtype above it
+    tensor_bound = g1_flops / g1_bytes > mma_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     achieved = g1_bytes / (g1_ms * 1e-3) / 1e9
     step_bytes = touched * (w1_bytes_per_expert + w2_bytes_per_expert) + act1 + M * H * 2
     traffic_path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
@@ -363,7 +369,8 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": tokens_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": {"w4a16": "bf16", "w4a4": "nvfp4->bf16", "w4a8": "mxfp8->bf16"}[cfg.mode],
+        "dtype": ("nvfp4" if native else
+                  {"w4a16": "bf16", "w4a4": "nvfp4->bf16", "w4a8": "mxfp8->bf16"}[cfg.mode]),
         "data": "synthetic (seeded generator; random NVFP4 weights)",
         "config": dict(workload_config(cfg, T), l2="inputs larger than L2: %.2f GB of weights "
                        "per step vs 126 MB L2" % (step_bytes / 1e9), parallelism="replicas" if world > 1 else "1 GPU"),
@@ -371,17 +378,24 @@ def run_ours(args, rank, world, local):
         "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
         "roofline": dict({"kernel": ("moe_gemv_kernel<0> (GEMM1 + SwiGLU, warp MMA)"
                                      if cfg.mode == "w4a16" and T == 16 else
+                                     "moe_gemm_nvfp4_kernel<%d, 1> (GEMM1 + SwiGLU, tcgen05 "
+                                     "kind::mxf4nvf4)" % T if native else
                                      "moe_gemm_kernel<%d, %d> (GEMM1 + SwiGLU, tcgen05)"
-                                     % (T, {"w4a16": 0, "w4a4": 1, "w4a8": 6}[cfg.mode]))},
+                                     % (T, {"w4a16": 0, "w4a4": 1, "w4a8": 6}[cfg.mode])),
+                          "mma_dtype": "nvfp4" if native else "bf16"},
                          **({"bound": "tensor", "achieved": g1_flops / (g1_ms * 1e-3) / 1e12,
-                             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                             "frac": g1_flops / (g1_ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                             "peak": mma_peak, "unit": "TFLOP/s",
+                             "frac": g1_flops / (g1_ms * 1e-3) / 1e12 / mma_peak,
                              "algorithmic_flops": g1_flops}
                             if tensor_bound else
                             {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                              "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                              "algorithmic_bytes": g1_bytes}),
-                         traffic=traffic, peak_source=peak_src, touched_experts=touched),
+                         traffic=traffic, peak_source=peak_src + (" (bf16 x 13.5/2.25 nominal "
+                                                                  "fp4 ratio)" if native and tensor_bound else ""),
+                         touched_experts=touched,
+                         tensor_frac=g1_flops / (g1_ms * 1e-3) / 1e12 / mma_peak,
+                         hbm_frac=achieved / peaks["hbm_gbs"]),
         "kernels_ms": kernels,
         "atomic_finalize": {"ms_per_step": ms_atomic, "value": tokens_per_s(world, cfg.M, ms_atomic),
                             "unit": UNIT},
@@ -391,8 +405,9 @@ def run_ours(args, rank, world, local):
         "clocks": clk.summary(),
         # per fused step: routing (1 kernel up to 4096 routes, else 3), x in slot
         # order, GEMM1, the w4a4 / w4a8 h -> BF16 expansion, GEMM2, finalize
+        # (native NVFP4: h goes to GEMM2 as it is, no expansion)
         "gpu_launches": args.steps * ((1 if cfg.routes <= 4096 else 3) + 1 + 3 +
-                                      (0 if cfg.mode == "w4a16" else 1)),
+                                      (0 if cfg.mode == "w4a16" or native else 1)),
     }
     return line, inp, T
 

@@ -223,6 +223,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
 
 // ---------------------------------------------------------------- numerics
 
+// E2M1 code -> its fp32 value, built from the bits: magnitude code 2e + m is
+// (1 + m/2) 2^(e-1) for e >= 1 and m/2 for e = 0 (0.5 = 2^-1: exponent field
+// 126), the sign from bit 3.  Integer operations only: no table lookup whose
+// address differs across the warp.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const uint32_t mag = e ? ((e + 126u) << 23) | (m << 22) : (m ? (126u << 23) : 0u);
+  return __uint_as_float(mag | ((c & 8u) << 28));
+}
+
 // E4M3 byte -> float (exact).
 __device__ __forceinline__ float e4m3_to_float(uint32_t b) {
   uint32_t r;

@@ -353,9 +353,19 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   // slot order (its TMA four-row gather needs one instruction per four rows,
   // which limited GEMM1 at large tiles); the decode-size kernel gathers itself.
   const bool slot_order = gather_rows != nullptr && !fragment_layout(s);
+  const bool native = native_fp4(s, 1);
   const void* act = a;
+  const uint8_t* act_sf = nullptr;
   cudaError_t e = cudaSuccess;
-  if (w4) {
+  if (native) {
+    // NVFP4 rows copied into slot order (or as given) with every scale's sign
+    // moved into its codes, for the native tensor-core MMA
+    uint8_t* q = ws + kWsHeader;
+    uint8_t* qsf = q + up((size_t)s.S * s.H / 2);
+    e = launch_permute(s, a, a_sf, gather_rows, num_tiles, q, qsf, cs, false, true, true);
+    act = q;
+    act_sf = qsf;
+  } else if (w4) {
     e = launch_dequant_rows(static_cast<const uint8_t*>(a), a_sf, slot_order ? s.S : act_rows, s.H,
                             gather_rows && !slot_order ? nullptr : num_tiles, s.T, ws + kWsHeader,
                             cs, false, slot_order ? gather_rows : nullptr, s.K, s.M, mx);
@@ -373,9 +383,10 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   g.tile_expert = tile_expert;
   g.tile_mn = tile_mn;
   g.num_tiles = num_tiles;
-  g.gather_rows = slot_order ? nullptr : gather_rows;
+  g.gather_rows = slot_order || native ? nullptr : gather_rows;
   g.act = act;
-  g.act_rows = slot_order ? s.S : act_rows;
+  g.act_sf = act_sf;
+  g.act_rows = slot_order || native ? s.S : act_rows;
   g.out = h;
   g.out_sf = h_sf;
   g.fc2_scale = fc2_input_scale;
@@ -402,7 +413,18 @@ fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const void* act = h;
-  if (w4) {
+  const uint8_t* act_sf = nullptr;
+  if (native_fp4(s, 2)) {
+    // h as given, copied with every scale's sign moved into its codes
+    Shape hs = s;
+    hs.H = s.I;
+    uint8_t* q = ws + kWsHeader;
+    uint8_t* qsf = q + up((size_t)s.S * s.I / 2);
+    if (launch_permute(hs, h, h_sf, nullptr, num_tiles, q, qsf, cs, false, true, true) != cudaSuccess)
+      return FP4MOE_ERR_CUDA;
+    act = q;
+    act_sf = qsf;
+  } else if (w4) {
     act = ws + kWsHeader;
     cudaError_t e = launch_dequant_rows(static_cast<const uint8_t*>(h), h_sf, s.S, s.I, num_tiles,
                                         s.T, ws + kWsHeader, cs, false, nullptr, 1, 0,
@@ -418,6 +440,7 @@ fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h
   g.tile_mn = tile_mn;
   g.num_tiles = num_tiles;
   g.act = act;
+  g.act_sf = act_sf;
   g.act_rows = s.S;
   g.out = y;
   g.split = gemm_split(s, 2, ws);
@@ -480,10 +503,13 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   // are left unwritten (no result of a padding slot is stored).  Plain row
   // tiles beat the TMA four-row gather in both GEMM kernels.
   const void* xb = ws + L.y;
+  const bool native1 = native_fp4(s, 1), native2 = native_fp4(s, 2);
+  uint8_t* xsf = ws + L.y + up((size_t)s.S * s.H / 2);   // native: NVFP4 x scales
   if (e == cudaSuccess)
-    e = w4 ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
-                                 ws + L.y, cs, true, p2e, s.K, s.M, mx)
-           : launch_permute(s, x, nullptr, p2e, nt, ws + L.y, nullptr, cs, true, false);
+    e = native1 ? launch_permute(s, x, x_sf, p2e, nt, ws + L.y, xsf, cs, true, false, true)
+        : w4    ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
+                                      ws + L.y, cs, true, p2e, s.K, s.M, mx)
+                : launch_permute(s, x, nullptr, p2e, nt, ws + L.y, nullptr, cs, true, false);
   GemmLaunch g1 = {};
   g1.which = 1;
   g1.epi = gemm1_epilogue(s);
@@ -494,6 +520,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g1.num_tiles = nt;
   g1.gather_rows = nullptr;
   g1.act = xb;
+  g1.act_sf = native1 ? xsf : nullptr;
   g1.act_rows = s.S;
   g1.out = ws + L.h;
   g1.out_sf = w4 ? ws + L.h_sf : nullptr;
@@ -504,7 +531,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g1.err = err;
   if (e == cudaSuccess) e = launch_gemm(s, g1, cs, true);
   const void* hin = ws + L.h;
-  if (e == cudaSuccess && w4) {
+  if (e == cudaSuccess && w4 && !native2) {
     e = launch_dequant_rows(ws + L.h, ws + L.h_sf, s.S, s.I, nt, s.T, ws + L.deq2, cs, true,
                             nullptr, 1, 0, mx);
     hin = ws + L.deq2;
@@ -519,6 +546,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g2.tile_mn = tm;
   g2.num_tiles = nt;
   g2.act = hin;
+  g2.act_sf = native2 ? ws + L.h_sf : nullptr;
   g2.act_rows = s.S;
   g2.out = ws + L.y;
   g2.p2e = p2e;
@@ -606,6 +634,8 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
   float* y = reinterpret_cast<float*>(ws + L.f.y);
   const int64_t c1 = s.I / 2, c2 = s.H / 2;   // h columns, output columns per domain
   const Shape s1 = domain_shape(s, 1), s2 = domain_shape(s, 2);
+  const bool native1 = native_fp4(s1, 1), native2 = native_fp4(s2, 2);
+  uint8_t* xsf = reinterpret_cast<uint8_t*>(y) + up((size_t)s.S * s.H / 2);
 
   DomainLock lock;
   cudaError_t e = cudaSuccess;
@@ -618,11 +648,13 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
     if (e == cudaSuccess)
       e = launch_route_sort(s, ids, e2p, p2e, te, tm, nt, nullptr, err, ws + L.f.route_scratch, cs,
                             true);
-    // x in slot order (w4a4 / w4a8 rows expanded to BF16), as in the fused path
+    // x in slot order (NVFP4 for the native MMA; other w4a4 / w4a8 rows
+    // expanded to BF16), as in the fused path
     if (e == cudaSuccess)
-      e = w4 ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T, y, cs,
-                                   true, p2e, s.K, s.M, mx)
-             : launch_permute(s, x, nullptr, p2e, nt, y, nullptr, cs, true, false);
+      e = native1 ? launch_permute(s, x, x_sf, p2e, nt, y, xsf, cs, true, false, true)
+          : w4    ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
+                                        y, cs, true, p2e, s.K, s.M, mx)
+                  : launch_permute(s, x, nullptr, p2e, nt, y, nullptr, cs, true, false);
     if (e == cudaSuccess && atomic && !side_seed)
       e = launch_seed_acc(s, out, accumulate ? 1 : 0, acc, cs, true);
     if (e == cudaSuccess) e = record_on(cs, kEvFork, &ev_fork);
@@ -657,6 +689,7 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
       g1.tile_mn = tm;
       g1.num_tiles = nt;
       g1.act = y;
+      g1.act_sf = native1 ? xsf : nullptr;
       g1.act_rows = s.S;
       g1.out = hq;
       g1.out_sf = hsf;
@@ -668,7 +701,7 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
       g1.grid_limit = loc->sm_count;
       g1.err = err;
       e = launch_gemm(s1, g1, ds[d], false);
-      if (e == cudaSuccess && w4)
+      if (e == cudaSuccess && w4 && !native2)
         e = launch_dequant_rows(hq, hsf, s.S, c1, nt, s.T, ws + L.f.deq2 + d * c1 * 2, ds[d], false,
                                 nullptr, 1, 0, mx, s.I);
     }
@@ -693,7 +726,8 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
       g2.tile_expert = te;
       g2.tile_mn = tm;
       g2.num_tiles = nt;
-      g2.act = w4 ? ws + L.f.deq2 : ws + L.f.h;
+      g2.act = w4 && !native2 ? ws + L.f.deq2 : ws + L.f.h;
+      g2.act_sf = native2 ? ws + L.f.h_sf : nullptr;
       g2.act_rows = s.S;
       g2.out = atomic ? acc + d * c2 : y + d * c2;
       g2.out_ld = s.H;

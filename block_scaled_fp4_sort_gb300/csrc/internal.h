@@ -55,7 +55,22 @@ inline int64_t k_chunks(const Shape& s, int which) { return which == 1 ? s.H / k
 // layouts have the same block size and the same scale region.
 inline bool fragment_layout(const Shape& s) { return s.mode == 0 && s.T == 16; }
 
+// w4a4 GEMMs whose reduction is a multiple of 256 run on the native NVFP4
+// tensor-core MMA (route tiles 32..128): their prepared weights are the
+// linear codes [E_local * rows, K/2] followed by the linear E4M3 scales
+// [E_local * rows, K/16], each block's scale sign moved into its codes.
+inline bool native_fp4(const Shape& s, int which) {
+  return s.mode == 1 && s.T >= 32 && (which == 1 ? s.H : s.I) % 256 == 0;
+}
+inline int64_t native_rows(const Shape& s, int which) {
+  return which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H;
+}
+
 inline size_t prepared_bytes(const Shape& s, int which) {
+  if (native_fp4(s, which)) {
+    const int64_t K = which == 1 ? s.H : s.I;
+    return (size_t)s.EL * native_rows(s, which) * (K / 2 + K / 16);
+  }
   return (size_t)s.EL * row_blocks(s, which) * k_chunks(s, which) * kWBlockBytes;
 }
 
@@ -70,7 +85,11 @@ cudaError_t launch_route_sort(const Shape& s, const int32_t* ids, int32_t* e2p, 
 // ---- elementwise steps (permute.cu) ----
 cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, const int32_t* p2e,
                            const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
-                           bool pdl, bool zero_pad = true);
+                           bool pdl, bool zero_pad = true, bool canon = false);
+// canon (NVFP4 rows): a block whose scale has the sign bit set is stored with
+// the sign moved into its 16 codes (the same values; the native MMA reads
+// scales unsigned).  p2e may be null: row s of x is row s (rows already in
+// slot order), for a canonical copy.
 cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, const float* w,
                             float rsf, int accumulate, void* out, cudaStream_t st, bool pdl);
 // atomic finalize: fp32 accumulator [M, H] seeded from out (or +0), rounded into out
@@ -112,7 +131,9 @@ struct GemmLaunch {
   const int32_t* tile_mn;
   const int32_t* num_tiles;
   const int32_t* gather_rows;  // GEMM1 row gather (permuted_idx_to_expanded_idx) or null
-  const void* act;             // bf16 activations: x [M, K] (gather) or permuted [S, K]
+  const void* act;             // bf16 activations: x [M, K] (gather) or permuted [S, K];
+                               //   native NVFP4 GEMM: E2M1 codes [S, K/2] in slot order
+  const uint8_t* act_sf;       //   native NVFP4 GEMM: their E4M3 scales [S, K/16]
   int64_t act_rows;            // rows of `act`
   void* out;                   // h bf16 [S, I] | hq [S, I/2] | y bf16 [S, H] | out bf16 [M, H]
   uint8_t* out_sf;             // hsf [S, I/16]

@@ -68,8 +68,23 @@ struct GemmArgs {
   const int32_t* p2e;          // atomic finalize: route of each slot
   const float* route_w;        //   token_final_scales [M, top_k]
   float rsf;                   //   routed_scaling_factor
+  int32_t a_rows;              // native NVFP4 GEMM: weight rows per expert in the prepared layout
+  int32_t up_rows;             //   gated GEMM1: offset of the up rows (I), else 0
   int* err;
 };
+
+// The FC1 NVFP4 quantiser of the epilogues, with a negative block scale (only
+// a negative fc2_input_scale gives one) stored as its magnitude and the sign
+// moved into the codes: the same values, in the form the native NVFP4 MMA
+// reads (it takes scale bytes unsigned).
+__device__ __forceinline__ uint32_t nvfp4_quant_canonical(float h, float s, uint32_t* sf) {
+  uint32_t code = nvfp4_quant_lane16(h, s, sf);
+  if (*sf & 0x80u) {
+    code ^= 8u;
+    *sf &= 0x7Fu;
+  }
+  return code;
+}
 
 // Atomic finalize (kEpiAtomicFinal): the GEMM2 value of slot s at output
 // column n goes straight into the fp32 token accumulator,
@@ -126,6 +141,110 @@ struct Cfg {
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kStages >= 2, "pipeline depth");
 };
+
+// Epilogue of the tcgen05 GEMMs: fp32 accumulators [128 weight rows x BN
+// slots] per 128-row tile in TMEM (tile 0 at column 0, tile 1 at column BN),
+// times `scale` (alpha, with any decode factor undone); thread t of the 256
+// epilogue threads owns row `row` of tile `tile` (its warp's TMEM lanes).
+template <int BN, int EPI>
+__device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, uint32_t lane_base,
+                                            int32_t tau, int32_t f, float scale, int warp,
+                                            int lane, int tile, int row) {
+  const int32_t mn = a.tile_mn[tau];
+  const int64_t s0 = (int64_t)tau * BN;
+  if (EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal) {
+    const int64_t n = (int64_t)f * 256 + tile * 128 + row;
+    float* y = static_cast<float*>(a.out);   // fp32 route storage
+#pragma unroll 1
+    for (int cc = 0; cc < BN; cc += 16) {
+      uint32_t v[16];
+      tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc), v);
+      tmem_wait_ld();
+      if (n < a.valid_rows) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int64_t s = s0 + cc + i;
+          if (s >= mn) continue;
+          const float yv = __uint_as_float(v[i]) * scale;
+          if (EPI == kEpiPlainBf16)
+            y[s * a.out_ld + n] = yv;
+          else
+            atomic_final_add(a, s, n, yv);
+        }
+      }
+    }
+  } else if (EPI == kEpiRelu2Bf16 || EPI == kEpiRelu2Nvfp4 || EPI == kEpiRelu2Mxfp8) {
+    // non-gated FC1: both 128-row tiles are outputs, feature n per thread
+    const int64_t n = (int64_t)f * 256 + tile * 128 + row;
+    const float fs = EPI == kEpiRelu2Nvfp4 ? a.fc2_scale[0] : 0.0f;
+    if (n < a.valid_rows) {  // warp-uniform: I is a multiple of 128
+#pragma unroll 1
+      for (int cc = 0; cc < BN; cc += 16) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc), v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int64_t s = s0 + cc + i;
+          const float hv = s < mn ? relu2(__uint_as_float(v[i]) * scale * token_factor(a, s)) : 0.0f;
+          if (EPI == kEpiRelu2Bf16) {
+            static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] = __float2bfloat16_rn(hv);
+          } else if (EPI == kEpiRelu2Mxfp8) {  // the warp's 32 rows are one MXFP8 block
+            uint32_t sf;
+            const uint32_t code = mxfp8_quant_warp(hv, &sf);
+            static_cast<uint8_t*>(a.out)[s * a.out_ld + n] = (uint8_t)code;
+            if (lane == 0) a.out_sf[s * (a.out_ld / 32) + n / 32] = (uint8_t)sf;
+          } else {
+            uint32_t sf;
+            const uint32_t code = nvfp4_quant_canonical(hv, fs, &sf);
+            const uint32_t other = __shfl_down_sync(0xffffffffu, code, 1);
+            if ((lane & 1) == 0)
+              static_cast<uint8_t*>(a.out)[s * (a.out_ld / 2) + n / 2] = (uint8_t)(code | (other << 4));
+            if ((lane & 15) == 0) a.out_sf[s * (a.out_ld / 16) + n / 16] = (uint8_t)sf;
+          }
+        }
+      }
+    }
+  } else {
+    constexpr int kCols = BN >= 32 ? BN / 2 : BN;
+    if (BN >= 32 || warp < 4) {
+      const int cbase = (BN >= 32 && warp >= 4) ? kCols : 0;
+      const int64_t n = (int64_t)f * 128 + row;
+      const float fs = EPI == kEpiSwigluNvfp4 ? a.fc2_scale[0] : 0.0f;
+#pragma unroll 1
+      for (int cc = 0; cc < kCols; cc += 16) {
+        uint32_t g[16], u[16];
+        tmem_ld16(tmem + lane_base + (uint32_t)(cbase + cc), g);
+        tmem_ld16(tmem + lane_base + (uint32_t)(BN + cbase + cc), u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int64_t s = s0 + cbase + cc + i;
+          float hv = 0.0f;
+          if (s < mn) {
+            const float sc = scale * token_factor(a, s);
+            hv = gemm1_act(a, __uint_as_float(g[i]) * sc, __uint_as_float(u[i]) * sc);
+          }
+          if (EPI == kEpiSwigluBf16) {
+            static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] = __float2bfloat16_rn(hv);
+          } else if (EPI == kEpiSwigluMxfp8) {  // the warp's 32 rows are one MXFP8 block
+            uint32_t sf;
+            const uint32_t code = mxfp8_quant_warp(hv, &sf);
+            static_cast<uint8_t*>(a.out)[s * a.out_ld + n] = (uint8_t)code;
+            if (lane == 0) a.out_sf[s * (a.out_ld / 32) + n / 32] = (uint8_t)sf;
+          } else {
+            uint32_t sf;
+            const uint32_t code = nvfp4_quant_canonical(hv, fs, &sf);
+            const uint32_t other = __shfl_down_sync(0xffffffffu, code, 1);
+            if ((lane & 1) == 0)
+              static_cast<uint8_t*>(a.out)[s * (a.out_ld / 2) + n / 2] = (uint8_t)(code | (other << 4));
+            if ((lane & 15) == 0) a.out_sf[s * (a.out_ld / 16) + n / 16] = (uint8_t)sf;
+          }
+        }
+      }
+    }
+  }
+}
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -336,101 +455,271 @@ __global__ void __launch_bounds__(kThreads, 1)
       accphase ^= 1u;
       tc_fence_after();
       const int32_t e = plan_expert_quiet(a, tau);
-      const int32_t mn = a.tile_mn[tau];
-      const float scale = a.alpha[e] * 256.0f;  // undo the decode's 2^-8
-      const int64_t s0 = (int64_t)tau * BN;
-      if (EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal) {
-        const int64_t n = (int64_t)f * 256 + tile * 128 + row;
-        float* y = static_cast<float*>(a.out);   // fp32 route storage
-#pragma unroll 1
-        for (int cc = 0; cc < BN; cc += 16) {
-          uint32_t v[16];
-          tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc), v);
-          tmem_wait_ld();
-          if (n < a.valid_rows) {
+      tc_epilogue<BN, EPI>(a, tmem, lane_base, tau, f, a.alpha[e] * 256.0f, warp, lane, tile, row);  // undo the decode's 2^-8
+      tc_fence_before();
+    }
+  }
+
+  __syncthreads();
+  launch_dependents();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ===========================================================================
+// Native NVFP4 grouped GEMM (w4a4): tcgen05.mma.kind::mxf4nvf4.block_scale.
+//
+// What is computed is the same as above, without the BF16 decode: the tensor
+// cores take E2M1 codes and their E4M3 block-16 scales directly (four times
+// the BF16 MMA rate), so the weights stream from memory as they are stored.
+//   A = 128 weight rows (K-major E2M1, 128-byte-swizzled shared memory, one
+//       128-byte row = 256 elements per chunk); B = the tile's BN NVFP4
+//       activation rows in slot order, likewise.
+//   Scale factors in tensor memory: for each 64-element K step, 4 columns x
+//       32 lanes per 128 rows -- row r in lane r % 32 of column r / 32, its
+//       four block scales in the four bytes -- present in all four lane
+//       quarters; consecutive K steps 4 columns apart.  The hardware reads a
+//       scale byte as an unsigned E4M3 (the sign bit is ignored; 0x7F/0xFF are
+//       NaN), so the sign of a negative scale is moved into the codes before
+//       (weight preparation, the slot-order copy of the activations).
+// Per CTA (persistent, 320 threads): warp 8 issues the TMA copies of a chunk
+// (two weight tiles, the activation tile and the three scale tiles), warps
+// 0-7 move the chunk's scales from shared into tensor memory (warps 0-3: the
+// weight scales, warps 4-7: the activation scales, each warp into its lane
+// quarter) and run the epilogue, warp 9 issues 8 MMAs per chunk (2 tiles x 4
+// K steps) and one commit.
+// ===========================================================================
+template <int BN>
+struct NCfg {
+  static constexpr int kAData = 128 * 128;        // one 128-row tile, 256 K elements
+  static constexpr int kBData = BN * 128;
+  static constexpr int kASf = 128 * 16;           // 16 block scales per row and chunk
+  static constexpr int kBSf = BN * 16;
+  static constexpr int kTx = 2 * kAData + kBData + 2 * kASf + kBSf;
+  static constexpr int kStage = (kTx + 1023) / 1024 * 1024;
+  static constexpr int kStagesRaw = (220 * 1024) / kStage;
+  static constexpr int kStages = kStagesRaw > 5 ? 5 : kStagesRaw;
+  static constexpr int kSfBase = 256;             // TMEM column of the scale ring
+  static constexpr int kSfCols = 48;              // per stage: A tile 0, A tile 1, B
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes;
+  static_assert(kSfBase + kStages * kSfCols <= 512, "tensor memory");
+  static_assert(2 * BN <= kSfBase, "accumulators");
+  static_assert(kStages >= 2, "pipeline depth");
+};
+
+__device__ __forceinline__ void mma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::mxf4nvf4: A and B E2M1, K-major, unsigned
+// E4M3 scales, scale-factor slots 0.
+__host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N) {
+  return (1u << 7)                       // A format: E2M1
+         | (1u << 10)                    // B format: E2M1
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// four 16-byte rows (r, r+32, r+64, r+96 of a 16-byte-per-row scale tile) into
+// the 16 registers of one 32x32b.x16 store: column 4 ks + m1 <- word ks of row
+// l + 32 m1; rows at or past `rows` give zero
+__device__ __forceinline__ void sf_regs(const uint8_t* tile, int l, int rows, uint32_t (&v)[16]) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int64_t s = s0 + cc + i;
-              if (s >= mn) continue;
-              const float yv = __uint_as_float(v[i]) * scale;
-              if (EPI == kEpiPlainBf16)
-                y[s * a.out_ld + n] = yv;
-              else
-                atomic_final_add(a, s, n, yv);
-            }
+  for (int m1 = 0; m1 < 4; ++m1) {
+    const int r = l + 32 * m1;
+    const uint4 q = r < rows ? *reinterpret_cast<const uint4*>(tile + r * 16) : make_uint4(0, 0, 0, 0);
+    v[0 + m1] = q.x;
+    v[4 + m1] = q.y;
+    v[8 + m1] = q.z;
+    v[12 + m1] = q.w;
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_gemm_nvfp4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap amap,
+                          const __grid_constant__ CUtensorMap asfmap,
+                          const __grid_constant__ CUtensorMap bmap,
+                          const __grid_constant__ CUtensorMap bsfmap) {
+  using C = NCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* sfready = empty + C::kStages;
+  uint64_t* accfull = sfready + C::kStages;
+  uint64_t* drain = accfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&sfready[i], kDecodeWarps);
+    }
+    mbar_init(accfull, 1);
+    mbar_init(drain, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    prefetch_tensormap(&amap);
+    prefetch_tensormap(&asfmap);
+    prefetch_tensormap(&bmap);
+    prefetch_tensormap(&bsfmap);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  grid_dependency_wait();
+  const int64_t n_items = plan_items(a);
+  // stage layout: A tile 0 | A tile 1 | B | A scales tile 0 | tile 1 | B scales
+  constexpr int kOffB = 2 * C::kAData;
+  constexpr int kOffASf = kOffB + C::kBData;
+  constexpr int kOffBSf = kOffASf + 2 * C::kASf;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    int stage = 0;
+    uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
+    bool ok = true;
+    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
+      const int32_t e = plan_expert(a, tau);
+      const int32_t row0 = e * a.a_rows + (a.up_rows ? 128 * f : 256 * f);
+      const int32_t row1 = a.up_rows ? e * a.a_rows + a.up_rows + 128 * f : row0 + 128;
+      for (int c = 0; c < a.C; ++c) {
+        if (lane == 0) {
+          ok = mbar_wait(&empty[stage], phase ^ 1u, a.err);
+          if (ok) {
+            uint8_t* st = stages + stage * C::kStage;
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)C::kTx);
+            tma_load_2d(st, &amap, c * 128, row0, &full[stage]);
+            tma_load_2d(st + C::kAData, &amap, c * 128, row1, &full[stage]);
+            tma_load_2d(st + kOffB, &bmap, c * 128, tau * BN, &full[stage]);
+            tma_load_2d(st + kOffASf, &asfmap, c * 16, row0, &full[stage]);
+            tma_load_2d(st + kOffASf + C::kASf, &asfmap, c * 16, row1, &full[stage]);
+            tma_load_2d(st + kOffBSf, &bsfmap, c * 16, tau * BN, &full[stage]);
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
         }
-      } else if (EPI == kEpiRelu2Bf16 || EPI == kEpiRelu2Nvfp4 || EPI == kEpiRelu2Mxfp8) {
-        // non-gated FC1: both 128-row tiles are outputs, feature n per thread
-        const int64_t n = (int64_t)f * 256 + tile * 128 + row;
-        const float fs = EPI == kEpiRelu2Nvfp4 ? a.fc2_scale[0] : 0.0f;
-        if (n < a.valid_rows) {  // warp-uniform: I is a multiple of 128
-#pragma unroll 1
-          for (int cc = 0; cc < BN; cc += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc), v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int64_t s = s0 + cc + i;
-              const float hv = s < mn ? relu2(__uint_as_float(v[i]) * scale * token_factor(a, s)) : 0.0f;
-              if (EPI == kEpiRelu2Bf16) {
-                static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] = __float2bfloat16_rn(hv);
-              } else if (EPI == kEpiRelu2Mxfp8) {  // the warp's 32 rows are one MXFP8 block
-                uint32_t sf;
-                const uint32_t code = mxfp8_quant_warp(hv, &sf);
-                static_cast<uint8_t*>(a.out)[s * a.out_ld + n] = (uint8_t)code;
-                if (lane == 0) a.out_sf[s * (a.out_ld / 32) + n / 32] = (uint8_t)sf;
-              } else {
-                uint32_t sf;
-                const uint32_t code = nvfp4_quant_lane16(hv, fs, &sf);
-                const uint32_t other = __shfl_down_sync(0xffffffffu, code, 1);
-                if ((lane & 1) == 0)
-                  static_cast<uint8_t*>(a.out)[s * (a.out_ld / 2) + n / 2] = (uint8_t)(code | (other << 4));
-                if ((lane & 15) == 0) a.out_sf[s * (a.out_ld / 16) + n / 16] = (uint8_t)sf;
-              }
-            }
-          }
-        }
-      } else {
-        constexpr int kCols = BN >= 32 ? BN / 2 : BN;
-        if (BN >= 32 || warp < 4) {
-          const int cbase = (BN >= 32 && warp >= 4) ? kCols : 0;
-          const int64_t n = (int64_t)f * 128 + row;
-          const float fs = EPI == kEpiSwigluNvfp4 ? a.fc2_scale[0] : 0.0f;
-#pragma unroll 1
-          for (int cc = 0; cc < kCols; cc += 16) {
-            uint32_t g[16], u[16];
-            tmem_ld16(tmem + lane_base + (uint32_t)(cbase + cc), g);
-            tmem_ld16(tmem + lane_base + (uint32_t)(BN + cbase + cc), u);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int64_t s = s0 + cbase + cc + i;
-              float hv = 0.0f;
-              if (s < mn) {
-                const float sc = scale * token_factor(a, s);
-                hv = gemm1_act(a, __uint_as_float(g[i]) * sc, __uint_as_float(u[i]) * sc);
-              }
-              if (EPI == kEpiSwigluBf16) {
-                static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] = __float2bfloat16_rn(hv);
-              } else if (EPI == kEpiSwigluMxfp8) {  // the warp's 32 rows are one MXFP8 block
-                uint32_t sf;
-                const uint32_t code = mxfp8_quant_warp(hv, &sf);
-                static_cast<uint8_t*>(a.out)[s * a.out_ld + n] = (uint8_t)code;
-                if (lane == 0) a.out_sf[s * (a.out_ld / 32) + n / 32] = (uint8_t)sf;
-              } else {
-                uint32_t sf;
-                const uint32_t code = nvfp4_quant_lane16(hv, fs, &sf);
-                const uint32_t other = __shfl_down_sync(0xffffffffu, code, 1);
-                if ((lane & 1) == 0)
-                  static_cast<uint8_t*>(a.out)[s * (a.out_ld / 2) + n / 2] = (uint8_t)(code | (other << 4));
-                if ((lane & 15) == 0) a.out_sf[s * (a.out_ld / 16) + n / 16] = (uint8_t)sf;
-              }
-            }
-          }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
+    }
+    if (lane == 0)
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_parity >> s) & 1u, a.err);
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_nvfp4(128, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        for (int c = 0; c < a.C; ++c) {
+          if (!mbar_wait(&full[stage], phase, a.err) || !mbar_wait(&sfready[stage], phase, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(stages + stage * C::kStage);
+          const uint32_t sf = tmem + (uint32_t)(C::kSfBase + stage * C::kSfCols);
+#pragma unroll
+          for (int tile = 0; tile < 2; ++tile) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = smem_desc_sw128(st + tile * C::kAData + ks * 32);
+              const uint64_t bd = smem_desc_sw128(st + kOffB + ks * 32);
+              mma_nvfp4(tmem + (uint32_t)(tile * BN), ad, bd, kIdesc, sf + tile * 16 + ks * 4,
+                        sf + 32 + ks * 4, (c > 0 || ks > 0) ? 1u : 0u);
+            }
+          }
+          tc_commit(&empty[stage]);   // frees the shared-memory stage and its scale columns
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit(accfull);
+      }
+      tc_commit(drain);
+      mbar_wait(drain, 0, a.err);
+    }
+  } else {
+    // ------------------------------------------------------------ scales + epilogue
+    const int t = threadIdx.x;  // 0..255
+    const int tile = t >> 7, row = t & 127;
+    const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
+    int stage = 0;
+    uint32_t phase = 0, accphase = 0;
+    bool ok = true;
+    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
+      for (int c = 0; c < a.C; ++c) {
+        // the stage's copies have landed; its scale columns were last read by
+        // the MMAs of the chunk kStages earlier, which completed before the
+        // producer could refill the stage
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) {
+          ok = false;
+          break;
+        }
+        const uint8_t* st = stages + stage * C::kStage;
+        const uint32_t col = tmem + lane_base + (uint32_t)(C::kSfBase + stage * C::kSfCols);
+        uint32_t v[16];
+        if (warp < 4) {
+          sf_regs(st + kOffASf, lane, 128, v);
+          tmem_st16(col, v);
+          sf_regs(st + kOffASf + C::kASf, lane, 128, v);
+          tmem_st16(col + 16, v);
+        } else {
+          sf_regs(st + kOffBSf, lane, BN, v);
+          tmem_st16(col + 32, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfready[stage]);
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(accfull, accphase, a.err))) {
+        ok = false;
+        break;
+      }
+      accphase ^= 1u;
+      tc_fence_after();
+      const int32_t e = plan_expert_quiet(a, tau);
+      tc_epilogue<BN, EPI>(a, tmem, lane_base, tau, f, a.alpha[e], warp, lane, tile, row);
       tc_fence_before();
     }
   }
@@ -891,6 +1180,85 @@ bool make_act_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// byte matrix [rows, row_bytes] -> tensor map with box {box_x bytes, box_rows}
+bool make_u8_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t row_bytes, int box_x,
+                 int box_rows, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)std::max<int64_t>(rows, 1)};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)box_x, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  using Cf = NCfg<BN>;
+  GemmArgs a = {};
+  a.wprep = g.wprep;
+  a.alpha = g.alpha;
+  a.tile_expert = g.tile_expert;
+  a.tile_mn = g.tile_mn;
+  a.num_tiles = g.num_tiles;
+  a.top_k = (int32_t)s.K;
+  a.F = (int32_t)row_blocks(s, g.which);
+  a.C = (int32_t)((g.which == 1 ? s.H : s.I) / 256);
+  a.out_ld = g.out_ld > 0 ? g.out_ld : (g.which == 1 ? s.I : s.H);
+  a.valid_rows = (int32_t)(g.which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H);
+  a.act = s.act;
+  a.token_scale = g.token_scale;
+  a.out = g.out;
+  a.out_sf = g.out_sf;
+  a.fc2_scale = g.fc2_scale;
+  a.max_tiles = (int32_t)s.tiles;
+  a.EL = (int32_t)s.EL;
+  a.R = s.R;
+  a.p2e = g.p2e;
+  a.route_w = g.route_w;
+  a.rsf = g.rsf;
+  a.a_rows = (int32_t)native_rows(s, g.which);
+  a.up_rows = (int32_t)(g.which == 1 && gated(s) ? s.I : 0);
+  a.err = g.err;
+  const int64_t K = g.which == 1 ? s.H : s.I;
+  const int64_t wrows = s.EL * a.a_rows;
+  CUtensorMap amap, asfmap, bmap, bsfmap;
+  if (!make_u8_map(&amap, g.wprep, wrows, K / 2, 128, 128, true) ||
+      !make_u8_map(&asfmap, g.wprep + wrows * (K / 2), wrows, K / 16, 16, 128, false) ||
+      !make_u8_map(&bmap, g.act, g.act_rows, K / 2, 128, BN, true) ||
+      !make_u8_map(&bsfmap, g.act_sf, g.act_rows, K / 16, 16, BN, false))
+    return cudaErrorInvalidValue;
+  auto kern = moe_gemm_nvfp4_kernel<BN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
+  if (e != cudaSuccess) return e;
+  const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min<int64_t>(grid_ctas(g), max_items));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cf::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, amap, asfmap, bmap, bsfmap);
+}
+
+template <int BN>
+cudaError_t launch_native_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  switch (g.epi) {
+    case kEpiSwigluNvfp4: return launch_native_t<BN, kEpiSwigluNvfp4>(s, g, st, pdl);
+    case kEpiRelu2Nvfp4: return launch_native_t<BN, kEpiRelu2Nvfp4>(s, g, st, pdl);
+    case kEpiPlainBf16: return launch_native_t<BN, kEpiPlainBf16>(s, g, st, pdl);
+    case kEpiAtomicFinal: return launch_native_t<BN, kEpiAtomicFinal>(s, g, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <int BN, int EPI>
 cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
   using Cf = Cfg<BN>;
@@ -1007,6 +1375,15 @@ cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
 }  // namespace
 
 cudaError_t launch_gemm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  if (native_fp4(s, g.which)) {
+    if (g.act_sf == nullptr) return cudaErrorInvalidValue;
+    switch (s.T) {
+      case 32: return launch_native_bn<32>(s, g, st, pdl);
+      case 64: return launch_native_bn<64>(s, g, st, pdl);
+      case 128: return launch_native_bn<128>(s, g, st, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (fragment_layout(s)) {
     switch (g.epi) {
       case kEpiSwigluBf16: return launch_gv<kEpiSwigluBf16>(s, g, st, pdl);

@@ -49,8 +49,8 @@ int num_sms() {
 __global__ void permute_rows(const uint8_t* __restrict__ x, const uint8_t* __restrict__ x_sf,
                              const int32_t* __restrict__ p2e, const int32_t* __restrict__ num_tiles,
                              int64_t T, int64_t top_k, int64_t row_bytes, int64_t sf_bytes,
-                             int zero_pad, int64_t S, int64_t M, uint8_t* __restrict__ px,
-                             uint8_t* __restrict__ px_sf) {
+                             int zero_pad, int canon, int64_t S, int64_t M,
+                             uint8_t* __restrict__ px, uint8_t* __restrict__ px_sf) {
   grid_dependency_wait();
   // a tile count or slot entry from outside [0, S) / [0, M*top_k) is not followed
   const int64_t rows = min(max((int64_t)num_tiles[0], (int64_t)0) * T, S);
@@ -58,11 +58,46 @@ __global__ void permute_rows(const uint8_t* __restrict__ x, const uint8_t* __res
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t s = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); s < rows;
        s += warps) {
-    const int32_t r = p2e[s];
-    const int64_t src = r >= 0 && r < M * top_k ? r / top_k : -1;
+    int64_t src = s;  // no slot map: the rows are already in slot order
+    if (p2e != nullptr) {
+      const int32_t r = p2e[s];
+      src = r >= 0 && r < M * top_k ? r / top_k : -1;
+    }
     if (src < 0 && !zero_pad) continue;
     uint4* dst = reinterpret_cast<uint4*>(px + s * row_bytes);
     const uint4* sp = reinterpret_cast<const uint4*>(x + src * row_bytes);
+    if (canon) {
+      // NVFP4, four 16-element blocks per step: 32 code bytes (block j in
+      // words 2j, 2j+1) and 4 scale bytes; a negative scale's sign goes into
+      // its block's codes
+      uint32_t* dsf = reinterpret_cast<uint32_t*>(px_sf + s * sf_bytes);
+      const uint32_t* ssf = reinterpret_cast<const uint32_t*>(x_sf + src * sf_bytes);
+      for (int64_t i = lane; i < sf_bytes / 4; i += 32) {
+        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+        uint32_t sc = 0;
+        if (src >= 0) {
+          c0 = sp[2 * i];
+          c1 = sp[2 * i + 1];
+          sc = ssf[i];
+          const uint32_t flip[4] = {(sc & 0x80u) ? 0x88888888u : 0u, (sc & 0x8000u) ? 0x88888888u : 0u,
+                                    (sc & 0x800000u) ? 0x88888888u : 0u,
+                                    (sc & 0x80000000u) ? 0x88888888u : 0u};
+          c0.x ^= flip[0];
+          c0.y ^= flip[0];
+          c0.z ^= flip[1];
+          c0.w ^= flip[1];
+          c1.x ^= flip[2];
+          c1.y ^= flip[2];
+          c1.z ^= flip[3];
+          c1.w ^= flip[3];
+          sc &= 0x7F7F7F7Fu;
+        }
+        dst[2 * i] = c0;
+        dst[2 * i + 1] = c1;
+        dsf[i] = sc;
+      }
+      continue;
+    }
     for (int64_t i = lane; i < row_bytes / 16; i += 32) dst[i] = src >= 0 ? sp[i] : make_uint4(0, 0, 0, 0);
     if (x_sf != nullptr) {  // 4-byte units: H/16 (NVFP4) and H/32 (MXFP8) scale bytes
       uint32_t* dsf = reinterpret_cast<uint32_t*>(px_sf + s * sf_bytes);
@@ -154,16 +189,6 @@ __global__ void round_acc(const float4* __restrict__ acc, uint4* __restrict__ ou
     out[i] = f32_to_bf16x8(v);
   }
   launch_dependents();
-}
-
-// E2M1 code -> its fp32 value, built from the bits: magnitude code 2e + m is
-// (1 + m/2) 2^(e-1) for e >= 1 and m/2 for e = 0 (0.5 = 2^-1: exponent field
-// 126), the sign from bit 3.  Integer operations only: no table lookup whose
-// address differs across the warp.
-__device__ __forceinline__ float e2m1_value(uint32_t c) {
-  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
-  const uint32_t mag = e ? ((e + 126u) << 23) | (m << 22) : (m ? (126u << 23) : 0u);
-  return __uint_as_float(mag | ((c & 8u) << 28));
 }
 
 // 2^(e - 127) of an E8M0 code, NaN for 255
@@ -266,14 +291,15 @@ cudaError_t launch_debug_quantize_mx(const float* in, int64_t n, uint8_t* q, uin
 
 cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, const int32_t* p2e,
                            const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
-                           bool pdl, bool zero_pad) {
+                           bool pdl, bool zero_pad, bool canon) {
   // w4a16 BF16 rows; w4a4 NVFP4 (H/2 + H/16 bytes); w4a8 MXFP8 (H + H/32 bytes)
   const int64_t row_bytes = s.mode == 0 ? s.H * 2 : s.mode == 2 ? s.H : s.H / 2;
   const int64_t sf_bytes = s.mode == 0 ? 0 : s.mode == 2 ? s.H / 32 : s.H / 16;
   const int64_t blocks = std::min<int64_t>((s.S + 7) / 8, (int64_t)num_sms() * 8);
   return launch_pdl(permute_rows, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), st, pdl,
                     static_cast<const uint8_t*>(x), s.mode == 0 ? nullptr : x_sf, p2e, num_tiles,
-                    s.T, s.K, row_bytes, sf_bytes, zero_pad ? 1 : 0, s.S, s.M, static_cast<uint8_t*>(px),
+                    s.T, s.K, row_bytes, sf_bytes, zero_pad ? 1 : 0, canon && s.mode == 1 ? 1 : 0,
+                    s.S, s.M, static_cast<uint8_t*>(px),
                     s.mode == 0 ? nullptr : px_sf);
 }
 

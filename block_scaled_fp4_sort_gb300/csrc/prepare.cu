@@ -205,6 +205,56 @@ __global__ void debug_decode_kernel(PrepArgs a) {
   }
 }
 
+// Native NVFP4 layout (w4a4 GEMMs with K a multiple of 256): the codes
+// [E_local * rows, K/2] as given, then the scales [E_local * rows, K/16]; a
+// block whose scale has the sign bit set stores the sign in its 16 codes and
+// the scale without it (the tensor cores read scales unsigned: the same
+// values).  One thread per row and 4-block unit (32 code bytes, 4 scales).
+__global__ void prepare_native_kernel(PrepArgs a, int64_t rows) {
+  const int64_t units = a.K / 64;
+  const int64_t n = rows * units;
+  uint4* codes = reinterpret_cast<uint4*>(a.prep);
+  uint32_t* scales = reinterpret_cast<uint32_t*>(a.prep + rows * (a.K / 2));
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.w) + 2 * i;
+    uint4 c0 = src[0], c1 = src[1];
+    uint32_t sc = reinterpret_cast<const uint32_t*>(a.w_sf)[i];
+    const uint32_t flip[4] = {(sc & 0x80u) ? 0x88888888u : 0u, (sc & 0x8000u) ? 0x88888888u : 0u,
+                              (sc & 0x800000u) ? 0x88888888u : 0u, (sc & 0x80000000u) ? 0x88888888u : 0u};
+    c0.x ^= flip[0];
+    c0.y ^= flip[0];
+    c0.z ^= flip[1];
+    c0.w ^= flip[1];
+    c1.x ^= flip[2];
+    c1.y ^= flip[2];
+    c1.z ^= flip[3];
+    c1.w ^= flip[3];
+    codes[2 * i] = c0;
+    codes[2 * i + 1] = c1;
+    scales[i] = sc & 0x7F7F7F7Fu;
+  }
+}
+
+// the native layout decoded: one thread per 16-element block
+__global__ void debug_decode_native_kernel(PrepArgs a, int64_t rows) {
+  const int64_t blocks = a.K / 16;
+  const int64_t n = rows * blocks;
+  const uint8_t* scales = a.prep + rows * (a.K / 2);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint2 q = reinterpret_cast<const uint2*>(a.prep)[i];
+    const float sc = e4m3_to_float(scales[i]);
+    const uint32_t w[2] = {q.x, q.y};
+    uint16_t* out = a.dbg_out + i * 16;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const __nv_bfloat16 v = __float2bfloat16_rn(e2m1_value((w[k >> 3] >> (4 * (k & 7))) & 15u) * sc);
+      out[k] = *reinterpret_cast<const uint16_t*>(&v);
+    }
+  }
+}
+
 PrepArgs make_args(const Shape& s, int which) {
   PrepArgs a = {};
   a.which = which;
@@ -227,6 +277,14 @@ cudaError_t launch_prepare(const Shape& s, int which, const uint8_t* w, const ui
   a.w = w;
   a.w_sf = w_sf;
   a.prep = prepared;
+  if (native_fp4(s, which)) {
+    const int64_t rows = s.EL * native_rows(s, which);
+    const int64_t n = rows * (a.K / 64);
+    if (n == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
+    prepare_native_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, rows);
+    return cudaGetLastError();
+  }
   const bool frag = fragment_layout(s);
   const int64_t n = a.EL * a.F * a.C * (frag ? 512 : kRowsPerItem);
   if (n == 0) return cudaSuccess;
@@ -243,6 +301,14 @@ cudaError_t launch_debug_decode(const Shape& s, int which, const uint8_t* prepar
   PrepArgs a = make_args(s, which);
   a.prep = const_cast<uint8_t*>(prepared);
   a.dbg_out = static_cast<uint16_t*>(out);
+  if (native_fp4(s, which)) {
+    const int64_t rows = s.EL * native_rows(s, which);
+    const int64_t n = rows * (a.K / 16);
+    if (n == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
+    debug_decode_native_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, rows);
+    return cudaGetLastError();
+  }
   const bool frag = fragment_layout(s);
   const int64_t n = a.EL * a.F * a.C * (frag ? 512 : kRowsPerItem);
   if (n == 0) return cudaSuccess;

@@ -155,6 +155,52 @@ def test_prepared_weights_decode_every_code_under_every_scale(T):
         assert np.array_equal(np.signbit(got[num]), np.signbit(want[num]))   # signed zeros too
 
 
+def test_native_nvfp4_prepared_weights_decode_every_code_under_every_scale():
+    # w4a4 with K a multiple of 256 and route tile >= 32: the native layout
+    # (linear codes and scales, a negative scale's sign moved into the codes)
+    H, I, E = 256, 256, 1
+    w1, sf1 = _every_code_every_scale(2 * I, H)
+    w2, sf2 = _every_code_every_scale(H, I)
+    sf2 = sf2[:, ::-1].copy()
+    p = fm.problem(1, H, I, E, 1, route_tile=32, mode=fm.W4A4)
+    assert fm.prepared_weight_size(p, 1) == 2 * I * (H // 2 + H // 16)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    B = MoEBuffers(p).prepare(t(w1), t(sf1), t(w2), t(sf2))
+    for which, w, sf, prep in ((1, w1, sf1, B.w1p), (2, w2, sf2, B.w2p)):
+        out = torch.zeros(E, w.shape[1], w.shape[2] * 2, dtype=torch.bfloat16, device="cuda")
+        fm.debug_decode_prepared(p, which, prep, out)
+        torch.cuda.synchronize()
+        got, want = f64(out), dequant_np(w, sf)
+        assert np.isnan(want).sum() > 0 and (want == 0).sum() > 0
+        assert np.array_equal(got, want, equal_nan=True)
+        num = ~np.isnan(want)
+        assert np.array_equal(np.signbit(got[num]), np.signbit(want[num]))
+        # scales stored unsigned
+        sfp = prep[w.shape[1] * w.shape[2]:].cpu().numpy()
+        assert not (sfp & 0x80).any()
+
+
+@pytest.mark.parametrize("T", [32, 128])
+def test_w4a4_native_mma_with_negative_scales(T):
+    # the native MMA reads scales unsigned: sign-set scale bytes of x and of
+    # the weights must still give the signed-E4M3 values the oracle computes
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a4")
+    inp = synth.generate(cfg, device="cpu")
+    rng = np.random.default_rng(3)
+    for name in ("x_sf", "w1_sf", "w2_sf"):
+        a = getattr(inp, name).numpy().copy()
+        a[rng.random(a.shape) < 0.3] |= 0x80
+        setattr(inp, name, torch.from_numpy(a))
+    orc = oracle.OracleMoE.from_inputs(inp, T=T)
+    dev = synth.MoEInputs(**{k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+                             for k, v in inp.__dict__.items()})
+    p = problem_for(cfg, T)
+    B = MoEBuffers(p).prepare(dev.w1, dev.w1_sf, dev.w2, dev.w2_sf)
+    out = _fused(dev, B)
+    _, exact, _ = orc.forward(nthreads=NTHREADS)
+    check_out(f64(out), exact, 2e-2, strict=False, what="w4a4 native, negative scales T=%d" % T)
+
+
 def test_fc1_quantiser_bit_exact_vs_oracle():
     rng = np.random.default_rng(11)
     n = 16 * 4096
