@@ -38,6 +38,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_w4a16")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override M (a smaller case of the workload, e.g. for a profiler)")
+    ap.add_argument("--experts", type=int, default=0, help="override E")
     ap.add_argument("--locality", action="store_true",
                     help="print the GEMM1 gather-locality measurement instead of the bench line")
     return ap.parse_args()
@@ -180,7 +183,10 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     fbuild.build()
-    cfg = replica_cfg(synth.CONFIGS[args.workload], rank)
+    cfg = synth.CONFIGS[args.workload]
+    if args.tokens or args.experts:
+        cfg = cfg.with_(M=args.tokens or cfg.M, E=args.experts or cfg.E, sample=0)
+    cfg = replica_cfg(cfg, rank)
     T = synth.route_tile_for(cfg)
     inp = synth.generate(cfg, device=dev)
     p = problem_for(cfg, T)

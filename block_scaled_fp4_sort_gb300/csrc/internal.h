@@ -56,21 +56,22 @@ inline int64_t k_chunks(const Shape& s, int which) { return which == 1 ? s.H / k
 inline bool fragment_layout(const Shape& s) { return s.mode == 0 && s.T == 16; }
 
 // w4a4 GEMMs whose reduction is a multiple of 256 run on the native NVFP4
-// tensor-core MMA (route tiles 32..128): their prepared weights are the
-// linear codes [E_local * rows, K/2] followed by the linear E4M3 scales
-// [E_local * rows, K/16], each block's scale sign moved into its codes.
+// tensor-core MMA (route tiles 32..128).  Their prepared weights come in
+// blocks of kNBlockBytes per (expert, 256-row block, 256-element K chunk),
+// one bulk copy each: the two 128-row tiles' E2M1 codes (128-byte rows, their
+// 16-byte units XOR-swizzled by row & 7: the tensor-core operand layout),
+// then the tiles' E4M3 scale rows (16 bytes per row), each block's scale sign
+// moved into its codes.  Row blocks as in row_blocks().
 inline bool native_fp4(const Shape& s, int which) {
   return s.mode == 1 && s.T >= 32 && (which == 1 ? s.H : s.I) % 256 == 0;
 }
-inline int64_t native_rows(const Shape& s, int which) {
-  return which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H;
-}
+constexpr int kNTileCodes = 128 * 128;
+constexpr int kNTileScales = 128 * 16;
+constexpr int kNBlockBytes = 2 * kNTileCodes + 2 * kNTileScales;   // 36864
 
 inline size_t prepared_bytes(const Shape& s, int which) {
-  if (native_fp4(s, which)) {
-    const int64_t K = which == 1 ? s.H : s.I;
-    return (size_t)s.EL * native_rows(s, which) * (K / 2 + K / 16);
-  }
+  if (native_fp4(s, which))
+    return (size_t)s.EL * row_blocks(s, which) * ((which == 1 ? s.H : s.I) / 256) * kNBlockBytes;
   return (size_t)s.EL * row_blocks(s, which) * k_chunks(s, which) * kWBlockBytes;
 }
 

@@ -68,8 +68,6 @@ struct GemmArgs {
   const int32_t* p2e;          // atomic finalize: route of each slot
   const float* route_w;        //   token_final_scales [M, top_k]
   float rsf;                   //   routed_scaling_factor
-  int32_t a_rows;              // native NVFP4 GEMM: weight rows per expert in the prepared layout
-  int32_t up_rows;             //   gated GEMM1: offset of the up rows (I), else 0
   int* err;
 };
 
@@ -485,8 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 //       scale byte as an unsigned E4M3 (the sign bit is ignored; 0x7F/0xFF are
 //       NaN), so the sign of a negative scale is moved into the codes before
 //       (weight preparation, the slot-order copy of the activations).
-// Per CTA (persistent, 320 threads): warp 8 issues the TMA copies of a chunk
-// (two weight tiles, the activation tile and the three scale tiles), warps
+// Per CTA (persistent, 320 threads): warp 8 issues the copies of a chunk (one
+// bulk copy of the prepared weight block: both tiles' codes and scales; a
+// tensor copy each of the activation tile and its scales), warps
 // 0-7 move the chunk's scales from shared into tensor memory (warps 0-3: the
 // weight scales, warps 4-7: the activation scales, each warp into its lane
 // quarter) and run the epilogue, warp 9 issues 8 MMAs per chunk (2 tiles x 4
@@ -494,11 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 template <int BN>
 struct NCfg {
-  static constexpr int kAData = 128 * 128;        // one 128-row tile, 256 K elements
-  static constexpr int kBData = BN * 128;
-  static constexpr int kASf = 128 * 16;           // 16 block scales per row and chunk
-  static constexpr int kBSf = BN * 16;
-  static constexpr int kTx = 2 * kAData + kBData + 2 * kASf + kBSf;
+  static constexpr int kBData = BN * 128;         // BN activation rows, 256 K elements
+  static constexpr int kBSf = BN * 16;            // 16 block scales per row and chunk
+  static constexpr int kTx = kNBlockBytes + kBData + kBSf;
   static constexpr int kStage = (kTx + 1023) / 1024 * 1024;
   static constexpr int kStagesRaw = (220 * 1024) / kStage;
   static constexpr int kStages = kStagesRaw > 5 ? 5 : kStagesRaw;
@@ -549,9 +546,7 @@ __device__ __forceinline__ void sf_regs(const uint8_t* tile, int l, int rows, ui
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    moe_gemm_nvfp4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap amap,
-                          const __grid_constant__ CUtensorMap asfmap,
-                          const __grid_constant__ CUtensorMap bmap,
+    moe_gemm_nvfp4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap,
                           const __grid_constant__ CUtensorMap bsfmap) {
   using C = NCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -562,7 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + C::kStages;
   uint64_t* sfready = empty + C::kStages;
   uint64_t* accfull = sfready + C::kStages;
-  uint64_t* drain = accfull + 1;
+  uint64_t* accempty = accfull + 1;   // the epilogue has read the accumulators
+  uint64_t* drain = accempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -570,9 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
-      mbar_init(&sfready[i], kDecodeWarps);
+      mbar_init(&sfready[i], kDecodeWarps / 2);
     }
     mbar_init(accfull, 1);
+    mbar_init(accempty, kDecodeWarps);
     mbar_init(drain, 1);
     fence_mbarrier_init();
   }
@@ -581,8 +578,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kTmaWarp && lane == 0) {
-    prefetch_tensormap(&amap);
-    prefetch_tensormap(&asfmap);
     prefetch_tensormap(&bmap);
     prefetch_tensormap(&bsfmap);
   }
@@ -593,10 +588,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   grid_dependency_wait();
   const int64_t n_items = plan_items(a);
-  // stage layout: A tile 0 | A tile 1 | B | A scales tile 0 | tile 1 | B scales
-  constexpr int kOffB = 2 * C::kAData;
-  constexpr int kOffASf = kOffB + C::kBData;
-  constexpr int kOffBSf = kOffASf + 2 * C::kASf;
+  // stage layout: the prepared weight block (A codes tile 0 | tile 1 | A
+  // scales tile 0 | tile 1) | B codes | B scales
+  constexpr int kOffASf = 2 * kNTileCodes;
+  constexpr int kOffB = kNBlockBytes;
+  constexpr int kOffBSf = kOffB + C::kBData;
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
@@ -606,19 +602,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       const int32_t e = plan_expert(a, tau);
-      const int32_t row0 = e * a.a_rows + (a.up_rows ? 128 * f : 256 * f);
-      const int32_t row1 = a.up_rows ? e * a.a_rows + a.up_rows + 128 * f : row0 + 128;
+      const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kNBlockBytes;
       for (int c = 0; c < a.C; ++c) {
         if (lane == 0) {
           ok = mbar_wait(&empty[stage], phase ^ 1u, a.err);
           if (ok) {
             uint8_t* st = stages + stage * C::kStage;
             mbar_arrive_expect_tx(&full[stage], (uint32_t)C::kTx);
-            tma_load_2d(st, &amap, c * 128, row0, &full[stage]);
-            tma_load_2d(st + C::kAData, &amap, c * 128, row1, &full[stage]);
+            tma_load_1d(st, wsrc + (int64_t)c * kNBlockBytes, kNBlockBytes, &full[stage]);
             tma_load_2d(st + kOffB, &bmap, c * 128, tau * BN, &full[stage]);
-            tma_load_2d(st + kOffASf, &asfmap, c * 16, row0, &full[stage]);
-            tma_load_2d(st + kOffASf + C::kASf, &asfmap, c * 16, row1, &full[stage]);
             tma_load_2d(st + kOffBSf, &bsfmap, c * 16, tau * BN, &full[stage]);
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -640,9 +632,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_nvfp4(128, BN);
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, emptyphase = 0;
       bool ok = true;
       for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        // the previous item's epilogue must have read the accumulators first
+        if (item != blockIdx.x) {
+          if (!mbar_wait(accempty, emptyphase, a.err)) break;
+          emptyphase ^= 1u;
+        }
         for (int c = 0; c < a.C; ++c) {
           if (!mbar_wait(&full[stage], phase, a.err) || !mbar_wait(&sfready[stage], phase, a.err)) {
             ok = false;
@@ -655,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int tile = 0; tile < 2; ++tile) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t ad = smem_desc_sw128(st + tile * C::kAData + ks * 32);
+              const uint64_t ad = smem_desc_sw128(st + tile * kNTileCodes + ks * 32);
               const uint64_t bd = smem_desc_sw128(st + kOffB + ks * 32);
               mma_nvfp4(tmem + (uint32_t)(tile * BN), ad, bd, kIdesc, sf + tile * 16 + ks * 4,
                         sf + 32 + ks * 4, (c > 0 || ks > 0) ? 1u : 0u);
@@ -674,38 +671,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ scales + epilogue
+    // Two groups of four warps take alternate chunks, so that each group's
+    // tensor-memory stores have two chunk periods to complete; each warp of a
+    // group writes all three scale tiles into its lane quarter.
     const int t = threadIdx.x;  // 0..255
     const int tile = t >> 7, row = t & 127;
     const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
+    const uint32_t group = (uint32_t)warp >> 2;
     int stage = 0;
-    uint32_t phase = 0, accphase = 0;
+    uint32_t phase = 0, accphase = 0, q = 0;   // q: chunks of this CTA so far
     bool ok = true;
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      for (int c = 0; c < a.C; ++c) {
-        // the stage's copies have landed; its scale columns were last read by
-        // the MMAs of the chunk kStages earlier, which completed before the
-        // producer could refill the stage
-        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) {
-          ok = false;
-          break;
-        }
-        const uint8_t* st = stages + stage * C::kStage;
-        const uint32_t col = tmem + lane_base + (uint32_t)(C::kSfBase + stage * C::kSfCols);
-        uint32_t v[16];
-        if (warp < 4) {
+      for (int c = 0; c < a.C; ++c, ++q) {
+        if ((q & 1u) == group) {
+          // the stage's copies have landed; its scale columns were last read by
+          // the MMAs of the chunk kStages earlier, which completed before the
+          // producer could refill the stage
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) {
+            ok = false;
+            break;
+          }
+          const uint8_t* st = stages + stage * C::kStage;
+          const uint32_t col = tmem + lane_base + (uint32_t)(C::kSfBase + stage * C::kSfCols);
+          uint32_t v[16];
           sf_regs(st + kOffASf, lane, 128, v);
           tmem_st16(col, v);
-          sf_regs(st + kOffASf + C::kASf, lane, 128, v);
+          sf_regs(st + kOffASf + kNTileScales, lane, 128, v);
           tmem_st16(col + 16, v);
-        } else {
           sf_regs(st + kOffBSf, lane, BN, v);
           tmem_st16(col + 32, v);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sfready[stage]);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sfready[stage]);
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
@@ -721,6 +721,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t e = plan_expert_quiet(a, tau);
       tc_epilogue<BN, EPI>(a, tmem, lane_base, tau, f, a.alpha[e], warp, lane, tile, row);
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty);
     }
   }
 
@@ -1220,15 +1222,10 @@ cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st
   a.p2e = g.p2e;
   a.route_w = g.route_w;
   a.rsf = g.rsf;
-  a.a_rows = (int32_t)native_rows(s, g.which);
-  a.up_rows = (int32_t)(g.which == 1 && gated(s) ? s.I : 0);
   a.err = g.err;
   const int64_t K = g.which == 1 ? s.H : s.I;
-  const int64_t wrows = s.EL * a.a_rows;
-  CUtensorMap amap, asfmap, bmap, bsfmap;
-  if (!make_u8_map(&amap, g.wprep, wrows, K / 2, 128, 128, true) ||
-      !make_u8_map(&asfmap, g.wprep + wrows * (K / 2), wrows, K / 16, 16, 128, false) ||
-      !make_u8_map(&bmap, g.act, g.act_rows, K / 2, 128, BN, true) ||
+  CUtensorMap bmap, bsfmap;
+  if (!make_u8_map(&bmap, g.act, g.act_rows, K / 2, 128, BN, true) ||
       !make_u8_map(&bsfmap, g.act_sf, g.act_rows, K / 16, 16, BN, false))
     return cudaErrorInvalidValue;
   auto kern = moe_gemm_nvfp4_kernel<BN, EPI>;
@@ -1245,7 +1242,7 @@ cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a, amap, asfmap, bmap, bsfmap);
+  return cudaLaunchKernelEx(&cfg, kern, a, bmap, bsfmap);
 }
 
 template <int BN>

@@ -205,46 +205,74 @@ __global__ void debug_decode_kernel(PrepArgs a) {
   }
 }
 
-// Native NVFP4 layout (w4a4 GEMMs with K a multiple of 256): the codes
-// [E_local * rows, K/2] as given, then the scales [E_local * rows, K/16]; a
-// block whose scale has the sign bit set stores the sign in its 16 codes and
-// the scale without it (the tensor cores read scales unsigned: the same
-// values).  One thread per row and 4-block unit (32 code bytes, 4 scales).
-__global__ void prepare_native_kernel(PrepArgs a, int64_t rows) {
-  const int64_t units = a.K / 64;
-  const int64_t n = rows * units;
-  uint4* codes = reinterpret_cast<uint4*>(a.prep);
-  uint32_t* scales = reinterpret_cast<uint32_t*>(a.prep + rows * (a.K / 2));
+// Native NVFP4 blocks (w4a4 GEMMs with K a multiple of 256; internal.h):
+// block (e, f, c) = tile 0 codes | tile 1 codes | tile 0 scales | tile 1
+// scales.  A 16-element block whose scale has the sign bit set stores the
+// sign in its codes and the scale without it (the tensor cores read scales
+// unsigned: the same values).  One thread per (block, tile, row, 16-byte code
+// unit j = 32 elements, two scale blocks).
+__global__ void prepare_native_kernel(PrepArgs a, int64_t C) {
+  const int64_t n = a.EL * a.F * C * 2 * 128 * 8;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const uint4* src = reinterpret_cast<const uint4*>(a.w) + 2 * i;
-    uint4 c0 = src[0], c1 = src[1];
-    uint32_t sc = reinterpret_cast<const uint32_t*>(a.w_sf)[i];
-    const uint32_t flip[4] = {(sc & 0x80u) ? 0x88888888u : 0u, (sc & 0x8000u) ? 0x88888888u : 0u,
-                              (sc & 0x800000u) ? 0x88888888u : 0u, (sc & 0x80000000u) ? 0x88888888u : 0u};
-    c0.x ^= flip[0];
-    c0.y ^= flip[0];
-    c0.z ^= flip[1];
-    c0.w ^= flip[1];
-    c1.x ^= flip[2];
-    c1.y ^= flip[2];
-    c1.z ^= flip[3];
-    c1.w ^= flip[3];
-    codes[2 * i] = c0;
-    codes[2 * i + 1] = c1;
-    scales[i] = sc & 0x7F7F7F7Fu;
+    const int j = (int)(i & 7), r = (int)((i >> 3) & 127), tile = (int)((i >> 10) & 1);
+    const int64_t blk = i >> 11;
+    const int64_t c = blk % C, f = (blk / C) % a.F, e = blk / (C * a.F);
+    const bool gated_rows = a.which == 1 && a.gated;   // gate tile + up tile
+    const int64_t row = gated_rows ? (tile ? a.I : 0) + 128 * f + r : 256 * f + 128 * tile + r;
+    const bool valid = row < a.rows_src;
+    uint8_t* dst = a.prep + blk * kNBlockBytes;
+    uint4 q = make_uint4(0, 0, 0, 0), sv = q;
+    if (valid) {
+      const int64_t g = e * a.rows_src + row;
+      q = *reinterpret_cast<const uint4*>(a.w + g * (a.K / 2) + c * 128 + j * 16);
+      sv = *reinterpret_cast<const uint4*>(a.w_sf + g * (a.K / 16) + c * 16);
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+      const uint32_t two = sw[j >> 1] >> (16 * (j & 1));   // scales of blocks 2j, 2j+1
+      if (two & 0x80u) {
+        q.x ^= 0x88888888u;
+        q.y ^= 0x88888888u;
+      }
+      if (two & 0x8000u) {
+        q.z ^= 0x88888888u;
+        q.w ^= 0x88888888u;
+      }
+    }
+    *reinterpret_cast<uint4*>(dst + tile * kNTileCodes + r * 128 + ((j ^ (r & 7)) << 4)) = q;
+    if (j == 0) {
+      sv.x &= 0x7F7F7F7Fu;
+      sv.y &= 0x7F7F7F7Fu;
+      sv.z &= 0x7F7F7F7Fu;
+      sv.w &= 0x7F7F7F7Fu;
+      *reinterpret_cast<uint4*>(dst + 2 * kNTileCodes + tile * kNTileScales + r * 16) = sv;
+    }
   }
 }
 
-// the native layout decoded: one thread per 16-element block
-__global__ void debug_decode_native_kernel(PrepArgs a, int64_t rows) {
-  const int64_t blocks = a.K / 16;
-  const int64_t n = rows * blocks;
-  const uint8_t* scales = a.prep + rows * (a.K / 2);
+// the native blocks decoded to bf16 [E_local, rows, K]: one thread per
+// 16-element block of a row
+__global__ void debug_decode_native_kernel(PrepArgs a, int64_t C) {
+  const int64_t nb = a.K / 16;
+  const int64_t n = a.EL * a.rows_src * nb;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const uint2 q = reinterpret_cast<const uint2*>(a.prep)[i];
-    const float sc = e4m3_to_float(scales[i]);
+    const int64_t b = i % nb, row = (i / nb) % a.rows_src, e = i / (nb * a.rows_src);
+    int64_t f, tile, r;
+    if (a.which == 1 && a.gated) {
+      tile = row >= a.I;
+      const int64_t rr = row - tile * a.I;
+      f = rr / 128;
+      r = rr % 128;
+    } else {
+      f = row / 256;
+      tile = (row % 256) / 128;
+      r = row % 128;
+    }
+    const int64_t c = b / 16, bb = b % 16;
+    const uint8_t* base = a.prep + ((e * a.F + f) * C + c) * kNBlockBytes;
+    const uint2 q = *reinterpret_cast<const uint2*>(base + tile * kNTileCodes + r * 128 +
+                                                    (((bb >> 1) ^ (r & 7)) << 4) + (bb & 1) * 8);
+    const float sc = e4m3_to_float(base[2 * kNTileCodes + tile * kNTileScales + r * 16 + bb]);
     const uint32_t w[2] = {q.x, q.y};
     uint16_t* out = a.dbg_out + i * 16;
 #pragma unroll
@@ -278,11 +306,11 @@ cudaError_t launch_prepare(const Shape& s, int which, const uint8_t* w, const ui
   a.w_sf = w_sf;
   a.prep = prepared;
   if (native_fp4(s, which)) {
-    const int64_t rows = s.EL * native_rows(s, which);
-    const int64_t n = rows * (a.K / 64);
+    const int64_t C = a.K / 256;
+    const int64_t n = a.EL * a.F * C * 2048;
     if (n == 0) return cudaSuccess;
     const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
-    prepare_native_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, rows);
+    prepare_native_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, C);
     return cudaGetLastError();
   }
   const bool frag = fragment_layout(s);
@@ -302,11 +330,10 @@ cudaError_t launch_debug_decode(const Shape& s, int which, const uint8_t* prepar
   a.prep = const_cast<uint8_t*>(prepared);
   a.dbg_out = static_cast<uint16_t*>(out);
   if (native_fp4(s, which)) {
-    const int64_t rows = s.EL * native_rows(s, which);
-    const int64_t n = rows * (a.K / 16);
+    const int64_t n = a.EL * a.rows_src * (a.K / 16);
     if (n == 0) return cudaSuccess;
     const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
-    debug_decode_native_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, rows);
+    debug_decode_native_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, a.K / 256);
     return cudaGetLastError();
   }
   const bool frag = fragment_layout(s);
