@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--tokens", type=int, default=0,
                     help="override M (a smaller case of the workload, e.g. for a profiler)")
     ap.add_argument("--experts", type=int, default=0, help="override E")
+    ap.add_argument("--no-localized", action="store_true",
+                    help="skip the two-domain timing (ncu cannot profile kernels launched into "
+                         "green contexts)")
     ap.add_argument("--locality", action="store_true",
                     help="print the GEMM1 gather-locality measurement instead of the bench line")
     return ap.parse_args()
@@ -239,7 +242,7 @@ def run_ours(args, rank, world, local):
     # ---------------- the same step over two locality domains: FC1 split on I,
     # FC2 on H, each half on a green context holding half of the SMs
     localized = None
-    if cfg.I % 256 == 0 and cfg.H % 256 == 0:
+    if cfg.I % 256 == 0 and cfg.H % 256 == 0 and not args.no_localized:
         try:
             doms = fm.Domains(local)
         except fm.Fp4MoeError as exc:
