@@ -630,6 +630,63 @@ def test_large_batch_sampled_and_row_independence():
     assert np.array_equal(bits(out2), bits(out)[toks])
 
 
+def test_w4a4_decode_size_route_tile_16():
+    # w4a4 at route tile 16 stays on the BF16-decode tcgen05 kernel
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a4")
+    inp, p, B, orc = _setup(cfg, 16)
+    out = _fused(inp, B)
+    _, exact, _ = orc.forward(nthreads=NTHREADS)
+    check_out(f64(out), exact, 2e-2, strict=False, what="w4a4 T=16")
+
+
+@pytest.mark.parametrize("T", [32, 128])
+def test_native_nvfp4_gather_matches_permuted(T):
+    # staged GEMM1 on the native kernel: rows gathered by the slot map equal
+    # the pre-permuted rows bit for bit
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a4", M=96)
+    inp = synth.generate(cfg, device="cuda")
+    p = problem_for(cfg, T)
+    B = MoEBuffers(p).prepare(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+    B.route(inp.token_selected_experts.cuda())
+    pq, psf = B.permute(inp.x_q, inp.x_sf)
+    h_perm, s_perm = B.gemm1(pq, psf, inp.w1_alpha, inp.fc2_input_scale, gather=False)
+    h_gath, s_gath = B.gemm1(inp.x_q, inp.x_sf, inp.w1_alpha, inp.fc2_input_scale, gather=True)
+    torch.cuda.synchronize()
+    valid = B.p2e.cpu().numpy() >= 0
+    assert valid.sum() == cfg.M * cfg.top_k
+    assert np.array_equal(h_perm.cpu().numpy()[valid], h_gath.cpu().numpy()[valid])
+    assert np.array_equal(s_perm.cpu().numpy()[valid], s_gath.cpu().numpy()[valid])
+
+
+def test_native_nvfp4_forward_replays_from_a_cuda_graph():
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a4")
+    inp, p, B, orc = _setup(cfg, 64)
+    ids = inp.token_selected_experts.cuda()
+    w = inp.token_final_scales.cuda()
+    xq, xsf = inp.x_q.clone(), inp.x_sf.clone()
+    out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device="cuda")
+    B.ensure_fused_ws()
+    args = lambda o: (xq, xsf, ids, w, inp.w1_alpha, inp.w2_alpha, o, inp.fc2_input_scale)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        B.forward(*args(out))
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.forward(*args(out))
+    xq.copy_(torch.flip(inp.x_q, dims=[0]))
+    xsf.copy_(torch.flip(inp.x_sf, dims=[0]))
+    g.replay()
+    torch.cuda.synchronize()
+    assert fm.read_error(B.fused_ws) == 0
+    eager = torch.zeros_like(out)
+    B.forward(*args(eager))
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(out), bits(eager))
+
+
 # ------------------------------------------------------------------ TMA row gather (kept last)
 
 @pytest.mark.parametrize("name,T", [("tiny_w4a16", 16), ("tiny_w4a16", 64), ("skewed_w4a16", 64)])
