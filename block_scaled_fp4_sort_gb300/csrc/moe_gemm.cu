@@ -142,19 +142,27 @@ struct Cfg {
 
 // Epilogue of the tcgen05 GEMMs: fp32 accumulators [128 weight rows x BN
 // slots] per 128-row tile in TMEM (tile 0 at column 0, tile 1 at column BN),
-// times `scale` (alpha, with any decode factor undone); thread t of the 256
-// epilogue threads owns row `row` of tile `tile` (its warp's TMEM lanes).
-template <int BN, int EPI>
+// times `scale` (alpha, with any decode factor undone).  PARTS groups of 128
+// threads run it; thread t owns TMEM lane `row` = t % 128 (its warp's lane
+// quarter) in group `part` = t / 128.  Outputs of both tiles (GEMM2, ReLU^2):
+// group part takes tile part % 2 and, with four groups, half of the slot
+// columns; gated FC1: the groups split the slot columns (at least 16 each).
+template <int BN, int EPI, int PARTS>
 __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, uint32_t lane_base,
                                             int32_t tau, int32_t f, float scale, int warp,
-                                            int lane, int tile, int row) {
+                                            int lane, int part, int row) {
+  static_assert(PARTS == 2 || PARTS == 4, "epilogue groups");
+  static_assert(PARTS == 2 || BN >= 32, "four groups need 16 columns each");
   const int32_t mn = a.tile_mn[tau];
   const int64_t s0 = (int64_t)tau * BN;
+  const int tile = part & 1;
+  constexpr int kCw = BN / (PARTS / 2);          // columns per group for the two-tile outputs
+  const int c0 = (part >> 1) * kCw;
   if (EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal) {
     const int64_t n = (int64_t)f * 256 + tile * 128 + row;
     float* y = static_cast<float*>(a.out);   // fp32 route storage
 #pragma unroll 1
-    for (int cc = 0; cc < BN; cc += 16) {
+    for (int cc = c0; cc < c0 + kCw; cc += 16) {
       uint32_t v[16];
       tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc), v);
       tmem_wait_ld();
@@ -177,7 +185,7 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
     const float fs = EPI == kEpiRelu2Nvfp4 ? a.fc2_scale[0] : 0.0f;
     if (n < a.valid_rows) {  // warp-uniform: I is a multiple of 128
 #pragma unroll 1
-      for (int cc = 0; cc < BN; cc += 16) {
+      for (int cc = c0; cc < c0 + kCw; cc += 16) {
         uint32_t v[16];
         tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc), v);
         tmem_wait_ld();
@@ -204,9 +212,9 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
       }
     }
   } else {
-    constexpr int kCols = BN >= 32 ? BN / 2 : BN;
-    if (BN >= 32 || warp < 4) {
-      const int cbase = (BN >= 32 && warp >= 4) ? kCols : 0;
+    constexpr int kCols = BN / PARTS >= 16 ? BN / PARTS : 16;
+    if (part * kCols < BN) {
+      const int cbase = part * kCols;
       const int64_t n = (int64_t)f * 128 + row;
       const float fs = EPI == kEpiSwigluNvfp4 ? a.fc2_scale[0] : 0.0f;
 #pragma unroll 1
@@ -453,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       accphase ^= 1u;
       tc_fence_after();
       const int32_t e = plan_expert_quiet(a, tau);
-      tc_epilogue<BN, EPI>(a, tmem, lane_base, tau, f, a.alpha[e] * 256.0f, warp, lane, tile, row);  // undo the decode's 2^-8
+      tc_epilogue<BN, EPI, 2>(a, tmem, lane_base, tau, f, a.alpha[e] * 256.0f, warp, lane, tile, row);  // undo the decode's 2^-8
       tc_fence_before();
     }
   }
@@ -483,14 +491,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 //       scale byte as an unsigned E4M3 (the sign bit is ignored; 0x7F/0xFF are
 //       NaN), so the sign of a negative scale is moved into the codes before
 //       (weight preparation, the slot-order copy of the activations).
-// Per CTA (persistent, 320 threads): warp 8 issues the copies of a chunk (one
-// bulk copy of the prepared weight block: both tiles' codes and scales; a
-// tensor copy each of the activation tile and its scales), warps
-// 0-7 move the chunk's scales from shared into tensor memory (warps 0-3: the
-// weight scales, warps 4-7: the activation scales, each warp into its lane
-// quarter) and run the epilogue, warp 9 issues 8 MMAs per chunk (2 tiles x 4
-// K steps) and one commit.
+// Per CTA (persistent, 576 threads): warp 16 issues the copies of a chunk
+// (one bulk copy of the prepared weight block: both tiles' codes and scales;
+// a tensor copy each of the activation tile and its scales), warps 0-7 move
+// the chunk's scales from shared into tensor memory (each warp into its lane
+// quarter, two groups on alternate chunks), warp 17 issues 8 MMAs per chunk
+// (2 tiles x 4 K steps) and one commit, and warps 0-15 run the epilogue --
+// four groups of 128 threads, since the epilogue, not the copies or the MMAs,
+// is the longest part of an item.
 // ===========================================================================
+// native kernel: warps 0-15 epilogue (0-7 also scale movers), 16 producer, 17 MMA
+constexpr int kNEpiWarps = 16;
+constexpr int kNSfWarps = 8;
+constexpr int kNTmaWarp = 16;
+constexpr int kNMmaWarp = 17;
+constexpr int kNThreads = 32 * (kNEpiWarps + 2);
+
 template <int BN>
 struct NCfg {
   static constexpr int kBData = BN * 128;         // BN activation rows, 256 K elements
@@ -545,7 +561,7 @@ __device__ __forceinline__ void sf_regs(const uint8_t* tile, int l, int rows, ui
 }
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kNThreads, 1)
     moe_gemm_nvfp4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap,
                           const __grid_constant__ CUtensorMap bsfmap) {
   using C = NCfg<BN>;
@@ -566,18 +582,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
-      mbar_init(&sfready[i], kDecodeWarps / 2);
+      mbar_init(&sfready[i], kNSfWarps / 2);
     }
     mbar_init(accfull, 1);
-    mbar_init(accempty, kDecodeWarps);
+    mbar_init(accempty, kNEpiWarps);
     mbar_init(drain, 1);
     fence_mbarrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kNMmaWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kTmaWarp && lane == 0) {
+  if (warp == kNTmaWarp && lane == 0) {
     prefetch_tensormap(&bmap);
     prefetch_tensormap(&bsfmap);
   }
@@ -594,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kOffB = kNBlockBytes;
   constexpr int kOffBSf = kOffB + C::kBData;
 
-  if (warp == kTmaWarp) {
+  if (warp == kNTmaWarp) {
     // ------------------------------------------------------------ producer
     int stage = 0;
     uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
@@ -627,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0)
       for (int s = 0; s < C::kStages; ++s)
         if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_parity >> s) & 1u, a.err);
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kNMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_nvfp4(128, BN);
@@ -671,19 +687,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ scales + epilogue
-    // Two groups of four warps take alternate chunks, so that each group's
-    // tensor-memory stores have two chunk periods to complete; each warp of a
-    // group writes all three scale tiles into its lane quarter.
-    const int t = threadIdx.x;  // 0..255
-    const int tile = t >> 7, row = t & 127;
+    // Warps 0-7 also move the scales: two groups of four take alternate
+    // chunks, so that each group's tensor-memory stores have two chunk periods
+    // to complete; each warp of a group writes all three scale tiles into its
+    // lane quarter.  All 16 warps run the epilogue, four groups of 128 threads.
+    const int t = threadIdx.x;  // 0..511
+    const int part = t >> 7, row = t & 127;
     const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
+    const bool mover = warp < kNSfWarps;
     const uint32_t group = (uint32_t)warp >> 2;
     int stage = 0;
     uint32_t phase = 0, accphase = 0, q = 0;   // q: chunks of this CTA so far
     bool ok = true;
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      for (int c = 0; c < a.C; ++c, ++q) {
+      for (int c = 0; c < a.C && mover; ++c, ++q) {
         if ((q & 1u) == group) {
           // the stage's copies have landed; its scale columns were last read by
           // the MMAs of the chunk kStages earlier, which completed before the
@@ -719,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       accphase ^= 1u;
       tc_fence_after();
       const int32_t e = plan_expert_quiet(a, tau);
-      tc_epilogue<BN, EPI>(a, tmem, lane_base, tau, f, a.alpha[e], warp, lane, tile, row);
+      tc_epilogue<BN, EPI, 4>(a, tmem, lane_base, tau, f, a.alpha[e], warp, lane, part, row);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(accempty);
@@ -728,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   __syncthreads();
   launch_dependents();
-  if (warp == kMmaWarp) {
+  if (warp == kNMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -1234,7 +1252,7 @@ cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st
   const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)std::min<int64_t>(grid_ctas(g), max_items));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kNThreads);
   cfg.dynamicSmemBytes = Cf::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
