@@ -11,8 +11,8 @@
 // 256-row weight block f): GEMM1 blocks are 128 gate rows + the matching 128
 // up rows, so SwiGLU pairs meet in one CTA; GEMM2 blocks are 256 rows of w2.
 //
-// Per CTA (persistent, one per SM, 320 threads):
-//   warp 8     TMA producer: 1D bulk copy of the prepared weight block
+// Per CTA (persistent, one per SM, 576 threads):
+//   warp 16    TMA producer: 1D bulk copy of the prepared weight block
 //              (codes + scales, 18 KB per 128-K chunk) and a 2D tiled (or
 //              four-row gather) tensor copy of the BF16 activation tile into
 //              a 128-byte-swizzled K-major shared-memory ring.
@@ -20,9 +20,11 @@
 //              scales, turns them into 64 BF16x2 words and stores them with
 //              tcgen05.st straight into tensor memory -- the A operand of the
 //              MMA lives in TMEM, so the decoded weights never touch shared
-//              memory.  After the last chunk the same warps run the epilogue
-//              (tcgen05.ld of the fp32 accumulators).
-//   warp 9     MMA issuer: tcgen05.mma.cta_group::1.kind::f16, A from TMEM,
+//              memory.
+//   warps 0-15 epilogue after an item's last chunk (tcgen05.ld of the fp32
+//              accumulators), then an arrival that lets the MMA warp start the
+//              next item.
+//   warp 17    MMA issuer: tcgen05.mma.cta_group::1.kind::f16, A from TMEM,
 //              B from shared memory, D in TMEM; one tcgen05.commit per chunk
 //              releases both the shared-memory stage and the TMEM A stage.
 // Every wait is bounded (common.cuh); on timeout the error word is set, the
@@ -37,10 +39,11 @@
 namespace fp4moe {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kDecodeWarps = 8;
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kDecodeWarps = 8;     // warps 0-7 decode the weights
+constexpr int kEpiWarps = 16;       // warps 0-15 run the epilogue
+constexpr int kTmaWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 32 * (kEpiWarps + 2);
 constexpr uint32_t kTmemCols = 512;
 
 struct GemmArgs {
@@ -264,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + C::kStages;
   uint64_t* afull = empty + C::kStages;
   uint64_t* accfull = afull + C::kAStages;
-  uint64_t* drain = accfull + 1;
+  uint64_t* accempty = accfull + 1;   // the epilogue has read the accumulators
+  uint64_t* drain = accempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int32_t* gidx = reinterpret_cast<int32_t*>(smem + C::kStages * C::kStage + C::kBarBytes);
 
@@ -278,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&afull[i], kDecodeWarps);
     }
     mbar_init(accfull, 1);
+    mbar_init(accempty, kEpiWarps);
     mbar_init(drain, 1);
     fence_mbarrier_init();
   }
@@ -357,9 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
       int stage = 0, astage = 0;
-      uint32_t phase = 0, aphase = 0;
+      uint32_t phase = 0, aphase = 0, emptyphase = 0;
       bool ok = true;
       for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        // all epilogue warps must have read the previous item's accumulators
+        if (item != blockIdx.x) {
+          if (!mbar_wait(accempty, emptyphase, a.err)) break;
+          emptyphase ^= 1u;
+        }
         for (int c = 0; c < a.C; ++c) {
           if (!mbar_wait(&afull[astage], aphase, a.err) || !mbar_wait(&full[stage], phase, a.err)) {
             ok = false;
@@ -394,15 +404,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ decode + epilogue
-    const int t = threadIdx.x;  // 0..255
-    const int tile = t >> 7, row = t & 127;
+    // warps 0-7 decode; warps 0-15 run the epilogue (four groups of 128
+    // threads for tiles of 32 or more slots, two below)
+    const int t = threadIdx.x;  // 0..511
+    const int tile = (t >> 7) & 1, row = t & 127;
+    const bool decoder = warp < kDecodeWarps;
+    constexpr int kParts = BN >= 32 ? 4 : 2;
     const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
     int stage = 0, astage = 0;
     uint32_t phase = 0, accphase = 0, qd = 0;   // qd: chunks decoded so far by this CTA
     bool ok = true;
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      for (int c = 0; c < a.C; ++c) {
+      for (int c = 0; c < a.C && decoder; ++c) {
         bool good = mbar_wait(&full[stage], phase, a.err);
         // TMEM A stage (qd % kAStages) was last read by the MMAs of chunk
         // qd - kAStages, whose commit completes SMEM stage (qd - kAStages) %
@@ -461,8 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       accphase ^= 1u;
       tc_fence_after();
       const int32_t e = plan_expert_quiet(a, tau);
-      tc_epilogue<BN, EPI, 2>(a, tmem, lane_base, tau, f, a.alpha[e] * 256.0f, warp, lane, tile, row);  // undo the decode's 2^-8
+      if ((t >> 7) < kParts)   // alpha * 256 undoes the decode's 2^-8
+        tc_epilogue<BN, EPI, kParts>(a, tmem, lane_base, tau, f, a.alpha[e] * 256.0f, warp, lane,
+                                     t >> 7, row);
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(accempty);
     }
   }
 
