@@ -57,21 +57,29 @@ inline bool fragment_layout(const Shape& s) { return s.mode == 0 && s.T == 16; }
 
 // w4a4 GEMMs whose reduction is a multiple of 256 run on the native NVFP4
 // tensor-core MMA (route tiles 32..128).  Their prepared weights come in
-// blocks of kNBlockBytes per (expert, 256-row block, 256-element K chunk),
-// one bulk copy each: the two 128-row tiles' E2M1 codes (128-byte rows, their
-// 16-byte units XOR-swizzled by row & 7: the tensor-core operand layout),
-// then the tiles' E4M3 scale rows (16 bytes per row), each block's scale sign
-// moved into its codes.  Row blocks as in row_blocks().
+// blocks of kNBlockBytes per (expert, 128-row tile, 256-element K chunk), one
+// bulk copy each: the tile's E2M1 codes (128-byte rows, their 16-byte units
+// XOR-swizzled by row & 7: the tensor-core operand layout), then its E4M3
+// scale rows (16 bytes per row), each block's scale sign moved into its codes.
+// Gated GEMM1 tile f holds 64 features 64f..64f+63: in lane quarter q, rows
+// 32q..32q+15 are the gate rows of features 64f+16q.. and rows 32q+16..32q+31
+// the matching up rows, so a SwiGLU pair is 16 lanes apart in one warp; the
+// other GEMMs' tile f is rows 128f..128f+127.
 inline bool native_fp4(const Shape& s, int which) {
   return s.mode == 1 && s.T >= 32 && (which == 1 ? s.H : s.I) % 256 == 0;
 }
 constexpr int kNTileCodes = 128 * 128;
 constexpr int kNTileScales = 128 * 16;
-constexpr int kNBlockBytes = 2 * kNTileCodes + 2 * kNTileScales;   // 36864
+constexpr int kNBlockBytes = kNTileCodes + kNTileScales;   // 18432
+inline int64_t native_row_blocks(const Shape& s, int which) {
+  if (which == 1) return gated(s) ? s.I / 64 : (s.I + 127) / 128;
+  return (s.H + 127) / 128;
+}
 
 inline size_t prepared_bytes(const Shape& s, int which) {
   if (native_fp4(s, which))
-    return (size_t)s.EL * row_blocks(s, which) * ((which == 1 ? s.H : s.I) / 256) * kNBlockBytes;
+    return (size_t)s.EL * native_row_blocks(s, which) * ((which == 1 ? s.H : s.I) / 256) *
+           kNBlockBytes;
   return (size_t)s.EL * row_blocks(s, which) * k_chunks(s, which) * kWBlockBytes;
 }
 

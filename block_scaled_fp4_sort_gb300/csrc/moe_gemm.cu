@@ -498,10 +498,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // What is computed is the same as above, without the BF16 decode: the tensor
 // cores take E2M1 codes and their E4M3 block-16 scales directly (four times
-// the BF16 MMA rate), so the weights stream from memory as they are stored.
-//   A = 128 weight rows (K-major E2M1, 128-byte-swizzled shared memory, one
-//       128-byte row = 256 elements per chunk); B = the tile's BN NVFP4
-//       activation rows in slot order, likewise.
+// the BF16 MMA rate per operand byte), so the weights stream from memory as
+// they are stored.
+//   A = one prepared 128-row weight tile (internal.h: gated FC1 tiles hold 64
+//       features, gate and up rows 16 lanes apart), K-major E2M1 in
+//       128-byte-swizzled shared memory, 256 elements per chunk; B = the
+//       tile's BN NVFP4 activation rows in slot order, likewise.
 //   Scale factors in tensor memory: for each 64-element K step, 4 columns x
 //       32 lanes per 128 rows -- row r in lane r % 32 of column r / 32, its
 //       four block scales in the four bytes -- present in all four lane
@@ -509,21 +511,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 //       scale byte as an unsigned E4M3 (the sign bit is ignored; 0x7F/0xFF are
 //       NaN), so the sign of a negative scale is moved into the codes before
 //       (weight preparation, the slot-order copy of the activations).
-// Per CTA (persistent, 576 threads): warp 16 issues the copies of a chunk
-// (one bulk copy of the prepared weight block: both tiles' codes and scales;
-// a tensor copy each of the activation tile and its scales), warps 0-7 move
-// the chunk's scales from shared into tensor memory (each warp into its lane
-// quarter, two groups on alternate chunks), warp 17 issues 8 MMAs per chunk
-// (2 tiles x 4 K steps) and one commit, and warps 0-15 run the epilogue --
-// four groups of 128 threads, since the epilogue, not the copies or the MMAs,
-// is the longest part of an item.
+// Per CTA (persistent, 704 threads): warp 20 issues the copies of a chunk (one
+// bulk copy of the prepared weight block, a tensor copy each of the
+// activation tile and its scales); warps 0-3 move the chunk's scales from
+// shared into tensor memory (each into its lane quarter); warp 21 issues 4
+// MMAs per chunk and one commit; warps 4-19 run the epilogue.  The fp32
+// accumulators are double-buffered in tensor memory (two items in flight), so
+// the epilogue of one item -- timed at about half of the kernel when it ran
+// between items -- overlaps the next item's copies and MMAs.
 // ===========================================================================
-// native kernel: warps 0-15 epilogue (0-7 also scale movers), 16 producer, 17 MMA
-constexpr int kNEpiWarps = 16;
-constexpr int kNSfWarps = 8;
-constexpr int kNTmaWarp = 16;
-constexpr int kNMmaWarp = 17;
-constexpr int kNThreads = 32 * (kNEpiWarps + 2);
+constexpr int kNSfWarps = 4;     // warps 0-3
+constexpr int kNEpiWarps = 16;   // warps 4-19: four groups of 128 threads
+constexpr int kNTmaWarp = 20;
+constexpr int kNMmaWarp = 21;
+constexpr int kNThreads = 32 * 22;
 
 template <int BN>
 struct NCfg {
@@ -532,9 +533,9 @@ struct NCfg {
   static constexpr int kTx = kNBlockBytes + kBData + kBSf;
   static constexpr int kStage = (kTx + 1023) / 1024 * 1024;
   static constexpr int kStagesRaw = (220 * 1024) / kStage;
-  static constexpr int kStages = kStagesRaw > 5 ? 5 : kStagesRaw;
-  static constexpr int kSfBase = 256;             // TMEM column of the scale ring
-  static constexpr int kSfCols = 48;              // per stage: A tile 0, A tile 1, B
+  static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
+  static constexpr int kSfBase = 256;             // TMEM: accumulators 2 x BN from column 0
+  static constexpr int kSfCols = 32;              // per stage: A scales, B scales
   static constexpr int kBarBytes = 256;
   static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes;
   static_assert(kSfBase + kStages * kSfCols <= 512, "tensor memory");
@@ -578,6 +579,84 @@ __device__ __forceinline__ void sf_regs(const uint8_t* tile, int l, int rows, ui
   }
 }
 
+// Epilogue of one item of the native GEMM: accumulators [128 rows x BN slots]
+// at TMEM column `acc`; groups of 128 threads split the slot columns (four
+// groups of BN / 4, or two of 16 for 32-slot tiles).
+// Gated FC1 (kEpiSwigluNvfp4): lanes 0-15 of a quarter hold gate rows, lanes
+// 16-31 the matching up rows; one exchange 16 lanes apart gives the gate lane
+// the up value of column j and the up lane the gate value of column 8 + j, so
+// each half-warp quantises one 16-feature NVFP4 block of one slot.  Other
+// epilogues: row = output feature 128 f + row.
+template <int BN, int EPI>
+__device__ __forceinline__ void n_epilogue(const GemmArgs& a, uint32_t acc, uint32_t lane_base,
+                                           int32_t tau, int32_t f, float scale, int lane, int row,
+                                           int grp) {
+  constexpr int kGroups = BN >= 64 ? 4 : 2;
+  if (grp >= kGroups) return;
+  const int32_t mn = a.tile_mn[tau];
+  const int64_t s0 = (int64_t)tau * BN;
+  constexpr int kCw = BN / kGroups;   // a multiple of 16
+  const int c0 = grp * kCw;
+  if (EPI == kEpiSwigluNvfp4) {
+    const bool up = lane >= 16;
+    const int64_t n = (int64_t)f * 64 + 16 * (row >> 5) + (lane & 15);
+    const float fs = a.fc2_scale[0];
+#pragma unroll 1
+    for (int cc = c0; cc < c0 + kCw; cc += 16) {
+      uint32_t v[16];
+      tmem_ld16(acc + lane_base + (uint32_t)cc, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[8 + j]);
+        const float other = __shfl_xor_sync(0xffffffffu, up ? lo : hi, 16);
+        const float g = up ? other : lo, u = up ? hi : other;
+        const int64_t s = s0 + cc + j + (up ? 8 : 0);
+        float hv = 0.0f;
+        if (s < mn) {
+          const float sc = scale * token_factor(a, s);
+          hv = gemm1_act(a, g * sc, u * sc);
+        }
+        uint32_t sf;
+        const uint32_t code = nvfp4_quant_canonical(hv, fs, &sf);
+        const uint32_t pair = __shfl_down_sync(0xffffffffu, code, 1);
+        if ((lane & 1) == 0)
+          static_cast<uint8_t*>(a.out)[s * (a.out_ld / 2) + n / 2] = (uint8_t)(code | (pair << 4));
+        if ((lane & 15) == 0) a.out_sf[s * (a.out_ld / 16) + n / 16] = (uint8_t)sf;
+      }
+    }
+  } else {
+    const int64_t n = (int64_t)f * 128 + row;
+    if (n >= a.valid_rows) return;   // warp-uniform: the valid rows are a multiple of 32
+    const float fs = EPI == kEpiRelu2Nvfp4 ? a.fc2_scale[0] : 0.0f;
+#pragma unroll 1
+    for (int cc = c0; cc < c0 + kCw; cc += 16) {
+      uint32_t v[16];
+      tmem_ld16(acc + lane_base + (uint32_t)cc, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int64_t s = s0 + cc + i;
+        if (EPI == kEpiRelu2Nvfp4) {
+          const float hv = s < mn ? relu2(__uint_as_float(v[i]) * scale * token_factor(a, s)) : 0.0f;
+          uint32_t sf;
+          const uint32_t code = nvfp4_quant_canonical(hv, fs, &sf);
+          const uint32_t pair = __shfl_down_sync(0xffffffffu, code, 1);
+          if ((lane & 1) == 0)
+            static_cast<uint8_t*>(a.out)[s * (a.out_ld / 2) + n / 2] = (uint8_t)(code | (pair << 4));
+          if ((lane & 15) == 0) a.out_sf[s * (a.out_ld / 16) + n / 16] = (uint8_t)sf;
+        } else if (s < mn) {
+          const float yv = __uint_as_float(v[i]) * scale;
+          if (EPI == kEpiPlainBf16)
+            static_cast<float*>(a.out)[s * a.out_ld + n] = yv;
+          else
+            atomic_final_add(a, s, n, yv);
+        }
+      }
+    }
+  }
+}
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kNThreads, 1)
     moe_gemm_nvfp4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap,
@@ -590,9 +669,9 @@ __global__ void __launch_bounds__(kNThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
   uint64_t* empty = full + C::kStages;
   uint64_t* sfready = empty + C::kStages;
-  uint64_t* accfull = sfready + C::kStages;
-  uint64_t* accempty = accfull + 1;   // the epilogue has read the accumulators
-  uint64_t* drain = accempty + 1;
+  uint64_t* accfull = sfready + C::kStages;   // [2]: accumulator buffer b complete
+  uint64_t* accempty = accfull + 2;           // [2]: the epilogue has read buffer b
+  uint64_t* drain = accempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -600,10 +679,12 @@ __global__ void __launch_bounds__(kNThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
-      mbar_init(&sfready[i], kNSfWarps / 2);
+      mbar_init(&sfready[i], kNSfWarps);
     }
-    mbar_init(accfull, 1);
-    mbar_init(accempty, kNEpiWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], kNEpiWarps);
+    }
     mbar_init(drain, 1);
     fence_mbarrier_init();
   }
@@ -622,9 +703,8 @@ __global__ void __launch_bounds__(kNThreads, 1)
 
   grid_dependency_wait();
   const int64_t n_items = plan_items(a);
-  // stage layout: the prepared weight block (A codes tile 0 | tile 1 | A
-  // scales tile 0 | tile 1) | B codes | B scales
-  constexpr int kOffASf = 2 * kNTileCodes;
+  // stage layout: the prepared weight block (codes | scales) | B codes | B scales
+  constexpr int kOffASf = kNTileCodes;
   constexpr int kOffB = kNBlockBytes;
   constexpr int kOffBSf = kOffB + C::kBData;
 
@@ -666,14 +746,13 @@ __global__ void __launch_bounds__(kNThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_nvfp4(128, BN);
       int stage = 0;
-      uint32_t phase = 0, emptyphase = 0;
+      uint32_t phase = 0, k = 0;   // k: items of this CTA so far; buffer k % 2
       bool ok = true;
-      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        // the previous item's epilogue must have read the accumulators first
-        if (item != blockIdx.x) {
-          if (!mbar_wait(accempty, emptyphase, a.err)) break;
-          emptyphase ^= 1u;
-        }
+      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++k) {
+        const uint32_t buf = k & 1u;
+        // the epilogue must have read this buffer's previous item (k - 2)
+        if (k >= 2 && !mbar_wait(&accempty[buf], ((k >> 1) - 1) & 1u, a.err)) break;
+        const uint32_t d = tmem + buf * (uint32_t)BN;
         for (int c = 0; c < a.C; ++c) {
           if (!mbar_wait(&full[stage], phase, a.err) || !mbar_wait(&sfready[stage], phase, a.err)) {
             ok = false;
@@ -683,82 +762,69 @@ __global__ void __launch_bounds__(kNThreads, 1)
           const uint32_t st = smem_u32(stages + stage * C::kStage);
           const uint32_t sf = tmem + (uint32_t)(C::kSfBase + stage * C::kSfCols);
 #pragma unroll
-          for (int tile = 0; tile < 2; ++tile) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t ad = smem_desc_sw128(st + tile * kNTileCodes + ks * 32);
-              const uint64_t bd = smem_desc_sw128(st + kOffB + ks * 32);
-              mma_nvfp4(tmem + (uint32_t)(tile * BN), ad, bd, kIdesc, sf + tile * 16 + ks * 4,
-                        sf + 32 + ks * 4, (c > 0 || ks > 0) ? 1u : 0u);
-            }
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            mma_nvfp4(d, smem_desc_sw128(st + ks * 32), smem_desc_sw128(st + kOffB + ks * 32), kIdesc,
+                      sf + ks * 4, sf + 16 + ks * 4, (c > 0 || ks > 0) ? 1u : 0u);
           tc_commit(&empty[stage]);   // frees the shared-memory stage and its scale columns
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) tc_commit(accfull);
+        if (ok) tc_commit(&accfull[buf]);
       }
       tc_commit(drain);
       mbar_wait(drain, 0, a.err);
     }
-  } else {
-    // ------------------------------------------------------------ scales + epilogue
-    // Warps 0-7 also move the scales: two groups of four take alternate
-    // chunks, so that each group's tensor-memory stores have two chunk periods
-    // to complete; each warp of a group writes all three scale tiles into its
-    // lane quarter.  All 16 warps run the epilogue, four groups of 128 threads.
-    const int t = threadIdx.x;  // 0..511
-    const int part = t >> 7, row = t & 127;
-    const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
-    const bool mover = warp < kNSfWarps;
-    const uint32_t group = (uint32_t)warp >> 2;
+  } else if (warp < kNSfWarps) {
+    // ------------------------------------------------------------ scale movers
+    // warp w writes the chunk's weight and activation scales into lane quarter w
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     int stage = 0;
-    uint32_t phase = 0, accphase = 0, q = 0;   // q: chunks of this CTA so far
+    uint32_t phase = 0;
     bool ok = true;
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      for (int c = 0; c < a.C && mover; ++c, ++q) {
-        if ((q & 1u) == group) {
-          // the stage's copies have landed; its scale columns were last read by
-          // the MMAs of the chunk kStages earlier, which completed before the
-          // producer could refill the stage
-          if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) {
-            ok = false;
-            break;
-          }
-          const uint8_t* st = stages + stage * C::kStage;
-          const uint32_t col = tmem + lane_base + (uint32_t)(C::kSfBase + stage * C::kSfCols);
-          uint32_t v[16];
-          sf_regs(st + kOffASf, lane, 128, v);
-          tmem_st16(col, v);
-          sf_regs(st + kOffASf + kNTileScales, lane, 128, v);
-          tmem_st16(col + 16, v);
-          sf_regs(st + kOffBSf, lane, BN, v);
-          tmem_st16(col + 32, v);
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sfready[stage]);
+      for (int c = 0; c < a.C; ++c) {
+        // the stage's copies have landed; its scale columns were last read by
+        // the MMAs of the chunk kStages earlier, which completed before the
+        // producer could refill the stage
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) {
+          ok = false;
+          break;
         }
+        const uint8_t* st = stages + stage * C::kStage;
+        const uint32_t col = tmem + lane_base + (uint32_t)(C::kSfBase + stage * C::kSfCols);
+        uint32_t v[16];
+        sf_regs(st + kOffASf, lane, 128, v);
+        tmem_st16(col, v);
+        sf_regs(st + kOffBSf, lane, BN, v);
+        tmem_st16(col + 16, v);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfready[stage]);
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (!ok) break;
-      if (!__all_sync(0xffffffffu, mbar_wait(accfull, accphase, a.err))) {
-        ok = false;
-        break;
-      }
-      accphase ^= 1u;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 4-19)
+    const int et = threadIdx.x - 32 * kNSfWarps;   // 0..511
+    const int row = et & 127, grp = et >> 7;
+    const uint32_t lane_base = (uint32_t)(row & ~31) << 16;   // warp w: lane quarter w % 4
+    uint32_t k = 0;
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
+      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
+      const uint32_t buf = k & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&accfull[buf], (k >> 1) & 1u, a.err))) break;
       tc_fence_after();
       const int32_t e = plan_expert_quiet(a, tau);
-      tc_epilogue<BN, EPI, 4>(a, tmem, lane_base, tau, f, a.alpha[e], warp, lane, part, row);
+      n_epilogue<BN, EPI>(a, tmem + buf * (uint32_t)BN, lane_base, tau, f, a.alpha[e], lane, row, grp);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(accempty);
+      if (lane == 0) mbar_arrive(&accempty[buf]);
     }
   }
 
@@ -1243,7 +1309,7 @@ cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st
   a.tile_mn = g.tile_mn;
   a.num_tiles = g.num_tiles;
   a.top_k = (int32_t)s.K;
-  a.F = (int32_t)row_blocks(s, g.which);
+  a.F = (int32_t)native_row_blocks(s, g.which);
   a.C = (int32_t)((g.which == 1 ? s.H : s.I) / 256);
   a.out_ld = g.out_ld > 0 ? g.out_ld : (g.which == 1 ? s.I : s.H);
   a.valid_rows = (int32_t)(g.which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H);

@@ -206,20 +206,26 @@ __global__ void debug_decode_kernel(PrepArgs a) {
 }
 
 // Native NVFP4 blocks (w4a4 GEMMs with K a multiple of 256; internal.h):
-// block (e, f, c) = tile 0 codes | tile 1 codes | tile 0 scales | tile 1
-// scales.  A 16-element block whose scale has the sign bit set stores the
-// sign in its codes and the scale without it (the tensor cores read scales
-// unsigned: the same values).  One thread per (block, tile, row, 16-byte code
-// unit j = 32 elements, two scale blocks).
+// block (e, f, c) = the tile's codes | its scales.  A 16-element block whose
+// scale has the sign bit set stores the sign in its codes and the scale
+// without it (the tensor cores read scales unsigned: the same values).
+__device__ __forceinline__ int64_t native_src_row(const PrepArgs& a, int64_t f, int r) {
+  if (a.which == 1 && a.gated) {   // 64 features per tile, gate and up 16 lanes apart
+    const int64_t feature = 64 * f + 16 * (r >> 5) + (r & 15);
+    return (r & 16) ? a.I + feature : feature;
+  }
+  return 128 * f + r;
+}
+
+// One thread per (block, row, 16-byte code unit j = 32 elements, two scale blocks).
 __global__ void prepare_native_kernel(PrepArgs a, int64_t C) {
-  const int64_t n = a.EL * a.F * C * 2 * 128 * 8;
+  const int64_t n = a.EL * a.F * C * 128 * 8;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int j = (int)(i & 7), r = (int)((i >> 3) & 127), tile = (int)((i >> 10) & 1);
-    const int64_t blk = i >> 11;
+    const int j = (int)(i & 7), r = (int)((i >> 3) & 127);
+    const int64_t blk = i >> 10;
     const int64_t c = blk % C, f = (blk / C) % a.F, e = blk / (C * a.F);
-    const bool gated_rows = a.which == 1 && a.gated;   // gate tile + up tile
-    const int64_t row = gated_rows ? (tile ? a.I : 0) + 128 * f + r : 256 * f + 128 * tile + r;
+    const int64_t row = native_src_row(a, f, r);
     const bool valid = row < a.rows_src;
     uint8_t* dst = a.prep + blk * kNBlockBytes;
     uint4 q = make_uint4(0, 0, 0, 0), sv = q;
@@ -238,13 +244,13 @@ __global__ void prepare_native_kernel(PrepArgs a, int64_t C) {
         q.w ^= 0x88888888u;
       }
     }
-    *reinterpret_cast<uint4*>(dst + tile * kNTileCodes + r * 128 + ((j ^ (r & 7)) << 4)) = q;
+    *reinterpret_cast<uint4*>(dst + r * 128 + ((j ^ (r & 7)) << 4)) = q;
     if (j == 0) {
       sv.x &= 0x7F7F7F7Fu;
       sv.y &= 0x7F7F7F7Fu;
       sv.z &= 0x7F7F7F7Fu;
       sv.w &= 0x7F7F7F7Fu;
-      *reinterpret_cast<uint4*>(dst + 2 * kNTileCodes + tile * kNTileScales + r * 16) = sv;
+      *reinterpret_cast<uint4*>(dst + kNTileCodes + r * 16) = sv;
     }
   }
 }
@@ -257,22 +263,23 @@ __global__ void debug_decode_native_kernel(PrepArgs a, int64_t C) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t b = i % nb, row = (i / nb) % a.rows_src, e = i / (nb * a.rows_src);
-    int64_t f, tile, r;
+    int64_t f;
+    int r;
     if (a.which == 1 && a.gated) {
-      tile = row >= a.I;
-      const int64_t rr = row - tile * a.I;
-      f = rr / 128;
-      r = rr % 128;
+      const bool up = row >= a.I;
+      const int64_t feature = up ? row - a.I : row;
+      f = feature / 64;
+      const int within = (int)(feature % 64);
+      r = 32 * (within >> 4) + (up ? 16 : 0) + (within & 15);
     } else {
-      f = row / 256;
-      tile = (row % 256) / 128;
-      r = row % 128;
+      f = row / 128;
+      r = (int)(row % 128);
     }
     const int64_t c = b / 16, bb = b % 16;
     const uint8_t* base = a.prep + ((e * a.F + f) * C + c) * kNBlockBytes;
-    const uint2 q = *reinterpret_cast<const uint2*>(base + tile * kNTileCodes + r * 128 +
-                                                    (((bb >> 1) ^ (r & 7)) << 4) + (bb & 1) * 8);
-    const float sc = e4m3_to_float(base[2 * kNTileCodes + tile * kNTileScales + r * 16 + bb]);
+    const uint2 q = *reinterpret_cast<const uint2*>(base + r * 128 + (((bb >> 1) ^ (r & 7)) << 4) +
+                                                    (bb & 1) * 8);
+    const float sc = e4m3_to_float(base[kNTileCodes + r * 16 + bb]);
     const uint32_t w[2] = {q.x, q.y};
     uint16_t* out = a.dbg_out + i * 16;
 #pragma unroll
@@ -287,7 +294,7 @@ PrepArgs make_args(const Shape& s, int which) {
   PrepArgs a = {};
   a.which = which;
   a.EL = s.EL;
-  a.F = row_blocks(s, which);
+  a.F = native_fp4(s, which) ? native_row_blocks(s, which) : row_blocks(s, which);
   a.C = k_chunks(s, which);
   a.gated = gated(s) ? 1 : 0;
   a.mx = s.mode == 2 ? 1 : 0;
@@ -307,7 +314,7 @@ cudaError_t launch_prepare(const Shape& s, int which, const uint8_t* w, const ui
   a.prep = prepared;
   if (native_fp4(s, which)) {
     const int64_t C = a.K / 256;
-    const int64_t n = a.EL * a.F * C * 2048;
+    const int64_t n = a.EL * a.F * C * 1024;
     if (n == 0) return cudaSuccess;
     const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
     prepare_native_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, C);

@@ -175,10 +175,10 @@ def test_native_nvfp4_prepared_weights_decode_every_code_under_every_scale():
         assert np.array_equal(got, want, equal_nan=True)
         num = ~np.isnan(want)
         assert np.array_equal(np.signbit(got[num]), np.signbit(want[num]))
-        # prepared blocks of 36864 bytes: both tiles' codes, then their scales,
-        # stored unsigned
-        blocks = prep.cpu().numpy().reshape(-1, 36864)
-        assert not (blocks[:, 32768:] & 0x80).any()
+        # prepared blocks of 18432 bytes: a 128-row tile's codes, then its
+        # scales, stored unsigned
+        blocks = prep.cpu().numpy().reshape(-1, 18432)
+        assert not (blocks[:, 16384:] & 0x80).any()
 
 
 @pytest.mark.parametrize("T", [32, 128])
