@@ -149,8 +149,9 @@ FP4MOE_API int64_t fp4moe_max_permuted_slots(const fp4moe_problem* p);
 /* Workspace bytes of moe_route_sort (per-block histogram tables + error word). */
 FP4MOE_API size_t fp4moe_route_workspace_size(const fp4moe_problem* p);
 
-/* Workspace bytes of moe_gemm1_swiglu / moe_gemm2 (error word; for w4a4 also
- * the BF16 copies of the NVFP4 activations the GEMM consumes). */
+/* Workspace bytes of moe_gemm1_swiglu / moe_gemm2 (error word; for w4a4 and
+ * w4a8 also the copy of the activations the GEMM consumes: NVFP4 in slot
+ * order for the FP4 MMA, else expanded to BF16). */
 FP4MOE_API size_t fp4moe_gemm_workspace_size(const fp4moe_problem* p, int32_t which /* 1 | 2 */);
 
 /* Workspace bytes of fused_moe_forward: routing plan, FC1 output h [S, I],
@@ -248,7 +249,10 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
 
 /* Grouped GEMM1 with the activation epilogue (vllm moe_cute module docstring:
  * E2M1*E4M3 decoded to BF16, BF16 MMAs, fp32 accumulation, alpha on the
- * accumulator, the activation in fp32 rounded once):
+ * accumulator, the activation in fp32 rounded once; w4a4 with route_tile >= 32
+ * and H a multiple of 256 takes the NVFP4 operands straight into the
+ * block-scaled FP4 tensor-core MMA -- the same exact products, fp32
+ * accumulation):
  *   h[s, n] = R( act(c_s a1_e G_e[n] . A_s, c_s a1_e U_e[n] . A_s) )
  * for valid slots s (padding rows of h are zeroed), e = tile_idx_to_expert,
  * act = p->activation (default silu(g) * u; ReLU^2 has no gate rows), and
@@ -308,7 +312,8 @@ FP4MOE_API fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y,
                            int32_t accumulate, void* out, void* stream);
 
 /* The whole forward on `stream`: route sort, x gathered into slot order in the
- * workspace (w4a4 rows expanded to BF16 on the way; padding rows unwritten),
+ * workspace (NVFP4 for the FP4 MMA path; w4a8 rows and decode-size w4a4 rows
+ * expanded to BF16 on the way; padding rows unwritten),
  * GEMM1 (+ activation), GEMM2, finalize, chained with programmatic dependent
  * launch.  Arguments as in the steps above; the
  * weights are prepared (fp4moe_prepare_weights).  finalize_mode:
@@ -375,8 +380,9 @@ FP4MOE_API fp4moe_status fp4moe_prepare_domain_weights(const fp4moe_problem* p, 
 FP4MOE_API size_t fp4moe_localized_workspace_size(const fp4moe_problem* p);
 
 /* fused_moe_forward over two domains.  On `stream`: route sort and x in slot
- * order; then on domain stream d: FC1 shard d (+ its columns of h expanded to
- * BF16 for w4a4 / w4a8), a wait for the other domain's FC1, FC2 shard d; then
+ * order; then on domain stream d: FC1 shard d (+ for w4a8 and decode-size w4a4
+ * its columns of h expanded to BF16), a wait for the other domain's FC1, FC2
+ * shard d; then
  * on `stream` again, after both domains: the finalize.  The results equal
  * fused_moe_forward's: bit for bit for route_tile >= 32 with the
  * deterministic finalize; for route_tile 16 the warp-MMA GEMM's K-split tail
