@@ -543,6 +543,19 @@ def test_atomic_finalize_accumulate(T):
     check_out(f64(c), exact, 5e-3, what="atomic accumulate")
 
 
+@pytest.mark.parametrize("T", [32, 128])
+def test_atomic_finalize_native_nvfp4(T):
+    # w4a4 on the native FP4 MMA: the atomic epilogue of its GEMM2
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a4")
+    inp, p, B, orc = _setup(cfg, T)
+    a = _fused(inp, B, rsf=0.75, mode=ATOMIC)
+    _, exact, _ = orc.forward(rsf=0.75, nthreads=NTHREADS)
+    check_out(f64(a), exact, 2e-2, strict=False, what="native atomic T=%d" % T)
+    c = _fused(inp, B, rsf=0.75, accumulate=True, out=a.clone(), mode=ATOMIC)
+    _, exact, _ = orc.forward(rsf=0.75, accumulate=True, out_old=bits(a), nthreads=NTHREADS)
+    check_out(f64(c), exact, 2e-2, strict=False, what="native atomic accumulate T=%d" % T)
+
+
 def test_atomic_finalize_expert_parallel_halves():
     cfg = synth.CONFIGS["tiny_w4a16"]
     inp = synth.generate(cfg, device="cuda")
