@@ -910,15 +910,21 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
     const uint32_t sc1[2] = {scale_code_bf16x2(__byte_perm(sb.x, 0u, sel)),
                              scale_code_bf16x2(__byte_perm(sb.y, 0u, sel))};
     const uint8_t* bt = blk + kWBlockBytes;
+    // per 64-element atom: decode its four words first, then their MMAs, so
+    // that the four decode chains interleave
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t af[4];
-      decode_word_frag(words[kk], sc0[kk >> 2], sc1[kk >> 2], af);
-      const uint8_t* atom = bt + (kk >> 2) * GvCfg::BN * 128;  // K 0..63 or 64..127
+    for (int at = 0; at < 2; ++at) {
+      uint32_t af[4][4];
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const uint2 bv = *reinterpret_cast<const uint2*>(atom + nb * 1024 + boff[kk & 3]);
-        mma_16816(acc[nb][kk % kGvChains], af, bv.x, bv.y);
+      for (int kq = 0; kq < 4; ++kq) decode_word_frag(words[4 * at + kq], sc0[at], sc1[at], af[kq]);
+      const uint8_t* atom = bt + at * GvCfg::BN * 128;  // K 0..63 or 64..127
+#pragma unroll
+      for (int kq = 0; kq < 4; ++kq) {
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+          const uint2 bv = *reinterpret_cast<const uint2*>(atom + nb * 1024 + boff[kq]);
+          mma_16816(acc[nb][(4 * at + kq) % kGvChains], af[kq], bv.x, bv.y);
+        }
       }
     }
     __syncwarp();
