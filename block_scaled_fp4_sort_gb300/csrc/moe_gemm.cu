@@ -1182,10 +1182,16 @@ __global__ void __launch_bounds__(kGvThreads, 1)
       const bool ok =
           two ? gv_k_loop<2>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc, c1 - c0)
               : gv_k_loop<1>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc, c1 - c0);
+      // the chains summed in a fixed order: deterministic
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) raw[nb][i] = acc[nb][0][i] + acc[nb][1][i];
+        for (int i = 0; i < 4; ++i) {
+          float r = acc[nb][0][i];
+#pragma unroll
+          for (int p = 1; p < kGvChains; ++p) r += acc[nb][p][i];
+          raw[nb][i] = r;
+        }
       return ok;
     };
     auto finish = [&](int64_t item, const float (&raw)[2][4]) -> bool {
