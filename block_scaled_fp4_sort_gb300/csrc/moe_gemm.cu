@@ -123,10 +123,25 @@ __device__ __forceinline__ int32_t plan_expert(const GemmArgs& a, int32_t tau) {
   set_error(a.err, kErrDevice);
   return 0;
 }
-// the same clamp without the report (the producer reports it for the tile)
-__device__ __forceinline__ int32_t plan_expert_quiet(const GemmArgs& a, int32_t tau) {
-  const int32_t e = a.tile_expert[tau];
-  return (uint32_t)e < (uint32_t)a.EL ? e : 0;
+// An item's plan entries as loaded, the expert id not yet clamped.  The
+// epilogue warps load them at the start of an item or one item ahead and
+// clamp the expert (the producer reports it) only where alpha is read, so
+// that the latency of these dependent global loads overlaps the item's main
+// loop instead of stalling every item boundary.
+struct ItemPlan {
+  int32_t mn, e;
+};
+__device__ __forceinline__ ItemPlan load_item_plan(const GemmArgs& a, int64_t item) {
+  const int32_t tau = (int32_t)(item / a.F);
+  return ItemPlan{a.tile_mn[tau], a.tile_expert[tau]};
+}
+__device__ __forceinline__ float item_alpha(const GemmArgs& a, const ItemPlan& p) {
+  return a.alpha[(uint32_t)p.e < (uint32_t)a.EL ? p.e : 0];
+}
+// the second global scale of the NVFP4 FC1 output, read once per CTA
+template <int EPI>
+__device__ __forceinline__ float fc1_out_scale(const GemmArgs& a) {
+  return EPI == kEpiSwigluNvfp4 || EPI == kEpiRelu2Nvfp4 ? a.fc2_scale[0] : 0.0f;
 }
 
 template <int BN>
@@ -152,11 +167,10 @@ struct Cfg {
 // columns; gated FC1: the groups split the slot columns (at least 16 each).
 template <int BN, int EPI, int PARTS>
 __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, uint32_t lane_base,
-                                            int32_t tau, int32_t f, float scale, int warp,
-                                            int lane, int part, int row) {
+                                            int32_t tau, int32_t f, int32_t mn, float scale,
+                                            float fs, int warp, int lane, int part, int row) {
   static_assert(PARTS == 2 || PARTS == 4, "epilogue groups");
   static_assert(PARTS == 2 || BN >= 32, "four groups need 16 columns each");
-  const int32_t mn = a.tile_mn[tau];
   const int64_t s0 = (int64_t)tau * BN;
   const int tile = part & 1;
   constexpr int kCw = BN / (PARTS / 2);          // columns per group for the two-tile outputs
@@ -185,7 +199,6 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
   } else if (EPI == kEpiRelu2Bf16 || EPI == kEpiRelu2Nvfp4 || EPI == kEpiRelu2Mxfp8) {
     // non-gated FC1: both 128-row tiles are outputs, feature n per thread
     const int64_t n = (int64_t)f * 256 + tile * 128 + row;
-    const float fs = EPI == kEpiRelu2Nvfp4 ? a.fc2_scale[0] : 0.0f;
     if (n < a.valid_rows) {  // warp-uniform: I is a multiple of 128
 #pragma unroll 1
       for (int cc = c0; cc < c0 + kCw; cc += 16) {
@@ -219,7 +232,6 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
     if (part * kCols < BN) {
       const int cbase = part * kCols;
       const int64_t n = (int64_t)f * 128 + row;
-      const float fs = EPI == kEpiSwigluNvfp4 ? a.fc2_scale[0] : 0.0f;
 #pragma unroll 1
       for (int cc = 0; cc < kCols; cc += 16) {
         uint32_t g[16], u[16];
@@ -414,8 +426,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, astage = 0;
     uint32_t phase = 0, accphase = 0, qd = 0;   // qd: chunks decoded so far by this CTA
     bool ok = true;
+    const float fs = fc1_out_scale<EPI>(a);
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
+      const ItemPlan plan = load_item_plan(a, item);   // arrives during the decode
       for (int c = 0; c < a.C && decoder; ++c) {
         bool good = mbar_wait(&full[stage], phase, a.err);
         // TMEM A stage (qd % kAStages) was last read by the MMAs of chunk
@@ -468,16 +482,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---------------- epilogue
+      const float alpha = item_alpha(a, plan);   // arrives during the wait
       if (!__all_sync(0xffffffffu, mbar_wait(accfull, accphase, a.err))) {
         ok = false;
         break;
       }
       accphase ^= 1u;
       tc_fence_after();
-      const int32_t e = plan_expert_quiet(a, tau);
       if ((t >> 7) < kParts)   // alpha * 256 undoes the decode's 2^-8
-        tc_epilogue<BN, EPI, kParts>(a, tmem, lane_base, tau, f, a.alpha[e] * 256.0f, warp, lane,
-                                     t >> 7, row);
+        tc_epilogue<BN, EPI, kParts>(a, tmem, lane_base, tau, f, plan.mn, alpha * 256.0f, fs, warp,
+                                     lane, t >> 7, row);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(accempty);
@@ -589,18 +603,16 @@ __device__ __forceinline__ void sf_regs(const uint8_t* tile, int l, int rows, ui
 // epilogues: row = output feature 128 f + row.
 template <int BN, int EPI>
 __device__ __forceinline__ void n_epilogue(const GemmArgs& a, uint32_t acc, uint32_t lane_base,
-                                           int32_t tau, int32_t f, float scale, int lane, int row,
-                                           int grp) {
+                                           int32_t tau, int32_t f, int32_t mn, float scale, float fs,
+                                           int lane, int row, int grp) {
   constexpr int kGroups = BN >= 64 ? 4 : 2;
   if (grp >= kGroups) return;
-  const int32_t mn = a.tile_mn[tau];
   const int64_t s0 = (int64_t)tau * BN;
   constexpr int kCw = BN / kGroups;   // a multiple of 16
   const int c0 = grp * kCw;
   if (EPI == kEpiSwigluNvfp4) {
     const bool up = lane >= 16;
     const int64_t n = (int64_t)f * 64 + 16 * (row >> 5) + (lane & 15);
-    const float fs = a.fc2_scale[0];
 #pragma unroll 1
     for (int cc = c0; cc < c0 + kCw; cc += 16) {
       uint32_t v[16];
@@ -628,7 +640,6 @@ __device__ __forceinline__ void n_epilogue(const GemmArgs& a, uint32_t acc, uint
   } else {
     const int64_t n = (int64_t)f * 128 + row;
     if (n >= a.valid_rows) return;   // warp-uniform: the valid rows are a multiple of 32
-    const float fs = EPI == kEpiRelu2Nvfp4 ? a.fc2_scale[0] : 0.0f;
 #pragma unroll 1
     for (int cc = c0; cc < c0 + kCw; cc += 16) {
       uint32_t v[16];
@@ -815,16 +826,30 @@ __global__ void __launch_bounds__(kNThreads, 1)
     const int row = et & 127, grp = et >> 7;
     const uint32_t lane_base = (uint32_t)(row & ~31) << 16;   // warp w: lane quarter w % 4
     uint32_t k = 0;
+    const float fs = fc1_out_scale<EPI>(a);
+    // the plan entries of the next item load during this item's epilogue and
+    // its alpha at the end of it
+    ItemPlan next = {0, 0};
+    float alpha_next = 0.0f;
+    if (blockIdx.x < n_items) {
+      next = load_item_plan(a, blockIdx.x);
+      alpha_next = item_alpha(a, next);
+    }
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       const uint32_t buf = k & 1u;
+      const ItemPlan cur = next;
+      const float alpha = alpha_next;
+      const bool more = item + gridDim.x < n_items;
+      if (more) next = load_item_plan(a, item + gridDim.x);
       if (!__all_sync(0xffffffffu, mbar_wait(&accfull[buf], (k >> 1) & 1u, a.err))) break;
       tc_fence_after();
-      const int32_t e = plan_expert_quiet(a, tau);
-      n_epilogue<BN, EPI>(a, tmem + buf * (uint32_t)BN, lane_base, tau, f, a.alpha[e], lane, row, grp);
+      n_epilogue<BN, EPI>(a, tmem + buf * (uint32_t)BN, lane_base, tau, f, cur.mn, alpha, fs, lane, row,
+                          grp);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[buf]);
+      if (more) alpha_next = item_alpha(a, next);
     }
   }
 
@@ -1194,9 +1219,12 @@ __global__ void __launch_bounds__(kGvThreads, 1)
         }
       return ok;
     };
+    // alpha is read here, after the K loop: reading it (and the next item's
+    // plan entries) ahead of the loop, as the tcgen05 kernels do, measured
+    // slower in this kernel, whose K loop runs at the 96-register limit
     auto finish = [&](int64_t item, const float (&raw)[2][4]) -> bool {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      const float scale = a.alpha[plan_expert_quiet(a, tau)] * 256.0f;  // undo the decode's 2^-8
+      const float scale = item_alpha(a, ItemPlan{0, a.tile_expert[tau]}) * 256.0f;  // undo the decode's 2^-8
       float d[2][4];
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
