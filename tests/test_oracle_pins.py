@@ -371,3 +371,48 @@ def test_accumulate_false_equals_zero_seed_bitwise_and_ep_split():
     c, ec, _ = orc.forward(rsf=1.5)
     _, ea, _ = orc.forward(rsf=0.75)
     np.testing.assert_allclose(ec, 2 * ea, rtol=1e-12, atol=1e-300)
+
+
+# ---------------------------------------------------------------- GEMM2 from arbitrary FC1 codes
+
+def test_expert_down_from_codes_matches_numpy():
+    """The oracle's GEMM2 on caller-given FC1 codes (what the GEMM2-only GPU
+    parity checks compare against) equals alpha2 * (W2_e @ decode(codes)) with
+    W2 and the codes decoded by the tests' own table and torch's E4M3: random
+    NVFP4 codes under random signed E4M3 scales (NaN bytes excluded), with an
+    all-zero-scale block."""
+    inp = _small_inputs("w4a4")
+    orc = oracle.OracleMoE.from_inputs(inp)
+    I = inp.cfg.I
+    rng = np.random.default_rng(11)
+    W2 = dequant_np(inp.w2.numpy(), inp.w2_sf.numpy())
+    a2 = inp.w2_alpha.double().numpy()
+    for e in (0, 5):
+        hq = rng.integers(0, 256, I // 2, dtype=np.uint8)
+        hsf = rng.integers(0, 256, I // 16, dtype=np.uint8)
+        hsf[(hsf & 0x7F) == 0x7F] = 0x38                  # no NaN scales
+        hsf[2] = 0x80                                     # a negative-zero scale
+        ref = a2[e] * (W2[e] @ dequant_np(hq[None], hsf[None])[0])
+        np.testing.assert_allclose(orc.expert_down_codes(e, hq, hsf), ref, rtol=1e-12, atol=1e-15)
+
+
+def test_expert_down_from_mxfp8_codes_matches_numpy():
+    """The same for w4a8: MXFP8 FC1 codes (E4M3 elements, E8M0 block-32 scales)
+    against MXFP4 weights, both decoded here."""
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a8")
+    inp = synth.generate(cfg, device="cpu")
+    orc = oracle.OracleMoE.from_inputs(inp)
+    I = cfg.I
+    rng = np.random.default_rng(12)
+    q2, s2 = inp.w2.numpy(), inp.w2_sf.numpy().astype(np.int64)
+    lo, hi = E2M1_TABLE[q2 & 15], E2M1_TABLE[q2 >> 4]
+    W2 = np.stack([lo, hi], -1).reshape(q2.shape[:-1] + (q2.shape[-1] * 2,)) * np.exp2(
+        np.repeat(s2 - 127, 32, axis=-1).astype(np.float64))
+    a2 = inp.w2_alpha.double().numpy()
+    for e in (1, 6):
+        hq = rng.integers(0, 256, I, dtype=np.uint8)
+        hq[(hq & 0x7F) == 0x7F] = 0x30                    # no NaN elements
+        hsf = rng.integers(118, 136, I // 32, dtype=np.uint8)
+        hin = e4m3_np(hq) * np.exp2(np.repeat(hsf.astype(np.int64) - 127, 32).astype(np.float64))
+        ref = a2[e] * (W2[e] @ hin)
+        np.testing.assert_allclose(orc.expert_down_codes(e, hq, hsf), ref, rtol=1e-12, atol=1e-15)
