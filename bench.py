@@ -1,21 +1,27 @@
 """Benchmark of the NVFP4 fused-MoE forward on GB300 (one JSON line on stdout).
 
-Workload (one step = one fused forward pass over one batch): the decode
-w4a16 case -- M=8 tokens, H=7168, I=2048, E=256, top_k=8, BF16 activations,
-NVFP4 weights, softmax top-8 routing, seed 0.  Weights are generated once and
-stay resident; each step re-runs routing, GEMM1+SwiGLU, GEMM2 and finalize.
+Headline workload (one step = one fused forward pass over one batch): the
+large-batch w4a16 case -- M=131072 tokens, H=6144, I=2048, E=256, top_k=8,
+BF16 activations, NVFP4 weights, uniform distinct top-8 routing with
+Dirichlet(1) weights, seed 0 (the route-window workload of the FlashInfer
+PR #4440 page, results table).  Weights are generated once and stay
+resident; each step re-runs routing, x into slot order, GEMM1 + SwiGLU,
+GEMM2 and finalize.  The line also carries the other single-GPU workloads
+under "workloads" (decode w4a16, skewed w4a16, prefill w4a4), each with its
+own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload decode_w4a16|...]
+                  [--workload large_w4a16|...] [--also decode_w4a16,...|none]
 
 `--impl reference` times the CPU oracle (test infrastructure, never tuned)
-on the host cores over the same workload.  Under torchrun every rank runs its
-own replica (independent batches, no collective on the data path: weak
-scaling); times are the max over ranks.
+on the host cores over bounded samples of the same workload.  Under torchrun
+every rank runs its own replica (independent batches, no collective on the
+data path: weak scaling); times are the max over ranks.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -28,19 +34,26 @@ sys.path.insert(0, ROOT)
 
 METRIC = "fused-MoE tokens/s"
 UNIT = "tokens/s"
+SECONDARY = "decode_w4a16,skewed_w4a16,prefill_w4a4"
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode_w4a16")
+    ap.add_argument("--workload", default="large_w4a16")
+    ap.add_argument("--also", default=SECONDARY,
+                    help="comma-separated workloads measured after the headline and reported "
+                         "under 'workloads' ('none' for the headline alone)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0,
+                    help="seconds of oracle work for the cpu_baseline leg (bounded sample)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override M (a smaller case of the workload, e.g. for a profiler)")
     ap.add_argument("--experts", type=int, default=0, help="override E")
+    ap.add_argument("--route-tile", type=int, default=0, help="override the route tile T")
     ap.add_argument("--no-localized", action="store_true",
                     help="skip the two-domain timing (ncu cannot profile kernels launched into "
                          "green contexts)")
@@ -149,48 +162,105 @@ class ClockSampler:
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def time_oracle(inp, T, steps, warmup, tokens=None):
+def oracle_tokens(cfg, inp):
+    """Tokens the oracle is timed on: every token of the small workloads, the
+    seeded sample (1024 tokens) of the large ones."""
     import numpy as np
+    return np.asarray(inp.sample_tokens) if cfg.sample else np.arange(cfg.M)
+
+
+def time_oracle_bounded(orc, toks, budget_s, max_runs=3):
+    """Time the oracle on a prefix of `toks` sized to about `budget_s` seconds
+    of host work: a 1-thread-per-token calibration pass on a few tokens picks
+    the prefix, then up to `max_runs` timed passes.  Returns (tokens/s,
+    seconds per pass, threads, tokens per pass, runs)."""
+    ncpu = os.cpu_count() or 1
+    probe = toks[:min(len(toks), ncpu)]
+    t0 = time.perf_counter()
+    orc.forward(probe, nthreads=min(ncpu, len(probe)))
+    per_round = time.perf_counter() - t0          # one token per thread
+    rounds = max(1, int(budget_s / max(per_round, 1e-9)))
+    n = min(len(toks), rounds * ncpu)
+    sub = toks[:n]
+    cores = min(ncpu, n)
+    runs = max(1, min(max_runs, int(budget_s / max(per_round * -(-n // cores), 1e-9))))
+    t0 = time.perf_counter()
+    for _ in range(runs):
+        orc.forward(sub, nthreads=cores)
+    dt = (time.perf_counter() - t0) / runs
+    return n / dt, dt, cores, n, runs
+
+
+def cpu_baseline(cfg, inp, T, budget_s):
     import oracle
     oracle.build()
-    cfg = inp.cfg
     orc = oracle.OracleMoE.from_inputs(inp, T=T)
-    toks = np.arange(cfg.M) if tokens is None else np.asarray(tokens)
-    cores = min(os.cpu_count() or 1, len(toks))
-    for _ in range(warmup):
-        orc.forward(toks, nthreads=cores)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        orc.forward(toks, nthreads=cores)
-    dt = (time.perf_counter() - t0) / max(steps, 1)
-    return len(toks) / dt, dt, cores, len(toks)
+    toks = oracle_tokens(cfg, inp)
+    v, dt, cores, n, runs = time_oracle_bounded(orc, toks, budget_s)
+    if cfg.sample:
+        what = ("the first %d of the %d seeded sampled tokens of %s, %d timed pass(es); the full "
+                "M=%d batch would take ~%.0f s on these cores (extrapolated from the sample)"
+                % (n, len(toks), cfg.name, runs, cfg.M, cfg.M / v))
+    else:
+        what = "%d of the %d tokens of one %s batch, %d timed pass(es)" % (n, cfg.M, cfg.name, runs)
+    return {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": what,
+            "host_cpus": os.cpu_count()}
 
 
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, rank, world, local):
+def src_digest(*names):
+    """Digest of kernel sources: a stored ncu traffic figure is used only while
+    the sources it was taken on are unchanged."""
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "block_scaled_fp4_sort_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+GEMM_SOURCES = ("moe_gemm.cu", "common.cuh", "decode.cuh", "nvfp4.cuh", "internal.h")
+
+
+def stored_traffic(workload):
+    """DRAM bytes per GEMM1 launch from a committed ncu summary of this
+    workload's GEMM1 (scaled to the full launch where the capture ran a
+    smaller case), or None if none was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
+    if not os.path.exists(path):
+        return None, None
+    with open(path) as f:
+        tj = json.load(f)
+    ent = tj.get(workload)
+    if not ent or ent.get("src_digest") != src_digest(*GEMM_SOURCES):
+        return None, None
+    return ent.get("dram_bytes_per_launch"), ent.get("source")
+
+
+def gemm1_kernel_name(cfg, T, native):
+    if cfg.mode == "w4a16" and T <= 16:
+        return "moe_gemv_kernel (GEMM1 + SwiGLU, warp MMA)"
+    if native:
+        return "moe_gemm_nvfp4_kernel<%d> (GEMM1 + SwiGLU, tcgen05 kind::mxf4nvf4)" % T
+    return "moe_gemm_kernel<%d> (GEMM1 + SwiGLU, tcgen05 kind::f16)" % T
+
+
+def measure(cfg, args, rank, world, local, dev, headline):
+    """Time one workload: the fused step (device-resident inputs), the atomic
+    finalize variant, the two-domain variant (headline only), the per-kernel
+    breakdown through the staged entry points, and the end-to-end step
+    through pinned host buffers.  Returns (line dict, inputs, route tile)."""
     import numpy as np
     import torch
 
     import block_scaled_fp4_sort_gb300 as fm
     import synth
-    from block_scaled_fp4_sort_gb300 import build as fbuild
     from block_scaled_fp4_sort_gb300.buffers import MoEBuffers, problem_for
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if rank == 0:
-        fbuild.build()
-    if world > 1:
-        torch.distributed.barrier()
-    fbuild.build()
-    cfg = synth.CONFIGS[args.workload]
-    if args.tokens or args.experts:
-        cfg = cfg.with_(M=args.tokens or cfg.M, E=args.experts or cfg.E, sample=0)
     cfg = replica_cfg(cfg, rank)
-    T = synth.route_tile_for(cfg)
+    T = args.route_tile or synth.route_tile_for(cfg)
     inp = synth.generate(cfg, device=dev)
     p = problem_for(cfg, T)
     B = MoEBuffers(p, dev).prepare(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
@@ -199,28 +269,36 @@ def run_ours(args, rank, world, local):
     x = inp.x if inp.x is not None else inp.x_q
     out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        B.forward(x, inp.x_sf, ids, wts, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale,
-                  stream=stream)
-
-    # ---------------- device-resident timed region
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    warm = max(args.warmup, 3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+
+    def timed(fn, clocks=False):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        clk = ClockSampler(local) if clocks else None
+        if clk:
+            clk.__enter__()
         torch.cuda.synchronize()
         e0.record(stream)
         for _ in range(args.steps):
-            step()
+            fn()
         e1.record(stream)
         torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
-    if world > 1:
-        torch.distributed.barrier()
+        if clk:
+            clk.__exit__(None, None, None)
+        ms_ = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+        if world > 1:
+            torch.distributed.barrier()
+        return ms_, (clk.summary() if clk else None)
+
+    # ---------------- device-resident timed region
+    def step():
+        B.forward(x, inp.x_sf, ids, wts, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale,
+                  stream=stream)
+    ms, clocks = timed(step, clocks=True)
     err = fm.read_error(B.fused_ws)
     if err:
         raise RuntimeError("device error word %d" % err)
@@ -229,20 +307,12 @@ def run_ours(args, rank, world, local):
     def step_atomic():
         B.forward(x, inp.x_sf, ids, wts, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale,
                   finalize_mode=fm.FINALIZE_ATOMIC, stream=stream)
-    for _ in range(max(args.warmup, 3)):
-        step_atomic()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        step_atomic()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms_atomic = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    ms_atomic, _ = timed(step_atomic)
 
     # ---------------- the same step over two locality domains: FC1 split on I,
     # FC2 on H, each half on a green context holding half of the SMs
     localized = None
-    if cfg.I % 256 == 0 and cfg.H % 256 == 0 and not args.no_localized:
+    if headline and cfg.I % 256 == 0 and cfg.H % 256 == 0 and not args.no_localized:
         try:
             doms = fm.Domains(local)
         except fm.Fp4MoeError as exc:
@@ -254,27 +324,20 @@ def run_ours(args, rank, world, local):
                 B.forward_localized(x, inp.x_sf, ids, wts, inp.w1_alpha, inp.w2_alpha, out,
                                     doms.streams, doms.sm_count, None, inp.fc2_input_scale,
                                     stream=stream)
-            for _ in range(max(args.warmup, 3)):
-                step_local()
-            torch.cuda.synchronize()
-            e0.record(stream)
-            for _ in range(args.steps):
-                step_local()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            ms_local = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+            ms_local, _ = timed(step_local)
             if fm.read_error(B.local_ws):
                 raise RuntimeError("device error word in the localized forward")
             localized = {"ms_per_step": ms_local, "value": tokens_per_s(world, cfg.M, ms_local),
                          "unit": UNIT, "sm_per_domain": doms.sm_count,
                          "streams": "green contexts"}
             B.w1d = B.w2d = None
+            B.local_ws = None
             torch.cuda.synchronize()
             doms.close()
 
     # ---------------- per-kernel breakdown through the staged entry points
     # (the fused call's kernels in its order: x into slot order, then GEMM1 on
-    # plain row tiles; events around each launch)
+    # plain row tiles; events on the launching stream around each launch)
     kernels = {}
     names = ["route_sort", "permute", "gemm1_swiglu", "gemm2", "finalize"]
     ev = {n: [] for n in names}
@@ -297,17 +360,18 @@ def run_ours(args, rank, world, local):
         elif name == "finalize":
             fm.moe_finalize(p, y, B.e2p, wts, 1.0, False, out, stream)
 
-    for it in range(max(args.warmup, 3) + args.steps):
+    for it in range(warm + args.steps):
         for n in names:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             launch(n)
             b.record(stream)
-            if it >= max(args.warmup, 3):
+            if it >= warm:
                 ev[n].append((a, b))
     torch.cuda.synchronize()
     for n in names:
         kernels[n] = statistics.mean(a.elapsed_time(b) for a, b in ev[n])
+    del px, pxsf, h, hsf, y
 
     # ---------------- end to end through host buffers
     pin = lambda t: t.detach().cpu().pin_memory()
@@ -330,17 +394,10 @@ def run_ours(args, rank, world, local):
         B.forward(dx, dxsf, dids, dw, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale,
                   stream=stream)
         hout.copy_(out, non_blocking=True)
-    for _ in range(max(args.warmup, 3)):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    e2e_ms, _ = timed(e2e_step)
     h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hw) + ((hxsf,) if hxsf is not None else ()))
     d2h = hout.numel() * hout.element_size()
+    del dx, dxsf, dids, dw, hx, hxsf, hout
 
     # ---------------- roofline of the dominant kernel (GEMM1)
     peaks, peak_src = load_peaks()
@@ -352,7 +409,8 @@ def run_ours(args, rank, world, local):
     w2_bytes_per_expert = H * I // 2 + H * I // sb
     act1 = {"w4a16": M * H * 2, "w4a4": M * H // 2 + M * H // 16,
             "w4a8": M * H + M * H // 32}[cfg.mode]
-    g1_bytes = touched * w1_bytes_per_expert + act1 + R * I * 2
+    h_bytes = {"w4a16": R * I * 2, "w4a4": R * I // 2 + R * I // 16, "w4a8": R * I + R * I // 32}[cfg.mode]
+    g1_bytes = touched * w1_bytes_per_expert + act1 + h_bytes
     g1_ms = kernels["gemm1_swiglu"]
     g1_flops = 4.0 * R * H * I
     # w4a4 with K a multiple of 256 and route tile >= 32 multiplies on the
@@ -360,65 +418,116 @@ def run_ours(args, rank, world, local):
     # weights.  The FP4 peak is the measured BF16 peak times the nominal
     # dense ratio 13.5 / 2.25 PFLOP/s.
     native = cfg.mode == "w4a4" and T >= 32 and H % 256 == 0
-    mma_peak = peaks["bf16_tflops"] * (13.5 / 2.25 if native else 1.0)
+    ratio = 13.5 / 2.25 if native else 1.0
+    # a kernel timed inside a loop that lasts about a second or more runs
+    # under the power cap: its denominator is the sustained cuBLAS rate
+    sustained = args.steps * ms > 500.0
+    bf16_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    mma_peak = bf16_peak * ratio
     # the roofline of GEMM1 is the HBM rate below the ridge (peak flops / peak
     # bytes) and the tensor rate of its MMA dtype above it
     tensor_bound = g1_flops / g1_bytes > mma_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    achieved = g1_bytes / (g1_ms * 1e-3) / 1e9
+    achieved_bw = g1_bytes / (g1_ms * 1e-3) / 1e9
+    achieved_tf = g1_flops / (g1_ms * 1e-3) / 1e12
     step_bytes = touched * (w1_bytes_per_expert + w2_bytes_per_expert) + act1 + M * H * 2
-    traffic_path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
-    traffic = None
-    if os.path.exists(traffic_path):
-        with open(traffic_path) as f:
-            tj = json.load(f)
-        if tj.get("workload") == cfg.name:
-            traffic = tj.get("dram_bytes_per_launch")
-    tokens_s = tokens_per_s(world, cfg.M, ms)
+    traffic, traffic_src = stored_traffic(cfg.name)
+    g2_ms = kernels["gemm2"]
+    roof = {"kernel": gemm1_kernel_name(cfg, T, native), "mma_dtype": "nvfp4" if native else "bf16"}
+    if tensor_bound:
+        roof.update({"bound": "tensor", "achieved": achieved_tf, "peak": mma_peak,
+                     "unit": "TFLOP/s", "frac": achieved_tf / mma_peak,
+                     "algorithmic_flops": g1_flops})
+    else:
+        roof.update({"bound": "hbm", "achieved": achieved_bw, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved_bw / peaks["hbm_gbs"],
+                     "algorithmic_bytes": g1_bytes})
+    roof.update({
+        "traffic": traffic, "traffic_source": traffic_src,
+        "peak_source": "%s (%s)" % (
+            peak_src, ("bf16_tflops_sustained: GEMM1 timed inside a %.1f s loop" % (args.steps * ms / 1e3)
+                       if sustained else "bf16_tflops burst") + (" x 13.5/2.25 nominal fp4 ratio"
+                                                                  if native else "")
+            if tensor_bound else "hbm_gbs"),
+        "touched_experts": touched,
+        "tensor_frac": achieved_tf / mma_peak,
+        "tensor_frac_of_burst": achieved_tf / (peaks["bf16_tflops"] * ratio),
+        "hbm_frac": achieved_bw / peaks["hbm_gbs"],
+        "gemm2": {"ms": g2_ms, "tflops": 2.0 * R * H * I / (g2_ms * 1e-3) / 1e12,
+                  "tensor_frac": 2.0 * R * H * I / (g2_ms * 1e-3) / 1e12 / mma_peak},
+    })
+    routes_kernels = 1 if R <= 4096 else 3
     line = {
-        "metric": METRIC, "value": tokens_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True,
+        "metric": METRIC, "value": tokens_per_s(world, cfg.M, ms), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": ("nvfp4" if native else
                   {"w4a16": "bf16", "w4a4": "nvfp4->bf16", "w4a8": "mxfp8->bf16"}[cfg.mode]),
         "data": "synthetic (seeded generator; random NVFP4 weights)",
         "config": dict(workload_config(cfg, T), l2="inputs larger than L2: %.2f GB of weights "
-                       "per step vs 126 MB L2" % (step_bytes / 1e9), parallelism="replicas" if world > 1 else "1 GPU"),
+                       "and activations per step vs 126 MB L2" % (step_bytes / 1e9),
+                       parallelism="replicas" if world > 1 else "1 GPU"),
         "tflops": world * cfg.flops() / (ms * 1e-3) / 1e12,
         "step_hbm_gbs": step_bytes / (ms * 1e-3) / 1e9,
-        "roofline": dict({"kernel": ("moe_gemv_kernel<0> (GEMM1 + SwiGLU, warp MMA)"
-                                     if cfg.mode == "w4a16" and T == 16 else
-                                     "moe_gemm_nvfp4_kernel<%d, 1> (GEMM1 + SwiGLU, tcgen05 "
-                                     "kind::mxf4nvf4)" % T if native else
-                                     "moe_gemm_kernel<%d, %d> (GEMM1 + SwiGLU, tcgen05)"
-                                     % (T, {"w4a16": 0, "w4a4": 1, "w4a8": 6}[cfg.mode])),
-                          "mma_dtype": "nvfp4" if native else "bf16"},
-                         **({"bound": "tensor", "achieved": g1_flops / (g1_ms * 1e-3) / 1e12,
-                             "peak": mma_peak, "unit": "TFLOP/s",
-                             "frac": g1_flops / (g1_ms * 1e-3) / 1e12 / mma_peak,
-                             "algorithmic_flops": g1_flops}
-                            if tensor_bound else
-                            {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                             "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                             "algorithmic_bytes": g1_bytes}),
-                         traffic=traffic, peak_source=peak_src + (" (bf16 x 13.5/2.25 nominal "
-                                                                  "fp4 ratio)" if native and tensor_bound else ""),
-                         touched_experts=touched,
-                         tensor_frac=g1_flops / (g1_ms * 1e-3) / 1e12 / mma_peak,
-                         hbm_frac=achieved / peaks["hbm_gbs"]),
+        "roofline": roof,
         "kernels_ms": kernels,
         "atomic_finalize": {"ms_per_step": ms_atomic, "value": tokens_per_s(world, cfg.M, ms_atomic),
                             "unit": UNIT},
         "localized": localized,
-        "e2e": {"value": tokens_per_s(world, cfg.M, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "clocks": clk.summary(),
+        "e2e": {"value": tokens_per_s(world, cfg.M, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
         # per fused step: routing (1 kernel up to 4096 routes, else 3), x in slot
-        # order, GEMM1, the w4a4 / w4a8 h -> BF16 expansion, GEMM2, finalize
-        # (native NVFP4: h goes to GEMM2 as it is, no expansion)
-        "gpu_launches": args.steps * ((1 if cfg.routes <= 4096 else 3) + 1 + 3 +
+        # order, GEMM1, the w4a8 / decode-size w4a4 h -> BF16 expansion, GEMM2, finalize
+        "gpu_launches": args.steps * (routes_kernels + 1 + 3 +
                                       (0 if cfg.mode == "w4a16" or native else 1)),
     }
+    del B, out
+    torch.cuda.synchronize()
     return line, inp, T
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import synth
+    from block_scaled_fp4_sort_gb300 import build as fbuild
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        fbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    fbuild.build()
+
+    def cfg_of(name):
+        cfg = synth.CONFIGS[name]
+        if args.tokens or args.experts:
+            cfg = cfg.with_(M=args.tokens or cfg.M, E=args.experts or cfg.E, sample=0)
+        return cfg
+
+    cfg = cfg_of(args.workload)
+    line, inp, T = measure(cfg, args, rank, world, local, dev, headline=True)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp.cfg, inp, T, args.cpu_budget)
+    del inp
+    torch.cuda.empty_cache()
+    others = [] if args.also in ("", "none") else [w for w in args.also.split(",")
+                                                    if w != args.workload]
+    if others:
+        line["workloads"] = {}
+    for name in others:
+        sub, sinp, sT = measure(cfg_of(name), args, rank, world, local, dev, headline=False)
+        if rank == 0 and not args.no_cpu_baseline:
+            sub["cpu_baseline"] = cpu_baseline(sinp.cfg, sinp, sT, args.cpu_budget / 4)
+        line["gpu_launches"] += sub["gpu_launches"]
+        line["workloads"][name] = {k: sub[k] for k in (
+            "value", "unit", "ms_per_step", "tflops", "step_hbm_gbs", "dtype", "config", "roofline",
+            "kernels_ms", "atomic_finalize", "e2e", "clocks", "gpu_launches") + (
+            ("cpu_baseline",) if "cpu_baseline" in sub else ())}
+        del sinp
+        torch.cuda.empty_cache()
+    return line
 
 
 def pages_per_tile(groups, top_k, row_bytes, page=2 << 20):
@@ -528,39 +637,70 @@ def run_locality(args):
     print(json.dumps(res))
 
 
+def run_reference(args, world):
+    """The reference arm: the CPU oracle, as it stands, on the host cores, over
+    bounded samples of the headline workload (each step a different slice of
+    the seeded token sample, sized so that the whole run stays within a few
+    minutes)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth
+    cfg = synth.CONFIGS[args.workload]
+    T = args.route_tile or synth.route_tile_for(cfg)
+    # inputs are drawn on the GPU when there is one (input preparation, not
+    # timed), then copied to the host for the oracle
+    inp = synth.generate(cfg, device="cuda" if torch.cuda.is_available() else "cpu").to("cpu")
+    oracle.build()
+    orc = oracle.OracleMoE.from_inputs(inp, T=T)
+    toks = oracle_tokens(cfg, inp)
+    ncpu = os.cpu_count() or 1
+    # calibration: one token per thread
+    t0 = time.perf_counter()
+    orc.forward(toks[:min(ncpu, len(toks))], nthreads=min(ncpu, len(toks)))
+    per_round = time.perf_counter() - t0
+    budget = 90.0 / max(1, args.steps + args.warmup)       # seconds per step
+    per_step = int(min(len(toks), max(1, int(budget / max(per_round, 1e-9))) * ncpu))
+    cores = min(ncpu, per_step)
+
+    def slice_of(i):
+        a = (i * per_step) % len(toks)
+        return np.take(toks, np.arange(a, a + per_step), mode="wrap")
+    for i in range(args.warmup):
+        orc.forward(slice_of(i), nthreads=cores)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        orc.forward(slice_of(args.warmup + i), nthreads=cores)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    v = per_step / dt
+    sample = ("%d tokens per step from the %d-token %s of %s (each step the next slice)"
+              % (per_step, len(toks), "seeded sample" if cfg.sample else "batch", cfg.name))
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(cfg, T),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample, "host_cpus": ncpu},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     if args.locality:
         return run_locality(args)
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; the other ranks have no work
+        if rank == 0:
+            run_reference(args, world)
+        return
     if world > 1:
         import torch
-        backend = "nccl" if args.impl == "ours" else "gloo"
-        torch.distributed.init_process_group(backend)
-    import synth
-    cfg = synth.CONFIGS[args.workload]
-    T = synth.route_tile_for(cfg)
-    if args.impl == "reference":
-        if rank != 0:
-            return
-        inp = synth.generate(cfg, device="cpu")
-        v, dt, cores, n = time_oracle(inp, T, args.steps, args.warmup)
-        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": workload_config(cfg, T),
-                "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                 "sample": "all %d tokens of one %s batch per step" % (n, cfg.name)},
-                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line), flush=True)
-        return
-    line, inp, T = run_ours(args, rank, world, local)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local)
     if rank == 0:
-        if not args.no_cpu_baseline:
-            inp_cpu = inp.to("cpu")
-            v, dt, cores, n = time_oracle(inp_cpu, T, 3, 1)
-            line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                    "sample": "all %d tokens of one %s batch, 3 timed runs" % (n, cfg.name)}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch

@@ -25,7 +25,7 @@ ABI_FUNCTIONS = (
     "fp4moe_prepared_weight_size", "fp4moe_read_error", "fp4moe_clear_error",
     "fp4moe_prepare_weights", "moe_route_sort", "moe_route_sort_noalloc", "moe_permute", "moe_gemm1_swiglu", "moe_gemm2",
     "moe_finalize", "fused_moe_forward", "fp4moe_debug_quantize_nvfp4",
-    "fp4moe_debug_quantize_mxfp8", "fp4moe_debug_decode_prepared",
+    "fp4moe_debug_quantize_mxfp8", "fp4moe_debug_decode_prepared", "fp4moe_debug_wait_timeout",
     "fp4moe_domain_weight_size", "fp4moe_prepare_domain_weights",
     "fp4moe_localized_workspace_size", "fused_moe_forward_localized", "fp4moe_domains_create",
     "fp4moe_domains_stream", "fp4moe_domains_destroy",
@@ -125,6 +125,7 @@ def lib() -> ctypes.CDLL:
             "fp4moe_debug_quantize_nvfp4": (i32, [vp, i64, vp, vp, vp, vp]),
             "fp4moe_debug_quantize_mxfp8": (i32, [vp, i64, vp, vp, vp]),
             "fp4moe_debug_decode_prepared": (i32, [P, i32, vp, vp, vp]),
+            "fp4moe_debug_wait_timeout": (i32, [i64, vp, vp]),
             "fp4moe_domain_weight_size": (sz, [P, i32]),
             "fp4moe_prepare_domain_weights": (i32, [P, i32, vp, vp, vp, vp]),
             "fp4moe_localized_workspace_size": (sz, [P]),
@@ -297,6 +298,11 @@ def debug_quantize_mxfp8(x, q, sf, stream=None):
 def debug_quantize_nvfp4(x, scale, q, sf, stream=None):
     _check(lib().fp4moe_debug_quantize_nvfp4(_p(x), x.numel(), _p(scale), _p(q), _p(sf),
                                              _stream(stream)), "fp4moe_debug_quantize_nvfp4")
+
+
+def debug_wait_timeout(limit_ns: int, workspace, stream=None):
+    _check(lib().fp4moe_debug_wait_timeout(int(limit_ns), _p(workspace), _stream(stream)),
+           "fp4moe_debug_wait_timeout")
 
 
 def debug_decode_prepared(p: Problem, which: int, prepared, out, stream=None):

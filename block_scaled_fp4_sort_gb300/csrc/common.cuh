@@ -79,18 +79,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait on phase `parity`.  Returns false (and records a timeout in
-// *err) if the phase did not complete within FP4MOE_WAIT_NS.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+// *err) if the phase did not complete within `limit_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, int* err,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer() - t0 > FP4MOE_WAIT_NS) {
+    if (globaltimer() - t0 > limit_ns) {
       set_error(err, kErrTimeout);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  return mbar_wait_for(bar, parity, err, FP4MOE_WAIT_NS);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -758,6 +758,12 @@ fp4moe_status fp4moe_debug_quantize_nvfp4(const float* in, int64_t n, const floa
   return cuda_status(launch_debug_quantize(in, n, scale, q, sf, static_cast<cudaStream_t>(stream)));
 }
 
+fp4moe_status fp4moe_debug_wait_timeout(int64_t limit_ns, void* workspace, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 1000000000LL || !ok_ptr(workspace)) return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_debug_wait((uint64_t)limit_ns, err_word(workspace),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 fp4moe_status fp4moe_debug_quantize_mxfp8(const float* in, int64_t n, uint8_t* q, uint8_t* sf,
                                           void* stream) {
   if (n < 0 || n % 32 != 0 || (n > 0 && (!ok_ptr(in) || !ok_ptr(q) || !ok_ptr(sf))))

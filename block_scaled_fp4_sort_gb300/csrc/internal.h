@@ -116,6 +116,8 @@ cudaError_t launch_debug_quantize_mx(const float* in, int64_t n, uint8_t* q, uin
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl);
 cudaError_t launch_debug_quantize(const float* in, int64_t n, const float* scale, uint8_t* q,
                                   uint8_t* sf, cudaStream_t st);
+// one warp waits on an mbarrier nothing completes, bounded by limit_ns
+cudaError_t launch_debug_wait(uint64_t limit_ns, int* err, cudaStream_t st);
 
 // ---- weight preparation (prepare.cu) ----
 cudaError_t launch_prepare(const Shape& s, int which, const uint8_t* w, const uint8_t* w_sf,

@@ -360,4 +360,27 @@ cudaError_t launch_debug_quantize(const float* in, int64_t n, const float* scale
   return cudaGetLastError();
 }
 
+// A wait that nothing completes: one warp initialises an mbarrier that no
+// thread arrives on and waits for its first phase with a `limit_ns` bound,
+// the way every pipeline wait of the GEMMs is bounded.  The wait must give
+// up, record FP4MOE_ERR_DEVICE_TIMEOUT in the error word and let the kernel
+// return (the same wind-down: a warp-wide vote, then exit).
+__global__ void debug_wait_kernel(uint64_t limit_ns, int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_for(&bar, 0, threadIdx.x == 0 ? err : nullptr,
+                                                        limit_ns));
+  if (!ok) return;
+  set_error(err, kErrDevice);   // unreachable unless the wait completed
+}
+
+cudaError_t launch_debug_wait(uint64_t limit_ns, int* err, cudaStream_t st) {
+  debug_wait_kernel<<<1, 32, 0, st>>>(limit_ns, err);
+  return cudaGetLastError();
+}
+
 }  // namespace fp4moe

@@ -11,15 +11,20 @@
 // loads the library and lives until the process exits.
 //
 // The host cannot pass the array's name to a kernel (in host code it is only
-// a stand-in symbol), so the first call on each device looks up its device
-// address with cudaGetSymbolAddress, with that device current, and caches
-// it; make that first call before any stream capture.  All calls share the
-// array: calls that overlap on the GPU (two streams, two threads) race on
-// it.  Each call clears the error word it uses before launching; the
+// a stand-in symbol), so the first call in each CUDA context looks up its
+// device address with cudaGetSymbolAddress, with that context current, and
+// caches it keyed by the context (a __device__ symbol's address belongs to
+// the context the module was loaded into: the device's primary context, a
+// caller's own driver-API context, or the primary context re-created after a
+// device reset); make that first call before any stream capture.  All calls
+// share the array: calls that overlap on the GPU (two streams, two threads)
+// race on it.  Each call clears the error word it uses before launching; the
 // histogram tables are fully rewritten by every call that needs them.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "fp4moe.h"
 #include "internal.h"
@@ -28,24 +33,54 @@ namespace fp4moe {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 1u << 20;  // 1 MiB: header + per-chunk tables
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
 static __device__ __align__(256) uint8_t g_route_scratch[kNoAllocScratchBytes];
 
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+struct ScratchEntry {
+  CUcontext ctx;
+  void* addr;
+};
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch_addr[kMaxContexts];
+int g_scratch_n = 0;
 
-// Device address of g_route_scratch on the current device (looked up once).
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    e = cudaGetSymbolAddress(&p, g_route_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev].store(p, std::memory_order_release);
+// The current context (driver API, reached through the runtime's entry-point
+// query so that the library needs no link against libcuda).
+cudaError_t current_context(CUcontext* ctx) {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return cudaErrorNotSupported;
+    fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
   }
+  return fn(ctx) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+// Device address of g_route_scratch in the current context, looked up once
+// per context.  With no context current yet, the lookup itself makes the
+// device's primary context current (runtime initialisation) and the address
+// is cached under that context.
+cudaError_t scratch_address(void** out) {
+  CUcontext ctx = nullptr;
+  cudaError_t e = current_context(&ctx);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (ctx != nullptr)
+    for (int i = 0; i < g_scratch_n; ++i)
+      if (g_scratch_addr[i].ctx == ctx) {
+        *out = g_scratch_addr[i].addr;
+        return cudaSuccess;
+      }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_route_scratch);
+  if (e != cudaSuccess) return e;
+  if (ctx == nullptr && (e = current_context(&ctx)) != cudaSuccess) return e;
+  if (ctx != nullptr && g_scratch_n < kMaxContexts) g_scratch_addr[g_scratch_n++] = ScratchEntry{ctx, p};
   *out = p;
   return cudaSuccess;
 }

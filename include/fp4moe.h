@@ -218,13 +218,18 @@ FP4MOE_API fp4moe_status moe_route_sort(const fp4moe_problem* p, const int32_t* 
  * until the process exits.  The library allocates nothing in this call.
  *   error_flag  int32 [1] or NULL: if given, zeroed and then set to
  *               FP4MOE_ERR_DEVICE when an expert id lies outside
- *               [0, num_experts); if NULL that word lives in the array.
+ *               [0, num_experts).  If NULL, that word lives in the array and
+ *               no call can read it back: an invalid id is then NOT
+ *               reported (its routes are still dropped).  Callers that need
+ *               the report must pass a flag.
  * Returns FP4MOE_ERR_UNSUPPORTED if the problem needs more scratch than the
  * array holds: ceil(M*top_k / 4096) * E_local * 4 bytes + 256 must fit in
- * 1 MiB (routes up to 4096 need none).  The first call on each device looks
- * up the array's device address (cudaGetSymbolAddress with that device
- * current); make it before any stream capture.  Every call shares the array,
- * so calls that overlap on the GPU (other streams, other threads) race. */
+ * 1 MiB (routes up to 4096 need none).  The first call in each CUDA context
+ * (a device's primary context, or a caller's own driver-API context) looks
+ * up the array's device address there (cudaGetSymbolAddress with that
+ * context current) and caches it per context; make that first call before
+ * any stream capture.  Every call shares the array, so calls that overlap
+ * on the GPU (other streams, other threads) race. */
 FP4MOE_API fp4moe_status moe_route_sort_noalloc(const fp4moe_problem* p,
                                                 const int32_t* token_selected_experts,
                                                 int32_t* expanded_idx_to_permuted_idx,
@@ -427,6 +432,14 @@ FP4MOE_API fp4moe_status fp4moe_debug_quantize_nvfp4(const float* in, int64_t n,
  * (n multiple of 32, device pointers): q gets n E4M3 bytes, sf n/32 E8M0. */
 FP4MOE_API fp4moe_status fp4moe_debug_quantize_mxfp8(const float* in, int64_t n, uint8_t* q,
                                                   uint8_t* sf, void* stream);
+
+/* The bounded-wait protocol of the kernels, made to expire: one warp waits
+ * on an mbarrier that nothing completes, giving up after limit_ns
+ * nanoseconds (1 .. 1e9) of %globaltimer, the way every pipeline wait of
+ * the GEMMs gives up after its 2 s bound.  The kernel then returns and sets
+ * the workspace's error word to FP4MOE_ERR_DEVICE_TIMEOUT; the stream stays
+ * usable.  Exported so that tests can check that path without a hang. */
+FP4MOE_API fp4moe_status fp4moe_debug_wait_timeout(int64_t limit_ns, void* workspace, void* stream);
 
 /* Decode prepared weights back to their BF16 values as the GEMM kernels see
  * them: out bf16 [E_local, rows, K] for GEMM `which` (rows = 2I or H).

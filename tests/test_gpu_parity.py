@@ -14,7 +14,7 @@ import torch
 import block_scaled_fp4_sort_gb300 as fm
 import oracle
 import synth
-from ref_decode import dequant_np
+from ref_decode import dequant_np, unexplained_mxfp8_flips, unexplained_nvfp4_flips
 from block_scaled_fp4_sort_gb300.buffers import MoEBuffers, problem_for
 
 pytestmark = pytest.mark.gpu
@@ -107,6 +107,25 @@ def test_route_sort_invalid_ids_set_the_error_word():
     assert e2p[1, 1] == -1 and e2p[2, 0] == -1
     plan = oracle.route_plan(3, 8, 2, 16, ids)
     assert np.array_equal(e2p.ravel(), plan["expanded_idx_to_permuted_idx"].ravel())
+
+
+def test_bounded_wait_expires_and_reports_timeout():
+    # an mbarrier wait that nothing completes gives up after its bound (1 ms
+    # here, 2 s in the GEMMs), records the timeout and lets the kernel return
+    import time
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    t0 = time.perf_counter()
+    fm.debug_wait_timeout(1_000_000, ws)
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 5.0
+    assert fm.read_error(ws) == fm.ERR_DEVICE_TIMEOUT
+    fm.clear_error(ws)
+    assert fm.read_error(ws) == 0
+    # the context stays usable: a routing plan afterwards is still exact
+    ids = np.array([[0, 1], [3, 2], [1, 0]], np.int32)
+    B = run_route(fm.problem(3, 256, 256, 4, 2), ids)
+    assert fm.read_error(B.route_ws) == 0
+    assert_plan_equal(B, oracle.route_plan(3, 4, 2, 16, ids))
 
 
 # ------------------------------------------------------------------ codecs
@@ -448,9 +467,13 @@ def test_w4a8_fused_forward_tiny(T, act):
         t, j = divmod(int(p2e[s]), cfg.top_k)
         e = int(inp.token_selected_experts[t, j])
         st = orc.expert_ffn(e, t)
-        flips += int(np.sum(st["hq"] != hq[s]))
+        flips += int(np.sum(st["hq"] != hq[s])) + int(np.sum(st["hsf"] != hs[s]))
+        # staged FC1 gate: a code or scale that differs from the oracle's sits
+        # at a rounding boundary of the oracle's pre-quantisation value
+        bad = unexplained_mxfp8_flips(st["h_pre"], hq[s], hs[s], st["hq"], st["hsf"])
+        assert not bad, ("w4a8 FC1 flips off a rounding boundary", int(s), bad[:8])
         check_out(yv[s], orc.expert_down_codes(e, hq[s], hs[s]), 5e-3, what="w4a8 GEMM2 slot %d" % s)
-    print("w4a8 FC1 code bytes differing from the oracle: %d" % flips)
+    print("w4a8 FC1 code/scale bytes differing from the oracle: %d" % flips)
 
 
 def test_prefill_w4a8_sampled():
@@ -613,14 +636,19 @@ def test_prefill_w4a4_sampled():
     rng = np.random.default_rng(0)
     slots = rng.choice(np.nonzero(p2e >= 0)[0], 24, replace=False)
     flips = 0
+    fs = float(inp.fc2_input_scale[0])
     for s in slots:
         t, j = divmod(int(p2e[s]), cfg.top_k)
         e = int(inp.token_selected_experts[t, j])
         st = orc.expert_ffn(e, t)
-        flips += int(np.sum(st["hq"] != hq[s]))
+        flips += int(np.sum(st["hq"] != hq[s])) + int(np.sum(st["hsf"] != hs[s]))
+        # staged FC1 gate (P8 step 1): every differing code or scale sits within
+        # 1e-3 (relative) of a rounding boundary of the oracle's value
+        bad = unexplained_nvfp4_flips(st["h_pre"], fs, hq[s], hs[s], st["hq"], st["hsf"])
+        assert not bad, ("w4a4 FC1 flips off a rounding boundary", int(s), bad[:8])
         y_ref = orc.expert_down_codes(e, hq[s], hs[s])
         check_out(yv[s], y_ref, 5e-3, what="w4a4 GEMM2 on GPU codes, slot %d" % s)
-    print("FC1 code bytes differing from the oracle: %d of %d" % (flips, len(slots) * cfg.I // 2))
+    print("FC1 code/scale bytes differing from the oracle: %d of %d" % (flips, len(slots) * cfg.I * 9 // 16))
 
 
 def test_large_batch_sampled_and_row_independence():
