@@ -49,7 +49,11 @@ fp4moe_status validate(const fp4moe_problem* p, Shape* s) {
     T = auto_tile(R, EL);
   } else if (T < 8 || T % 8 != 0) {
     return FP4MOE_ERR_INVALID_ARG;
-  } else if (T != 16 && T != 32 && T != 64 && T != 128) {
+  } else if (T != 8 && T != 16 && T != 32 && T != 64 && T != 128 && T != 256) {
+    return FP4MOE_ERR_UNSUPPORTED;
+  } else if ((T == 8 || T == 256) && p->mode != FP4MOE_W4A16) {
+    // 8 runs on the warp-MMA kernel and 256 on the one-tile tcgen05 kernel,
+    // both for BF16 activations only
     return FP4MOE_ERR_UNSUPPORTED;
   }
   const int64_t ne = std::min<int64_t>(R, EL);

@@ -49,11 +49,20 @@ inline int64_t row_blocks(const Shape& s, int which) {
   return (s.H + 255) / 256;
 }
 inline int64_t k_chunks(const Shape& s, int which) { return which == 1 ? s.H / kBK : s.I / kBK; }
-// Decode-size problems (BF16 activations, route tile 16) run on the
+// Decode-size problems (BF16 activations, route tile 8 or 16) run on the
 // warp-level MMA kernel, whose prepared blocks hold the codes in MMA fragment
-// order; every other problem uses the row order of the tcgen05 kernel.  Both
+// order; every other problem uses the row order of the tcgen05 kernels.  Both
 // layouts have the same block size and the same scale region.
-inline bool fragment_layout(const Shape& s) { return s.mode == 0 && s.T == 16; }
+inline bool fragment_layout(const Shape& s) { return s.mode == 0 && s.T <= 16; }
+
+// BF16 activations with route tiles of 32..256 slots run on the one-tile
+// tcgen05 kernel: work items of one 128-row weight tile (half of a prepared
+// 256-row block; a gated GEMM1 tile holds 64 gate rows and their 64 up rows).
+inline bool one_tile(const Shape& s) { return s.mode == 0 && s.T >= 32; }
+inline int64_t one_tile_blocks(const Shape& s, int which) {
+  if (which == 1) return gated(s) ? s.I / 64 : (s.I + 127) / 128;
+  return (s.H + 127) / 128;
+}
 
 // w4a4 GEMMs whose reduction is a multiple of 256 run on the native NVFP4
 // tensor-core MMA (route tiles 32..128).  Their prepared weights come in

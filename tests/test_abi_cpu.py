@@ -52,7 +52,8 @@ def test_product_does_not_reach_the_oracle():
 
 
 @pytest.mark.parametrize("M,E,k,T", [(8, 256, 8, 16), (4096, 256, 8, 128), (2048, 128, 4, 64),
-                                     (131072, 256, 8, 128), (16, 8, 2, 16), (1, 1, 1, 32), (0, 4, 2, 16)])
+                                     (131072, 256, 8, 128), (16, 8, 2, 16), (1, 1, 1, 32), (0, 4, 2, 16),
+                                     (8, 256, 8, 8), (131072, 256, 8, 256), (2048, 128, 4, 256)])
 def test_slot_bound_matches_oracle(lib, M, E, k, T):
     p = fm.problem(M, 256, 256, E, k, route_tile=T)
     assert fm.max_permuted_slots(p) == oracle.max_permuted_slots(M * k, E, T)
@@ -80,8 +81,12 @@ def test_sizes(lib):
     (dict(inter=100), fm.ERR_INVALID_ARG),
     (dict(top_k=0), fm.ERR_INVALID_ARG),
     (dict(route_tile=7), fm.ERR_INVALID_ARG),
-    (dict(route_tile=8), fm.ERR_UNSUPPORTED),
-    (dict(route_tile=256), fm.ERR_UNSUPPORTED),
+    (dict(route_tile=12), fm.ERR_INVALID_ARG),
+    (dict(route_tile=24), fm.ERR_UNSUPPORTED),
+    (dict(route_tile=512), fm.ERR_UNSUPPORTED),
+    (dict(route_tile=8, mode=fm.W4A4), fm.ERR_UNSUPPORTED),
+    (dict(route_tile=256, mode=fm.W4A4), fm.ERR_UNSUPPORTED),
+    (dict(route_tile=256, mode=fm.W4A8), fm.ERR_UNSUPPORTED),
     (dict(num_local_experts=300), fm.ERR_INVALID_ARG),
     (dict(num_local_experts=16, local_expert_offset=250), fm.ERR_INVALID_ARG),
     (dict(mode=5), fm.ERR_INVALID_ARG),

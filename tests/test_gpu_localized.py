@@ -101,6 +101,7 @@ def _side_streams():
 
 
 @pytest.mark.parametrize("mode,act,T", [("w4a16", "swiglu", 32), ("w4a16", "swiglu", 128),
+                                        ("w4a16", "swiglu", 256), ("w4a16", "relu2", 256),
                                         ("w4a4", "swiglu", 64), ("w4a8", "swiglu", 32),
                                         ("w4a16", "relu2", 32), ("w4a4", "geglu_tanh", 32),
                                         ("w4a16", "swiglu_oai", 64)])

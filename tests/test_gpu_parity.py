@@ -269,7 +269,8 @@ def _fused(inp, B, rsf=1.0, accumulate=False, out=None, mode=fm.FINALIZE_DETERMI
 
 
 @pytest.mark.parametrize("name,T", [("tiny_w4a16", 16), ("tiny_w4a16", 32), ("tiny_w4a16", 64),
-                                    ("tiny_w4a16", 128), ("decode_w4a16", 16)])
+                                    ("tiny_w4a16", 128), ("tiny_w4a16", 256), ("tiny_w4a16", 8),
+                                    ("decode_w4a16", 16), ("decode_w4a16", 8)])
 def test_fused_forward_w4a16_full(name, T):
     cfg = synth.CONFIGS[name]
     inp, p, B, orc = _setup(cfg, T)
@@ -278,12 +279,13 @@ def test_fused_forward_w4a16_full(name, T):
     check_out(f64(out), exact, 5e-3, what="%s T=%d" % (name, T))
 
 
-def test_fused_forward_skewed_full():
+@pytest.mark.parametrize("T", [0, 256])   # 0: the workload's route tile
+def test_fused_forward_skewed_full(T):
     cfg = synth.CONFIGS["skewed_w4a16"]
-    inp, p, B, orc = _setup(cfg)
+    inp, p, B, orc = _setup(cfg, T or None)
     out = _fused(inp, B)
     _, exact, _ = orc.forward(nthreads=NTHREADS)
-    check_out(f64(out), exact, 5e-3, what="skewed")
+    check_out(f64(out), exact, 5e-3, what="skewed T=%d" % B.T)
 
 
 def test_staged_path_matches_oracle_and_fused():
@@ -489,6 +491,7 @@ def test_prefill_w4a8_sampled():
 
 @pytest.mark.parametrize("name,T,mode", [("tiny_w4a16", 16, fm.FINALIZE_DETERMINISTIC),
                                          ("tiny_w4a16", 32, fm.FINALIZE_DETERMINISTIC),
+                                         ("skewed_w4a16", 256, fm.FINALIZE_DETERMINISTIC),
                                          ("skewed_w4a16", 64, fm.FINALIZE_ATOMIC)])
 def test_fused_forward_replays_from_a_cuda_graph(name, T, mode):
     # the library never allocates, synchronises or reads device memory on the
@@ -536,7 +539,7 @@ ATOMIC = fm.FINALIZE_ATOMIC
 
 
 @pytest.mark.parametrize("name,T", [("tiny_w4a16", 16), ("tiny_w4a16", 32), ("decode_w4a16", 16),
-                                    ("skewed_w4a16", 64)])
+                                    ("skewed_w4a16", 64), ("skewed_w4a16", 256), ("tiny_w4a16", 8)])
 def test_atomic_finalize_matches_oracle(name, T):
     # warp-MMA kernel at T = 16, tcgen05 kernel otherwise; same bar as the
     # deterministic path (the terms are the same, only their order varies)
@@ -651,13 +654,14 @@ def test_prefill_w4a4_sampled():
     print("FC1 code/scale bytes differing from the oracle: %d of %d" % (flips, len(slots) * cfg.I * 9 // 16))
 
 
-def test_large_batch_sampled_and_row_independence():
+@pytest.mark.parametrize("T", [128, 256])
+def test_large_batch_sampled_and_row_independence(T):
     cfg = synth.CONFIGS["large_w4a16"]
-    inp, p, B, orc = _setup(cfg)
+    inp, p, B, orc = _setup(cfg, T)
     out = _fused(inp, B)
     toks = inp.sample_tokens
     _, exact, _ = orc.forward(toks, nthreads=NTHREADS)
-    check_out(f64(out)[toks], exact, 5e-3, what="large sampled")
+    check_out(f64(out)[toks], exact, 5e-3, what="large sampled T=%d" % T)
     # row independence: the sampled tokens alone give the same rows bit for bit
     import dataclasses
     sub = dataclasses.replace(inp, cfg=cfg.with_(M=len(toks), sample=0),
@@ -730,7 +734,8 @@ def test_native_nvfp4_forward_replays_from_a_cuda_graph():
 
 # ------------------------------------------------------------------ TMA row gather (kept last)
 
-@pytest.mark.parametrize("name,T", [("tiny_w4a16", 16), ("tiny_w4a16", 64), ("skewed_w4a16", 64)])
+@pytest.mark.parametrize("name,T", [("tiny_w4a16", 16), ("tiny_w4a16", 64), ("skewed_w4a16", 64),
+                                    ("skewed_w4a16", 256), ("tiny_w4a16", 8)])
 def test_gather_matches_permuted(name, T):
     cfg = synth.CONFIGS[name]
     if name == "skewed_w4a16":
