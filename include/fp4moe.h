@@ -126,7 +126,9 @@ typedef struct {
   int32_t top_k;               /* 1 <= top_k <= num_experts */
   int32_t num_local_experts;   /* 0 means num_experts */
   int32_t local_expert_offset; /* offset + num_local_experts <= num_experts */
-  int32_t route_tile;          /* T: 0 = automatic, else 16, 32, 64 or 128 */
+  int32_t route_tile;          /* T: 0 = automatic, else 8, 16, 32, 64, 128 or 256
+                                  (8 and 256 for FP4MOE_W4A16 only; another
+                                  multiple of 8 returns FP4MOE_ERR_UNSUPPORTED) */
   int32_t mode;                /* fp4moe_quant_mode */
   fp4moe_activation activation;  /* FC1 activation; all zero = SwiGLU */
 } fp4moe_problem;
@@ -259,7 +261,9 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
  * block-scaled FP4 tensor-core MMA -- the same exact products, fp32
  * accumulation):
  *   h[s, n] = R( act(c_s a1_e G_e[n] . A_s, c_s a1_e U_e[n] . A_s) )
- * for valid slots s (padding rows of h are zeroed), e = tile_idx_to_expert,
+ * for valid slots s, e = tile_idx_to_expert (rows of padding slots are
+ * zeroed by the decode-size and w4a4 / w4a8 kernels and left unwritten by the
+ * BF16 kernel of route tiles 32..256; no later step reads them),
  * act = p->activation (default silu(g) * u; ReLU^2 has no gate rows), and
  * c_s = per_token_scale[t] of the slot's token t = gather_rows[s] / top_k
  * (cute_dsl_fused_moe per_token_scale) or 1 when per_token_scale is NULL;
