@@ -17,14 +17,14 @@ LIB_PATH = os.path.join(_HERE, "libfp4moe.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA, ERR_DEVICE, ERR_DEVICE_TIMEOUT = range(7)
 W4A16, W4A4, W4A8 = 0, 1, 2
-FINALIZE_DETERMINISTIC, FINALIZE_ATOMIC = 0, 1
+FINALIZE_DETERMINISTIC, FINALIZE_ATOMIC, FINALIZE_PARTIAL_F32 = 0, 1, 2
 
 ABI_FUNCTIONS = (
     "fp4moe_status_string", "fp4moe_route_tile", "fp4moe_max_permuted_slots",
     "fp4moe_route_workspace_size", "fp4moe_gemm_workspace_size", "fp4moe_workspace_size",
     "fp4moe_prepared_weight_size", "fp4moe_read_error", "fp4moe_clear_error",
     "fp4moe_prepare_weights", "moe_route_sort", "moe_route_sort_noalloc", "moe_permute", "moe_gemm1_swiglu", "moe_gemm2",
-    "moe_finalize", "fused_moe_forward", "fp4moe_debug_quantize_nvfp4",
+    "moe_finalize", "fused_moe_forward", "moe_combine", "fp4moe_debug_quantize_nvfp4",
     "fp4moe_debug_quantize_mxfp8", "fp4moe_debug_decode_prepared", "fp4moe_debug_wait_timeout",
     "fp4moe_domain_weight_size", "fp4moe_prepare_domain_weights",
     "fp4moe_localized_workspace_size", "fused_moe_forward_localized", "fp4moe_domains_create",
@@ -122,6 +122,7 @@ def lib() -> ctypes.CDLL:
             "moe_finalize": (i32, [P, vp, vp, vp, f32, i32, vp, vp]),
             "fused_moe_forward": (i32, [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, i32, i32, vp,
                                         vp, sz, vp]),
+            "moe_combine": (i32, [P, vp, i32, vp, vp]),
             "fp4moe_debug_quantize_nvfp4": (i32, [vp, i64, vp, vp, vp, vp]),
             "fp4moe_debug_quantize_mxfp8": (i32, [vp, i64, vp, vp, vp]),
             "fp4moe_debug_decode_prepared": (i32, [P, i32, vp, vp, vp]),
@@ -288,6 +289,11 @@ def fused_moe_forward(p: Problem, x, x_sf, token_selected_experts, token_final_s
                                    float(routed_scaling_factor), int(bool(accumulate)),
                                    int(finalize_mode), _p(out), _p(workspace), _nbytes(workspace),
                                    _stream(stream)), "fused_moe_forward")
+
+
+def moe_combine(p: Problem, partial, accumulate, out, stream=None):
+    _check(lib().moe_combine(ctypes.byref(p), _p(partial), int(bool(accumulate)), _p(out),
+                             _stream(stream)), "moe_combine")
 
 
 def debug_quantize_mxfp8(x, q, sf, stream=None):

@@ -474,7 +474,8 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   if (st != FP4MOE_OK) return st;
   const bool w4 = s.mode != FP4MOE_W4A16;   // packed activations
   const bool mx = s.mode == FP4MOE_W4A8;
-  if (finalize_mode != FP4MOE_FINALIZE_DETERMINISTIC && finalize_mode != FP4MOE_FINALIZE_ATOMIC)
+  if (finalize_mode != FP4MOE_FINALIZE_DETERMINISTIC && finalize_mode != FP4MOE_FINALIZE_ATOMIC &&
+      finalize_mode != FP4MOE_FINALIZE_PARTIAL_F32)
     return FP4MOE_ERR_INVALID_ARG;
   if (!ok_ptr(w1_prepared) || !ok_ptr(w1_alpha) || !ok_ptr(w2_prepared) || !ok_ptr(w2_alpha) ||
       !ok_ptr(workspace))
@@ -561,8 +562,19 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   if (e == cudaSuccess) e = launch_gemm(s, g2, cs, true);
   if (e == cudaSuccess)
     e = atomic ? launch_round_acc(s, acc, out, cs, true)
-               : launch_finalize(s, ws + L.y, e2p, wts, rsf, accumulate ? 1 : 0, out, cs, true);
+               : launch_finalize(s, ws + L.y, e2p, wts, rsf, accumulate ? 1 : 0, out, cs, true,
+                                 finalize_mode == FP4MOE_FINALIZE_PARTIAL_F32);
   return cuda_status(e);
+}
+
+fp4moe_status moe_combine(const fp4moe_problem* p, const float* partial, int32_t accumulate,
+                          void* out, void* stream) {
+  Shape s;
+  fp4moe_status st = validate(p, &s);
+  if (st != FP4MOE_OK) return st;
+  if (s.M > 0 && (!ok_ptr(partial) || !ok_ptr(out))) return FP4MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(s, partial, accumulate ? 1 : 0, out,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 size_t fp4moe_domain_weight_size(const fp4moe_problem* p, int32_t which) {

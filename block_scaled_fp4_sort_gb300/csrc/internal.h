@@ -108,8 +108,14 @@ cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, c
 // the sign moved into its 16 codes (the same values; the native MMA reads
 // scales unsigned).  p2e may be null: row s of x is row s (rows already in
 // slot order), for a canonical copy.
+// partial: out is an fp32 [M, H] expert-parallel partial sum (seeded with
+// itself when accumulate), not rounded
 cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, const float* w,
-                            float rsf, int accumulate, void* out, cudaStream_t st, bool pdl);
+                            float rsf, int accumulate, void* out, cudaStream_t st, bool pdl,
+                            bool partial = false);
+// expert-parallel combine: out bf16 [M, H] = bf16(partial + (accumulate ? out : +0))
+cudaError_t launch_combine(const Shape& s, const float* partial, int accumulate, void* out,
+                           cudaStream_t st);
 // atomic finalize: fp32 accumulator [M, H] seeded from out (or +0), rounded into out
 cudaError_t launch_seed_acc(const Shape& s, const void* out, int accumulate, float* acc,
                             cudaStream_t st, bool pdl);

@@ -1378,6 +1378,7 @@ __device__ __forceinline__ bool gv_epilogue(const GemmArgs& a, int32_t tau, int3
                                             int lane, uint32_t r0, uint32_t r1,
                                             const float (&d)[2][4], float* xchg, uint64_t* xready,
                                             uint64_t* xfree, uint32_t& xphase) {
+  constexpr int kNB = BN / 8;   // 8-column n-blocks of the route tile
   const int t = lane & 3;
   const int32_t mn = a.tile_mn[tau];
   const int64_t s0 = (int64_t)tau * BN;
@@ -1385,7 +1386,7 @@ __device__ __forceinline__ bool gv_epilogue(const GemmArgs& a, int32_t tau, int3
   if (EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal) {
     float* y = static_cast<float*>(a.out);  // fp32 route storage
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
+    for (int nb = 0; nb < kNB; ++nb) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int64_t feat = (int64_t)f * 256 + (i < 2 ? r0 : r1);
@@ -1402,7 +1403,7 @@ __device__ __forceinline__ bool gv_epilogue(const GemmArgs& a, int32_t tau, int3
   if (EPI == kEpiRelu2Bf16) {  // non-gated FC1: every row is an output
     __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
+    for (int nb = 0; nb < kNB; ++nb) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int64_t feat = (int64_t)f * 256 + (i < 2 ? r0 : r1);
@@ -1418,7 +1419,7 @@ __device__ __forceinline__ bool gv_epilogue(const GemmArgs& a, int32_t tau, int3
   if (w >= kGvWarps / 2) {
     if (!__all_sync(0xffffffffu, mbar_wait(xfree, xphase ^ 1u, a.err))) return false;
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
+    for (int nb = 0; nb < kNB; ++nb)
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         xchg[((i < 2 ? r0 : r1) - 128) * BN + 8 * nb + 2 * t + (i & 1)] = d[nb][i];
@@ -1428,7 +1429,7 @@ __device__ __forceinline__ bool gv_epilogue(const GemmArgs& a, int32_t tau, int3
     if (!__all_sync(0xffffffffu, mbar_wait(xready, xphase, a.err))) return false;
     __nv_bfloat16* h = static_cast<__nv_bfloat16*>(a.out);
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) {
+    for (int nb = 0; nb < kNB; ++nb) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t row = i < 2 ? r0 : r1;

@@ -129,17 +129,29 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
 
 // out[t] = bf16(seed + sum_j (rsf * w[t,j]) * y[e2p[t,j]]), fp32, route order;
 // y is the fp32 route storage GEMM2 writes.  One thread per 8 outputs.
+// Deterministic finalize of token row t (eight columns per thread):
+// out[t] = seed + sum_j (rsf * w[t,j]) * y[e2p[t,j]] in fp32, routes in order.
+// PARTIAL = 0: out is BF16, seed = float(out) or +0, one RNE rounding;
+// PARTIAL = 1: out is fp32 (an expert-parallel rank's partial sum), seed =
+// out itself or +0, no rounding.
+template <int PARTIAL>
 __global__ void finalize_rows(const float4* __restrict__ y, const int32_t* __restrict__ e2p,
                               const float* __restrict__ w, float rsf, int accumulate,
-                              uint4* __restrict__ out, int64_t M, int64_t H8, int top_k,
+                              void* __restrict__ outp, int64_t M, int64_t H8, int top_k,
                               int64_t S) {
   grid_dependency_wait();
   const int64_t n = M * H8;
+  uint4* out = static_cast<uint4*>(outp);
+  float4* outf = static_cast<float4*>(outp);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = i / H8, c = i % H8;
     float acc[8];
-    if (accumulate) {
+    if (accumulate && PARTIAL) {
+      const float4 a = outf[2 * i], b = outf[2 * i + 1];
+      acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+      acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+    } else if (accumulate) {
       bf16x8_to_f32(out[i], acc);
     } else {
 #pragma unroll
@@ -154,7 +166,36 @@ __global__ void finalize_rows(const float4* __restrict__ y, const int32_t* __res
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[k] = fmaf(wk, yv[k], acc[k]);
     }
-    out[i] = f32_to_bf16x8(acc);
+    if (PARTIAL) {
+      outf[2 * i] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      outf[2 * i + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+      out[i] = f32_to_bf16x8(acc);
+    }
+  }
+  launch_dependents();
+}
+
+// Expert-parallel combine: out = bf16(partial + seed), seed = float(out)
+// (accumulate) or +0, one RNE rounding; partial is the sum over the ranks
+// of their fp32 partial outputs.
+__global__ void combine_rows(const float4* __restrict__ partial, int accumulate,
+                             uint4* __restrict__ out, int64_t n8) {
+  grid_dependency_wait();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float v[8];
+    if (accumulate) {
+      bf16x8_to_f32(out[i], v);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+    }
+    const float4 a = partial[2 * i], b = partial[2 * i + 1];
+    const float p[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] += p[k];
+    out[i] = f32_to_bf16x8(v);
   }
   launch_dependents();
 }
@@ -304,13 +345,26 @@ cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, c
 }
 
 cudaError_t launch_finalize(const Shape& s, const void* y, const int32_t* e2p, const float* w,
-                            float rsf, int accumulate, void* out, cudaStream_t st, bool pdl) {
+                            float rsf, int accumulate, void* out, cudaStream_t st, bool pdl,
+                            bool partial) {
   if (s.M == 0) return cudaSuccess;
   const int64_t n = s.M * (s.H / 8);
   const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 16);
-  return launch_pdl(finalize_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
-                    static_cast<const float4*>(y), e2p, w, rsf, accumulate,
-                    static_cast<uint4*>(out), s.M, s.H / 8, (int)s.K, s.S);
+  return partial ? launch_pdl(finalize_rows<1>, dim3((unsigned)blocks), dim3(256), st, pdl,
+                              static_cast<const float4*>(y), e2p, w, rsf, accumulate, out, s.M,
+                              s.H / 8, (int)s.K, s.S)
+                 : launch_pdl(finalize_rows<0>, dim3((unsigned)blocks), dim3(256), st, pdl,
+                              static_cast<const float4*>(y), e2p, w, rsf, accumulate, out, s.M,
+                              s.H / 8, (int)s.K, s.S);
+}
+
+cudaError_t launch_combine(const Shape& s, const float* partial, int accumulate, void* out,
+                           cudaStream_t st) {
+  const int64_t n8 = s.M * (s.H / 8);
+  if (n8 == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, (int64_t)num_sms() * 16);
+  return launch_pdl(combine_rows, dim3((unsigned)blocks), dim3(256), st, false,
+                    reinterpret_cast<const float4*>(partial), accumulate, static_cast<uint4*>(out), n8);
 }
 
 cudaError_t launch_seed_acc(const Shape& s, const void* out, int accumulate, float* acc,

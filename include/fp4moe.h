@@ -80,7 +80,10 @@ typedef enum { FP4MOE_W4A16 = 0, FP4MOE_W4A4 = 1, FP4MOE_W4A8 = 2 } fp4moe_quant
 
 typedef enum {
   FP4MOE_FINALIZE_DETERMINISTIC = 0,   /* GEMM2 writes y; a second pass sums in route order */
-  FP4MOE_FINALIZE_ATOMIC = 1           /* GEMM2's epilogue adds rsf*w*y into out atomically */
+  FP4MOE_FINALIZE_ATOMIC = 1,          /* GEMM2's epilogue adds rsf*w*y into out atomically */
+  FP4MOE_FINALIZE_PARTIAL_F32 = 2      /* as DETERMINISTIC, but out is an fp32 [M, H] partial
+                                          sum, not rounded (one expert-parallel rank's share;
+                                          see moe_combine) */
 } fp4moe_finalize_mode;
 
 /* FC1 activation (cute_dsl_fused_moe: activation_type, swiglu_alpha /
@@ -320,6 +323,20 @@ FP4MOE_API fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y,
                            const float* token_final_scales, float routed_scaling_factor,
                            int32_t accumulate, void* out, void* stream);
 
+/* Expert-parallel combine (cute_dsl_fused_moe num_local_experts /
+ * local_expert_offset; cutlass_fused_moe ep_size / ep_rank).  With the
+ * experts split over ranks, each rank runs fused_moe_forward on its local
+ * experts with FP4MOE_FINALIZE_PARTIAL_F32 into an fp32 [M, H] partial (its
+ * routes' terms in route order, seeded with +0); the ranks sum the partials
+ * (one all-reduce) and this call rounds the sum into the BF16 output:
+ *   out[t] = bf16( seed_t + partial[t] ),  seed_t = float(out[t]) if
+ *   accumulate else +0.0f, one RNE rounding.
+ * The terms equal those of the single-GPU finalize; only the fp32 summation
+ * order differs (per rank, then across ranks).
+ * partial: fp32 [M, H]; out: bf16 [M, H]. */
+FP4MOE_API fp4moe_status moe_combine(const fp4moe_problem* p, const float* partial,
+                                     int32_t accumulate, void* out, void* stream);
+
 /* The whole forward on `stream`: route sort, x gathered into slot order in the
  * workspace (NVFP4 for the FP4 MMA path; w4a8 rows and decode-size w4a4 rows
  * expanded to BF16 on the way; padding rows unwritten),
@@ -333,6 +350,9 @@ FP4MOE_API fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y,
  *     (rsf * w[t,j]) * y term into it with fp32 atomic adds, and a last pass
  *     rounds it into out (RNE).  The terms are those of the deterministic
  *     path; only their summation order varies from run to run.
+ *   FP4MOE_FINALIZE_PARTIAL_F32: out is fp32 [M, H]; the deterministic sum
+ *     is stored unrounded, seeded with out itself (accumulate = 1) or +0
+ *     (one expert-parallel rank's partial, see moe_combine).
  * per_token_scale: fp32 [M] or NULL, as in moe_gemm1_swiglu.
  * workspace: fp4moe_workspace_size(p) bytes. */
 FP4MOE_API fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const uint8_t* x_sf,

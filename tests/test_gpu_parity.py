@@ -620,6 +620,40 @@ def test_expert_parallel_halves_sum_to_full():
     check_out(f64(out), exact, 5e-3, what="EP halves")
 
 
+@pytest.mark.parametrize("world,T", [(2, 16), (3, 32), (2, 256)])
+def test_expert_parallel_partials_combine(world, T):
+    # the expert-parallel path on one GPU: each rank's fp32 partial (its
+    # experts only), their sum (the all-reduce, here a plain add) and the
+    # combine into BF16 meet the oracle's bar, and stay within one BF16 ulp of
+    # the single-GPU deterministic forward almost everywhere (same terms,
+    # another fp32 summation order)
+    from block_scaled_fp4_sort_gb300.ep import ExpertParallelMoE
+    cfg = synth.CONFIGS["tiny_w4a16"]
+    inp = synth.generate(cfg, device="cuda")
+    ids = inp.token_selected_experts.cuda()
+    w = inp.token_final_scales.cuda()
+    p_full = problem_for(cfg, T)
+    total = torch.zeros(cfg.M, cfg.H, dtype=torch.float32, device="cuda")
+    for r in range(world):
+        rank = ExpertParallelMoE(p_full, world, r).prepare(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+        total += rank.local_partial(inp.x, None, ids, w, inp.w1_alpha, inp.w2_alpha, rsf=0.5)
+    out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device="cuda")
+    rank.combine(total, out)
+    torch.cuda.synchronize()
+    _, exact, _ = oracle.OracleMoE.from_inputs(inp).forward(rsf=0.5)
+    check_out(f64(out), exact, 5e-3, what="EP world=%d T=%d" % (world, T))
+    inp_T, p, B, _ = _setup(cfg, T)
+    d = f64(_fused(inp, B, rsf=0.5))
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(d), 1e-30))) - 7)
+    assert (np.abs(f64(out) - d) <= ulp).mean() > 0.99
+    # combine with accumulate adds the existing output once more
+    out2 = out.clone()
+    rank.combine(total, out2, accumulate=True)
+    torch.cuda.synchronize()
+    want = (torch.from_numpy(f64(out)).float() + total.cpu()).to(torch.bfloat16)
+    assert np.array_equal(bits(out2), want.view(torch.int16).numpy().view(np.uint16))
+
+
 def test_prefill_w4a4_sampled():
     cfg = synth.CONFIGS["prefill_w4a4"]
     inp, p, B, orc = _setup(cfg)
