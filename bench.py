@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--no-localized", action="store_true",
                     help="skip the two-domain timing (ncu cannot profile kernels launched into "
                          "green contexts)")
+    ap.add_argument("--parallel", default="replicas", choices=["replicas", "ep"],
+                    help="N > 1: independent replicas per rank (weak scaling), or one batch with "
+                         "the experts split over the ranks and one all-reduce (strong scaling)")
     ap.add_argument("--locality", action="store_true",
                     help="print the GEMM1 gather-locality measurement instead of the bench line")
     return ap.parse_args()
@@ -373,31 +376,73 @@ def measure(cfg, args, rank, world, local, dev, headline):
         kernels[n] = statistics.mean(a.elapsed_time(b) for a, b in ev[n])
     del px, pxsf, h, hsf, y
 
-    # ---------------- end to end through host buffers
+    # ---------------- end to end through host buffers.  Every step copies its
+    # inputs from pinned host memory and its output back; the copies run on
+    # their own streams, double-buffered, so that step i's inputs travel while
+    # step i-1 computes (the way a serving loop feeds the library)
     pin = lambda t: t.detach().cpu().pin_memory()
     hx = pin(x)
     hxsf = pin(inp.x_sf) if inp.x_sf is not None else None
     hids = pin(inp.token_selected_experts)
     hw = pin(inp.token_final_scales)
-    hout = torch.empty(cfg.M, cfg.H, dtype=torch.bfloat16).pin_memory()
-    dx = torch.empty_like(x)
-    dxsf = torch.empty_like(inp.x_sf) if inp.x_sf is not None else None
-    dids = torch.empty_like(ids)
-    dw = torch.empty_like(wts)
-
-    def e2e_step():
-        dx.copy_(hx, non_blocking=True)
-        if dxsf is not None:
-            dxsf.copy_(hxsf, non_blocking=True)
-        dids.copy_(hids, non_blocking=True)
-        dw.copy_(hw, non_blocking=True)
-        B.forward(dx, dxsf, dids, dw, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale,
-                  stream=stream)
-        hout.copy_(out, non_blocking=True)
-    e2e_ms, _ = timed(e2e_step)
+    houts = [torch.empty(cfg.M, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dev_in = [dict(x=torch.empty_like(x), ids=torch.empty_like(ids), w=torch.empty_like(wts),
+                   xsf=torch.empty_like(inp.x_sf) if inp.x_sf is not None else None)
+              for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_ready, done, out_back = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hw) + ((hxsf,) if hxsf is not None else ()))
-    d2h = hout.numel() * hout.element_size()
-    del dx, dxsf, dids, dw, hx, hxsf, hout
+    d2h = houts[0].numel() * houts[0].element_size()
+
+    def e2e_run(n):
+        # step i uses buffer set b = i % 2; its copy-in waits for step i-2's
+        # compute (same inputs buffer), its compute for its copy-in and for
+        # step i-2's copy-out (same output buffer)
+        for i in range(n):
+            b = i % 2
+            d = dev_in[b]
+            with torch.cuda.stream(h2d_s):
+                if i >= 2:
+                    h2d_s.wait_event(done[b])
+                d["x"].copy_(hx, non_blocking=True)
+                if d["xsf"] is not None:
+                    d["xsf"].copy_(hxsf, non_blocking=True)
+                d["ids"].copy_(hids, non_blocking=True)
+                d["w"].copy_(hw, non_blocking=True)
+                in_ready[b].record(h2d_s)
+            stream.wait_event(in_ready[b])
+            if i >= 2:
+                stream.wait_event(out_back[b])
+            B.forward(d["x"], d["xsf"], d["ids"], d["w"], inp.w1_alpha, inp.w2_alpha, outs[b],
+                      inp.fc2_input_scale, stream=stream)
+            done[b].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(done[b])
+                houts[b].copy_(outs[b], non_blocking=True)
+                out_back[b].record(d2h_s)
+        stream.wait_event(out_back[(n - 1) % 2])
+        if n >= 2:
+            stream.wait_event(out_back[(n - 2) % 2])
+
+    e2e_run(max(args.warmup, 3))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    h2d_s.wait_stream(stream)
+    e2e_run(args.steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    if world > 1:
+        torch.distributed.barrier()
+    # the pipelined outputs are the forward's outputs
+    if not torch.equal(outs[(args.steps - 1) % 2].view(torch.int16).cpu(),
+                       houts[(args.steps - 1) % 2].view(torch.int16)):
+        raise RuntimeError("end-to-end output copy mismatch")
+    del dev_in, outs, hx, hxsf, houts
 
     # ---------------- roofline of the dominant kernel (GEMM1)
     peaks, peak_src = load_peaks()
@@ -474,7 +519,10 @@ def measure(cfg, args, rank, world, local, dev, headline):
                             "unit": UNIT},
         "localized": localized,
         "e2e": {"value": tokens_per_s(world, cfg.M, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": "pinned host buffers; every step copies its inputs in and its output "
+                          "back on two copy streams, double-buffered so that step i's copies "
+                          "overlap step i-1's compute"},
         "clocks": clocks,
         # per fused step: routing (1 kernel up to 4096 routes, else 3), x in slot
         # order, GEMM1, the w4a8 / decode-size w4a4 h -> BF16 expansion, GEMM2, finalize
@@ -637,6 +685,92 @@ def run_locality(args):
     print(json.dumps(res))
 
 
+def run_ep(args, rank, world, local):
+    """Expert parallelism: every rank holds the same batch, owns a contiguous
+    range of the experts, computes its fp32 partial output and joins one
+    all-reduce (NCCL); moe_combine rounds the sum.  The whole job processes
+    one batch: strong scaling."""
+    import torch
+
+    import synth
+    from block_scaled_fp4_sort_gb300 import build as fbuild
+    from block_scaled_fp4_sort_gb300.buffers import problem_for
+    from block_scaled_fp4_sort_gb300.ep import ExpertParallelMoE, expert_range
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        fbuild.build()
+    torch.distributed.barrier()
+    fbuild.build()
+    cfg = synth.CONFIGS[args.workload]
+    T = args.route_tile or synth.route_tile_for(cfg)
+    inp = synth.generate(cfg, device=dev)          # the same seed on every rank
+    epm = ExpertParallelMoE(problem_for(cfg, T), world, rank, dev).prepare(
+        inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+    ids = inp.token_selected_experts.to(dev)
+    wts = inp.token_final_scales.to(dev)
+    x = inp.x if inp.x is not None else inp.x_q
+    out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(xx=x, ii=ids, ww=wts):
+        epm.forward(xx, inp.x_sf, ii, ww, inp.w1_alpha, inp.w2_alpha, out, inp.fc2_input_scale,
+                    stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, clocks=False):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        torch.distributed.barrier()
+        clk = ClockSampler(local) if clocks else None
+        if clk:
+            clk.__enter__()
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if clk:
+            clk.__exit__(None, None, None)
+        ms_ = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+        torch.distributed.barrier()
+        return ms_, (clk.summary() if clk else None)
+    ms, clocks = timed(step, clocks=True)
+    hx = x.detach().cpu().pin_memory()
+    hids = inp.token_selected_experts.pin_memory()
+    hw = inp.token_final_scales.pin_memory()
+    hout = torch.empty(cfg.M, cfg.H, dtype=torch.bfloat16).pin_memory()
+    dx, dids, dw = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(wts)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dids.copy_(hids, non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        step(dx, dids, dw)
+        hout.copy_(out, non_blocking=True)
+    e2e_ms, _ = timed(e2e_step)
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hids, hw))
+    line = {
+        "metric": METRIC, "value": cfg.M / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+        "dtype": "bf16" if cfg.mode == "w4a16" else cfg.mode,
+        "data": "synthetic (seeded generator; random NVFP4 weights)",
+        "config": dict(workload_config(cfg, T), parallelism="ep%d" % world,
+                       experts_per_rank=[expert_range(cfg.E, world, r)[1] for r in range(world)],
+                       l2="inputs larger than L2"),
+        "tflops": cfg.flops() / (ms * 1e-3) / 1e12,
+        "e2e": {"value": cfg.M / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * 2},
+        "clocks": clocks,
+        "collective": "one NCCL all-reduce (sum) of the fp32 [M, H] partial per step",
+        "gpu_launches": args.steps * (3 + 1 + 3 + 1),
+    }
+    return line
+
+
 def run_reference(args, world):
     """The reference arm: the CPU oracle, as it stands, on the host cores, over
     bounded samples of the headline workload (each step a different slice of
@@ -699,7 +833,10 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
-    line = run_ours(args, rank, world, local)
+    if args.parallel == "ep" and world > 1:
+        line = run_ep(args, rank, world, local)
+    else:
+        line = run_ours(args, rank, world, local)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -64,13 +64,14 @@ class ExpertParallelMoE:
         """Prepare this rank's experts from the full weight tensors [E, ...]."""
         if self.count:
             sl = slice(self.offset, self.offset + self.count)
-            self.buffers.prepare(w1[sl].contiguous(), w1_sf[sl].contiguous(),
-                                 w2[sl].contiguous(), w2_sf[sl].contiguous())
+            self.buffers.prepare(w1[sl].clone(), w1_sf[sl].clone(), w2[sl].clone(),
+                                 w2_sf[sl].clone())
         return self
 
     def local_alphas(self, w1_alpha, w2_alpha):
+        # copies: a slice of the [E] tensors may start off a 16-byte boundary
         sl = slice(self.offset, self.offset + self.count)
-        return w1_alpha[sl].contiguous(), w2_alpha[sl].contiguous()
+        return w1_alpha[sl].clone(), w2_alpha[sl].clone()
 
     def local_partial(self, x, x_sf, ids, token_final_scales, w1_alpha, w2_alpha,
                       fc2_input_scale=None, rsf=1.0, stream=None, per_token_scale=None):
