@@ -55,10 +55,12 @@ inline int64_t k_chunks(const Shape& s, int which) { return which == 1 ? s.H / k
 // layouts have the same block size and the same scale region.
 inline bool fragment_layout(const Shape& s) { return s.mode == 0 && s.T <= 16; }
 
-// BF16 activations with route tiles of 32..256 slots run on the one-tile
-// tcgen05 kernel: work items of one 128-row weight tile (half of a prepared
-// 256-row block; a gated GEMM1 tile holds 64 gate rows and their 64 up rows).
-inline bool one_tile(const Shape& s) { return s.mode == 0 && s.T >= 32; }
+// BF16 activations with route tiles of 256 slots run on the one-tile tcgen05
+// kernel: work items of one 128-row weight tile (half of a prepared 256-row
+// block; a gated GEMM1 tile holds 64 gate rows and their 64 up rows).  Route
+// tiles 32..128 keep the two-tile kernel, whose items share each activation
+// tile between 256 weight rows (half the activation bytes per flop).
+inline bool one_tile(const Shape& s) { return s.mode == 0 && s.T == 256; }
 inline int64_t one_tile_blocks(const Shape& s, int which) {
   if (which == 1) return gated(s) ? s.I / 64 : (s.I + 127) / 128;
   return (s.H + 127) / 128;
