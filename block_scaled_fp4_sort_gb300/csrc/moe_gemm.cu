@@ -881,6 +881,316 @@ __global__ void __launch_bounds__(kTThreads, 1)
 }
 
 // ===========================================================================
+// CTA-pair BF16-decode grouped GEMM (w4a16, route tile 256).
+//
+// The one-tile kernel's items, computed by two CTAs of a cluster together:
+// the pair takes one prepared 256-row weight block (CTA r decodes its half,
+// rows of one-tile tile 2p + r, into its own TMEM) and one route tile of up
+// to 256 slots, and rank 0 issues tcgen05.mma.cta_group::2 with M = 256:
+// each CTA's TMEM receives the accumulators of its own 128 weight rows over
+// all N slots, while each CTA loads only half of the N activation rows (the
+// MMA reads the other half from the peer's shared memory).  Per CTA and
+// 128-element chunk the shared-memory traffic is 9 KB of weights and N/2
+// activation rows, against N rows for the one-tile kernel: the activation
+// bytes, not the MMA, bound the wide single-CTA tiles.
+// Synchronisation: every CTA's producer and decoders wait on their own
+// barriers; the decoders of both CTAs arrive on rank 0's A-stage barriers and
+// the epilogue warps of both on rank 0's accumulator-free barriers (remote
+// arrivals, release at cluster scope); rank 0's commits arrive on the stage
+// and accumulator barriers of both CTAs (multicast).  N is the tile's valid
+// slot count rounded up to 32 (16 activation rows per CTA and copy).
+// ===========================================================================
+constexpr int kPBox = 16;   // activation rows per tensor copy (per CTA: N / 2 rows)
+
+template <int BN>
+struct PCfg {
+  static constexpr int kBBytes = BN * 128;                 // two K atoms of BN / 2 rows
+  static constexpr int kStage = kTWBytes + kBBytes;
+  static constexpr int kStagesRaw = (222 * 1024) / kStage;
+  static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
+  static constexpr int kAStages = kStages < 4 ? kStages : 4;
+  static constexpr int kNBuf = BN <= 128 ? 2 : 1;
+  static constexpr int kABase = 256;
+  static constexpr int kCols = BN / 4 >= 16 ? BN / 4 : 16;
+  static constexpr int kGroups = BN / kCols;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes;
+  static_assert(kStage % 1024 == 0, "stage alignment");
+  static_assert(kStages >= 2 && kStages >= kAStages, "pipeline depth");
+  static_assert(kABase + kAStages * 64 <= 512, "tensor memory");
+  static_assert(kNBuf * BN <= kABase, "accumulators");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+};
+
+// the pair's MMA width for route tile tau: valid slots rounded up to 32, in [32, BN]
+template <int BN>
+__device__ __forceinline__ uint32_t pair_n(const GemmArgs& a, int32_t tau) {
+  return (uint32_t)(tile_valid<BN>(a, tau) + 31) & ~31u;
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kTThreads, 1)
+    moe_gemm_2sm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap) {
+  using C = PCfg<BN>;
+  constexpr bool kGated = EPI == kEpiSwigluBf16;
+  constexpr bool kEarly = C::kNBuf == 2 || EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* afull = empty + C::kStages;      // rank 0's: both CTAs' decoders
+  uint64_t* accfull = afull + C::kAStages;   // [2]
+  uint64_t* accempty = accfull + 2;          // [2] rank 0's: both CTAs' epilogue warps
+  uint64_t* drain = accempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();   // 0 or 1
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < C::kAStages; ++i) mbar_init(&afull[i], 2 * kTDecWarps);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], 2 * kTEpiWarps);
+    }
+    mbar_init(drain, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == kTMmaWarp) {
+    tmem_alloc2(tmem_slot, kTmemCols);
+    tmem_relinquish2();
+  }
+  if (warp == kTTmaWarp && lane == 0) prefetch_tensormap(&bmap);
+  tc_fence_before();
+  cluster_sync();   // barriers initialised and TMEM allocated in both CTAs
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  grid_dependency_wait();
+  const int64_t n_items = plan_items(a);
+  const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+  if (warp == kTTmaWarp) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    int stage = 0;
+    uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
+    bool ok = true;
+    for (int64_t item = cid; item < n_items && ok; item += ncl) {
+      const int32_t tau = (int32_t)(item / a.F), pb = (int32_t)(item % a.F);
+      const int32_t e = plan_expert(a, tau);
+      const uint32_t half_rows = pair_n<BN>(a, tau) / 2;          // this CTA's activation rows
+      const uint32_t nbox = half_rows / kPBox;
+      const uint32_t tx = (uint32_t)kTWBytes + 2u * half_rows * 128u;
+      const int hf = (int)rank;
+      const uint8_t* wsrc = a.wprep + ((int64_t)e * a.FB + pb) * a.C * (int64_t)kWBlockBytes;
+      for (int c = 0; c < a.C; ++c) {
+        if (lane == 0) {
+          ok = mbar_wait_cluster(&empty[stage], phase ^ 1u, a.err);
+          if (ok) {
+            uint8_t* sw = stages + stage * C::kStage;
+            uint8_t* sb = sw + kTWBytes;
+            const uint8_t* blk = wsrc + (int64_t)c * kWBlockBytes;
+            mbar_arrive_expect_tx(&full[stage], tx);
+            if (kGated) {
+              tma_load_1d(sw, blk + hf * 4096, 4096, &full[stage]);
+              tma_load_1d(sw + 4096, blk + 8192 + hf * 4096, 4096, &full[stage]);
+              tma_load_1d(sw + kTWCodes, blk + kWDataBytes + hf * 512, 512, &full[stage]);
+              tma_load_1d(sw + kTWCodes + 512, blk + kWDataBytes + 1024 + hf * 512, 512, &full[stage]);
+            } else {
+              tma_load_1d(sw, blk + hf * kTWCodes, kTWCodes, &full[stage]);
+              tma_load_1d(sw + kTWCodes, blk + kWDataBytes + hf * 1024, 1024, &full[stage]);
+            }
+#pragma unroll
+            for (int at = 0; at < 2; ++at)
+              for (uint32_t b = 0; b < nbox; ++b)
+                tma_load_2d(sb + at * (BN / 2) * 128 + b * kPBox * 128, &bmap, c * kBK + at * 64,
+                            tau * BN + (int32_t)(rank * half_rows + b * kPBox), &full[stage]);
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (lane == 0)
+      for (int q = 0; q < C::kStages; ++q)
+        if (issued_mask & (1u << q)) mbar_wait(&full[q], (issued_parity >> q) & 1u, a.err);
+  } else if (warp == kTMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    if (rank == 0 && lane == 0) {
+      int stage = 0, astage = 0;
+      uint32_t phase = 0, aphase = 0, k = 0;
+      bool ok = true;
+      for (int64_t item = cid; item < n_items && ok; item += ncl, ++k) {
+        const uint32_t buf = C::kNBuf == 2 ? (k & 1u) : 0u;
+        if (k >= (uint32_t)C::kNBuf &&
+            !mbar_wait_cluster(&accempty[buf], (k / C::kNBuf - 1) & 1u, a.err))
+          break;
+        const int32_t tau = (int32_t)(item / a.F);
+        const uint32_t idesc = idesc_bf16_f32(256, (int)pair_n<BN>(a, tau));
+        const uint32_t d = tmem + buf * (uint32_t)BN;
+        for (int c = 0; c < a.C; ++c) {
+          // both CTAs' decoders have stored this chunk's A (after their own
+          // copies, activation halves included, had landed)
+          if (!mbar_wait_cluster(&afull[astage], aphase, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sb = smem_u32(stages + stage * C::kStage + kTWBytes);
+          const uint32_t abase = tmem + (uint32_t)(C::kABase + astage * 64);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bd = smem_desc_sw128(sb + (kk >> 2) * (BN / 2) * 128 + (kk & 3) * 32);
+            mma2_bf16_ts(d, abase + kk * 8, bd, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit2(&empty[stage], 0x3);   // frees the stage and A stage of both CTAs
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++astage == C::kAStages) {
+            astage = 0;
+            aphase ^= 1u;
+          }
+        }
+        if (ok) tc_commit2(&accfull[buf], 0x3);
+      }
+      tc_commit2(drain, 0x1);
+      mbar_wait(drain, 0, a.err);
+    }
+  } else if (warp < kTDecWarps) {
+    // ------------------------------------------------------------ decode (both CTAs)
+    const int q = warp;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const int rloc = kGated ? 16 * q + (lane & 15) : 32 * q + lane;
+    const int code_base = kGated && lane >= 16 ? 4096 : 0;
+    const int sf_off = kTWCodes + (kGated && lane >= 16 ? 512 : 0) + rloc * 8;
+    int stage = 0, astage = 0;
+    uint32_t phase = 0, qd = 0;
+    bool ok = true;
+    for (int64_t item = cid; item < n_items && ok; item += ncl) {
+      for (int c = 0; c < a.C; ++c) {
+        bool good = mbar_wait(&full[stage], phase, a.err);
+        if (qd >= (uint32_t)C::kAStages) {
+          const uint32_t qp = qd - (uint32_t)C::kAStages;
+          good = good && mbar_wait_cluster(&empty[qp % C::kStages], (qp / C::kStages) & 1u, a.err);
+        }
+        ++qd;
+        if (!__all_sync(0xffffffffu, good)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t* blk = stages + stage * C::kStage;
+        const uint2 sv = *reinterpret_cast<const uint2*>(blk + sf_off);
+        const uint32_t acol = tmem + lane_base + (uint32_t)(C::kABase + astage * 64);
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          const uint4 d4 = *reinterpret_cast<const uint4*>(blk + code_base + prep_chunk_offset(rloc, qq));
+          const uint32_t sp = (qq < 2 ? sv.x : sv.y) >> (16 * (qq & 1));
+          const uint32_t sa = scale_code_bf16x2(sp & 0xFFu), sb = scale_code_bf16x2((sp >> 8) & 0xFFu);
+          uint32_t o[16];
+          decode_word(d4.x, sa, o);
+          decode_word(d4.y, sa, o + 4);
+          decode_word(d4.z, sb, o + 8);
+          decode_word(d4.w, sb, o + 12);
+          tmem_st16(acol + 16 * qq, o);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(&afull[astage], 0));
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++astage == C::kAStages) astage = 0;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int et = threadIdx.x - 32 * kTDecWarps;
+    const int grp = et >> 7, q = warp & 3, r = 32 * q + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+    const int c0 = grp * C::kCols;
+    const uint32_t accempty0 = mapa_shared(accempty, 0);   // rank 0's barriers
+    uint32_t k = 0;
+    ItemPlan next = {0, 0};
+    float alpha_next = 0.0f;
+    if (cid < n_items) {
+      next = load_item_plan(a, cid);
+      alpha_next = item_alpha(a, next);
+    }
+    for (int64_t item = cid; item < n_items; item += ncl, ++k) {
+      const int32_t tau = (int32_t)(item / a.F);
+      const int32_t f = (int32_t)(item % a.F) * 2 + (int32_t)rank;   // one-tile weight tile
+      const uint32_t buf = C::kNBuf == 2 ? (k & 1u) : 0u;
+      const ItemPlan cur = next;
+      const float scale = alpha_next * 256.0f;   // undoes the decode's 2^-8
+      const bool more = item + ncl < n_items;
+      if (more) next = load_item_plan(a, item + ncl);
+      const int64_t s0 = (int64_t)tau * BN;
+      int32_t nv = cur.mn - tau * BN;
+      nv = nv < 0 ? 0 : nv > BN ? BN : nv;
+      const int nch = grp < C::kGroups ? (min(max(nv - c0, 0), C::kCols) + 15) >> 4 : 0;
+      if (!__all_sync(0xffffffffu, mbar_wait_cluster(&accfull[buf], (k / C::kNBuf) & 1u, a.err)))
+        break;
+      tc_fence_after();
+      const uint32_t acc = tmem + lane_base + buf * (uint32_t)BN + (uint32_t)c0;
+      const uint32_t release = accempty0 + buf * 8u;
+      if (kEarly) {
+        uint32_t v[C::kCols];
+#pragma unroll
+        for (int j = 0; j < C::kCols / 16; ++j)
+          if (j < nch) tmem_ld16p(acc + 16 * j, v + 16 * j);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(release);
+#pragma unroll
+        for (int j = 0; j < C::kCols / 16; ++j) {
+          if (j >= nch) break;
+          t_epilogue_chunk<EPI>(a, v + 16 * j, s0 + c0 + 16 * j, cur.mn, f, q, r, lane, scale);
+        }
+      } else {
+#pragma unroll 1
+        for (int j = 0; j < nch; ++j) {
+          uint32_t v[16];
+          tmem_ld16p(acc + 16 * j, v);
+          tmem_wait_ld();
+          t_epilogue_chunk<EPI>(a, v, s0 + c0 + 16 * j, cur.mn, f, q, r, lane, scale);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(release);
+      }
+      if (more) alpha_next = item_alpha(a, next);
+    }
+  }
+
+  __syncthreads();
+  launch_dependents();
+  tc_fence_before();
+  cluster_sync();   // neither CTA leaves while its peer may still reach its memory
+  tc_fence_after();
+  if (warp == kTMmaWarp) {
+    __syncwarp();
+    tmem_dealloc2(tmem, kTmemCols);
+  }
+}
+
+// ===========================================================================
 // Native NVFP4 grouped GEMM (w4a4): tcgen05.mma.kind::mxf4nvf4.block_scale.
 //
 // What is computed is the same as above, without the BF16 decode: the tensor
@@ -1892,6 +2202,80 @@ cudaError_t launch_1t_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, b
 }
 
 template <int BN, int EPI>
+cudaError_t launch_2sm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  using Cf = PCfg<BN>;
+  if (g.gather_rows != nullptr) return cudaErrorInvalidValue;   // reads x in slot order
+  GemmArgs a = {};
+  a.wprep = g.wprep;
+  a.alpha = g.alpha;
+  a.tile_expert = g.tile_expert;
+  a.tile_mn = g.tile_mn;
+  a.num_tiles = g.num_tiles;
+  a.top_k = (int32_t)s.K;
+  a.FB = (int32_t)row_blocks(s, g.which);
+  a.F = a.FB;                       // a pair's item: one prepared 256-row block
+  a.C = (int32_t)k_chunks(s, g.which);
+  a.out_ld = g.out_ld > 0 ? g.out_ld : (g.which == 1 ? s.I : s.H);
+  a.valid_rows = (int32_t)(g.which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H);
+  a.act = s.act;
+  a.token_scale = g.token_scale;
+  a.out = g.out;
+  a.max_tiles = (int32_t)s.tiles;
+  a.EL = (int32_t)s.EL;
+  a.R = s.R;
+  a.p2e = g.p2e;
+  a.route_w = g.route_w;
+  a.rsf = g.rsf;
+  a.err = g.err;
+  const int64_t Kdim = g.which == 1 ? s.H : s.I;
+  CUtensorMap map;
+  if (!make_act_map(&map, g.act, g.act_rows, Kdim, kPBox)) return cudaErrorInvalidValue;
+  auto kern = moe_gemm_2sm_kernel<BN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kTThreads);
+  cfg.dynamicSmemBytes = Cf::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  // persistent grid: as many CTA pairs as can be resident at once (at most
+  // one pair per two SMs of the device or of the caller's partition)
+  static int max_pairs = 0;
+  if (max_pairs == 0) {
+    cfg.gridDim = dim3(2 * (unsigned)(sm_count() / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = sm_count() / 2;
+    }
+    max_pairs = n;
+  }
+  const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
+  const int64_t pairs = std::min<int64_t>({(int64_t)max_pairs, grid_ctas(g) / 2, max_items});
+  cfg.gridDim = dim3(2 * (unsigned)std::max<int64_t>(pairs, 1));
+  return cudaLaunchKernelEx(&cfg, kern, a, map);
+}
+
+template <int BN>
+cudaError_t launch_2sm_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  switch (g.epi) {
+    case kEpiSwigluBf16: return launch_2sm<BN, kEpiSwigluBf16>(s, g, st, pdl);
+    case kEpiPlainBf16: return launch_2sm<BN, kEpiPlainBf16>(s, g, st, pdl);
+    case kEpiAtomicFinal: return launch_2sm<BN, kEpiAtomicFinal>(s, g, st, pdl);
+    case kEpiRelu2Bf16: return launch_2sm<BN, kEpiRelu2Bf16>(s, g, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int BN, int EPI>
 cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
   GemmArgs a = {};
   a.wprep = g.wprep;
@@ -1967,15 +2351,7 @@ cudaError_t launch_gemm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bo
       default: return cudaErrorInvalidValue;
     }
   }
-  if (one_tile(s)) {
-    switch (s.T) {
-      case 32: return launch_1t_bn<32>(s, g, st, pdl);
-      case 64: return launch_1t_bn<64>(s, g, st, pdl);
-      case 128: return launch_1t_bn<128>(s, g, st, pdl);
-      case 256: return launch_1t_bn<256>(s, g, st, pdl);
-      default: return cudaErrorInvalidValue;
-    }
-  }
+  if (one_tile(s)) return s.T == 256 ? launch_2sm_bn<256>(s, g, st, pdl) : cudaErrorInvalidValue;
   switch (s.T) {
     case 16: return launch_bn<16>(s, g, st, pdl);
     case 32: return launch_bn<32>(s, g, st, pdl);
