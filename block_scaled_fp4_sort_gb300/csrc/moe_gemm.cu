@@ -901,6 +901,11 @@ __global__ void __launch_bounds__(kTThreads, 1)
 // slot count rounded up to 32 (16 activation rows per CTA and copy).
 // ===========================================================================
 constexpr int kPBox = 16;   // activation rows per tensor copy (per CTA: N / 2 rows)
+constexpr int kPDecWarps = 8;    // warps 0-7: decode, lane quarter w % 4, K half w / 4
+constexpr int kPEpiWarps = 16;   // warps 8-23: epilogue
+constexpr int kPTmaWarp = 24;
+constexpr int kPMmaWarp = 25;
+constexpr int kPThreads = 32 * 26;
 
 template <int BN>
 struct PCfg {
@@ -929,11 +934,13 @@ __device__ __forceinline__ uint32_t pair_n(const GemmArgs& a, int32_t tau) {
 }
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(kTThreads, 1)
+__global__ void __launch_bounds__(kPThreads, 1)
     moe_gemm_2sm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap) {
   using C = PCfg<BN>;
   constexpr bool kGated = EPI == kEpiSwigluBf16;
-  constexpr bool kEarly = C::kNBuf == 2 || EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal;
+  // with 832 threads the register budget holds 16 accumulator columns per
+  // thread at a time: the single (256-slot) buffer is drained chunk by chunk
+  constexpr bool kEarly = C::kNBuf == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -953,19 +960,19 @@ __global__ void __launch_bounds__(kTThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < C::kAStages; ++i) mbar_init(&afull[i], 2 * kTDecWarps);
+    for (int i = 0; i < C::kAStages; ++i) mbar_init(&afull[i], 2 * kPDecWarps);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accfull[b], 1);
-      mbar_init(&accempty[b], 2 * kTEpiWarps);
+      mbar_init(&accempty[b], 2 * kPEpiWarps);
     }
     mbar_init(drain, 1);
     fence_mbarrier_init();
   }
-  if (warp == kTMmaWarp) {
+  if (warp == kPMmaWarp) {
     tmem_alloc2(tmem_slot, kTmemCols);
     tmem_relinquish2();
   }
-  if (warp == kTTmaWarp && lane == 0) prefetch_tensormap(&bmap);
+  if (warp == kPTmaWarp && lane == 0) prefetch_tensormap(&bmap);
   tc_fence_before();
   cluster_sync();   // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
@@ -975,7 +982,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
   const int64_t n_items = plan_items(a);
   const int64_t cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
-  if (warp == kTTmaWarp) {
+  if (warp == kPTmaWarp) {
     // ------------------------------------------------------------ producer (both CTAs)
     int stage = 0;
     uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
@@ -1025,7 +1032,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     if (lane == 0)
       for (int q = 0; q < C::kStages; ++q)
         if (issued_mask & (1u << q)) mbar_wait(&full[q], (issued_parity >> q) & 1u, a.err);
-  } else if (warp == kTMmaWarp) {
+  } else if (warp == kPMmaWarp) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
     if (rank == 0 && lane == 0) {
       int stage = 0, astage = 0;
@@ -1069,13 +1076,15 @@ __global__ void __launch_bounds__(kTThreads, 1)
       tc_commit2(drain, 0x1);
       mbar_wait(drain, 0, a.err);
     }
-  } else if (warp < kTDecWarps) {
+  } else if (warp < kPDecWarps) {
     // ------------------------------------------------------------ decode (both CTAs)
-    const int q = warp;
+    // warp w: TMEM lane quarter w % 4 (thread = A row), K half w / 4 of
+    // each chunk: 8 code words and 4 scales -> 32 BF16x2 columns
+    const int q = warp & 3, kh = warp >> 2;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const int rloc = kGated ? 16 * q + (lane & 15) : 32 * q + lane;
     const int code_base = kGated && lane >= 16 ? 4096 : 0;
-    const int sf_off = kTWCodes + (kGated && lane >= 16 ? 512 : 0) + rloc * 8;
+    const int sf_off = kTWCodes + (kGated && lane >= 16 ? 512 : 0) + rloc * 8 + kh * 4;
     int stage = 0, astage = 0;
     uint32_t phase = 0, qd = 0;
     bool ok = true;
@@ -1093,20 +1102,21 @@ __global__ void __launch_bounds__(kTThreads, 1)
         }
         tc_fence_after();
         const uint8_t* blk = stages + stage * C::kStage;
-        const uint2 sv = *reinterpret_cast<const uint2*>(blk + sf_off);
-        const uint32_t acol = tmem + lane_base + (uint32_t)(C::kABase + astage * 64);
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const uint4 d4 = *reinterpret_cast<const uint4*>(blk + code_base + prep_chunk_offset(rloc, qq));
-          const uint32_t sp = (qq < 2 ? sv.x : sv.y) >> (16 * (qq & 1));
-          const uint32_t sa = scale_code_bf16x2(sp & 0xFFu), sb = scale_code_bf16x2((sp >> 8) & 0xFFu);
-          uint32_t o[16];
-          decode_word(d4.x, sa, o);
-          decode_word(d4.y, sa, o + 4);
-          decode_word(d4.z, sb, o + 8);
-          decode_word(d4.w, sb, o + 12);
-          tmem_st16(acol + 16 * qq, o);
-        }
+        const uint32_t sv = *reinterpret_cast<const uint32_t*>(blk + sf_off);   // scale blocks 4kh..4kh+3
+        const uint4 d0 = *reinterpret_cast<const uint4*>(blk + code_base + prep_chunk_offset(rloc, 2 * kh));
+        const uint4 d1 = *reinterpret_cast<const uint4*>(blk + code_base + prep_chunk_offset(rloc, 2 * kh + 1));
+        const uint32_t acol = tmem + lane_base + (uint32_t)(C::kABase + astage * 64 + kh * 32);
+        uint32_t o[16];
+        decode_word(d0.x, scale_code_bf16x2(sv & 0xFFu), o);
+        decode_word(d0.y, scale_code_bf16x2(sv & 0xFFu), o + 4);
+        decode_word(d0.z, scale_code_bf16x2((sv >> 8) & 0xFFu), o + 8);
+        decode_word(d0.w, scale_code_bf16x2((sv >> 8) & 0xFFu), o + 12);
+        tmem_st16(acol, o);
+        decode_word(d1.x, scale_code_bf16x2((sv >> 16) & 0xFFu), o);
+        decode_word(d1.y, scale_code_bf16x2((sv >> 16) & 0xFFu), o + 4);
+        decode_word(d1.z, scale_code_bf16x2(sv >> 24), o + 8);
+        decode_word(d1.w, scale_code_bf16x2(sv >> 24), o + 12);
+        tmem_st16(acol + 16, o);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -1120,7 +1130,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int et = threadIdx.x - 32 * kTDecWarps;
+    const int et = threadIdx.x - 32 * kPDecWarps;
     const int grp = et >> 7, q = warp & 3, r = 32 * q + lane;
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
     const int c0 = grp * C::kCols;
@@ -1184,7 +1194,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
   tc_fence_before();
   cluster_sync();   // neither CTA leaves while its peer may still reach its memory
   tc_fence_after();
-  if (warp == kTMmaWarp) {
+  if (warp == kPMmaWarp) {
     __syncwarp();
     tmem_dealloc2(tmem, kTmemCols);
   }
@@ -2234,7 +2244,7 @@ cudaError_t launch_2sm(const Shape& s, const GemmLaunch& g, cudaStream_t st, boo
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kTThreads);
+  cfg.blockDim = dim3(kPThreads);
   cfg.dynamicSmemBytes = Cf::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
