@@ -935,7 +935,8 @@ __device__ __forceinline__ uint32_t pair_n(const GemmArgs& a, int32_t tau) {
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kPThreads, 1)
-    moe_gemm_2sm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap) {
+    moe_gemm_2sm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap,
+                        const __grid_constant__ CUtensorMap bmap_wide) {
   using C = PCfg<BN>;
   constexpr bool kGated = EPI == kEpiSwigluBf16;
   // with 832 threads the register budget holds 16 accumulator columns per
@@ -972,7 +973,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     tmem_alloc2(tmem_slot, kTmemCols);
     tmem_relinquish2();
   }
-  if (warp == kPTmaWarp && lane == 0) prefetch_tensormap(&bmap);
+  if (warp == kPTmaWarp && lane == 0) {
+    prefetch_tensormap(&bmap);
+    prefetch_tensormap(&bmap_wide);
+  }
   tc_fence_before();
   cluster_sync();   // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
@@ -1012,11 +1016,20 @@ __global__ void __launch_bounds__(kPThreads, 1)
               tma_load_1d(sw, blk + hf * kTWCodes, kTWCodes, &full[stage]);
               tma_load_1d(sw + kTWCodes, blk + kWDataBytes + hf * 1024, 1024, &full[stage]);
             }
+            // a full tile's half in one copy per K atom (each copy instruction
+            // costs about as much issue time as a tenth of the chunk's MMAs);
+            // a partly filled tile in copies of 16 rows
 #pragma unroll
-            for (int at = 0; at < 2; ++at)
-              for (uint32_t b = 0; b < nbox; ++b)
-                tma_load_2d(sb + at * (BN / 2) * 128 + b * kPBox * 128, &bmap, c * kBK + at * 64,
-                            tau * BN + (int32_t)(rank * half_rows + b * kPBox), &full[stage]);
+            for (int at = 0; at < 2; ++at) {
+              if (half_rows == BN / 2) {
+                tma_load_2d(sb + at * (BN / 2) * 128, &bmap_wide, c * kBK + at * 64,
+                            tau * BN + (int32_t)(rank * half_rows), &full[stage]);
+              } else {
+                for (uint32_t b = 0; b < nbox; ++b)
+                  tma_load_2d(sb + at * (BN / 2) * 128 + b * kPBox * 128, &bmap, c * kBK + at * 64,
+                              tau * BN + (int32_t)(rank * half_rows + b * kPBox), &full[stage]);
+              }
+            }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -2238,8 +2251,10 @@ cudaError_t launch_2sm(const Shape& s, const GemmLaunch& g, cudaStream_t st, boo
   a.rsf = g.rsf;
   a.err = g.err;
   const int64_t Kdim = g.which == 1 ? s.H : s.I;
-  CUtensorMap map;
-  if (!make_act_map(&map, g.act, g.act_rows, Kdim, kPBox)) return cudaErrorInvalidValue;
+  CUtensorMap map, map_wide;
+  if (!make_act_map(&map, g.act, g.act_rows, Kdim, kPBox) ||
+      !make_act_map(&map_wide, g.act, g.act_rows, Kdim, BN / 2))
+    return cudaErrorInvalidValue;
   auto kern = moe_gemm_2sm_kernel<BN, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
   if (e != cudaSuccess) return e;
@@ -2271,7 +2286,7 @@ cudaError_t launch_2sm(const Shape& s, const GemmLaunch& g, cudaStream_t st, boo
   const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
   const int64_t pairs = std::min<int64_t>({(int64_t)max_pairs, grid_ctas(g) / 2, max_items});
   cfg.gridDim = dim3(2 * (unsigned)std::max<int64_t>(pairs, 1));
-  return cudaLaunchKernelEx(&cfg, kern, a, map);
+  return cudaLaunchKernelEx(&cfg, kern, a, map, map_wide);
 }
 
 template <int BN>
