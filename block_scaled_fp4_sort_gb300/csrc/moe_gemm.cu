@@ -157,6 +157,7 @@ struct Cfg {
   static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes + 4 * 128;
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kStages >= 2, "pipeline depth");
+  static_assert((3 * kStages + kAStages + 3) * 8 + 4 <= kBarBytes, "barrier region");
 };
 
 // Epilogue of the tcgen05 GEMMs: fp32 accumulators [128 weight rows x BN
@@ -276,19 +277,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);   // activations
   uint64_t* empty = full + C::kStages;
   uint64_t* afull = empty + C::kStages;
+  uint64_t* wfull = afull + C::kAStages + 3;   // weights (after accfull, accempty, drain)
   uint64_t* accfull = afull + C::kAStages;
   uint64_t* accempty = accfull + 1;   // the epilogue has read the accumulators
   uint64_t* drain = accempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wfull + C::kStages);
   int32_t* gidx = reinterpret_cast<int32_t*>(smem + C::kStages * C::kStage + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
+      mbar_init(&wfull[i], 1);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < C::kAStages; ++i) {
@@ -340,8 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) {
             uint8_t* sw = stages + stage * C::kStage;
             uint8_t* sb = sw + kWBlockBytes;
-            mbar_arrive_expect_tx(&full[stage], (uint32_t)kWBlockBytes + btx);
-            tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &full[stage]);
+            // the weights on a barrier of their own, issued first: the
+            // decoders start on them while the activation tile is in flight
+            mbar_arrive_expect_tx(&wfull[stage], (uint32_t)kWBlockBytes);
+            tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &wfull[stage]);
+            mbar_arrive_expect_tx(&full[stage], btx);
 #pragma unroll
             for (int at = 0; at < 2; ++at) {
               const int32_t kc = c * kBK + at * 64;
@@ -369,7 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // copies still in flight must land before the CTA exits
     if (lane == 0)
       for (int s = 0; s < C::kStages; ++s)
-        if (issued_mask & (1u << s)) mbar_wait(&full[s], (issued_parity >> s) & 1u, a.err);
+        if (issued_mask & (1u << s)) {
+          mbar_wait(&wfull[s], (issued_parity >> s) & 1u, a.err);
+          mbar_wait(&full[s], (issued_parity >> s) & 1u, a.err);
+        }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -432,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       const ItemPlan plan = load_item_plan(a, item);   // arrives during the decode
       for (int c = 0; c < a.C && decoder; ++c) {
-        bool good = mbar_wait(&full[stage], phase, a.err);
+        bool good = mbar_wait(&wfull[stage], phase, a.err);
         // TMEM A stage (qd % kAStages) was last read by the MMAs of chunk
         // qd - kAStages, whose commit completes SMEM stage (qd - kAStages) %
         // kStages.  That barrier cannot run a further phase ahead: the next one
@@ -1001,7 +1010,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const uint8_t* wsrc = a.wprep + ((int64_t)e * a.FB + pb) * a.C * (int64_t)kWBlockBytes;
       for (int c = 0; c < a.C; ++c) {
         if (lane == 0) {
-          ok = mbar_wait_cluster(&empty[stage], phase ^ 1u, a.err);
+          ok = mbar_wait(&empty[stage], phase ^ 1u, a.err);
           if (ok) {
             uint8_t* sw = stages + stage * C::kStage;
             uint8_t* sb = sw + kTWBytes;
@@ -1054,7 +1063,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       for (int64_t item = cid; item < n_items && ok; item += ncl, ++k) {
         const uint32_t buf = C::kNBuf == 2 ? (k & 1u) : 0u;
         if (k >= (uint32_t)C::kNBuf &&
-            !mbar_wait_cluster(&accempty[buf], (k / C::kNBuf - 1) & 1u, a.err))
+            !mbar_wait(&accempty[buf], (k / C::kNBuf - 1) & 1u, a.err))
           break;
         const int32_t tau = (int32_t)(item / a.F);
         const uint32_t idesc = idesc_bf16_f32(256, (int)pair_n<BN>(a, tau));
@@ -1062,7 +1071,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         for (int c = 0; c < a.C; ++c) {
           // both CTAs' decoders have stored this chunk's A (after their own
           // copies, activation halves included, had landed)
-          if (!mbar_wait_cluster(&afull[astage], aphase, a.err)) {
+          if (!mbar_wait(&afull[astage], aphase, a.err)) {
             ok = false;
             break;
           }
@@ -1106,7 +1115,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         bool good = mbar_wait(&full[stage], phase, a.err);
         if (qd >= (uint32_t)C::kAStages) {
           const uint32_t qp = qd - (uint32_t)C::kAStages;
-          good = good && mbar_wait_cluster(&empty[qp % C::kStages], (qp / C::kStages) & 1u, a.err);
+          good = good && mbar_wait(&empty[qp % C::kStages], (qp / C::kStages) & 1u, a.err);
         }
         ++qd;
         if (!__all_sync(0xffffffffu, good)) {
@@ -1167,7 +1176,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       int32_t nv = cur.mn - tau * BN;
       nv = nv < 0 ? 0 : nv > BN ? BN : nv;
       const int nch = grp < C::kGroups ? (min(max(nv - c0, 0), C::kCols) + 15) >> 4 : 0;
-      if (!__all_sync(0xffffffffu, mbar_wait_cluster(&accfull[buf], (k / C::kNBuf) & 1u, a.err)))
+      if (!__all_sync(0xffffffffu, mbar_wait(&accfull[buf], (k / C::kNBuf) & 1u, a.err)))
         break;
       tc_fence_after();
       const uint32_t acc = tmem + lane_base + buf * (uint32_t)BN + (uint32_t)c0;
