@@ -124,6 +124,14 @@ __device__ __forceinline__ int32_t plan_expert(const GemmArgs& a, int32_t tau) {
   set_error(a.err, kErrDevice);
   return 0;
 }
+// valid slots of route tile tau, clamped to [1, BN] (a malformed plan costs
+// work, never an out-of-range access)
+template <int BN>
+__device__ __forceinline__ int32_t tile_valid(const GemmArgs& a, int32_t tau) {
+  const int32_t v = a.tile_mn[tau] - tau * BN;
+  return v < 1 ? 1 : v > BN ? BN : v;
+}
+
 // An item's plan entries as loaded, the expert id not yet clamped.  The
 // epilogue warps load them at the start of an item or one item ahead and
 // clamp the expert (the producer reports it) only where alpha is read, so
@@ -271,7 +279,8 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap) {
+    moe_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap,
+                    const __grid_constant__ CUtensorMap bmap_part) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -306,7 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kTmaWarp && lane == 0) prefetch_tensormap(&bmap);
+  if (warp == kTmaWarp && lane == 0) {
+    prefetch_tensormap(&bmap);
+    prefetch_tensormap(&bmap_part);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -315,6 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependency_wait();
   const int64_t n_items = plan_items(a);
   const bool gather = a.gather_rows != nullptr;
+  // A tile with few valid slots multiplies only those: the MMA's N is the
+  // valid count rounded up to 16, and the activation rows are loaded in
+  // boxes of kPartRows up to that count (the full tile in one box when it is
+  // (nearly) full), so a lightly used expert's tile costs its weight stream
+  // rather than a full-width MMA.
+  constexpr int kPartRows = 32;
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
@@ -335,7 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      const uint32_t btx = gather ? (uint32_t)nq * 2u * 512u : (uint32_t)C::kBBytes;
+      const int32_t nv = tile_valid<BN>(a, tau);
+      const int32_t nbox = BN > kPartRows && nv <= BN - kPartRows ? (nv + kPartRows - 1) / kPartRows : 0;
+      const uint32_t btx = gather     ? (uint32_t)nq * 2u * 512u
+                           : nbox > 0 ? 2u * (uint32_t)nbox * kPartRows * 128u
+                                      : (uint32_t)C::kBBytes;
       const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kWBlockBytes;
       for (int c = 0; c < a.C; ++c) {
         if (lane == 0) {
@@ -356,6 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int g = 0; g < nq; ++g)
                   tma_gather4(dst + g * 512, &bmap, kc, gidx[4 * g], gidx[4 * g + 1],
                               gidx[4 * g + 2], gidx[4 * g + 3], &full[stage]);
+              } else if (nbox > 0) {
+                for (int b = 0; b < nbox; ++b)
+                  tma_load_2d(dst + b * kPartRows * 128, &bmap_part, kc, tau * BN + b * kPartRows,
+                              &full[stage]);
               } else {
                 tma_load_2d(dst, &bmap, kc, tau * BN, &full[stage]);
               }
@@ -382,7 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
       int stage = 0, astage = 0;
       uint32_t phase = 0, aphase = 0, emptyphase = 0;
       bool ok = true;
@@ -392,6 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(accempty, emptyphase, a.err)) break;
           emptyphase ^= 1u;
         }
+        const uint32_t kIdesc =
+            idesc_bf16_f32(128, (tile_valid<BN>(a, (int32_t)(item / a.F)) + 15) & ~15);
         for (int c = 0; c < a.C; ++c) {
           if (!mbar_wait(&afull[astage], aphase, a.err) || !mbar_wait(&full[stage], phase, a.err)) {
             ok = false;
@@ -518,66 +545,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ===========================================================================
-// One-tile BF16-decode grouped GEMM (w4a16, route tiles 32..256).
-//
-// The same arithmetic as moe_gemm_kernel, organised so that the MMA never
-// waits on the epilogue and its N dimension can reach 256:
-//   * one work item = (route tile tau, one 128-row weight tile f): a gated
-//     GEMM1 tile holds 64 features -- in lane quarter q, lanes 0-15 the gate
-//     rows of features 64f+16q.., lanes 16-31 the matching up rows, so a
-//     SwiGLU pair is 16 lanes apart in one warp -- and the other GEMMs' tile
-//     is rows 128f..128f+127.  Its weights are one half of a prepared 256-row
-//     block (two or four bulk copies per chunk, no other layout);
-//   * the MMA width follows the tile's valid slots: N = the valid count
-//     rounded up to 16 (at most the route tile), and only the activation rows
-//     up to the next multiple of 32 are loaded, so a lightly used expert's
-//     tile costs its weight stream, not a full-width MMA;
-//   * decode, MMA issue and epilogue run in separate warps: the fp32
-//     accumulators are double-buffered in tensor memory for route tiles up to
-//     128 (the epilogue of one item overlaps the next item's main loop); at
-//     256 slots they fill 256 columns, so the epilogue copies them into
-//     registers and releases them before its arithmetic and stores.
-// TMEM: accumulators in columns 0..255, decoded A stages of 64 columns from
-// column 256.  Per CTA (persistent, 704 threads): warps 0-3 decode (warp q
-// owns lane quarter q), warps 4-19 epilogue (four groups of 128 threads,
-// each a quarter of the slot columns), warp 20 TMA producer, warp 21 MMA.
+// Helpers of the CTA-pair kernel below: a prepared 256-row weight block's
+// 128-row half (a gated FC1 half holds 64 gate rows and their 64 up rows,
+// lanes 0-15 / 16-31 of each lane quarter), and its epilogue per 16 columns.
 // ===========================================================================
-constexpr int kTDecWarps = 4;
-constexpr int kTEpiWarps = 16;
-constexpr int kTTmaWarp = 20;
-constexpr int kTMmaWarp = 21;
-constexpr int kTThreads = 32 * 22;
 constexpr int kTWBytes = kWBlockBytes / 2;   // 9216: codes and scales of 128 rows
 constexpr int kTWCodes = kWDataBytes / 2;    // 8192
-constexpr int kTBox = 32;                    // activation rows per tensor copy
-
-template <int BN>
-struct TCfg {
-  static constexpr int kBBytes = 2 * BN * 128;             // two 64-element K atoms of BN rows
-  static constexpr int kStage = kTWBytes + kBBytes;        // 9216 + 256 BN
-  static constexpr int kStagesRaw = (222 * 1024) / kStage;
-  static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
-  static constexpr int kAStages = kStages < 4 ? kStages : 4;
-  static constexpr int kNBuf = BN <= 128 ? 2 : 1;          // accumulator buffers
-  static constexpr int kABase = 256;
-  static constexpr int kCols = BN / 4 >= 16 ? BN / 4 : 16; // epilogue columns per group
-  static constexpr int kGroups = BN / kCols;               // 2 (BN = 32) or 4
-  static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes;
-  static_assert(kStage % 1024 == 0, "stage alignment");
-  static_assert(kStages >= 2 && kStages >= kAStages, "pipeline depth");
-  static_assert(kABase + kAStages * 64 <= 512, "tensor memory");
-  static_assert(kNBuf * BN <= kABase, "accumulators");
-  static_assert(kSmem <= 227 * 1024, "shared memory");
-};
-
-// valid slots of route tile tau, clamped to [1, BN] (a malformed plan costs
-// work, never an out-of-range access)
-template <int BN>
-__device__ __forceinline__ int32_t tile_valid(const GemmArgs& a, int32_t tau) {
-  const int32_t v = a.tile_mn[tau] - tau * BN;
-  return v < 1 ? 1 : v > BN ? BN : v;
-}
 
 // Epilogue of one 16-column chunk of the one-tile kernel: fp32 accumulators
 // v[0..15] of TMEM lane r (lane quarter q) for slots s0..s0+15 of weight tile f.
@@ -619,273 +592,6 @@ __device__ __forceinline__ void t_epilogue_chunk(const GemmArgs& a, const uint32
         static_cast<__nv_bfloat16*>(a.out)[s * a.out_ld + n] =
             __float2bfloat16_rn(relu2(acc * token_factor(a, s)));
     }
-  }
-}
-
-template <int BN, int EPI>
-__global__ void __launch_bounds__(kTThreads, 1)
-    moe_gemm_1t_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap) {
-  using C = TCfg<BN>;
-  constexpr bool kGated = EPI == kEpiSwigluBf16;
-  // early release of the accumulators: always with two buffers; with one
-  // (256 slots) only for the fp32 epilogues, whose 64 values per thread fit
-  // the register budget beside their few live values
-  constexpr bool kEarly = C::kNBuf == 2 || EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
-  uint64_t* empty = full + C::kStages;
-  uint64_t* afull = empty + C::kStages;
-  uint64_t* accfull = afull + C::kAStages;   // [2]
-  uint64_t* accempty = accfull + 2;          // [2]
-  uint64_t* drain = accempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    for (int i = 0; i < C::kAStages; ++i) mbar_init(&afull[i], kTDecWarps);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&accfull[b], 1);
-      mbar_init(&accempty[b], kTEpiWarps);
-    }
-    mbar_init(drain, 1);
-    fence_mbarrier_init();
-  }
-  if (warp == kTMmaWarp) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
-  if (warp == kTTmaWarp && lane == 0) prefetch_tensormap(&bmap);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  grid_dependency_wait();
-  const int64_t n_items = plan_items(a);
-
-  if (warp == kTTmaWarp) {
-    // ------------------------------------------------------------ producer
-    int stage = 0;
-    uint32_t phase = 0, issued_mask = 0, issued_parity = 0;
-    bool ok = true;
-    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      const int32_t e = plan_expert(a, tau);
-      const int32_t nbox = (tile_valid<BN>(a, tau) + kTBox - 1) / kTBox;
-      const uint32_t tx = (uint32_t)kTWBytes + 2u * (uint32_t)nbox * kTBox * 128u;
-      const int hf = f & 1;   // which half of the prepared 256-row block
-      const uint8_t* wsrc = a.wprep + ((int64_t)e * a.FB + (f >> 1)) * a.C * (int64_t)kWBlockBytes;
-      for (int c = 0; c < a.C; ++c) {
-        if (lane == 0) {
-          ok = mbar_wait(&empty[stage], phase ^ 1u, a.err);
-          if (ok) {
-            uint8_t* sw = stages + stage * C::kStage;
-            uint8_t* sb = sw + kTWBytes;
-            const uint8_t* blk = wsrc + (int64_t)c * kWBlockBytes;
-            mbar_arrive_expect_tx(&full[stage], tx);
-            if (kGated) {   // gate rows 64hf.., up rows 128 + 64hf.., then their scales
-              tma_load_1d(sw, blk + hf * 4096, 4096, &full[stage]);
-              tma_load_1d(sw + 4096, blk + 8192 + hf * 4096, 4096, &full[stage]);
-              tma_load_1d(sw + kTWCodes, blk + kWDataBytes + hf * 512, 512, &full[stage]);
-              tma_load_1d(sw + kTWCodes + 512, blk + kWDataBytes + 1024 + hf * 512, 512, &full[stage]);
-            } else {        // rows 128hf..128hf+127
-              tma_load_1d(sw, blk + hf * kTWCodes, kTWCodes, &full[stage]);
-              tma_load_1d(sw + kTWCodes, blk + kWDataBytes + hf * 1024, 1024, &full[stage]);
-            }
-#pragma unroll
-            for (int at = 0; at < 2; ++at)
-              for (int b = 0; b < nbox; ++b)
-                tma_load_2d(sb + at * BN * 128 + b * kTBox * 128, &bmap, c * kBK + at * 64,
-                            tau * BN + b * kTBox, &full[stage]);
-            issued_mask |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    // copies still in flight must land before the CTA exits
-    if (lane == 0)
-      for (int q = 0; q < C::kStages; ++q)
-        if (issued_mask & (1u << q)) mbar_wait(&full[q], (issued_parity >> q) & 1u, a.err);
-  } else if (warp == kTMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0, astage = 0;
-      uint32_t phase = 0, aphase = 0, k = 0;
-      bool ok = true;
-      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++k) {
-        const uint32_t buf = C::kNBuf == 2 ? (k & 1u) : 0u;
-        // the epilogue must have taken this buffer's previous item
-        if (k >= (uint32_t)C::kNBuf &&
-            !mbar_wait(&accempty[buf], (k / C::kNBuf - 1) & 1u, a.err))
-          break;
-        const int32_t tau = (int32_t)(item / a.F);
-        const uint32_t n_mma = (uint32_t)(tile_valid<BN>(a, tau) + 15) & ~15u;
-        const uint32_t idesc = idesc_bf16_f32(128, (int)n_mma);
-        const uint32_t d = tmem + buf * (uint32_t)BN;
-        for (int c = 0; c < a.C; ++c) {
-          if (!mbar_wait(&afull[astage], aphase, a.err) || !mbar_wait(&full[stage], phase, a.err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sb = smem_u32(stages + stage * C::kStage + kTWBytes);
-          const uint32_t abase = tmem + (uint32_t)(C::kABase + astage * 64);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bd = smem_desc_sw128(sb + (kk >> 2) * BN * 128 + (kk & 3) * 32);
-            mma_bf16_ts(d, abase + kk * 8, bd, idesc, (c > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc_commit(&empty[stage]);   // frees the shared-memory stage and the TMEM A stage
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
-          if (++astage == C::kAStages) {
-            astage = 0;
-            aphase ^= 1u;
-          }
-        }
-        if (ok) tc_commit(&accfull[buf]);
-      }
-      tc_commit(drain);
-      mbar_wait(drain, 0, a.err);
-    }
-  } else if (warp < kTDecWarps) {
-    // ------------------------------------------------------------ decode
-    // thread = TMEM lane r = A row r: its weight row's 64 code bytes and 8
-    // scales -> 64 BF16x2 words, stored into the chunk's A stage
-    const int q = warp;
-    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    const int rloc = kGated ? 16 * q + (lane & 15) : 32 * q + lane;   // row in its part
-    const int code_base = kGated && lane >= 16 ? 4096 : 0;
-    const int sf_off = kTWCodes + (kGated && lane >= 16 ? 512 : 0) + rloc * 8;
-    int stage = 0, astage = 0;
-    uint32_t phase = 0, qd = 0;   // qd: chunks decoded so far by this CTA
-    bool ok = true;
-    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      for (int c = 0; c < a.C; ++c) {
-        bool good = mbar_wait(&full[stage], phase, a.err);
-        // A stage qd % kAStages was last read by the MMAs of chunk qd -
-        // kAStages, whose commit completes the shared-memory stage of that
-        // chunk; kStages >= kAStages keeps that barrier from running a
-        // further phase ahead (which would need chunk qd, not yet decoded)
-        if (qd >= (uint32_t)C::kAStages) {
-          const uint32_t qp = qd - (uint32_t)C::kAStages;
-          good = good && mbar_wait(&empty[qp % C::kStages], (qp / C::kStages) & 1u, a.err);
-        }
-        ++qd;
-        if (!__all_sync(0xffffffffu, good)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint8_t* blk = stages + stage * C::kStage;
-        const uint2 sv = *reinterpret_cast<const uint2*>(blk + sf_off);
-        const uint32_t acol = tmem + lane_base + (uint32_t)(C::kABase + astage * 64);
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {   // 32 K elements: 4 words under scale blocks 2qq, 2qq+1
-          const uint4 d4 = *reinterpret_cast<const uint4*>(blk + code_base + prep_chunk_offset(rloc, qq));
-          const uint32_t sp = (qq < 2 ? sv.x : sv.y) >> (16 * (qq & 1));
-          const uint32_t sa = scale_code_bf16x2(sp & 0xFFu), sb = scale_code_bf16x2((sp >> 8) & 0xFFu);
-          uint32_t o[16];
-          decode_word(d4.x, sa, o);
-          decode_word(d4.y, sa, o + 4);
-          decode_word(d4.z, sb, o + 8);
-          decode_word(d4.w, sb, o + 12);
-          tmem_st16(acol + 16 * qq, o);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[astage]);
-        if (++stage == C::kStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (++astage == C::kAStages) astage = 0;
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue (warps 4-19)
-    const int et = threadIdx.x - 32 * kTDecWarps;   // 0..511
-    const int grp = et >> 7, q = warp & 3, r = 32 * q + lane;
-    const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    const int c0 = grp * C::kCols;
-    uint32_t k = 0;
-    ItemPlan next = {0, 0};
-    float alpha_next = 0.0f;
-    if (blockIdx.x < n_items) {
-      next = load_item_plan(a, blockIdx.x);
-      alpha_next = item_alpha(a, next);
-    }
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
-      const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      const uint32_t buf = C::kNBuf == 2 ? (k & 1u) : 0u;
-      const ItemPlan cur = next;
-      const float scale = alpha_next * 256.0f;   // undoes the decode's 2^-8
-      const bool more = item + gridDim.x < n_items;
-      if (more) next = load_item_plan(a, item + gridDim.x);
-      const int64_t s0 = (int64_t)tau * BN;
-      int32_t nv = cur.mn - tau * BN;
-      nv = nv < 0 ? 0 : nv > BN ? BN : nv;
-      // this group's 16-column chunks that hold valid slots (warp-uniform)
-      const int nch = grp < C::kGroups ? (min(max(nv - c0, 0), C::kCols) + 15) >> 4 : 0;
-      if (!__all_sync(0xffffffffu, mbar_wait(&accfull[buf], (k / C::kNBuf) & 1u, a.err))) break;
-      tc_fence_after();
-      const uint32_t acc = tmem + lane_base + buf * (uint32_t)BN + (uint32_t)c0;
-      if (kEarly) {
-        // all of this group's accumulators into registers, then the buffer
-        // goes back to the MMA warp before the arithmetic and the stores
-        uint32_t v[C::kCols];
-#pragma unroll
-        for (int j = 0; j < C::kCols / 16; ++j)
-          if (j < nch) tmem_ld16p(acc + 16 * j, v + 16 * j);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&accempty[buf]);
-#pragma unroll
-        for (int j = 0; j < C::kCols / 16; ++j) {
-          if (j >= nch) break;
-          t_epilogue_chunk<EPI>(a, v + 16 * j, s0 + c0 + 16 * j, cur.mn, f, q, r, lane, scale);
-        }
-      } else {
-        // 16 columns at a time (register budget), the buffer released after
-#pragma unroll 1
-        for (int j = 0; j < nch; ++j) {
-          uint32_t v[16];
-          tmem_ld16p(acc + 16 * j, v);
-          tmem_wait_ld();
-          t_epilogue_chunk<EPI>(a, v, s0 + c0 + 16 * j, cur.mn, f, q, r, lane, scale);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&accempty[buf]);
-      }
-      if (more) alpha_next = item_alpha(a, next);
-    }
-  }
-
-  __syncthreads();
-  launch_dependents();
-  if (warp == kTMmaWarp) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -2141,8 +1847,9 @@ cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool 
   a.rsf = g.rsf;
   a.err = g.err;
   const int64_t Kdim = g.which == 1 ? s.H : s.I;
-  CUtensorMap map;
-  if (!make_act_map(&map, g.act, g.act_rows, Kdim, g.gather_rows ? 1 : BN))
+  CUtensorMap map, map_part;
+  if (!make_act_map(&map, g.act, g.act_rows, Kdim, g.gather_rows ? 1 : BN) ||
+      !make_act_map(&map_part, g.act, g.act_rows, Kdim, BN < 32 ? BN : 32))
     return cudaErrorInvalidValue;
   auto kern = moe_gemm_kernel<BN, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
@@ -2158,7 +1865,7 @@ cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a, map);
+  return cudaLaunchKernelEx(&cfg, kern, a, map, map_part);
 }
 
 template <int BN>
@@ -2172,63 +1879,6 @@ cudaError_t launch_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
     case kEpiRelu2Nvfp4: return launch_t<BN, kEpiRelu2Nvfp4>(s, g, st, pdl);
     case kEpiSwigluMxfp8: return launch_t<BN, kEpiSwigluMxfp8>(s, g, st, pdl);
     case kEpiRelu2Mxfp8: return launch_t<BN, kEpiRelu2Mxfp8>(s, g, st, pdl);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
-template <int BN, int EPI>
-cudaError_t launch_1t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
-  using Cf = TCfg<BN>;
-  if (g.gather_rows != nullptr) return cudaErrorInvalidValue;   // reads x in slot order
-  GemmArgs a = {};
-  a.wprep = g.wprep;
-  a.alpha = g.alpha;
-  a.tile_expert = g.tile_expert;
-  a.tile_mn = g.tile_mn;
-  a.num_tiles = g.num_tiles;
-  a.top_k = (int32_t)s.K;
-  a.FB = (int32_t)row_blocks(s, g.which);
-  a.F = (int32_t)one_tile_blocks(s, g.which);
-  a.C = (int32_t)k_chunks(s, g.which);
-  a.out_ld = g.out_ld > 0 ? g.out_ld : (g.which == 1 ? s.I : s.H);
-  a.valid_rows = (int32_t)(g.which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H);
-  a.act = s.act;
-  a.token_scale = g.token_scale;
-  a.out = g.out;
-  a.max_tiles = (int32_t)s.tiles;
-  a.EL = (int32_t)s.EL;
-  a.R = s.R;
-  a.p2e = g.p2e;
-  a.route_w = g.route_w;
-  a.rsf = g.rsf;
-  a.err = g.err;
-  const int64_t Kdim = g.which == 1 ? s.H : s.I;
-  CUtensorMap map;
-  if (!make_act_map(&map, g.act, g.act_rows, Kdim, kTBox)) return cudaErrorInvalidValue;
-  auto kern = moe_gemm_1t_kernel<BN, EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
-  if (e != cudaSuccess) return e;
-  const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)std::min<int64_t>(grid_ctas(g), max_items));
-  cfg.blockDim = dim3(kTThreads);
-  cfg.dynamicSmemBytes = Cf::kSmem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a, map);
-}
-
-template <int BN>
-cudaError_t launch_1t_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
-  switch (g.epi) {
-    case kEpiSwigluBf16: return launch_1t<BN, kEpiSwigluBf16>(s, g, st, pdl);
-    case kEpiPlainBf16: return launch_1t<BN, kEpiPlainBf16>(s, g, st, pdl);
-    case kEpiAtomicFinal: return launch_1t<BN, kEpiAtomicFinal>(s, g, st, pdl);
-    case kEpiRelu2Bf16: return launch_1t<BN, kEpiRelu2Bf16>(s, g, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
