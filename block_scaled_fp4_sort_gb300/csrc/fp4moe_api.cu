@@ -23,8 +23,14 @@ inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
 
-int32_t auto_tile(int64_t R, int64_t EL) {
-  const int64_t avg = std::max<int64_t>(1, (R + EL - 1) / EL);
+// Automatic route tile: the average routes per local expert rounded up to a
+// power of two, clamped to [16, 128].  BF16-activation GEMMs size each MMA to
+// a tile's valid slots, so lightly used experts cost little in a wide tile and
+// heavily used ones stream their weights for fewer tiles: above 16 they take
+// twice the average.
+int32_t auto_tile(int64_t R, int64_t EL, int32_t mode) {
+  int64_t avg = std::max<int64_t>(1, (R + EL - 1) / EL);
+  if (mode == FP4MOE_W4A16 && avg > 16) avg *= 2;
   int32_t t = 16;
   while (t < avg && t < 128) t *= 2;
   return t;
@@ -46,7 +52,7 @@ fp4moe_status validate(const fp4moe_problem* p, Shape* s) {
   const int64_t R = (int64_t)p->num_tokens * p->top_k;
   int32_t T = p->route_tile;
   if (T == 0) {
-    T = auto_tile(R, EL);
+    T = auto_tile(R, EL, p->mode);
   } else if (T < 8 || T % 8 != 0) {
     return FP4MOE_ERR_INVALID_ARG;
   } else if (T != 8 && T != 16 && T != 32 && T != 64 && T != 128 && T != 256) {

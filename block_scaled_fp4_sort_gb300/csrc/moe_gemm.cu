@@ -411,14 +411,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, astage = 0;
       uint32_t phase = 0, aphase = 0, emptyphase = 0;
       bool ok = true;
+      // each item's MMA width from its tile's valid slots, loaded one item ahead
+      int32_t nv_next = blockIdx.x < n_items ? tile_valid<BN>(a, (int32_t)(blockIdx.x / a.F)) : 1;
       for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const uint32_t kIdesc = idesc_bf16_f32(128, (nv_next + 15) & ~15);
+        if (item + gridDim.x < n_items) nv_next = tile_valid<BN>(a, (int32_t)((item + gridDim.x) / a.F));
         // all epilogue warps must have read the previous item's accumulators
         if (item != blockIdx.x) {
           if (!mbar_wait(accempty, emptyphase, a.err)) break;
           emptyphase ^= 1u;
         }
-        const uint32_t kIdesc =
-            idesc_bf16_f32(128, (tile_valid<BN>(a, (int32_t)(item / a.F)) + 15) & ~15);
         for (int c = 0; c < a.C; ++c) {
           if (!mbar_wait(&afull[astage], aphase, a.err) || !mbar_wait(&full[stage], phase, a.err)) {
             ok = false;

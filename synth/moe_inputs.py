@@ -97,9 +97,13 @@ CONFIGS = {
 
 
 def route_tile_for(cfg: MoEConfig) -> int:
-    """Route tile the benchmarks use: the average routes per expert, rounded
-    up to a power of two and clamped to the tile sizes the GEMMs implement."""
+    """Route tile the benchmarks use (the library's automatic choice): the
+    average routes per expert -- doubled above 16 for BF16 activations, whose
+    GEMMs size each MMA to a tile's valid slots -- rounded up to a power of
+    two and clamped to [16, 128]."""
     avg = max(1, -(-cfg.routes // cfg.E))
+    if cfg.mode == "w4a16" and avg > 16:
+        avg *= 2
     t = 16
     while t < avg and t < 128:
         t *= 2

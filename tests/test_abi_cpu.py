@@ -63,7 +63,10 @@ def test_slot_bound_matches_oracle(lib, M, E, k, T):
 def test_auto_route_tile(lib):
     assert fm.route_tile(fm.problem(8, 7168, 2048, 256, 8)) == 16
     assert fm.route_tile(fm.problem(4096, 7168, 2048, 256, 8)) == 128
-    assert fm.route_tile(fm.problem(2048, 4096, 1536, 128, 4)) == 64
+    assert fm.route_tile(fm.problem(2048, 4096, 1536, 128, 4)) == 128   # BF16: twice the average
+    assert fm.route_tile(fm.problem(2048, 4096, 1536, 128, 4, mode=fm.W4A4)) == 64
+    assert fm.route_tile(fm.problem(128, 256, 256, 8, 2)) == 64            # average 32, doubled
+    assert fm.route_tile(fm.problem(64, 256, 256, 8, 2)) == 16             # average 16: as it is
     assert fm.route_tile(fm.problem(131072, 6144, 2048, 256, 8)) == 128
 
 

@@ -48,7 +48,12 @@ def test_workload_statistics():
 
 def test_route_tiles():
     got = {n: route_tile_for(c) for n, c in synth.CONFIGS.items()}
-    assert got == {"tiny_w4a16": 16, "decode_w4a16": 16, "prefill_w4a4": 128, "skewed_w4a16": 64,
+    # the benchmarks' tile is the library's automatic choice
+    import block_scaled_fp4_sort_gb300 as fm
+    from block_scaled_fp4_sort_gb300.buffers import problem_for
+    for n, c in synth.CONFIGS.items():
+        assert fm.route_tile(problem_for(c, 0)) == got[n], n
+    assert got == {"tiny_w4a16": 16, "decode_w4a16": 16, "prefill_w4a4": 128, "skewed_w4a16": 128,
                    "prefill_w4a8": 128, "large_w4a16": 128}
 
 
