@@ -124,14 +124,6 @@ __device__ __forceinline__ int32_t plan_expert(const GemmArgs& a, int32_t tau) {
   set_error(a.err, kErrDevice);
   return 0;
 }
-// valid slots of route tile tau, clamped to [1, BN] (a malformed plan costs
-// work, never an out-of-range access)
-template <int BN>
-__device__ __forceinline__ int32_t tile_valid(const GemmArgs& a, int32_t tau) {
-  const int32_t v = a.tile_mn[tau] - tau * BN;
-  return v < 1 ? 1 : v > BN ? BN : v;
-}
-
 // An item's plan entries as loaded, the expert id not yet clamped.  The
 // epilogue warps load them at the start of an item or one item ahead and
 // clamp the expert (the producer reports it) only where alpha is read, so
@@ -161,11 +153,11 @@ struct Cfg {
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kABase = 2 * BN <= 128 ? 128 : 256;     // TMEM column of A stage 0
   static constexpr int kAStages = (512 - kABase) / 128;        // 128 columns per A stage
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes + 4 * 128;
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kStages >= 2, "pipeline depth");
-  static_assert((3 * kStages + kAStages + 3) * 8 + 4 <= kBarBytes, "barrier region");
+  static_assert((3 * kStages + kAStages + 3) * 8 + 8 + 4 * kStages <= kBarBytes, "barrier region");
 };
 
 // Epilogue of the tcgen05 GEMMs: fp32 accumulators [128 weight rows x BN
@@ -294,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accempty = accfull + 1;   // the epilogue has read the accumulators
   uint64_t* drain = accempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wfull + C::kStages);
+  int32_t* stage_nv = reinterpret_cast<int32_t*>(tmem_slot + 2);   // valid slots of each stage's tile
   int32_t* gidx = reinterpret_cast<int32_t*>(smem + C::kStages * C::kStage + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -341,10 +334,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      const int32_t e = plan_expert(a, tau);
+      // both plan entries loaded together (one memory latency per item); the
+      // valid count reaches the MMA thread through shared memory with each stage
+      const int32_t e_raw = a.tile_expert[tau], mn_raw = a.tile_mn[tau];
+      int32_t e = e_raw;
+      if (e < 0 || e >= a.EL) {
+        set_error(a.err, kErrDevice);
+        e = 0;
+      }
+      const int32_t nv = min(max(mn_raw - tau * BN, 1), BN);
       // gathered tiles fetch only their valid rows, four at a time; the rows
       // past them feed only output columns the epilogue discards
-      const int32_t nq = gather ? (min(max(a.tile_mn[tau] - tau * BN, 0), BN) + 3) >> 2 : 0;
+      const int32_t nq = gather ? (min(max(mn_raw - tau * BN, 0), BN) + 3) >> 2 : 0;
       if (gather) {
         __syncwarp();
         for (int i = lane; i < BN; i += 32) {
@@ -353,7 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      const int32_t nv = tile_valid<BN>(a, tau);
       const int32_t nbox = BN > kPartRows && nv <= BN - kPartRows ? (nv + kPartRows - 1) / kPartRows : 0;
       const uint32_t btx = gather     ? (uint32_t)nq * 2u * 512u
                            : nbox > 0 ? 2u * (uint32_t)nbox * kPartRows * 128u
@@ -369,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // decoders start on them while the activation tile is in flight
             mbar_arrive_expect_tx(&wfull[stage], (uint32_t)kWBlockBytes);
             tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &wfull[stage]);
+            stage_nv[stage] = nv;   // released to the MMA thread by the arrive below
             mbar_arrive_expect_tx(&full[stage], btx);
 #pragma unroll
             for (int at = 0; at < 2; ++at) {
@@ -411,11 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, astage = 0;
       uint32_t phase = 0, aphase = 0, emptyphase = 0;
       bool ok = true;
-      // each item's MMA width from its tile's valid slots, loaded one item ahead
-      int32_t nv_next = blockIdx.x < n_items ? tile_valid<BN>(a, (int32_t)(blockIdx.x / a.F)) : 1;
       for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const uint32_t kIdesc = idesc_bf16_f32(128, (nv_next + 15) & ~15);
-        if (item + gridDim.x < n_items) nv_next = tile_valid<BN>(a, (int32_t)((item + gridDim.x) / a.F));
         // all epilogue warps must have read the previous item's accumulators
         if (item != blockIdx.x) {
           if (!mbar_wait(accempty, emptyphase, a.err)) break;
@@ -427,6 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          // the MMA width: this tile's valid slots rounded up to 16
+          const uint32_t kIdesc = idesc_bf16_f32(128, (stage_nv[stage] + 15) & ~15);
           const uint32_t sb = smem_u32(stages + stage * C::kStage + kWBlockBytes);
 #pragma unroll
           for (int tile = 0; tile < 2; ++tile) {
@@ -639,16 +638,11 @@ struct PCfg {
   static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes;
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kStages >= 2 && kStages >= kAStages, "pipeline depth");
+  static_assert((2 * kStages + kAStages + 5) * 8 + 8 + 4 * kStages <= kBarBytes, "barrier region");
   static_assert(kABase + kAStages * 64 <= 512, "tensor memory");
   static_assert(kNBuf * BN <= kABase, "accumulators");
   static_assert(kSmem <= 227 * 1024, "shared memory");
 };
-
-// the pair's MMA width for route tile tau: valid slots rounded up to 32, in [32, BN]
-template <int BN>
-__device__ __forceinline__ uint32_t pair_n(const GemmArgs& a, int32_t tau) {
-  return (uint32_t)(tile_valid<BN>(a, tau) + 31) & ~31u;
-}
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kPThreads, 1)
@@ -670,6 +664,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint64_t* accempty = accfull + 2;          // [2] rank 0's: both CTAs' epilogue warps
   uint64_t* drain = accempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int32_t* stage_n = reinterpret_cast<int32_t*>(tmem_slot + 2);   // MMA width of each stage's tile
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();   // 0 or 1
@@ -710,8 +705,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bool ok = true;
     for (int64_t item = cid; item < n_items && ok; item += ncl) {
       const int32_t tau = (int32_t)(item / a.F), pb = (int32_t)(item % a.F);
-      const int32_t e = plan_expert(a, tau);
-      const uint32_t half_rows = pair_n<BN>(a, tau) / 2;          // this CTA's activation rows
+      // both plan entries loaded together; the MMA width reaches rank 0's MMA
+      // thread through shared memory with each stage
+      const int32_t e_raw = a.tile_expert[tau], mn_raw = a.tile_mn[tau];
+      int32_t e = e_raw;
+      if (e < 0 || e >= a.EL) {
+        set_error(a.err, kErrDevice);
+        e = 0;
+      }
+      const uint32_t n_pair = (uint32_t)(min(max(mn_raw - tau * BN, 1), BN) + 31) & ~31u;
+      const uint32_t half_rows = n_pair / 2;          // this CTA's activation rows
       const uint32_t nbox = half_rows / kPBox;
       const uint32_t tx = (uint32_t)kTWBytes + 2u * half_rows * 128u;
       const int hf = (int)rank;
@@ -723,6 +726,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             uint8_t* sw = stages + stage * C::kStage;
             uint8_t* sb = sw + kTWBytes;
             const uint8_t* blk = wsrc + (int64_t)c * kWBlockBytes;
+            stage_n[stage] = (int32_t)n_pair;   // released to the MMA thread by the arrive below
             mbar_arrive_expect_tx(&full[stage], tx);
             if (kGated) {
               tma_load_1d(sw, blk + hf * 4096, 4096, &full[stage]);
@@ -773,8 +777,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (k >= (uint32_t)C::kNBuf &&
             !mbar_wait(&accempty[buf], (k / C::kNBuf - 1) & 1u, a.err))
           break;
-        const int32_t tau = (int32_t)(item / a.F);
-        const uint32_t idesc = idesc_bf16_f32(256, (int)pair_n<BN>(a, tau));
         const uint32_t d = tmem + buf * (uint32_t)BN;
         for (int c = 0; c < a.C; ++c) {
           // both CTAs' decoders have stored this chunk's A (after their own
@@ -784,6 +786,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             break;
           }
           tc_fence_after();
+          const uint32_t idesc = idesc_bf16_f32(256, stage_n[stage]);
           const uint32_t sb = smem_u32(stages + stage * C::kStage + kTWBytes);
           const uint32_t abase = tmem + (uint32_t)(C::kABase + astage * 64);
 #pragma unroll
