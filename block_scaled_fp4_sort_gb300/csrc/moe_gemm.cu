@@ -269,7 +269,11 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
   }
 }
 
-template <int BN, int EPI>
+// ADAPT: size each item's MMA to its tile's valid slots (and load only
+// those activation rows); without it every MMA is BN wide.  The host picks
+// ADAPT when tiles are often partly filled: the per-item width costs a few
+// percent on problems whose tiles are all full.
+template <int BN, int EPI, bool ADAPT>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap,
                     const __grid_constant__ CUtensorMap bmap_part) {
@@ -336,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       // both plan entries loaded together (one memory latency per item); the
       // valid count reaches the MMA thread through shared memory with each stage
-      const int32_t e_raw = a.tile_expert[tau], mn_raw = a.tile_mn[tau];
+      const int32_t e_raw = a.tile_expert[tau];
+      const int32_t mn_raw = ADAPT || gather ? a.tile_mn[tau] : tau * BN + BN;
       int32_t e = e_raw;
       if (e < 0 || e >= a.EL) {
         set_error(a.err, kErrDevice);
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
-      const int32_t nbox = BN > kPartRows && nv <= BN - kPartRows ? (nv + kPartRows - 1) / kPartRows : 0;
+      const int32_t nbox = ADAPT && BN > kPartRows && nv <= BN - kPartRows ? (nv + kPartRows - 1) / kPartRows : 0;
       const uint32_t btx = gather     ? (uint32_t)nq * 2u * 512u
                            : nbox > 0 ? 2u * (uint32_t)nbox * kPartRows * 128u
                                       : (uint32_t)C::kBBytes;
@@ -369,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // decoders start on them while the activation tile is in flight
             mbar_arrive_expect_tx(&wfull[stage], (uint32_t)kWBlockBytes);
             tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &wfull[stage]);
-            stage_nv[stage] = nv;   // released to the MMA thread by the arrive below
+            if (ADAPT) stage_nv[stage] = nv;   // released to the MMA thread by the arrive below
             mbar_arrive_expect_tx(&full[stage], btx);
 #pragma unroll
             for (int at = 0; at < 2; ++at) {
@@ -425,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           // the MMA width: this tile's valid slots rounded up to 16
-          const uint32_t kIdesc = idesc_bf16_f32(128, (stage_nv[stage] + 15) & ~15);
+          const uint32_t kIdesc =
+              ADAPT ? idesc_bf16_f32(128, (stage_nv[stage] + 15) & ~15) : idesc_bf16_f32(128, BN);
           const uint32_t sb = smem_u32(stages + stage * C::kStage + kWBlockBytes);
 #pragma unroll
           for (int tile = 0; tile < 2; ++tile) {
@@ -1824,7 +1830,7 @@ cudaError_t launch_native_bn(const Shape& s, const GemmLaunch& g, cudaStream_t s
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool ADAPT>
 cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
   using Cf = Cfg<BN>;
   GemmArgs a = {};
@@ -1856,7 +1862,7 @@ cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool 
   if (!make_act_map(&map, g.act, g.act_rows, Kdim, g.gather_rows ? 1 : BN) ||
       !make_act_map(&map_part, g.act, g.act_rows, Kdim, BN < 32 ? BN : 32))
     return cudaErrorInvalidValue;
-  auto kern = moe_gemm_kernel<BN, EPI>;
+  auto kern = moe_gemm_kernel<BN, EPI, ADAPT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
@@ -1873,17 +1879,39 @@ cudaError_t launch_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool 
   return cudaLaunchKernelEx(&cfg, kern, a, map, map_part);
 }
 
+// Partly filled tiles are common when the average routes per local expert
+// is below four tiles: then the per-item MMA width pays
+inline bool adaptive_width(const Shape& s) { return s.R < 4 * s.T * s.EL; }
+
+template <int BN, int EPI>
+cudaError_t launch_ad(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  return adaptive_width(s) ? launch_t<BN, EPI, true>(s, g, st, pdl)
+                           : launch_t<BN, EPI, false>(s, g, st, pdl);
+}
+
+// Route tile 16 reaches this kernel only for packed activations (w4a4 and
+// w4a8; BF16 ones take the warp-MMA kernel), and w4a4 with tiles of 32 or more
+// takes the native NVFP4 kernel: only the reachable epilogues are built.
 template <int BN>
 cudaError_t launch_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  if (BN == 16) {
+    switch (g.epi) {
+      case kEpiSwigluNvfp4: return launch_t<BN, kEpiSwigluNvfp4, false>(s, g, st, pdl);
+      case kEpiRelu2Nvfp4: return launch_t<BN, kEpiRelu2Nvfp4, false>(s, g, st, pdl);
+      case kEpiSwigluMxfp8: return launch_t<BN, kEpiSwigluMxfp8, false>(s, g, st, pdl);
+      case kEpiRelu2Mxfp8: return launch_t<BN, kEpiRelu2Mxfp8, false>(s, g, st, pdl);
+      case kEpiPlainBf16: return launch_t<BN, kEpiPlainBf16, false>(s, g, st, pdl);
+      case kEpiAtomicFinal: return launch_t<BN, kEpiAtomicFinal, false>(s, g, st, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (g.epi) {
-    case kEpiSwigluBf16: return launch_t<BN, kEpiSwigluBf16>(s, g, st, pdl);
-    case kEpiSwigluNvfp4: return launch_t<BN, kEpiSwigluNvfp4>(s, g, st, pdl);
-    case kEpiPlainBf16: return launch_t<BN, kEpiPlainBf16>(s, g, st, pdl);
-    case kEpiAtomicFinal: return launch_t<BN, kEpiAtomicFinal>(s, g, st, pdl);
-    case kEpiRelu2Bf16: return launch_t<BN, kEpiRelu2Bf16>(s, g, st, pdl);
-    case kEpiRelu2Nvfp4: return launch_t<BN, kEpiRelu2Nvfp4>(s, g, st, pdl);
-    case kEpiSwigluMxfp8: return launch_t<BN, kEpiSwigluMxfp8>(s, g, st, pdl);
-    case kEpiRelu2Mxfp8: return launch_t<BN, kEpiRelu2Mxfp8>(s, g, st, pdl);
+    case kEpiSwigluBf16: return launch_ad<BN, kEpiSwigluBf16>(s, g, st, pdl);
+    case kEpiPlainBf16: return launch_ad<BN, kEpiPlainBf16>(s, g, st, pdl);
+    case kEpiAtomicFinal: return launch_ad<BN, kEpiAtomicFinal>(s, g, st, pdl);
+    case kEpiRelu2Bf16: return launch_ad<BN, kEpiRelu2Bf16>(s, g, st, pdl);
+    case kEpiSwigluMxfp8: return launch_ad<BN, kEpiSwigluMxfp8>(s, g, st, pdl);
+    case kEpiRelu2Mxfp8: return launch_ad<BN, kEpiRelu2Mxfp8>(s, g, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
