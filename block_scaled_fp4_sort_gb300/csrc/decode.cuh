@@ -144,9 +144,30 @@ __host__ __device__ constexpr uint32_t frag_half_offset(uint32_t w, uint32_t lan
   return (w * 32u + lane) * 32u + ((h ^ ((lane >> 2) & 1u)) * 16u);
 }
 
-// byte offset, inside a prepared block's data region, of 16-byte chunk q of row r
+// byte offset, inside a 128-row code region, of 16-byte chunk q of row r
 __host__ __device__ constexpr uint32_t prep_chunk_offset(uint32_t r, uint32_t q) {
   return r * 64u + ((q ^ ((r >> 1) & 3u)) * 16u);
+}
+
+// Row-order prepared blocks (256 rows x 128 K elements) are two contiguous
+// 128-row halves of kPrepHalfBytes, each [128 rows x 64 code bytes | 128 rows
+// x 8 scale codes], so that one copy fetches a half.  Half h of a gated FC1
+// block holds gate rows 64h..64h+63 (local rows 0..63) and the matching up
+// rows (local rows 64..127); otherwise half h holds rows 128h..128h+127.
+// Block row r counts as before: gated, r < 128 is gate feature r and r >= 128
+// up feature r - 128 of the block's 128 features.
+constexpr uint32_t kPrepHalfBytes = 9216;
+__host__ __device__ constexpr uint32_t prep_half(bool gated, uint32_t r) {
+  return gated ? (r & 127u) >> 6 : r >> 7;
+}
+__host__ __device__ constexpr uint32_t prep_local(bool gated, uint32_t r) {
+  return gated ? ((r >> 7) << 6) | (r & 63u) : (r & 127u);
+}
+__host__ __device__ constexpr uint32_t prep_code_offset(bool gated, uint32_t r, uint32_t q) {
+  return prep_half(gated, r) * kPrepHalfBytes + prep_chunk_offset(prep_local(gated, r), q);
+}
+__host__ __device__ constexpr uint32_t prep_scale_offset(bool gated, uint32_t r) {
+  return prep_half(gated, r) * kPrepHalfBytes + 8192u + prep_local(gated, r) * 8u;
 }
 
 }  // namespace fp4moe

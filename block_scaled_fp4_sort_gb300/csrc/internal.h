@@ -11,8 +11,9 @@ namespace fp4moe {
 // ---- prepared weight layout (see prepare.cu) ----
 // A work item covers 256 weight rows (two 128-row MMA tiles) and the whole K
 // range in chunks of kBK elements.  One (expert, row block, K chunk) block is
-// kWBlockBytes contiguous bytes: 256 rows x 64 bytes of bit-permuted E2M1
-// codes, then 256 rows x 8 E4M3 scale bytes.
+// kWBlockBytes contiguous bytes: two 128-row halves, each 128 rows x 64 bytes
+// of bit-permuted E2M1 codes, then 128 rows x 8 scale codes (decode.cuh:
+// prep_code_offset, prep_scale_offset).
 constexpr int kBK = 128;
 constexpr int kRowsPerItem = 256;
 constexpr int kWDataBytes = kRowsPerItem * kBK / 2;     // 16384

@@ -278,6 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap,
                     const __grid_constant__ CUtensorMap bmap_part) {
   using C = Cfg<BN>;
+  // gated FC1 blocks pair gate and up rows in each prepared half
+  constexpr bool kGatedW = EPI == kEpiSwigluBf16 || EPI == kEpiSwigluNvfp4 || EPI == kEpiSwigluMxfp8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -494,8 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t r = (uint32_t)(tile * 128 + row);
         uint4 dv[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) dv[q] = *reinterpret_cast<const uint4*>(blk + prep_chunk_offset(r, q));
-        const uint2 sv = *reinterpret_cast<const uint2*>(blk + kWDataBytes + r * 8);
+        for (int q = 0; q < 4; ++q) dv[q] = *reinterpret_cast<const uint4*>(blk + prep_code_offset(kGatedW, r, q));
+        const uint2 sv = *reinterpret_cast<const uint2*>(blk + prep_scale_offset(kGatedW, r));
         uint32_t o[64];
 #pragma unroll
         for (int sblk = 0; sblk < 8; ++sblk) {
@@ -619,8 +621,12 @@ __device__ __forceinline__ void t_epilogue_chunk(const GemmArgs& a, const uint32
 // barriers; the decoders of both CTAs arrive on rank 0's A-stage barriers and
 // the epilogue warps of both on rank 0's accumulator-free barriers (remote
 // arrivals, release at cluster scope); rank 0's commits arrive on the stage
-// and accumulator barriers of both CTAs (multicast).  N is the tile's valid
-// slot count rounded up to 32 (16 activation rows per CTA and copy).
+// and accumulator barriers of both CTAs (multicast).  Each stage has separate
+// barriers for its weight half (the decoders wait on it) and its activation
+// half (rank 0's MMA thread waits on its own and, through a relay arrival from
+// rank 1, on its peer's), so that decode overlaps the activation copy.  N is
+// the tile's valid slot count rounded up to 32 (16 activation rows per CTA
+// and copy, or one copy of 128 rows for a full tile).
 // ===========================================================================
 constexpr int kPBox = 16;   // activation rows per tensor copy (per CTA: N / 2 rows)
 constexpr int kPDecWarps = 8;    // warps 0-7: decode, lane quarter w % 4, K half w / 4
@@ -640,11 +646,11 @@ struct PCfg {
   static constexpr int kABase = 256;
   static constexpr int kCols = BN / 4 >= 16 ? BN / 4 : 16;
   static constexpr int kGroups = BN / kCols;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes;
   static_assert(kStage % 1024 == 0, "stage alignment");
   static_assert(kStages >= 2 && kStages >= kAStages, "pipeline depth");
-  static_assert((2 * kStages + kAStages + 5) * 8 + 8 + 4 * kStages <= kBarBytes, "barrier region");
+  static_assert((4 * kStages + kAStages + 5) * 8 + 8 + 4 * kStages <= kBarBytes, "barrier region");
   static_assert(kABase + kAStages * 64 <= 512, "tensor memory");
   static_assert(kNBuf * BN <= kABase, "accumulators");
   static_assert(kSmem <= 227 * 1024, "shared memory");
@@ -663,9 +669,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);   // activation half
   uint64_t* empty = full + C::kStages;
-  uint64_t* afull = empty + C::kStages;      // rank 0's: both CTAs' decoders
+  uint64_t* wfull = empty + C::kStages;      // weight half
+  uint64_t* bready = wfull + C::kStages;     // rank 0's: rank 1's activation half has landed
+  uint64_t* afull = bready + C::kStages;     // rank 0's: both CTAs' decoders
   uint64_t* accfull = afull + C::kAStages;   // [2]
   uint64_t* accempty = accfull + 2;          // [2] rank 0's: both CTAs' epilogue warps
   uint64_t* drain = accempty + 2;
@@ -678,6 +686,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
+      mbar_init(&wfull[i], 1);
+      mbar_init(&bready[i], 1);
     }
     for (int i = 0; i < C::kAStages; ++i) mbar_init(&afull[i], 2 * kPDecWarps);
     for (int b = 0; b < 2; ++b) {
@@ -732,17 +742,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
             uint8_t* sw = stages + stage * C::kStage;
             uint8_t* sb = sw + kTWBytes;
             const uint8_t* blk = wsrc + (int64_t)c * kWBlockBytes;
+            // this CTA's half of the prepared block: one contiguous copy, on a
+            // barrier of its own so that decode overlaps the activation copy
+            mbar_arrive_expect_tx(&wfull[stage], (uint32_t)kPrepHalfBytes);
+            tma_load_1d(sw, blk + hf * kPrepHalfBytes, kPrepHalfBytes, &wfull[stage]);
             stage_n[stage] = (int32_t)n_pair;   // released to the MMA thread by the arrive below
-            mbar_arrive_expect_tx(&full[stage], tx);
-            if (kGated) {
-              tma_load_1d(sw, blk + hf * 4096, 4096, &full[stage]);
-              tma_load_1d(sw + 4096, blk + 8192 + hf * 4096, 4096, &full[stage]);
-              tma_load_1d(sw + kTWCodes, blk + kWDataBytes + hf * 512, 512, &full[stage]);
-              tma_load_1d(sw + kTWCodes + 512, blk + kWDataBytes + 1024 + hf * 512, 512, &full[stage]);
-            } else {
-              tma_load_1d(sw, blk + hf * kTWCodes, kTWCodes, &full[stage]);
-              tma_load_1d(sw + kTWCodes, blk + kWDataBytes + hf * 1024, 1024, &full[stage]);
-            }
+            mbar_arrive_expect_tx(&full[stage], tx - (uint32_t)kPrepHalfBytes);
             // a full tile's half in one copy per K atom (each copy instruction
             // costs about as much issue time as a tenth of the chunk's MMAs);
             // a partly filled tile in copies of 16 rows
@@ -771,10 +776,35 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
     if (lane == 0)
       for (int q = 0; q < C::kStages; ++q)
-        if (issued_mask & (1u << q)) mbar_wait(&full[q], (issued_parity >> q) & 1u, a.err);
+        if (issued_mask & (1u << q)) {
+          mbar_wait(&wfull[q], (issued_parity >> q) & 1u, a.err);
+          mbar_wait(&full[q], (issued_parity >> q) & 1u, a.err);
+        }
+  } else if (warp == kPMmaWarp && rank == 1) {
+    // ------------------------------------------------------------ relay (rank 1)
+    // tells rank 0's MMA thread, chunk by chunk, that this CTA's activation
+    // half has landed (the MMA reads it from here)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t item = cid; item < n_items && ok; item += ncl) {
+        for (int c = 0; c < a.C; ++c) {
+          if (!mbar_wait(&full[stage], phase, a.err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(mapa_shared(&bready[stage], 0));
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
   } else if (warp == kPMmaWarp) {
     // ------------------------------------------------------------ MMA issuer (rank 0)
-    if (rank == 0 && lane == 0) {
+    if (lane == 0) {
       int stage = 0, astage = 0;
       uint32_t phase = 0, aphase = 0, k = 0;
       bool ok = true;
@@ -785,9 +815,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
           break;
         const uint32_t d = tmem + buf * (uint32_t)BN;
         for (int c = 0; c < a.C; ++c) {
-          // both CTAs' decoders have stored this chunk's A (after their own
-          // copies, activation halves included, had landed)
-          if (!mbar_wait(&afull[astage], aphase, a.err)) {
+          // both CTAs' decoders have stored this chunk's A, and both
+          // activation halves have landed (this CTA's, and the peer's as relayed)
+          if (!mbar_wait(&afull[astage], aphase, a.err) || !mbar_wait(&full[stage], phase, a.err) ||
+              !mbar_wait(&bready[stage], phase, a.err)) {
             ok = false;
             break;
           }
@@ -829,7 +860,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     bool ok = true;
     for (int64_t item = cid; item < n_items && ok; item += ncl) {
       for (int c = 0; c < a.C; ++c) {
-        bool good = mbar_wait(&full[stage], phase, a.err);
+        bool good = mbar_wait(&wfull[stage], phase, a.err);
         if (qd >= (uint32_t)C::kAStages) {
           const uint32_t qp = qd - (uint32_t)C::kAStages;
           good = good && mbar_wait(&empty[qp % C::kStages], (qp / C::kStages) & 1u, a.err);

@@ -5,15 +5,17 @@
 // take, cute_dsl_fused_moe, localized_weights).  Lossless bit re-encoding:
 // every decoded weight equals e2m1(code) * e4m3(scale) bit for bit.
 //
-// Block (e, f, c) = 256 weight rows x 128 K elements, contiguous:
-//   [0, 16384)      row r: 64 bytes = 16 prepared words, 16-byte chunks
-//                   XOR-swizzled by (r >> 1) & 3 (conflict-free 128-bit
-//                   shared-memory reads when thread r reads row r)
-//   [16384, 18432)  row r: the 8 scale codes of its 128 elements
-//                   (decode.cuh: prep_scale_code; the scale's sign and zero
-//                   are moved into the codes by prep_fix_codes)
-// GEMM1 (which = 1): rows 0..127 are gate rows 128f.., rows 128..255 the up
-// rows I+128f..; GEMM2 (which = 2): rows 256f.. of w2, zero past H.
+// Block (e, f, c) = 256 weight rows x 128 K elements, contiguous, as two
+// 128-row halves (decode.cuh: prep_code_offset, prep_scale_offset), each
+//   128 rows x 64 bytes = 16 prepared words per row, 16-byte chunks
+//                   XOR-swizzled by (local row >> 1) & 3 (conflict-free
+//                   128-bit shared-memory reads when thread r reads row r)
+//   128 rows x 8 scale codes of their 128 elements (decode.cuh:
+//                   prep_scale_code; the scale's sign and zero are moved
+//                   into the codes by prep_fix_codes)
+// GEMM1 (which = 1): block rows 0..127 are gate rows 128f.., 128..255 the up
+// rows I+128f..; half h holds gate rows 64h.. and their up rows.  GEMM2
+// (which = 2): rows 256f.. of w2, zero past H; half h holds rows 128h..
 // Decode-size problems store the code bytes in MMA fragment order instead
 // (decode.cuh, frag_half_offset); the scale region is the same.
 #include <algorithm>
@@ -62,6 +64,7 @@ __device__ uint32_t block_scale_byte(const PrepArgs& a, int64_t e, int64_t row, 
 
 // one thread per (block, row)
 __global__ void prepare_kernel(PrepArgs a) {
+  const bool gated1 = a.which == 1 && a.gated;
   const int64_t n = a.EL * a.F * a.C * kRowsPerItem;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -85,12 +88,12 @@ __global__ void prepare_kernel(PrepArgs a) {
           v[i] = prep_permute_word(prep_fix_codes(src[word], b, 0x88888888u));
         }
       }
-      *reinterpret_cast<uint4*>(dst + prep_chunk_offset((uint32_t)r, q)) = make_uint4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<uint4*>(dst + prep_code_offset(gated1, (uint32_t)r, q)) = make_uint4(v[0], v[1], v[2], v[3]);
     }
     uint32_t codes[2] = {0, 0};
 #pragma unroll
     for (int i = 0; i < 8; ++i) codes[i >> 2] |= block_scale_code(a, e, sr, c, i) << (8 * (i & 3));
-    *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = make_uint2(codes[0], codes[1]);
+    *reinterpret_cast<uint2*>(dst + prep_scale_offset(gated1, (uint32_t)r)) = make_uint2(codes[0], codes[1]);
   }
 }
 
@@ -174,6 +177,7 @@ __global__ void debug_decode_fragment_kernel(PrepArgs a) {
 
 // Decode prepared blocks exactly as the GEMMs do, then undo the 2^-8.
 __global__ void debug_decode_kernel(PrepArgs a) {
+  const bool gated1 = a.which == 1 && a.gated;
   const int64_t n = a.EL * a.F * a.C * kRowsPerItem;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -183,11 +187,11 @@ __global__ void debug_decode_kernel(PrepArgs a) {
     const int64_t sr = src_row(a, f, r);
     if (sr < 0) continue;
     const uint8_t* b = a.prep + blk * kWBlockBytes;
-    const uint2 sv = *reinterpret_cast<const uint2*>(b + kWDataBytes + r * 8);
+    const uint2 sv = *reinterpret_cast<const uint2*>(b + prep_scale_offset(gated1, (uint32_t)r));
     const uint32_t sbytes[2] = {sv.x, sv.y};
     uint16_t* out = a.dbg_out + (e * a.rows_src + sr) * a.K + c * kBK;
     for (int q = 0; q < 4; ++q) {
-      const uint4 v = *reinterpret_cast<const uint4*>(b + prep_chunk_offset((uint32_t)r, q));
+      const uint4 v = *reinterpret_cast<const uint4*>(b + prep_code_offset(gated1, (uint32_t)r, q));
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       for (int k = 0; k < 4; ++k) {
         const int word = 4 * q + k;                 // elements 8*word .. 8*word+7
