@@ -242,9 +242,18 @@ def stored_traffic(workload):
     return ent.get("dram_bytes_per_launch"), ent.get("source")
 
 
+def mma_dtype(cfg, T, native):
+    """Operand type of GEMM1's MMAs: the decode-size w4a16 kernel multiplies
+    FP16 (hardware E2M1 -> FP16 decode, activations as FP16 rows with a
+    power-of-two scale each), the other w4a16 / expanded kernels BF16."""
+    if native:
+        return "nvfp4"
+    return "f16" if cfg.mode == "w4a16" and T <= 16 else "bf16"
+
+
 def gemm1_kernel_name(cfg, T, native):
     if cfg.mode == "w4a16" and T <= 16:
-        return "moe_gemv_kernel (GEMM1 + SwiGLU, warp MMA)"
+        return "moe_gemv_kernel (GEMM1 + SwiGLU, warp MMA, f16)"
     if native:
         return "moe_gemm_nvfp4_kernel<%d> (GEMM1 + SwiGLU, tcgen05 kind::mxf4nvf4)" % T
     return "moe_gemm_kernel<%d> (GEMM1 + SwiGLU, tcgen05 kind::f16)" % T
@@ -477,7 +486,7 @@ def measure(cfg, args, rank, world, local, dev, headline):
     step_bytes = touched * (w1_bytes_per_expert + w2_bytes_per_expert) + act1 + M * H * 2
     traffic, traffic_src = stored_traffic(cfg.name)
     g2_ms = kernels["gemm2"]
-    roof = {"kernel": gemm1_kernel_name(cfg, T, native), "mma_dtype": "nvfp4" if native else "bf16"}
+    roof = {"kernel": gemm1_kernel_name(cfg, T, native), "mma_dtype": mma_dtype(cfg, T, native)}
     if tensor_bound:
         roof.update({"bound": "tensor", "achieved": achieved_tf, "peak": mma_peak,
                      "unit": "TFLOP/s", "frac": achieved_tf / mma_peak,
@@ -505,7 +514,7 @@ def measure(cfg, args, rank, world, local, dev, headline):
         "metric": METRIC, "value": tokens_per_s(world, cfg.M, ms), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": ("nvfp4" if native else
+        "dtype": ("nvfp4" if native else "f16" if mma_dtype(cfg, T, native) == "f16" else
                   {"w4a16": "bf16", "w4a4": "nvfp4->bf16", "w4a8": "mxfp8->bf16"}[cfg.mode]),
         "data": "synthetic (seeded generator; random NVFP4 weights)",
         "config": dict(workload_config(cfg, T), l2="inputs larger than L2: %.2f GB of weights "
@@ -756,7 +765,7 @@ def run_ep(args, rank, world, local):
         "metric": METRIC, "value": cfg.M / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
-        "dtype": "bf16" if cfg.mode == "w4a16" else cfg.mode,
+        "dtype": mma_dtype(cfg, T, False) if cfg.mode == "w4a16" else cfg.mode,
         "data": "synthetic (seeded generator; random NVFP4 weights)",
         "config": dict(workload_config(cfg, T), parallelism="ep%d" % world,
                        experts_per_rank=[expert_range(cfg.E, world, r)[1] for r in range(world)],

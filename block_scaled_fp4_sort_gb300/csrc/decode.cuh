@@ -123,6 +123,42 @@ __device__ __forceinline__ void decode_word_frag(uint32_t w, uint32_t sc0, uint3
   o[3] = bf16x2_mul(r3, sc1);
 }
 
+// FP16 fragment decode (decode-size kernel).  A prepared fragment word holds
+// the four bytes of a lane's m16n8k16 A fragment for one K step, two E2M1
+// codes per byte (low nibble = the lower K element), the block scales' sign
+// and zero already moved into the codes; the hardware conversion
+// (cvt.rn.f16x2.e2m1x2) turns a byte into the exact f16x2 pair, and one
+// f16x2 multiply by the row's block scale (an E4M3 magnitude, also exact in
+// f16: every e2m1 * e4m3 product has at most 6 significant bits and lies in
+// [2^-10, 2688]) gives the weights.  Bytes 0 and 2 belong to row R0, 1 and 3
+// to row R1 = R0 + 8.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t w, int byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(r)
+      : "r"(w >> (8 * byte)));
+  return r;
+}
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// an E4M3 scale magnitude byte (bits 0..7 of b) -> f16x2 (scale, scale)
+__device__ __forceinline__ uint32_t e4m3_to_f16x2_dup(uint32_t b) {
+  uint32_t r;
+  const uint16_t pair = (uint16_t)((b & 0xFFu) * 0x101u);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+  return r;
+}
+__device__ __forceinline__ void decode_word_frag_f16(uint32_t w, uint32_t s0, uint32_t s1,
+                                                     uint32_t* o) {
+  o[0] = f16x2_mul(e2m1x2_to_f16x2(w, 0), s0);
+  o[1] = f16x2_mul(e2m1x2_to_f16x2(w, 1), s1);
+  o[2] = f16x2_mul(e2m1x2_to_f16x2(w, 2), s0);
+  o[3] = f16x2_mul(e2m1x2_to_f16x2(w, 3), s1);
+}
+
 // Fragment layout (decode-size kernel): fragment slot w (0..15) holds block
 // rows 16w..16w+15; lane l (g = l/4, t = l%4) owns rows R0 = 16w+g and
 // R1 = R0+8 and, for each 16-element K step kk, one prepared word holding

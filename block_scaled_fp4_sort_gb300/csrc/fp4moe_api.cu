@@ -112,13 +112,19 @@ RouteWs route_ws(const Shape& s) {
   return w;
 }
 
-// staged GEMM workspace: header | BF16 activations in slot order (w4a4, or
-// gathered rows for the tcgen05 GEMM) | warp-MMA K-split scratch
+// staged GEMM workspace: header | activations in slot order (w4a4 / w4a8
+// expanded to BF16, gathered rows for the tcgen05 GEMM, FP16 rows and their
+// scales for the warp-MMA GEMM) | warp-MMA K-split scratch
+size_t f16_scale_offset(const Shape& s, int which) {
+  return kWsHeader + up((size_t)s.S * (which == 1 ? s.H : s.I) * 2);
+}
 size_t gemm_split_offset(const Shape& s, int which) {
   size_t b = kWsHeader;
-  if (s.mode != FP4MOE_W4A16 || (which == 1 && !fragment_layout(s))) {
+  const int64_t K = which == 1 ? s.H : s.I;
+  if (fragment_layout(s)) {
+    b = f16_scale_offset(s, which) + up((size_t)s.S * 4);
+  } else if (s.mode != FP4MOE_W4A16 || which == 1) {
     const int64_t rows = which == 1 ? std::max(s.M, s.S) : s.S;
-    const int64_t K = which == 1 ? s.H : s.I;
     b += up((size_t)rows * K * 2);
   }
   return up(b);
@@ -131,7 +137,9 @@ void* gemm_split(const Shape& s, int which, uint8_t* ws) {
 }
 
 struct FusedWs {
-  size_t e2p, p2e, tile_expert, tile_mn, num_tiles, route_scratch, h, h_sf, y, deq2, split, total;
+  size_t e2p, p2e, tile_expert, tile_mn, num_tiles, route_scratch, h, h_sf, y, deq2, split;
+  size_t x_scale, h16, h_scale;   // warp-MMA GEMMs: FP16 row scales of x and h, FP16 h
+  size_t total;
 };
 FusedWs fused_ws(const Shape& s) {
   FusedWs w = {};
@@ -153,8 +161,12 @@ FusedWs fused_ws(const Shape& s) {
   // fp32 route storage; until GEMM2 it holds x in slot order (BF16, 2 S H
   // bytes) for the tcgen05 GEMM1, in atomic mode the fp32 [M, H] accumulator
   w.y = o; o = up(o + (size_t)s.S * s.H * 4);
-  if (fragment_layout(s)) {                     // K-split scratch, shared by GEMM1 and GEMM2
-    w.split = o; o = up(o + kSplitBytes);
+  if (fragment_layout(s)) {
+    w.split = o; o = up(o + kSplitBytes);     // K-split scratch, shared by GEMM1 and GEMM2
+    // FP16 x (in the y region) and h for the FP16 MMAs, with their row scales
+    w.x_scale = o; o = up(o + (size_t)s.S * 4);
+    w.h16 = o; o = up(o + (size_t)s.S * s.I * 2);
+    w.h_scale = o; o = up(o + (size_t)s.S * 4);
   }
   w.total = o;
   return w;
@@ -361,9 +373,12 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   // The tcgen05 GEMM reads plain row tiles: gathered rows are first written in
   // slot order (its TMA four-row gather needs one instruction per four rows,
-  // which limited GEMM1 at large tiles); the decode-size kernel gathers itself.
-  const bool slot_order = gather_rows != nullptr && !fragment_layout(s);
+  // which limited GEMM1 at large tiles); the decode-size kernel reads FP16
+  // rows in slot order with a power-of-two scale per row.
+  const bool frag = fragment_layout(s);
+  const bool slot_order = gather_rows != nullptr && !frag;
   const bool native = native_fp4(s, 1);
+  float* f16_scale = frag ? reinterpret_cast<float*>(ws + f16_scale_offset(s, 1)) : nullptr;
   const void* act = a;
   const uint8_t* act_sf = nullptr;
   cudaError_t e = cudaSuccess;
@@ -383,8 +398,13 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   } else if (slot_order) {
     e = launch_permute(s, a, nullptr, gather_rows, num_tiles, ws + kWsHeader, nullptr, cs, false);
     act = ws + kWsHeader;
+  } else if (frag) {
+    e = launch_to_f16(a, act_rows, s.H, s.H, gather_rows, s.K, tile_mn, num_tiles, s.T, s.S,
+                      ws + kWsHeader, f16_scale, cs, false);
+    act = ws + kWsHeader;
   }
   if (e != cudaSuccess) return FP4MOE_ERR_CUDA;
+  const bool in_slots = slot_order || native || frag;   // act is in slot order now
   GemmLaunch g = {};
   g.which = 1;
   g.epi = gemm1_epilogue(s);
@@ -393,10 +413,11 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   g.tile_expert = tile_expert;
   g.tile_mn = tile_mn;
   g.num_tiles = num_tiles;
-  g.gather_rows = slot_order || native ? nullptr : gather_rows;
+  g.gather_rows = in_slots ? nullptr : gather_rows;
   g.act = act;
   g.act_sf = act_sf;
-  g.act_rows = slot_order || native ? s.S : act_rows;
+  g.act_rows = in_slots ? s.S : act_rows;
+  g.slot_scale = f16_scale;
   g.out = h;
   g.out_sf = h_sf;
   g.fc2_scale = fc2_input_scale;
@@ -404,7 +425,7 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   g.p2e = gather_rows;
   g.split = gemm_split(s, 1, ws);
   g.err = err_word(ws);
-  return cuda_status(launch_gemm(s, g, cs, w4 || slot_order));
+  return cuda_status(launch_gemm(s, g, cs, w4 || slot_order || frag));
 }
 
 fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h_sf,
@@ -424,7 +445,15 @@ fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const void* act = h;
   const uint8_t* act_sf = nullptr;
-  if (native_fp4(s, 2)) {
+  const bool frag = fragment_layout(s);
+  float* f16_scale = frag ? reinterpret_cast<float*>(ws + f16_scale_offset(s, 2)) : nullptr;
+  if (frag) {
+    // FP16 rows with a power-of-two scale per row for the decode-size kernel
+    act = ws + kWsHeader;
+    if (launch_to_f16(h, s.S, s.I, s.I, nullptr, 1, tile_mn, num_tiles, s.T, s.S, ws + kWsHeader,
+                      f16_scale, cs, false) != cudaSuccess)
+      return FP4MOE_ERR_CUDA;
+  } else if (native_fp4(s, 2)) {
     // h as given, copied with every scale's sign moved into its codes
     Shape hs = s;
     hs.H = s.I;
@@ -453,9 +482,10 @@ fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h
   g.act_sf = act_sf;
   g.act_rows = s.S;
   g.out = y;
+  g.slot_scale = f16_scale;
   g.split = gemm_split(s, 2, ws);
   g.err = err_word(ws);
-  return cuda_status(launch_gemm(s, g, cs, w4));
+  return cuda_status(launch_gemm(s, g, cs, w4 || frag));
 }
 
 fp4moe_status moe_finalize(const fp4moe_problem* p, const void* y, const int32_t* e2p,
@@ -513,13 +543,19 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   // region, which GEMM2 overwrites only after GEMM1 has read it; padding rows
   // are left unwritten (no result of a padding slot is stored).  Plain row
   // tiles beat the TMA four-row gather in both GEMM kernels.
+  // Decode sizes (warp-MMA GEMMs): FP16 rows with a power-of-two scale per
+  // slot, for x here and for h before GEMM2.
   const void* xb = ws + L.y;
   const bool native1 = native_fp4(s, 1), native2 = native_fp4(s, 2);
+  const bool frag = fragment_layout(s);
+  float* xs = frag ? reinterpret_cast<float*>(ws + L.x_scale) : nullptr;
+  float* hs = frag ? reinterpret_cast<float*>(ws + L.h_scale) : nullptr;
   uint8_t* xsf = ws + L.y + up((size_t)s.S * s.H / 2);   // native: NVFP4 x scales
   if (e == cudaSuccess)
     e = native1 ? launch_permute(s, x, x_sf, p2e, nt, ws + L.y, xsf, cs, true, false, true)
         : w4    ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
                                       ws + L.y, cs, true, p2e, s.K, s.M, mx)
+        : frag  ? launch_to_f16(x, s.M, s.H, s.H, p2e, s.K, tm, nt, s.T, s.S, ws + L.y, xs, cs, true)
                 : launch_permute(s, x, nullptr, p2e, nt, ws + L.y, nullptr, cs, true, false);
   GemmLaunch g1 = {};
   g1.which = 1;
@@ -538,7 +574,8 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g1.fc2_scale = fc2_input_scale;
   g1.token_scale = per_token_scale;
   g1.p2e = p2e;
-  g1.split = fragment_layout(s) ? ws + L.split : nullptr;
+  g1.slot_scale = xs;
+  g1.split = frag ? ws + L.split : nullptr;
   g1.err = err;
   if (e == cudaSuccess) e = launch_gemm(s, g1, cs, true);
   const void* hin = ws + L.h;
@@ -546,6 +583,10 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
     e = launch_dequant_rows(ws + L.h, ws + L.h_sf, s.S, s.I, nt, s.T, ws + L.deq2, cs, true,
                             nullptr, 1, 0, mx);
     hin = ws + L.deq2;
+  }
+  if (e == cudaSuccess && frag) {
+    e = launch_to_f16(ws + L.h, s.S, s.I, s.I, nullptr, 1, tm, nt, s.T, s.S, ws + L.h16, hs, cs, true);
+    hin = ws + L.h16;
   }
   if (e == cudaSuccess && atomic) e = launch_seed_acc(s, out, accumulate ? 1 : 0, acc, cs, true);
   GemmLaunch g2 = {};
@@ -563,7 +604,8 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g2.p2e = p2e;
   g2.route_w = wts;
   g2.rsf = rsf;
-  g2.split = fragment_layout(s) ? ws + L.split : nullptr;
+  g2.slot_scale = hs;
+  g2.split = frag ? ws + L.split : nullptr;
   g2.err = err;
   if (e == cudaSuccess) e = launch_gemm(s, g2, cs, true);
   if (e == cudaSuccess)
@@ -658,10 +700,15 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
   const Shape s1 = domain_shape(s, 1), s2 = domain_shape(s, 2);
   const bool native1 = native_fp4(s1, 1), native2 = native_fp4(s2, 2);
   uint8_t* xsf = reinterpret_cast<uint8_t*>(y) + up((size_t)s.S * s.H / 2);
+  // decode sizes: FP16 x and h with power-of-two row scales (as in the fused path)
+  const bool frag = fragment_layout(s);
+  float* xs = frag ? reinterpret_cast<float*>(ws + L.f.x_scale) : nullptr;
+  float* hs = frag ? reinterpret_cast<float*>(ws + L.f.h_scale) : nullptr;
 
   DomainLock lock;
   cudaError_t e = cudaSuccess;
-  cudaEvent_t ev_start = nullptr, ev_fork = nullptr, ev_seed = nullptr, ev_fc1[2], ev_fc2[2];
+  cudaEvent_t ev_start = nullptr, ev_fork = nullptr, ev_seed = nullptr, ev_conv = nullptr;
+  cudaEvent_t ev_fc1[2], ev_fc2[2];
   {
     StreamCtxGuard g(cs);
     if (!g.ok()) return FP4MOE_ERR_CUDA;
@@ -676,6 +723,7 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
       e = native1 ? launch_permute(s, x, x_sf, p2e, nt, y, xsf, cs, true, false, true)
           : w4    ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
                                         y, cs, true, p2e, s.K, s.M, mx)
+          : frag  ? launch_to_f16(x, s.M, s.H, s.H, p2e, s.K, tm, nt, s.T, s.S, y, xs, cs, true)
                   : launch_permute(s, x, nullptr, p2e, nt, y, nullptr, cs, true, false);
     if (e == cudaSuccess && atomic && !side_seed)
       e = launch_seed_acc(s, out, accumulate ? 1 : 0, acc, cs, true);
@@ -719,7 +767,8 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
       g1.fc2_scale = fc2_input_scale;
       g1.token_scale = per_token_scale;
       g1.p2e = p2e;
-      g1.split = fragment_layout(s) ? ws + (d == 0 ? L.f.split : L.split2) : nullptr;
+      g1.slot_scale = xs;
+      g1.split = frag ? ws + (d == 0 ? L.f.split : L.split2) : nullptr;
       g1.grid_limit = loc->sm_count;
       g1.err = err;
       e = launch_gemm(s1, g1, ds[d], false);
@@ -729,9 +778,20 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
     }
     if (e == cudaSuccess) e = record_on(ds[d], kEvFc1 + d, &ev_fc1[d]);
   }
+  // decode sizes: h to FP16 once, on domain 0 after both FC1 shards
+  if (e == cudaSuccess && frag) {
+    e = wait_on(ds[0], ev_fc1[1]);
+    if (e == cudaSuccess) {
+      StreamCtxGuard g(ds[0]);
+      e = g.ok() ? launch_to_f16(ws + L.f.h, s.S, s.I, s.I, nullptr, 1, tm, nt, s.T, s.S,
+                                 ws + L.f.h16, hs, ds[0], false)
+                 : cudaErrorDeviceUninitialized;
+    }
+    if (e == cudaSuccess) e = record_on(ds[0], kEvConv, &ev_conv);
+  }
   // FC2 shard d -> output columns [d c2, (d+1) c2), after both FC1 shards
   for (int d = 0; d < 2 && e == cudaSuccess; ++d) {
-    e = wait_on(ds[d], ev_fc1[1 - d]);
+    e = frag ? (d == 0 ? cudaSuccess : wait_on(ds[d], ev_conv)) : wait_on(ds[d], ev_fc1[1 - d]);
     if (e == cudaSuccess && side_seed) e = wait_on(ds[d], ev_seed);
     if (e != cudaSuccess) break;
     {
@@ -748,7 +808,7 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
       g2.tile_expert = te;
       g2.tile_mn = tm;
       g2.num_tiles = nt;
-      g2.act = w4 && !native2 ? ws + L.f.deq2 : ws + L.f.h;
+      g2.act = frag ? ws + L.f.h16 : w4 && !native2 ? ws + L.f.deq2 : ws + L.f.h;
       g2.act_sf = native2 ? ws + L.f.h_sf : nullptr;
       g2.act_rows = s.S;
       g2.out = atomic ? acc + d * c2 : y + d * c2;
@@ -756,7 +816,8 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
       g2.p2e = p2e;
       g2.route_w = wts;
       g2.rsf = rsf;
-      g2.split = fragment_layout(s) ? ws + (d == 0 ? L.f.split : L.split2) : nullptr;
+      g2.slot_scale = hs;
+      g2.split = frag ? ws + (d == 0 ? L.f.split : L.split2) : nullptr;
       g2.grid_limit = loc->sm_count;
       g2.err = err;
       e = launch_gemm(s2, g2, ds[d], false);

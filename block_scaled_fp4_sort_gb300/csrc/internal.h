@@ -132,6 +132,15 @@ cudaError_t launch_dequant_rows(const uint8_t* q, const uint8_t* sf, int64_t row
 cudaError_t launch_debug_quantize_mx(const float* in, int64_t n, uint8_t* q, uint8_t* sf,
                                      cudaStream_t st);
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t st, bool pdl);
+// BF16 rows -> FP16 rows [rows, K] scaled by a power of two per row
+// (scale[row] = the factor to multiply back), for the decode-size GEMMs;
+// gather as in launch_permute (row s from source row gather[s] / top_k) or
+// null (row s); padding slots (gather < 0, or past tile_mn of their tile when
+// tile_mn is given) are skipped
+cudaError_t launch_to_f16(const void* src, int64_t src_rows, int64_t K, int64_t src_ld,
+                          const int32_t* gather, int64_t top_k, const int32_t* tile_mn,
+                          const int32_t* num_tiles, int64_t T, int64_t rows, void* out,
+                          float* scale, cudaStream_t st, bool pdl);
 cudaError_t launch_debug_quantize(const float* in, int64_t n, const float* scale, uint8_t* q,
                                   uint8_t* sf, cudaStream_t st);
 // one warp waits on an mbarrier nothing completes, bounded by limit_ns
@@ -169,6 +178,7 @@ struct GemmLaunch {
   const float* fc2_scale;      // [1]
   const float* token_scale;    // per_token_scale [M] (GEMM1) or null; needs p2e
   void* split;                 // warp-MMA K-split tail scratch (kSplitBytes, zero-filled once) or null
+  const float* slot_scale;     // warp-MMA kernel: FP16 activation row s was scaled by 1 / slot_scale[s]
   int64_t out_ld;              // output row stride in elements (0: I for GEMM1, H for GEMM2)
   int grid_limit;              // CTAs of the persistent grid at most (0: the device's SMs)
   // atomic finalize epilogue
@@ -198,7 +208,7 @@ class StreamCtxGuard {
 // of its own context), cached per context and slot; callers serialise
 // through domain_lock().
 constexpr int kEventSlots = 8;
-enum EventSlot { kEvStart = 0, kEvFork = 1, kEvSeed = 2, kEvFc1 = 3, kEvFc2 = 5 };  // Fc1/Fc2 + domain
+enum EventSlot { kEvStart = 0, kEvFork = 1, kEvSeed = 2, kEvFc1 = 3, kEvFc2 = 5, kEvConv = 7 };  // Fc1/Fc2 + domain
 cudaError_t stream_event(cudaStream_t st, int slot, cudaEvent_t* ev);
 void domain_lock();
 void domain_unlock();

@@ -72,6 +72,7 @@ struct GemmArgs {
   const int32_t* p2e;          // atomic finalize: route of each slot
   const float* route_w;        //   token_final_scales [M, top_k]
   float rsf;                   //   routed_scaling_factor
+  const float* slot_scale;     // warp-MMA kernel: FP16 activation row s is the BF16 row / slot_scale[s]
   int* err;
 };
 
@@ -1333,10 +1334,14 @@ __global__ void __launch_bounds__(kNThreads, 1)
 // for N <= 64 (79 with a commit in the stream, ~97 with concurrent TMEM
 // stores, measured on GB300), which caps a 16-column tile well below the HBM
 // rate.  This kernel keeps the TMA producer and the work items of the
-// tcgen05 kernel but multiplies on warp-level MMAs (mma.sync m16n8k16, BF16
+// tcgen05 kernel but multiplies on warp-level MMAs (mma.sync m16n8k16, FP16
 // in, fp32 accumulate): the prepared weights are stored in A-fragment order,
 // so one decoded 32-bit word is a lane's A fragment for one 16-element K step
-// and the decoded weights never leave registers.
+// and the decoded weights never leave registers.  FP16 because the hardware
+// E2M1 conversion produces FP16 (four conversions and four multiplies by the
+// block scale per eight weights, all exact); the activation rows arrive as
+// FP16 scaled by a power of two per slot (to_f16_rows), which the epilogue
+// multiplies back.
 //   warps 0-15  compute: warp w owns block rows 16w..16w+15 (GEMM1: warps
 //               0-7 gate rows, 8-15 the matching up rows); fp32 accumulators
 //               in registers over the whole K range (four chains, summed in a
@@ -1359,14 +1364,14 @@ struct GvCfg {
   static constexpr int kStages = 8;
   static constexpr int kBarBytes = 256;
   static constexpr int kXchgBytes = 128 * BN * 4;
-  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes + 4 * 128 + kXchgBytes;
+  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes + kXchgBytes;
   static_assert(kStage % 1024 == 0, "stage alignment");
 };
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                           uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -1394,10 +1399,10 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
     const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
     // one scale multiplier per row per atom: block 4a + t (fragment K order)
     const uint32_t sel = 0x4440u + ((uint32_t)lane & 3u);
-    const uint32_t sc0[2] = {scale_code_bf16x2(__byte_perm(sa.x, 0u, sel)),
-                             scale_code_bf16x2(__byte_perm(sa.y, 0u, sel))};
-    const uint32_t sc1[2] = {scale_code_bf16x2(__byte_perm(sb.x, 0u, sel)),
-                             scale_code_bf16x2(__byte_perm(sb.y, 0u, sel))};
+    const uint32_t sc0[2] = {e4m3_to_f16x2_dup(__byte_perm(sa.x, 0u, sel)),
+                             e4m3_to_f16x2_dup(__byte_perm(sa.y, 0u, sel))};
+    const uint32_t sc1[2] = {e4m3_to_f16x2_dup(__byte_perm(sb.x, 0u, sel)),
+                             e4m3_to_f16x2_dup(__byte_perm(sb.y, 0u, sel))};
     const uint8_t* bt = blk + kWBlockBytes;
     // per 64-element atom: decode its four words first, then their MMAs, so
     // that the four decode chains interleave
@@ -1405,7 +1410,7 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
     for (int at = 0; at < 2; ++at) {
       uint32_t af[4][4];
 #pragma unroll
-      for (int kq = 0; kq < 4; ++kq) decode_word_frag(words[4 * at + kq], sc0[at], sc1[at], af[kq]);
+      for (int kq = 0; kq < 4; ++kq) decode_word_frag_f16(words[4 * at + kq], sc0[at], sc1[at], af[kq]);
       const uint8_t* atom = bt + at * BN * 128;  // K 0..63 or 64..127
 #pragma unroll
       for (int kq = 0; kq < 4; ++kq) {
@@ -1557,8 +1562,7 @@ __global__ void __launch_bounds__(kGvThreads, 1)
   uint64_t* xready = empty + C::kStages;
   uint64_t* xfree = xready + 1;
   int32_t* last_flag = reinterpret_cast<int32_t*>(xfree + 1);
-  int32_t* gidx = reinterpret_cast<int32_t*>(smem + C::kStages * C::kStage + C::kBarBytes);
-  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kBarBytes + 4 * 128);
+  float* xchg = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kBarBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -1575,7 +1579,6 @@ __global__ void __launch_bounds__(kGvThreads, 1)
 
   grid_dependency_wait();
   const GvSchedule sch(a);
-  const bool gather = a.gather_rows != nullptr;
 
   if (warp == kGvWarps) {
     // ------------------------------------------------------------ producer
@@ -1585,17 +1588,6 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     auto produce = [&](int64_t item, int32_t c0, int32_t c1) -> bool {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       const int32_t e = plan_expert(a, tau);
-      // only the valid rows are gathered (see the tcgen05 producer)
-      const int32_t nq = gather ? (min(max(a.tile_mn[tau] - tau * BN, 0), BN) + 3) >> 2 : 0;
-      if (gather) {
-        __syncwarp();
-        if (lane < BN) {
-          const int32_t r = a.gather_rows[(int64_t)tau * BN + lane];
-          gidx[lane] = r >= 0 && r < a.R ? r / a.top_k : 0;
-        }
-        __syncwarp();
-      }
-      const uint32_t btx = gather ? (uint32_t)nq * 2u * 512u : (uint32_t)C::kBBytes;
       const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kWBlockBytes;
       for (int c = c0; c < c1; ++c) {
         bool ok = true;
@@ -1604,20 +1596,11 @@ __global__ void __launch_bounds__(kGvThreads, 1)
           if (ok) {
             uint8_t* sw = stages + stage * C::kStage;
             uint8_t* sb = sw + kWBlockBytes;
-            mbar_arrive_expect_tx(&full[stage], (uint32_t)kWBlockBytes + btx);
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWBlockBytes + C::kBBytes));
             tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &full[stage]);
 #pragma unroll
-            for (int at = 0; at < 2; ++at) {
-              const int32_t kc = c * kBK + at * 64;
-              uint8_t* dst = sb + at * BN * 128;
-              if (gather) {
-                for (int q = 0; q < nq; ++q)
-                  tma_gather4(dst + q * 512, &bmap, kc, gidx[4 * q], gidx[4 * q + 1],
-                              gidx[4 * q + 2], gidx[4 * q + 3], &full[stage]);
-              } else {
-                tma_load_2d(dst, &bmap, kc, tau * BN, &full[stage]);
-              }
-            }
+            for (int at = 0; at < 2; ++at)
+              tma_load_2d(sb + at * BN * 128, &bmap, c * kBK + at * 64, tau * BN, &full[stage]);
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -1687,12 +1670,18 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     // slower in this kernel, whose K loop runs at the 96-register limit
     auto finish = [&](int64_t item, const float (&raw)[2][4]) -> bool {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
-      const float scale = item_alpha(a, ItemPlan{0, a.tile_expert[tau]}) * 256.0f;  // undo the decode's 2^-8
+      const float alpha = item_alpha(a, ItemPlan{0, a.tile_expert[tau]});
+      const int32_t mn = a.tile_mn[tau];
       float d[2][4];
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d[nb][i] = raw[nb][i] * scale;
+        for (int i = 0; i < 4; ++i) {
+          // column s: the slot's power-of-two activation scale (padding
+          // columns, whose values are never stored, read none)
+          const int64_t s = (int64_t)tau * BN + 8 * nb + 2 * t + (i & 1);
+          d[nb][i] = raw[nb][i] * alpha * (s < mn ? a.slot_scale[s] : 0.0f);
+        }
       return gv_epilogue<BN, EPI>(a, tau, f, w, lane, r0, r1, d, xchg, xready, xfree, xphase);
     };
     bool ok = true;
@@ -2052,10 +2041,12 @@ cudaError_t launch_gv(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool
     a.split_cnt = static_cast<int32_t*>(g.split);
     a.part = reinterpret_cast<float*>(static_cast<uint8_t*>(g.split) + kSplitCountBytes);
   }
+  // FP16 activation rows in slot order, with their power-of-two scales
+  if (g.gather_rows != nullptr || g.slot_scale == nullptr) return cudaErrorInvalidValue;
+  a.slot_scale = g.slot_scale;
   const int64_t Kdim = g.which == 1 ? s.H : s.I;
   CUtensorMap map;
-  if (!make_act_map(&map, g.act, g.act_rows, Kdim, g.gather_rows ? 1 : BN))
-    return cudaErrorInvalidValue;
+  if (!make_act_map(&map, g.act, g.act_rows, Kdim, BN)) return cudaErrorInvalidValue;
   auto kern = moe_gemv_kernel<BN, EPI>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GvCfg<BN>::kSmem);

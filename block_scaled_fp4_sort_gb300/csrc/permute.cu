@@ -437,4 +437,82 @@ cudaError_t launch_debug_wait(uint64_t limit_ns, int* err, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// BF16 rows -> FP16 rows for the decode-size GEMMs' FP16 MMAs, one warp per
+// output row: each row is multiplied by a power of two 2^-e chosen so that its
+// largest finite magnitude lands in [2^14, 2^15) (e = floor(log2 max) - 14,
+// clamped to [-126, 126], which no finite BF16 row reaches from above and
+// only rows below 2^-112 from below; e = 0 for a row without a non-zero
+// finite value)
+// and rounded to FP16, and scale[row] = 2^e is stored for the GEMM's epilogue
+// to multiply back.  A finite BF16 value keeps all of its 8 significant bits
+// unless it lies below 2^-31 of the row's largest finite magnitude; infinities
+// and NaNs stay what they are.  Output row s comes from source row
+// gather[s] / top_k (gather = permuted_idx_to_expanded_idx) or from row s.
+// Padding slots (gather[s] < 0, or s at or past tile_mn[s / T] when tile_mn is
+// given) and rows at or past num_tiles * T are left unwritten: the GEMM's
+// column for a padding slot is never stored.
+__global__ void to_f16_rows(const uint4* __restrict__ src, int64_t src_rows, int64_t K8,
+                            int64_t src_ld8, const int32_t* __restrict__ gather, int top_k,
+                            const int32_t* __restrict__ tile_mn,
+                            const int32_t* __restrict__ num_tiles, int64_t T, int64_t rows,
+                            uint4* __restrict__ out, int64_t out_ld8, float* __restrict__ scale) {
+  grid_dependency_wait();
+  const int64_t lim = num_tiles ? min(rows, max((int64_t)num_tiles[0], (int64_t)0) * T) : rows;
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < lim; r += warps) {
+    int64_t sr = r;
+    if (gather) {
+      const int32_t g = gather[r];
+      sr = g >= 0 ? g / top_k : -1;
+    }
+    if (tile_mn && r >= tile_mn[r / T]) sr = -1;
+    if (sr < 0 || sr >= src_rows) continue;
+    const uint4* x = src + sr * src_ld8;
+    uint4* o = out + r * out_ld8;
+    float m = 0.0f;
+    for (int64_t c = lane; c < K8; c += 32) {
+      float v[8];
+      bf16x8_to_f32(x[c], v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float av = fabsf(v[k]);
+        if (av <= 3.4028235e38f) m = fmaxf(m, av);   // finite values only
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    int ex = 0;
+    if (m > 0.0f) {
+      frexpf(m, &ex);   // m = f 2^ex, f in [0.5, 1): floor(log2 m) = ex - 1
+      ex = min(max(ex - 15, -126), 126);
+    }
+    const float down = __int_as_float((127 - ex) << 23);   // 2^-ex, exact
+    for (int64_t c = lane; c < K8; c += 32) {
+      float v[8];
+      bf16x8_to_f32(x[c], v);
+      uint32_t h[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __half2 p = __floats2half2_rn(v[2 * k] * down, v[2 * k + 1] * down);
+        h[k] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      o[c] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    if (lane == 0) scale[r] = __int_as_float((127 + ex) << 23);
+  }
+  launch_dependents();
+}
+
+cudaError_t launch_to_f16(const void* src, int64_t src_rows, int64_t K, int64_t src_ld,
+                          const int32_t* gather, int64_t top_k, const int32_t* tile_mn,
+                          const int32_t* num_tiles, int64_t T, int64_t rows, void* out,
+                          float* scale, cudaStream_t st, bool pdl) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 16);
+  return launch_pdl(to_f16_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
+                    static_cast<const uint4*>(src), src_rows, K / 8, src_ld / 8, gather, (int)top_k,
+                    tile_mn, num_tiles, T, rows, static_cast<uint4*>(out), K / 8, scale);
+}
+
 }  // namespace fp4moe

@@ -17,7 +17,9 @@
 // rows I+128f..; half h holds gate rows 64h.. and their up rows.  GEMM2
 // (which = 2): rows 256f.. of w2, zero past H; half h holds rows 128h..
 // Decode-size problems store the code bytes in MMA fragment order instead
-// (decode.cuh, frag_half_offset); the scale region is the same.
+// (decode.cuh, frag_half_offset), as plain nibble pairs for the hardware
+// E2M1 -> f16 conversion, and the scale region holds each block scale's E4M3
+// magnitude (its sign and zero are in the codes).
 #include <algorithm>
 
 #include "common.cuh"
@@ -122,19 +124,19 @@ __global__ void prepare_fragment_kernel(PrepArgs a) {
           byte = prep_fix_codes(a.w[(e * a.rows_src + row) * (a.K / 2) + k / 2], sc[j & 1][(k / 16) % 8], 0x88u);
         v |= byte << (8 * j);
       }
-      words[kk] = prep_permute_word(v);
+      words[kk] = v;
     }
     *reinterpret_cast<uint4*>(dst + frag_half_offset(w, lane, 0)) =
         make_uint4(words[0], words[1], words[2], words[3]);
     *reinterpret_cast<uint4*>(dst + frag_half_offset(w, lane, 1)) =
         make_uint4(words[4], words[5], words[6], words[7]);
-    if (t == 0) {  // scale region: the same row-major layout as the row-order blocks
+    if (t == 0) {  // scale region: row r's 8 scale magnitudes (row-major, 8 bytes per row)
       for (int h = 0; h < 2; ++h) {
         const uint32_t r = 16 * w + g + 8 * h;
-        uint32_t codes[2] = {0, 0};
+        uint32_t mags[2] = {0, 0};
         for (int kk = 0; kk < 8; ++kk)
-          codes[kk >> 2] |= block_scale_code(a, e, rows[h], c, kk) << (8 * (kk & 3));
-        *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = make_uint2(codes[0], codes[1]);
+          mags[kk >> 2] |= (rows[h] >= 0 ? (uint32_t)sc[h][kk] & 0x7Fu : 0u) << (8 * (kk & 3));
+        *reinterpret_cast<uint2*>(dst + kWDataBytes + r * 8) = make_uint2(mags[0], mags[1]);
       }
     }
   }
@@ -161,15 +163,14 @@ __global__ void debug_decode_fragment_kernel(PrepArgs a) {
       const uint32_t b0 = ((kk < 4 ? s0.x : s0.y) >> (8 * t)) & 0xFFu;
       const uint32_t b1 = ((kk < 4 ? s1.x : s1.y) >> (8 * t)) & 0xFFu;
       uint32_t o[4];
-      decode_word_frag(words[kk], scale_code_bf16x2(b0), scale_code_bf16x2(b1), o);
+      decode_word_frag_f16(words[kk], e4m3_to_f16x2_dup(b0), e4m3_to_f16x2_dup(b1), o);
       for (int j = 0; j < 4; ++j) {
         const int64_t row = rows[j & 1];
         if (row < 0) continue;
         const int64_t k = c * kBK + frag_k((uint32_t)kk, t) + 2 * (j >> 1);
-        const float lo = __uint_as_float(o[j] << 16) * 256.0f;
-        const float hi = __uint_as_float(o[j] & 0xFFFF0000u) * 256.0f;
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&o[j]));   // exact
         *reinterpret_cast<__nv_bfloat162*>(a.dbg_out + (e * a.rows_src + row) * a.K + k) =
-            __floats2bfloat162_rn(lo, hi);
+            __floats2bfloat162_rn(f.x, f.y);
       }
     }
   }

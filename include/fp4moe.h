@@ -262,7 +262,10 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
  * accumulator, the activation in fp32 rounded once; w4a4 with route_tile >= 32
  * and H a multiple of 256 takes the NVFP4 operands straight into the
  * block-scaled FP4 tensor-core MMA -- the same exact products, fp32
- * accumulation):
+ * accumulation; w4a16 with route_tile 8 or 16 decodes to FP16 and carries
+ * each activation row as FP16 times a power of two chosen from the row's
+ * largest finite magnitude, multiplied back on the accumulator -- the same
+ * exact products for every element not below 2^-31 of that magnitude):
  *   h[s, n] = R( act(c_s a1_e G_e[n] . A_s, c_s a1_e U_e[n] . A_s) )
  * for valid slots s, e = tile_idx_to_expert (rows of padding slots are
  * zeroed by the decode-size and w4a4 / w4a8 kernels and left unwritten by the
@@ -275,9 +278,9 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
  *      [M, H/2] + a_sf [M, H/16] for w4a4) and row s is row
  *      gather_rows[s] / top_k (gather_rows = permuted_idx_to_expanded_idx);
  *      otherwise a is already permuted ([S, ...]).  Gathered rows go through
- *      the workspace in slot order when route_tile >= 32 (the tcgen05 GEMM
- *      reads plain row tiles) and are fetched by TMA inside the decode-size
- *      GEMM (route_tile 16); the result is the same bit for bit.
+ *      the workspace in slot order (the GEMMs read plain row tiles; for
+ *      w4a16 route_tile 8 / 16 every activation row goes there as FP16 with
+ *      its power-of-two scale); the result is the same bit for bit.
  *   w1_prepared: fp4moe_prepare_weights(p, 1, ...).  w1_alpha fp32 [E_local].
  *   w4a16: h bf16 [S, I] (R = round to BF16); h_sf, fc2_input_scale NULL.
  *   w4a8 : h e4m3 [S, I] + h_sf e8m0 [S, I/32]: R = MXFP8 quantisation (OCP MX
@@ -302,8 +305,9 @@ FP4MOE_API fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a
  *   "FP32 route storage" option of alphamoe_nvfp4_routed_moe; BF16 storage of
  *   y would put ~0.2% of outputs outside the parity bound through
  *   cancellation in the weighted sum).  y: fp32 [S, H].
- *   h: bf16 [S, I] (w4a16), uint8 [S, I/2] + h_sf [S, I/16] (w4a4) or e4m3
- *   [S, I] + h_sf e8m0 [S, I/32] (w4a8).
+ *   h: bf16 [S, I] (w4a16; route_tile 8 / 16: converted in the workspace to
+ *   FP16 rows with a power-of-two scale each, as in GEMM1), uint8 [S, I/2] +
+ *   h_sf [S, I/16] (w4a4) or e4m3 [S, I] + h_sf e8m0 [S, I/32] (w4a8).
  *   w2_prepared: fp4moe_prepare_weights(p, 2, ...).  w2_alpha fp32 [E_local]. */
 FP4MOE_API fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h_sf,
                         const void* w2_prepared, const float* w2_alpha,
@@ -339,9 +343,10 @@ FP4MOE_API fp4moe_status moe_combine(const fp4moe_problem* p, const float* parti
 
 /* The whole forward on `stream`: route sort, x gathered into slot order in the
  * workspace (NVFP4 for the FP4 MMA path; w4a8 rows and decode-size w4a4 rows
- * expanded to BF16 on the way; padding rows unwritten),
- * GEMM1 (+ activation), GEMM2, finalize, chained with programmatic dependent
- * launch.  Arguments as in the steps above; the
+ * expanded to BF16 on the way; w4a16 route_tile 8 / 16 rows as FP16 with a
+ * power-of-two scale each, and h likewise before GEMM2; padding rows
+ * unwritten), GEMM1 (+ activation), GEMM2, finalize, chained with
+ * programmatic dependent launch.  Arguments as in the steps above; the
  * weights are prepared (fp4moe_prepare_weights).  finalize_mode:
  *   FP4MOE_FINALIZE_DETERMINISTIC: bit-reproducible (default);
  *   FP4MOE_FINALIZE_ATOMIC (cute_dsl_fused_moe use_fused_finalize): no y
@@ -410,8 +415,9 @@ FP4MOE_API size_t fp4moe_localized_workspace_size(const fp4moe_problem* p);
 
 /* fused_moe_forward over two domains.  On `stream`: route sort and x in slot
  * order; then on domain stream d: FC1 shard d (+ for w4a8 and decode-size w4a4
- * its columns of h expanded to BF16), a wait for the other domain's FC1, FC2
- * shard d; then
+ * its columns of h expanded to BF16), a wait for the other domain's FC1 (for
+ * w4a16 route_tile 8 / 16: domain 0 then converts all of h to FP16 once and
+ * domain 1 waits for that), FC2 shard d; then
  * on `stream` again, after both domains: the finalize.  The results equal
  * fused_moe_forward's: bit for bit for route_tile >= 32 with the
  * deterministic finalize; for route_tile 16 the warp-MMA GEMM's K-split tail

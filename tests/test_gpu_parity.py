@@ -397,6 +397,56 @@ def test_decode_size_geglu_full():
     check_out(f64(out), exact, 5e-3, what="decode geglu")
 
 
+@pytest.mark.parametrize("T", [8, 16])
+@pytest.mark.parametrize("staged", [False, True])
+def test_decode_size_fp16_rows_over_wide_ranges(T, staged):
+    """The decode-size GEMMs take activation rows as FP16 times a power of two
+    per slot: token rows scaled by 2^-40..2^40 (and one of BF16 subnormals,
+    whose output rounds to zero on both sides),
+    with a tenth of their elements a further 2^-24 down, match the oracle
+    token by token, through the fused forward and through the staged GEMMs
+    (which convert x and h in their own workspaces)."""
+    import dataclasses
+    cfg = synth.CONFIGS["tiny_w4a16"]
+    inp = synth.generate(cfg, device="cuda")
+    g = torch.Generator().manual_seed(11)
+    x = inp.x.float().cpu()
+    k = torch.randint(-40, 41, (cfg.M, 1), generator=g).float()
+    k[0] = -130.0   # a row of BF16 subnormals
+    k[1] = 0.0
+    x = x * torch.exp2(k)
+    small = torch.rand(x.shape, generator=g) < 0.1
+    small[0] = False
+    x = torch.where(small, x * 2.0 ** -24, x).to(torch.bfloat16)
+    assert torch.all(torch.isfinite(x.float())) and bool((x[0] != 0).any())
+    inp = dataclasses.replace(inp, x=x.cuda())
+    p = problem_for(cfg, T)
+    B = MoEBuffers(p).prepare(inp.w1, inp.w1_sf, inp.w2, inp.w2_sf)
+    orc = oracle.OracleMoE.from_inputs(inp, T=T)
+    if staged:
+        B.route(inp.token_selected_experts.cuda())
+        h, _ = B.gemm1(inp.x, None, inp.w1_alpha, gather=True)
+        y = B.gemm2(h, None, inp.w2_alpha)
+        out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device="cuda")
+        B.finalize(y, inp.token_final_scales.cuda(), out, rsf=1.0)
+        torch.cuda.synchronize()
+    else:
+        out = _fused(inp, B)
+    _, exact, _ = orc.forward(nthreads=NTHREADS)
+    got = f64(out)
+    assert np.all(np.isfinite(got))
+    for t in range(cfg.M):
+        ref = exact[t]
+        scale = np.abs(ref).max()
+        if scale == 0:
+            assert np.all(got[t] == 0), t
+            continue
+        err = np.abs(got[t] - ref)
+        rel = np.linalg.norm(got[t] - ref) / np.linalg.norm(ref)
+        assert rel <= 5e-3, (t, float(k[t]), rel)
+        assert np.all(err <= RTOL * np.abs(ref) + 1e-3 * scale), (t, float(k[t]))
+
+
 # ------------------------------------------------------------------ w4a8 (MXFP8 x MXFP4)
 
 def test_mxfp8_quantiser_bit_exact_vs_oracle():
