@@ -1344,16 +1344,14 @@ __global__ void __launch_bounds__(kNThreads, 1)
 // multiplies back.
 //   warps 0-15  compute: warp w owns block rows 16w..16w+15 (GEMM1: warps
 //               0-7 gate rows, 8-15 the matching up rows); fp32 accumulators
-//               in registers over the whole K range (four chains, summed in a
-//               fixed order); the second 8-column n-block runs only when the
-//               tile holds more than 8 tokens.
+//               in registers over the whole K range; the second 8-column
+//               n-block runs only when the tile holds more than 8 tokens.
 //   warp 16     TMA producer, as in the tcgen05 kernel.
 // SwiGLU pairs gate and up rows through shared memory with two bounded
 // mbarrier handshakes per item.
 // ===========================================================================
 
 constexpr int kGvWarps = 16;
-constexpr int kGvChains = 2;  // accumulator chains per n-block
 constexpr int kGvThreads = 32 * (kGvWarps + 1);
 
 template <int BN_>
@@ -1379,16 +1377,17 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
 
 // The K loop of one work item for NB n-blocks (1 or 2), a compile-time
 // count so that the eight unrolled K steps of a chunk form one basic block
-// the compiler can interleave.  acc[nb][j] are kGvChains independent
-// accumulator chains per n-block (K step kk feeds chain kk % kGvChains).
-// boff[q]: byte offset of this lane's 8-byte B fragment for K step q of a
-// 64-element activation atom.  Runs nchunks consecutive chunks of the
-// stage ring.  Returns false on a bounded-wait timeout.
+// the compiler can interleave.  acc[nb]: one accumulator chain per n-block
+// (two chains per n-block, to hide the MMA latency, measured slower: the K
+// loop is at its register limit).  boff[p]: byte offset of this lane's
+// 16-byte B chunk for K steps 2p and 2p+1 of a 64-element activation atom.
+// Runs nchunks consecutive chunks of the stage ring.  Returns false on a
+// bounded-wait timeout.
 template <int BN, int NB>
 __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, uint64_t* full,
-                                          uint64_t* empty, const uint32_t (&boff)[4], int w, int lane, uint32_t r0,
+                                          uint64_t* empty, const uint32_t (&boff)[2], int w, int lane, uint32_t r0,
                                           uint32_t r1, int& stage, uint32_t& phase,
-                                          float (&acc)[2][kGvChains][4], int nchunks) {
+                                          float (&acc)[2][4], int nchunks) {
   for (int c = 0; c < nchunks; ++c) {
     if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) return false;
     const uint8_t* blk = stages + stage * GvCfg<BN>::kStage;
@@ -1397,12 +1396,13 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
     const uint2 sa = *reinterpret_cast<const uint2*>(blk + kWDataBytes + r0 * 8);
     const uint2 sb = *reinterpret_cast<const uint2*>(blk + kWDataBytes + r1 * 8);
     const uint32_t words[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-    // one scale multiplier per row per atom: block 4a + t (fragment K order)
-    const uint32_t sel = 0x4440u + ((uint32_t)lane & 3u);
-    const uint32_t sc0[2] = {e4m3_to_f16x2_dup(__byte_perm(sa.x, 0u, sel)),
-                             e4m3_to_f16x2_dup(__byte_perm(sa.y, 0u, sel))};
-    const uint32_t sc1[2] = {e4m3_to_f16x2_dup(__byte_perm(sb.x, 0u, sel)),
-                             e4m3_to_f16x2_dup(__byte_perm(sb.y, 0u, sel))};
+    // one scale multiplier per row per atom: block 4a + t (fragment K order),
+    // byte t of the row's scale word doubled by one byte permute
+    const uint32_t sel = 0x4400u + ((uint32_t)lane & 3u) * 0x11u;
+    const uint32_t sc0[2] = {e4m3x2_to_f16x2(__byte_perm(sa.x, 0u, sel)),
+                             e4m3x2_to_f16x2(__byte_perm(sa.y, 0u, sel))};
+    const uint32_t sc1[2] = {e4m3x2_to_f16x2(__byte_perm(sb.x, 0u, sel)),
+                             e4m3x2_to_f16x2(__byte_perm(sb.y, 0u, sel))};
     const uint8_t* bt = blk + kWBlockBytes;
     // per 64-element atom: decode its four words first, then their MMAs, so
     // that the four decode chains interleave
@@ -1412,12 +1412,14 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
 #pragma unroll
       for (int kq = 0; kq < 4; ++kq) decode_word_frag_f16(words[4 * at + kq], sc0[at], sc1[at], af[kq]);
       const uint8_t* atom = bt + at * BN * 128;  // K 0..63 or 64..127
+      // K steps 2p and 2p+1 take the two halves of one 16-byte B chunk
 #pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
+      for (int kp = 0; kp < 2; ++kp) {
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          const uint2 bv = *reinterpret_cast<const uint2*>(atom + nb * 1024 + boff[kq]);
-          mma_16816(acc[nb][(4 * at + kq) % kGvChains], af[kq], bv.x, bv.y);
+          const uint4 bv = *reinterpret_cast<const uint4*>(atom + nb * 1024 + boff[kp]);
+          mma_16816(acc[nb], af[2 * kp], bv.x, bv.y);
+          mma_16816(acc[nb], af[2 * kp + 1], bv.z, bv.w);
         }
       }
     }
@@ -1626,16 +1628,16 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     // ------------------------------------------------------------ compute warps
     const int w = warp, g = lane >> 2, t = lane & 3;
     const uint32_t r0 = (uint32_t)(16 * w + g), r1 = r0 + 8;
-    // B fragment of K step q (0..3) of a 64-element atom: token row g, K
-    // elements k = frag_k(q, t)..+3 (the fragment K order of decode.cuh), at
-    // byte 2 (k % 8) of 16-byte chunk k / 8; the activation tile is 128-byte
-    // swizzled (chunk j of row n at j ^ (n & 7)); row 8+g of the second
-    // n-block is 1024 bytes further with the same swizzle
-    uint32_t boff[4];
+    // B fragments of K steps 2p, 2p+1 of a 64-element atom: token row g, K
+    // elements frag_k(2p, t) = 16t + 8p .. +7 (the fragment K order of
+    // decode.cuh), 16-byte chunk 2t + p of the row; the activation tile is
+    // 128-byte swizzled (chunk j of row n at j ^ (n & 7)); row 8+g of the
+    // second n-block is 1024 bytes further with the same swizzle
+    uint32_t boff[2];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t k = frag_k((uint32_t)q, (uint32_t)t);
-      boff[q] = (uint32_t)g * 128u + (((k >> 3) ^ (uint32_t)g) << 4) + 2u * (k & 7u);
+    for (int p = 0; p < 2; ++p) {
+      const uint32_t k = frag_k(2u * (uint32_t)p, (uint32_t)t);
+      boff[p] = (uint32_t)g * 128u + (((k >> 3) ^ (uint32_t)g) << 4);
     }
     int stage = 0;
     uint32_t phase = 0, xphase = 0;
@@ -1643,27 +1645,12 @@ __global__ void __launch_bounds__(kGvThreads, 1)
     auto k_range = [&](int64_t item, int32_t c0, int32_t c1, float (&raw)[2][4]) -> bool {
       const int32_t tau = (int32_t)(item / a.F);
       const bool two = BN > 8 && a.tile_mn[tau] - (int64_t)tau * BN > 8;  // second n-block (warp-uniform)
-      float acc[2][kGvChains][4];
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-        for (int p = 0; p < kGvChains; ++p)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[nb][p][i] = 0.0f;
-      const bool ok =
-          two ? gv_k_loop<BN, 2>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc, c1 - c0)
-              : gv_k_loop<BN, 1>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, acc, c1 - c0);
-      // the chains summed in a fixed order: deterministic
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float r = acc[nb][0][i];
-#pragma unroll
-          for (int p = 1; p < kGvChains; ++p) r += acc[nb][p][i];
-          raw[nb][i] = r;
-        }
-      return ok;
+        for (int i = 0; i < 4; ++i) raw[nb][i] = 0.0f;
+      return two ? gv_k_loop<BN, 2>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, raw, c1 - c0)
+                 : gv_k_loop<BN, 1>(a, stages, full, empty, boff, w, lane, r0, r1, stage, phase, raw, c1 - c0);
     };
     // alpha is read here, after the K loop: reading it (and the next item's
     // plan entries) ahead of the loop, as the tcgen05 kernels do, measured

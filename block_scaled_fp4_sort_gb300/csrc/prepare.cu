@@ -163,7 +163,7 @@ __global__ void debug_decode_fragment_kernel(PrepArgs a) {
       const uint32_t b0 = ((kk < 4 ? s0.x : s0.y) >> (8 * t)) & 0xFFu;
       const uint32_t b1 = ((kk < 4 ? s1.x : s1.y) >> (8 * t)) & 0xFFu;
       uint32_t o[4];
-      decode_word_frag_f16(words[kk], e4m3_to_f16x2_dup(b0), e4m3_to_f16x2_dup(b1), o);
+      decode_word_frag_f16(words[kk], e4m3x2_to_f16x2(b0 * 0x101u), e4m3x2_to_f16x2(b1 * 0x101u), o);
       for (int j = 0; j < 4; ++j) {
         const int64_t row = rows[j & 1];
         if (row < 0) continue;
