@@ -224,20 +224,31 @@ def src_digest(*names):
     return h.hexdigest()[:16]
 
 
-GEMM_SOURCES = ("moe_gemm.cu", "common.cuh", "decode.cuh", "nvfp4.cuh", "internal.h")
+# the sources of each GEMM kernel family (its own file and the shared headers)
+_SHARED = ("gemm_common.cuh", "common.cuh", "decode.cuh", "nvfp4.cuh", "internal.h")
+GEMM_SOURCES = {"tcgen05": ("moe_gemm.cu",) + _SHARED,
+                "nvfp4": ("moe_gemm_nvfp4.cu",) + _SHARED,
+                "gemv": ("moe_gemv.cu",) + _SHARED}
 
 
-def stored_traffic(workload):
+def gemm_family(cfg, T, native):
+    if native:
+        return "nvfp4"
+    return "gemv" if cfg.mode == "w4a16" and T <= 16 else "tcgen05"
+
+
+def stored_traffic(workload, family):
     """DRAM bytes per GEMM1 launch from a committed ncu summary of this
     workload's GEMM1 (scaled to the full launch where the capture ran a
-    smaller case), or None if none was taken on the current kernel sources."""
+    smaller case), or None if none was taken on the current sources of the
+    kernel family that runs it."""
     path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
     if not os.path.exists(path):
         return None, None
     with open(path) as f:
         tj = json.load(f)
     ent = tj.get(workload)
-    if not ent or ent.get("src_digest") != src_digest(*GEMM_SOURCES):
+    if not ent or ent.get("src_digest") != src_digest(*GEMM_SOURCES[family]):
         return None, None
     return ent.get("dram_bytes_per_launch"), ent.get("source")
 
@@ -484,7 +495,7 @@ def measure(cfg, args, rank, world, local, dev, headline):
     achieved_bw = g1_bytes / (g1_ms * 1e-3) / 1e9
     achieved_tf = g1_flops / (g1_ms * 1e-3) / 1e12
     step_bytes = touched * (w1_bytes_per_expert + w2_bytes_per_expert) + act1 + M * H * 2
-    traffic, traffic_src = stored_traffic(cfg.name)
+    traffic, traffic_src = stored_traffic(cfg.name, gemm_family(cfg, T, native))
     g2_ms = kernels["gemm2"]
     roof = {"kernel": gemm1_kernel_name(cfg, T, native), "mma_dtype": mma_dtype(cfg, T, native)}
     if tensor_bound:

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp4moe.so")
 SOURCES = ["fp4moe_api.cu", "route_sort.cu", "route_noalloc.cu", "permute.cu", "prepare.cu",
-           "moe_gemm.cu", "domains.cu"]
+           "moe_gemm.cu", "moe_gemm_nvfp4.cu", "moe_gemv.cu", "domains.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", os.path.join(HERE, "..", "include")]
