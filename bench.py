@@ -253,12 +253,24 @@ def stored_traffic(workload, family):
     return ent.get("dram_bytes_per_launch"), ent.get("source")
 
 
+def native_mma(cfg, T):
+    """GEMM1's block-scaled tensor-core MMA, if any: 'nvfp4' (w4a4, K a
+    multiple of 256), 'mxfp8' (w4a8, K a multiple of 128; the E2M1 weights
+    stored as E4M3 bytes), route tiles of 32 or more; else None."""
+    if T >= 32 and cfg.mode == "w4a4" and cfg.H % 256 == 0:
+        return "nvfp4"
+    if T >= 32 and cfg.mode == "w4a8" and cfg.H % 128 == 0:
+        return "mxfp8"
+    return None
+
+
 def mma_dtype(cfg, T, native):
-    """Operand type of GEMM1's MMAs: the decode-size w4a16 kernel multiplies
-    FP16 (hardware E2M1 -> FP16 decode, activations as FP16 rows with a
+    """Operand type of GEMM1's MMAs: the native block-scaled MMAs (NVFP4, or
+    E4M3 x E4M3 with E8M0 block scales), the decode-size w4a16 kernel's FP16
+    (hardware E2M1 -> FP16 decode, activations as FP16 rows with a
     power-of-two scale each), the other w4a16 / expanded kernels BF16."""
     if native:
-        return "nvfp4"
+        return native
     return "f16" if cfg.mode == "w4a16" and T <= 16 else "bf16"
 
 
@@ -266,7 +278,8 @@ def gemm1_kernel_name(cfg, T, native):
     if cfg.mode == "w4a16" and T <= 16:
         return "moe_gemv_kernel (GEMM1 + SwiGLU, warp MMA, f16)"
     if native:
-        return "moe_gemm_nvfp4_kernel<%d> (GEMM1 + SwiGLU, tcgen05 kind::mxf4nvf4)" % T
+        return "moe_gemm_nvfp4_kernel<%d> (GEMM1 + SwiGLU, tcgen05 %s)" % (
+            T, "kind::mxf4nvf4" if native == "nvfp4" else "kind::mxf8f6f4")
     return "moe_gemm_kernel<%d> (GEMM1 + SwiGLU, tcgen05 kind::f16)" % T
 
 
@@ -478,12 +491,13 @@ def measure(cfg, args, rank, world, local, dev, headline):
     g1_bytes = touched * w1_bytes_per_expert + act1 + h_bytes
     g1_ms = kernels["gemm1_swiglu"]
     g1_flops = 4.0 * R * H * I
-    # w4a4 with K a multiple of 256 and route tile >= 32 multiplies on the
-    # native NVFP4 tensor-core MMA; everything else on BF16 MMAs of decoded
-    # weights.  The FP4 peak is the measured BF16 peak times the nominal
-    # dense ratio 13.5 / 2.25 PFLOP/s.
-    native = cfg.mode == "w4a4" and T >= 32 and H % 256 == 0
-    ratio = 13.5 / 2.25 if native else 1.0
+    # w4a4 (K % 256 == 0) and w4a8 (K % 128 == 0) with route tiles >= 32
+    # multiply on the native block-scaled tensor-core MMAs (NVFP4; MXFP8 x
+    # E4M3-stored MXFP4); everything else on BF16 / FP16 MMAs of decoded
+    # weights.  Their peaks: the measured BF16 peak times the nominal dense
+    # ratios 13.5 / 2.25 (FP4) and 4.5 / 2.25 (FP8) PFLOP/s.
+    native = native_mma(cfg, T)
+    ratio = {"nvfp4": 13.5 / 2.25, "mxfp8": 4.5 / 2.25}.get(native, 1.0)
     # a kernel timed inside a loop that lasts about a second or more runs
     # under the power cap: its denominator is the sustained cuBLAS rate
     sustained = args.steps * ms > 500.0
@@ -510,8 +524,9 @@ def measure(cfg, args, rank, world, local, dev, headline):
         "traffic": traffic, "traffic_source": traffic_src,
         "peak_source": "%s (%s)" % (
             peak_src, ("bf16_tflops_sustained: GEMM1 timed inside a %.1f s loop" % (args.steps * ms / 1e3)
-                       if sustained else "bf16_tflops burst") + (" x 13.5/2.25 nominal fp4 ratio"
-                                                                  if native else "")
+                       if sustained else "bf16_tflops burst") + (
+                {"nvfp4": " x 13.5/2.25 nominal fp4 ratio", "mxfp8": " x 4.5/2.25 nominal fp8 ratio"}
+                .get(native, ""))
             if tensor_bound else "hbm_gbs"),
         "touched_experts": touched,
         "tensor_frac": achieved_tf / mma_peak,
@@ -525,8 +540,8 @@ def measure(cfg, args, rank, world, local, dev, headline):
         "metric": METRIC, "value": tokens_per_s(world, cfg.M, ms), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": warm, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": ("nvfp4" if native else "f16" if mma_dtype(cfg, T, native) == "f16" else
-                  {"w4a16": "bf16", "w4a4": "nvfp4->bf16", "w4a8": "mxfp8->bf16"}[cfg.mode]),
+        "dtype": (native or ("f16" if mma_dtype(cfg, T, native) == "f16" else
+                             {"w4a16": "bf16", "w4a4": "nvfp4->bf16", "w4a8": "mxfp8->bf16"}[cfg.mode])),
         "data": "synthetic (seeded generator; random NVFP4 weights)",
         "config": dict(workload_config(cfg, T), l2="inputs larger than L2: %.2f GB of weights "
                        "and activations per step vs 126 MB L2" % (step_bytes / 1e9),
@@ -545,9 +560,12 @@ def measure(cfg, args, rank, world, local, dev, headline):
                           "overlap step i-1's compute"},
         "clocks": clocks,
         # per fused step: routing (1 kernel up to 4096 routes, else 3), x in slot
-        # order, GEMM1, the w4a8 / decode-size w4a4 h -> BF16 expansion, GEMM2, finalize
-        "gpu_launches": args.steps * (routes_kernels + 1 + 3 +
-                                      (0 if cfg.mode == "w4a16" or native else 1)),
+        # order, GEMM1, one pass over h before GEMM2 (BF16 expansion for w4a4 on
+        # BF16 MMAs and w4a8 on them, the MXFP8 scales' chunk-major copy for w4a8
+        # on the MX MMA, FP16 rows for decode-size w4a16), GEMM2, finalize
+        "gpu_launches": args.steps * (routes_kernels + 1 + 3 + (
+            1 if (cfg.mode == "w4a16" and T <= 16) or (cfg.mode != "w4a16" and native != "nvfp4")
+            else 0)),
     }
     del B, out
     torch.cuda.synchronize()

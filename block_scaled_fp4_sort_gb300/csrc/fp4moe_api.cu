@@ -377,17 +377,18 @@ fp4moe_status moe_gemm1_swiglu(const fp4moe_problem* p, const void* a, const uin
   // rows in slot order with a power-of-two scale per row.
   const bool frag = fragment_layout(s);
   const bool slot_order = gather_rows != nullptr && !frag;
-  const bool native = native_fp4(s, 1);
+  const bool native = native_mma(s, 1);
   float* f16_scale = frag ? reinterpret_cast<float*>(ws + f16_scale_offset(s, 1)) : nullptr;
   const void* act = a;
   const uint8_t* act_sf = nullptr;
   cudaError_t e = cudaSuccess;
   if (native) {
-    // NVFP4 rows copied into slot order (or as given) with every scale's sign
-    // moved into its codes, for the native tensor-core MMA
+    // rows copied into slot order (or as given) for the native tensor-core
+    // MMA: NVFP4 with every scale's sign moved into its codes; MXFP8 with its
+    // scales chunk-major
     uint8_t* q = ws + kWsHeader;
-    uint8_t* qsf = q + up((size_t)s.S * s.H / 2);
-    e = launch_permute(s, a, a_sf, gather_rows, num_tiles, q, qsf, cs, false, true, true);
+    uint8_t* qsf = q + up((size_t)s.S * (mx ? s.H : s.H / 2));
+    e = launch_permute(s, a, a_sf, gather_rows, num_tiles, q, qsf, cs, false, true, true, true);
     act = q;
     act_sf = qsf;
   } else if (w4) {
@@ -452,6 +453,11 @@ fp4moe_status moe_gemm2(const fp4moe_problem* p, const void* h, const uint8_t* h
     act = ws + kWsHeader;
     if (launch_to_f16(h, s.S, s.I, s.I, nullptr, 1, tile_mn, num_tiles, s.T, s.S, ws + kWsHeader,
                       f16_scale, cs, false) != cudaSuccess)
+      return FP4MOE_ERR_CUDA;
+  } else if (native_mx(s, 2)) {
+    // the MXFP8 codes as given; their scales chunk-major in the workspace
+    act_sf = ws + kWsHeader;
+    if (launch_sf_chunk_major(h_sf, s.S, s.I, num_tiles, s.T, ws + kWsHeader, cs, false) != cudaSuccess)
       return FP4MOE_ERR_CUDA;
   } else if (native_fp4(s, 2)) {
     // h as given, copied with every scale's sign moved into its codes
@@ -546,13 +552,14 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   // Decode sizes (warp-MMA GEMMs): FP16 rows with a power-of-two scale per
   // slot, for x here and for h before GEMM2.
   const void* xb = ws + L.y;
-  const bool native1 = native_fp4(s, 1), native2 = native_fp4(s, 2);
+  const bool native1 = native_mma(s, 1), native2 = native_mma(s, 2);
   const bool frag = fragment_layout(s);
   float* xs = frag ? reinterpret_cast<float*>(ws + L.x_scale) : nullptr;
   float* hs = frag ? reinterpret_cast<float*>(ws + L.h_scale) : nullptr;
-  uint8_t* xsf = ws + L.y + up((size_t)s.S * s.H / 2);   // native: NVFP4 x scales
+  // native MMA: NVFP4 or MXFP8 x scales after the codes (MXFP8 chunk-major)
+  uint8_t* xsf = ws + L.y + up((size_t)s.S * (mx ? s.H : s.H / 2));
   if (e == cudaSuccess)
-    e = native1 ? launch_permute(s, x, x_sf, p2e, nt, ws + L.y, xsf, cs, true, false, true)
+    e = native1 ? launch_permute(s, x, x_sf, p2e, nt, ws + L.y, xsf, cs, true, false, true, true)
         : w4    ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
                                       ws + L.y, cs, true, p2e, s.K, s.M, mx)
         : frag  ? launch_to_f16(x, s.M, s.H, s.H, p2e, s.K, tm, nt, s.T, s.S, ws + L.y, xs, cs, true)
@@ -584,6 +591,12 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
                             nullptr, 1, 0, mx);
     hin = ws + L.deq2;
   }
+  // native MX GEMM2: h's scales chunk-major (in the BF16-expansion region)
+  const uint8_t* h_sf2 = ws + L.h_sf;
+  if (e == cudaSuccess && native2 && mx) {
+    e = launch_sf_chunk_major(ws + L.h_sf, s.S, s.I, nt, s.T, ws + L.deq2, cs, true);
+    h_sf2 = ws + L.deq2;
+  }
   if (e == cudaSuccess && frag) {
     e = launch_to_f16(ws + L.h, s.S, s.I, s.I, nullptr, 1, tm, nt, s.T, s.S, ws + L.h16, hs, cs, true);
     hin = ws + L.h16;
@@ -598,7 +611,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
   g2.tile_mn = tm;
   g2.num_tiles = nt;
   g2.act = hin;
-  g2.act_sf = native2 ? ws + L.h_sf : nullptr;
+  g2.act_sf = native2 ? h_sf2 : nullptr;
   g2.act_rows = s.S;
   g2.out = ws + L.y;
   g2.p2e = p2e;
@@ -698,8 +711,8 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
   float* y = reinterpret_cast<float*>(ws + L.f.y);
   const int64_t c1 = s.I / 2, c2 = s.H / 2;   // h columns, output columns per domain
   const Shape s1 = domain_shape(s, 1), s2 = domain_shape(s, 2);
-  const bool native1 = native_fp4(s1, 1), native2 = native_fp4(s2, 2);
-  uint8_t* xsf = reinterpret_cast<uint8_t*>(y) + up((size_t)s.S * s.H / 2);
+  const bool native1 = native_mma(s1, 1), native2 = native_mma(s2, 2);
+  uint8_t* xsf = reinterpret_cast<uint8_t*>(y) + up((size_t)s.S * (mx ? s.H : s.H / 2));
   // decode sizes: FP16 x and h with power-of-two row scales (as in the fused path)
   const bool frag = fragment_layout(s);
   float* xs = frag ? reinterpret_cast<float*>(ws + L.f.x_scale) : nullptr;
@@ -720,7 +733,7 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
     // x in slot order (NVFP4 for the native MMA; other w4a4 / w4a8 rows
     // expanded to BF16), as in the fused path
     if (e == cudaSuccess)
-      e = native1 ? launch_permute(s, x, x_sf, p2e, nt, y, xsf, cs, true, false, true)
+      e = native1 ? launch_permute(s, x, x_sf, p2e, nt, y, xsf, cs, true, false, true, true)
           : w4    ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
                                         y, cs, true, p2e, s.K, s.M, mx)
           : frag  ? launch_to_f16(x, s.M, s.H, s.H, p2e, s.K, tm, nt, s.T, s.S, y, xs, cs, true)
@@ -778,20 +791,23 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
     }
     if (e == cudaSuccess) e = record_on(ds[d], kEvFc1 + d, &ev_fc1[d]);
   }
-  // decode sizes: h to FP16 once, on domain 0 after both FC1 shards
-  if (e == cudaSuccess && frag) {
+  // decode sizes: h to FP16 once; native MX GEMM2: h's scales chunk-major
+  // once -- on domain 0 after both FC1 shards
+  const bool conv = frag || (native2 && mx);
+  if (e == cudaSuccess && conv) {
     e = wait_on(ds[0], ev_fc1[1]);
     if (e == cudaSuccess) {
       StreamCtxGuard g(ds[0]);
-      e = g.ok() ? launch_to_f16(ws + L.f.h, s.S, s.I, s.I, nullptr, 1, tm, nt, s.T, s.S,
-                                 ws + L.f.h16, hs, ds[0], false)
-                 : cudaErrorDeviceUninitialized;
+      e = !g.ok() ? cudaErrorDeviceUninitialized
+          : frag  ? launch_to_f16(ws + L.f.h, s.S, s.I, s.I, nullptr, 1, tm, nt, s.T, s.S,
+                                  ws + L.f.h16, hs, ds[0], false)
+                  : launch_sf_chunk_major(ws + L.f.h_sf, s.S, s.I, nt, s.T, ws + L.f.deq2, ds[0], false);
     }
     if (e == cudaSuccess) e = record_on(ds[0], kEvConv, &ev_conv);
   }
   // FC2 shard d -> output columns [d c2, (d+1) c2), after both FC1 shards
   for (int d = 0; d < 2 && e == cudaSuccess; ++d) {
-    e = frag ? (d == 0 ? cudaSuccess : wait_on(ds[d], ev_conv)) : wait_on(ds[d], ev_fc1[1 - d]);
+    e = conv ? (d == 0 ? cudaSuccess : wait_on(ds[d], ev_conv)) : wait_on(ds[d], ev_fc1[1 - d]);
     if (e == cudaSuccess && side_seed) e = wait_on(ds[d], ev_seed);
     if (e != cudaSuccess) break;
     {
@@ -809,7 +825,7 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
       g2.tile_mn = tm;
       g2.num_tiles = nt;
       g2.act = frag ? ws + L.f.h16 : w4 && !native2 ? ws + L.f.deq2 : ws + L.f.h;
-      g2.act_sf = native2 ? ws + L.f.h_sf : nullptr;
+      g2.act_sf = !native2 ? nullptr : mx ? ws + L.f.deq2 : ws + L.f.h_sf;
       g2.act_rows = s.S;
       g2.out = atomic ? acc + d * c2 : y + d * c2;
       g2.out_ld = s.H;

@@ -48,6 +48,8 @@ struct GemmArgs {
   const float* route_w;        //   token_final_scales [M, top_k]
   float rsf;                   //   routed_scaling_factor
   const float* slot_scale;     // warp-MMA kernel: FP16 activation row s is the BF16 row / slot_scale[s]
+  const uint8_t* bsf;          // native MX GEMM: activation scales, chunk-major [C][bsf_rows] x 4 bytes
+  int64_t bsf_rows;
   int* err;
 };
 

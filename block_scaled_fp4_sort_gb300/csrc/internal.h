@@ -88,10 +88,29 @@ inline int64_t native_row_blocks(const Shape& s, int which) {
   return (s.H + 127) / 128;
 }
 
+// w4a8 GEMMs whose reduction is a multiple of 128 run on the block-scaled
+// MX tensor-core MMA (kind::mxf8f6f4, route tiles 32..128).  The weights are
+// stored one byte per element as E4M3 (every E2M1 value is one, sign
+// included), so that both operands are E4M3 with E8M0 block-32 scales: per
+// (expert, 128-row tile, 128-element K chunk) one block of kMBlockBytes, the
+// codes as in the native NVFP4 layout (128-byte rows, 16-byte units
+// XOR-swizzled by row & 7; the same rows per tile), then the tile's E8M0
+// scales, 4 bytes per row.
+inline bool native_mx(const Shape& s, int which) {
+  return s.mode == 2 && s.T >= 32 && (which == 1 ? s.H : s.I) % 128 == 0;
+}
+constexpr int kMTileScales = 128 * 4;
+constexpr int kMBlockBytes = kNTileCodes + kMTileScales;   // 16896
+// either native layout (same tiles, same rows per tile)
+inline bool native_mma(const Shape& s, int which) { return native_fp4(s, which) || native_mx(s, which); }
+
 inline size_t prepared_bytes(const Shape& s, int which) {
   if (native_fp4(s, which))
     return (size_t)s.EL * native_row_blocks(s, which) * ((which == 1 ? s.H : s.I) / 256) *
            kNBlockBytes;
+  if (native_mx(s, which))
+    return (size_t)s.EL * native_row_blocks(s, which) * ((which == 1 ? s.H : s.I) / 128) *
+           kMBlockBytes;
   return (size_t)s.EL * row_blocks(s, which) * k_chunks(s, which) * kWBlockBytes;
 }
 
@@ -106,7 +125,12 @@ cudaError_t launch_route_sort(const Shape& s, const int32_t* ids, int32_t* e2p, 
 // ---- elementwise steps (permute.cu) ----
 cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, const int32_t* p2e,
                            const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
-                           bool pdl, bool zero_pad = true, bool canon = false);
+                           bool pdl, bool zero_pad = true, bool canon = false,
+                           bool sf_chunk_major = false);
+// MXFP8 scales [rows, K/32] -> chunk-major [K/128, rows] 4-byte units (the
+// native MX GEMM's activation scales); rows past num_tiles * T untouched
+cudaError_t launch_sf_chunk_major(const uint8_t* sf, int64_t rows, int64_t K, const int32_t* num_tiles,
+                                  int64_t T, uint8_t* out, cudaStream_t st, bool pdl);
 // canon (NVFP4 rows): a block whose scale has the sign bit set is stored with
 // the sign moved into its 16 codes (the same values; the native MMA reads
 // scales unsigned).  p2e may be null: row s of x is row s (rows already in
@@ -171,7 +195,8 @@ struct GemmLaunch {
   const int32_t* gather_rows;  // GEMM1 row gather (permuted_idx_to_expanded_idx) or null
   const void* act;             // bf16 activations: x [M, K] (gather) or permuted [S, K];
                                //   native NVFP4 GEMM: E2M1 codes [S, K/2] in slot order
-  const uint8_t* act_sf;       //   native NVFP4 GEMM: their E4M3 scales [S, K/16]
+  const uint8_t* act_sf;       //   native NVFP4 GEMM: their E4M3 scales [S, K/16]; native MX
+                               //   GEMM: their E8M0 scales chunk-major [K/128, S] x 4 bytes
   int64_t act_rows;            // rows of `act`
   void* out;                   // h bf16 [S, I] | hq [S, I/2] | y bf16 [S, H] | out bf16 [M, H]
   uint8_t* out_sf;             // hsf [S, I/16]

@@ -1030,7 +1030,7 @@ cudaError_t launch_2sm_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, 
 }  // namespace
 
 cudaError_t launch_gemm(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
-  if (native_fp4(s, g.which)) return launch_gemm_native(s, g, st, pdl);
+  if (native_mma(s, g.which)) return launch_gemm_native(s, g, st, pdl);
   if (fragment_layout(s)) return launch_gemm_gv(s, g, st, pdl);
   if (one_tile(s)) return s.T == 256 ? launch_2sm_bn<256>(s, g, st, pdl) : cudaErrorInvalidValue;
   switch (s.T) {

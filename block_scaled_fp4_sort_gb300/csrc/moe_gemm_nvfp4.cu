@@ -39,18 +39,30 @@ constexpr int kNTmaWarp = 20;
 constexpr int kNMmaWarp = 21;
 constexpr int kNThreads = 32 * 22;
 
-template <int BN>
+template <int BN, bool MX>
 struct NCfg {
-  static constexpr int kBData = BN * 128;         // BN activation rows, 256 K elements
-  static constexpr int kBSf = BN * 16;            // 16 block scales per row and chunk
-  static constexpr int kTx = kNBlockBytes + kBData + kBSf;
+  static constexpr int kABytes = MX ? kMBlockBytes : kNBlockBytes;   // one prepared weight block
+  static constexpr int kBData = BN * 128;         // BN activation rows of 128 code bytes per chunk
+  static constexpr int kBSf = MX ? BN * 4 : BN * 16;   // block scales per row and chunk
+  static constexpr int kTx = kABytes + kBData + kBSf;
+  // stage layout: NVFP4 [weight codes | weight scales | B codes | B scales];
+  // MX [B codes | weight codes | weight scales | B scales] -- both code tiles
+  // on 1024-byte boundaries (the 128-byte swizzle)
+  static constexpr int kOffA = MX ? kBData : 0;
+  static constexpr int kOffASf = kOffA + kNTileCodes;
+  static constexpr int kOffB = MX ? 0 : kNBlockBytes;
+  static constexpr int kOffBSf = MX ? kBData + kMBlockBytes : kNBlockBytes + kBData;
   static constexpr int kStage = (kTx + 1023) / 1024 * 1024;
   static constexpr int kStagesRaw = (220 * 1024) / kStage;
   static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
   static constexpr int kSfBase = 256;             // TMEM: accumulators 2 x BN from column 0
   static constexpr int kSfCols = 32;              // per stage: A scales, B scales
   static constexpr int kBarBytes = 256;
-  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes;
+  // MX gated FC1: the half-block amax exchange of the epilogue (two buffers,
+  // 16 warps x 16 columns)
+  static constexpr int kXchBytes = MX ? 2 * 16 * 16 * 4 : 0;
+  static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes + kXchBytes;
+  static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffBSf % 16 == 0, "stage layout");
   static_assert(kSfBase + kStages * kSfCols <= 512, "tensor memory");
   static_assert(2 * BN <= kSfBase, "accumulators");
   static_assert(kStages >= 2, "pipeline depth");
@@ -77,6 +89,42 @@ __host__ __device__ constexpr uint32_t idesc_nvfp4(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
+// kind::mxf8f6f4 with E8M0 block-32 scales, one scale per row per MMA (K =
+// 32): the chunk's four MMAs take the scales from four sets of columns laid
+// out as for the NVFP4 MMA, each scale in byte 0 of its cell (scale-factor
+// slot 0).
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor, kind::mxf8f6f4: A and B E4M3 (format 0), K-major,
+// E8M0 scales (bit 23), scale-factor slots 0.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N) {
+  return (1u << 23)                      // scale type: UE8M0
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// the MX scale tile (4 bytes per row: the chunk's four block-32 scales) into
+// the 16 registers of one 32x32b.x16 store: column 4 ks + m1 <- scale ks of
+// row l + 32 m1 in byte 0; rows at or past `rows` give zero
+__device__ __forceinline__ void sf_regs_mx(const uint8_t* tile, int l, int rows, uint32_t (&v)[16]) {
+#pragma unroll
+  for (int m1 = 0; m1 < 4; ++m1) {
+    const int r = l + 32 * m1;
+    const uint32_t w = r < rows ? *reinterpret_cast<const uint32_t*>(tile + r * 4) : 0u;
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) v[4 * ks + m1] = (w >> (8 * ks)) & 0xFFu;
+  }
+}
+
 // four 16-byte rows (r, r+32, r+64, r+96 of a 16-byte-per-row scale tile) into
 // the 16 registers of one 32x32b.x16 store: column 4 ks + m1 <- word ks of row
 // l + 32 m1; rows at or past `rows` give zero
@@ -95,15 +143,21 @@ __device__ __forceinline__ void sf_regs(const uint8_t* tile, int l, int rows, ui
 // Epilogue of one item of the native GEMM: accumulators [128 rows x BN slots]
 // at TMEM column `acc`; groups of 128 threads split the slot columns (four
 // groups of BN / 4, or two of 16 for 32-slot tiles).
-// Gated FC1 (kEpiSwigluNvfp4): lanes 0-15 of a quarter hold gate rows, lanes
-// 16-31 the matching up rows; one exchange 16 lanes apart gives the gate lane
-// the up value of column j and the up lane the gate value of column 8 + j, so
-// each half-warp quantises one 16-feature NVFP4 block of one slot.  Other
-// epilogues: row = output feature 128 f + row.
+// Gated FC1 (kEpiSwigluNvfp4, kEpiSwigluMxfp8): lanes 0-15 of a quarter hold
+// gate rows, lanes 16-31 the matching up rows; one exchange 16 lanes apart
+// gives the gate lane the up value of column j and the up lane the gate value
+// of column 8 + j, so each half-warp holds 16 features of one slot: one NVFP4
+// block, or half of an MXFP8 block whose other half is the same half-warp of
+// the neighbouring lane quarter (their block maxima meet in shared memory,
+// `xch`, under a named barrier of the two warps).  Other epilogues: row =
+// output feature 128 f + row (an MXFP8 block = one warp's 32 rows).
+__device__ __forceinline__ void pair_bar_sync(int id) {   // the two warps of an MXFP8 block
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
 template <int BN, int EPI>
 __device__ __forceinline__ void n_epilogue(const GemmArgs& a, uint32_t acc, uint32_t lane_base,
                                            int32_t tau, int32_t f, int32_t mn, float scale, float fs,
-                                           int lane, int row, int grp) {
+                                           int lane, int row, int grp, float* xch, uint32_t& xbuf) {
   constexpr int kGroups = BN >= 64 ? 4 : 2;
   if (grp >= kGroups) return;
   const int64_t s0 = (int64_t)tau * BN;
@@ -136,6 +190,51 @@ __device__ __forceinline__ void n_epilogue(const GemmArgs& a, uint32_t acc, uint
         if ((lane & 15) == 0) a.out_sf[s * (a.out_ld / 16) + n / 16] = (uint8_t)sf;
       }
     }
+  } else if (EPI == kEpiSwigluMxfp8) {
+    const bool up = lane >= 16;
+    const int q = row >> 5;   // lane quarter
+    const int64_t n = (int64_t)f * 64 + 16 * q + (lane & 15);
+    uint8_t* hq = static_cast<uint8_t*>(a.out);
+#pragma unroll 1
+    for (int cc = c0; cc < c0 + kCw; cc += 16) {
+      uint32_t v[16];
+      tmem_ld16(acc + lane_base + (uint32_t)cc, v);
+      tmem_wait_ld();
+      float hv[8], am[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float lo = __uint_as_float(v[j]), hi = __uint_as_float(v[8 + j]);
+        const float other = __shfl_xor_sync(0xffffffffu, up ? lo : hi, 16);
+        const float g = up ? other : lo, u = up ? hi : other;
+        const int64_t s = s0 + cc + j + (up ? 8 : 0);
+        hv[j] = 0.0f;
+        if (s < mn) {
+          const float sc = scale * token_factor(a, s);
+          hv[j] = gemm1_act(a, g * sc, u * sc);
+        }
+        am[j] = mxfp8_abs_key(hv[j]);
+      }
+      // the half-warp's maxima (16 features), exchanged with the partner quarter
+#pragma unroll
+      for (int d = 8; d >= 1; d >>= 1)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], d));
+      float* mine = xch + (xbuf * 16 + grp * 4 + q) * 16 + (up ? 8 : 0);
+      const float* theirs = xch + (xbuf * 16 + grp * 4 + (q ^ 1)) * 16 + (up ? 8 : 0);
+      if ((lane & 15) == 0)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mine[j] = am[j];
+      pair_bar_sync(1 + grp * 2 + (q >> 1));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int64_t s = s0 + cc + j + (up ? 8 : 0);
+        uint32_t sf;
+        const uint32_t code = mxfp8_quant_amax(hv[j], fmaxf(am[j], theirs[j]), &sf);
+        hq[s * a.out_ld + n] = (uint8_t)code;
+        if ((q & 1) == 0 && (lane & 15) == 0) a.out_sf[s * (a.out_ld / 32) + n / 32] = (uint8_t)sf;
+      }
+      xbuf ^= 1u;
+    }
   } else {
     const int64_t n = (int64_t)f * 128 + row;
     if (n >= a.valid_rows) return;   // warp-uniform: the valid rows are a multiple of 32
@@ -147,7 +246,13 @@ __device__ __forceinline__ void n_epilogue(const GemmArgs& a, uint32_t acc, uint
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int64_t s = s0 + cc + i;
-        if (EPI == kEpiRelu2Nvfp4) {
+        if (EPI == kEpiRelu2Mxfp8) {   // the warp's 32 rows are one MXFP8 block
+          const float hv = s < mn ? relu2(__uint_as_float(v[i]) * scale * token_factor(a, s)) : 0.0f;
+          uint32_t sf;
+          const uint32_t code = mxfp8_quant_warp(hv, &sf);
+          static_cast<uint8_t*>(a.out)[s * a.out_ld + n] = (uint8_t)code;
+          if (lane == 0) a.out_sf[s * (a.out_ld / 32) + n / 32] = (uint8_t)sf;
+        } else if (EPI == kEpiRelu2Nvfp4) {
           const float hv = s < mn ? relu2(__uint_as_float(v[i]) * scale * token_factor(a, s)) : 0.0f;
           uint32_t sf;
           const uint32_t code = nvfp4_quant_canonical(hv, fs, &sf);
@@ -167,11 +272,11 @@ __device__ __forceinline__ void n_epilogue(const GemmArgs& a, uint32_t acc, uint
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool MX>
 __global__ void __launch_bounds__(kNThreads, 1)
     moe_gemm_nvfp4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap,
                           const __grid_constant__ CUtensorMap bsfmap) {
-  using C = NCfg<BN>;
+  using C = NCfg<BN, MX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -183,6 +288,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
   uint64_t* accempty = accfull + 2;           // [2]: the epilogue has read buffer b
   uint64_t* drain = accempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  float* xch = reinterpret_cast<float*>(smem + C::kStages * C::kStage + C::kBarBytes);   // MX only
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -204,7 +310,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
   }
   if (warp == kNTmaWarp && lane == 0) {
     prefetch_tensormap(&bmap);
-    prefetch_tensormap(&bsfmap);
+    if (!MX) prefetch_tensormap(&bsfmap);
   }
   tc_fence_before();
   __syncthreads();
@@ -213,10 +319,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
 
   grid_dependency_wait();
   const int64_t n_items = plan_items(a);
-  // stage layout: the prepared weight block (codes | scales) | B codes | B scales
-  constexpr int kOffASf = kNTileCodes;
-  constexpr int kOffB = kNBlockBytes;
-  constexpr int kOffBSf = kOffB + C::kBData;
+  constexpr int kOffA = C::kOffA, kOffASf = C::kOffASf, kOffB = C::kOffB, kOffBSf = C::kOffBSf;
 
   if (warp == kNTmaWarp) {
     // ------------------------------------------------------------ producer
@@ -226,16 +329,20 @@ __global__ void __launch_bounds__(kNThreads, 1)
     for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const int32_t tau = (int32_t)(item / a.F), f = (int32_t)(item % a.F);
       const int32_t e = plan_expert(a, tau);
-      const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)kNBlockBytes;
+      const uint8_t* wsrc = a.wprep + ((int64_t)e * a.F + f) * a.C * (int64_t)C::kABytes;
       for (int c = 0; c < a.C; ++c) {
         if (lane == 0) {
           ok = mbar_wait(&empty[stage], phase ^ 1u, a.err);
           if (ok) {
             uint8_t* st = stages + stage * C::kStage;
             mbar_arrive_expect_tx(&full[stage], (uint32_t)C::kTx);
-            tma_load_1d(st, wsrc + (int64_t)c * kNBlockBytes, kNBlockBytes, &full[stage]);
+            tma_load_1d(st + kOffA, wsrc + (int64_t)c * C::kABytes, C::kABytes, &full[stage]);
             tma_load_2d(st + kOffB, &bmap, c * 128, tau * BN, &full[stage]);
-            tma_load_2d(st + kOffBSf, &bsfmap, c * 16, tau * BN, &full[stage]);
+            if (MX)   // the chunk's activation scales: BN rows x 4 bytes, chunk-major
+              tma_load_1d(st + kOffBSf, a.bsf + ((int64_t)c * a.bsf_rows + (int64_t)tau * BN) * 4,
+                          (uint32_t)C::kBSf, &full[stage]);
+            else
+              tma_load_2d(st + kOffBSf, &bsfmap, c * 16, tau * BN, &full[stage]);
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -254,7 +361,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
   } else if (warp == kNMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdesc = idesc_nvfp4(128, BN);
+      constexpr uint32_t kIdesc = MX ? idesc_mx(128, BN) : idesc_nvfp4(128, BN);
       int stage = 0;
       uint32_t phase = 0, k = 0;   // k: items of this CTA so far; buffer k % 2
       bool ok = true;
@@ -272,9 +379,13 @@ __global__ void __launch_bounds__(kNThreads, 1)
           const uint32_t st = smem_u32(stages + stage * C::kStage);
           const uint32_t sf = tmem + (uint32_t)(C::kSfBase + stage * C::kSfCols);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_nvfp4(d, smem_desc_sw128(st + ks * 32), smem_desc_sw128(st + kOffB + ks * 32), kIdesc,
-                      sf + ks * 4, sf + 16 + ks * 4, (c > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 4; ++ks) {   // 32 bytes of K per MMA: 64 E2M1 or 32 E4M3 elements
+            const uint64_t ad = smem_desc_sw128(st + kOffA + ks * 32), bd = smem_desc_sw128(st + kOffB + ks * 32);
+            if (MX)
+              mma_mx(d, ad, bd, kIdesc, sf + ks * 4, sf + 16 + ks * 4, (c > 0 || ks > 0) ? 1u : 0u);
+            else
+              mma_nvfp4(d, ad, bd, kIdesc, sf + ks * 4, sf + 16 + ks * 4, (c > 0 || ks > 0) ? 1u : 0u);
+          }
           tc_commit(&empty[stage]);   // frees the shared-memory stage and its scale columns
           if (++stage == C::kStages) {
             stage = 0;
@@ -305,9 +416,11 @@ __global__ void __launch_bounds__(kNThreads, 1)
         const uint8_t* st = stages + stage * C::kStage;
         const uint32_t col = tmem + lane_base + (uint32_t)(C::kSfBase + stage * C::kSfCols);
         uint32_t v[16];
-        sf_regs(st + kOffASf, lane, 128, v);
+        if (MX) sf_regs_mx(st + kOffASf, lane, 128, v);
+        else sf_regs(st + kOffASf, lane, 128, v);
         tmem_st16(col, v);
-        sf_regs(st + kOffBSf, lane, BN, v);
+        if (MX) sf_regs_mx(st + kOffBSf, lane, BN, v);
+        else sf_regs(st + kOffBSf, lane, BN, v);
         tmem_st16(col + 16, v);
         tmem_wait_st();
         tc_fence_before();
@@ -324,7 +437,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
     const int et = threadIdx.x - 32 * kNSfWarps;   // 0..511
     const int row = et & 127, grp = et >> 7;
     const uint32_t lane_base = (uint32_t)(row & ~31) << 16;   // warp w: lane quarter w % 4
-    uint32_t k = 0;
+    uint32_t k = 0, xbuf = 0;
     const float fs = fc1_out_scale<EPI>(a);
     // the plan entries of the next item load during this item's epilogue and
     // its alpha at the end of it
@@ -344,7 +457,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&accfull[buf], (k >> 1) & 1u, a.err))) break;
       tc_fence_after();
       n_epilogue<BN, EPI>(a, tmem + buf * (uint32_t)BN, lane_base, tau, f, cur.mn, alpha, fs, lane, row,
-                          grp);
+                          grp, xch, xbuf);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&accempty[buf]);
@@ -361,9 +474,9 @@ __global__ void __launch_bounds__(kNThreads, 1)
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool MX>
 cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
-  using Cf = NCfg<BN>;
+  using Cf = NCfg<BN, MX>;
   GemmArgs a = {};
   a.wprep = g.wprep;
   a.alpha = g.alpha;
@@ -372,7 +485,7 @@ cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st
   a.num_tiles = g.num_tiles;
   a.top_k = (int32_t)s.K;
   a.F = (int32_t)native_row_blocks(s, g.which);
-  a.C = (int32_t)((g.which == 1 ? s.H : s.I) / 256);
+  a.C = (int32_t)((g.which == 1 ? s.H : s.I) / (MX ? 128 : 256));
   a.out_ld = g.out_ld > 0 ? g.out_ld : (g.which == 1 ? s.I : s.H);
   a.valid_rows = (int32_t)(g.which == 1 ? (gated(s) ? 2 * s.I : s.I) : s.H);
   a.act = s.act;
@@ -389,10 +502,16 @@ cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st
   a.err = g.err;
   const int64_t K = g.which == 1 ? s.H : s.I;
   CUtensorMap bmap, bsfmap;
-  if (!make_u8_map(&bmap, g.act, g.act_rows, K / 2, 128, BN, true) ||
-      !make_u8_map(&bsfmap, g.act_sf, g.act_rows, K / 16, 16, BN, false))
+  if (MX) {   // E4M3 rows of K bytes; scales copied by address (chunk-major)
+    a.bsf = g.act_sf;
+    a.bsf_rows = g.act_rows;
+    if (!make_u8_map(&bmap, g.act, g.act_rows, K, 128, BN, true)) return cudaErrorInvalidValue;
+    bsfmap = bmap;
+  } else if (!make_u8_map(&bmap, g.act, g.act_rows, K / 2, 128, BN, true) ||
+             !make_u8_map(&bsfmap, g.act_sf, g.act_rows, K / 16, 16, BN, false)) {
     return cudaErrorInvalidValue;
-  auto kern = moe_gemm_nvfp4_kernel<BN, EPI>;
+  }
+  auto kern = moe_gemm_nvfp4_kernel<BN, EPI, MX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t max_items = std::max<int64_t>(1, s.tiles * a.F);
@@ -411,11 +530,20 @@ cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st
 
 template <int BN>
 cudaError_t launch_native_bn(const Shape& s, const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  if (native_mx(s, g.which)) {
+    switch (g.epi) {
+      case kEpiSwigluMxfp8: return launch_native_t<BN, kEpiSwigluMxfp8, true>(s, g, st, pdl);
+      case kEpiRelu2Mxfp8: return launch_native_t<BN, kEpiRelu2Mxfp8, true>(s, g, st, pdl);
+      case kEpiPlainBf16: return launch_native_t<BN, kEpiPlainBf16, true>(s, g, st, pdl);
+      case kEpiAtomicFinal: return launch_native_t<BN, kEpiAtomicFinal, true>(s, g, st, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (g.epi) {
-    case kEpiSwigluNvfp4: return launch_native_t<BN, kEpiSwigluNvfp4>(s, g, st, pdl);
-    case kEpiRelu2Nvfp4: return launch_native_t<BN, kEpiRelu2Nvfp4>(s, g, st, pdl);
-    case kEpiPlainBf16: return launch_native_t<BN, kEpiPlainBf16>(s, g, st, pdl);
-    case kEpiAtomicFinal: return launch_native_t<BN, kEpiAtomicFinal>(s, g, st, pdl);
+    case kEpiSwigluNvfp4: return launch_native_t<BN, kEpiSwigluNvfp4, false>(s, g, st, pdl);
+    case kEpiRelu2Nvfp4: return launch_native_t<BN, kEpiRelu2Nvfp4, false>(s, g, st, pdl);
+    case kEpiPlainBf16: return launch_native_t<BN, kEpiPlainBf16, false>(s, g, st, pdl);
+    case kEpiAtomicFinal: return launch_native_t<BN, kEpiAtomicFinal, false>(s, g, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

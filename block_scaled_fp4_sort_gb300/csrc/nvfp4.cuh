@@ -74,19 +74,10 @@ __device__ __forceinline__ uint32_t nvfp4_quant_lane16(float h, float s, uint32_
   return code_of_quotient<true>(__fmul_rn(h, s), dsf, __frcp_rn(dsf));
 }
 
-// Quantise one value of a 32-element MXFP8 block held by the 32 lanes of the
-// warp (the w4a8 FC1 intermediate, FlashInfer PR #4440; the OCP MX recipe):
-//   X = clamp(floor(log2(amax)) - 8, -127, 127), amax = 0 giving -127
-//   sf = X + 127 (E8M0);  q = E4M3_RNE_satfinite(h * 2^-X), the product in fp32
-// A block holding a NaN or an infinity gets sf 255 and q 0x7F.  Every lane
-// returns its own E4M3 byte; *sf receives the block's E8M0 code.
-__device__ __forceinline__ uint32_t mxfp8_quant_warp(float h, uint32_t* sf) {
-  const float a = fabsf(h);
-  const bool special = !(a <= 3.402823466e38f);  // NaN or infinity
-  float amax = special ? 0.0f : a;
-#pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-  if (__any_sync(0xffffffffu, special)) {
+// The MXFP8 code (recipe below) of h in a block whose largest magnitude is
+// amax, given as +infinity when the block holds a NaN or an infinity.
+__device__ __forceinline__ uint32_t mxfp8_quant_amax(float h, float amax, uint32_t* sf) {
+  if (!(amax <= 3.402823466e38f)) {
     *sf = 255u;
     return 0x7Fu;
   }
@@ -98,6 +89,23 @@ __device__ __forceinline__ uint32_t mxfp8_quant_warp(float h, uint32_t* sf) {
   *sf = (uint32_t)(X + 127);
   const float inv = __uint_as_float((uint32_t)(127 - X) << 23);   // 2^-X, exponent field 8..254
   return f32_to_e4m3_satfinite(__fmul_rn(h, inv));
+}
+// |h| for the block maximum: +infinity for a NaN or an infinity
+__device__ __forceinline__ float mxfp8_abs_key(float h) {
+  const float a = fabsf(h);
+  return a <= 3.402823466e38f ? a : __int_as_float(0x7f800000);
+}
+// Quantise one value of a 32-element MXFP8 block held by the 32 lanes of the
+// warp (the w4a8 FC1 intermediate, FlashInfer PR #4440; the OCP MX recipe):
+//   X = clamp(floor(log2(amax)) - 8, -127, 127), amax = 0 giving -127
+//   sf = X + 127 (E8M0);  q = E4M3_RNE_satfinite(h * 2^-X), the product in fp32
+// A block holding a NaN or an infinity gets sf 255 and q 0x7F.  Every lane
+// returns its own E4M3 byte; *sf receives the block's E8M0 code.
+__device__ __forceinline__ uint32_t mxfp8_quant_warp(float h, uint32_t* sf) {
+  float amax = mxfp8_abs_key(h);
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  return mxfp8_quant_amax(h, amax, sf);
 }
 
 // silu(g) * u with the sigmoid from ex2.approx and rcp.approx

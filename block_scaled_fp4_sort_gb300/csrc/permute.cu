@@ -49,7 +49,7 @@ int num_sms() {
 __global__ void permute_rows(const uint8_t* __restrict__ x, const uint8_t* __restrict__ x_sf,
                              const int32_t* __restrict__ p2e, const int32_t* __restrict__ num_tiles,
                              int64_t T, int64_t top_k, int64_t row_bytes, int64_t sf_bytes,
-                             int zero_pad, int canon, int64_t S, int64_t M,
+                             int zero_pad, int canon, int sf_chunk_major, int64_t S, int64_t M,
                              uint8_t* __restrict__ px, uint8_t* __restrict__ px_sf) {
   grid_dependency_wait();
   // a tile count or slot entry from outside [0, S) / [0, M*top_k) is not followed
@@ -100,9 +100,12 @@ __global__ void permute_rows(const uint8_t* __restrict__ x, const uint8_t* __res
     }
     for (int64_t i = lane; i < row_bytes / 16; i += 32) dst[i] = src >= 0 ? sp[i] : make_uint4(0, 0, 0, 0);
     if (x_sf != nullptr) {  // 4-byte units: H/16 (NVFP4) and H/32 (MXFP8) scale bytes
-      uint32_t* dsf = reinterpret_cast<uint32_t*>(px_sf + s * sf_bytes);
+      // slot-major [S, units], or chunk-major [units, S] (unit i = the MXFP8
+      // scales of 128-element chunk i, as the native MX GEMM copies them)
+      uint32_t* dsf = reinterpret_cast<uint32_t*>(px_sf);
       const uint32_t* ssf = reinterpret_cast<const uint32_t*>(x_sf + src * sf_bytes);
-      for (int64_t i = lane; i < sf_bytes / 4; i += 32) dsf[i] = src >= 0 ? ssf[i] : 0u;
+      for (int64_t i = lane; i < sf_bytes / 4; i += 32)
+        dsf[sf_chunk_major ? i * S + s : s * (sf_bytes / 4) + i] = src >= 0 ? ssf[i] : 0u;
     }
   }
   launch_dependents();
@@ -332,7 +335,7 @@ cudaError_t launch_debug_quantize_mx(const float* in, int64_t n, uint8_t* q, uin
 
 cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, const int32_t* p2e,
                            const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
-                           bool pdl, bool zero_pad, bool canon) {
+                           bool pdl, bool zero_pad, bool canon, bool sf_chunk_major) {
   // w4a16 BF16 rows; w4a4 NVFP4 (H/2 + H/16 bytes); w4a8 MXFP8 (H + H/32 bytes)
   const int64_t row_bytes = s.mode == 0 ? s.H * 2 : s.mode == 2 ? s.H : s.H / 2;
   const int64_t sf_bytes = s.mode == 0 ? 0 : s.mode == 2 ? s.H / 32 : s.H / 16;
@@ -340,7 +343,7 @@ cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, c
   return launch_pdl(permute_rows, dim3((unsigned)std::max<int64_t>(blocks, 1)), dim3(256), st, pdl,
                     static_cast<const uint8_t*>(x), s.mode == 0 ? nullptr : x_sf, p2e, num_tiles,
                     s.T, s.K, row_bytes, sf_bytes, zero_pad ? 1 : 0, canon && s.mode == 1 ? 1 : 0,
-                    s.S, s.M, static_cast<uint8_t*>(px),
+                    sf_chunk_major && s.mode == 2 ? 1 : 0, s.S, s.M, static_cast<uint8_t*>(px),
                     s.mode == 0 ? nullptr : px_sf);
 }
 
@@ -513,6 +516,34 @@ cudaError_t launch_to_f16(const void* src, int64_t src_rows, int64_t K, int64_t 
   return launch_pdl(to_f16_rows, dim3((unsigned)blocks), dim3(256), st, pdl,
                     static_cast<const uint4*>(src), src_rows, K / 8, src_ld / 8, gather, (int)top_k,
                     tile_mn, num_tiles, T, rows, static_cast<uint4*>(out), K / 8, scale);
+}
+
+// MXFP8 scales [rows, units * 4] (slot-major, as the FC1 epilogue and the
+// staged entry points hold them) -> chunk-major [units, rows] 4-byte units,
+// the layout the native MX GEMM copies per 128-element chunk.  Rows at or
+// past num_tiles * T are left unwritten.
+__global__ void sf_to_chunk_major(const uint32_t* __restrict__ sf, int64_t rows, int64_t units,
+                                  const int32_t* __restrict__ num_tiles, int64_t T,
+                                  uint32_t* __restrict__ out) {
+  grid_dependency_wait();
+  const int64_t lim = num_tiles ? min(rows, max((int64_t)num_tiles[0], (int64_t)0) * T) : rows;
+  const int64_t n = lim * units;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / units, u = i % units;
+    out[u * rows + r] = sf[i];
+  }
+  launch_dependents();
+}
+
+cudaError_t launch_sf_chunk_major(const uint8_t* sf, int64_t rows, int64_t K, const int32_t* num_tiles,
+                                  int64_t T, uint8_t* out, cudaStream_t st, bool pdl) {
+  const int64_t units = K / 128;
+  if (rows * units == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((rows * units + 255) / 256, (int64_t)num_sms() * 8);
+  return launch_pdl(sf_to_chunk_major, dim3((unsigned)blocks), dim3(256), st, pdl,
+                    reinterpret_cast<const uint32_t*>(sf), rows, units, num_tiles, T,
+                    reinterpret_cast<uint32_t*>(out));
 }
 
 }  // namespace fp4moe

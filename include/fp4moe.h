@@ -156,7 +156,9 @@ FP4MOE_API size_t fp4moe_route_workspace_size(const fp4moe_problem* p);
 
 /* Workspace bytes of moe_gemm1_swiglu / moe_gemm2 (error word; for w4a4 and
  * w4a8 also the copy of the activations the GEMM consumes: NVFP4 in slot
- * order for the FP4 MMA, else expanded to BF16). */
+ * order for the FP4 MMA, MXFP8 with chunk-ordered scales for the MX MMA,
+ * else expanded to BF16; for decode-size w4a16 FP16 rows, their scales and a
+ * K-split scratch). */
 FP4MOE_API size_t fp4moe_gemm_workspace_size(const fp4moe_problem* p, int32_t which /* 1 | 2 */);
 
 /* Workspace bytes of fused_moe_forward: routing plan, FC1 output h [S, I],
@@ -186,7 +188,10 @@ FP4MOE_API fp4moe_status fp4moe_clear_error(void* workspace, void* stream);
  *   which = 2: w = w2 uint8 [E_local, H, I/2],  w_sf = e4m3 [E_local, H, I/16]
  * prepared: fp4moe_prepared_weight_size(p, which) bytes.  A lossless
  * re-encoding: every weight the kernels decode equals e2m1(code) *
- * e4m3(scale) bit for bit.  Inputs are not modified. */
+ * e4m3(scale) bit for bit (w4a8: e2m1(code) * 2^(e8m0 - 127)).  w4a8 with
+ * route_tile >= 32 and K a multiple of 128 stores each E2M1 code as the equal
+ * E4M3 byte (the MX tensor-core MMA takes E4M3 operands with E8M0 block-32
+ * scales): twice the bytes of the packed codes.  Inputs are not modified. */
 FP4MOE_API fp4moe_status fp4moe_prepare_weights(const fp4moe_problem* p, int32_t which, const uint8_t* w,
                                      const uint8_t* w_sf, void* prepared, void* stream);
 
@@ -262,7 +267,11 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
  * accumulator, the activation in fp32 rounded once; w4a4 with route_tile >= 32
  * and H a multiple of 256 takes the NVFP4 operands straight into the
  * block-scaled FP4 tensor-core MMA -- the same exact products, fp32
- * accumulation; w4a16 with route_tile 8 or 16 decodes to FP16 and carries
+ * accumulation; w4a8 with route_tile >= 32 and H a multiple of 128 takes the
+ * MXFP8 activations and the weights, stored as E4M3 bytes, with their E8M0
+ * block-32 scales straight into the block-scaled MX tensor-core MMA
+ * (kind::mxf8f6f4) -- the same exact products, fp32 accumulation; w4a16 with
+ * route_tile 8 or 16 decodes to FP16 and carries
  * each activation row as FP16 times a power of two chosen from the row's
  * largest finite magnitude, multiplied back on the accumulator -- the same
  * exact products for every element not below 2^-31 of that magnitude):
@@ -342,8 +351,9 @@ FP4MOE_API fp4moe_status moe_combine(const fp4moe_problem* p, const float* parti
                                      int32_t accumulate, void* out, void* stream);
 
 /* The whole forward on `stream`: route sort, x gathered into slot order in the
- * workspace (NVFP4 for the FP4 MMA path; w4a8 rows and decode-size w4a4 rows
- * expanded to BF16 on the way; w4a16 route_tile 8 / 16 rows as FP16 with a
+ * workspace (NVFP4 for the FP4 MMA path, MXFP8 with its scales by 128-element
+ * chunk for the MX MMA path; w4a8 rows of route tile 16 and decode-size w4a4
+ * rows expanded to BF16 on the way; w4a16 route_tile 8 / 16 rows as FP16 with a
  * power-of-two scale each, and h likewise before GEMM2; padding rows
  * unwritten), GEMM1 (+ activation), GEMM2, finalize, chained with
  * programmatic dependent launch.  Arguments as in the steps above; the
@@ -414,8 +424,10 @@ FP4MOE_API fp4moe_status fp4moe_prepare_domain_weights(const fp4moe_problem* p, 
 FP4MOE_API size_t fp4moe_localized_workspace_size(const fp4moe_problem* p);
 
 /* fused_moe_forward over two domains.  On `stream`: route sort and x in slot
- * order; then on domain stream d: FC1 shard d (+ for w4a8 and decode-size w4a4
- * its columns of h expanded to BF16), a wait for the other domain's FC1 (for
+ * order; then on domain stream d: FC1 shard d (+ for w4a8 of route tile 16 and
+ * decode-size w4a4 its columns of h expanded to BF16), a wait for the other
+ * domain's FC1 (for w4a8 on the MX MMA: domain 0 then copies h's scales by
+ * 128-element chunk once and domain 1 waits for that; for
  * w4a16 route_tile 8 / 16: domain 0 then converts all of h to FP16 once and
  * domain 1 waits for that), FC2 shard d; then
  * on `stream` again, after both domains: the finalize.  The results equal

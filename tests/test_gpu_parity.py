@@ -468,7 +468,7 @@ def test_mxfp8_quantiser_bit_exact_vs_oracle():
     assert np.array_equal(q.cpu().numpy(), oq)
 
 
-@pytest.mark.parametrize("T", [16, 32])
+@pytest.mark.parametrize("T", [16, 32])   # BF16-decode layout, native MX layout
 def test_mxfp4_prepared_weights_decode_every_code_under_every_scale(T):
     H, I, E = 256, 256, 1
     k = np.arange(H)
@@ -489,17 +489,24 @@ def test_mxfp4_prepared_weights_decode_every_code_under_every_scale(T):
     from ref_decode import E2M1_TABLE
     e = np.repeat(sf[0].astype(np.int64), 32, axis=1)
     val = E2M1_TABLE[codes] * np.exp2((e - 127).astype(np.float64))
-    mag = (codes & 7) != 0
-    half_nonzero = mag.reshape(rows, H // 16, 16).any(-1).repeat(16, axis=1)
-    nan = (e == 255) | (((e < 106) | (e > 136)) & half_nonzero)
-    want = np.where(nan, np.nan, np.where(((e < 106) | (e > 136)) & ~half_nonzero, val * 0, val))
+    if T >= 32:
+        # native MX layout (E4M3 bytes, E8M0 scales for the MX MMA): every
+        # exponent exact, 255 NaN; the decode's BF16 rounding of the exact value
+        val_bf16 = torch.from_numpy(val).to(torch.bfloat16).double().numpy()
+        want = np.where(e == 255, np.nan, val_bf16)
+    else:
+        mag = (codes & 7) != 0
+        half_nonzero = mag.reshape(rows, H // 16, 16).any(-1).repeat(16, axis=1)
+        nan = (e == 255) | (((e < 106) | (e > 136)) & half_nonzero)
+        want = np.where(nan, np.nan, np.where(((e < 106) | (e > 136)) & ~half_nonzero, val * 0, val))
     assert np.array_equal(np.isnan(got), np.isnan(want))
     ok = ~np.isnan(want)
     assert np.array_equal(got[ok], want[ok])
     assert np.array_equal(np.signbit(got[ok]), np.signbit(want[ok]))
 
 
-@pytest.mark.parametrize("T,act", [(16, "swiglu"), (32, "swiglu"), (32, "relu2")])
+@pytest.mark.parametrize("T,act", [(16, "swiglu"), (32, "swiglu"), (32, "relu2"), (64, "relu2"),
+                                   (128, "swiglu")])
 def test_w4a8_fused_forward_tiny(T, act):
     cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a8", act=act)
     inp, p, B, orc = _setup(cfg, T)
@@ -526,6 +533,19 @@ def test_w4a8_fused_forward_tiny(T, act):
         assert not bad, ("w4a8 FC1 flips off a rounding boundary", int(s), bad[:8])
         check_out(yv[s], orc.expert_down_codes(e, hq[s], hs[s]), 5e-3, what="w4a8 GEMM2 slot %d" % s)
     print("w4a8 FC1 code/scale bytes differing from the oracle: %d" % flips)
+
+
+@pytest.mark.parametrize("T", [16, 64])   # BF16 expansion, MX MMA
+def test_w4a8_per_token_scale(T):
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a8", per_token_scale=True)
+    inp, p, B, orc = _setup(cfg, T)
+    out = torch.zeros(cfg.M, cfg.H, dtype=torch.bfloat16, device="cuda")
+    B.forward(inp.x_q, inp.x_sf, inp.token_selected_experts.cuda(), inp.token_final_scales.cuda(),
+              inp.w1_alpha, inp.w2_alpha, out, None, per_token_scale=inp.per_token_scale)
+    torch.cuda.synchronize()
+    assert fm.read_error(B.fused_ws) == 0
+    _, exact, _ = orc.forward(nthreads=NTHREADS)
+    check_out(f64(out), exact, 1e-2, strict=False, what="w4a8 per-token scale T=%d" % T)
 
 
 def test_prefill_w4a8_sampled():
@@ -619,17 +639,17 @@ def test_atomic_finalize_accumulate(T):
     check_out(f64(c), exact, 5e-3, what="atomic accumulate")
 
 
-@pytest.mark.parametrize("T", [32, 128])
-def test_atomic_finalize_native_nvfp4(T):
-    # w4a4 on the native FP4 MMA: the atomic epilogue of its GEMM2
-    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode="w4a4")
+@pytest.mark.parametrize("mode,T", [("w4a4", 32), ("w4a4", 128), ("w4a8", 32), ("w4a8", 128)])
+def test_atomic_finalize_native_mma(mode, T):
+    # w4a4 on the native FP4 MMA, w4a8 on the MX MMA: the atomic epilogue of GEMM2
+    cfg = synth.CONFIGS["tiny_w4a16"].with_(mode=mode)
     inp, p, B, orc = _setup(cfg, T)
     a = _fused(inp, B, rsf=0.75, mode=ATOMIC)
     _, exact, _ = orc.forward(rsf=0.75, nthreads=NTHREADS)
-    check_out(f64(a), exact, 2e-2, strict=False, what="native atomic T=%d" % T)
+    check_out(f64(a), exact, 2e-2, strict=False, what="native atomic %s T=%d" % (mode, T))
     c = _fused(inp, B, rsf=0.75, accumulate=True, out=a.clone(), mode=ATOMIC)
     _, exact, _ = orc.forward(rsf=0.75, accumulate=True, out_old=bits(a), nthreads=NTHREADS)
-    check_out(f64(c), exact, 2e-2, strict=False, what="native atomic accumulate T=%d" % T)
+    check_out(f64(c), exact, 2e-2, strict=False, what="native atomic accumulate %s T=%d" % (mode, T))
 
 
 def test_atomic_finalize_expert_parallel_halves():
