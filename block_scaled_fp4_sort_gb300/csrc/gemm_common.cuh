@@ -50,6 +50,7 @@ struct GemmArgs {
   const float* slot_scale;     // warp-MMA kernel: FP16 activation row s is the BF16 row / slot_scale[s]
   const uint8_t* bsf;          // native MX GEMM: activation scales, chunk-major [C][bsf_rows] x 4 bytes
   int64_t bsf_rows;
+  const uint8_t* wsf;          // native MX GEMM: weight scales, [tile][C][128 rows] x 4 bytes
   int* err;
 };
 
@@ -166,6 +167,22 @@ bool make_act_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, in
   const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// packed 4-bit matrix [rows, K elements] (K / 2 bytes per row) -> tensor map
+// with box {128 elements, box_rows} that unpacks into shared memory as 16
+// codes per 16 bytes (8 data bytes, an 8-byte gap), 128-byte swizzle: the
+// tensor cores' operand layout for 4-bit elements
+bool make_u4_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)std::max<int64_t>(rows, 1)};
+  const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+  const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

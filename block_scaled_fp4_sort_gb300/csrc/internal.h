@@ -89,18 +89,22 @@ inline int64_t native_row_blocks(const Shape& s, int which) {
 }
 
 // w4a8 GEMMs whose reduction is a multiple of 128 run on the block-scaled
-// MX tensor-core MMA (kind::mxf8f6f4, route tiles 32..128).  The weights are
-// stored one byte per element as E4M3 (every E2M1 value is one, sign
-// included), so that both operands are E4M3 with E8M0 block-32 scales: per
-// (expert, 128-row tile, 128-element K chunk) one block of kMBlockBytes, the
-// codes as in the native NVFP4 layout (128-byte rows, 16-byte units
-// XOR-swizzled by row & 7; the same rows per tile), then the tile's E8M0
-// scales, 4 bytes per row.
+// MX tensor-core MMA (kind::mxf8f6f4, route tiles 32..128): E2M1 weights x
+// E4M3 activations, E8M0 block-32 scales.  The prepared weights stay packed
+// (half a byte per element): region 1 holds the codes of every 128-row tile
+// (the native NVFP4 layout's rows per tile) as a plain [tiles * 128 rows,
+// K / 2 bytes] matrix, which a 4-bit tensor map copies into shared memory
+// unpacked to the MMA's operand layout (16 codes per 16 bytes, the second 8
+// bytes a gap); region 2 holds, per (expert, tile, 128-element K chunk), the
+// tile's E8M0 scales, 4 bytes per row.
 inline bool native_mx(const Shape& s, int which) {
   return s.mode == 2 && s.T >= 32 && (which == 1 ? s.H : s.I) % 128 == 0;
 }
 constexpr int kMTileScales = 128 * 4;
-constexpr int kMBlockBytes = kNTileCodes + kMTileScales;   // 16896
+constexpr int kMBlockBytes = kNTileCodes + kMTileScales;   // 16896: one chunk's weights in shared memory
+inline size_t mx_code_bytes(const Shape& s, int which) {   // region 1
+  return (size_t)s.EL * native_row_blocks(s, which) * 128 * ((which == 1 ? s.H : s.I) / 2);
+}
 // either native layout (same tiles, same rows per tile)
 inline bool native_mma(const Shape& s, int which) { return native_fp4(s, which) || native_mx(s, which); }
 
@@ -109,8 +113,8 @@ inline size_t prepared_bytes(const Shape& s, int which) {
     return (size_t)s.EL * native_row_blocks(s, which) * ((which == 1 ? s.H : s.I) / 256) *
            kNBlockBytes;
   if (native_mx(s, which))
-    return (size_t)s.EL * native_row_blocks(s, which) * ((which == 1 ? s.H : s.I) / 128) *
-           kMBlockBytes;
+    return mx_code_bytes(s, which) +
+           (size_t)s.EL * native_row_blocks(s, which) * ((which == 1 ? s.H : s.I) / 128) * kMTileScales;
   return (size_t)s.EL * row_blocks(s, which) * k_chunks(s, which) * kWBlockBytes;
 }
 

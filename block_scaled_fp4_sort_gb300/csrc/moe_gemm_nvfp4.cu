@@ -44,7 +44,11 @@ struct NCfg {
   static constexpr int kABytes = MX ? kMBlockBytes : kNBlockBytes;   // one prepared weight block
   static constexpr int kBData = BN * 128;         // BN activation rows of 128 code bytes per chunk
   static constexpr int kBSf = MX ? BN * 4 : BN * 16;   // block scales per row and chunk
-  static constexpr int kTx = kABytes + kBData + kBSf;
+  // a stage's shared-memory footprint, and the bytes its copies complete: a
+  // 4-bit tensor copy counts the packed bytes it reads (8 KB per MX weight
+  // tile), not the 16 KB it writes
+  static constexpr int kFootprint = kABytes + kBData + kBSf;
+  static constexpr int kTx = (MX ? kNTileCodes / 2 + kMTileScales : kABytes) + kBData + kBSf;
   // stage layout: NVFP4 [weight codes | weight scales | B codes | B scales];
   // MX [B codes | weight codes | weight scales | B scales] -- both code tiles
   // on 1024-byte boundaries (the 128-byte swizzle)
@@ -52,7 +56,7 @@ struct NCfg {
   static constexpr int kOffASf = kOffA + kNTileCodes;
   static constexpr int kOffB = MX ? 0 : kNBlockBytes;
   static constexpr int kOffBSf = MX ? kBData + kMBlockBytes : kNBlockBytes + kBData;
-  static constexpr int kStage = (kTx + 1023) / 1024 * 1024;
+  static constexpr int kStage = (kFootprint + 1023) / 1024 * 1024;
   static constexpr int kStagesRaw = (220 * 1024) / kStage;
   static constexpr int kStages = kStagesRaw > 6 ? 6 : kStagesRaw;
   static constexpr int kSfBase = 256;             // TMEM: accumulators 2 x BN from column 0
@@ -63,6 +67,7 @@ struct NCfg {
   static constexpr int kXchBytes = MX ? 2 * 16 * 16 * 4 : 0;
   static constexpr int kSmem = 1024 + kStages * kStage + kBarBytes + kXchBytes;
   static_assert(kOffA % 1024 == 0 && kOffB % 1024 == 0 && kOffBSf % 16 == 0, "stage layout");
+  static_assert(kOffBSf + kBSf <= kStage && kOffASf + kMTileScales <= kStage, "stage footprint");
   static_assert(kSfBase + kStages * kSfCols <= 512, "tensor memory");
   static_assert(2 * BN <= kSfBase, "accumulators");
   static_assert(kStages >= 2, "pipeline depth");
@@ -104,10 +109,11 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
-// Instruction descriptor, kind::mxf8f6f4: A and B E4M3 (format 0), K-major,
-// E8M0 scales (bit 23), scale-factor slots 0.
+// Instruction descriptor, kind::mxf8f6f4: A E2M1 (format 5), B E4M3 (format
+// 0), K-major, E8M0 scales (bit 23), scale-factor slots 0.
 __host__ __device__ constexpr uint32_t idesc_mx(int M, int N) {
-  return (1u << 23)                      // scale type: UE8M0
+  return (5u << 7)                       // A format: E2M1
+         | (1u << 23)                    // scale type: UE8M0
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
@@ -276,6 +282,9 @@ template <int BN, int EPI, bool MX>
 __global__ void __launch_bounds__(kNThreads, 1)
     moe_gemm_nvfp4_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap bmap,
                           const __grid_constant__ CUtensorMap bsfmap) {
+  // MX: bsfmap is the weights' 4-bit tensor map (the activation scales go by
+  // address); NVFP4: the activation scales' map
+
   using C = NCfg<BN, MX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -310,7 +319,7 @@ __global__ void __launch_bounds__(kNThreads, 1)
   }
   if (warp == kNTmaWarp && lane == 0) {
     prefetch_tensormap(&bmap);
-    if (!MX) prefetch_tensormap(&bsfmap);
+    prefetch_tensormap(&bsfmap);
   }
   tc_fence_before();
   __syncthreads();
@@ -336,13 +345,21 @@ __global__ void __launch_bounds__(kNThreads, 1)
           if (ok) {
             uint8_t* st = stages + stage * C::kStage;
             mbar_arrive_expect_tx(&full[stage], (uint32_t)C::kTx);
-            tma_load_1d(st + kOffA, wsrc + (int64_t)c * C::kABytes, C::kABytes, &full[stage]);
-            tma_load_2d(st + kOffB, &bmap, c * 128, tau * BN, &full[stage]);
-            if (MX)   // the chunk's activation scales: BN rows x 4 bytes, chunk-major
+            if (MX) {
+              // the weight tile unpacked by its 4-bit map (16 KB in shared
+              // memory), its scales, the activation codes, and their scales
+              // (BN rows x 4 bytes, chunk-major)
+              const int64_t tile = (int64_t)e * a.F + f;
+              tma_load_2d(st + kOffA, &bsfmap, c * 128, (int32_t)(tile * 128), &full[stage]);
+              tma_load_1d(st + kOffASf, a.wsf + ((tile * a.C + c) * 128) * 4, kMTileScales, &full[stage]);
+              tma_load_2d(st + kOffB, &bmap, c * 128, tau * BN, &full[stage]);
               tma_load_1d(st + kOffBSf, a.bsf + ((int64_t)c * a.bsf_rows + (int64_t)tau * BN) * 4,
                           (uint32_t)C::kBSf, &full[stage]);
-            else
+            } else {
+              tma_load_1d(st + kOffA, wsrc + (int64_t)c * C::kABytes, C::kABytes, &full[stage]);
+              tma_load_2d(st + kOffB, &bmap, c * 128, tau * BN, &full[stage]);
               tma_load_2d(st + kOffBSf, &bsfmap, c * 16, tau * BN, &full[stage]);
+            }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -502,11 +519,13 @@ cudaError_t launch_native_t(const Shape& s, const GemmLaunch& g, cudaStream_t st
   a.err = g.err;
   const int64_t K = g.which == 1 ? s.H : s.I;
   CUtensorMap bmap, bsfmap;
-  if (MX) {   // E4M3 rows of K bytes; scales copied by address (chunk-major)
+  if (MX) {   // E4M3 activation rows of K bytes (their scales by address); packed E2M1 weights
     a.bsf = g.act_sf;
     a.bsf_rows = g.act_rows;
-    if (!make_u8_map(&bmap, g.act, g.act_rows, K, 128, BN, true)) return cudaErrorInvalidValue;
-    bsfmap = bmap;
+    a.wsf = g.wprep + mx_code_bytes(s, g.which);
+    if (!make_u8_map(&bmap, g.act, g.act_rows, K, 128, BN, true) ||
+        !make_u4_map(&bsfmap, g.wprep, (int64_t)s.EL * a.F * 128, K, 128))
+      return cudaErrorInvalidValue;
   } else if (!make_u8_map(&bmap, g.act, g.act_rows, K / 2, 128, BN, true) ||
              !make_u8_map(&bsfmap, g.act_sf, g.act_rows, K / 16, 16, BN, false)) {
     return cudaErrorInvalidValue;

@@ -295,49 +295,35 @@ __global__ void debug_decode_native_kernel(PrepArgs a, int64_t C) {
   }
 }
 
-// Native MX blocks (w4a8 GEMMs with K a multiple of 128; internal.h): block
-// (e, f, c) = the tile's E2M1 codes rewritten as E4M3 bytes | its E8M0
-// scales.  One thread per (block, row, 16-byte output unit j = 16 elements).
-__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t nib16) {
-  // E4M3 bytes of 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 of a code is its sign
-  uint32_t out = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint32_t c = (nib16 >> (4 * k)) & 15u;
-    const uint32_t m = c & 7u;
-    const uint32_t mag = m == 0 ? 0u : m == 1 ? 0x30u : 0x38u + ((m - 2u) << 2);
-    out |= (mag | ((c & 8u) << 4)) << (8 * k);
-  }
-  return out;
-}
-__global__ void prepare_native_mx_kernel(PrepArgs a, int64_t C) {
-  const int64_t n = a.EL * a.F * C * 128 * 8;
+// Native MX weights (w4a8 GEMMs with K a multiple of 128; internal.h): the
+// packed codes of tile row (e, f, r) at row (e F + f) 128 + r of region 1, the
+// E8M0 scales of (e, f, c) in region 2.  One thread per (tile row, 16-byte
+// unit of the packed row); the first unit of each 128-element chunk also
+// writes the row's four scales of that chunk.
+__global__ void prepare_native_mx_kernel(PrepArgs a, int64_t C, int64_t code_bytes) {
+  const int64_t units = a.K / 32;   // 16-byte units (32 codes) per packed row
+  const int64_t n = a.EL * a.F * 128 * units;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const int j = (int)(i & 7), r = (int)((i >> 3) & 127);
-    const int64_t blk = i >> 10;
-    const int64_t c = blk % C, f = (blk / C) % a.F, e = blk / (C * a.F);
+    const int64_t u = i % units, tr = i / units;   // tile row tr = (e F + f) 128 + r
+    const int r = (int)(tr & 127);
+    const int64_t f = (tr >> 7) % a.F, e = (tr >> 7) / a.F;
     const int64_t row = native_src_row(a, f, r);
     const bool valid = row < a.rows_src;
-    uint8_t* dst = a.prep + blk * kMBlockBytes;
-    uint4 q = make_uint4(0, 0, 0, 0);
-    uint32_t sv = 0;
-    if (valid) {
-      const int64_t g = e * a.rows_src + row;
-      // 16 elements = 8 packed bytes at element 128 c + 16 j
-      const uint2 p = *reinterpret_cast<const uint2*>(a.w + g * (a.K / 2) + c * 64 + j * 8);
-      q = make_uint4(e2m1x4_to_e4m3x4(p.x & 0xFFFFu), e2m1x4_to_e4m3x4(p.x >> 16),
-                     e2m1x4_to_e4m3x4(p.y & 0xFFFFu), e2m1x4_to_e4m3x4(p.y >> 16));
-      sv = *reinterpret_cast<const uint32_t*>(a.w_sf + g * (a.K / 32) + c * 4);
+    const int64_t g = e * a.rows_src + row;
+    *reinterpret_cast<uint4*>(a.prep + tr * (a.K / 2) + u * 16) =
+        valid ? *reinterpret_cast<const uint4*>(a.w + g * (a.K / 2) + u * 16) : make_uint4(0, 0, 0, 0);
+    if ((u & 3) == 0) {   // chunk c = u / 4: scales of K blocks 4c..4c+3
+      const int64_t c = u >> 2;
+      const uint32_t sv = valid ? *reinterpret_cast<const uint32_t*>(a.w_sf + g * (a.K / 32) + c * 4) : 0u;
+      *reinterpret_cast<uint32_t*>(a.prep + code_bytes + (((e * a.F + f) * C + c) * 128 + r) * 4) = sv;
     }
-    *reinterpret_cast<uint4*>(dst + r * 128 + ((j ^ (r & 7)) << 4)) = q;
-    if (j == 0) *reinterpret_cast<uint32_t*>(dst + kNTileCodes + r * 4) = sv;
   }
 }
 
-// the native MX blocks decoded to bf16 [E_local, rows, K]: one thread per
-// 32-element block of a row; e4m3 * 2^(scale - 127), the scale 255 NaN
-__global__ void debug_decode_native_mx_kernel(PrepArgs a, int64_t C) {
+// the native MX weights decoded to bf16 [E_local, rows, K]: one thread per
+// 32-element block of a row; e2m1 * 2^(scale - 127), the scale 255 NaN
+__global__ void debug_decode_native_mx_kernel(PrepArgs a, int64_t C, int64_t code_bytes) {
   const int64_t nb = a.K / 32;
   const int64_t n = a.EL * a.rows_src * nb;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
@@ -356,20 +342,16 @@ __global__ void debug_decode_native_mx_kernel(PrepArgs a, int64_t C) {
       r = (int)(row % 128);
     }
     const int64_t c = b / 4, bb = b % 4;
-    const uint8_t* base = a.prep + ((e * a.F + f) * C + c) * kMBlockBytes;
-    const uint32_t sc = base[kNTileCodes + r * 4 + bb];
+    const int64_t tr = (e * a.F + f) * 128 + r;
+    const uint32_t sc = a.prep[code_bytes + (((e * a.F + f) * C + c) * 128 + r) * 4 + bb];
     const float scale = sc == 255u ? __int_as_float(0x7fc00000) : ldexpf(1.0f, (int)sc - 127);
+    const uint4 q = *reinterpret_cast<const uint4*>(a.prep + tr * (a.K / 2) + b * 16);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     uint16_t* out = a.dbg_out + i * 32;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {   // two 16-byte units of the block
-      const int jj = (int)(bb * 2 + u);
-      const uint4 q = *reinterpret_cast<const uint4*>(base + r * 128 + ((jj ^ (r & 7)) << 4));
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const __nv_bfloat16 v = __float2bfloat16_rn(e4m3_to_float((w[k >> 2] >> (8 * (k & 3))) & 0xFFu) * scale);
-        out[16 * u + k] = *reinterpret_cast<const uint16_t*>(&v);
-      }
+    for (int k = 0; k < 32; ++k) {
+      const __nv_bfloat16 v = __float2bfloat16_rn(e2m1_value((w[k >> 3] >> (4 * (k & 7))) & 15u) * scale);
+      out[k] = *reinterpret_cast<const uint16_t*>(&v);
     }
   }
 }
@@ -399,11 +381,11 @@ cudaError_t launch_prepare(const Shape& s, int which, const uint8_t* w, const ui
   if (native_mma(s, which)) {
     const bool mx = native_mx(s, which);
     const int64_t C = a.K / (mx ? 128 : 256);
-    const int64_t n = a.EL * a.F * C * 1024;
+    const int64_t n = mx ? a.EL * a.F * 128 * (a.K / 32) : a.EL * a.F * C * 1024;
     if (n == 0) return cudaSuccess;
     const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
     if (mx)
-      prepare_native_mx_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, C);
+      prepare_native_mx_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, C, (int64_t)mx_code_bytes(s, which));
     else
       prepare_native_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, C);
     return cudaGetLastError();
@@ -435,7 +417,8 @@ cudaError_t launch_debug_decode(const Shape& s, int which, const uint8_t* prepar
     const int64_t n = a.EL * a.rows_src * (a.K / 32);
     if (n == 0) return cudaSuccess;
     const int64_t blocks = std::min<int64_t>((n + 255) / 256, 65535 * 8);
-    debug_decode_native_mx_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, a.K / 128);
+    debug_decode_native_mx_kernel<<<(unsigned)blocks, 256, 0, st>>>(a, a.K / 128,
+                                                                      (int64_t)mx_code_bytes(s, which));
     return cudaGetLastError();
   }
   const bool frag = fragment_layout(s);
