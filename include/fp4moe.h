@@ -188,10 +188,9 @@ FP4MOE_API fp4moe_status fp4moe_clear_error(void* workspace, void* stream);
  *   which = 2: w = w2 uint8 [E_local, H, I/2],  w_sf = e4m3 [E_local, H, I/16]
  * prepared: fp4moe_prepared_weight_size(p, which) bytes.  A lossless
  * re-encoding: every weight the kernels decode equals e2m1(code) *
- * e4m3(scale) bit for bit (w4a8: e2m1(code) * 2^(e8m0 - 127)).  w4a8 with
- * route_tile >= 32 and K a multiple of 128 stores each E2M1 code as the equal
- * E4M3 byte (the MX tensor-core MMA takes E4M3 operands with E8M0 block-32
- * scales): twice the bytes of the packed codes.  Inputs are not modified. */
+ * e4m3(scale) bit for bit (w4a8: e2m1(code) * 2^(e8m0 - 127), every
+ * exponent exact on the MX MMA path of route_tile >= 32 and K a multiple of
+ * 128, whose prepared codes stay packed).  Inputs are not modified. */
 FP4MOE_API fp4moe_status fp4moe_prepare_weights(const fp4moe_problem* p, int32_t which, const uint8_t* w,
                                      const uint8_t* w_sf, void* prepared, void* stream);
 
@@ -268,9 +267,9 @@ FP4MOE_API fp4moe_status moe_permute(const fp4moe_problem* p, const void* x, con
  * and H a multiple of 256 takes the NVFP4 operands straight into the
  * block-scaled FP4 tensor-core MMA -- the same exact products, fp32
  * accumulation; w4a8 with route_tile >= 32 and H a multiple of 128 takes the
- * MXFP8 activations and the weights, stored as E4M3 bytes, with their E8M0
- * block-32 scales straight into the block-scaled MX tensor-core MMA
- * (kind::mxf8f6f4) -- the same exact products, fp32 accumulation; w4a16 with
+ * E2M1 weights and MXFP8 activations with their E8M0 block-32 scales straight
+ * into the block-scaled MX tensor-core MMA (kind::mxf8f6f4) -- the same exact
+ * products, fp32 accumulation; w4a16 with
  * route_tile 8 or 16 decodes to FP16 and carries
  * each activation row as FP16 times a power of two chosen from the row's
  * largest finite magnitude, multiplied back on the accumulator -- the same
