@@ -563,7 +563,7 @@ fp4moe_status fused_moe_forward(const fp4moe_problem* p, const void* x, const ui
         : w4    ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
                                       ws + L.y, cs, true, p2e, s.K, s.M, mx)
         : frag  ? launch_to_f16(x, s.M, s.H, s.H, p2e, s.K, tm, nt, s.T, s.S, ws + L.y, xs, cs, true)
-                : launch_permute(s, x, nullptr, p2e, nt, ws + L.y, nullptr, cs, true, false);
+                : launch_permute_token_major(s, x, e2p, ws + L.y, cs, true);
   GemmLaunch g1 = {};
   g1.which = 1;
   g1.epi = gemm1_epilogue(s);
@@ -737,7 +737,7 @@ fp4moe_status fused_moe_forward_localized(const fp4moe_problem* p, const void* x
           : w4    ? launch_dequant_rows(static_cast<const uint8_t*>(x), x_sf, s.S, s.H, nt, s.T,
                                         y, cs, true, p2e, s.K, s.M, mx)
           : frag  ? launch_to_f16(x, s.M, s.H, s.H, p2e, s.K, tm, nt, s.T, s.S, y, xs, cs, true)
-                  : launch_permute(s, x, nullptr, p2e, nt, y, nullptr, cs, true, false);
+                  : launch_permute_token_major(s, x, e2p, y, cs, true);
     if (e == cudaSuccess && atomic && !side_seed)
       e = launch_seed_acc(s, out, accumulate ? 1 : 0, acc, cs, true);
     if (e == cudaSuccess) e = record_on(cs, kEvFork, &ev_fork);

@@ -131,6 +131,10 @@ cudaError_t launch_permute(const Shape& s, const void* x, const uint8_t* x_sf, c
                            const int32_t* num_tiles, void* px, uint8_t* px_sf, cudaStream_t st,
                            bool pdl, bool zero_pad = true, bool canon = false,
                            bool sf_chunk_major = false);
+// BF16 x [M, H] into slot order by token (each row read once, written to the
+// slots e2p gives its routes); padding slots untouched
+cudaError_t launch_permute_token_major(const Shape& s, const void* x, const int32_t* e2p, void* px,
+                                       cudaStream_t st, bool pdl);
 // MXFP8 scales [rows, K/32] -> chunk-major [K/128, rows] 4-byte units (the
 // native MX GEMM's activation scales); rows past num_tiles * T untouched
 cudaError_t launch_sf_chunk_major(const uint8_t* sf, int64_t rows, int64_t K, const int32_t* num_tiles,

@@ -546,4 +546,51 @@ cudaError_t launch_sf_chunk_major(const uint8_t* sf, int64_t rows, int64_t K, co
                     reinterpret_cast<uint32_t*>(out));
 }
 
+// The slot-order copy of BF16 x, token-major: one warp per token reads the
+// token's row once and writes it to the slot of each of its routes
+// (expanded_idx_to_permuted_idx), instead of one warp per slot reading the
+// row again for every route: the row is read from memory once instead of
+// top_k times.  Routes with no slot (-1, or past `slots`) are skipped; padding
+// slots are left unwritten, as by the slot-major copy.  Rows go in pieces of
+// up to 8 x 16 bytes per lane, each loaded once and stored top_k times.
+__global__ void permute_token_major(const uint4* __restrict__ x, const int32_t* __restrict__ e2p,
+                                    int64_t M, int top_k, int64_t units, int64_t slots,
+                                    uint4* __restrict__ px) {
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < M; t += warps) {
+    const int32_t* route_slot = e2p + t * top_k;
+    const uint4* src = x + t * units;
+    for (int64_t u0 = 0; u0 < units; u0 += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int64_t u = u0 + k * 32 + lane;
+        v[k] = u < units ? src[u] : make_uint4(0, 0, 0, 0);
+      }
+      for (int j = 0; j < top_k; ++j) {
+        const int32_t sl = route_slot[j];   // the same for every lane
+        if (sl < 0 || sl >= slots) continue;
+        uint4* dst = px + (int64_t)sl * units;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int64_t u = u0 + k * 32 + lane;
+          if (u < units) dst[u] = v[k];
+        }
+      }
+    }
+  }
+  launch_dependents();
+}
+
+cudaError_t launch_permute_token_major(const Shape& s, const void* x, const int32_t* e2p, void* px,
+                                       cudaStream_t st, bool pdl) {
+  if (s.M == 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((s.M + 7) / 8, (int64_t)num_sms() * 8);
+  return launch_pdl(permute_token_major, dim3((unsigned)blocks), dim3(256), st, pdl,
+                    static_cast<const uint4*>(x), e2p, s.M, (int)s.K, s.H * 2 / 16, s.S,
+                    static_cast<uint4*>(px));
+}
+
 }  // namespace fp4moe

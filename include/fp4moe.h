@@ -350,7 +350,7 @@ FP4MOE_API fp4moe_status moe_combine(const fp4moe_problem* p, const float* parti
                                      int32_t accumulate, void* out, void* stream);
 
 /* The whole forward on `stream`: route sort, x gathered into slot order in the
- * workspace (NVFP4 for the FP4 MMA path, MXFP8 with its scales by 128-element
+ * workspace (BF16 rows copied token by token to their routes' slots; NVFP4 for the FP4 MMA path, MXFP8 with its scales by 128-element
  * chunk for the MX MMA path; w4a8 rows of route tile 16 and decode-size w4a4
  * rows expanded to BF16 on the way; w4a16 route_tile 8 / 16 rows as FP16 with a
  * power-of-two scale each, and h likewise before GEMM2; padding rows
