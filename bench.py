@@ -255,8 +255,9 @@ def stored_traffic(workload, family):
 
 def native_mma(cfg, T):
     """GEMM1's block-scaled tensor-core MMA, if any: 'nvfp4' (w4a4, K a
-    multiple of 256), 'mxfp8' (w4a8, K a multiple of 128; the E2M1 weights
-    stored as E4M3 bytes), route tiles of 32 or more; else None."""
+    multiple of 256), 'mxfp8' (w4a8, K a multiple of 128; the packed E2M1
+    weights unpacked on the way into shared memory), route tiles of 32 or
+    more; else None."""
     if T >= 32 and cfg.mode == "w4a4" and cfg.H % 256 == 0:
         return "nvfp4"
     if T >= 32 and cfg.mode == "w4a8" and cfg.H % 128 == 0:
