@@ -75,17 +75,20 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
   if (EPI == kEpiPlainBf16 || EPI == kEpiAtomicFinal) {
     const int64_t n = (int64_t)f * 256 + tile * 128 + row;
     float* y = static_cast<float*>(a.out);   // fp32 route storage
-#pragma unroll 1
-    for (int cc = c0; cc < c0 + kCw; cc += 16) {
-      uint32_t v[16];
-      tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc), v);
+    // the next 16 columns load from tensor memory while these are stored
+    uint32_t v[2][16];
+    tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + c0), v[0]);
+#pragma unroll
+    for (int j = 0; j < kCw / 16; ++j) {
+      const int cc = c0 + 16 * j;
       tmem_wait_ld();
+      if (j + 1 < kCw / 16) tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc + 16), v[(j + 1) & 1]);
       if (n < a.valid_rows) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int64_t s = s0 + cc + i;
           if (s >= mn) continue;
-          const float yv = __uint_as_float(v[i]) * scale;
+          const float yv = __uint_as_float(v[j & 1][i]) * scale;
           if (EPI == kEpiPlainBf16)
             y[s * a.out_ld + n] = yv;
           else
