@@ -237,11 +237,12 @@ def gemm_family(cfg, T, native):
     return "gemv" if cfg.mode == "w4a16" and T <= 16 else "tcgen05"
 
 
-def stored_traffic(workload, family):
+def stored_traffic(workload, family, T=None, cfg=None):
     """DRAM bytes per GEMM1 launch from a committed ncu summary of this
     workload's GEMM1 (scaled to the full launch where the capture ran a
     smaller case), or None if none was taken on the current sources of the
-    kernel family that runs it."""
+    kernel family that runs it, or the run changed the workload's sizes or
+    route tile."""
     path = os.path.join(ROOT, "profiles", "gemm1_traffic.json")
     if not os.path.exists(path):
         return None, None
@@ -250,6 +251,12 @@ def stored_traffic(workload, family):
     ent = tj.get(workload)
     if not ent or ent.get("src_digest") != src_digest(*GEMM_SOURCES[family]):
         return None, None
+    if T is not None and ent.get("route_tile") != T:
+        return None, None
+    if cfg is not None:
+        import synth
+        if workload in synth.CONFIGS and cfg != synth.CONFIGS[workload]:
+            return None, None
     return ent.get("dram_bytes_per_launch"), ent.get("source")
 
 
@@ -510,7 +517,7 @@ def measure(cfg, args, rank, world, local, dev, headline):
     achieved_bw = g1_bytes / (g1_ms * 1e-3) / 1e9
     achieved_tf = g1_flops / (g1_ms * 1e-3) / 1e12
     step_bytes = touched * (w1_bytes_per_expert + w2_bytes_per_expert) + act1 + M * H * 2
-    traffic, traffic_src = stored_traffic(cfg.name, gemm_family(cfg, T, native))
+    traffic, traffic_src = stored_traffic(cfg.name, gemm_family(cfg, T, native), T, cfg)
     g2_ms = kernels["gemm2"]
     roof = {"kernel": gemm1_kernel_name(cfg, T, native), "mma_dtype": mma_dtype(cfg, T, native)}
     if tensor_bound:

@@ -40,3 +40,18 @@ def test_bounded_oracle_timer_uses_a_prefix_of_the_sample():
     assert v == n / dt
     big = synth.CONFIGS["large_w4a16"]
     assert big.sample == 1024      # the large workload is timed on its seeded sample
+
+
+def test_stored_traffic_only_for_the_captured_case():
+    # a stored ncu traffic figure belongs to one workload at its default sizes
+    # and route tile: another route tile or a resized run reports none
+    with open(os.path.join(ROOT, "profiles", "gemm1_traffic.json")) as f:
+        tj = json.load(f)
+    for name in ("decode_w4a16", "skewed_w4a16", "large_w4a16"):
+        cfg = synth.CONFIGS[name]
+        T = tj[name]["route_tile"]
+        fam = bench.gemm_family(cfg, T, None)
+        assert bench.stored_traffic(name, fam, 2 * T, cfg) == (None, None)
+        assert bench.stored_traffic(name, fam, T, cfg.with_(M=cfg.M // 2)) == (None, None)
+        got, src = bench.stored_traffic(name, fam, T, cfg)
+        assert got is None or (got == tj[name]["dram_bytes_per_launch"] and src == tj[name]["source"])
