@@ -78,6 +78,10 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
     // the next 16 columns load from tensor memory while these are stored
     uint32_t v[2][16];
     tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + c0), v[0]);
+    // this group's valid columns, and slot s0 + c0's element of feature n
+    const int64_t nv64 = (int64_t)mn - s0 - c0;
+    const int nvalid = nv64 <= 0 ? 0 : nv64 >= kCw ? kCw : (int)nv64;
+    float* yp = y + (s0 + c0) * a.out_ld + n;
 #pragma unroll
     for (int j = 0; j < kCw / 16; ++j) {
       const int cc = c0 + 16 * j;
@@ -86,13 +90,13 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
       if (n < a.valid_rows) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int64_t s = s0 + cc + i;
-          if (s >= mn) continue;
           const float yv = __uint_as_float(v[j & 1][i]) * scale;
-          if (EPI == kEpiPlainBf16)
-            y[s * a.out_ld + n] = yv;
-          else
-            atomic_final_add(a, s, n, yv);
+          if (EPI == kEpiPlainBf16) {
+            if (16 * j + i < nvalid) *yp = yv;
+            yp += a.out_ld;
+          } else if (s0 + cc + i < mn) {
+            atomic_final_add(a, s0 + cc + i, n, yv);
+          }
         }
       }
     }
