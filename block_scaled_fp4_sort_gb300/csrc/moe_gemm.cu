@@ -87,15 +87,39 @@ __device__ __forceinline__ void tc_epilogue(const GemmArgs& a, uint32_t tmem, ui
       const int cc = c0 + 16 * j;
       tmem_wait_ld();
       if (j + 1 < kCw / 16) tmem_ld16(tmem + lane_base + (uint32_t)(tile * BN + cc + 16), v[(j + 1) & 1]);
-      if (n < a.valid_rows) {
+      if (n < a.valid_rows && EPI == kEpiPlainBf16) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float yv = __uint_as_float(v[j & 1][i]) * scale;
-          if (EPI == kEpiPlainBf16) {
-            if (16 * j + i < nvalid) *yp = yv;
-            yp += a.out_ld;
-          } else if (s0 + cc + i < mn) {
-            atomic_final_add(a, s0 + cc + i, n, yv);
+          if (16 * j + i < nvalid) *yp = __uint_as_float(v[j & 1][i]) * scale;
+          yp += a.out_ld;
+        }
+      } else if (n < a.valid_rows) {   // warp-uniform: the valid rows are a multiple of 32
+        // atomic finalize, four features per add: within each quad of lanes
+        // (features 4g..4g+3 of the warp) a 4 x 4 transpose gives lane q the
+        // four features of slot column 4c + q; one 16-byte add per lane
+        const int q = lane & 3;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float b[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int si = (q + r) & 3, k = (q - r) & 3;
+            const uint32_t send = si == 0 ? v[j & 1][4 * c] : si == 1 ? v[j & 1][4 * c + 1]
+                                : si == 2 ? v[j & 1][4 * c + 2] : v[j & 1][4 * c + 3];
+            const float got = __uint_as_float(__shfl_sync(0xffffffffu, send, (lane & ~3) | k));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) b[e] = e == k ? got : b[e];
+          }
+          const int64_t s = s0 + cc + 4 * c + q;
+          if (s < mn) {
+            const int32_t r = a.p2e[s];
+            if (r >= 0 && r < a.R) {
+              const float fw = a.rsf * a.route_w[r];
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) +
+                                                      (int64_t)(r / a.top_k) * a.out_ld + (n - q));
+              atomicAdd(dst, make_float4(fw * (b[0] * scale), fw * (b[1] * scale),
+                                         fw * (b[2] * scale), fw * (b[3] * scale)));
+            }
           }
         }
       }
