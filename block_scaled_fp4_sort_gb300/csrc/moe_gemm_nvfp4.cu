@@ -241,6 +241,42 @@ __device__ __forceinline__ void n_epilogue(const GemmArgs& a, uint32_t acc, uint
       }
       xbuf ^= 1u;
     }
+  } else if (EPI == kEpiAtomicFinal) {
+    // atomic finalize, four features per add: within each quad of lanes
+    // (features 4g..4g+3 of the warp) a 4 x 4 transpose gives lane q the four
+    // features of slot column 4c + q; one 16-byte fp32 atomic add per lane
+    const int64_t n = (int64_t)f * 128 + row;
+    if (n >= a.valid_rows) return;   // warp-uniform: the valid rows are a multiple of 32
+    const int q = lane & 3;
+#pragma unroll 1
+    for (int cc = c0; cc < c0 + kCw; cc += 16) {
+      uint32_t v[16];
+      tmem_ld16(acc + lane_base + (uint32_t)cc, v);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float b[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int si = (q + r) & 3, k = (q - r) & 3;
+          const uint32_t send = si == 0 ? v[4 * c] : si == 1 ? v[4 * c + 1] : si == 2 ? v[4 * c + 2] : v[4 * c + 3];
+          const float got = __uint_as_float(__shfl_sync(0xffffffffu, send, (lane & ~3) | k));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) b[e] = e == k ? got : b[e];
+        }
+        const int64_t s = s0 + cc + 4 * c + q;
+        if (s < mn) {
+          const int32_t r = a.p2e[s];
+          if (r >= 0 && r < a.R) {
+            const float fw = a.rsf * a.route_w[r];
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) +
+                                                    (int64_t)(r / a.top_k) * a.out_ld + (n - q));
+            atomicAdd(dst, make_float4(fw * (b[0] * scale), fw * (b[1] * scale), fw * (b[2] * scale),
+                                       fw * (b[3] * scale)));
+          }
+        }
+      }
+    }
   } else {
     const int64_t n = (int64_t)f * 128 + row;
     if (n >= a.valid_rows) return;   // warp-uniform: the valid rows are a multiple of 32
